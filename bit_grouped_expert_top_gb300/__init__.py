@@ -1,0 +1,10 @@
+"""GB300 (sm_103a) mixture-of-experts layer: routing, int4 grouped expert GEMMs and decode.
+
+The compute lives in liblily_moe.so (CUDA kernels behind a C ABI, see
+include/lily_moe.h); ``_abi`` is its ctypes binding.  Importing this package
+loads nothing; the library is built / loaded on first use.
+"""
+from ._abi import (LilyError, alloc_routing, alloc_workspace, lily_moe_block_capacity, lily_moe_check_shape,  # noqa: F401
+                   lily_moe_clear_status, lily_moe_decode, lily_moe_device_status, lily_moe_forward,
+                   lily_moe_forward_timed, lily_moe_grouped_gemm, lily_moe_route, lily_moe_status_string,
+                   lily_moe_version, lily_moe_workspace_bytes, load, make_routing, make_shape, make_weights)

@@ -1,0 +1,573 @@
+// C-ABI entry points of liblily_moe.so (declared in include/lily_moe.h):
+// argument validation, workspace carving, TMA tensor-map encoding and the
+// launch sequence of each call.  No entry point allocates device memory or
+// synchronises, except lily_moe_device_status.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "lily_internal.h"
+#include "lily_moe.h"
+
+namespace lily {
+size_t decode_smem_route(int T, int d);
+size_t decode_smem_gateup(int T, int d);
+size_t decode_smem_down(int T, int I);
+cudaError_t launch_decode_final_norm(const float *prev_out, uint16_t *x_export, int T, int d, cudaStream_t stream);
+}  // namespace lily
+
+namespace {
+
+using namespace lily;
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ workspace layouts
+struct PrefillLayout {
+    size_t ctrl, chunk_counts, chunk_base, h, logits, idx, w, counts, offsets, perm, block_map, n_blocks, total;
+};
+
+int64_t block_capacity(const lily_moe_shape &s)
+{
+    const int64_t a = static_cast<int64_t>(s.T) * s.top_k;
+    return std::max<int64_t>(1, std::min<int64_t>(a, s.E + ceil_div(a, s.block_rows)));
+}
+
+PrefillLayout prefill_layout(const lily_moe_shape &s)
+{
+    PrefillLayout L{};
+    const int64_t T = s.T, E = s.E, k = s.top_k;
+    const int64_t C = std::max<int64_t>(1, ceil_div(T, kRouteChunkTokens));
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + std::max<size_t>(bytes, 1));
+        return at;
+    };
+    L.ctrl = take(sizeof(Ctrl));
+    L.chunk_counts = take(C * E * 4);
+    L.chunk_base = take(C * E * 4);
+    L.h = take((k + 1) * T * s.I * 2);
+    L.logits = take(T * E * 4);
+    L.idx = take(T * k * 4);
+    L.w = take(T * k * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm = take(T * k * 4);
+    L.block_map = take(block_capacity(s) * 3 * 4);
+    L.n_blocks = take(4);
+    L.total = off;
+    return L;
+}
+
+struct DecodeLayout {
+    size_t ctrl, x_cur, logits, n_units, unit_expert, unit_mask, unit_w, h, total;
+};
+
+DecodeLayout decode_layout(const lily_moe_shape &s)
+{
+    DecodeLayout L{};
+    const int64_t T = s.T, U = static_cast<int64_t>(s.top_k) * s.T + 1;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + std::max<size_t>(bytes, 1));
+        return at;
+    };
+    L.ctrl = take(sizeof(Ctrl));
+    L.x_cur = take(T * s.d * 2);
+    L.logits = take(T * s.E * 4);
+    L.n_units = take(4);
+    L.unit_expert = take(U * 4);
+    L.unit_mask = take(U * 4);
+    L.unit_w = take(U * 8 * 4);
+    L.h = take(U * 8 * s.I * 2);
+    L.total = off;
+    return L;
+}
+
+template <typename P>
+P *at(void *ws, size_t off)
+{
+    return reinterpret_cast<P *>(static_cast<uint8_t *>(ws) + off);
+}
+
+// ------------------------------------------------------------------ validation
+int check_shape(const lily_moe_shape *s)
+{
+    if (!s) return LILY_ERR_INVALID;
+    if (s->T < 0 || s->d <= 0 || s->E <= 0 || s->top_k <= 0 || s->I <= 0 || s->I_shared <= 0 || s->group <= 0 ||
+        s->block_rows <= 0)
+        return LILY_ERR_INVALID;
+    if (s->E != 256 || s->top_k != 8 || s->group != 64) return LILY_ERR_UNSUPPORTED;
+    if (s->d % 256 != 0 || s->d > 16384) return LILY_ERR_UNSUPPORTED;
+    if (s->I % 128 != 0 || s->I > 4096) return LILY_ERR_UNSUPPORTED;
+    if (s->I_shared != s->I) return LILY_ERR_UNSUPPORTED;
+    if (s->block_rows != 16 && s->block_rows != 32 && s->block_rows != 64 && s->block_rows != 128)
+        return LILY_ERR_UNSUPPORTED;
+    if (s->T > (1 << 20)) return LILY_ERR_UNSUPPORTED;
+    return LILY_OK;
+}
+
+int check_q4(const lily_q4 &m)
+{
+    if (!m.q || !m.scale || !m.bias) return LILY_ERR_INVALID;
+    if (!aligned16(m.q) || !aligned16(m.scale) || !aligned16(m.bias)) return LILY_ERR_MISALIGNED;
+    return LILY_OK;
+}
+
+int check_weights(const lily_moe_weights *w)
+{
+    if (!w || !w->router_w) return LILY_ERR_INVALID;
+    if (!aligned16(w->router_w) || (w->router_bias && !aligned16(w->router_bias))) return LILY_ERR_MISALIGNED;
+    for (const lily_q4 *m : {&w->gate, &w->up, &w->down, &w->sh_gate, &w->sh_up, &w->sh_down}) {
+        const int rc = check_q4(*m);
+        if (rc) return rc;
+    }
+    return LILY_OK;
+}
+
+int check_ptr(const void *p)
+{
+    if (!p) return LILY_ERR_INVALID;
+    if (!aligned16(p)) return LILY_ERR_MISALIGNED;
+    return LILY_OK;
+}
+
+int check_ws(const void *ws, size_t ws_bytes, size_t need)
+{
+    const int rc = check_ptr(ws);
+    if (rc) return rc;
+    if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return LILY_ERR_MISALIGNED;
+    if (ws_bytes < need) return LILY_ERR_WORKSPACE;
+    return LILY_OK;
+}
+
+// ------------------------------------------------------------------ device properties
+int num_sms_current()
+{
+    static std::mutex mu;
+    static std::unordered_map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+    return n;
+}
+
+// ------------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor [rows][inner] with a box of [box_rows][box_inner].
+bool make_tmap(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int elem_bytes, uint64_t inner, uint64_t rows,
+               uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, std::max<uint64_t>(rows, 1)};
+    const cuuint64_t strides[1] = {inner * elem_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tmap_bf16_sw128(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows)
+{
+    return make_tmap(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool tmap_q4(CUtensorMap *m, const uint8_t *q, uint64_t K, uint64_t rows)
+{
+    return make_tmap(m, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+}  // namespace
+
+namespace {
+
+// ------------------------------------------------------------------ enqueue helpers
+cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, const uint16_t *x,
+                          const lily_moe_routing &r, float *logits, void *ws, cudaStream_t stream)
+{
+    const PrefillLayout L = prefill_layout(s);
+    Ctrl *ctrl = at<Ctrl>(ws, L.ctrl);
+    CUtensorMap tmX, tmWr;
+    if (!tmap_bf16_sw128(&tmX, x, s.d, s.T) || !tmap_bf16_sw128(&tmWr, w.router_w, s.d, s.E))
+        return cudaErrorInvalidValue;
+
+    GemmArgs g{};
+    g.mode = kModeRouter;
+    g.T = s.T; g.d = s.d; g.E = s.E; g.top_k = s.top_k; g.I = s.I;
+    g.bm = 128;
+    g.K = s.d;
+    g.m_tiles = 1;
+    g.n_shared_blocks = static_cast<int>(ceil_div(s.T, 128));
+    g.n_routed_max = 0;
+    g.router_bias = w.router_bias;
+    g.logits = logits;
+    g.ctrl = ctrl;
+    const int sms = num_sms_current();
+    const int grid = std::max(1, std::min(sms, g.n_shared_blocks));
+    cudaError_t e = launch_grouped_gemm(g, tmX, tmWr, tmWr, tmWr, tmWr, grid, stream);
+    if (e != cudaSuccess) return e;
+
+    RouteArgs ra{};
+    ra.T = s.T; ra.E = s.E; ra.top_k = s.top_k; ra.bm = s.block_rows;
+    ra.logits = logits;
+    ra.topk_idx = r.topk_idx; ra.topk_w = r.topk_w;
+    ra.counts = r.counts; ra.offsets = r.offsets; ra.perm = r.perm;
+    ra.block_map = r.block_map; ra.n_blocks = r.n_blocks;
+    ra.chunk_counts = at<int>(ws, L.chunk_counts);
+    ra.chunk_base = at<int>(ws, L.chunk_base);
+    ra.n_chunks = static_cast<int>(ceil_div(s.T, kRouteChunkTokens));
+    ra.ctrl = ctrl;
+    if ((e = launch_topk_count(ra, stream)) != cudaSuccess) return e;
+    return launch_scatter(ra, stream);
+}
+
+cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, const uint16_t *x,
+                            const lily_moe_routing &r, float *out, void *ws, cudaStream_t stream,
+                            cudaEvent_t *events)
+{
+    const PrefillLayout L = prefill_layout(s);
+    Ctrl *ctrl = at<Ctrl>(ws, L.ctrl);
+    __nv_bfloat16 *h = at<__nv_bfloat16>(ws, L.h);
+    const int64_t hrows = static_cast<int64_t>(s.top_k + 1) * s.T;
+    CUtensorMap tmX, tmH, tmG, tmU, tmD, tmSG, tmSU, tmSD;
+    if (!tmap_bf16_sw128(&tmX, x, s.d, s.T) || !tmap_bf16_sw128(&tmH, h, s.I, hrows) ||
+        !tmap_q4(&tmG, w.gate.q, s.d, static_cast<uint64_t>(s.E) * s.I) ||
+        !tmap_q4(&tmU, w.up.q, s.d, static_cast<uint64_t>(s.E) * s.I) ||
+        !tmap_q4(&tmD, w.down.q, s.I, static_cast<uint64_t>(s.E) * s.d) || !tmap_q4(&tmSG, w.sh_gate.q, s.d, s.I) ||
+        !tmap_q4(&tmSU, w.sh_up.q, s.d, s.I) || !tmap_q4(&tmSD, w.sh_down.q, s.I, s.d))
+        return cudaErrorInvalidValue;
+
+    cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(s.T) * s.d * sizeof(float), stream);
+    if (e != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[3], stream)) != cudaSuccess) return e;
+
+    const int sms = num_sms_current();
+    const int64_t cap = block_capacity(s);
+    GemmArgs g{};
+    g.T = s.T; g.d = s.d; g.E = s.E; g.top_k = s.top_k; g.I = s.I;
+    g.bm = s.block_rows;
+    g.n_shared_blocks = static_cast<int>(ceil_div(s.T, s.block_rows));
+    g.n_routed_max = static_cast<int>(cap);
+    g.n_blocks = r.n_blocks;
+    g.block_map = r.block_map;
+    g.perm = r.perm;
+    g.topk_w = r.topk_w;
+    g.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    g.h = h;
+    g.out = out;
+    g.ctrl = ctrl;
+
+    // gate/up + SwiGLU
+    g.mode = kModeGateUp;
+    g.K = s.d;
+    g.m_tiles = s.I / 128;
+    g.s0 = w.gate.scale; g.b0 = w.gate.bias; g.s1 = w.up.scale; g.b1 = w.up.bias;
+    g.ss0 = w.sh_gate.scale; g.sb0 = w.sh_gate.bias; g.ss1 = w.sh_up.scale; g.sb1 = w.sh_up.bias;
+    int64_t units = (cap + g.n_shared_blocks) * g.m_tiles;
+    int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, units)));
+    if ((e = launch_grouped_gemm(g, tmX, tmG, tmU, tmSG, tmSU, grid, stream)) != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[4], stream)) != cudaSuccess) return e;
+
+    // down + weighted combine
+    g.mode = kModeDown;
+    g.K = s.I;
+    g.m_tiles = s.d / 256;
+    g.s0 = g.s1 = w.down.scale; g.b0 = g.b1 = w.down.bias;
+    g.ss0 = g.ss1 = w.sh_down.scale; g.sb0 = g.sb1 = w.sh_down.bias;
+    units = (cap + g.n_shared_blocks) * g.m_tiles;
+    grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, units)));
+    if ((e = launch_grouped_gemm(g, tmH, tmD, tmD, tmSD, tmSD, grid, stream)) != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[5], stream)) != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
+int check_routing(const lily_moe_routing *r, bool for_route)
+{
+    if (!r) return LILY_ERR_INVALID;
+    int rc;
+    if ((rc = check_ptr(r->topk_w)) || (rc = check_ptr(r->perm)) || (rc = check_ptr(r->block_map)) ||
+        (rc = check_ptr(r->n_blocks)))
+        return rc;
+    if (for_route) {
+        if ((rc = check_ptr(r->topk_idx)) || (rc = check_ptr(r->counts)) || (rc = check_ptr(r->offsets))) return rc;
+        if (r->logits && !aligned16(r->logits)) return LILY_ERR_MISALIGNED;
+    }
+    return LILY_OK;
+}
+
+lily_moe_routing internal_routing(const lily_moe_shape &s, void *ws)
+{
+    const PrefillLayout L = prefill_layout(s);
+    lily_moe_routing r{};
+    r.logits = at<float>(ws, L.logits);
+    r.topk_idx = at<int32_t>(ws, L.idx);
+    r.topk_w = at<float>(ws, L.w);
+    r.counts = at<int32_t>(ws, L.counts);
+    r.offsets = at<int32_t>(ws, L.offsets);
+    r.perm = at<int32_t>(ws, L.perm);
+    r.block_map = at<int32_t>(ws, L.block_map);
+    r.n_blocks = at<int32_t>(ws, L.n_blocks);
+    return r;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? LILY_OK : LILY_ERR_LAUNCH; }
+
+// ------------------------------------------------------------------ decode graph cache
+struct GraphCache {
+    std::mutex mu;
+    std::unordered_map<std::string, cudaGraphExec_t> execs;
+};
+GraphCache &graph_cache()
+{
+    static GraphCache *c = new GraphCache();  // never destroyed: graphs live until process exit
+    return *c;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lily_moe_version(void) { return kVersion; }
+
+const char *lily_moe_status_string(int status)
+{
+    switch (status) {
+    case LILY_OK: return "ok";
+    case LILY_ERR_INVALID: return "invalid argument";
+    case LILY_ERR_UNSUPPORTED: return "unsupported shape";
+    case LILY_ERR_MISALIGNED: return "misaligned device pointer (16 bytes required; workspace 256 bytes)";
+    case LILY_ERR_WORKSPACE: return "workspace too small";
+    case LILY_ERR_LAUNCH: return "CUDA error while enqueueing";
+    case LILY_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case LILY_ERR_DEVICE_INDEX: return "device index out of range";
+    default: return "unknown status";
+    }
+}
+
+int lily_moe_check_shape(const lily_moe_shape *shape) { return check_shape(shape); }
+
+int64_t lily_moe_block_capacity(const lily_moe_shape *shape)
+{
+    if (check_shape(shape) != LILY_OK) return 0;
+    return block_capacity(*shape);
+}
+
+size_t lily_moe_workspace_bytes(const lily_moe_shape *shape, int32_t n_layers_decode)
+{
+    if (check_shape(shape) != LILY_OK) return 0;
+    size_t need = prefill_layout(*shape).total;
+    if (n_layers_decode > 0) {
+        if (shape->T < 1 || shape->T > 8 || shape->d > 8192 || shape->I > 1024) return 0;
+        need = std::max(need, decode_layout(*shape).total);
+    }
+    return need;
+}
+
+int lily_moe_route(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x, lily_moe_routing *r,
+                   void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    int rc;
+    if ((rc = check_shape(shape)) || (rc = check_weights(w)) || (rc = check_routing(r, true))) return rc;
+    if ((rc = check_ws(ws, ws_bytes, prefill_layout(*shape).total))) return rc;
+    if (shape->T == 0) return LILY_OK;
+    if ((rc = check_ptr(x))) return rc;
+    float *logits = r->logits ? r->logits : at<float>(ws, prefill_layout(*shape).logits);
+    return to_status(enqueue_route(*shape, *w, x, *r, logits, ws, stream));
+}
+
+int lily_moe_grouped_gemm(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,
+                          const lily_moe_routing *r, float *out, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    int rc;
+    if ((rc = check_shape(shape)) || (rc = check_weights(w)) || (rc = check_routing(r, false))) return rc;
+    if ((rc = check_ws(ws, ws_bytes, prefill_layout(*shape).total))) return rc;
+    if (shape->T == 0) return LILY_OK;
+    if ((rc = check_ptr(x)) || (rc = check_ptr(out))) return rc;
+    return to_status(enqueue_experts(*shape, *w, x, *r, out, ws, stream, nullptr));
+}
+
+int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x, float *out,
+                           lily_moe_routing *r, void *ws, size_t ws_bytes, cudaStream_t stream, cudaEvent_t *events)
+{
+    int rc;
+    if ((rc = check_shape(shape)) || (rc = check_weights(w))) return rc;
+    if (r && (rc = check_routing(r, true))) return rc;
+    if ((rc = check_ws(ws, ws_bytes, prefill_layout(*shape).total))) return rc;
+    if (shape->T == 0) return LILY_OK;
+    if ((rc = check_ptr(x)) || (rc = check_ptr(out))) return rc;
+    const lily_moe_routing rr = r ? *r : internal_routing(*shape, ws);
+    float *logits = rr.logits ? rr.logits : at<float>(ws, prefill_layout(*shape).logits);
+    cudaError_t e = cudaSuccess;
+    if (events && (e = cudaEventRecord(events[0], stream)) != cudaSuccess) return LILY_ERR_LAUNCH;
+    if ((e = enqueue_route(*shape, *w, x, rr, logits, ws, stream)) != cudaSuccess) return LILY_ERR_LAUNCH;
+    if (events) {
+        // the router GEMM and the two routing kernels are one unit here
+        if (cudaEventRecord(events[1], stream) != cudaSuccess || cudaEventRecord(events[2], stream) != cudaSuccess)
+            return LILY_ERR_LAUNCH;
+    }
+    return to_status(enqueue_experts(*shape, *w, x, rr, out, ws, stream, events));
+}
+
+int lily_moe_forward(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x, float *out,
+                     lily_moe_routing *r, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    return lily_moe_forward_timed(shape, w, x, out, r, ws, ws_bytes, stream, nullptr);
+}
+
+int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_moe_weights *layers, const uint16_t *x,
+                    float *out, uint16_t *x_next, const lily_moe_decode_trace *trace, void *ws, size_t ws_bytes,
+                    cudaStream_t stream)
+{
+    int rc;
+    if ((rc = check_shape(shape))) return rc;
+    if (n_layers < 1 || !layers) return LILY_ERR_INVALID;
+    if (shape->T < 1 || shape->T > 8 || shape->d > 8192 || shape->I > 1024) return LILY_ERR_UNSUPPORTED;
+    for (int l = 0; l < n_layers; ++l)
+        if ((rc = check_weights(&layers[l]))) return rc;
+    if ((rc = check_ws(ws, ws_bytes, decode_layout(*shape).total))) return rc;
+    if ((rc = check_ptr(x)) || (rc = check_ptr(out))) return rc;
+    if (x_next && !aligned16(x_next)) return LILY_ERR_MISALIGNED;
+    if (trace && ((trace->logits && !aligned16(trace->logits)) || (trace->topk_idx && !aligned16(trace->topk_idx)) ||
+                  (trace->topk_w && !aligned16(trace->topk_w))))
+        return LILY_ERR_MISALIGNED;
+
+    const lily_moe_shape s = *shape;
+    const DecodeLayout L = decode_layout(s);
+    const int sms = num_sms_current();
+    const size_t td = static_cast<size_t>(s.T) * s.d;
+
+    auto enqueue_all = [&](cudaStream_t st) -> cudaError_t {
+        Ctrl *ctrl = at<Ctrl>(ws, L.ctrl);
+        cudaError_t e = cudaMemsetAsync(&ctrl->ticket2, 0, sizeof(unsigned int), st);
+        if (e != cudaSuccess) return e;
+        for (int l = 0; l < n_layers; ++l) {
+            const lily_moe_weights &w = layers[l];
+            DecodeLayerArgs a{};
+            a.T = s.T; a.d = s.d; a.E = s.E; a.top_k = s.top_k; a.I = s.I; a.layer = l;
+            a.router_w = w.router_w; a.router_bias = w.router_bias;
+            a.gate_q = w.gate.q; a.up_q = w.up.q; a.down_q = w.down.q;
+            a.gate_s = w.gate.scale; a.gate_b = w.gate.bias; a.up_s = w.up.scale; a.up_b = w.up.bias;
+            a.down_s = w.down.scale; a.down_b = w.down.bias;
+            a.sh_gate_q = w.sh_gate.q; a.sh_up_q = w.sh_up.q; a.sh_down_q = w.sh_down.q;
+            a.sh_gate_s = w.sh_gate.scale; a.sh_gate_b = w.sh_gate.bias; a.sh_up_s = w.sh_up.scale;
+            a.sh_up_b = w.sh_up.bias; a.sh_down_s = w.sh_down.scale; a.sh_down_b = w.sh_down.bias;
+            a.x_in = l == 0 ? x : nullptr;
+            a.prev_out = l == 0 ? nullptr : out + (l - 1) * td;
+            a.out = out + l * td;
+            a.x_export = (l > 0 && x_next) ? x_next + (l - 1) * td : nullptr;
+            if (trace) {
+                a.trace_logits = trace->logits ? trace->logits + static_cast<size_t>(l) * s.T * s.E : nullptr;
+                a.trace_idx = trace->topk_idx ? trace->topk_idx + static_cast<size_t>(l) * s.T * s.top_k : nullptr;
+                a.trace_w = trace->topk_w ? trace->topk_w + static_cast<size_t>(l) * s.T * s.top_k : nullptr;
+            }
+            a.x_cur = at<uint16_t>(ws, L.x_cur);
+            a.logits = at<float>(ws, L.logits);
+            a.n_units = at<int>(ws, L.n_units);
+            a.unit_expert = at<int>(ws, L.unit_expert);
+            a.unit_mask = at<int>(ws, L.unit_mask);
+            a.unit_w = at<float>(ws, L.unit_w);
+            a.h = at<__nv_bfloat16>(ws, L.h);
+            a.ctrl = ctrl;
+            if ((e = launch_decode_layer(a, sms, st)) != cudaSuccess) return e;
+        }
+        if (x_next)
+            return launch_decode_final_norm(out + (n_layers - 1) * td, x_next + (n_layers - 1) * td, s.T, s.d, st);
+        return cudaSuccess;
+    };
+
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return LILY_ERR_LAUNCH;
+    if (cs != cudaStreamCaptureStatusNone) return to_status(enqueue_all(stream));
+
+    // Key: every argument value that the recorded launches depend on.
+    std::string key;
+    auto put = [&key](const void *p, size_t n) { key.append(static_cast<const char *>(p), n); };
+    int dev = 0;
+    cudaGetDevice(&dev);
+    put(&dev, sizeof dev);
+    put(&s, sizeof s);
+    put(&n_layers, sizeof n_layers);
+    put(layers, sizeof(lily_moe_weights) * n_layers);
+    put(&x, sizeof x); put(&out, sizeof out); put(&x_next, sizeof x_next); put(&ws, sizeof ws);
+    const lily_moe_decode_trace tr = trace ? *trace : lily_moe_decode_trace{};
+    put(&tr, sizeof tr);
+
+    GraphCache &gc = graph_cache();
+    std::lock_guard<std::mutex> lock(gc.mu);
+    auto it = gc.execs.find(key);
+    if (it == gc.execs.end()) {
+        cudaStream_t cap;
+        if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) return LILY_ERR_LAUNCH;
+        cudaGraph_t graph = nullptr;
+        cudaError_t e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+        if (e == cudaSuccess) {
+            const cudaError_t e1 = enqueue_all(cap);
+            const cudaError_t e2 = cudaStreamEndCapture(cap, &graph);
+            e = e1 != cudaSuccess ? e1 : e2;
+        }
+        cudaGraphExec_t exec = nullptr;
+        if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+        if (graph) cudaGraphDestroy(graph);
+        cudaStreamDestroy(cap);
+        if (e != cudaSuccess) return LILY_ERR_LAUNCH;
+        if (gc.execs.size() >= 64) {
+            for (auto &kv : gc.execs) cudaGraphExecDestroy(kv.second);
+            gc.execs.clear();
+        }
+        it = gc.execs.emplace(key, exec).first;
+    }
+    return to_status(cudaGraphLaunch(it->second, stream));
+}
+
+int lily_moe_device_status(const void *ws, cudaStream_t stream)
+{
+    if (!ws) return LILY_ERR_INVALID;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return LILY_ERR_LAUNCH;
+    int status = 0;
+    if (cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LILY_ERR_LAUNCH;
+    return status;
+}
+
+int lily_moe_clear_status(void *ws, cudaStream_t stream)
+{
+    if (!ws) return LILY_ERR_INVALID;
+    return to_status(cudaMemsetAsync(ws, 0, sizeof(int), stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,504 @@
+// Persistent, warp-specialised tcgen05 grouped GEMM for the MoE layer on sm_103a.
+//
+// Method (page "Perplexity libera o Lily", noticiai.com.br, section "Prefill e
+// decode: onde estao os ganhos"): the expert GEMMs run over uneven per-expert
+// token groups, and the 4-bit group-64 affine weights are rebuilt to bf16 one
+// tile at a time inside the GEMM, held on chip, with FP32 accumulation.
+//
+// GB300 design.  The weights take the UMMA M side (128 rows per tile, two
+// tiles per work unit sharing one B operand: gate+up rows of the same
+// intermediate slice, or two adjacent 128-row slices of the down projection)
+// and the tokens of one block-map entry take the N side (N = rows rounded up
+// to 16, at most 128), so small expert groups waste little tensor work.
+// One CTA per SM loops over work units:
+//   warp 0        producer: TMA of the packed int4 tile (and of bf16 A for the
+//                 router), TMA of contiguous B rows, or cp.async gathers of
+//                 token rows of x by the routing permutation (gate/up);
+//   warp 1        TMEM allocator + single-thread tcgen05.mma issuer;
+//   warps 4..11   dequantisers: int4 -> bf16 (one matrix per warpgroup, one
+//                 row per thread) written in the 128-byte swizzled K-major
+//                 layout the tensor core reads;
+//   warps 12..15  epilogue: tcgen05.ld from TMEM, then per mode the router
+//                 logits (+bias), SwiGLU into h (bf16), or the down projection
+//                 scaled by the routing weight and added (red.global.add.f32)
+//                 into token order.
+// Accumulators are double-buffered in TMEM (2 x 2 x 128 fp32 columns), so the
+// epilogue of one unit overlaps the main loop of the next.
+// Every wait is bounded; on timeout the kernel records the error, drains its
+// in-flight copies and tensor-core work, frees TMEM and returns.
+#include <cstdio>
+
+#include "lily_device.cuh"
+#include "lily_internal.h"
+
+namespace lily {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kAStages = 3;   // dequantised A ring
+constexpr int kLStages = 4;   // load ring: raw int4 + B
+constexpr int kLag = 2;       // cp.async groups kept in flight by the gathering producer
+constexpr int kTileM = 128;
+constexpr int kBK = 64;       // one quantisation group, one 128-byte swizzle row
+constexpr int kTileN = 128;
+constexpr int kABytes = kTileM * kBK * 2;    // 16 KB bf16
+constexpr int kBBytes = kTileN * kBK * 2;    // 16 KB bf16
+constexpr int kRawBytes = kTileM * kBK / 2;  // 4 KB int4
+constexpr uint32_t kTmemCols = 512;
+
+struct __align__(1024) Smem {
+    uint8_t a[kAStages][2][kABytes];
+    uint8_t b[kLStages][kBBytes];
+    uint8_t raw[kLStages][2][kRawBytes];
+    uint64_t full_l[kLStages], empty_l[kLStages];
+    uint64_t full_a[kAStages], empty_a[kAStages];
+    uint64_t full_acc[2], empty_acc[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int prod_tok[kTileN];  // producer: source row of each B row of the current unit
+    int ep_tok[kTileN];    // epilogue: token of each column (down)
+    float ep_w[kTileN];    // epilogue: routing weight of each column (down)
+};
+
+struct Unit {
+    int e, p0, rows, n_mma, mt;
+    bool shared;
+};
+
+__device__ __forceinline__ Unit unit_info(const GemmArgs &g, int tile, int n_routed)
+{
+    Unit u;
+    const int b = tile / g.m_tiles;
+    u.mt = tile - b * g.m_tiles;
+    if (g.mode != kModeRouter && b < n_routed) {
+        const int *bm = g.block_map + 3 * b;
+        u.e = bm[0];
+        u.p0 = bm[1];
+        u.rows = bm[2];
+        u.shared = false;
+        if (u.e < 0 || u.e >= g.E || u.p0 < 0 || u.rows < 1 || u.rows > g.bm || u.p0 + u.rows > g.T * g.top_k) {
+            record_error(&g.ctrl->status, kErrDeviceIndex);
+            u.rows = 0;
+        }
+    } else {
+        const int sb = (g.mode == kModeRouter) ? b : b - n_routed;
+        u.e = -1;
+        u.p0 = sb * g.bm;
+        u.rows = min(g.bm, g.T - u.p0);
+        u.shared = true;
+    }
+    u.n_mma = (u.rows + 15) & ~15;
+    return u;
+}
+
+// First weight row of the two 128-row A tiles of a unit.
+__device__ __forceinline__ void a_rows(const GemmArgs &g, const Unit &u, int &r0, int &r1)
+{
+    if (g.mode == kModeRouter) {
+        r0 = 0;
+        r1 = kTileM;
+    } else if (g.mode == kModeGateUp) {
+        r0 = (u.shared ? 0 : u.e * g.I) + u.mt * kTileM;
+        r1 = r0;
+    } else {
+        r0 = (u.shared ? 0 : u.e * g.d) + u.mt * 2 * kTileM;
+        r1 = r0 + kTileM;
+    }
+}
+
+// Wait used on the exit path: bounded, ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, int *status)
+{
+    const uint32_t addr = smem_u32(bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(addr, parity)) {
+        if (global_timer_ns() - t0 > LILY_WAIT_LIMIT_NS) {
+            record_error(status, kErrDeviceTimeout);
+            return;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                    const __grid_constant__ CUtensorMap tmSA0, const __grid_constant__ CUtensorMap tmSA1)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem &S = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int *status = &g.ctrl->status;
+    const bool dequant_mode = g.mode != kModeRouter;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kLStages; ++s) {
+            mbar_init(&S.full_l[s], g.mode == kModeGateUp ? 1 + 32 : 1);
+            mbar_init(&S.empty_l[s], dequant_mode ? 3 : 1);
+        }
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(&S.full_a[s], dequant_mode ? 2 : 1);
+            mbar_init(&S.empty_a[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&S.full_acc[s], 1);
+            mbar_init(&S.empty_acc[s], 4);
+        }
+        mbar_init(&S.drain, 1);
+        S.abort_flag = 0;
+        fence_mbar_init();
+        if (g.mode == kModeRouter && blockIdx.x == 0) g.ctrl->ticket = 0u;  // reset for the routing kernel
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA0);
+        prefetch_tmap(&tmA1);
+        if (g.mode != kModeGateUp) prefetch_tmap(&tmB);
+        if (g.mode != kModeRouter) {
+            prefetch_tmap(&tmSA0);
+            prefetch_tmap(&tmSA1);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(&S.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = S.tmem_base;
+    volatile int *abort_flag = &S.abort_flag;
+
+    int n_routed = 0;
+    if (g.mode != kModeRouter) {
+        n_routed = *g.n_blocks;
+        if (n_routed < 0 || n_routed > g.n_routed_max) {
+            if (threadIdx.x == 0) record_error(status, kErrDeviceIndex);
+            n_routed = 0;
+        }
+    }
+    const int total_tiles = (n_routed + g.n_shared_blocks) * g.m_tiles;
+    const int KT = g.K / kBK;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int ls = 0, as = 0;
+        uint32_t lph = 0, aph = 0;
+        int issued = 0;       // load-ring steps issued
+        int p_old = 0, p_new = 0, n_pend = 0;  // gate/up: stages awaiting their cp.async group
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            const Unit u = unit_info(g, tile, n_routed);
+            if (u.rows <= 0) continue;
+            int r0, r1;
+            a_rows(g, u, r0, r1);
+            const CUtensorMap *mA0 = u.shared ? &tmSA0 : &tmA0;
+            const CUtensorMap *mA1 = u.shared ? &tmSA1 : &tmA1;
+            if (g.mode == kModeGateUp) {
+                for (int r = lane; r < u.n_mma; r += 32) {
+                    const int rr = min(r, u.rows - 1);
+                    int src = u.p0 + rr;
+                    if (!u.shared) src = g.perm[u.p0 + rr] / g.top_k;
+                    if (src < 0 || src >= g.T) {
+                        record_error(status, kErrDeviceIndex);
+                        src = 0;
+                    }
+                    S.prod_tok[r] = src;
+                }
+                __syncwarp();
+            }
+            const int b_row0 = (g.mode == kModeDown && u.shared) ? g.T * g.top_k + u.p0 : u.p0;
+            for (int kt = 0; kt < KT; ++kt) {
+                int good = 1;
+                if (lane == 0) {
+                    good = mbar_wait(&S.empty_l[ls], lph ^ 1, abort_flag, status);
+                    if (good && g.mode == kModeRouter) good = mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status);
+                }
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    if (g.mode == kModeRouter) {
+                        mbar_arrive_expect_tx(&S.full_a[as], 2 * kABytes);
+                        tma_load_2d(S.a[as][0], &tmA0, &S.full_a[as], kt * kBK, r0);
+                        tma_load_2d(S.a[as][1], &tmA0, &S.full_a[as], kt * kBK, r1);
+                        mbar_arrive_expect_tx(&S.full_l[ls], kBBytes);
+                        tma_load_2d(S.b[ls], &tmB, &S.full_l[ls], kt * kBK, b_row0);
+                    } else if (g.mode == kModeDown) {
+                        mbar_arrive_expect_tx(&S.full_l[ls], 2 * kRawBytes + kBBytes);
+                        tma_load_2d(S.raw[ls][0], mA0, &S.full_l[ls], kt * (kBK / 2), r0);
+                        tma_load_2d(S.raw[ls][1], mA1, &S.full_l[ls], kt * (kBK / 2), r1);
+                        tma_load_2d(S.b[ls], &tmB, &S.full_l[ls], kt * kBK, b_row0);
+                    } else {
+                        mbar_arrive_expect_tx(&S.full_l[ls], 2 * kRawBytes);
+                        tma_load_2d(S.raw[ls][0], mA0, &S.full_l[ls], kt * (kBK / 2), r0);
+                        tma_load_2d(S.raw[ls][1], mA1, &S.full_l[ls], kt * (kBK / 2), r1);
+                    }
+                }
+                if (g.mode == kModeGateUp) {
+                    // Gather token rows: each (row, 16-byte chunk) pair lands in its
+                    // 128-byte-swizzled position.
+                    const int c = lane & 7;
+                    const __nv_bfloat16 *xk = g.x + kt * kBK + c * 8;
+                    uint8_t *bst = S.b[ls];
+                    for (int r = lane >> 3; r < u.n_mma; r += 4) {
+                        const int src = S.prod_tok[r];
+                        cp_async_16(bst + r * 128 + ((c ^ (r & 7)) << 4), xk + static_cast<size_t>(src) * g.d);
+                    }
+                    cp_async_commit();
+                    if (n_pend == kLag) {
+                        cp_async_wait_group<kLag>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(&S.full_l[p_old]);
+                        p_old = p_new;
+                        p_new = ls;
+                    } else if (n_pend == 1) {
+                        p_new = ls;
+                        n_pend = 2;
+                    } else {
+                        p_old = ls;
+                        n_pend = 1;
+                    }
+                }
+                ++issued;
+                if (++ls == kLStages) {
+                    ls = 0;
+                    lph ^= 1;
+                }
+                if (g.mode == kModeRouter && ++as == kAStages) {
+                    as = 0;
+                    aph ^= 1;
+                }
+            }
+        }
+        if (g.mode == kModeGateUp) {
+            cp_async_wait_all();
+            fence_proxy_async_smem();
+            if (n_pend >= 1) mbar_arrive(&S.full_l[p_old]);
+            if (n_pend == 2) mbar_arrive(&S.full_l[p_new]);
+        }
+        // Exit: make sure no copy into this CTA's shared memory is still in flight.
+        if (lane == 0) {
+            const int last = issued < kLStages ? issued : kLStages;
+            for (int i = 1; i <= last; ++i) {
+                const int step = issued - i;
+                drain_wait(&S.full_l[step % kLStages], (step / kLStages) & 1, status);
+            }
+            if (g.mode == kModeRouter) {
+                const int lasta = issued < kAStages ? issued : kAStages;
+                for (int i = 1; i <= lasta; ++i) {
+                    const int step = issued - i;
+                    drain_wait(&S.full_a[step % kAStages], (step / kAStages) & 1, status);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int ls = 0, as = 0, ab = 0;
+            uint32_t lph = 0, aph = 0, acc_ph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+                const Unit u = unit_info(g, tile, n_routed);
+                if (u.rows <= 0) continue;
+                if (!mbar_wait(&S.empty_acc[ab], acc_ph ^ 1, abort_flag, status)) break;
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(kTileM, u.n_mma);
+                const uint32_t d0 = tmem_base + static_cast<uint32_t>(ab * 2 * kTileM);
+                const uint32_t d1 = d0 + kTileM;
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(&S.full_a[as], aph, abort_flag, status) ||
+                        !mbar_wait(&S.full_l[ls], lph, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(S.a[as][0]);
+                    const uint32_t a1 = smem_u32(S.a[as][1]);
+                    const uint32_t bb = smem_u32(S.b[ls]);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint32_t acc = (kt | kk) != 0;
+                        umma_bf16_ss(d0, sdesc_sw128(a0 + kk * 32), sdesc_sw128(bb + kk * 32), idesc, acc);
+                        umma_bf16_ss(d1, sdesc_sw128(a1 + kk * 32), sdesc_sw128(bb + kk * 32), idesc, acc);
+                    }
+                    umma_commit(&S.empty_a[as]);
+                    umma_commit(&S.empty_l[ls]);
+                    if (++as == kAStages) {
+                        as = 0;
+                        aph ^= 1;
+                    }
+                    if (++ls == kLStages) {
+                        ls = 0;
+                        lph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&S.full_acc[ab]);
+                if (++ab == 2) {
+                    ab = 0;
+                    acc_ph ^= 1;
+                }
+            }
+            // All tensor-core work of this CTA must finish before TMEM is freed.
+            umma_commit(&S.drain);
+            drain_wait(&S.drain, 0, status);
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------------------ dequantisers
+        if (dequant_mode) {
+            const int mi = (warp - 4) >> 2;              // which matrix of the pair
+            const int r = ((warp - 4) & 3) * 32 + lane;  // row within the 128-row tile
+            const int ngroups = g.K / kBK;
+            int ls = 0, as = 0;
+            uint32_t lph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+                const Unit u = unit_info(g, tile, n_routed);
+                if (u.rows <= 0) continue;
+                int r0, r1;
+                a_rows(g, u, r0, r1);
+                const int row = (mi ? r1 : r0) + r;
+                const uint16_t *srow = (u.shared ? (mi ? g.ss1 : g.ss0) : (mi ? g.s1 : g.s0)) + static_cast<size_t>(row) * ngroups;
+                const uint16_t *brow = (u.shared ? (mi ? g.sb1 : g.sb0) : (mi ? g.b1 : g.b0)) + static_cast<size_t>(row) * ngroups;
+                uint16_t sc = __ldg(srow), bi = __ldg(brow);
+                for (int kt = 0; kt < KT; ++kt) {
+                    uint16_t sc_n = 0, bi_n = 0;
+                    if (kt + 1 < KT) {
+                        sc_n = __ldg(srow + kt + 1);
+                        bi_n = __ldg(brow + kt + 1);
+                    }
+                    if (!mbar_wait(&S.full_l[ls], lph, abort_flag, status) ||
+                        !mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint4 *src = reinterpret_cast<const uint4 *>(S.raw[ls][mi] + r * (kBK / 2));
+                    const uint4 q0 = src[0], q1 = src[1];
+                    const __nv_bfloat162 s2 = bf16x2_splat(sc), b2 = bf16x2_splat(bi);
+                    uint8_t *dst = S.a[as][mi] + (r >> 3) * 1024 + (r & 7) * 128;
+                    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) = dequant8_bf16(words[c], s2, b2);
+                    fence_proxy_async_smem();
+                    named_barrier_sync(1 + mi, 128);
+                    if (r == 0) {
+                        mbar_arrive(&S.full_a[as]);
+                        mbar_arrive(&S.empty_l[ls]);
+                    }
+                    sc = sc_n;
+                    bi = bi_n;
+                    if (++ls == kLStages) {
+                        ls = 0;
+                        lph ^= 1;
+                    }
+                    if (++as == kAStages) {
+                        as = 0;
+                        aph ^= 1;
+                    }
+                }
+            }
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp & 3;         // TMEM lane quarter this warp may access
+        const int et = ew * 32 + lane;   // accumulator row (weight row within the tile)
+        int ab = 0;
+        uint32_t acc_ph = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            const Unit u = unit_info(g, tile, n_routed);
+            if (u.rows <= 0) continue;
+            if (g.mode == kModeDown && et < u.rows) {
+                int tok = u.p0 + et;
+                float wt = 1.0f;
+                if (!u.shared) {
+                    const int a = g.perm[u.p0 + et];
+                    tok = a / g.top_k;
+                    wt = g.topk_w[a];
+                }
+                if (tok < 0 || tok >= g.T) {
+                    record_error(status, kErrDeviceIndex);
+                    tok = 0;
+                    wt = 0.0f;
+                }
+                S.ep_tok[et] = tok;
+                S.ep_w[et] = wt;
+            }
+            named_barrier_sync(3, 128);
+            if (!mbar_wait(&S.full_acc[ab], acc_ph, abort_flag, status)) break;
+            tc_fence_after();
+            const uint32_t t0 = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(ab * 2 * kTileM);
+            const uint32_t t1 = t0 + kTileM;
+            float bias0 = 0.0f, bias1 = 0.0f;
+            if (g.mode == kModeRouter && g.router_bias) {
+                bias0 = g.router_bias[et];
+                bias1 = g.router_bias[kTileM + et];
+            }
+            for (int c0 = 0; c0 < u.n_mma; c0 += 32) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(t0 + c0, v0);
+                tmem_ld_32x32b_x32(t1 + c0, v1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int n = c0 + j;
+                    if (n < u.rows) {
+                        const float f0 = __uint_as_float(v0[j]), f1 = __uint_as_float(v1[j]);
+                        if (g.mode == kModeRouter) {
+                            float *lrow = g.logits + static_cast<size_t>(u.p0 + n) * g.E;
+                            lrow[et] = f0 + bias0;
+                            lrow[kTileM + et] = f1 + bias1;
+                        } else if (g.mode == kModeGateUp) {
+                            const size_t p = u.shared ? static_cast<size_t>(g.T) * g.top_k + u.p0 + n : static_cast<size_t>(u.p0 + n);
+                            g.h[p * g.I + u.mt * kTileM + et] = __float2bfloat16_rn(silu_f(f0) * f1);
+                        } else {
+                            float *orow = g.out + static_cast<size_t>(S.ep_tok[n]) * g.d + u.mt * 2 * kTileM;
+                            const float wt = S.ep_w[n];
+                            atomicAdd(orow + et, wt * f0);
+                            atomicAdd(orow + kTileM + et, wt * f1);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty_acc[ab]);
+            named_barrier_sync(3, 128);
+            if (++ab == 2) {
+                ab = 0;
+                acc_ph ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+}  // namespace
+
+size_t grouped_gemm_smem_bytes() { return sizeof(Smem) + 1024; }
+
+cudaError_t launch_grouped_gemm(const GemmArgs &g, const CUtensorMap &tmB, const CUtensorMap &tmA0,
+                                const CUtensorMap &tmA1, const CUtensorMap &tmSA0, const CUtensorMap &tmSA1,
+                                int grid, cudaStream_t stream)
+{
+    static bool configured = false;
+    const size_t smem = grouped_gemm_smem_bytes();
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    grouped_gemm_kernel<<<grid, kThreads, smem, stream>>>(g, tmB, tmA0, tmA1, tmSA0, tmSA1);
+    return cudaGetLastError();
+}
+
+}  // namespace lily

@@ -1,0 +1,337 @@
+// Device-side building blocks for the sm_103a kernels: inline PTX wrappers for
+// mbarrier, TMA (cp.async.bulk.tensor), cp.async, the 5th-generation tensor core
+// (tcgen05.mma / tcgen05.ld with accumulators in tensor memory), bounded waits
+// that report a timeout instead of hanging, and the int4 -> bf16 dequantisation.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace lily {
+
+// Device-detected error codes (same values as LILY_ERR_DEVICE_* in lily_moe.h).
+constexpr int kErrDeviceTimeout = -6;
+constexpr int kErrDeviceIndex = -7;
+
+// Control block at the start of every workspace.
+struct Ctrl {
+    int status;             // sticky device status, 0 = OK
+    unsigned int ticket;    // last-block-done counter of the routing kernel
+    unsigned int ticket2;   // last-block-done counter of the decode router
+    int pad[61];
+};
+static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
+
+// Wall-clock bound of every spin-wait (nanoseconds).  A wait that exceeds it
+// records kErrDeviceTimeout and gives up.
+#ifndef LILY_WAIT_LIMIT_NS
+#define LILY_WAIT_LIMIT_NS 2000000000ull
+#endif
+
+__device__ __forceinline__ void record_error(int *status, int code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ----------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Gives up (returns
+// false) when another role raised `abort_flag`, or after LILY_WAIT_LIMIT_NS, in
+// which case it records kErrDeviceTimeout and raises `abort_flag`.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status)
+{
+    const uint32_t addr = smem_u32(bar);
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+        if (mbar_try_wait(addr, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+    while (true) {
+        if (mbar_try_wait(addr, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > LILY_WAIT_LIMIT_NS) {
+            record_error(status, kErrDeviceTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- TMA
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2-D tiled tensor load into shared memory; completion is signalled on `bar`
+// as transaction bytes.  c0 is the innermost coordinate (elements).
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ----------------------------------------------------------------- cp.async (16-byte gathers)
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads (tensor core operands).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ----------------------------------------------------------------- tcgen05 (UMMA + TMEM)
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, both K-major.
+__device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on `bar` when every tcgen05.mma issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major bf16 operand in the 128-byte
+// swizzled layout: rows of 64 elements (128 B), 8-row atoms 1024 B apart.
+// Bits: [0,14) start >> 4, [16,30) leading byte offset >> 4 (unused for this
+// layout, set to 1), [32,46) stride byte offset >> 4 (1024 B between 8-row
+// atoms), [46,48) descriptor version 1, [61,64) layout 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFF);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// 32 lanes x 32 columns of 32-bit accumulator: thread i of the warp gets lane
+// (base lane + i), columns [col, col + 32).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ----------------------------------------------------------------- int4 -> bf16
+// Eight packed 4-bit weights (one 32-bit word: element i in bits [4i, 4i+4),
+// i.e. low nibble first within each byte) -> eight bf16 values
+// w_i = q_i * s + b, each rounded once to bf16 (fma.rn.bf16x2), returned in
+// element order as four bf16x2 words.
+//
+// Nibbles are placed into the mantissa of the bf16 number 128 (0x4300): the
+// pattern 0x4300 | q encodes exactly 128 + q for q in 0..15, so subtracting 128
+// recovers q exactly (the int -> float trick of placing an integer in the
+// mantissa of a power of two).
+__device__ __forceinline__ uint4 dequant8_bf16(uint32_t v, __nv_bfloat162 s2, __nv_bfloat162 b2)
+{
+    const uint32_t kMagic = 0x43004300u;
+    const uint32_t kMask = 0x000F000Fu;
+    uint32_t p04 = (v & kMask) | kMagic;          // (q0, q4)
+    uint32_t p15 = ((v >> 4) & kMask) | kMagic;   // (q1, q5)
+    uint32_t p26 = ((v >> 8) & kMask) | kMagic;   // (q2, q6)
+    uint32_t p37 = ((v >> 12) & kMask) | kMagic;  // (q3, q7)
+    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
+    __nv_bfloat162 f04 = __hfma2(__hsub2(*reinterpret_cast<__nv_bfloat162 *>(&p04), k128), s2, b2);
+    __nv_bfloat162 f15 = __hfma2(__hsub2(*reinterpret_cast<__nv_bfloat162 *>(&p15), k128), s2, b2);
+    __nv_bfloat162 f26 = __hfma2(__hsub2(*reinterpret_cast<__nv_bfloat162 *>(&p26), k128), s2, b2);
+    __nv_bfloat162 f37 = __hfma2(__hsub2(*reinterpret_cast<__nv_bfloat162 *>(&p37), k128), s2, b2);
+    const uint32_t u04 = *reinterpret_cast<uint32_t *>(&f04), u15 = *reinterpret_cast<uint32_t *>(&f15);
+    const uint32_t u26 = *reinterpret_cast<uint32_t *>(&f26), u37 = *reinterpret_cast<uint32_t *>(&f37);
+    uint4 o;
+    o.x = __byte_perm(u04, u15, 0x5410);  // (w0, w1)
+    o.y = __byte_perm(u26, u37, 0x5410);  // (w2, w3)
+    o.z = __byte_perm(u04, u15, 0x7632);  // (w4, w5)
+    o.w = __byte_perm(u26, u37, 0x7632);  // (w6, w7)
+    return o;
+}
+
+__device__ __forceinline__ __nv_bfloat162 bf16x2_splat(uint16_t bits)
+{
+    uint32_t u = static_cast<uint32_t>(bits) | (static_cast<uint32_t>(bits) << 16);
+    return *reinterpret_cast<__nv_bfloat162 *>(&u);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t bits)
+{
+    return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+// ----------------------------------------------------------------- top-8 of 256 (one warp)
+// Order-preserving map of a float to uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_order_key(float v)
+{
+    const uint32_t u = __float_as_uint(v + 0.0f);  // -0 -> +0, so equal values tie
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+// Selects the 8 largest of 256 fp32 logits (row in global memory, 16-byte
+// aligned), ordered by descending logit with the lower expert index first among
+// equal logits, and their renormalised softmax weights
+// w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0).  Lane j < 8 receives slot j.
+__device__ __forceinline__ void warp_top8_of_256(const float *row, int lane, int &sel_e, float &sel_w)
+{
+    const float4 *src = reinterpret_cast<const float4 *>(row + lane * 8);
+    const float4 l0 = __ldcg(src), l1 = __ldcg(src + 1);
+    const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+    unsigned long long key[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        key[j] = (static_cast<unsigned long long>(float_order_key(lv[j])) << 32) |
+                 static_cast<unsigned long long>(255 - (lane * 8 + j));
+    float sel_v = 0.0f;
+    sel_e = 0;
+#pragma unroll 1
+    for (int r = 0; r < 8; ++r) {
+        unsigned long long best = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) best = key[j] > best ? key[j] : best;
+        best = warp_max_u64(best);
+        const int e = 255 - static_cast<int>(best & 0xFFFFFFFFull);
+        float v = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j == (e & 7)) {
+                v = lv[j];
+                if ((e >> 3) == lane) key[j] = 0;
+            }
+        }
+        v = __shfl_sync(0xffffffffu, v, e >> 3);
+        if (lane == r) {
+            sel_e = e;
+            sel_v = v;
+        }
+    }
+    const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
+    const float ex = lane < 8 ? expf(sel_v - vmax) : 0.0f;
+    float den = ex;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    sel_w = ex / den;
+}
+
+}  // namespace lily

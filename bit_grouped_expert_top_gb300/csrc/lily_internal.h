@@ -1,0 +1,100 @@
+// Internal host-side interface between the C-ABI entry points (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "lily_device.cuh"
+
+namespace lily {
+
+enum GemmMode : int { kModeRouter = 0, kModeGateUp = 1, kModeDown = 2 };
+
+// Arguments of the persistent tcgen05 grouped GEMM (one launch per mode).
+//   kModeRouter : logits[t][e] = x[t] . Wr[e] + router_bias[e]      (A = Wr bf16 via TMA)
+//   kModeGateUp : h[p][i] = bf16(silu(Wg_e x_t)_i * (Wu_e x_t)_i)   (A = dequant(int4), B = x gathered)
+//   kModeDown   : out[t][j] += w * (Wd_e h_p)_j                      (A = dequant(int4), B = h rows)
+// Work units are blocks of token rows (the routing block map for routed
+// experts, then ceil(T/block_rows) identity blocks for the shared expert) times
+// m_tiles pairs of 128-row weight tiles.
+struct GemmArgs {
+    int mode;
+    int T, d, E, top_k, I;
+    int bm;               // token rows per block (UMMA N <= 128)
+    int K;                // reduction length: d (router, gate/up) or I (down)
+    int m_tiles;          // weight-tile pairs per block: 1 (router), I/128 (gate/up), d/256 (down)
+    int n_shared_blocks;  // identity blocks: ceil(T/bm)
+    int n_routed_max;     // capacity of block_map
+    const int *n_blocks;  // device: routed blocks
+    const int *block_map; // device [n][3]: expert, first sorted row, rows
+    const int *perm;      // device [T*top_k]
+    const float *topk_w;  // device [T*top_k]
+    // bf16 scale / bias of the routed (s0,b0: first tile of the pair; s1,b1: second)
+    // and shared (ss*, sb*) weights; rows of K/64 groups.
+    const uint16_t *s0, *b0, *s1, *b1, *ss0, *sb0, *ss1, *sb1;
+    const float *router_bias;
+    const __nv_bfloat16 *x;  // gate/up gather source [T][d]
+    float *logits;           // router output [T][E]
+    __nv_bfloat16 *h;        // gate/up output, down input [(top_k+1)*T][I]
+    float *out;              // down output [T][d], accumulated
+    Ctrl *ctrl;
+};
+
+// Dynamic shared memory bytes of grouped_gemm_kernel.
+size_t grouped_gemm_smem_bytes();
+
+// tmB: B operand (x for router, h for down; unused for gate/up which gathers x).
+// tmA0/tmA1: routed weight maps of the two 128-row tiles (router: Wr for both);
+// tmSA0/tmSA1: shared-expert weight maps.
+cudaError_t launch_grouped_gemm(const GemmArgs &g, const CUtensorMap &tmB, const CUtensorMap &tmA0,
+                                const CUtensorMap &tmA1, const CUtensorMap &tmSA0, const CUtensorMap &tmSA1,
+                                int grid, cudaStream_t stream);
+
+// Routing: top-k + per-chunk histogram (+ last-block scan and block map), then scatter.
+struct RouteArgs {
+    int T, E, top_k, bm;
+    const float *logits;
+    int *topk_idx;
+    float *topk_w;
+    int *counts, *offsets, *perm, *block_map, *n_blocks;
+    int *chunk_counts;  // [C][E]
+    int *chunk_base;    // [C][E]
+    int n_chunks;
+    Ctrl *ctrl;
+};
+constexpr int kRouteChunkTokens = 64;
+cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream);
+cudaError_t launch_scatter(const RouteArgs &a, cudaStream_t stream);
+
+// Decode path (1 <= T <= 8).
+struct DecodeLayerArgs {
+    int T, d, E, top_k, I, layer;
+    const uint16_t *router_w;
+    const float *router_bias;
+    const uint8_t *gate_q, *up_q, *down_q;
+    const uint16_t *gate_s, *gate_b, *up_s, *up_b, *down_s, *down_b;
+    const uint8_t *sh_gate_q, *sh_up_q, *sh_down_q;
+    const uint16_t *sh_gate_s, *sh_gate_b, *sh_up_s, *sh_up_b, *sh_down_s, *sh_down_b;
+    const uint16_t *x_in;     // layer 0 input bf16 [T][d] (NULL for later layers)
+    const float *prev_out;    // previous layer output f32 [T][d] (NULL for layer 0)
+    float *out;               // this layer's output f32 [T][d]
+    uint16_t *x_export;       // bf16 [T][d] or NULL: normalised input of this layer (x_next of the previous)
+    float *trace_logits;      // [T][E] or NULL
+    int *trace_idx;           // [T][top_k] or NULL
+    float *trace_w;           // [T][top_k] or NULL
+    // workspace
+    uint16_t *x_cur;          // bf16 [T][d]
+    float *logits;            // [T][E]
+    int *n_units;             // [1]: distinct experts used + 1 (shared last)
+    int *unit_expert;         // [top_k*T+1]
+    int *unit_mask;           // [top_k*T+1] token bitmask
+    float *unit_w;            // [top_k*T+1][8]
+    __nv_bfloat16 *h;         // [top_k*T+1][8][I]
+    Ctrl *ctrl;
+};
+cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStream_t stream);
+
+}  // namespace lily

@@ -1,0 +1,189 @@
+// Routing tables of the MoE layer, kept entirely on the GPU.
+//
+// Method (page "Perplexity libera o Lily", noticiai.com.br): a router scores 256
+// experts and picks eight (section "O modelo em tres formatos de carga"); the
+// routing histogram, prefix scan, scatter and block map stay inside one GPU
+// submission with no CPU synchronisation (section "Prefill e decode").
+//
+// Two kernels, one stream, no host sync:
+//   topk_count_kernel : one warp per token selects the top 8 of 256 fp32 logits
+//                       (descending; lower index first among equal logits) with
+//                       shuffle arg-max rounds and computes the renormalised
+//                       softmax weights; each CTA then counts its 64-token chunk
+//                       per expert.  The last CTA to finish (ticket counter)
+//                       scans the per-chunk counts column-wise (per expert) into
+//                       each chunk's write base, produces counts, the exclusive
+//                       scan over experts, and the block map.
+//   scatter_kernel    : each CTA writes its chunk's assignments into
+//                       expert-sorted order; ranks inside the chunk come from
+//                       __match_any_sync plus per-warp counts, so the order
+//                       within an expert is ascending (token, slot) and the
+//                       result is deterministic (no atomics decide positions).
+#include "lily_device.cuh"
+#include "lily_internal.h"
+
+namespace lily {
+namespace {
+
+constexpr int kRouteThreads = 256;               // 8 warps
+constexpr int kTokPerWarp = kRouteChunkTokens / 8;
+constexpr int kE = 256;                          // experts (one per thread in the scans)
+constexpr int kTopK = 8;
+
+// Exclusive scan over the 256 threads of the block; returns the exclusive
+// prefix, writes the total to *total.
+__device__ __forceinline__ int block_exclusive_scan_256(int v, int *scratch /* [8] */, int *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    int warp_off = 0, sum = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const int s = scratch[w];
+        if (w < warp) warp_off += s;
+        sum += s;
+    }
+    __syncthreads();
+    *total = sum;
+    return warp_off + incl - v;
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+topk_count_kernel(const RouteArgs a)
+{
+    __shared__ int hist[kE];
+    __shared__ int scratch[8];
+    __shared__ int is_last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int chunk = blockIdx.x;
+
+    hist[threadIdx.x] = 0;
+    __syncthreads();
+
+    for (int i = 0; i < kTokPerWarp; ++i) {
+        const int t = chunk * kRouteChunkTokens + warp * kTokPerWarp + i;
+        if (t >= a.T) break;
+        int sel_e;
+        float sel_w;
+        warp_top8_of_256(a.logits + static_cast<size_t>(t) * kE, lane, sel_e, sel_w);
+        if (lane < kTopK) {
+            a.topk_idx[static_cast<size_t>(t) * kTopK + lane] = sel_e;
+            a.topk_w[static_cast<size_t>(t) * kTopK + lane] = sel_w;
+            atomicAdd(&hist[sel_e], 1);
+        }
+    }
+    __syncthreads();
+    a.chunk_counts[static_cast<size_t>(chunk) * kE + threadIdx.x] = hist[threadIdx.x];
+
+    // Last CTA to finish builds the scans and the block map.
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned int prev = atomicAdd(&a.ctrl->ticket, 1u);
+        is_last = (prev == static_cast<unsigned int>(gridDim.x) - 1u);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+
+    const int e = threadIdx.x;
+    int total_e = 0;
+    for (int c = 0; c < a.n_chunks; ++c) total_e += __ldcg(a.chunk_counts + static_cast<size_t>(c) * kE + e);
+    int sum_all;
+    const int off = block_exclusive_scan_256(total_e, scratch, &sum_all);
+    const int nb = (total_e + a.bm - 1) / a.bm;
+    int nb_all;
+    const int bstart = block_exclusive_scan_256(nb, scratch, &nb_all);
+
+    a.counts[e] = total_e;
+    a.offsets[e] = off;
+    if (e == kE - 1) a.offsets[kE] = off + total_e;
+    if (e == 0) *a.n_blocks = nb_all;
+    int running = off;
+    for (int c = 0; c < a.n_chunks; ++c) {
+        const size_t i = static_cast<size_t>(c) * kE + e;
+        const int v = __ldcg(a.chunk_counts + i);
+        a.chunk_base[i] = running;
+        running += v;
+    }
+    for (int b = 0; b < nb; ++b) {
+        int *ent = a.block_map + 3 * static_cast<size_t>(bstart + b);
+        ent[0] = e;
+        ent[1] = off + b * a.bm;
+        ent[2] = min(a.bm, total_e - b * a.bm);
+    }
+    if (threadIdx.x == 0) a.ctrl->ticket = 0u;
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+scatter_kernel(const RouteArgs a)
+{
+    __shared__ int cnt[8][kE];
+    __shared__ int base[kE];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int chunk = blockIdx.x;
+    const int n_assign = kRouteChunkTokens * kTopK;  // 512 per chunk
+    const int total = a.T * kTopK;
+
+    base[threadIdx.x] = a.chunk_base[static_cast<size_t>(chunk) * kE + threadIdx.x];
+    const unsigned lt_mask = (1u << lane) - 1u;
+
+    for (int round = 0; round < n_assign / kRouteThreads; ++round) {
+        const int ga = chunk * n_assign + round * kRouteThreads + threadIdx.x;  // = t*8 + j
+        const bool valid = ga < total;
+        int e = valid ? a.topk_idx[ga] : -1;
+        if (valid && (e < 0 || e >= kE)) {
+            record_error(&a.ctrl->status, kErrDeviceIndex);
+            e = -1;
+        }
+#pragma unroll
+        for (int w = 0; w < 8; ++w) cnt[w][threadIdx.x] = 0;
+        __syncthreads();
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & lt_mask);
+        if (e >= 0 && rank == 0) cnt[warp][e] = __popc(same);
+        __syncthreads();
+        // per expert: exclusive prefix over the 8 warps
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const int c = cnt[w][threadIdx.x];
+            cnt[w][threadIdx.x] = run;
+            run += c;
+        }
+        __syncthreads();
+        if (e >= 0) {
+            const int pos = base[e] + cnt[warp][e] + rank;
+            if (pos >= 0 && pos < total)
+                a.perm[pos] = ga;
+            else
+                record_error(&a.ctrl->status, kErrDeviceIndex);
+        }
+        __syncthreads();
+        base[threadIdx.x] += run;
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream)
+{
+    topk_count_kernel<<<a.n_chunks, kRouteThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const RouteArgs &a, cudaStream_t stream)
+{
+    scatter_kernel<<<a.n_chunks, kRouteThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace lily

@@ -1,0 +1,99 @@
+"""GPU parity of the prefill path (lily_moe_forward through the C ABI) against
+the fp64 oracle: routing tables bit-exact, logits and layer outputs within the
+stated bounds.  Full oracle comparison on small and ragged shapes; sampled
+tokens on the full-size workloads (the same configs the benchmark runs)."""
+import numpy as np
+import pytest
+import torch
+
+from bit_grouped_expert_top_gb300.inputs import CONFIGS, LayerConfig
+from gpu_util import (Layer, assert_logits_close, assert_out_close, assert_routing_exact, oracle_layer_out,
+                      run_forward, sample_tokens, x_for)
+from helpers import bits
+
+pytestmark = pytest.mark.gpu
+
+TINY = CONFIGS["tiny"]
+
+
+def _full_check(cfg: LayerConfig, T: int, block_rows=None, overrides=None, seed_offset=0):
+    layer = Layer(cfg, overrides=overrides)
+    x = x_for(cfg, T=T, seed_offset=seed_offset)
+    res = run_forward(cfg, layer, x, block_rows=block_rows)
+    xb = bits(x)
+    assert_logits_close(cfg, layer, xb, res["logits"])
+    assert_routing_exact(cfg, res, block_rows=block_rows)
+    ref = oracle_layer_out(cfg, layer, xb, res["logits"])
+    return assert_out_close(res["out"], ref), res
+
+
+def test_tiny_config_full_parity():
+    err, res = _full_check(TINY, TINY.T)
+    assert err < 1e-2
+
+
+@pytest.mark.parametrize("T", [1, 3, 17, 127, 300])
+def test_ragged_token_counts(T):
+    _full_check(TINY, T, seed_offset=T)
+
+
+@pytest.mark.parametrize("block_rows", [16, 32, 64])
+def test_block_rows_variants(block_rows):
+    _full_check(TINY, 200, block_rows=block_rows, seed_offset=block_rows)
+
+
+def test_all_tokens_forced_to_eight_experts():
+    # +100 logit bias on 8 experts: every token picks exactly these; 248 experts get 0 rows,
+    # each chosen expert gets T rows (several full blocks and a ragged tail).
+    bias = torch.zeros(256, dtype=torch.float32)
+    chosen = [3, 40, 41, 100, 128, 200, 254, 255]
+    bias[chosen] = 100.0
+    err, res = _full_check(TINY, 300, overrides={"router_bias": bias})
+    counts = res["counts"]
+    assert (counts[chosen] == 300).all() and counts.sum() == 300 * 8
+    assert res["n_blocks"] == 8 * 3
+
+
+def test_zero_routed_weights_leave_shared_expert():
+    cfg = TINY
+    L = Layer(cfg)
+    over = {}
+    for n in ("gate", "up", "down"):
+        over[n + "_q"] = torch.zeros_like(L.t[n + "_q"])
+        over[n + "_b"] = torch.zeros_like(L.t[n + "_b"])
+    _full_check(cfg, 64, overrides=over)
+
+
+def test_medium_full_hidden_size():
+    # d = 2048, I = 512 at a token count the oracle finishes in seconds:
+    # many weight tiles per unit and ragged expert groups.
+    cfg = CONFIGS["prefill_t512"].with_(T=48)
+    _full_check(cfg, 48)
+
+
+@pytest.mark.parametrize("name,n_sample", [("prefill_t512", 24), ("prefill_t2048_zipf", 24), ("prefill_t8192", 16)])
+def test_full_size_workloads_sampled(name, n_sample):
+    cfg = CONFIGS[name]
+    layer = Layer(cfg)
+    x = x_for(cfg)
+    res = run_forward(cfg, layer, x)
+    xb = bits(x)
+    toks = sample_tokens(cfg.T, n_sample, seed=cfg.seed)
+    assert_logits_close(cfg, layer, xb, res["logits"], toks)
+    assert_routing_exact(cfg, res)
+    ref = oracle_layer_out(cfg, layer, xb, res["logits"], toks)
+    assert_out_close(res["out"][toks], ref)
+    if cfg.zipf_s is not None:
+        counts = res["counts"]
+        assert (counts == 0).sum() >= 1 and (counts > 300).sum() >= 2
+
+
+def test_repeat_calls_are_deterministic():
+    cfg = TINY
+    layer = Layer(cfg)
+    x = x_for(cfg, T=100)
+    a = run_forward(cfg, layer, x)
+    b = run_forward(cfg, layer, x)
+    for k in ("topk_idx", "counts", "offsets", "perm", "block_map"):
+        np.testing.assert_array_equal(a[k], b[k])
+    np.testing.assert_array_equal(a["logits"], b["logits"])
