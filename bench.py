@@ -1,0 +1,401 @@
+"""Benchmark of the GB300 MoE layer.
+
+One step = one whole MoE layer (router GEMM, top-8 + weights, histogram, scan,
+scatter, block map, gate/up grouped GEMM + SwiGLU, down grouped GEMM + weighted
+combine) over the T=8192 prefill workload, 4 distinct weight sets and 4
+activation sets cycled so every step streams its weights from HBM (inputs
+larger than L2).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload per step.  Under torchrun (N>1)
+every rank runs an independent replica of the layer on its own GPU (the path
+has no exchange step); rank 0 prints the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer prefill tokens/s @T=2048/8192; decode µs/layer; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = [ln.split(",") for ln in open(self.path).read().strip().splitlines() if ln.count(",") >= 8]
+        os.remove(self.path)
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_setup(n_gpus: int):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU baseline (oracle)
+def oracle_sample_rate(cfg, layer_np, x_bits, logits_f32, n_tokens: int):
+    """Tokens/s of the fp64 oracle on n_tokens of the workload (all host threads)."""
+    import numpy as np
+    import oracle
+    toks = np.arange(n_tokens, dtype=np.int64)
+    t0 = time.perf_counter()
+    idx, w = oracle.select(logits_f32[:n_tokens].astype(np.float64), cfg.top_k)
+    lg = oracle.logits(x_bits[:n_tokens], layer_np["router_w"], layer_np.get("router_bias"))
+    oracle.moe_tokens(layer_np, x_bits[:n_tokens], idx, w, None, d=cfg.d, E=cfg.E, I=cfg.I,
+                      I_shared=cfg.I_shared)
+    dt = time.perf_counter() - t0
+    del lg, toks
+    return n_tokens / dt, dt
+
+
+def _np_layer(layer_t):
+    import numpy as np
+    import torch
+    out = {}
+    for k, v in layer_t.items():
+        v = v.detach().cpu().contiguous()
+        out[k] = v.view(torch.int16).numpy().view(np.uint16) if v.dtype == torch.bfloat16 else v.numpy()
+    return out
+
+
+def _bits(t):
+    import numpy as np
+    import torch
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------------ our arm
+def prefill_flops(cfg, T):
+    per_tok = 2 * 3 * cfg.d * cfg.I * (cfg.top_k + 1) + 2 * cfg.d * cfg.E
+    return T * per_tok, T * 2 * 2 * cfg.d * cfg.I * (cfg.top_k + 1), T * 2 * cfg.d * cfg.I * (cfg.top_k + 1)
+
+
+def time_prefill(cfg, steps, warmup, n_sets, stream, with_stages=True):
+    """Device time of `steps` forward passes cycling n_sets weight/activation sets."""
+    import torch
+    import bit_grouped_expert_top_gb300 as lm
+    from bit_grouped_expert_top_gb300.inputs import make_layer, make_x
+    layers = [make_layer(cfg, "cuda", i) for i in range(n_sets)]
+    ws_l = [lm.make_weights(L) for L in layers]
+    xs = [make_x(cfg, "cuda", seed_offset=i) for i in range(n_sets)]
+    s = lm.make_shape(T=cfg.T, d=cfg.d, E=cfg.E, top_k=cfg.top_k, I=cfg.I, I_shared=cfg.I_shared,
+                      group=cfg.group, block_rows=cfg.block_rows)
+    ws = lm.alloc_workspace(s)
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            lm.lily_moe_forward(s, ws_l[i % n_sets], xs[i % n_sets], out, ws, stream=stream)
+    stream.synchronize()
+    status = lm.lily_moe_device_status(ws, stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)] if with_stages else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    return dict(layers=layers, ws_l=ws_l, xs=xs, shape=s, ws=ws, out=out, evs=evs, start=start, end=end)
+
+
+def run_timed(ctx, steps, stream, n_sets):
+    import bit_grouped_expert_top_gb300 as lm
+    s, ws, out = ctx["shape"], ctx["ws"], ctx["out"]
+    ctx["start"].record(stream)
+    for i in range(steps):
+        j = i % n_sets
+        if ctx["evs"] is not None:
+            lm.lily_moe_forward_timed(s, ctx["ws_l"][j], ctx["xs"][j], out, ws, ctx["evs"][i], stream=stream)
+        else:
+            lm.lily_moe_forward(s, ctx["ws_l"][j], ctx["xs"][j], out, ws, stream=stream)
+    ctx["end"].record(stream)
+
+
+def stage_means(ctx):
+    evs = ctx["evs"]
+    names = ["route", "route_tables", "prep", "gateup", "down"]
+    acc = {n: [] for n in names}
+    for e in evs:
+        for k, n in enumerate(names):
+            acc[n].append(e[k].elapsed_time(e[k + 1]) * 1e3)  # us
+    return {n: statistics.mean(v) for n, v in acc.items()}
+
+
+def bench_decode(cfg, Ts, reps, stream):
+    """µs per layer of lily_moe_decode over cfg.n_layers distinct layers."""
+    import numpy as np
+    import torch
+    import bit_grouped_expert_top_gb300 as lm
+    from bit_grouped_expert_top_gb300.inputs import make_layer, make_x, weight_bytes
+    L = cfg.n_layers
+    layers = [make_layer(cfg, "cuda", i) for i in range(L)]
+    wl = [lm.make_weights(x) for x in layers]
+    wb = weight_bytes(cfg)
+    res = {}
+    for T in Ts:
+        s = lm.make_shape(T=T, d=cfg.d, E=cfg.E, top_k=cfg.top_k, I=cfg.I, I_shared=cfg.I_shared,
+                          group=cfg.group, block_rows=cfg.block_rows)
+        ws = lm.alloc_workspace(s, n_layers_decode=L)
+        x = make_x(cfg, "cuda", seed_offset=500 + T, T=T)
+        out = torch.empty((L, T, cfg.d), dtype=torch.float32, device="cuda")
+        idx = torch.empty((L, T, cfg.top_k), dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            lm.lily_moe_decode(s, wl, x, out, ws, trace={"topk_idx": idx}, stream=stream)
+        stream.synchronize()
+        assert lm.lily_moe_device_status(ws, stream) == 0
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            lm.lily_moe_decode(s, wl, x, out, ws, trace={"topk_idx": idx}, stream=stream)
+        b.record(stream)
+        b.synchronize()
+        us_layer = a.elapsed_time(b) * 1e3 / (reps * L)
+        ids = idx.cpu().numpy()
+        distinct = np.mean([len(np.unique(ids[l])) for l in range(L)])
+        expert_bytes = (distinct + 1) * wb["expert"]
+        total_bytes = expert_bytes + wb["router"]
+        res[f"T{T}"] = {"us_per_layer": round(us_layer, 3), "experts_read_per_layer": round(float(distinct) + 1, 2),
+                        "weight_bytes_per_layer": int(total_bytes),
+                        "achieved_gbs": round(total_bytes / (us_layer * 1e-6) / 1e9, 1),
+                        "expert_bytes_gbs": round(expert_bytes / (us_layer * 1e-6) / 1e9, 1)}
+    return res
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import bit_grouped_expert_top_gb300 as lm
+    from bit_grouped_expert_top_gb300.inputs import CONFIGS
+    import oracle
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    lm.load()
+    peaks = load_peaks()
+    cfg = CONFIGS["prefill_t8192"]
+    n_sets = cfg.n_weight_sets
+    stream = torch.cuda.Stream()
+    ctx = time_prefill(cfg, args.steps, args.warmup, n_sets, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = ClockSampler(local)
+    clk.start()
+    run_timed(ctx, args.steps, stream, n_sets)
+    stream.synchronize()
+    clocks = clk.stop()
+    ms = ctx["start"].elapsed_time(ctx["end"]) / args.steps
+    ms = max_over_ranks(ms, world)
+    st = stage_means(ctx)
+    if lm.lily_moe_device_status(ctx["ws"], stream) != 0:
+        raise RuntimeError("device status error in timed region")
+    tokens_per_s = cfg.T * world / (ms * 1e-3)
+    flops_total, flops_gu, flops_down = prefill_flops(cfg, cfg.T)
+    peak_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])  # fp16 dense rate = bf16 rate
+    achieved = flops_gu / (st["gateup"] * 1e-6) / 1e12
+
+    # e2e: host buffers through the public call, H2D of x and D2H of out inside the timed region
+    x_host = [x.cpu().pin_memory() for x in ctx["xs"]]
+    out_host = torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(ctx["xs"][0])
+    e2e_steps = max(5, min(args.steps, 40))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            x_dev.copy_(x_host[i % n_sets], non_blocking=True)
+            lm.lily_moe_forward(ctx["shape"], ctx["ws_l"][i % n_sets], x_dev, ctx["out"], ctx["ws"], stream=stream)
+            out_host.copy_(ctx["out"], non_blocking=True)
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(e2e_steps):
+            x_dev.copy_(x_host[i % n_sets], non_blocking=True)
+            lm.lily_moe_forward(ctx["shape"], ctx["ws_l"][i % n_sets], x_dev, ctx["out"], ctx["ws"], stream=stream)
+            out_host.copy_(ctx["out"], non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, world)
+
+    also = {}
+    if not args.quick:
+        for name in ("prefill_t2048_zipf", "prefill_t512"):
+            c = CONFIGS[name]
+            cx = time_prefill(c, 50, 5, 1, stream, with_stages=True)
+            run_timed(cx, 50, stream, 1)
+            stream.synchronize()
+            ms_c = cx["start"].elapsed_time(cx["end"]) / 50
+            stc = stage_means(cx)
+            also[name] = {"tokens_per_s": round(c.T / (ms_c * 1e-3)), "us_per_layer": round(ms_c * 1e3, 2),
+                          "stage_us": {k: round(v, 2) for k, v in stc.items()}, "inputs_vs_l2": "weights 456 MB > L2"}
+            del cx
+        torch.cuda.empty_cache()
+        also["decode_l40"] = bench_decode(CONFIGS["decode_t1_l40"], (1, 2, 4, 8), 20, stream)
+
+    line = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16xint4 (fp32 accumulate); router bf16",
+        "data": "synthetic (seeded; int4 g64 affine weights, N(0,1) activations)",
+        "config": {"workload": "prefill_t8192: one MoE layer, T=8192, d=2048, E=256 top-8 + 1 shared, I=512, "
+                               "int4 group-64 bf16 scale/bias, 4 weight+activation sets cycled",
+                   "global_batch": cfg.T * world, "seq_len": cfg.T, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (each step reads a 456 MB weight set)"},
+        "stage_us": {k: round(v, 2) for k, v in st.items()},
+        "roofline": {"kernel": "grouped_gemm_kernel (gate/up + SwiGLU)", "bound": "tensor",
+                     "achieved": round(achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tc, 4), "traffic": None,
+                     "peak_note": f"{peaks['source']} bf16 sustained (fp16 dense rate = bf16 rate)",
+                     "algorithmic_flops_per_launch": flops_gu},
+        "layer_tflops": round(flops_total / (ms * 1e-3) / 1e12, 1),
+        "clocks": clocks,
+        "e2e": {"value": round(cfg.T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 4},
+        "gpu_launches": 6 * args.steps,
+        "also": also,
+    }
+    if rank == 0:
+        # CPU baseline: the oracle as it stands, on a bounded token sample of the same workload
+        lg = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+        rt = lm.alloc_routing(ctx["shape"])
+        rt["logits"] = lg
+        r = lm.make_routing(rt)
+        lm.lily_moe_route(ctx["shape"], ctx["ws_l"][0], ctx["xs"][0], r, ctx["ws"], stream=stream)
+        stream.synchronize()
+        n_tok = args.cpu_tokens
+        rate, dt = oracle_sample_rate(cfg, _np_layer(ctx["layers"][0]), _bits(ctx["xs"][0]), lg.cpu().numpy(), n_tok)
+        line["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+                                "kind": "oracle",
+                                "sample": f"{n_tok} tokens of prefill_t8192 (router + top-8 + 9 experts each), "
+                                          f"{dt:.1f} s wall"}
+        print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+def run_reference(args):
+    import numpy as np
+    import torch
+    from bit_grouped_expert_top_gb300.inputs import CONFIGS, make_layer, make_x
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = CONFIGS["prefill_t8192"]
+    L = _np_layer(make_layer(cfg, "cpu", 0))
+    xb = _bits(make_x(cfg, "cpu"))
+    n_tok = args.cpu_tokens
+    lg = oracle.logits(xb[:n_tok], L["router_w"], L.get("router_bias")).astype(np.float32)
+    for _ in range(args.warmup if args.warmup < 2 else 1):
+        oracle_sample_rate(cfg, L, xb, lg, max(1, n_tok // 4))
+    times = []
+    for _ in range(args.steps):
+        _, dt = oracle_sample_rate(cfg, L, xb, lg, n_tok)
+        times.append(dt)
+    total = sum(times)
+    rate = n_tok * len(times) / total
+    line = {"impl": "reference", "metric": METRIC, "value": round(rate, 3), "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": "prefill_t8192 (bounded sample per step)", "global_batch": cfg.T,
+                       "seq_len": cfg.T, "parallelism": "cpu"},
+            "cpu_baseline": {"value": round(rate, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": f"{n_tok} tokens of prefill_t8192 per step"},
+            "e2e": {"value": round(rate, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=24, help="oracle sample size (tokens)")
+    ap.add_argument("--quick", action="store_true", help="headline workload only (no extra configs / decode)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -34,7 +34,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // ------------------------------------------------------------------ workspace layouts
 struct PrefillLayout {
-    size_t ctrl, chunk_counts, chunk_base, h, logits, idx, w, counts, offsets, perm, block_map, n_blocks, total;
+    size_t ctrl, chunk_counts, chunk_base, h, xh, logits, idx, w, counts, offsets, perm, block_map, n_blocks, total;
 };
 
 int64_t block_capacity(const lily_moe_shape &s)
@@ -58,6 +58,7 @@ PrefillLayout prefill_layout(const lily_moe_shape &s)
     L.chunk_counts = take(C * E * 4);
     L.chunk_base = take(C * E * 4);
     L.h = take((k + 1) * T * s.I * 2);
+    L.xh = take(T * s.d * 2);
     L.logits = take(T * E * 4);
     L.idx = take(T * k * 4);
     L.w = take(T * k * 4);
@@ -208,6 +209,11 @@ bool tmap_bf16_sw128(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t r
     return make_tmap(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+bool tmap_f16_sw128(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows)
+{
+    return make_tmap(m, ptr, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, inner, rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool tmap_q4(CUtensorMap *m, const uint8_t *q, uint64_t K, uint64_t rows)
 {
     return make_tmap(m, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -263,17 +269,18 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
 {
     const PrefillLayout L = prefill_layout(s);
     Ctrl *ctrl = at<Ctrl>(ws, L.ctrl);
-    __nv_bfloat16 *h = at<__nv_bfloat16>(ws, L.h);
+    __half *h = at<__half>(ws, L.h);
+    __half *xh = at<__half>(ws, L.xh);
     const int64_t hrows = static_cast<int64_t>(s.top_k + 1) * s.T;
     CUtensorMap tmX, tmH, tmG, tmU, tmD, tmSG, tmSU, tmSD;
-    if (!tmap_bf16_sw128(&tmX, x, s.d, s.T) || !tmap_bf16_sw128(&tmH, h, s.I, hrows) ||
+    if (!tmap_bf16_sw128(&tmX, x, s.d, s.T) || !tmap_f16_sw128(&tmH, h, s.I, hrows) ||
         !tmap_q4(&tmG, w.gate.q, s.d, static_cast<uint64_t>(s.E) * s.I) ||
         !tmap_q4(&tmU, w.up.q, s.d, static_cast<uint64_t>(s.E) * s.I) ||
         !tmap_q4(&tmD, w.down.q, s.I, static_cast<uint64_t>(s.E) * s.d) || !tmap_q4(&tmSG, w.sh_gate.q, s.d, s.I) ||
         !tmap_q4(&tmSU, w.sh_up.q, s.d, s.I) || !tmap_q4(&tmSD, w.sh_down.q, s.I, s.d))
         return cudaErrorInvalidValue;
 
-    cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(s.T) * s.d * sizeof(float), stream);
+    cudaError_t e = launch_prep_experts(x, xh, out, static_cast<int64_t>(s.T) * s.d, stream);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[3], stream)) != cudaSuccess) return e;
 
@@ -288,7 +295,7 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
     g.block_map = r.block_map;
     g.perm = r.perm;
     g.topk_w = r.topk_w;
-    g.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    g.xh = xh;
     g.h = h;
     g.out = out;
     g.ctrl = ctrl;
@@ -433,9 +440,8 @@ int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *
     if ((rc = check_ptr(x)) || (rc = check_ptr(out))) return rc;
     const lily_moe_routing rr = r ? *r : internal_routing(*shape, ws);
     float *logits = rr.logits ? rr.logits : at<float>(ws, prefill_layout(*shape).logits);
-    cudaError_t e = cudaSuccess;
-    if (events && (e = cudaEventRecord(events[0], stream)) != cudaSuccess) return LILY_ERR_LAUNCH;
-    if ((e = enqueue_route(*shape, *w, x, rr, logits, ws, stream)) != cudaSuccess) return LILY_ERR_LAUNCH;
+    if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return LILY_ERR_LAUNCH;
+    if (enqueue_route(*shape, *w, x, rr, logits, ws, stream) != cudaSuccess) return LILY_ERR_LAUNCH;
     if (events) {
         // the router GEMM and the two routing kernels are one unit here
         if (cudaEventRecord(events[1], stream) != cudaSuccess || cudaEventRecord(events[2], stream) != cudaSuccess)
@@ -502,7 +508,7 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
             a.unit_expert = at<int>(ws, L.unit_expert);
             a.unit_mask = at<int>(ws, L.unit_mask);
             a.unit_w = at<float>(ws, L.unit_w);
-            a.h = at<__nv_bfloat16>(ws, L.h);
+            a.h = at<__half>(ws, L.h);
             a.ctrl = ctrl;
             if ((e = launch_decode_layer(a, sms, st)) != cudaSuccess) return e;
         }

@@ -4,8 +4,8 @@
 // decode: onde estao os ganhos"): at batch 1 there is almost no weight reuse,
 // so memory bandwidth sets the ceiling.  Only the bytes of the selected
 // experts (plus the shared expert and the router) are read, each exactly once,
-// with 16-byte coalesced loads, dequantised in registers (same bf16 rounding as
-// the prefill path) and accumulated in fp32.
+// with 16-byte coalesced loads, dequantised in registers (weights rounded once
+// to fp16, as in the prefill path) and accumulated in fp32.
 //
 // Three kernels per layer:
 //   dec_route_kernel  : builds the layer input (layer 0: x; later layers: the
@@ -16,7 +16,7 @@
 //                       shared expert is the last unit with weight 1.
 //   dec_gateup_kernel : one warp per (unit, intermediate row): gate and up rows
 //                       dequantised and dotted with the unit's tokens, SwiGLU,
-//                       h stored as bf16.
+//                       h stored as fp16.
 //   dec_down_kernel   : one warp per output row: the down rows of every unit,
 //                       dotted with h, scaled by the routing weight and summed
 //                       in registers (deterministic, no atomics).
@@ -38,23 +38,35 @@ __device__ __forceinline__ int pad_index(int row, int k, int n_chunks)
     return (row * n_chunks + (k >> 5)) * kPadChunk + (k & 31);
 }
 
-// dot of 32 dequantised weights (one 16-byte chunk) with 32 bf16 activations
-// stored contiguously in shared memory.
-__device__ __forceinline__ float dot32(const uint4 q, __nv_bfloat162 s2, __nv_bfloat162 b2, const __nv_bfloat16 *xs)
+// 16-bit activation pair -> float2 (bf16 layer input or fp16 h).
+__device__ __forceinline__ float2 act2_to_float2(uint32_t u, const __nv_bfloat16 *)
+{
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+}
+__device__ __forceinline__ float2 act2_to_float2(uint32_t u, const __half *)
+{
+    return __half22float2(*reinterpret_cast<const __half2 *>(&u));
+}
+
+// dot of 32 dequantised weights (one 16-byte int4 chunk; each weight rounded
+// once to fp16, as in the prefill path) with 32 activations stored
+// contiguously in shared memory; fp32 accumulation.
+template <typename Act>
+__device__ __forceinline__ float dot32(const uint4 q, __half2 s2, __half2 b2, const Act *xs)
 {
     const uint32_t words[4] = {q.x, q.y, q.z, q.w};
     const uint4 *xv = reinterpret_cast<const uint4 *>(xs);
     float acc = 0.0f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint4 wv = dequant8_bf16(words[c], s2, b2);
+        const uint4 wv = dequant8_f16(words[c], s2, b2);
         const uint4 x8 = xv[c];
         const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
         const uint32_t xu[4] = {x8.x, x8.y, x8.z, x8.w};
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-            const float2 wf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wu[p]));
-            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xu[p]));
+            const float2 wf = __half22float2(*reinterpret_cast<const __half2 *>(&wu[p]));
+            const float2 xf = act2_to_float2(xu[p], xs);
             acc = fmaf(wf.x, xf.x, acc);
             acc = fmaf(wf.y, xf.y, acc);
         }
@@ -224,7 +236,8 @@ dec_route_kernel(const DecodeLayerArgs a)
 }
 
 // Loads the layer input x_cur [T][d] into the padded shared layout.
-__device__ __forceinline__ void load_padded(const uint16_t *src, __nv_bfloat16 *dst, int rows, int K)
+template <typename Act>
+__device__ __forceinline__ void load_padded(const uint16_t *src, Act *dst, int rows, int K)
 {
     const int n_chunks = K / kChunk;
     for (int i = threadIdx.x; i < rows * K / 8; i += kDecThreads) {
@@ -268,8 +281,8 @@ dec_gateup_kernel(const DecodeLayerArgs a)
         for (int c = lane; c < n_chunks; c += 32) {
             const uint4 qg = __ldg(gq + c), qu = __ldg(uq + c);
             const int grp = c >> 1;
-            const __nv_bfloat162 sg = bf16x2_splat(__ldg(gs + grp)), bg = bf16x2_splat(__ldg(gb + grp));
-            const __nv_bfloat162 su = bf16x2_splat(__ldg(us + grp)), bu = bf16x2_splat(__ldg(ub + grp));
+            const __half2 sg = half2_from_bf16_bits(__ldg(gs + grp)), bg = half2_from_bf16_bits(__ldg(gb + grp));
+            const __half2 su = half2_from_bf16_bits(__ldg(us + grp)), bu = half2_from_bf16_bits(__ldg(ub + grp));
 #pragma unroll
             for (int t = 0; t < kMaxT; ++t) {
                 if (t < T && ((mask >> t) & 1)) {
@@ -284,7 +297,7 @@ dec_gateup_kernel(const DecodeLayerArgs a)
             if (t < T && ((mask >> t) & 1)) {
                 const float g = warp_sum(accg[t]);
                 const float v = warp_sum(accu[t]);
-                if (lane == 0) a.h[(static_cast<size_t>(u) * kMaxT + t) * I + i] = __float2bfloat16_rn(silu_f(g) * v);
+                if (lane == 0) a.h[(static_cast<size_t>(u) * kMaxT + t) * I + i] = __float2half_rn(silu_f(g) * v);
             }
         }
     }
@@ -294,7 +307,7 @@ __global__ void __launch_bounds__(kDecThreads)
 dec_down_kernel(const DecodeLayerArgs a)
 {
     extern __shared__ __align__(16) uint8_t dsm[];
-    __nv_bfloat16 *hs = reinterpret_cast<__nv_bfloat16 *>(dsm);  // [unit*8 + t][I] padded
+    __half *hs = reinterpret_cast<__half *>(dsm);  // compact (unit, token) rows of h, padded
     __shared__ int s_expert[kMaxT * 8 + 1];
     __shared__ int s_mask[kMaxT * 8 + 1];
     __shared__ int s_slot[kMaxT * 8 + 1];  // first compact h slot of each unit
@@ -349,8 +362,8 @@ dec_down_kernel(const DecodeLayerArgs a)
             const size_t row = sh ? static_cast<size_t>(j) : static_cast<size_t>(e) * d + j;
             const uint4 q = __ldg(reinterpret_cast<const uint4 *>((sh ? a.sh_down_q : a.down_q) + row * (I / 2)) + c);
             const int grp = c >> 1;
-            const __nv_bfloat162 s2 = bf16x2_splat(__ldg((sh ? a.sh_down_s : a.down_s) + row * ngroups + grp));
-            const __nv_bfloat162 b2 = bf16x2_splat(__ldg((sh ? a.sh_down_b : a.down_b) + row * ngroups + grp));
+            const __half2 s2 = half2_from_bf16_bits(__ldg((sh ? a.sh_down_s : a.down_s) + row * ngroups + grp));
+            const __half2 b2 = half2_from_bf16_bits(__ldg((sh ? a.sh_down_b : a.down_b) + row * ngroups + grp));
             const int mask = s_mask[u];
             int slot = s_slot[u];
 #pragma unroll

@@ -2,8 +2,12 @@
 //
 // Method (page "Perplexity libera o Lily", noticiai.com.br, section "Prefill e
 // decode: onde estao os ganhos"): the expert GEMMs run over uneven per-expert
-// token groups, and the 4-bit group-64 affine weights are rebuilt to bf16 one
-// tile at a time inside the GEMM, held on chip, with FP32 accumulation.
+// token groups, and the 4-bit group-64 affine weights are rebuilt one tile at a
+// time inside the GEMM, held on chip, with FP32 accumulation.  The page rebuilds
+// to bf16 because its tensor ops take bf16; tcgen05 takes fp16 at the same
+// rate and fp16 rounds the rebuilt weight 8x more finely, so the expert GEMMs
+// here run on fp16 operands (x converted once; h written as fp16).  The router
+// GEMM stays bf16 (its inputs are bf16 and the products are exact in fp32).
 //
 // GB300 design.  The weights take the UMMA M side (128 rows per tile, two
 // tiles per work unit sharing one B operand: gate+up rows of the same
@@ -15,17 +19,18 @@
 //                 router), TMA of contiguous B rows, or cp.async gathers of
 //                 token rows of x by the routing permutation (gate/up);
 //   warp 1        TMEM allocator + single-thread tcgen05.mma issuer;
-//   warps 4..11   dequantisers: int4 -> bf16 (one matrix per warpgroup, one
+//   warps 4..11   dequantisers: int4 -> fp16 (one matrix per warpgroup, one
 //                 row per thread) written in the 128-byte swizzled K-major
 //                 layout the tensor core reads;
 //   warps 12..15  epilogue: tcgen05.ld from TMEM, then per mode the router
-//                 logits (+bias), SwiGLU into h (bf16), or the down projection
+//                 logits (+bias), SwiGLU into h (fp16), or the down projection
 //                 scaled by the routing weight and added (red.global.add.f32)
 //                 into token order.
 // Accumulators are double-buffered in TMEM (2 x 2 x 128 fp32 columns), so the
 // epilogue of one unit overlaps the main loop of the next.
 // Every wait is bounded; on timeout the kernel records the error, drains its
 // in-flight copies and tensor-core work, frees TMEM and returns.
+#include <algorithm>
 #include <cstdio>
 
 #include "lily_device.cuh"
@@ -41,8 +46,8 @@ constexpr int kLag = 2;       // cp.async groups kept in flight by the gathering
 constexpr int kTileM = 128;
 constexpr int kBK = 64;       // one quantisation group, one 128-byte swizzle row
 constexpr int kTileN = 128;
-constexpr int kABytes = kTileM * kBK * 2;    // 16 KB bf16
-constexpr int kBBytes = kTileN * kBK * 2;    // 16 KB bf16
+constexpr int kABytes = kTileM * kBK * 2;    // 16 KB of 16-bit elements
+constexpr int kBBytes = kTileN * kBK * 2;    // 16 KB of 16-bit elements
 constexpr int kRawBytes = kTileM * kBK / 2;  // 4 KB int4
 constexpr uint32_t kTmemCols = 512;
 
@@ -241,7 +246,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     // Gather token rows: each (row, 16-byte chunk) pair lands in its
                     // 128-byte-swizzled position.
                     const int c = lane & 7;
-                    const __nv_bfloat16 *xk = g.x + kt * kBK + c * 8;
+                    const __half *xk = g.xh + kt * kBK + c * 8;
                     uint8_t *bst = S.b[ls];
                     for (int r = lane >> 3; r < u.n_mma; r += 4) {
                         const int src = S.prod_tok[r];
@@ -305,7 +310,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 if (u.rows <= 0) continue;
                 if (!mbar_wait(&S.empty_acc[ab], acc_ph ^ 1, abort_flag, status)) break;
                 tc_fence_after();
-                const uint32_t idesc = idesc_bf16_f32(kTileM, u.n_mma);
+                const uint32_t idesc = idesc_f32acc(g.mode == kModeRouter ? kFmtBF16 : kFmtF16, kTileM, u.n_mma);
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(ab * 2 * kTileM);
                 const uint32_t d1 = d0 + kTileM;
                 for (int kt = 0; kt < KT; ++kt) {
@@ -378,12 +383,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     }
                     const uint4 *src = reinterpret_cast<const uint4 *>(S.raw[ls][mi] + r * (kBK / 2));
                     const uint4 q0 = src[0], q1 = src[1];
-                    const __nv_bfloat162 s2 = bf16x2_splat(sc), b2 = bf16x2_splat(bi);
+                    const __half2 s2 = half2_from_bf16_bits(sc), b2 = half2_from_bf16_bits(bi);
                     uint8_t *dst = S.a[as][mi] + (r >> 3) * 1024 + (r & 7) * 128;
                     const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) = dequant8_bf16(words[c], s2, b2);
+                        *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) = dequant8_f16(words[c], s2, b2);
                     fence_proxy_async_smem();
                     named_barrier_sync(1 + mi, 128);
                     if (r == 0) {
@@ -454,7 +459,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                             lrow[kTileM + et] = f1 + bias1;
                         } else if (g.mode == kModeGateUp) {
                             const size_t p = u.shared ? static_cast<size_t>(g.T) * g.top_k + u.p0 + n : static_cast<size_t>(u.p0 + n);
-                            g.h[p * g.I + u.mt * kTileM + et] = __float2bfloat16_rn(silu_f(f0) * f1);
+                            g.h[p * g.I + u.mt * kTileM + et] = __float2half_rn(silu_f(f0) * f1);
                         } else {
                             float *orow = g.out + static_cast<size_t>(S.ep_tok[n]) * g.d + u.mt * 2 * kTileM;
                             const float wt = S.ep_w[n];
@@ -481,7 +486,40 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+__global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, uint4 *xh, float4 *out, int64_t n8)
+{
+    for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n8; i += static_cast<int64_t>(gridDim.x) * 256) {
+        const uint4 v = x[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
+            const __half2 hv = __floats2half2_rn(f.x, f.y);
+            o[j] = *reinterpret_cast<const uint32_t *>(&hv);
+        }
+        xh[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        out[2 * i] = z;
+        out[2 * i + 1] = z;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_prep_experts(const uint16_t *x, __half *xh, float *out, int64_t n_elems, cudaStream_t stream)
+{
+    const int64_t n8 = n_elems / 8;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (n8 + 255) / 256;
+    const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sms) * 8));
+    prep_experts_kernel<<<grid > 0 ? grid : 1, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(x),
+                                                                reinterpret_cast<uint4 *>(xh),
+                                                                reinterpret_cast<float4 *>(out), n8);
+    return cudaGetLastError();
+}
 
 size_t grouped_gemm_smem_bytes() { return sizeof(Smem) + 1024; }
 

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace lily {
@@ -199,12 +200,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr)
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
+// Instruction descriptor of tcgen05.mma.kind::f16 with an fp32 accumulator
+// (bits 4-5 = 1).  A and B always share one input type, given by `ab_fmt`
+// (0 = f16, 1 = bf16) in bits 7-9 and 10-12; both K-major (bits 15, 16 = 0);
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
+constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1;
+__host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t ab_fmt, int M, int N)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+    return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
@@ -256,6 +259,41 @@ __device__ __forceinline__ uint4 dequant8_bf16(uint32_t v, __nv_bfloat162 s2, __
     o.z = __byte_perm(u04, u15, 0x7632);  // (w4, w5)
     o.w = __byte_perm(u26, u37, 0x7632);  // (w6, w7)
     return o;
+}
+
+// Same as dequant8_bf16 but the eight weights are rounded once to fp16
+// (fma.rn.f16x2), whose 11-bit significand holds q*s+b 8x more finely than
+// bf16.  The nibble goes into the mantissa of the fp16 number 1024 (0x6400):
+// 0x6400 | q encodes exactly 1024 + q.  s2/b2 are fp16 copies of the bf16
+// scale and bias (exact for magnitudes in [2^-14, 65504]).
+__device__ __forceinline__ uint4 dequant8_f16(uint32_t v, __half2 s2, __half2 b2)
+{
+    const uint32_t kMagic = 0x64006400u;
+    const uint32_t kMask = 0x000F000Fu;
+    uint32_t p04 = (v & kMask) | kMagic;
+    uint32_t p15 = ((v >> 4) & kMask) | kMagic;
+    uint32_t p26 = ((v >> 8) & kMask) | kMagic;
+    uint32_t p37 = ((v >> 12) & kMask) | kMagic;
+    const __half2 k1024 = __floats2half2_rn(1024.0f, 1024.0f);
+    __half2 f04 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p04), k1024), s2, b2);
+    __half2 f15 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p15), k1024), s2, b2);
+    __half2 f26 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p26), k1024), s2, b2);
+    __half2 f37 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p37), k1024), s2, b2);
+    const uint32_t u04 = *reinterpret_cast<uint32_t *>(&f04), u15 = *reinterpret_cast<uint32_t *>(&f15);
+    const uint32_t u26 = *reinterpret_cast<uint32_t *>(&f26), u37 = *reinterpret_cast<uint32_t *>(&f37);
+    uint4 o;
+    o.x = __byte_perm(u04, u15, 0x5410);
+    o.y = __byte_perm(u26, u37, 0x5410);
+    o.z = __byte_perm(u04, u15, 0x7632);
+    o.w = __byte_perm(u26, u37, 0x7632);
+    return o;
+}
+
+// bf16 bit pattern -> fp16 pair (value converted with round-to-nearest).
+__device__ __forceinline__ __half2 half2_from_bf16_bits(uint16_t bits)
+{
+    const __half h = __float2half_rn(__uint_as_float(static_cast<uint32_t>(bits) << 16));
+    return __halves2half2(h, h);
 }
 
 __device__ __forceinline__ __nv_bfloat162 bf16x2_splat(uint16_t bits)

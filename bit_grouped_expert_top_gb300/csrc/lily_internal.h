@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "lily_device.cuh"
@@ -15,7 +16,7 @@ enum GemmMode : int { kModeRouter = 0, kModeGateUp = 1, kModeDown = 2 };
 
 // Arguments of the persistent tcgen05 grouped GEMM (one launch per mode).
 //   kModeRouter : logits[t][e] = x[t] . Wr[e] + router_bias[e]      (A = Wr bf16 via TMA)
-//   kModeGateUp : h[p][i] = bf16(silu(Wg_e x_t)_i * (Wu_e x_t)_i)   (A = dequant(int4), B = x gathered)
+//   kModeGateUp : h[p][i] = f16(silu(Wg_e x_t)_i * (Wu_e x_t)_i)    (A = dequant(int4), B = fp16 x gathered)
 //   kModeDown   : out[t][j] += w * (Wd_e h_p)_j                      (A = dequant(int4), B = h rows)
 // Work units are blocks of token rows (the routing block map for routed
 // experts, then ceil(T/block_rows) identity blocks for the shared expert) times
@@ -36,15 +37,18 @@ struct GemmArgs {
     // and shared (ss*, sb*) weights; rows of K/64 groups.
     const uint16_t *s0, *b0, *s1, *b1, *ss0, *sb0, *ss1, *sb1;
     const float *router_bias;
-    const __nv_bfloat16 *x;  // gate/up gather source [T][d]
+    const __half *xh;        // gate/up gather source: x converted to fp16 [T][d]
     float *logits;           // router output [T][E]
-    __nv_bfloat16 *h;        // gate/up output, down input [(top_k+1)*T][I]
+    __half *h;               // gate/up output, down input, fp16 [(top_k+1)*T][I]
     float *out;              // down output [T][d], accumulated
     Ctrl *ctrl;
 };
 
 // Dynamic shared memory bytes of grouped_gemm_kernel.
 size_t grouped_gemm_smem_bytes();
+
+// Before the expert GEMMs: out = 0 and xh = fp16(x)  (T x d elements).
+cudaError_t launch_prep_experts(const uint16_t *x, __half *xh, float *out, int64_t n_elems, cudaStream_t stream);
 
 // tmB: B operand (x for router, h for down; unused for gate/up which gathers x).
 // tmA0/tmA1: routed weight maps of the two 128-row tiles (router: Wr for both);
@@ -92,7 +96,7 @@ struct DecodeLayerArgs {
     int *unit_expert;         // [top_k*T+1]
     int *unit_mask;           // [top_k*T+1] token bitmask
     float *unit_w;            // [top_k*T+1][8]
-    __nv_bfloat16 *h;         // [top_k*T+1][8][I]
+    __half *h;                // fp16 [top_k*T+1][8][I]
     Ctrl *ctrl;
 };
 cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStream_t stream);
