@@ -209,6 +209,9 @@ def lily_moe_forward_timed(shape, weights, x, out, ws, events: Sequence[torch.cu
     """As lily_moe_forward, recording 6 events (start, after router GEMM, after
     routing tables, after zeroing out, after gate/up, after down)."""
     assert len(events) == 6
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on first record
+            e.record(torch.cuda.current_stream() if stream is None else stream)
     arr = (ctypes.c_void_p * 6)(*[e.cuda_event for e in events])
     rc = load().lily_moe_forward_timed(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), _ptr(out),
                                        None if routing is None else ctypes.byref(routing), _ptr(ws),

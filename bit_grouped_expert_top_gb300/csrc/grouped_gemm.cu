@@ -358,6 +358,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             const int mi = (warp - 4) >> 2;              // which matrix of the pair
             const int r = ((warp - 4) & 3) * 32 + lane;  // row within the 128-row tile
             const int ngroups = g.K / kBK;
+            const bool vec8 = (ngroups & 7) == 0;
             int ls = 0, as = 0;
             uint32_t lph = 0, aph = 0;
             bool ok = true;
@@ -369,13 +370,33 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 const int row = (mi ? r1 : r0) + r;
                 const uint16_t *srow = (u.shared ? (mi ? g.ss1 : g.ss0) : (mi ? g.s1 : g.s0)) + static_cast<size_t>(row) * ngroups;
                 const uint16_t *brow = (u.shared ? (mi ? g.sb1 : g.sb0) : (mi ? g.b1 : g.b0)) + static_cast<size_t>(row) * ngroups;
-                uint16_t sc = __ldg(srow), bi = __ldg(brow);
-                for (int kt = 0; kt < KT; ++kt) {
-                    uint16_t sc_n = 0, bi_n = 0;
-                    if (kt + 1 < KT) {
-                        sc_n = __ldg(srow + kt + 1);
-                        bi_n = __ldg(brow + kt + 1);
+                {
+                    // warm L2 with the next unit's scale / bias rows of this thread
+                    const int nt = tile + gridDim.x;
+                    if (nt < total_tiles) {
+                        const Unit un = unit_info(g, nt, n_routed);
+                        if (un.rows > 0) {
+                            int n0, n1;
+                            a_rows(g, un, n0, n1);
+                            const size_t nrow = static_cast<size_t>((mi ? n1 : n0) + r) * ngroups;
+                            prefetch_l2((un.shared ? (mi ? g.ss1 : g.ss0) : (mi ? g.s1 : g.s0)) + nrow);
+                            prefetch_l2((un.shared ? (mi ? g.sb1 : g.sb0) : (mi ? g.b1 : g.b0)) + nrow);
+                        }
                     }
+                }
+                // scale / bias of 8 consecutive groups per 16-byte register block,
+                // fetched one block (8 k-steps) ahead
+                uint4 s_cur = load_groups8(srow, 0, ngroups, vec8), b_cur = load_groups8(brow, 0, ngroups, vec8);
+                uint4 s_nxt = load_groups8(srow, 8, ngroups, vec8), b_nxt = load_groups8(brow, 8, ngroups, vec8);
+                for (int kt = 0; kt < KT; ++kt) {
+                    const int j = kt & 7;
+                    if (j == 0 && kt > 0) {
+                        s_cur = s_nxt;
+                        b_cur = b_nxt;
+                        s_nxt = load_groups8(srow, kt + 8, ngroups, vec8);
+                        b_nxt = load_groups8(brow, kt + 8, ngroups, vec8);
+                    }
+                    const uint16_t sc = pick16(s_cur, j), bi = pick16(b_cur, j);
                     if (!mbar_wait(&S.full_l[ls], lph, abort_flag, status) ||
                         !mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status)) {
                         ok = false;
@@ -395,8 +416,6 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         mbar_arrive(&S.full_a[as]);
                         mbar_arrive(&S.empty_l[ls]);
                     }
-                    sc = sc_n;
-                    bi = bi_n;
                     if (++ls == kLStages) {
                         ls = 0;
                         lph ^= 1;

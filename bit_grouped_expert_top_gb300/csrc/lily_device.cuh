@@ -307,6 +307,31 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t bits)
     return __uint_as_float(static_cast<uint32_t>(bits) << 16);
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// 16-bit values [g0, g0 + 8) of a row of n values, packed two per word (zero
+// past the end).  `vec` allows one 16-byte load (row 16-byte aligned, n % 8 == 0).
+__device__ __forceinline__ uint4 load_groups8(const uint16_t *row, int g0, int n, bool vec)
+{
+    if (g0 >= n) return make_uint4(0u, 0u, 0u, 0u);
+    if (vec) return __ldg(reinterpret_cast<const uint4 *>(row + g0));
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (g0 + j < n) w[j >> 1] |= static_cast<uint32_t>(__ldg(row + g0 + j)) << (16 * (j & 1));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Value j (0..7) of a block loaded by load_groups8.
+__device__ __forceinline__ uint16_t pick16(const uint4 v, int j)
+{
+    const uint32_t w = (j & 4) ? ((j & 2) ? v.w : v.z) : ((j & 2) ? v.y : v.x);
+    return static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
 // ----------------------------------------------------------------- top-8 of 256 (one warp)
