@@ -147,6 +147,22 @@ __device__ __forceinline__ void named_barrier_sync(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also returns the OR of `pred` over the participating
+// threads, so a group can leave a loop together.
+__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred)
+{
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %2, 0;\n\t"
+        "bar.red.or.pred q, %0, %1, p;\n\t"
+        "selp.u32 %3, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"(id), "r"(nthreads), "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return out != 0;
+}
+
 // ----------------------------------------------------------------- tcgen05 (UMMA + TMEM)
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
 {
@@ -165,8 +181,9 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, both K-major.
-__device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit inputs (type from idesc), fp32
+// accumulate, both K-major.
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate)
 {
     asm volatile(
@@ -287,6 +304,41 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t v, __half2 s2, __half2 b2
     o.z = __byte_perm(u04, u15, 0x7632);
     o.w = __byte_perm(u26, u37, 0x7632);
     return o;
+}
+
+// Eight packed 4-bit weights (element i in bits [4i, 4i+4)) -> eight fp16
+// weights w_i = q_i * s + b, each rounded once (fma.rn.f16x2), written in the
+// K order (0,4, 1,5, 2,6, 3,7) of one 16-byte chunk: the order that needs no
+// byte permutes.  The other GEMM operand must use the same order within each
+// group of 8 (see kperm8).  Nibbles 1,3,5,7 are used in place (16*q) with the
+// scale s/16 (s2_16), exact for |s| >= 2^-10.
+__device__ __forceinline__ uint4 dequant8_f16_kperm(uint32_t v, __half2 s2, __half2 s2_16, __half2 b2)
+{
+    const uint32_t kMagic = 0x64006400u;
+    const uint32_t v8 = v >> 8;
+    uint32_t p04 = (v & 0x000F000Fu) | kMagic;    // (1024 + q0, 1024 + q4)
+    uint32_t p15 = (v & 0x00F000F0u) | kMagic;    // (1024 + 16 q1, 1024 + 16 q5)
+    uint32_t p26 = (v8 & 0x000F000Fu) | kMagic;   // (1024 + q2, 1024 + q6)
+    uint32_t p37 = (v8 & 0x00F000F0u) | kMagic;   // (1024 + 16 q3, 1024 + 16 q7)
+    const __half2 k1024 = __floats2half2_rn(1024.0f, 1024.0f);
+    __half2 f04 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p04), k1024), s2, b2);
+    __half2 f15 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p15), k1024), s2_16, b2);
+    __half2 f26 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p26), k1024), s2, b2);
+    __half2 f37 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p37), k1024), s2_16, b2);
+    uint4 o;
+    o.x = *reinterpret_cast<uint32_t *>(&f04);
+    o.y = *reinterpret_cast<uint32_t *>(&f15);
+    o.z = *reinterpret_cast<uint32_t *>(&f26);
+    o.w = *reinterpret_cast<uint32_t *>(&f37);
+    return o;
+}
+
+// Position of logical K index k in the order used by dequant8_f16_kperm:
+// inside each group of 8, element j sits at 2j (j < 4) or 2(j-4)+1 (j >= 4).
+__host__ __device__ __forceinline__ int kperm8(int k)
+{
+    const int j = k & 7;
+    return (k & ~7) | (j < 4 ? 2 * j : 2 * (j - 4) + 1);
 }
 
 // bf16 bit pattern -> fp16 pair (value converted with round-to-nearest).
