@@ -494,6 +494,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             }
             const bool got = mbar_wait(&S.full_acc[ab], acc_ph, abort_flag, status);
             if (named_barrier_or(kBarEpilogue, 128, !got)) break;  // uniform stop; publishes ep_tok / ep_w
+            __syncwarp();  // tcgen05.ld is warp-collective (.sync.aligned)
             tc_fence_after();
             const uint32_t t0 = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(ab * 2 * kTileM);
             const uint32_t t1 = t0 + kTileM;
@@ -541,6 +542,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         }
     }
 
+    __syncwarp();  // every role reconverges its warp before the CTA-wide barrier
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
