@@ -142,30 +142,9 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Named barrier over `nthreads` threads (whole warps).  The warp is first
-// reconverged (__syncwarp), and the non-aligned barrier form is used, so the
-// barrier is legal after per-lane divergent code such as bounded spin-waits.
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads)
 {
-    __syncwarp();
-    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Named barrier that also returns the OR of `pred` over the participating
-// threads, so a group can leave a loop together.
-__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred)
-{
-    uint32_t out;
-    __syncwarp();
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %2, 0;\n\t"
-        "barrier.red.or.pred q, %0, %1, p;\n\t"
-        "selp.u32 %3, 1, 0, q;\n\t}"
-        : "=r"(out)
-        : "r"(id), "r"(nthreads), "r"(static_cast<uint32_t>(pred))
-        : "memory");
-    return out != 0;
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ----------------------------------------------------------------- tcgen05 (UMMA + TMEM)
