@@ -40,9 +40,10 @@ namespace lily {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kAStages = 3;   // dequantised A ring
-constexpr int kLStages = 4;   // load ring: raw int4 + B
-constexpr int kLag = 2;       // cp.async groups kept in flight by the gathering producer
+constexpr int kRStages = 8;   // raw int4 ring (TMA), consumed by the dequantisers
+constexpr int kBStages = 4;   // B ring (tokens), consumed by the MMA issuer
+constexpr int kAStages = 2;   // A ring (fp16 dequantised weights, or bf16 router weights by TMA)
+constexpr int kLag = 2;       // cp.async groups a gathering lane keeps in flight
 constexpr int kTileM = 128;
 constexpr int kBK = 64;       // one quantisation group, one 128-byte swizzle row
 constexpr int kTileN = 128;
@@ -50,21 +51,24 @@ constexpr int kABytes = kTileM * kBK * 2;    // 16 KB of 16-bit elements
 constexpr int kBBytes = kTileN * kBK * 2;    // 16 KB of 16-bit elements
 constexpr int kRawBytes = kTileM * kBK / 2;  // 4 KB int4
 constexpr uint32_t kTmemCols = 512;
+constexpr int kBarDequant0 = 1, kBarEpilogue = 3, kBarBProducer = 4;  // named barrier ids
 
 struct __align__(1024) Smem {
     uint8_t a[kAStages][2][kABytes];
-    uint8_t b[kLStages][kBBytes];
-    uint8_t raw[kLStages][2][kRawBytes];
-    uint64_t full_l[kLStages], empty_l[kLStages];
+    uint8_t b[kBStages][kBBytes];
+    uint8_t raw[kRStages][2][kRawBytes];
+    uint64_t full_r[kRStages], empty_r[kRStages];
+    uint64_t full_b[kBStages], empty_b[kBStages];
     uint64_t full_a[kAStages], empty_a[kAStages];
     uint64_t full_acc[2], empty_acc[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    int prod_tok[kTileN];  // producer: source row of each B row of the current unit
+    int prod_tok[kTileN];  // B producers: source row of each B row of the current unit
     int ep_tok[kTileN];    // epilogue: token of each column (down)
     float ep_w[kTileN];    // epilogue: routing weight of each column (down)
 };
+static_assert(sizeof(Smem) + 1024 <= 200 * 1024, "shared memory budget of one CTA");
 
 struct Unit {
     int e, p0, rows, n_mma, mt;
@@ -125,6 +129,16 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, int *
     }
 }
 
+// Waits for the last min(issued, depth) phases of a ring's full barriers.
+__device__ __forceinline__ void drain_ring(uint64_t *full, int depth, int issued, int *status)
+{
+    const int last = issued < depth ? issued : depth;
+    for (int i = 1; i <= last; ++i) {
+        const int step = issued - i;
+        drain_wait(&full[step % depth], (step / depth) & 1, status);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -136,11 +150,16 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     const int lane = threadIdx.x & 31;
     int *status = &g.ctrl->status;
     const bool dequant_mode = g.mode != kModeRouter;
+    const bool gather_b = g.mode == kModeGateUp;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kLStages; ++s) {
-            mbar_init(&S.full_l[s], g.mode == kModeGateUp ? 1 + 32 : 1);
-            mbar_init(&S.empty_l[s], dequant_mode ? 3 : 1);
+        for (int s = 0; s < kRStages; ++s) {
+            mbar_init(&S.full_r[s], 1);
+            mbar_init(&S.empty_r[s], 2);
+        }
+        for (int s = 0; s < kBStages; ++s) {
+            mbar_init(&S.full_b[s], gather_b ? 64 : 1);
+            mbar_init(&S.empty_b[s], 1);
         }
         for (int s = 0; s < kAStages; ++s) {
             mbar_init(&S.full_a[s], dequant_mode ? 2 : 1);
@@ -158,8 +177,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA0);
         prefetch_tmap(&tmA1);
-        if (g.mode != kModeGateUp) prefetch_tmap(&tmB);
-        if (g.mode != kModeRouter) {
+        if (!gather_b) prefetch_tmap(&tmB);
+        if (dequant_mode) {
             prefetch_tmap(&tmSA0);
             prefetch_tmap(&tmSA1);
         }
@@ -185,22 +204,76 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     const int total_tiles = (n_routed + g.n_shared_blocks) * g.m_tiles;
     const int KT = g.K / kBK;
 
+    // Abort handling: a bounded wait that gives up raises abort_flag; every
+    // later wait then returns at once.  Single-thread roles leave their loops;
+    // multi-warp groups keep walking their loops (skipping work) so that every
+    // thread still reaches every named barrier of its group.
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        int ls = 0, as = 0;
-        uint32_t lph = 0, aph = 0;
-        int issued = 0;       // load-ring steps issued
-        int p_old = 0, p_new = 0, n_pend = 0;  // gate/up: stages awaiting their cp.async group
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-            const Unit u = unit_info(g, tile, n_routed);
-            if (u.rows <= 0) continue;
-            int r0, r1;
-            a_rows(g, u, r0, r1);
-            const CUtensorMap *mA0 = u.shared ? &tmSA0 : &tmA0;
-            const CUtensorMap *mA1 = u.shared ? &tmSA1 : &tmA1;
-            if (g.mode == kModeGateUp) {
-                for (int r = lane; r < u.n_mma; r += 32) {
+        // ------------------------------------------------ A-side producer (one thread)
+        // dequant modes: packed int4 tiles into the raw ring; router: bf16 Wr tiles into the A ring
+        if (lane == 0) {
+            int rs = 0, as = 0;
+            uint32_t rph = 0, aph = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+                const Unit u = unit_info(g, tile, n_routed);
+                if (u.rows <= 0) continue;
+                int r0, r1;
+                a_rows(g, u, r0, r1);
+                const CUtensorMap *mA0 = u.shared ? &tmSA0 : &tmA0;
+                const CUtensorMap *mA1 = u.shared ? &tmSA1 : &tmA1;
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (dequant_mode) {
+                        if (!mbar_wait(&S.empty_r[rs], rph ^ 1, abort_flag, status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&S.full_r[rs], 2 * kRawBytes);
+                        tma_load_2d(S.raw[rs][0], mA0, &S.full_r[rs], kt * (kBK / 2), r0);
+                        tma_load_2d(S.raw[rs][1], mA1, &S.full_r[rs], kt * (kBK / 2), r1);
+                        if (++rs == kRStages) {
+                            rs = 0;
+                            rph ^= 1;
+                        }
+                    } else {
+                        if (!mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&S.full_a[as], 2 * kABytes);
+                        tma_load_2d(S.a[as][0], &tmA0, &S.full_a[as], kt * kBK, r0);
+                        tma_load_2d(S.a[as][1], &tmA0, &S.full_a[as], kt * kBK, r1);
+                        if (++as == kAStages) {
+                            as = 0;
+                            aph ^= 1;
+                        }
+                    }
+                    ++issued;
+                }
+            }
+            // Exit: no copy into this CTA's shared memory may still be in flight.
+            if (dequant_mode)
+                drain_ring(S.full_r, kRStages, issued, status);
+            else
+                drain_ring(S.full_a, kAStages, issued, status);
+        }
+        __syncwarp();
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------------------ B producers (token rows)
+        const int bl = (warp - 2) * 32 + lane;  // 0..63
+        if (gather_b) {
+            // two warps gather token rows of fp16 x with 16-byte cp.async into the
+            // 128-byte-swizzled layout; each lane signals a stage once its copies landed
+            int bs = 0;
+            uint32_t bph = 0;
+            int p_old = 0, p_new = 0, n_pend = 0;  // stages awaiting their cp.async group
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+                const Unit u = unit_info(g, tile, n_routed);
+                if (u.rows <= 0) continue;
+                named_barrier_sync(kBarBProducer, 64);  // previous unit's rows no longer read
+                for (int r = bl; r < u.n_mma; r += 64) {
                     const int rr = min(r, u.rows - 1);
                     int src = u.p0 + rr;
                     if (!u.shared) src = g.perm[u.p0 + rr] / g.top_k;
@@ -210,119 +283,98 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     }
                     S.prod_tok[r] = src;
                 }
-                __syncwarp();
-            }
-            const int b_row0 = (g.mode == kModeDown && u.shared) ? g.T * g.top_k + u.p0 : u.p0;
-            for (int kt = 0; kt < KT; ++kt) {
-                int good = 1;
-                if (lane == 0) {
-                    good = mbar_wait(&S.empty_l[ls], lph ^ 1, abort_flag, status);
-                    if (good && g.mode == kModeRouter) good = mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status);
-                }
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    if (g.mode == kModeRouter) {
-                        mbar_arrive_expect_tx(&S.full_a[as], 2 * kABytes);
-                        tma_load_2d(S.a[as][0], &tmA0, &S.full_a[as], kt * kBK, r0);
-                        tma_load_2d(S.a[as][1], &tmA0, &S.full_a[as], kt * kBK, r1);
-                        mbar_arrive_expect_tx(&S.full_l[ls], kBBytes);
-                        tma_load_2d(S.b[ls], &tmB, &S.full_l[ls], kt * kBK, b_row0);
-                    } else if (g.mode == kModeDown) {
-                        mbar_arrive_expect_tx(&S.full_l[ls], 2 * kRawBytes + kBBytes);
-                        tma_load_2d(S.raw[ls][0], mA0, &S.full_l[ls], kt * (kBK / 2), r0);
-                        tma_load_2d(S.raw[ls][1], mA1, &S.full_l[ls], kt * (kBK / 2), r1);
-                        tma_load_2d(S.b[ls], &tmB, &S.full_l[ls], kt * kBK, b_row0);
-                    } else {
-                        mbar_arrive_expect_tx(&S.full_l[ls], 2 * kRawBytes);
-                        tma_load_2d(S.raw[ls][0], mA0, &S.full_l[ls], kt * (kBK / 2), r0);
-                        tma_load_2d(S.raw[ls][1], mA1, &S.full_l[ls], kt * (kBK / 2), r1);
+                named_barrier_sync(kBarBProducer, 64);
+                for (int kt = 0; kt < KT; ++kt) {
+                    int good = 0;
+                    if (ok) {
+                        if (lane == 0) good = mbar_wait(&S.empty_b[bs], bph ^ 1, abort_flag, status);
+                        good = __shfl_sync(0xffffffffu, good, 0);
+                        if (!good) ok = false;
                     }
-                }
-                if (g.mode == kModeGateUp) {
-                    // Gather token rows: each (row, 16-byte chunk) pair lands in its
-                    // 128-byte-swizzled position.
-                    const int c = lane & 7;
-                    const __half *xk = g.xh + kt * kBK + c * 8;
-                    uint8_t *bst = S.b[ls];
-                    for (int r = lane >> 3; r < u.n_mma; r += 4) {
-                        const int src = S.prod_tok[r];
-                        cp_async_16(bst + r * 128 + ((c ^ (r & 7)) << 4), xk + static_cast<size_t>(src) * g.d);
+                    if (good) {
+                        const int c = bl & 7;
+                        const __half *xk = g.xh + kt * kBK + c * 8;
+                        uint8_t *bst = S.b[bs];
+                        for (int r = bl >> 3; r < u.n_mma; r += 8)
+                            cp_async_16(bst + r * 128 + ((c ^ (r & 7)) << 4),
+                                        xk + static_cast<size_t>(S.prod_tok[r]) * g.d);
+                        cp_async_commit();
+                        if (n_pend == kLag) {
+                            cp_async_wait_group<kLag>();
+                            fence_proxy_async_smem();
+                            mbar_arrive(&S.full_b[p_old]);
+                            p_old = p_new;
+                            p_new = bs;
+                        } else if (n_pend == 1) {
+                            p_new = bs;
+                            n_pend = 2;
+                        } else {
+                            p_old = bs;
+                            n_pend = 1;
+                        }
                     }
-                    cp_async_commit();
-                    if (n_pend == kLag) {
-                        cp_async_wait_group<kLag>();
-                        fence_proxy_async_smem();
-                        mbar_arrive(&S.full_l[p_old]);
-                        p_old = p_new;
-                        p_new = ls;
-                    } else if (n_pend == 1) {
-                        p_new = ls;
-                        n_pend = 2;
-                    } else {
-                        p_old = ls;
-                        n_pend = 1;
+                    if (++bs == kBStages) {
+                        bs = 0;
+                        bph ^= 1;
                     }
-                }
-                ++issued;
-                if (++ls == kLStages) {
-                    ls = 0;
-                    lph ^= 1;
-                }
-                if (g.mode == kModeRouter && ++as == kAStages) {
-                    as = 0;
-                    aph ^= 1;
                 }
             }
-        }
-        if (g.mode == kModeGateUp) {
             cp_async_wait_all();
             fence_proxy_async_smem();
-            if (n_pend >= 1) mbar_arrive(&S.full_l[p_old]);
-            if (n_pend == 2) mbar_arrive(&S.full_l[p_new]);
-        }
-        // Exit: make sure no copy into this CTA's shared memory is still in flight.
-        if (lane == 0) {
-            const int last = issued < kLStages ? issued : kLStages;
-            for (int i = 1; i <= last; ++i) {
-                const int step = issued - i;
-                drain_wait(&S.full_l[step % kLStages], (step / kLStages) & 1, status);
-            }
-            if (g.mode == kModeRouter) {
-                const int lasta = issued < kAStages ? issued : kAStages;
-                for (int i = 1; i <= lasta; ++i) {
-                    const int step = issued - i;
-                    drain_wait(&S.full_a[step % kAStages], (step / kAStages) & 1, status);
+            if (n_pend >= 1) mbar_arrive(&S.full_b[p_old]);
+            if (n_pend == 2) mbar_arrive(&S.full_b[p_new]);
+        } else if (bl == 0) {
+            // contiguous rows (x for the router, h for the down projection): one 2-D TMA per stage
+            int bs = 0;
+            uint32_t bph = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+                const Unit u = unit_info(g, tile, n_routed);
+                if (u.rows <= 0) continue;
+                const int b_row0 = (g.mode == kModeDown && u.shared) ? g.T * g.top_k + u.p0 : u.p0;
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(&S.empty_b[bs], bph ^ 1, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&S.full_b[bs], kBBytes);
+                    tma_load_2d(S.b[bs], &tmB, &S.full_b[bs], kt * kBK, b_row0);
+                    ++issued;
+                    if (++bs == kBStages) {
+                        bs = 0;
+                        bph ^= 1;
+                    }
                 }
             }
+            drain_ring(S.full_b, kBStages, issued, status);
         }
+        __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------ MMA issuer (one thread)
         if (lane == 0) {
-            int ls = 0, as = 0, ab = 0;
-            uint32_t lph = 0, aph = 0, acc_ph = 0;
+            int bs = 0, as = 0, ab = 0;
+            uint32_t bph = 0, aph = 0, acc_ph = 0;
             bool ok = true;
+            const uint32_t fmt = dequant_mode ? kFmtF16 : kFmtBF16;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 const Unit u = unit_info(g, tile, n_routed);
                 if (u.rows <= 0) continue;
                 if (!mbar_wait(&S.empty_acc[ab], acc_ph ^ 1, abort_flag, status)) break;
                 tc_fence_after();
-                const uint32_t idesc = idesc_f32acc(g.mode == kModeRouter ? kFmtBF16 : kFmtF16, kTileM, u.n_mma);
+                const uint32_t idesc = idesc_f32acc(fmt, kTileM, u.n_mma);
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(ab * 2 * kTileM);
                 const uint32_t d1 = d0 + kTileM;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!mbar_wait(&S.full_a[as], aph, abort_flag, status) ||
-                        !mbar_wait(&S.full_l[ls], lph, abort_flag, status)) {
+                        !mbar_wait(&S.full_b[bs], bph, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(S.a[as][0]);
                     const uint32_t a1 = smem_u32(S.a[as][1]);
-                    const uint32_t bb = smem_u32(S.b[ls]);
+                    const uint32_t bb = smem_u32(S.b[bs]);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint32_t acc = (kt | kk) != 0;
@@ -330,14 +382,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         umma_ss(d1, sdesc_sw128(a1 + kk * 32), sdesc_sw128(bb + kk * 32), idesc, acc);
                     }
                     umma_commit(&S.empty_a[as]);
-                    umma_commit(&S.empty_l[ls]);
+                    umma_commit(&S.empty_b[bs]);
                     if (++as == kAStages) {
                         as = 0;
                         aph ^= 1;
                     }
-                    if (++ls == kLStages) {
-                        ls = 0;
-                        lph ^= 1;
+                    if (++bs == kBStages) {
+                        bs = 0;
+                        bph ^= 1;
                     }
                 }
                 if (!ok) break;
@@ -353,16 +405,16 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         }
         __syncwarp();
     } else if (warp >= 4 && warp < 12) {
-        // ------------------------------------------------------------ dequantisers
+        // ------------------------------------------------ dequantisers
         if (dequant_mode) {
             const int mi = (warp - 4) >> 2;              // which matrix of the pair
             const int r = ((warp - 4) & 3) * 32 + lane;  // row within the 128-row tile
             const int ngroups = g.K / kBK;
             const bool vec8 = (ngroups & 7) == 0;
-            int ls = 0, as = 0;
-            uint32_t lph = 0, aph = 0;
+            int rs = 0, as = 0;
+            uint32_t rph = 0, aph = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
                 const Unit u = unit_info(g, tile, n_routed);
                 if (u.rows <= 0) continue;
                 int r0, r1;
@@ -396,30 +448,31 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         s_nxt = load_groups8(srow, kt + 8, ngroups, vec8);
                         b_nxt = load_groups8(brow, kt + 8, ngroups, vec8);
                     }
-                    const uint16_t sc = pick16(s_cur, j), bi = pick16(b_cur, j);
-                    if (!mbar_wait(&S.full_l[ls], lph, abort_flag, status) ||
-                        !mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint4 *src = reinterpret_cast<const uint4 *>(S.raw[ls][mi] + r * (kBK / 2));
-                    const uint4 q0 = src[0], q1 = src[1];
-                    const __half2 s2 = half2_from_bf16_bits(sc), b2 = half2_from_bf16_bits(bi);
-                    const __half2 s2_16 = __hmul2(s2, __floats2half2_rn(0.0625f, 0.0625f));
-                    uint8_t *dst = S.a[as][mi] + (r >> 3) * 1024 + (r & 7) * 128;
-                    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    const bool got = ok && mbar_wait(&S.full_r[rs], rph, abort_flag, status) &&
+                                     mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status);
+                    if (!got) ok = false;
+                    if (got) {
+                        const uint16_t sc = pick16(s_cur, j), bi = pick16(b_cur, j);
+                        const uint4 *src = reinterpret_cast<const uint4 *>(S.raw[rs][mi] + r * (kBK / 2));
+                        const uint4 q0 = src[0], q1 = src[1];
+                        const __half2 s2 = half2_from_bf16_bits(sc), b2 = half2_from_bf16_bits(bi);
+                        const __half2 s2_16 = __hmul2(s2, __floats2half2_rn(0.0625f, 0.0625f));
+                        uint8_t *dst = S.a[as][mi] + (r >> 3) * 1024 + (r & 7) * 128;
+                        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) = dequant8_f16_kperm(words[c], s2, s2_16, b2);
-                    fence_proxy_async_smem();
-                    named_barrier_sync(1 + mi, 128);
-                    if (r == 0) {
-                        mbar_arrive(&S.full_a[as]);
-                        mbar_arrive(&S.empty_l[ls]);
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) =
+                                dequant8_f16_kperm(words[c], s2, s2_16, b2);
+                        fence_proxy_async_smem();
                     }
-                    if (++ls == kLStages) {
-                        ls = 0;
-                        lph ^= 1;
+                    named_barrier_sync(kBarDequant0 + mi, 128);
+                    if (r == 0 && ok) {
+                        mbar_arrive(&S.full_a[as]);
+                        mbar_arrive(&S.empty_r[rs]);
+                    }
+                    if (++rs == kRStages) {
+                        rs = 0;
+                        rph ^= 1;
                     }
                     if (++as == kAStages) {
                         as = 0;
@@ -429,11 +482,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             }
         }
     } else if (warp >= 12) {
-        // ------------------------------------------------------------ epilogue
+        // ------------------------------------------------ epilogue
         const int ew = warp & 3;         // TMEM lane quarter this warp may access
         const int et = ew * 32 + lane;   // accumulator row (weight row within the tile)
         int ab = 0;
         uint32_t acc_ph = 0;
+        bool ok = true;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             const Unit u = unit_info(g, tile, n_routed);
             if (u.rows <= 0) continue;
@@ -453,8 +507,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 S.ep_tok[et] = tok;
                 S.ep_w[et] = wt;
             }
-            named_barrier_sync(3, 128);
-            if (!mbar_wait(&S.full_acc[ab], acc_ph, abort_flag, status)) break;
+            named_barrier_sync(kBarEpilogue, 128);  // publishes ep_tok / ep_w
+            // warp-uniform decision: tcgen05.ld below is warp-collective
+            const bool got = __all_sync(0xffffffffu, ok && mbar_wait(&S.full_acc[ab], acc_ph, abort_flag, status));
+            if (!got) ok = false;
+            if (got) {
             tc_fence_after();
             const uint32_t t0 = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(ab * 2 * kTileM);
             const uint32_t t1 = t0 + kTileM;
@@ -463,6 +520,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 bias0 = g.router_bias[et];
                 bias1 = g.router_bias[kTileM + et];
             }
+            // h columns are stored with K permuted inside each group of 8 (see dequant8_f16_kperm)
+            const int hcol = kperm8(u.mt * kTileM + et);
             for (int c0 = 0; c0 < u.n_mma; c0 += 32) {
                 uint32_t v0[32], v1[32];
                 tmem_ld_32x32b_x32(t0 + c0, v0);
@@ -479,8 +538,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                             lrow[kTileM + et] = f1 + bias1;
                         } else if (g.mode == kModeGateUp) {
                             const size_t p = u.shared ? static_cast<size_t>(g.T) * g.top_k + u.p0 + n : static_cast<size_t>(u.p0 + n);
-                            // h columns in the K order of dequant8_f16_kperm (the down GEMM's A)
-                            g.h[p * g.I + kperm8(u.mt * kTileM + et)] = __float2half_rn(silu_f(f0) * f1);
+                            g.h[p * g.I + hcol] = __float2half_rn(silu_f(f0) * f1);
                         } else {
                             float *orow = g.out + static_cast<size_t>(S.ep_tok[n]) * g.d + u.mt * 2 * kTileM;
                             const float wt = S.ep_w[n];
@@ -493,7 +551,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty_acc[ab]);
-            named_barrier_sync(3, 128);
+            }
+            named_barrier_sync(kBarEpilogue, 128);  // ep_tok / ep_w free for the next unit
             if (++ab == 2) {
                 ab = 0;
                 acc_ph ^= 1;
@@ -501,12 +560,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         }
     }
 
+    __syncwarp();  // every role reconverges its warp before the CTA-wide barrier
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+// Before the expert GEMMs: xh = fp16(x) with K permuted inside each group of 8
+// (the order the dequantisers write the weights in), and out = 0.
 __global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, uint4 *xh, float4 *out, int64_t n8)
 {
     for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n8; i += static_cast<int64_t>(gridDim.x) * 256) {
@@ -521,7 +583,7 @@ __global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, uint4
         }
         uint32_t o[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // K order of dequant8_f16_kperm: slot pair j holds (j, j + 4)
+        for (int j = 0; j < 4; ++j) {  // slot pair j holds elements (j, j + 4)
             const __half2 hv = __floats2half2_rn(f[j], f[j + 4]);
             o[j] = *reinterpret_cast<const uint32_t *>(&hv);
         }

@@ -142,8 +142,11 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Named barrier over `nthreads` threads (whole warps); the warp is reconverged
+// first, as bar.sync is warp-aligned.
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads)
 {
+    __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
