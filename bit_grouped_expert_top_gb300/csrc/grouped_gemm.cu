@@ -40,9 +40,9 @@ namespace lily {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kRStages = 8;   // raw int4 ring (TMA), consumed by the dequantisers
+constexpr int kRStages = 4;   // raw int4 ring (TMA), consumed by the dequantisers
 constexpr int kBStages = 4;   // B ring (tokens), consumed by the MMA issuer
-constexpr int kAStages = 2;   // A ring (fp16 dequantised weights, or bf16 router weights by TMA)
+constexpr int kAStages = 3;   // A ring (fp16 dequantised weights, or bf16 router weights by TMA)
 constexpr int kLag = 2;       // cp.async groups a gathering lane keeps in flight
 constexpr int kTileM = 128;
 constexpr int kBK = 64;       // one quantisation group, one 128-byte swizzle row
@@ -284,6 +284,18 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     S.prod_tok[r] = src;
                 }
                 named_barrier_sync(kBarBProducer, 64);
+                {
+                    // warm L2 with the token rows of this CTA's next unit
+                    const int nt = tile + gridDim.x;
+                    if (nt < total_tiles) {
+                        const Unit un = unit_info(g, nt, n_routed);
+                        for (int r = bl; r < un.rows; r += 64) {
+                            int src = un.shared ? un.p0 + r : g.perm[un.p0 + r] / g.top_k;
+                            if (src >= 0 && src < g.T)
+                                bulk_prefetch_l2(g.xh + static_cast<size_t>(src) * g.d, static_cast<uint32_t>(g.d) * 2u);
+                        }
+                    }
+                }
                 for (int kt = 0; kt < KT; ++kt) {
                     int good = 0;
                     if (ok) {
@@ -333,6 +345,17 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 const Unit u = unit_info(g, tile, n_routed);
                 if (u.rows <= 0) continue;
                 const int b_row0 = (g.mode == kModeDown && u.shared) ? g.T * g.top_k + u.p0 : u.p0;
+                if (g.mode == kModeDown) {
+                    // warm L2 with the h rows of this CTA's next unit (contiguous rows)
+                    const int nt = tile + gridDim.x;
+                    if (nt < total_tiles) {
+                        const Unit un = unit_info(g, nt, n_routed);
+                        if (un.rows > 0) {
+                            const size_t row0 = un.shared ? static_cast<size_t>(g.T) * g.top_k + un.p0 : un.p0;
+                            bulk_prefetch_l2(g.h + row0 * g.I, static_cast<uint32_t>(un.rows) * g.I * 2u);
+                        }
+                    }
+                }
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!mbar_wait(&S.empty_b[bs], bph ^ 1, abort_flag, status)) {
                         ok = false;

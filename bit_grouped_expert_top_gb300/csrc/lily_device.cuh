@@ -83,19 +83,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the waiting thread is parked by the
+// hardware until the phase completes or about `hint_ns` nanoseconds pass, so a
+// waiting warp does not take issue slots from working warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up (returns
 // false) when another role raised `abort_flag`, or after LILY_WAIT_LIMIT_NS, in
 // which case it records kErrDeviceTimeout and raises `abort_flag`.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status)
 {
     const uint32_t addr = smem_u32(bar);
-#pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-        if (mbar_try_wait(addr, parity)) return true;
+    if (mbar_try_wait(addr, parity)) return true;
     const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait(addr, parity)) return true;
+        if (mbar_try_wait_sleep(addr, parity, 20000u)) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > LILY_WAIT_LIMIT_NS) {
             record_error(status, kErrDeviceTimeout);
@@ -349,6 +363,13 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t bits)
 __device__ __forceinline__ void prefetch_l2(const void *p)
 {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Asynchronous prefetch of `bytes` (multiple of 16, 16-byte aligned address)
+// of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // 16-bit values [g0, g0 + 8) of a row of n values, packed two per word (zero
