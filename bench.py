@@ -163,6 +163,8 @@ def time_prefill(cfg, steps, warmup, n_sets, stream, with_stages=True):
                       group=cfg.group, block_rows=cfg.block_rows)
     ws = lm.alloc_workspace(s)
     out = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
+    # inputs and the zeroed workspace were made on the default stream
+    stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         for i in range(warmup):
             lm.lily_moe_forward(s, ws_l[i % n_sets], xs[i % n_sets], out, ws, stream=stream)
@@ -216,6 +218,7 @@ def bench_decode(cfg, Ts, reps, stream):
         x = make_x(cfg, "cuda", seed_offset=500 + T, T=T)
         out = torch.empty((L, T, cfg.d), dtype=torch.float32, device="cuda")
         idx = torch.empty((L, T, cfg.top_k), dtype=torch.int32, device="cuda")
+        stream.wait_stream(torch.cuda.current_stream())
         for _ in range(3):
             lm.lily_moe_decode(s, wl, x, out, ws, trace={"topk_idx": idx}, stream=stream)
         stream.synchronize()
@@ -274,6 +277,7 @@ def run_ours(args):
     x_host = [x.cpu().pin_memory() for x in ctx["xs"]]
     out_host = torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory()
     x_dev = torch.empty_like(ctx["xs"][0])
+    stream.wait_stream(torch.cuda.current_stream())
     e2e_steps = max(5, min(args.steps, 40))
     with torch.cuda.stream(stream):
         for i in range(3):
@@ -334,6 +338,7 @@ def run_ours(args):
         rt = lm.alloc_routing(ctx["shape"])
         rt["logits"] = lg
         r = lm.make_routing(rt)
+        stream.wait_stream(torch.cuda.current_stream())
         lm.lily_moe_route(ctx["shape"], ctx["ws_l"][0], ctx["xs"][0], r, ctx["ws"], stream=stream)
         stream.synchronize()
         n_tok = args.cpu_tokens
