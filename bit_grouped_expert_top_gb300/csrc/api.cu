@@ -400,7 +400,7 @@ size_t lily_moe_workspace_bytes(const lily_moe_shape *shape, int32_t n_layers_de
     if (check_shape(shape) != LILY_OK) return 0;
     size_t need = prefill_layout(*shape).total;
     if (n_layers_decode > 0) {
-        if (shape->T < 1 || shape->T > 8 || shape->d > 8192 || shape->I > 1024) return 0;
+        if (shape->T < 1 || shape->T > 8 || shape->d > 4096 || shape->I > 1024) return 0;
         need = std::max(need, decode_layout(*shape).total);
     }
     return need;
@@ -463,7 +463,7 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
     int rc;
     if ((rc = check_shape(shape))) return rc;
     if (n_layers < 1 || !layers) return LILY_ERR_INVALID;
-    if (shape->T < 1 || shape->T > 8 || shape->d > 8192 || shape->I > 1024) return LILY_ERR_UNSUPPORTED;
+    if (shape->T < 1 || shape->T > 8 || shape->d > 4096 || shape->I > 1024) return LILY_ERR_UNSUPPORTED;
     for (int l = 0; l < n_layers; ++l)
         if ((rc = check_weights(&layers[l]))) return rc;
     if ((rc = check_ws(ws, ws_bytes, decode_layout(*shape).total))) return rc;

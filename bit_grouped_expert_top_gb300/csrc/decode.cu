@@ -91,6 +91,18 @@ dec_route_kernel(const DecodeLayerArgs a)
     __shared__ int is_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int T = a.T, d = a.d;
+    const int e = blockIdx.x * kDecWarps + warp;  // this warp's expert
+    const uint4 *wrow = reinterpret_cast<const uint4 *>(a.router_w + static_cast<size_t>(e < a.E ? e : 0) * d);
+    const int n8 = d / 8;  // 16-byte chunks of a router row
+
+    // The router row does not depend on the layer input: start its loads first.
+    constexpr int kPre = 8;
+    uint4 wpre[kPre];
+#pragma unroll
+    for (int m = 0; m < kPre; ++m) {
+        const int c = lane + 32 * m;
+        if (e < a.E && c < n8) wpre[m] = __ldg(wrow + c);
+    }
 
     // ---- layer input
     if (a.prev_out == nullptr) {
@@ -100,6 +112,7 @@ dec_route_kernel(const DecodeLayerArgs a)
         float ss[kMaxT];
 #pragma unroll
         for (int t = 0; t < kMaxT; ++t) ss[t] = 0.0f;
+#pragma unroll 4
         for (int c = threadIdx.x; c < d; c += kDecThreads) {
 #pragma unroll
             for (int t = 0; t < kMaxT; ++t)
@@ -135,26 +148,29 @@ dec_route_kernel(const DecodeLayerArgs a)
     }
 
     // ---- router GEMV: one warp per expert
-    const int e = blockIdx.x * kDecWarps + warp;
     if (e < a.E) {
         float acc[kMaxT];
 #pragma unroll
         for (int t = 0; t < kMaxT; ++t) acc[t] = 0.0f;
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(a.router_w + static_cast<size_t>(e) * d);
-        for (int c = lane; c < d / 8; c += 32) {
-            const uint4 wv = __ldg(wrow + c);
-            const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+        for (int m0 = 0; m0 * 32 < n8; m0 += kPre) {
 #pragma unroll
-            for (int t = 0; t < kMaxT; ++t) {
-                if (t < T) {
-                    const uint4 xv = reinterpret_cast<const uint4 *>(xs + static_cast<size_t>(t) * d)[c];
-                    const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
+            for (int m = 0; m < kPre; ++m) {
+                const int c = lane + 32 * (m0 + m);
+                if (c >= n8) continue;
+                const uint4 wv = m0 == 0 ? wpre[m] : __ldg(wrow + c);
+                const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const float2 wf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wu[p]));
-                        const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xu[p]));
-                        acc[t] = fmaf(wf.x, xf.x, acc[t]);
-                        acc[t] = fmaf(wf.y, xf.y, acc[t]);
+                for (int t = 0; t < kMaxT; ++t) {
+                    if (t < T) {
+                        const uint4 xv = reinterpret_cast<const uint4 *>(xs + static_cast<size_t>(t) * d)[c];
+                        const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) {
+                            const float2 wf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wu[p]));
+                            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xu[p]));
+                            acc[t] = fmaf(wf.x, xf.x, acc[t]);
+                            acc[t] = fmaf(wf.y, xf.y, acc[t]);
+                        }
                     }
                 }
             }
@@ -246,7 +262,7 @@ __device__ __forceinline__ void load_padded(const uint16_t *src, Act *dst, int r
     }
 }
 
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, 2)
 dec_gateup_kernel(const DecodeLayerArgs a)
 {
     extern __shared__ __align__(16) uint8_t dsm[];
@@ -259,47 +275,88 @@ dec_gateup_kernel(const DecodeLayerArgs a)
 
     const int n_units = *a.n_units;
     const int items = n_units * I;
-    for (int item = blockIdx.x * kDecWarps + warp; item < items; item += gridDim.x * kDecWarps) {
-        const int u = item / I, i = item - u * I;
-        const int e = a.unit_expert[u];
-        const int mask = a.unit_mask[u];
-        if (e >= a.E || mask == 0) {
-            if (lane == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
-            continue;
-        }
-        const bool sh = e < 0;
-        const size_t row = sh ? static_cast<size_t>(i) : static_cast<size_t>(e) * I + i;
-        const uint4 *gq = reinterpret_cast<const uint4 *>((sh ? a.sh_gate_q : a.gate_q) + row * (d / 2));
-        const uint4 *uq = reinterpret_cast<const uint4 *>((sh ? a.sh_up_q : a.up_q) + row * (d / 2));
-        const uint16_t *gs = (sh ? a.sh_gate_s : a.gate_s) + row * ngroups;
-        const uint16_t *gb = (sh ? a.sh_gate_b : a.gate_b) + row * ngroups;
-        const uint16_t *us = (sh ? a.sh_up_s : a.up_s) + row * ngroups;
-        const uint16_t *ub = (sh ? a.sh_up_b : a.up_b) + row * ngroups;
-        float accg[kMaxT], accu[kMaxT];
+    const int n_pairs = (items + 1) / 2;
+    // A warp takes two (unit, row) items at a time; each lane first issues every
+    // 16-byte weight load of both items (gate and up), then computes.
+    for (int pr = blockIdx.x * kDecWarps + warp; pr < n_pairs; pr += gridDim.x * kDecWarps) {
+        const uint4 *gq[2], *uq[2];
+        const uint16_t *gs[2], *gb[2], *us[2], *ub[2];
+        int mask[2], uu[2], ii[2];
 #pragma unroll
-        for (int t = 0; t < kMaxT; ++t) accg[t] = accu[t] = 0.0f;
-        for (int c = lane; c < n_chunks; c += 32) {
-            const uint4 qg = __ldg(gq + c), qu = __ldg(uq + c);
-            const int grp = c >> 1;
-            const __half2 sg = half2_from_bf16_bits(__ldg(gs + grp)), bg = half2_from_bf16_bits(__ldg(gb + grp));
-            const __half2 su = half2_from_bf16_bits(__ldg(us + grp)), bu = half2_from_bf16_bits(__ldg(ub + grp));
+        for (int k = 0; k < 2; ++k) {
+            const int item = min(2 * pr + k, items - 1);
+            const int u = item / I, i = item - u * I;
+            const int e = a.unit_expert[u];
+            int m = a.unit_mask[u] & ((1 << T) - 1);
+            if (e >= a.E || m == 0) {
+                if (lane == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
+                m = 0;
+            }
+            if (2 * pr + k >= items) m = 0;  // odd tail: the duplicate item does nothing
+            const bool sh = e < 0;
+            const size_t row = sh ? static_cast<size_t>(i) : static_cast<size_t>(e < a.E ? e : 0) * I + i;
+            gq[k] = reinterpret_cast<const uint4 *>((sh ? a.sh_gate_q : a.gate_q) + row * (d / 2));
+            uq[k] = reinterpret_cast<const uint4 *>((sh ? a.sh_up_q : a.up_q) + row * (d / 2));
+            gs[k] = (sh ? a.sh_gate_s : a.gate_s) + row * ngroups;
+            gb[k] = (sh ? a.sh_gate_b : a.gate_b) + row * ngroups;
+            us[k] = (sh ? a.sh_up_s : a.up_s) + row * ngroups;
+            ub[k] = (sh ? a.sh_up_b : a.up_b) + row * ngroups;
+            mask[k] = m;
+            uu[k] = u;
+            ii[k] = i;
+        }
+        float accg[2][kMaxT], accu[2][kMaxT];
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int t = 0; t < kMaxT; ++t) accg[k][t] = accu[k][t] = 0.0f;
+        for (int c0 = 0; c0 < n_chunks; c0 += 2 * 32) {
+            uint4 qg[2][2], qu[2][2];
+            uint16_t vgs[2][2], vgb[2][2], vus[2][2], vub[2][2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int c = c0 + q * 32 + lane;
+                    if (c < n_chunks && mask[k]) {
+                        qg[k][q] = __ldg(gq[k] + c);
+                        qu[k][q] = __ldg(uq[k] + c);
+                        vgs[k][q] = __ldg(gs[k] + (c >> 1));
+                        vgb[k][q] = __ldg(gb[k] + (c >> 1));
+                        vus[k][q] = __ldg(us[k] + (c >> 1));
+                        vub[k][q] = __ldg(ub[k] + (c >> 1));
+                    }
+                }
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int c = c0 + q * 32 + lane;
+                    if (c < n_chunks && mask[k]) {
+                        const __half2 sg = half2_from_bf16_bits(vgs[k][q]), bg = half2_from_bf16_bits(vgb[k][q]);
+                        const __half2 su = half2_from_bf16_bits(vus[k][q]), bu = half2_from_bf16_bits(vub[k][q]);
+#pragma unroll
+                        for (int t = 0; t < kMaxT; ++t) {
+                            if (t < T && ((mask[k] >> t) & 1)) {
+                                const __nv_bfloat16 *xr = xs + pad_index(t, c * kChunk, n_chunks);
+                                accg[k][t] += dot32(qg[k][q], sg, bg, xr);
+                                accu[k][t] += dot32(qu[k][q], su, bu, xr);
+                            }
+                        }
+                    }
+                }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
 #pragma unroll
             for (int t = 0; t < kMaxT; ++t) {
-                if (t < T && ((mask >> t) & 1)) {
-                    const __nv_bfloat16 *xr = xs + pad_index(t, c * kChunk, n_chunks);
-                    accg[t] += dot32(qg, sg, bg, xr);
-                    accu[t] += dot32(qu, su, bu, xr);
+                if (t < T && ((mask[k] >> t) & 1)) {
+                    const float gv = warp_sum(accg[k][t]);
+                    const float uv = warp_sum(accu[k][t]);
+                    if (lane == 0)
+                        a.h[(static_cast<size_t>(uu[k]) * kMaxT + t) * I + ii[k]] = __float2half_rn(silu_f(gv) * uv);
                 }
             }
-        }
-#pragma unroll
-        for (int t = 0; t < kMaxT; ++t) {
-            if (t < T && ((mask >> t) & 1)) {
-                const float g = warp_sum(accg[t]);
-                const float v = warp_sum(accu[t]);
-                if (lane == 0) a.h[(static_cast<size_t>(u) * kMaxT + t) * I + i] = __float2half_rn(silu_f(g) * v);
-            }
-        }
     }
 }
 
@@ -354,31 +411,46 @@ dec_down_kernel(const DecodeLayerArgs a)
 #pragma unroll
         for (int t = 0; t < kMaxT; ++t) acc[t] = 0.0f;
         const int n_items = n_units * n_chunks;
-#pragma unroll 2
-        for (int it = lane; it < n_items; it += 32) {
-            const int u = it / n_chunks, c = it - u * n_chunks;
-            const int e = s_expert[u];
-            const bool sh = e < 0;
-            const size_t row = sh ? static_cast<size_t>(j) : static_cast<size_t>(e) * d + j;
-            const uint4 q = __ldg(reinterpret_cast<const uint4 *>((sh ? a.sh_down_q : a.down_q) + row * (I / 2)) + c);
-            const int grp = c >> 1;
-            const __half2 s2 = half2_from_bf16_bits(__ldg((sh ? a.sh_down_s : a.down_s) + row * ngroups + grp));
-            const __half2 b2 = half2_from_bf16_bits(__ldg((sh ? a.sh_down_b : a.down_b) + row * ngroups + grp));
-            const int mask = s_mask[u];
-            int slot = s_slot[u];
+        constexpr int kB = 8;  // chunk-items per lane with loads in flight together
+        for (int it0 = 0; it0 < n_items; it0 += kB * 32) {
+            uint4 q[kB];
+            uint16_t vs[kB], vb[kB];
 #pragma unroll
-            for (int t = 0; t < kMaxT; ++t) {
-                if (t < T && ((mask >> t) & 1)) {
-                    acc[t] += s_w[u][t] * dot32(q, s2, b2, hs + pad_index(slot, c * kChunk, n_chunks));
-                    ++slot;
+            for (int m = 0; m < kB; ++m) {
+                const int it = it0 + m * 32 + lane;
+                if (it < n_items) {
+                    const int u = it / n_chunks, c = it - u * n_chunks;
+                    const int e = s_expert[u];
+                    const bool sh = e < 0;
+                    const size_t row = sh ? static_cast<size_t>(j) : static_cast<size_t>(e) * d + j;
+                    q[m] = __ldg(reinterpret_cast<const uint4 *>((sh ? a.sh_down_q : a.down_q) + row * (I / 2)) + c);
+                    vs[m] = __ldg((sh ? a.sh_down_s : a.down_s) + row * ngroups + (c >> 1));
+                    vb[m] = __ldg((sh ? a.sh_down_b : a.down_b) + row * ngroups + (c >> 1));
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < kB; ++m) {
+                const int it = it0 + m * 32 + lane;
+                if (it < n_items) {
+                    const int u = it / n_chunks, c = it - u * n_chunks;
+                    const __half2 s2 = half2_from_bf16_bits(vs[m]), b2 = half2_from_bf16_bits(vb[m]);
+                    const int mask = s_mask[u];
+                    int slot = s_slot[u];
+#pragma unroll
+                    for (int t = 0; t < kMaxT; ++t) {
+                        if (t < T && ((mask >> t) & 1)) {
+                            acc[t] += s_w[u][t] * dot32(q[m], s2, b2, hs + pad_index(slot, c * kChunk, n_chunks));
+                            ++slot;
+                        }
+                    }
                 }
             }
         }
 #pragma unroll
         for (int t = 0; t < kMaxT; ++t) {
             if (t < T) {
-                const float s = warp_sum(acc[t]);
-                if (lane == 0) a.out[static_cast<size_t>(t) * d + j] = s;
+                const float sm = warp_sum(acc[t]);
+                if (lane == 0) a.out[static_cast<size_t>(t) * d + j] = sm;
             }
         }
     }
@@ -401,8 +473,8 @@ cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStrea
         configured = true;
     }
     dec_route_kernel<<<(a.E + kDecWarps - 1) / kDecWarps, kDecThreads, decode_smem_route(a.T, a.d), stream>>>(a);
-    dec_gateup_kernel<<<num_sms, kDecThreads, decode_smem_gateup(a.T, a.d), stream>>>(a);
-    dec_down_kernel<<<num_sms, kDecThreads, decode_smem_down(a.T, a.I), stream>>>(a);
+    dec_gateup_kernel<<<2 * num_sms, kDecThreads, decode_smem_gateup(a.T, a.d), stream>>>(a);
+    dec_down_kernel<<<(a.d + kDecWarps - 1) / kDecWarps, kDecThreads, decode_smem_down(a.T, a.I), stream>>>(a);
     return cudaGetLastError();
 }
 

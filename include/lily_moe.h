@@ -58,7 +58,7 @@ enum {
  *   E = 256, top_k = 8, group = 64,
  *   d a multiple of 256 in [256, 16384], I a multiple of 128 in [128, 4096],
  *   I_shared = I, block_rows in {16, 32, 64, 128}, 0 <= T <= 1048576.
- * lily_moe_decode additionally needs 1 <= T <= 8.
+ * lily_moe_decode additionally needs 1 <= T <= 8, d <= 4096 and I <= 1024.
  */
 typedef struct lily_moe_shape {
     int32_t T;          /* tokens */
