@@ -23,7 +23,7 @@ _lib: Optional[ctypes.CDLL] = None
 LILY_OK = 0
 STATUS_NAMES = {0: "LILY_OK", -1: "LILY_ERR_INVALID", -2: "LILY_ERR_UNSUPPORTED", -3: "LILY_ERR_MISALIGNED",
                 -4: "LILY_ERR_WORKSPACE", -5: "LILY_ERR_LAUNCH", -6: "LILY_ERR_DEVICE_TIMEOUT",
-                -7: "LILY_ERR_DEVICE_INDEX"}
+                -7: "LILY_ERR_DEVICE_INDEX", -8: "LILY_ERR_SCRATCH_LIMIT"}
 
 
 class LilyError(RuntimeError):
@@ -79,10 +79,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             L.lily_moe_forward_timed.argtypes = [PS, PW, P, P, PR, P, S, P, ctypes.POINTER(ctypes.c_void_p)]
             L.lily_moe_decode.argtypes = [PS, ctypes.c_int32, PW, P, P, P, ctypes.POINTER(lily_moe_decode_trace),
                                           P, S, P]
+            L.lily_moe_route_noalloc.argtypes = [PS, PW, P, PR, P, P]
             L.lily_moe_device_status.argtypes = [P, P]
             L.lily_moe_clear_status.argtypes = [P, P]
             for n in ("lily_moe_check_shape", "lily_moe_route", "lily_moe_grouped_gemm", "lily_moe_forward",
-                      "lily_moe_forward_timed", "lily_moe_decode", "lily_moe_device_status",
+                      "lily_moe_forward_timed", "lily_moe_decode", "lily_moe_device_status", "lily_moe_route_noalloc",
                       "lily_moe_clear_status"):
                 getattr(L, n).restype = I32
             _lib = L
@@ -237,3 +238,15 @@ def lily_moe_device_status(ws, stream=None) -> int:
 
 def lily_moe_clear_status(ws, stream=None) -> int:
     return _check("lily_moe_clear_status", load().lily_moe_clear_status(_ptr(ws), _stream(stream)))
+
+
+def lily_moe_route_noalloc(shape, weights, x, routing, device_status=None, stream=None, *, check: bool = True) -> int:
+    """Routing without a caller workspace: for callers that may not allocate
+    device memory when they run the layer (e.g. inside another engine's fixed
+    memory budget).  Scratch lives in a fixed device array owned by the
+    library (T <= 8192); calls that may overlap on the GPU race.  `routing`
+    must include logits; `device_status` (device int32 tensor) receives the
+    call's device status."""
+    rc = load().lily_moe_route_noalloc(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), ctypes.byref(routing),
+                                       _ptr(device_status), _stream(stream))
+    return _check("lily_moe_route_noalloc", rc) if check else rc

@@ -368,6 +368,32 @@ GraphCache &graph_cache()
 
 }  // namespace
 
+// Fixed scratch of lily_moe_route_noalloc.  Every GPU that loads the library
+// holds it until the process exits.  In host code `g_noalloc_scratch` is only a
+// host-side stand-in: its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LILY_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device (with that device current).  Returns nullptr if the lookup fails.
+void *noalloc_scratch_address()
+{
+    static std::mutex mu;
+    static std::unordered_map<int, void *> addr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = addr.find(dev);
+    if (it != addr.end()) return it->second;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    addr[dev] = p;
+    return p;
+}
+
+}  // namespace
+
 extern "C" {
 
 int lily_moe_version(void) { return kVersion; }
@@ -383,6 +409,7 @@ const char *lily_moe_status_string(int status)
     case LILY_ERR_LAUNCH: return "CUDA error while enqueueing";
     case LILY_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case LILY_ERR_DEVICE_INDEX: return "device index out of range";
+    case LILY_ERR_SCRATCH_LIMIT: return "token count above the fixed scratch of lily_moe_route_noalloc";
     default: return "unknown status";
     }
 }
@@ -559,6 +586,33 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
         it = gc.execs.emplace(key, exec).first;
     }
     return to_status(cudaGraphLaunch(it->second, stream));
+}
+
+int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,
+                           lily_moe_routing *r, int32_t *device_status, cudaStream_t stream)
+{
+    int rc;
+    if ((rc = check_shape(shape)) || (rc = check_weights(w)) || (rc = check_routing(r, true))) return rc;
+    if (shape->T > LILY_NOALLOC_MAX_TOKENS) return LILY_ERR_SCRATCH_LIMIT;
+    if ((rc = check_ptr(r->logits))) return rc;
+    if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u)) return LILY_ERR_MISALIGNED;
+    // The routing kernels touch only the control block and the two per-chunk
+    // tables of the prefill workspace layout, which fit in the fixed scratch.
+    const PrefillLayout L = prefill_layout(*shape);
+    if (L.chunk_base + static_cast<size_t>(ceil_div(shape->T, kRouteChunkTokens)) * shape->E * 4 >
+        LILY_NOALLOC_SCRATCH_BYTES)
+        return LILY_ERR_SCRATCH_LIMIT;
+    if (shape->T == 0) return LILY_OK;
+    if ((rc = check_ptr(x))) return rc;
+    void *scratch = noalloc_scratch_address();
+    if (!scratch) return LILY_ERR_LAUNCH;
+    // The scratch keeps the previous call's contents: start from a clear control block.
+    if (cudaMemsetAsync(scratch, 0, sizeof(Ctrl), stream) != cudaSuccess) return LILY_ERR_LAUNCH;
+    if (enqueue_route(*shape, *w, x, *r, r->logits, scratch, stream) != cudaSuccess) return LILY_ERR_LAUNCH;
+    if (device_status &&
+        cudaMemcpyAsync(device_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return LILY_ERR_LAUNCH;
+    return LILY_OK;
 }
 
 int lily_moe_device_status(const void *ws, cudaStream_t stream)

@@ -50,7 +50,8 @@ enum {
     LILY_ERR_WORKSPACE = -4,      /* workspace smaller than lily_moe_workspace_bytes() */
     LILY_ERR_LAUNCH = -5,         /* a CUDA call failed while enqueueing */
     LILY_ERR_DEVICE_TIMEOUT = -6, /* a kernel's bounded wait ran out (device-detected) */
-    LILY_ERR_DEVICE_INDEX = -7    /* a kernel saw an index out of range (device-detected) */
+    LILY_ERR_DEVICE_INDEX = -7,   /* a kernel saw an index out of range (device-detected) */
+    LILY_ERR_SCRATCH_LIMIT = -8   /* size above the fixed scratch of lily_moe_route_noalloc */
 };
 
 /*
@@ -227,6 +228,35 @@ int lily_moe_device_status(const void *ws, cudaStream_t stream);
 
 /* Enqueues a reset of the workspace's status word to LILY_OK. */
 int lily_moe_clear_status(void *ws, cudaStream_t stream);
+
+/*
+ * Routing without a caller workspace.  The paper has no counterpart: this entry
+ * point exists for callers that may not allocate device memory when they call
+ * the layer, e.g. a plugin that runs inside another engine's fixed memory
+ * budget, or a serving loop that forbids device allocation after start-up, and
+ * so cannot provide the workspace that lily_moe_route needs.
+ *
+ * It computes exactly what lily_moe_route computes (same kernels, same
+ * results), but keeps its scratch (per-chunk expert counts, their scanned
+ * write offsets, the last-block counter and the status word) in a fixed
+ * array that the library holds in device memory on every GPU that loads it,
+ * LILY_NOALLOC_SCRATCH_BYTES bytes, for the life of the process.
+ *   - T must be <= LILY_NOALLOC_MAX_TOKENS, else LILY_ERR_SCRATCH_LIMIT.
+ *   - r->logits must be non-NULL (the logits are an output here, not scratch).
+ *   - device_status: device int32 or NULL; if given, the call's device status
+ *     (LILY_OK or a LILY_ERR_DEVICE_* code) is copied there on `stream` at the
+ *     end.  The scratch status word is cleared at the start of every call.
+ *   - The first call on a device looks up the array's device address (no
+ *     allocation); make that first call outside any stream capture.
+ *   - Every call on a device shares the one array: calls that may overlap on
+ *     the GPU (other streams, other threads) race and must be serialised by the
+ *     caller.
+ * Allocates nothing: no cudaMalloc, no cudaFree, no library allocation.
+ */
+#define LILY_NOALLOC_MAX_TOKENS 8192
+#define LILY_NOALLOC_SCRATCH_BYTES (256 + 2 * 4 * 256 * (LILY_NOALLOC_MAX_TOKENS / 64))
+int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,
+                           lily_moe_routing *r, int32_t *device_status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }
