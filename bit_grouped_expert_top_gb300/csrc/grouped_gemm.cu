@@ -40,16 +40,18 @@ namespace lily {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kRStages = 4;   // raw int4 ring (TMA), consumed by the dequantisers
+constexpr int kRStages = 2;   // raw int4 ring (TMA), consumed by the dequantisers
+constexpr int kRK = 4;        // k-steps per raw stage (at most): 128 contiguous bytes of every row
 constexpr int kBStages = 4;   // B ring (tokens), consumed by the MMA issuer
-constexpr int kAStages = 3;   // A ring (fp16 dequantised weights, or bf16 router weights by TMA)
+constexpr int kAStages = 2;   // A ring (fp16 dequantised weights, or bf16 router weights by TMA)
 constexpr int kLag = 2;       // cp.async groups a gathering lane keeps in flight
 constexpr int kTileM = 128;
 constexpr int kBK = 64;       // one quantisation group, one 128-byte swizzle row
 constexpr int kTileN = 128;
 constexpr int kABytes = kTileM * kBK * 2;    // 16 KB of 16-bit elements
 constexpr int kBBytes = kTileN * kBK * 2;    // 16 KB of 16-bit elements
-constexpr int kRawBytes = kTileM * kBK / 2;  // 4 KB int4
+constexpr int kRawRow = kRK * kBK / 2;       // 128 B of packed int4 per row per raw stage
+constexpr int kRawBytes = kTileM * kRawRow;  // 16 KB int4 per matrix
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarDequant0 = 1, kBarEpilogue = 3, kBarBProducer = 4;  // named barrier ids
 
@@ -225,11 +227,13 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 const CUtensorMap *mA1 = u.shared ? &tmSA1 : &tmA1;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (dequant_mode) {
+                        // one raw stage = g.raw_k k-steps: g.raw_k * 32 contiguous bytes of each row
+                        if (kt % g.raw_k != 0) continue;
                         if (!mbar_wait(&S.empty_r[rs], rph ^ 1, abort_flag, status)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&S.full_r[rs], 2 * kRawBytes);
+                        mbar_arrive_expect_tx(&S.full_r[rs], 2 * kTileM * g.raw_k * (kBK / 2));
                         tma_load_2d(S.raw[rs][0], mA0, &S.full_r[rs], kt * (kBK / 2), r0);
                         tma_load_2d(S.raw[rs][1], mA1, &S.full_r[rs], kt * (kBK / 2), r1);
                         if (++rs == kRStages) {
@@ -249,7 +253,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                             aph ^= 1;
                         }
                     }
-                    ++issued;
+                    ++issued;  // raw stages (dequant modes) or A stages (router)
                 }
             }
             // Exit: no copy into this CTA's shared memory may still be in flight.
@@ -471,13 +475,25 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         s_nxt = load_groups8(srow, kt + 8, ngroups, vec8);
                         b_nxt = load_groups8(brow, kt + 8, ngroups, vec8);
                     }
-                    const bool got = ok && mbar_wait(&S.full_r[rs], rph, abort_flag, status) &&
-                                     mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status);
+                    const int jr = kt % g.raw_k;  // k-step within the raw stage
+                    bool got = ok;
+                    if (got && jr == 0) got = mbar_wait(&S.full_r[rs], rph, abort_flag, status);
+                    if (got) got = mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status);
                     if (!got) ok = false;
                     if (got) {
                         const uint16_t sc = pick16(s_cur, j), bi = pick16(b_cur, j);
-                        const uint4 *src = reinterpret_cast<const uint4 *>(S.raw[rs][mi] + r * (kBK / 2));
-                        const uint4 q0 = src[0], q1 = src[1];
+                        uint4 q0, q1;
+                        if (g.raw_k == kRK) {
+                            // 128-byte rows written by TMA with the 128-byte swizzle:
+                            // 16-byte chunk c of row r sits at chunk c ^ (r % 8)
+                            const uint8_t *rowp = S.raw[rs][mi] + r * kRawRow;
+                            q0 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr) ^ (r & 7)) << 4));
+                            q1 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr + 1) ^ (r & 7)) << 4));
+                        } else {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(S.raw[rs][mi] + r * (g.raw_k * kBK / 2) + jr * (kBK / 2));
+                            q0 = src[0];
+                            q1 = src[1];
+                        }
                         const __half2 s2 = half2_from_bf16_bits(sc), b2 = half2_from_bf16_bits(bi);
                         const __half2 s2_16 = __hmul2(s2, __floats2half2_rn(0.0625f, 0.0625f));
                         uint8_t *dst = S.a[as][mi] + (r >> 3) * 1024 + (r & 7) * 128;
@@ -491,9 +507,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     named_barrier_sync(kBarDequant0 + mi, 128);
                     if (r == 0 && ok) {
                         mbar_arrive(&S.full_a[as]);
-                        mbar_arrive(&S.empty_r[rs]);
+                        if (jr == g.raw_k - 1) mbar_arrive(&S.empty_r[rs]);
                     }
-                    if (++rs == kRStages) {
+                    if (jr == g.raw_k - 1 && ++rs == kRStages) {
                         rs = 0;
                         rph ^= 1;
                     }
