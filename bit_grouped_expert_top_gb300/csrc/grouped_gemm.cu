@@ -67,6 +67,8 @@ struct __align__(1024) Smem {
     uint32_t tmem_base;
     int abort_flag;
     int prod_tok[kTileN];  // B producers: source row of each B row of the current unit
+    int dq_go[2];          // dequant group's wait result, published by its waiting thread
+    int ep_go;             // epilogue's wait result, published by its waiting thread
     int ep_tok[kTileN];    // epilogue: token of each column (down)
     float ep_w[kTileN];    // epilogue: routing weight of each column (down)
 };
@@ -393,8 +395,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(ab * 2 * kTileM);
                 const uint32_t d1 = d0 + kTileM;
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(&S.full_a[as], aph, abort_flag, status) ||
-                        !mbar_wait(&S.full_b[bs], bph, abort_flag, status)) {
+                    if (!mbar_wait_spin(&S.full_a[as], aph, abort_flag, status) ||
+                        !mbar_wait_spin(&S.full_b[bs], bph, abort_flag, status)) {
                         ok = false;
                         break;
                     }
@@ -476,9 +478,17 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         b_nxt = load_groups8(brow, kt + 8, ngroups, vec8);
                     }
                     const int jr = kt % g.raw_k;  // k-step within the raw stage
-                    bool got = ok;
-                    if (got && jr == 0) got = mbar_wait(&S.full_r[rs], rph, abort_flag, status);
-                    if (got) got = mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status);
+                    // One thread per group polls the mbarriers (polling is shared-memory
+                    // traffic that would slow the tensor core's operand reads); the rest
+                    // wait at the group's hardware barrier.
+                    if (r == 0) {
+                        bool w = ok;
+                        if (w && jr == 0) w = mbar_wait_spin(&S.full_r[rs], rph, abort_flag, status);
+                        if (w) w = mbar_wait_spin(&S.empty_a[as], aph ^ 1, abort_flag, status);
+                        S.dq_go[mi] = w;
+                    }
+                    named_barrier_sync(kBarDequant0 + mi, 128);
+                    const bool got = S.dq_go[mi] != 0;
                     if (!got) ok = false;
                     if (got) {
                         const uint16_t sc = pick16(s_cur, j), bi = pick16(b_cur, j);
@@ -546,9 +556,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 S.ep_tok[et] = tok;
                 S.ep_w[et] = wt;
             }
-            named_barrier_sync(kBarEpilogue, 128);  // publishes ep_tok / ep_w
-            // warp-uniform decision: tcgen05.ld below is warp-collective
-            const bool got = __all_sync(0xffffffffu, ok && mbar_wait(&S.full_acc[ab], acc_ph, abort_flag, status));
+            // one thread waits for the accumulator; the group-wide result keeps the
+            // warp-collective tcgen05.ld below uniform
+            if (et == 0) S.ep_go = ok && mbar_wait(&S.full_acc[ab], acc_ph, abort_flag, status);
+            named_barrier_sync(kBarEpilogue, 128);  // also publishes ep_tok / ep_w
+            const bool got = S.ep_go != 0;
             if (!got) ok = false;
             if (got) {
             tc_fence_after();

@@ -119,6 +119,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Latency-critical wait: polls with the non-blocking test_wait so the thread
+// sees the phase flip at once; same bounds and abort handling as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status)
+{
+    const uint32_t addr = smem_u32(bar);
+#pragma unroll 1
+    for (int i = 0; i < 4096; ++i)
+        if (mbar_test_wait(addr, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+    while (true) {
+        if (mbar_test_wait(addr, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > LILY_WAIT_LIMIT_NS) {
+            record_error(status, kErrDeviceTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 {
