@@ -43,7 +43,8 @@ constexpr int kThreads = 512;
 constexpr int kRStages = 2;   // raw int4 ring (TMA), consumed by the dequantisers
 constexpr int kRK = 4;        // k-steps per raw stage (at most): 128 contiguous bytes of every row
 constexpr int kBStages = 4;   // B ring (tokens), consumed by the MMA issuer
-constexpr int kAStages = 2;   // A ring (fp16 dequantised weights, or bf16 router weights by TMA)
+constexpr int kAStages = 2;   // shared-memory A ring (bf16 router weights by TMA)
+constexpr int kTAStages = 4;  // tensor-memory A ring (fp16 dequantised weights, expert modes)
 constexpr int kLag = 2;       // cp.async groups a gathering lane keeps in flight
 constexpr int kTileM = 128;
 constexpr int kBK = 64;       // one quantisation group, one 128-byte swizzle row
@@ -53,6 +54,9 @@ constexpr int kBBytes = kTileN * kBK * 2;    // 16 KB of 16-bit elements
 constexpr int kRawRow = kRK * kBK / 2;       // 128 B of packed int4 per row per raw stage
 constexpr int kRawBytes = kTileM * kRawRow;  // 16 KB int4 per matrix
 constexpr uint32_t kTmemCols = 512;
+// TMEM columns: accumulators at [0, 256) per buffer (router: two buffers, [0, 512));
+// expert modes: one accumulator buffer and the A ring at [256, 512), 64 columns per stage.
+constexpr uint32_t kTmemAOffset = 256;
 constexpr int kBarDequant0 = 1, kBarEpilogue = 3, kBarBProducer = 4;  // named barrier ids
 
 struct __align__(1024) Smem {
@@ -61,7 +65,7 @@ struct __align__(1024) Smem {
     uint8_t raw[kRStages][2][kRawBytes];
     uint64_t full_r[kRStages], empty_r[kRStages];
     uint64_t full_b[kBStages], empty_b[kBStages];
-    uint64_t full_a[kAStages], empty_a[kAStages];
+    uint64_t full_a[kTAStages], empty_a[kTAStages];
     uint64_t full_acc[2], empty_acc[2];
     uint64_t drain;
     uint32_t tmem_base;
@@ -165,7 +169,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             mbar_init(&S.full_b[s], gather_b ? 64 : 1);
             mbar_init(&S.empty_b[s], 1);
         }
-        for (int s = 0; s < kAStages; ++s) {
+        for (int s = 0; s < kTAStages; ++s) {
             mbar_init(&S.full_a[s], dequant_mode ? 2 : 1);
             mbar_init(&S.empty_a[s], 1);
         }
@@ -386,6 +390,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             uint32_t bph = 0, aph = 0, acc_ph = 0;
             bool ok = true;
             const uint32_t fmt = dequant_mode ? kFmtF16 : kFmtBF16;
+            const int a_stages = dequant_mode ? kTAStages : kAStages;
+            const int n_acc = dequant_mode ? 1 : 2;  // accumulator buffers in TMEM
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 const Unit u = unit_info(g, tile, n_routed);
                 if (u.rows <= 0) continue;
@@ -401,18 +407,30 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(S.a[as][0]);
-                    const uint32_t a1 = smem_u32(S.a[as][1]);
                     const uint32_t bb = smem_u32(S.b[bs]);
+                    if (dequant_mode) {
+                        // A from tensor memory: 64 K elements of a stage = 32 columns per matrix
+                        const uint32_t at0 = tmem_base + kTmemAOffset + static_cast<uint32_t>(as * 64);
+                        const uint32_t at1 = at0 + 32;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint32_t acc = (kt | kk) != 0;
-                        umma_ss(d0, sdesc_sw128(a0 + kk * 32), sdesc_sw128(bb + kk * 32), idesc, acc);
-                        umma_ss(d1, sdesc_sw128(a1 + kk * 32), sdesc_sw128(bb + kk * 32), idesc, acc);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint32_t acc = (kt | kk) != 0;
+                            umma_ts(d0, at0 + kk * 8, sdesc_sw128(bb + kk * 32), idesc, acc);
+                            umma_ts(d1, at1 + kk * 8, sdesc_sw128(bb + kk * 32), idesc, acc);
+                        }
+                    } else {
+                        const uint32_t a0 = smem_u32(S.a[as][0]);
+                        const uint32_t a1 = smem_u32(S.a[as][1]);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint32_t acc = (kt | kk) != 0;
+                            umma_ss(d0, sdesc_sw128(a0 + kk * 32), sdesc_sw128(bb + kk * 32), idesc, acc);
+                            umma_ss(d1, sdesc_sw128(a1 + kk * 32), sdesc_sw128(bb + kk * 32), idesc, acc);
+                        }
                     }
                     umma_commit(&S.empty_a[as]);
                     umma_commit(&S.empty_b[bs]);
-                    if (++as == kAStages) {
+                    if (++as == a_stages) {
                         as = 0;
                         aph ^= 1;
                     }
@@ -423,7 +441,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 }
                 if (!ok) break;
                 umma_commit(&S.full_acc[ab]);
-                if (++ab == 2) {
+                if (++ab == n_acc) {
                     ab = 0;
                     acc_ph ^= 1;
                 }
@@ -490,6 +508,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     named_barrier_sync(kBarDequant0 + mi, 128);
                     const bool got = S.dq_go[mi] != 0;
                     if (!got) ok = false;
+                    tc_fence_after();  // the MMAs that read this TMEM stage are complete (empty_a)
                     if (got) {
                         const uint16_t sc = pick16(s_cur, j), bi = pick16(b_cur, j);
                         uint4 q0, q1;
@@ -506,13 +525,22 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         }
                         const __half2 s2 = half2_from_bf16_bits(sc), b2 = half2_from_bf16_bits(bi);
                         const __half2 s2_16 = __hmul2(s2, __floats2half2_rn(0.0625f, 0.0625f));
-                        uint8_t *dst = S.a[as][mi] + (r >> 3) * 1024 + (r & 7) * 128;
                         const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                        uint32_t cols[32];  // TMEM column 4c + j holds K positions 8c + 2j, 8c + 2j + 1
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) =
-                                dequant8_f16_kperm(words[c], s2, s2_16, b2);
-                        fence_proxy_async_smem();
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 o = dequant8_f16_kperm(words[c], s2, s2_16, b2);
+                            cols[4 * c + 0] = o.x;
+                            cols[4 * c + 1] = o.y;
+                            cols[4 * c + 2] = o.z;
+                            cols[4 * c + 3] = o.w;
+                        }
+                        // this warp's TMEM lane quarter holds rows [32 * (warp % 4), +32)
+                        const uint32_t ta = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kTmemAOffset +
+                                            static_cast<uint32_t>(as * 64 + mi * 32);
+                        tmem_st_32x32b_x32(ta, cols);
+                        tmem_st_wait();
+                        tc_fence_before();
                     }
                     named_barrier_sync(kBarDequant0 + mi, 128);
                     if (r == 0 && ok) {
@@ -523,7 +551,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         rs = 0;
                         rph ^= 1;
                     }
-                    if (++as == kAStages) {
+                    if (++as == kTAStages) {
                         as = 0;
                         aph ^= 1;
                     }
@@ -537,6 +565,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         int ab = 0;
         uint32_t acc_ph = 0;
         bool ok = true;
+        const int n_acc = dequant_mode ? 1 : 2;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             const Unit u = unit_info(g, tile, n_routed);
             if (u.rows <= 0) continue;
@@ -604,7 +633,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             if (lane == 0) mbar_arrive(&S.empty_acc[ab]);
             }
             named_barrier_sync(kBarEpilogue, 128);  // ep_tok / ep_w free for the next unit
-            if (++ab == 2) {
+            if (++ab == n_acc) {
                 ab = 0;
                 acc_ph ^= 1;
             }
