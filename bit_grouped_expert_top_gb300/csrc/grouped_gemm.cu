@@ -39,7 +39,7 @@
 namespace lily {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;  // 20 warps: 4 producer/MMA, 8 dequant, 8 epilogue
 constexpr int kRStages = 2;   // raw int4 ring (TMA), consumed by the dequantisers
 constexpr int kRK = 4;        // k-steps per raw stage (at most): 128 contiguous bytes of every row
 constexpr int kBStages = 4;   // B ring (tokens), consumed by the MMA issuer
@@ -175,7 +175,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&S.full_acc[s], 1);
-            mbar_init(&S.empty_acc[s], 4);
+            mbar_init(&S.empty_acc[s], 8);
         }
         mbar_init(&S.drain, 1);
         S.abort_flag = 0;
@@ -559,9 +559,13 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             }
         }
     } else if (warp >= 12) {
-        // ------------------------------------------------ epilogue
-        const int ew = warp & 3;         // TMEM lane quarter this warp may access
-        const int et = ew * 32 + lane;   // accumulator row (weight row within the tile)
+        // ------------------------------------------------ epilogue (8 warps)
+        // Two warps per TMEM lane quarter; they split the accumulator columns in
+        // 16-column chunks (even / odd chunks).
+        const int ew = warp & 3;             // TMEM lane quarter this warp may access
+        const int half = (warp - 12) >> 2;   // which chunks of columns
+        const int et = ew * 32 + lane;       // accumulator row (weight row within the tile)
+        const int eid = (warp - 12) * 32 + lane;  // 0..255
         int ab = 0;
         uint32_t acc_ph = 0;
         bool ok = true;
@@ -569,11 +573,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             const Unit u = unit_info(g, tile, n_routed);
             if (u.rows <= 0) continue;
-            if (g.mode == kModeDown && et < u.rows) {
-                int tok = u.p0 + et;
+            if (g.mode == kModeDown && eid < u.rows) {
+                int tok = u.p0 + eid;
                 float wt = 1.0f;
                 if (!u.shared) {
-                    const int a = g.perm[u.p0 + et];
+                    const int a = g.perm[u.p0 + eid];
                     tok = a / g.top_k;
                     wt = g.topk_w[a];
                 }
@@ -582,57 +586,83 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     tok = 0;
                     wt = 0.0f;
                 }
-                S.ep_tok[et] = tok;
-                S.ep_w[et] = wt;
+                S.ep_tok[eid] = tok;
+                S.ep_w[eid] = wt;
             }
             // one thread waits for the accumulator; the group-wide result keeps the
             // warp-collective tcgen05.ld below uniform
-            if (et == 0) S.ep_go = ok && mbar_wait(&S.full_acc[ab], acc_ph, abort_flag, status);
-            named_barrier_sync(kBarEpilogue, 128);  // also publishes ep_tok / ep_w
+            if (eid == 0) S.ep_go = ok && mbar_wait(&S.full_acc[ab], acc_ph, abort_flag, status);
+            named_barrier_sync(kBarEpilogue, 256);  // also publishes ep_tok / ep_w
             const bool got = S.ep_go != 0;
             if (!got) ok = false;
             if (got) {
-            tc_fence_after();
-            const uint32_t t0 = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(ab * 2 * kTileM);
-            const uint32_t t1 = t0 + kTileM;
-            float bias0 = 0.0f, bias1 = 0.0f;
-            if (g.mode == kModeRouter && g.router_bias) {
-                bias0 = g.router_bias[et];
-                bias1 = g.router_bias[kTileM + et];
-            }
-            // h columns are stored with K permuted inside each group of 8 (see dequant8_f16_kperm)
-            const int hcol = kperm8(u.mt * kTileM + et);
-            for (int c0 = 0; c0 < u.n_mma; c0 += 32) {
-                uint32_t v0[32], v1[32];
-                tmem_ld_32x32b_x32(t0 + c0, v0);
-                tmem_ld_32x32b_x32(t1 + c0, v1);
-                tmem_ld_wait();
+                tc_fence_after();
+                const uint32_t t0 = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(ab * 2 * kTileM);
+                const uint32_t t1 = t0 + kTileM;
+                if (g.mode == kModeGateUp) {
+                    // h columns in the K order of dequant8_f16_kperm (the down GEMM's A)
+                    const int hcol = kperm8(u.mt * kTileM + et);
+                    const size_t prow0 = u.shared ? static_cast<size_t>(g.T) * g.top_k + u.p0 : static_cast<size_t>(u.p0);
+                    __half *hbase = g.h + prow0 * g.I + hcol;
+                    for (int c0 = half * 16; c0 < u.n_mma; c0 += 32) {
+                        uint32_t v0[16], v1[16];
+                        tmem_ld_32x32b_x16(t0 + c0, v0);
+                        tmem_ld_32x32b_x16(t1 + c0, v1);
+                        tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int n = c0 + j;
-                    if (n < u.rows) {
-                        const float f0 = __uint_as_float(v0[j]), f1 = __uint_as_float(v1[j]);
-                        if (g.mode == kModeRouter) {
-                            float *lrow = g.logits + static_cast<size_t>(u.p0 + n) * g.E;
-                            lrow[et] = f0 + bias0;
-                            lrow[kTileM + et] = f1 + bias1;
-                        } else if (g.mode == kModeGateUp) {
-                            const size_t p = u.shared ? static_cast<size_t>(g.T) * g.top_k + u.p0 + n : static_cast<size_t>(u.p0 + n);
-                            g.h[p * g.I + hcol] = __float2half_rn(silu_f(f0) * f1);
-                        } else {
-                            float *orow = g.out + static_cast<size_t>(S.ep_tok[n]) * g.d + u.mt * 2 * kTileM;
-                            const float wt = S.ep_w[n];
-                            atomicAdd(orow + et, wt * f0);
-                            atomicAdd(orow + kTileM + et, wt * f1);
+                        for (int j = 0; j < 16; ++j) {
+                            const int n = c0 + j;
+                            if (n < u.rows)
+                                hbase[static_cast<size_t>(n) * g.I] =
+                                    __float2half_rn(silu_f(__uint_as_float(v0[j])) * __uint_as_float(v1[j]));
+                        }
+                    }
+                } else if (g.mode == kModeDown) {
+                    float *obase = g.out + u.mt * 2 * kTileM + et;
+                    for (int c0 = half * 16; c0 < u.n_mma; c0 += 32) {
+                        uint32_t v0[16], v1[16];
+                        tmem_ld_32x32b_x16(t0 + c0, v0);
+                        tmem_ld_32x32b_x16(t1 + c0, v1);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int n = c0 + j;
+                            if (n < u.rows) {
+                                float *orow = obase + static_cast<size_t>(S.ep_tok[n]) * g.d;
+                                const float wt = S.ep_w[n];
+                                atomicAdd(orow, wt * __uint_as_float(v0[j]));
+                                atomicAdd(orow + kTileM, wt * __uint_as_float(v1[j]));
+                            }
+                        }
+                    }
+                } else {
+                    float bias0 = 0.0f, bias1 = 0.0f;
+                    if (g.router_bias) {
+                        bias0 = g.router_bias[et];
+                        bias1 = g.router_bias[kTileM + et];
+                    }
+                    float *lbase = g.logits + static_cast<size_t>(u.p0) * g.E + et;
+                    for (int c0 = half * 16; c0 < u.n_mma; c0 += 32) {
+                        uint32_t v0[16], v1[16];
+                        tmem_ld_32x32b_x16(t0 + c0, v0);
+                        tmem_ld_32x32b_x16(t1 + c0, v1);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int n = c0 + j;
+                            if (n < u.rows) {
+                                float *lrow = lbase + static_cast<size_t>(n) * g.E;
+                                lrow[0] = __uint_as_float(v0[j]) + bias0;
+                                lrow[kTileM] = __uint_as_float(v1[j]) + bias1;
+                            }
                         }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty_acc[ab]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.empty_acc[ab]);
-            }
-            named_barrier_sync(kBarEpilogue, 128);  // ep_tok / ep_w free for the next unit
+            named_barrier_sync(kBarEpilogue, 256);  // ep_tok / ep_w free for the next unit
             if (++ab == n_acc) {
                 ab = 0;
                 acc_ph ^= 1;
