@@ -42,10 +42,11 @@ namespace {
 constexpr int kThreads = 640;  // 20 warps: 4 producer/MMA, 8 dequant, 8 epilogue
 constexpr int kRStages = 2;   // raw int4 ring (TMA), consumed by the dequantisers
 constexpr int kRK = 4;        // k-steps per raw stage (at most): 128 contiguous bytes of every row
-constexpr int kBStages = 4;   // B ring (tokens), consumed by the MMA issuer
+constexpr int kBStages = 4;   // B ring in the dedicated buffers (router)
+constexpr int kBStagesMax = 8; // expert modes add 4 stages in the shared-memory A buffers they do not use
 constexpr int kAStages = 2;   // shared-memory A ring (bf16 router weights by TMA)
 constexpr int kTAStages = 4;  // tensor-memory A ring (fp16 dequantised weights, expert modes)
-constexpr int kLag = 2;       // cp.async groups a gathering lane keeps in flight
+constexpr int kLag = 4;       // cp.async groups a gathering lane keeps in flight (< B stages)
 constexpr int kTileM = 128;
 constexpr int kBK = 64;       // one quantisation group, one 128-byte swizzle row
 constexpr int kTileN = 128;
@@ -64,7 +65,7 @@ struct __align__(1024) Smem {
     uint8_t b[kBStages][kBBytes];
     uint8_t raw[kRStages][2][kRawBytes];
     uint64_t full_r[kRStages], empty_r[kRStages];
-    uint64_t full_b[kBStages], empty_b[kBStages];
+    uint64_t full_b[kBStagesMax], empty_b[kBStagesMax];
     uint64_t full_a[kTAStages], empty_a[kTAStages];
     uint64_t full_acc[2], empty_acc[2];
     uint64_t drain;
@@ -77,6 +78,7 @@ struct __align__(1024) Smem {
     float ep_w[kTileN];    // epilogue: routing weight of each column (down)
 };
 static_assert(sizeof(Smem) + 1024 <= 200 * 1024, "shared memory budget of one CTA");
+static_assert(sizeof(Smem::a) >= (kBStagesMax - kBStages) * kBBytes, "extra B stages fit in the A buffers");
 
 struct Unit {
     int e, p0, rows, n_mma, mt;
@@ -107,6 +109,13 @@ __device__ __forceinline__ Unit unit_info(const GemmArgs &g, int tile, int n_rou
     }
     u.n_mma = (u.rows + 15) & ~15;
     return u;
+}
+
+// B stage buffer i: stages 0..3 in the dedicated buffers, 4..7 (expert modes)
+// in the shared-memory A buffers, which only the router uses.
+__device__ __forceinline__ uint8_t *b_stage(Smem &S, int i)
+{
+    return i < kBStages ? S.b[i] : &S.a[0][0][0] + (i - kBStages) * kBBytes;
 }
 
 // First weight row of the two 128-row A tiles of a unit.
@@ -165,7 +174,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             mbar_init(&S.full_r[s], 1);
             mbar_init(&S.empty_r[s], 2);
         }
-        for (int s = 0; s < kBStages; ++s) {
+        for (int s = 0; s < kBStagesMax; ++s) {
             mbar_init(&S.full_b[s], gather_b ? 64 : 1);
             mbar_init(&S.empty_b[s], 1);
         }
@@ -272,12 +281,13 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     } else if (warp == 2 || warp == 3) {
         // ------------------------------------------------ B producers (token rows)
         const int bl = (warp - 2) * 32 + lane;  // 0..63
+        const int b_stages = dequant_mode ? kBStagesMax : kBStages;
         if (gather_b) {
             // two warps gather token rows of fp16 x with 16-byte cp.async into the
             // 128-byte-swizzled layout; each lane signals a stage once its copies landed
             int bs = 0;
             uint32_t bph = 0;
-            int p_old = 0, p_new = 0, n_pend = 0;  // stages awaiting their cp.async group
+            int gi = 0;  // stages issued; stage gi - kLag is signalled once its copies landed
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
                 const Unit u = unit_info(g, tile, n_routed);
@@ -316,26 +326,19 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     if (good) {
                         const int c = bl & 7;
                         const __half *xk = g.xh + kt * kBK + c * 8;
-                        uint8_t *bst = S.b[bs];
+                        uint8_t *bst = b_stage(S, bs);
                         for (int r = bl >> 3; r < u.n_mma; r += 8)
                             cp_async_16(bst + r * 128 + ((c ^ (r & 7)) << 4),
                                         xk + static_cast<size_t>(S.prod_tok[r]) * g.d);
                         cp_async_commit();
-                        if (n_pend == kLag) {
-                            cp_async_wait_group<kLag>();
+                        ++gi;
+                        if (gi > kLag) {
+                            cp_async_wait_group<kLag>();  // the copies of stage gi - 1 - kLag landed
                             fence_proxy_async_smem();
-                            mbar_arrive(&S.full_b[p_old]);
-                            p_old = p_new;
-                            p_new = bs;
-                        } else if (n_pend == 1) {
-                            p_new = bs;
-                            n_pend = 2;
-                        } else {
-                            p_old = bs;
-                            n_pend = 1;
+                            mbar_arrive(&S.full_b[(gi - 1 - kLag) % b_stages]);
                         }
                     }
-                    if (++bs == kBStages) {
+                    if (++bs == b_stages) {
                         bs = 0;
                         bph ^= 1;
                     }
@@ -343,8 +346,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             }
             cp_async_wait_all();
             fence_proxy_async_smem();
-            if (n_pend >= 1) mbar_arrive(&S.full_b[p_old]);
-            if (n_pend == 2) mbar_arrive(&S.full_b[p_new]);
+            for (int i = gi - (gi < kLag ? gi : kLag); i < gi; ++i) mbar_arrive(&S.full_b[i % b_stages]);
         } else if (bl == 0) {
             // contiguous rows (x for the router, h for the down projection): one 2-D TMA per stage
             int bs = 0;
@@ -372,15 +374,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         break;
                     }
                     mbar_arrive_expect_tx(&S.full_b[bs], kBBytes);
-                    tma_load_2d(S.b[bs], &tmB, &S.full_b[bs], kt * kBK, b_row0);
+                    tma_load_2d(b_stage(S, bs), &tmB, &S.full_b[bs], kt * kBK, b_row0);
                     ++issued;
-                    if (++bs == kBStages) {
+                    if (++bs == b_stages) {
                         bs = 0;
                         bph ^= 1;
                     }
                 }
             }
-            drain_ring(S.full_b, kBStages, issued, status);
+            drain_ring(S.full_b, b_stages, issued, status);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -392,6 +394,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             const uint32_t fmt = dequant_mode ? kFmtF16 : kFmtBF16;
             const int a_stages = dequant_mode ? kTAStages : kAStages;
             const int n_acc = dequant_mode ? 1 : 2;  // accumulator buffers in TMEM
+            const int b_stages = dequant_mode ? kBStagesMax : kBStages;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 const Unit u = unit_info(g, tile, n_routed);
                 if (u.rows <= 0) continue;
@@ -407,7 +410,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t bb = smem_u32(S.b[bs]);
+                    const uint32_t bb = smem_u32(b_stage(S, bs));
                     if (dequant_mode) {
                         // A from tensor memory: 64 K elements of a stage = 32 columns per matrix
                         const uint32_t at0 = tmem_base + kTmemAOffset + static_cast<uint32_t>(as * 64);
@@ -434,7 +437,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         as = 0;
                         aph ^= 1;
                     }
-                    if (++bs == kBStages) {
+                    if (++bs == b_stages) {
                         bs = 0;
                         bph ^= 1;
                     }
