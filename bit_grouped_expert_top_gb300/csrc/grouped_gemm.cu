@@ -85,12 +85,13 @@ struct Unit {
     bool shared;
 };
 
+template <int MODE>
 __device__ __forceinline__ Unit unit_info(const GemmArgs &g, int tile, int n_routed)
 {
     Unit u;
     const int b = tile / g.m_tiles;
     u.mt = tile - b * g.m_tiles;
-    if (g.mode != kModeRouter && b < n_routed) {
+    if (MODE != kModeRouter && b < n_routed) {
         const int *bm = g.block_map + 3 * b;
         u.e = bm[0];
         u.p0 = bm[1];
@@ -101,7 +102,7 @@ __device__ __forceinline__ Unit unit_info(const GemmArgs &g, int tile, int n_rou
             u.rows = 0;
         }
     } else {
-        const int sb = (g.mode == kModeRouter) ? b : b - n_routed;
+        const int sb = (MODE == kModeRouter) ? b : b - n_routed;
         u.e = -1;
         u.p0 = sb * g.bm;
         u.rows = min(g.bm, g.T - u.p0);
@@ -119,12 +120,13 @@ __device__ __forceinline__ uint8_t *b_stage(Smem &S, int i)
 }
 
 // First weight row of the two 128-row A tiles of a unit.
+template <int MODE>
 __device__ __forceinline__ void a_rows(const GemmArgs &g, const Unit &u, int &r0, int &r1)
 {
-    if (g.mode == kModeRouter) {
+    if (MODE == kModeRouter) {
         r0 = 0;
         r1 = kTileM;
-    } else if (g.mode == kModeGateUp) {
+    } else if (MODE == kModeGateUp) {
         r0 = (u.shared ? 0 : u.e * g.I) + u.mt * kTileM;
         r1 = r0;
     } else {
@@ -156,6 +158,7 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, int depth, int issued
     }
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -166,8 +169,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     int *status = &g.ctrl->status;
-    const bool dequant_mode = g.mode != kModeRouter;
-    const bool gather_b = g.mode == kModeGateUp;
+    constexpr bool dequant_mode = MODE != kModeRouter;
+    constexpr bool gather_b = MODE == kModeGateUp;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRStages; ++s) {
@@ -189,7 +192,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         mbar_init(&S.drain, 1);
         S.abort_flag = 0;
         fence_mbar_init();
-        if (g.mode == kModeRouter && blockIdx.x == 0) g.ctrl->ticket = 0u;  // reset for the routing kernel
+        if (MODE == kModeRouter && blockIdx.x == 0) g.ctrl->ticket = 0u;  // reset for the routing kernel
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA0);
@@ -211,7 +214,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     volatile int *abort_flag = &S.abort_flag;
 
     int n_routed = 0;
-    if (g.mode != kModeRouter) {
+    if (MODE != kModeRouter) {
         n_routed = *g.n_blocks;
         if (n_routed < 0 || n_routed > g.n_routed_max) {
             if (threadIdx.x == 0) record_error(status, kErrDeviceIndex);
@@ -234,10 +237,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             int issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const Unit u = unit_info(g, tile, n_routed);
+                const Unit u = unit_info<MODE>(g, tile, n_routed);
                 if (u.rows <= 0) continue;
                 int r0, r1;
-                a_rows(g, u, r0, r1);
+                a_rows<MODE>(g, u, r0, r1);
                 const CUtensorMap *mA0 = u.shared ? &tmSA0 : &tmA0;
                 const CUtensorMap *mA1 = u.shared ? &tmSA1 : &tmA1;
                 for (int kt = 0; kt < KT; ++kt) {
@@ -290,7 +293,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             int gi = 0;  // stages issued; stage gi - kLag is signalled once its copies landed
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-                const Unit u = unit_info(g, tile, n_routed);
+                const Unit u = unit_info<MODE>(g, tile, n_routed);
                 if (u.rows <= 0) continue;
                 named_barrier_sync(kBarBProducer, 64);  // previous unit's rows no longer read
                 for (int r = bl; r < u.n_mma; r += 64) {
@@ -308,7 +311,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     // warm L2 with the token rows of this CTA's next unit
                     const int nt = tile + gridDim.x;
                     if (nt < total_tiles) {
-                        const Unit un = unit_info(g, nt, n_routed);
+                        const Unit un = unit_info<MODE>(g, nt, n_routed);
                         for (int r = bl; r < un.rows; r += 64) {
                             int src = un.shared ? un.p0 + r : g.perm[un.p0 + r] / g.top_k;
                             if (src >= 0 && src < g.T)
@@ -354,14 +357,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             int issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const Unit u = unit_info(g, tile, n_routed);
+                const Unit u = unit_info<MODE>(g, tile, n_routed);
                 if (u.rows <= 0) continue;
-                const int b_row0 = (g.mode == kModeDown && u.shared) ? g.T * g.top_k + u.p0 : u.p0;
-                if (g.mode == kModeDown) {
+                const int b_row0 = (MODE == kModeDown && u.shared) ? g.T * g.top_k + u.p0 : u.p0;
+                if (MODE == kModeDown) {
                     // warm L2 with the h rows of this CTA's next unit (contiguous rows)
                     const int nt = tile + gridDim.x;
                     if (nt < total_tiles) {
-                        const Unit un = unit_info(g, nt, n_routed);
+                        const Unit un = unit_info<MODE>(g, nt, n_routed);
                         if (un.rows > 0) {
                             const size_t row0 = un.shared ? static_cast<size_t>(g.T) * g.top_k + un.p0 : un.p0;
                             bulk_prefetch_l2(g.h + row0 * g.I, static_cast<uint32_t>(un.rows) * g.I * 2u);
@@ -396,7 +399,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             const int n_acc = dequant_mode ? 1 : 2;  // accumulator buffers in TMEM
             const int b_stages = dequant_mode ? kBStagesMax : kBStages;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const Unit u = unit_info(g, tile, n_routed);
+                const Unit u = unit_info<MODE>(g, tile, n_routed);
                 if (u.rows <= 0) continue;
                 if (!mbar_wait(&S.empty_acc[ab], acc_ph ^ 1, abort_flag, status)) break;
                 tc_fence_after();
@@ -404,8 +407,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(ab * 2 * kTileM);
                 const uint32_t d1 = d0 + kTileM;
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait_spin(&S.full_a[as], aph, abort_flag, status) ||
-                        !mbar_wait_spin(&S.full_b[bs], bph, abort_flag, status)) {
+                    if (!mbar_wait(&S.full_a[as], aph, abort_flag, status) ||
+                        !mbar_wait(&S.full_b[bs], bph, abort_flag, status)) {
                         ok = false;
                         break;
                     }
@@ -465,10 +468,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             uint32_t rph = 0, aph = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-                const Unit u = unit_info(g, tile, n_routed);
+                const Unit u = unit_info<MODE>(g, tile, n_routed);
                 if (u.rows <= 0) continue;
                 int r0, r1;
-                a_rows(g, u, r0, r1);
+                a_rows<MODE>(g, u, r0, r1);
                 const int row = (mi ? r1 : r0) + r;
                 const uint16_t *srow = (u.shared ? (mi ? g.ss1 : g.ss0) : (mi ? g.s1 : g.s0)) + static_cast<size_t>(row) * ngroups;
                 const uint16_t *brow = (u.shared ? (mi ? g.sb1 : g.sb0) : (mi ? g.b1 : g.b0)) + static_cast<size_t>(row) * ngroups;
@@ -476,10 +479,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     // warm L2 with the next unit's scale / bias rows of this thread
                     const int nt = tile + gridDim.x;
                     if (nt < total_tiles) {
-                        const Unit un = unit_info(g, nt, n_routed);
+                        const Unit un = unit_info<MODE>(g, nt, n_routed);
                         if (un.rows > 0) {
                             int n0, n1;
-                            a_rows(g, un, n0, n1);
+                            a_rows<MODE>(g, un, n0, n1);
                             const size_t nrow = static_cast<size_t>((mi ? n1 : n0) + r) * ngroups;
                             prefetch_l2((un.shared ? (mi ? g.ss1 : g.ss0) : (mi ? g.s1 : g.s0)) + nrow);
                             prefetch_l2((un.shared ? (mi ? g.sb1 : g.sb0) : (mi ? g.b1 : g.b0)) + nrow);
@@ -504,8 +507,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     // wait at the group's hardware barrier.
                     if (r == 0) {
                         bool w = ok;
-                        if (w && jr == 0) w = mbar_wait_spin(&S.full_r[rs], rph, abort_flag, status);
-                        if (w) w = mbar_wait_spin(&S.empty_a[as], aph ^ 1, abort_flag, status);
+                        if (w && jr == 0) w = mbar_wait(&S.full_r[rs], rph, abort_flag, status);
+                        if (w) w = mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status);
                         S.dq_go[mi] = w;
                     }
                     named_barrier_sync(kBarDequant0 + mi, 128);
@@ -574,9 +577,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         bool ok = true;
         const int n_acc = dequant_mode ? 1 : 2;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const Unit u = unit_info(g, tile, n_routed);
+            const Unit u = unit_info<MODE>(g, tile, n_routed);
             if (u.rows <= 0) continue;
-            if (g.mode == kModeDown && eid < u.rows) {
+            if (MODE == kModeDown && eid < u.rows) {
                 int tok = u.p0 + eid;
                 float wt = 1.0f;
                 if (!u.shared) {
@@ -602,7 +605,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 tc_fence_after();
                 const uint32_t t0 = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(ab * 2 * kTileM);
                 const uint32_t t1 = t0 + kTileM;
-                if (g.mode == kModeGateUp) {
+                if (MODE == kModeGateUp) {
                     // h columns in the K order of dequant8_f16_kperm (the down GEMM's A)
                     const int hcol = kperm8(u.mt * kTileM + et);
                     const size_t prow0 = u.shared ? static_cast<size_t>(g.T) * g.top_k + u.p0 : static_cast<size_t>(u.p0);
@@ -620,7 +623,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                                     __float2half_rn(silu_f(__uint_as_float(v0[j])) * __uint_as_float(v1[j]));
                         }
                     }
-                } else if (g.mode == kModeDown) {
+                } else if (MODE == kModeDown) {
                     float *obase = g.out + u.mt * 2 * kTileM + et;
                     for (int c0 = half * 16; c0 < u.n_mma; c0 += 32) {
                         uint32_t v0[16], v1[16];
@@ -725,20 +728,32 @@ cudaError_t launch_prep_experts(const uint16_t *x, __half *xh, float *out, int64
 
 size_t grouped_gemm_smem_bytes() { return sizeof(Smem) + 1024; }
 
-cudaError_t launch_grouped_gemm(const GemmArgs &g, const CUtensorMap &tmB, const CUtensorMap &tmA0,
-                                const CUtensorMap &tmA1, const CUtensorMap &tmSA0, const CUtensorMap &tmSA1,
-                                int grid, cudaStream_t stream)
+template <int MODE>
+static cudaError_t launch_mode(const GemmArgs &g, const CUtensorMap &tmB, const CUtensorMap &tmA0, const CUtensorMap &tmA1,
+                               const CUtensorMap &tmSA0, const CUtensorMap &tmSA1, int grid, cudaStream_t stream)
 {
     static bool configured = false;
     const size_t smem = grouped_gemm_smem_bytes();
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    grouped_gemm_kernel<<<grid, kThreads, smem, stream>>>(g, tmB, tmA0, tmA1, tmSA0, tmSA1);
+    grouped_gemm_kernel<MODE><<<grid, kThreads, smem, stream>>>(g, tmB, tmA0, tmA1, tmSA0, tmSA1);
     return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(const GemmArgs &g, const CUtensorMap &tmB, const CUtensorMap &tmA0,
+                                const CUtensorMap &tmA1, const CUtensorMap &tmSA0, const CUtensorMap &tmSA1,
+                                int grid, cudaStream_t stream)
+{
+    switch (g.mode) {
+    case kModeRouter: return launch_mode<kModeRouter>(g, tmB, tmA0, tmA1, tmSA0, tmSA1, grid, stream);
+    case kModeGateUp: return launch_mode<kModeGateUp>(g, tmB, tmA0, tmA1, tmSA0, tmSA1, grid, stream);
+    case kModeDown: return launch_mode<kModeDown>(g, tmB, tmA0, tmA1, tmSA0, tmSA1, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace lily
