@@ -214,20 +214,19 @@ bool tmap_f16_sw128(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t ro
     return make_tmap(m, ptr, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, inner, rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// k-steps of 64 weights per raw int4 TMA stage of the grouped GEMM for reduction length K.
-int raw_k_steps(int64_t K)
+// k-steps of 64 of the grouped GEMM for reduction length K: K / 64 rounded up
+// to whole blocks of four (the kernel reads zeros past K).
+int gemm_k_steps(int64_t K)
 {
-    const int64_t kt = K / 64;
-    return kt % 4 == 0 ? 4 : (kt % 2 == 0 ? 2 : 1);
+    return static_cast<int>(((K / 64) + 3) / 4 * 4);
 }
 
-// Packed int4 rows: a box of raw_k * 32 bytes x 128 rows; 4-step boxes (128-byte
-// rows) use the 128-byte swizzle so the dequantisers read them without bank conflicts.
+// Packed int4 rows: a box of 128 bytes (four k-steps of 64 weights) x 128 rows
+// with the 128-byte swizzle, so the dequantisers read it without bank
+// conflicts; boxes past the end of a row read zeros.
 bool tmap_q4(CUtensorMap *m, const uint8_t *q, uint64_t K, uint64_t rows)
 {
-    const int rk = raw_k_steps(static_cast<int64_t>(K));
-    return make_tmap(m, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, rows, static_cast<uint32_t>(rk * 32), 128,
-                     rk == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+    return make_tmap(m, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, rows, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
@@ -246,7 +245,7 @@ cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, co
 
     GemmArgs g{};
     g.mode = kModeRouter;
-    g.raw_k = 1;
+    g.KT = gemm_k_steps(s.d);
     g.T = s.T; g.d = s.d; g.E = s.E; g.top_k = s.top_k; g.I = s.I;
     g.bm = 128;
     g.K = s.d;
@@ -315,7 +314,7 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
     // gate/up + SwiGLU
     g.mode = kModeGateUp;
     g.K = s.d;
-    g.raw_k = raw_k_steps(s.d);
+    g.KT = gemm_k_steps(s.d);
     g.m_tiles = s.I / 128;
     g.s0 = w.gate.scale; g.b0 = w.gate.bias; g.s1 = w.up.scale; g.b1 = w.up.bias;
     g.ss0 = w.sh_gate.scale; g.sb0 = w.sh_gate.bias; g.ss1 = w.sh_up.scale; g.sb1 = w.sh_up.bias;
@@ -327,7 +326,7 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
     // down + weighted combine
     g.mode = kModeDown;
     g.K = s.I;
-    g.raw_k = raw_k_steps(s.I);
+    g.KT = gemm_k_steps(s.I);
     g.m_tiles = s.d / 256;
     g.s0 = g.s1 = w.down.scale; g.b0 = g.b1 = w.down.bias;
     g.ss0 = g.ss1 = w.sh_down.scale; g.sb0 = g.sb1 = w.sh_down.bias;

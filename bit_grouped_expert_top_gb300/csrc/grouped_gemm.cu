@@ -15,22 +15,28 @@
 // and the tokens of one block-map entry take the N side (N = rows rounded up
 // to 16, at most 128), so small expert groups waste little tensor work.
 // One CTA per SM loops over work units:
-//   warp 0        producer: TMA of the packed int4 tile (and of bf16 A for the
-//                 router), TMA of contiguous B rows, or cp.async gathers of
-//                 token rows of x by the routing permutation (gate/up);
+//   warp 0        A-side producer: TMA of the packed int4 tiles (expert modes)
+//                 or of the bf16 router weights;
+//   warps 2-3     B producer: one TMA per k-step for contiguous rows (router x,
+//                 down h), or cp.async gathers of token rows of x by the
+//                 routing permutation (gate/up);
 //   warp 1        TMEM allocator + single-thread tcgen05.mma issuer;
-//   warps 4..11   dequantisers: int4 -> fp16 (one matrix per warpgroup, one
-//                 row per thread) written in the 128-byte swizzled K-major
-//                 layout the tensor core reads;
-//   warps 12..15  epilogue: tcgen05.ld from TMEM, then per mode the router
+//   warps 4..11   dequantisers (expert modes): int4 -> fp16, one matrix per
+//                 warpgroup, one row per thread, written to tensor memory with
+//                 tcgen05.st; the MMA reads A from tensor memory (TS form);
+//   warps 12..19  epilogue: tcgen05.ld from TMEM, then per mode the router
 //                 logits (+bias), SwiGLU into h (fp16), or the down projection
 //                 scaled by the routing weight and added (red.global.add.f32)
 //                 into token order.
-// Accumulators are double-buffered in TMEM (2 x 2 x 128 fp32 columns), so the
-// epilogue of one unit overlaps the main loop of the next.
+// The K loop runs in blocks of four 64-wide k-steps (one raw int4 stage, one
+// pass over the 4-stage tensor-memory A ring), so every ring slot and phase
+// parity inside a block is a compile-time constant and the single-thread roles
+// spend few instructions per k-step.  K is padded up to a multiple of 256: the
+// copies read zeros past the end of K and the padded weights rebuild to zero.
 // Every wait is bounded; on timeout the kernel records the error, drains its
 // in-flight copies and tensor-core work, frees TMEM and returns.
 #include <algorithm>
+#include <cstddef>
 #include <cstdio>
 
 #include "lily_device.cuh"
@@ -40,32 +46,35 @@ namespace lily {
 namespace {
 
 constexpr int kThreads = 640;  // 20 warps: 4 producer/MMA, 8 dequant, 8 epilogue
-constexpr int kRStages = 2;   // raw int4 ring (TMA), consumed by the dequantisers
-constexpr int kRK = 4;        // k-steps per raw stage (at most): 128 contiguous bytes of every row
-constexpr int kBStages = 4;   // B ring in the dedicated buffers (router)
-constexpr int kBStagesMax = 8; // expert modes add 4 stages in the shared-memory A buffers they do not use
-constexpr int kAStages = 2;   // shared-memory A ring (bf16 router weights by TMA)
-constexpr int kTAStages = 4;  // tensor-memory A ring (fp16 dequantised weights, expert modes)
-constexpr int kLag = 4;       // cp.async groups a gathering lane keeps in flight (< B stages)
+constexpr int kBlk = 4;        // k-steps per block: one raw stage, one tensor-memory A ring cycle
+constexpr int kRStages = 2;    // raw int4 ring (TMA), one block per stage
+constexpr int kBStages = 4;    // B ring in the dedicated buffers (router)
+constexpr int kBStagesX = 8;   // expert modes: 4 more B stages in the shared-memory A buffers they do not use
+constexpr int kAStages = 2;    // shared-memory A ring (bf16 router weights by TMA)
+constexpr int kTAStages = 4;   // tensor-memory A ring (fp16 dequantised weights, expert modes) = kBlk
+constexpr int kLag = 4;        // cp.async groups a gathering lane keeps in flight (< B stages)
 constexpr int kTileM = 128;
-constexpr int kBK = 64;       // one quantisation group, one 128-byte swizzle row
+constexpr int kBK = 64;        // one quantisation group, one 128-byte swizzle row
 constexpr int kTileN = 128;
 constexpr int kABytes = kTileM * kBK * 2;    // 16 KB of 16-bit elements
 constexpr int kBBytes = kTileN * kBK * 2;    // 16 KB of 16-bit elements
-constexpr int kRawRow = kRK * kBK / 2;       // 128 B of packed int4 per row per raw stage
+constexpr int kRawRow = kBlk * kBK / 2;      // 128 B of packed int4 per row per raw stage
 constexpr int kRawBytes = kTileM * kRawRow;  // 16 KB int4 per matrix
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: accumulators at [0, 256) per buffer (router: two buffers, [0, 512));
 // expert modes: one accumulator buffer and the A ring at [256, 512), 64 columns per stage.
 constexpr uint32_t kTmemAOffset = 256;
 constexpr int kBarDequant0 = 1, kBarEpilogue = 3, kBarBProducer = 4;  // named barrier ids
+static_assert(kTAStages == kBlk, "one tensor-memory A stage per k-step of a block");
+static_assert(kBStagesX == 2 * kBlk && kBStages == kBlk && kAStages == 2, "ring slots are compile-time within a block");
+static_assert(kLag == kBlk, "a gathered stage is signalled one block after it was issued");
 
 struct __align__(1024) Smem {
-    uint8_t a[kAStages][2][kABytes];
-    uint8_t b[kBStages][kBBytes];
+    uint8_t b[kBStages][kBBytes];         // B ring; expert modes continue into `a`
+    uint8_t a[kAStages][2][kABytes];      // router: bf16 A ring; expert modes: B stages 4..7
     uint8_t raw[kRStages][2][kRawBytes];
     uint64_t full_r[kRStages], empty_r[kRStages];
-    uint64_t full_b[kBStagesMax], empty_b[kBStagesMax];
+    uint64_t full_b[kBStagesX], empty_b[kBStagesX];
     uint64_t full_a[kTAStages], empty_a[kTAStages];
     uint64_t full_acc[2], empty_acc[2];
     uint64_t drain;
@@ -78,7 +87,9 @@ struct __align__(1024) Smem {
     float ep_w[kTileN];    // epilogue: routing weight of each column (down)
 };
 static_assert(sizeof(Smem) + 1024 <= 200 * 1024, "shared memory budget of one CTA");
-static_assert(sizeof(Smem::a) >= (kBStagesMax - kBStages) * kBBytes, "extra B stages fit in the A buffers");
+static_assert(offsetof(Smem, a) == offsetof(Smem, b) + sizeof(Smem::b) &&
+                  sizeof(Smem::a) == (kBStagesX - kBStages) * kBBytes,
+              "expert-mode B stages 4..7 continue the B ring in the A buffers");
 
 struct Unit {
     int e, p0, rows, n_mma, mt;
@@ -112,13 +123,6 @@ __device__ __forceinline__ Unit unit_info(const GemmArgs &g, int tile, int n_rou
     return u;
 }
 
-// B stage buffer i: stages 0..3 in the dedicated buffers, 4..7 (expert modes)
-// in the shared-memory A buffers, which only the router uses.
-__device__ __forceinline__ uint8_t *b_stage(Smem &S, int i)
-{
-    return i < kBStages ? S.b[i] : &S.a[0][0][0] + (i - kBStages) * kBBytes;
-}
-
 // First weight row of the two 128-row A tiles of a unit.
 template <int MODE>
 __device__ __forceinline__ void a_rows(const GemmArgs &g, const Unit &u, int &r0, int &r1)
@@ -148,6 +152,13 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, int *
     }
 }
 
+// 64-bit shared-memory descriptor from its two halves (the low half holds the
+// start address >> 4, so a byte offset o within 256 KB adds o >> 4 to it).
+__device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi)
+{
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // Waits for the last min(issued, depth) phases of a ring's full barriers.
 __device__ __forceinline__ void drain_ring(uint64_t *full, int depth, int issued, int *status)
 {
@@ -156,6 +167,13 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, int depth, int issued
         const int step = issued - i;
         drain_wait(&full[step % depth], (step / depth) & 1, status);
     }
+}
+
+// B stage i (0..7): stages 0..3 in the dedicated buffers, 4..7 (expert modes)
+// in the shared-memory A buffers that follow them.
+__device__ __forceinline__ uint8_t *b_stage(Smem &S, int i)
+{
+    return reinterpret_cast<uint8_t *>(&S) + offsetof(Smem, b) + static_cast<size_t>(i) * kBBytes;
 }
 
 template <int MODE>
@@ -171,13 +189,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     int *status = &g.ctrl->status;
     constexpr bool dequant_mode = MODE != kModeRouter;
     constexpr bool gather_b = MODE == kModeGateUp;
+    constexpr int b_stages = dequant_mode ? kBStagesX : kBStages;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRStages; ++s) {
             mbar_init(&S.full_r[s], 1);
             mbar_init(&S.empty_r[s], 2);
         }
-        for (int s = 0; s < kBStagesMax; ++s) {
+        for (int s = 0; s < kBStagesX; ++s) {
             mbar_init(&S.full_b[s], gather_b ? 64 : 1);
             mbar_init(&S.empty_b[s], 1);
         }
@@ -222,19 +241,22 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         }
     }
     const int total_tiles = (n_routed + g.n_shared_blocks) * g.m_tiles;
-    const int KT = g.K / kBK;
+    const int KB = g.KT / kBlk;  // blocks of four k-steps per unit (K padded)
 
     // Abort handling: a bounded wait that gives up raises abort_flag; every
     // later wait then returns at once.  Single-thread roles leave their loops;
     // multi-warp groups keep walking their loops (skipping work) so that every
     // thread still reaches every named barrier of its group.
+    //
+    // Ring bookkeeping: `blk` counts blocks over all units of this CTA.  Raw
+    // stage = blk % 2 (phase (blk / 2) % 2); tensor-memory A stage = k-step of
+    // the block (phase blk % 2); router shared-memory A stage = k-step % 2
+    // (phase k-step / 2); B stage = k-step (router, phase blk % 2) or
+    // 4 (blk % 2) + k-step (expert modes, phase (blk / 2) % 2).
     if (warp == 0) {
         // ------------------------------------------------ A-side producer (one thread)
-        // dequant modes: packed int4 tiles into the raw ring; router: bf16 Wr tiles into the A ring
         if (lane == 0) {
-            int rs = 0, as = 0;
-            uint32_t rph = 0, aph = 0;
-            int issued = 0;
+            int blk = 0, issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 const Unit u = unit_info<MODE>(g, tile, n_routed);
@@ -243,35 +265,33 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 a_rows<MODE>(g, u, r0, r1);
                 const CUtensorMap *mA0 = u.shared ? &tmSA0 : &tmA0;
                 const CUtensorMap *mA1 = u.shared ? &tmSA1 : &tmA1;
-                for (int kt = 0; kt < KT; ++kt) {
+                for (int kb = 0; kb < KB && ok; ++kb, ++blk) {
                     if (dequant_mode) {
-                        // one raw stage = g.raw_k k-steps: g.raw_k * 32 contiguous bytes of each row
-                        if (kt % g.raw_k != 0) continue;
-                        if (!mbar_wait(&S.empty_r[rs], rph ^ 1, abort_flag, status)) {
+                        // one raw stage: 4 k-steps = 128 contiguous bytes of each row
+                        const int rs = blk & 1;
+                        if (!mbar_wait(&S.empty_r[rs], ((blk >> 1) & 1) ^ 1, abort_flag, status)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&S.full_r[rs], 2 * kTileM * g.raw_k * (kBK / 2));
-                        tma_load_2d(S.raw[rs][0], mA0, &S.full_r[rs], kt * (kBK / 2), r0);
-                        tma_load_2d(S.raw[rs][1], mA1, &S.full_r[rs], kt * (kBK / 2), r1);
-                        if (++rs == kRStages) {
-                            rs = 0;
-                            rph ^= 1;
-                        }
+                        mbar_arrive_expect_tx(&S.full_r[rs], 2 * kRawBytes);
+                        tma_load_2d(S.raw[rs][0], mA0, &S.full_r[rs], kb * kRawRow, r0);
+                        tma_load_2d(S.raw[rs][1], mA1, &S.full_r[rs], kb * kRawRow, r1);
+                        ++issued;
                     } else {
-                        if (!mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&S.full_a[as], 2 * kABytes);
-                        tma_load_2d(S.a[as][0], &tmA0, &S.full_a[as], kt * kBK, r0);
-                        tma_load_2d(S.a[as][1], &tmA0, &S.full_a[as], kt * kBK, r1);
-                        if (++as == kAStages) {
-                            as = 0;
-                            aph ^= 1;
+#pragma unroll
+                        for (int jr = 0; jr < kBlk; ++jr) {
+                            const int as = jr & 1;
+                            if (!mbar_wait(&S.empty_a[as], ((jr >> 1) & 1) ^ 1, abort_flag, status)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&S.full_a[as], 2 * kABytes);
+                            const int kc = (kb * kBlk + jr) * kBK;
+                            tma_load_2d(S.a[as][0], &tmA0, &S.full_a[as], kc, r0);
+                            tma_load_2d(S.a[as][1], &tmA0, &S.full_a[as], kc, r1);
+                            ++issued;
                         }
                     }
-                    ++issued;  // raw stages (dequant modes) or A stages (router)
                 }
             }
             // Exit: no copy into this CTA's shared memory may still be in flight.
@@ -284,13 +304,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     } else if (warp == 2 || warp == 3) {
         // ------------------------------------------------ B producers (token rows)
         const int bl = (warp - 2) * 32 + lane;  // 0..63
-        const int b_stages = dequant_mode ? kBStagesMax : kBStages;
         if (gather_b) {
             // two warps gather token rows of fp16 x with 16-byte cp.async into the
-            // 128-byte-swizzled layout; each lane signals a stage once its copies landed
-            int bs = 0;
-            uint32_t bph = 0;
-            int gi = 0;  // stages issued; stage gi - kLag is signalled once its copies landed
+            // 128-byte-swizzled layout; each lane signals a stage once its copies
+            // landed, one block (kLag k-steps) after issuing them
+            int gi = 0, blk = 0;  // stages issued; blocks walked
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
                 const Unit u = unit_info<MODE>(g, tile, n_routed);
@@ -319,42 +337,40 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         }
                     }
                 }
-                for (int kt = 0; kt < KT; ++kt) {
-                    int good = 0;
-                    if (ok) {
-                        if (lane == 0) good = mbar_wait(&S.empty_b[bs], bph ^ 1, abort_flag, status);
-                        good = __shfl_sync(0xffffffffu, good, 0);
-                        if (!good) ok = false;
-                    }
-                    if (good) {
-                        const int c = bl & 7;
-                        const __half *xk = g.xh + kt * kBK + c * 8;
-                        uint8_t *bst = b_stage(S, bs);
-                        for (int r = bl >> 3; r < u.n_mma; r += 8)
-                            cp_async_16(bst + r * 128 + ((c ^ (r & 7)) << 4),
-                                        xk + static_cast<size_t>(S.prod_tok[r]) * g.d);
-                        cp_async_commit();
-                        ++gi;
-                        if (gi > kLag) {
-                            cp_async_wait_group<kLag>();  // the copies of stage gi - 1 - kLag landed
-                            fence_proxy_async_smem();
-                            mbar_arrive(&S.full_b[(gi - 1 - kLag) % b_stages]);
+                const int c = bl & 7;
+                const int sw = c;  // chunk c of row r lands at chunk c ^ (r % 8)
+                for (int kb = 0; kb < KB; ++kb, ++blk) {
+                    const int bs0 = (blk & 1) * kBlk;
+                    const uint32_t bpar = (blk >> 1) & 1;
+#pragma unroll
+                    for (int jr = 0; jr < kBlk; ++jr) {
+                        int good = 0;
+                        if (ok) {
+                            if (lane == 0) good = mbar_wait(&S.empty_b[bs0 + jr], bpar ^ 1, abort_flag, status);
+                            good = __shfl_sync(0xffffffffu, good, 0);
+                            if (!good) ok = false;
                         }
-                    }
-                    if (++bs == b_stages) {
-                        bs = 0;
-                        bph ^= 1;
+                        if (good) {
+                            const __half *xk = g.xh + (kb * kBlk + jr) * kBK + c * 8;
+                            uint8_t *bst = b_stage(S, bs0 + jr);
+                            for (int r = bl >> 3; r < u.n_mma; r += 8)
+                                cp_async_16(bst + r * 128 + ((sw ^ (r & 7)) << 4), xk + static_cast<size_t>(S.prod_tok[r]) * g.d);
+                            cp_async_commit();
+                            if (++gi > kLag) {
+                                cp_async_wait_group<kLag>();  // the copies of the previous block's stage jr landed
+                                fence_proxy_async_smem();
+                                mbar_arrive(&S.full_b[(bs0 ^ kBlk) + jr]);
+                            }
+                        }
                     }
                 }
             }
             cp_async_wait_all();
             fence_proxy_async_smem();
-            for (int i = gi - (gi < kLag ? gi : kLag); i < gi; ++i) mbar_arrive(&S.full_b[i % b_stages]);
+            for (int i = gi - (gi < kLag ? gi : kLag); i < gi; ++i) mbar_arrive(&S.full_b[i % kBStagesX]);
         } else if (bl == 0) {
-            // contiguous rows (x for the router, h for the down projection): one 2-D TMA per stage
-            int bs = 0;
-            uint32_t bph = 0;
-            int issued = 0;
+            // contiguous rows (x for the router, h for the down projection): one 2-D TMA per k-step
+            int blk = 0, issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 const Unit u = unit_info<MODE>(g, tile, n_routed);
@@ -371,17 +387,18 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         }
                     }
                 }
-                for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(&S.empty_b[bs], bph ^ 1, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&S.full_b[bs], kBBytes);
-                    tma_load_2d(b_stage(S, bs), &tmB, &S.full_b[bs], kt * kBK, b_row0);
-                    ++issued;
-                    if (++bs == b_stages) {
-                        bs = 0;
-                        bph ^= 1;
+                for (int kb = 0; kb < KB && ok; ++kb, ++blk) {
+                    const int bs0 = dequant_mode ? (blk & 1) * kBlk : 0;
+                    const uint32_t bpar = dequant_mode ? ((blk >> 1) & 1) : (blk & 1);
+#pragma unroll
+                    for (int jr = 0; jr < kBlk; ++jr) {
+                        if (!mbar_wait(&S.empty_b[bs0 + jr], bpar ^ 1, abort_flag, status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&S.full_b[bs0 + jr], kBBytes);
+                        tma_load_2d(b_stage(S, bs0 + jr), &tmB, &S.full_b[bs0 + jr], (kb * kBlk + jr) * kBK, b_row0);
+                        ++issued;
                     }
                 }
             }
@@ -391,13 +408,16 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (one thread)
         if (lane == 0) {
-            int bs = 0, as = 0, ab = 0;
-            uint32_t bph = 0, aph = 0, acc_ph = 0;
+            int blk = 0, ab = 0;
+            uint32_t acc_ph = 0;
             bool ok = true;
             const uint32_t fmt = dequant_mode ? kFmtF16 : kFmtBF16;
-            const int a_stages = dequant_mode ? kTAStages : kAStages;
             const int n_acc = dequant_mode ? 1 : 2;  // accumulator buffers in TMEM
-            const int b_stages = dequant_mode ? kBStagesMax : kBStages;
+            const uint64_t bd0 = sdesc_sw128(smem_u32(b_stage(S, 0)));
+            const uint32_t b_lo = static_cast<uint32_t>(bd0), b_hi = static_cast<uint32_t>(bd0 >> 32);
+            const uint64_t ad0 = sdesc_sw128(smem_u32(S.a[0][0]));
+            const uint32_t a_lo = static_cast<uint32_t>(ad0), a_hi = static_cast<uint32_t>(ad0 >> 32);
+            const uint32_t ta = tmem_base + kTmemAOffset;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 const Unit u = unit_info<MODE>(g, tile, n_routed);
                 if (u.rows <= 0) continue;
@@ -406,43 +426,42 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 const uint32_t idesc = idesc_f32acc(fmt, kTileM, u.n_mma);
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(ab * 2 * kTileM);
                 const uint32_t d1 = d0 + kTileM;
-                for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(&S.full_a[as], aph, abort_flag, status) ||
-                        !mbar_wait(&S.full_b[bs], bph, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t bb = smem_u32(b_stage(S, bs));
-                    if (dequant_mode) {
-                        // A from tensor memory: 64 K elements of a stage = 32 columns per matrix
-                        const uint32_t at0 = tmem_base + kTmemAOffset + static_cast<uint32_t>(as * 64);
-                        const uint32_t at1 = at0 + 32;
+                for (int kb = 0; kb < KB && ok; ++kb, ++blk) {
+                    const int bs0 = dequant_mode ? (blk & 1) * kBlk : 0;
+                    const uint32_t bpar = dequant_mode ? ((blk >> 1) & 1) : (blk & 1);
+                    const uint32_t apar = blk & 1;
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint32_t acc = (kt | kk) != 0;
-                            umma_ts(d0, at0 + kk * 8, sdesc_sw128(bb + kk * 32), idesc, acc);
-                            umma_ts(d1, at1 + kk * 8, sdesc_sw128(bb + kk * 32), idesc, acc);
+                    for (int jr = 0; jr < kBlk; ++jr) {
+                        const int as = dequant_mode ? jr : (jr & 1);
+                        const uint32_t ap = dequant_mode ? apar : ((jr >> 1) & 1);
+                        if (!mbar_wait(&S.full_a[as], ap, abort_flag, status) ||
+                            !mbar_wait(&S.full_b[bs0 + jr], bpar, abort_flag, status)) {
+                            ok = false;
+                            break;
                         }
-                    } else {
-                        const uint32_t a0 = smem_u32(S.a[as][0]);
-                        const uint32_t a1 = smem_u32(S.a[as][1]);
+                        tc_fence_after();
+                        const uint32_t blo = b_lo + static_cast<uint32_t>((bs0 + jr) * (kBBytes >> 4));
+                        if (dequant_mode) {
+                            // A from tensor memory: 64 K elements of a stage = 32 columns per matrix
+                            const uint32_t at = ta + static_cast<uint32_t>(jr * 64);
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint32_t acc = (kt | kk) != 0;
-                            umma_ss(d0, sdesc_sw128(a0 + kk * 32), sdesc_sw128(bb + kk * 32), idesc, acc);
-                            umma_ss(d1, sdesc_sw128(a1 + kk * 32), sdesc_sw128(bb + kk * 32), idesc, acc);
+                            for (int kk = 0; kk < kBK / 16; ++kk) {
+                                const uint32_t acc = (kb | jr | kk) != 0;
+                                umma_ts(d0, at + kk * 8, desc64(blo + kk * 2, b_hi), idesc, acc);
+                                umma_ts(d1, at + 32 + kk * 8, desc64(blo + kk * 2, b_hi), idesc, acc);
+                            }
+                        } else {
+                            const uint32_t alo = a_lo + static_cast<uint32_t>(as * (2 * kABytes >> 4));
+#pragma unroll
+                            for (int kk = 0; kk < kBK / 16; ++kk) {
+                                const uint32_t acc = (kb | jr | kk) != 0;
+                                umma_ss(d0, desc64(alo + kk * 2, a_hi), desc64(blo + kk * 2, b_hi), idesc, acc);
+                                umma_ss(d1, desc64(alo + (kABytes >> 4) + kk * 2, a_hi), desc64(blo + kk * 2, b_hi), idesc,
+                                        acc);
+                            }
                         }
-                    }
-                    umma_commit(&S.empty_a[as]);
-                    umma_commit(&S.empty_b[bs]);
-                    if (++as == a_stages) {
-                        as = 0;
-                        aph ^= 1;
-                    }
-                    if (++bs == b_stages) {
-                        bs = 0;
-                        bph ^= 1;
+                        umma_commit(&S.empty_a[as]);
+                        umma_commit(&S.empty_b[bs0 + jr]);
                     }
                 }
                 if (!ok) break;
@@ -462,10 +481,13 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         if (dequant_mode) {
             const int mi = (warp - 4) >> 2;              // which matrix of the pair
             const int r = ((warp - 4) & 3) * 32 + lane;  // row within the 128-row tile
+            const int sw = r & 7;                        // 128-byte swizzle of this row
             const int ngroups = g.K / kBK;
             const bool vec8 = (ngroups & 7) == 0;
-            int rs = 0, as = 0;
-            uint32_t rph = 0, aph = 0;
+            // this warp's TMEM lane quarter holds rows [32 * (warp % 4), +32)
+            const uint32_t ta_row = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kTmemAOffset +
+                                    static_cast<uint32_t>(mi * 32);
+            int blk = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
                 const Unit u = unit_info<MODE>(g, tile, n_routed);
@@ -489,77 +511,62 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         }
                     }
                 }
-                // scale / bias of 8 consecutive groups per 16-byte register block,
-                // fetched one block (8 k-steps) ahead
+                // scale / bias of 8 consecutive groups (two blocks) per 16-byte register
+                // block, fetched one register block ahead; groups past K read as zero
                 uint4 s_cur = load_groups8(srow, 0, ngroups, vec8), b_cur = load_groups8(brow, 0, ngroups, vec8);
                 uint4 s_nxt = load_groups8(srow, 8, ngroups, vec8), b_nxt = load_groups8(brow, 8, ngroups, vec8);
-                for (int kt = 0; kt < KT; ++kt) {
-                    const int j = kt & 7;
-                    if (j == 0 && kt > 0) {
+                for (int kb = 0; kb < KB; ++kb, ++blk) {
+                    if ((kb & 1) == 0 && kb > 0) {
                         s_cur = s_nxt;
                         b_cur = b_nxt;
-                        s_nxt = load_groups8(srow, kt + 8, ngroups, vec8);
-                        b_nxt = load_groups8(brow, kt + 8, ngroups, vec8);
+                        s_nxt = load_groups8(srow, kb * kBlk + 8, ngroups, vec8);
+                        b_nxt = load_groups8(brow, kb * kBlk + 8, ngroups, vec8);
                     }
-                    const int jr = kt % g.raw_k;  // k-step within the raw stage
-                    // One thread per group polls the mbarriers (polling is shared-memory
-                    // traffic that would slow the tensor core's operand reads); the rest
-                    // wait at the group's hardware barrier.
-                    if (r == 0) {
-                        bool w = ok;
-                        if (w && jr == 0) w = mbar_wait(&S.full_r[rs], rph, abort_flag, status);
-                        if (w) w = mbar_wait(&S.empty_a[as], aph ^ 1, abort_flag, status);
-                        S.dq_go[mi] = w;
-                    }
-                    named_barrier_sync(kBarDequant0 + mi, 128);
-                    const bool got = S.dq_go[mi] != 0;
-                    if (!got) ok = false;
-                    tc_fence_after();  // the MMAs that read this TMEM stage are complete (empty_a)
-                    if (got) {
-                        const uint16_t sc = pick16(s_cur, j), bi = pick16(b_cur, j);
-                        uint4 q0, q1;
-                        if (g.raw_k == kRK) {
+                    const int rs = blk & 1;
+                    const uint32_t rpar = (blk >> 1) & 1, apar = blk & 1;
+                    const int jb = (kb & 1) * kBlk;  // first group of this block within the register block
+                    const uint8_t *rowp = S.raw[rs][mi] + r * kRawRow;
+#pragma unroll
+                    for (int jr = 0; jr < kBlk; ++jr) {
+                        // One thread per group polls the mbarriers; the rest wait at
+                        // the group's hardware barrier.
+                        if (r == 0) {
+                            bool w = ok;
+                            if (w && jr == 0) w = mbar_wait(&S.full_r[rs], rpar, abort_flag, status);
+                            if (w) w = mbar_wait(&S.empty_a[jr], apar ^ 1, abort_flag, status);
+                            S.dq_go[mi] = w;
+                        }
+                        named_barrier_sync(kBarDequant0 + mi, 128);
+                        const bool got = S.dq_go[mi] != 0;
+                        if (!got) ok = false;
+                        tc_fence_after();  // the MMAs that read this TMEM stage are complete (empty_a)
+                        if (got) {
+                            const uint16_t sc = pick16(s_cur, jb + jr), bi = pick16(b_cur, jb + jr);
                             // 128-byte rows written by TMA with the 128-byte swizzle:
                             // 16-byte chunk c of row r sits at chunk c ^ (r % 8)
-                            const uint8_t *rowp = S.raw[rs][mi] + r * kRawRow;
-                            q0 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr) ^ (r & 7)) << 4));
-                            q1 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr + 1) ^ (r & 7)) << 4));
-                        } else {
-                            const uint4 *src = reinterpret_cast<const uint4 *>(S.raw[rs][mi] + r * (g.raw_k * kBK / 2) + jr * (kBK / 2));
-                            q0 = src[0];
-                            q1 = src[1];
-                        }
-                        const __half2 s2 = half2_from_bf16_bits(sc), b2 = half2_from_bf16_bits(bi);
-                        const __half2 s2_16 = __hmul2(s2, __floats2half2_rn(0.0625f, 0.0625f));
-                        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                        uint32_t cols[32];  // TMEM column 4c + j holds K positions 8c + 2j, 8c + 2j + 1
+                            const uint4 q0 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr) ^ sw) << 4));
+                            const uint4 q1 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr + 1) ^ sw) << 4));
+                            const __half2 s2 = half2_from_bf16_bits(sc), b2 = half2_from_bf16_bits(bi);
+                            const __half2 s2_16 = __hmul2(s2, __floats2half2_rn(0.0625f, 0.0625f));
+                            const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                            uint32_t cols[32];  // TMEM column 4c + j holds K positions 8c + 2j, 8c + 2j + 1
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint4 o = dequant8_f16_kperm(words[c], s2, s2_16, b2);
-                            cols[4 * c + 0] = o.x;
-                            cols[4 * c + 1] = o.y;
-                            cols[4 * c + 2] = o.z;
-                            cols[4 * c + 3] = o.w;
+                            for (int c = 0; c < 8; ++c) {
+                                const uint4 o = dequant8_f16_kperm(words[c], s2, s2_16, b2);
+                                cols[4 * c + 0] = o.x;
+                                cols[4 * c + 1] = o.y;
+                                cols[4 * c + 2] = o.z;
+                                cols[4 * c + 3] = o.w;
+                            }
+                            tmem_st_32x32b_x32(ta_row + static_cast<uint32_t>(jr * 64), cols);
+                            tmem_st_wait();
+                            tc_fence_before();
                         }
-                        // this warp's TMEM lane quarter holds rows [32 * (warp % 4), +32)
-                        const uint32_t ta = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kTmemAOffset +
-                                            static_cast<uint32_t>(as * 64 + mi * 32);
-                        tmem_st_32x32b_x32(ta, cols);
-                        tmem_st_wait();
-                        tc_fence_before();
-                    }
-                    named_barrier_sync(kBarDequant0 + mi, 128);
-                    if (r == 0 && ok) {
-                        mbar_arrive(&S.full_a[as]);
-                        if (jr == g.raw_k - 1) mbar_arrive(&S.empty_r[rs]);
-                    }
-                    if (jr == g.raw_k - 1 && ++rs == kRStages) {
-                        rs = 0;
-                        rph ^= 1;
-                    }
-                    if (++as == kTAStages) {
-                        as = 0;
-                        aph ^= 1;
+                        named_barrier_sync(kBarDequant0 + mi, 128);
+                        if (r == 0 && ok) {
+                            mbar_arrive(&S.full_a[jr]);
+                            if (jr == kBlk - 1) mbar_arrive(&S.empty_r[rs]);
+                        }
                     }
                 }
             }

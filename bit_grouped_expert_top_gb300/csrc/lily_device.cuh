@@ -170,6 +170,21 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Row gather: four rows (r0..r3) of a 2-D tensor whose box is one row high,
+// each box_inner elements from column c0, written one after another into
+// shared memory (the swizzle follows the shared-memory address, so four-row
+// groups at 512-byte offsets of a 1024-aligned buffer form the same layout as
+// one tiled load).  Completion is signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int4 rows)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ----------------------------------------------------------------- cp.async (16-byte gathers)
 __device__ __forceinline__ void cp_async_16(void *dst, const void *src)
 {
@@ -182,6 +197,27 @@ __device__ __forceinline__ void cp_async_wait_group()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Bulk (non-tensor) asynchronous copies shared -> global, tracked per thread in
+// bulk groups.  Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+// gdst[i] += ssrc[i] (fp32), performed by the memory system.
+__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const float *ssrc, uint32_t bytes)
+{
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the shared-memory sources of this thread's bulk groups have been read.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until this thread's bulk groups have fully completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tensor core operands).

@@ -27,7 +27,7 @@ struct GemmArgs {
     int bm;               // token rows per block (UMMA N <= 128)
     int K;                // reduction length: d (router, gate/up) or I (down)
     int m_tiles;          // weight-tile pairs per block: 1 (router), I/128 (gate/up), d/256 (down)
-    int raw_k;            // k-steps of 64 per raw int4 TMA stage: 4 (128-byte rows, 128B swizzle), 2 or 1
+    int KT;               // k-steps of 64 per unit, K / 64 rounded up to a multiple of 4
     int n_shared_blocks;  // identity blocks: ceil(T/bm)
     int n_routed_max;     // capacity of block_map
     const int *n_blocks;  // device: routed blocks
