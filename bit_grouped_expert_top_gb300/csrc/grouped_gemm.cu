@@ -52,7 +52,6 @@ constexpr int kBStages = 4;    // B ring in the dedicated buffers (router)
 constexpr int kBStagesX = 8;   // expert modes: 4 more B stages in the shared-memory A buffers they do not use
 constexpr int kAStages = 2;    // shared-memory A ring (bf16 router weights by TMA)
 constexpr int kTAStages = 4;   // tensor-memory A ring (fp16 dequantised weights, expert modes) = kBlk
-constexpr int kLag = 4;        // cp.async groups a gathering lane keeps in flight (< B stages)
 constexpr int kTileM = 128;
 constexpr int kBK = 64;        // one quantisation group, one 128-byte swizzle row
 constexpr int kTileN = 128;
@@ -67,7 +66,6 @@ constexpr uint32_t kTmemAOffset = 256;
 constexpr int kBarDequant0 = 1, kBarEpilogue = 3, kBarBProducer = 4;  // named barrier ids
 static_assert(kTAStages == kBlk, "one tensor-memory A stage per k-step of a block");
 static_assert(kBStagesX == 2 * kBlk && kBStages == kBlk && kAStages == 2, "ring slots are compile-time within a block");
-static_assert(kLag == kBlk, "a gathered stage is signalled one block after it was issued");
 
 struct __align__(1024) Smem {
     uint8_t b[kBStages][kBBytes];         // B ring; expert modes continue into `a`
@@ -306,9 +304,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         const int bl = (warp - 2) * 32 + lane;  // 0..63
         if (gather_b) {
             // two warps gather token rows of fp16 x with 16-byte cp.async into the
-            // 128-byte-swizzled layout; each lane signals a stage once its copies
-            // landed, one block (kLag k-steps) after issuing them
-            int gi = 0, blk = 0;  // stages issued; blocks walked
+            // 128-byte-swizzled layout; the copy hardware arrives on the stage's
+            // full barrier (64 arrivals) once each lane's copies have landed
+            int blk = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
                 const Unit u = unit_info<MODE>(g, tile, n_routed);
@@ -355,19 +353,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                             uint8_t *bst = b_stage(S, bs0 + jr);
                             for (int r = bl >> 3; r < u.n_mma; r += 8)
                                 cp_async_16(bst + r * 128 + ((sw ^ (r & 7)) << 4), xk + static_cast<size_t>(S.prod_tok[r]) * g.d);
-                            cp_async_commit();
-                            if (++gi > kLag) {
-                                cp_async_wait_group<kLag>();  // the copies of the previous block's stage jr landed
-                                fence_proxy_async_smem();
-                                mbar_arrive(&S.full_b[(bs0 ^ kBlk) + jr]);
-                            }
+                            cp_async_mbar_arrive_noinc(&S.full_b[bs0 + jr]);
                         }
                     }
                 }
             }
-            cp_async_wait_all();
-            fence_proxy_async_smem();
-            for (int i = gi - (gi < kLag ? gi : kLag); i < gi; ++i) mbar_arrive(&S.full_b[i % kBStagesX]);
+            cp_async_wait_all();  // no copy into shared memory in flight at exit
         } else if (bl == 0) {
             // contiguous rows (x for the router, h for the down projection): one 2-D TMA per k-step
             int blk = 0, issued = 0;
@@ -440,6 +431,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                             break;
                         }
                         tc_fence_after();
+                        if (gather_b) fence_proxy_async_smem();  // gathered rows were written by cp.async
                         const uint32_t blo = b_lo + static_cast<uint32_t>((bs0 + jr) * (kBBytes >> 4));
                         if (dequant_mode) {
                             // A from tensor memory: 64 K elements of a stage = 32 columns per matrix
