@@ -200,7 +200,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         }
         for (int s = 0; s < kTAStages; ++s) {
             mbar_init(&S.full_a[s], dequant_mode ? 2 : 1);
-            mbar_init(&S.empty_a[s], 1);
+            mbar_init(&S.empty_a[s], 1);  // router only
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&S.full_acc[s], 1);
@@ -248,9 +248,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     //
     // Ring bookkeeping: `blk` counts blocks over all units of this CTA.  Raw
     // stage = blk % 2 (phase (blk / 2) % 2); tensor-memory A stage = k-step of
-    // the block (phase blk % 2); router shared-memory A stage = k-step % 2
-    // (phase k-step / 2); B stage = k-step (router, phase blk % 2) or
-    // 4 (blk % 2) + k-step (expert modes, phase (blk / 2) % 2).
+    // the block (full phase blk % 2; it is free again once the MMAs of the
+    // k-step four back, in B slot 4 ((blk - 1) % 2) + k-step, completed);
+    // router shared-memory A stage = k-step % 2 (phase k-step / 2); B stage =
+    // k-step (router, phase blk % 2) or 4 (blk % 2) + k-step (expert modes,
+    // phase (blk / 2) % 2).
     if (warp == 0) {
         // ------------------------------------------------ A-side producer (one thread)
         if (lane == 0) {
@@ -425,8 +427,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     for (int jr = 0; jr < kBlk; ++jr) {
                         const int as = dequant_mode ? jr : (jr & 1);
                         const uint32_t ap = dequant_mode ? apar : ((jr >> 1) & 1);
-                        if (!mbar_wait(&S.full_a[as], ap, abort_flag, status) ||
-                            !mbar_wait(&S.full_b[bs0 + jr], bpar, abort_flag, status)) {
+                        if (!mbar_wait2(&S.full_a[as], ap, &S.full_b[bs0 + jr], bpar, abort_flag, status)) {
                             ok = false;
                             break;
                         }
@@ -452,7 +453,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                                         acc);
                             }
                         }
-                        umma_commit(&S.empty_a[as]);
+                        // expert modes: one release per k-step; the dequantisers wait on the
+                        // B slot of the k-step four back, whose MMAs read the same A stage
+                        if (!dequant_mode) umma_commit(&S.empty_a[as]);
                         umma_commit(&S.empty_b[bs0 + jr]);
                     }
                 }
@@ -515,7 +518,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         b_nxt = load_groups8(brow, kb * kBlk + 8, ngroups, vec8);
                     }
                     const int rs = blk & 1;
-                    const uint32_t rpar = (blk >> 1) & 1, apar = blk & 1;
+                    const uint32_t rpar = (blk >> 1) & 1;
                     const int jb = (kb & 1) * kBlk;  // first group of this block within the register block
                     const uint8_t *rowp = S.raw[rs][mi] + r * kRawRow;
 #pragma unroll
@@ -525,7 +528,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         if (r == 0) {
                             bool w = ok;
                             if (w && jr == 0) w = mbar_wait(&S.full_r[rs], rpar, abort_flag, status);
-                            if (w) w = mbar_wait(&S.empty_a[jr], apar ^ 1, abort_flag, status);
+                            // TMEM A stage jr was last read by the MMAs of the k-step four
+                            // back, which released B slot (bs0 ^ 4) + jr
+                            if (w) w = mbar_wait(&S.empty_b[((blk & 1) ^ 1) * kBlk + jr], ((blk - 1) >> 1) & 1, abort_flag, status);
                             S.dq_go[mi] = w;
                         }
                         named_barrier_sync(kBarDequant0 + mi, 128);

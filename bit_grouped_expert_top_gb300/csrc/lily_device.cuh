@@ -132,6 +132,25 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parit
     return ok != 0;
 }
 
+// Waits for two phases; both barriers are tested at once first, so that when
+// both are already complete the thread pays one shared-memory round trip.
+__device__ __forceinline__ bool mbar_wait2(uint64_t *bar0, uint32_t parity0, uint64_t *bar1, uint32_t parity1,
+                                           volatile int *abort_flag, int *status)
+{
+    uint32_t ok0, ok1;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%2], %3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q, [%4], %5;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "selp.u32 %1, 1, 0, q;\n\t}"
+        : "=r"(ok0), "=r"(ok1)
+        : "r"(smem_u32(bar0)), "r"(parity0), "r"(smem_u32(bar1)), "r"(parity1)
+        : "memory");
+    if (ok0 && ok1) return true;
+    return (ok0 || mbar_wait(bar0, parity0, abort_flag, status)) && (ok1 || mbar_wait(bar1, parity1, abort_flag, status));
+}
+
 // Latency-critical wait: polls with the non-blocking test_wait so the thread
 // sees the phase flip at once; same bounds and abort handling as mbar_wait.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status)
