@@ -337,8 +337,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         }
                     }
                 }
+                // this lane copies 16-byte chunk c of B rows (bl / 8) + 8 i, i < 16; the
+                // source rows live in registers for the whole unit, and chunk c of
+                // row r lands at chunk c ^ (r % 8) = c ^ (bl / 8) of its 128-byte row
                 const int c = bl & 7;
-                const int sw = c;  // chunk c of row r lands at chunk c ^ (r % 8)
+                const int r0 = bl >> 3;
+                const uint32_t dst0 = static_cast<uint32_t>(r0 * 128 + ((c ^ r0) << 4));
+                int tok[kTileN / 8];
+#pragma unroll
+                for (int i = 0; i < kTileN / 8; ++i) tok[i] = S.prod_tok[min(r0 + 8 * i, u.n_mma - 1)];
                 for (int kb = 0; kb < KB; ++kb, ++blk) {
                     const int bs0 = (blk & 1) * kBlk;
                     const uint32_t bpar = (blk >> 1) & 1;
@@ -352,9 +359,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         }
                         if (good) {
                             const __half *xk = g.xh + (kb * kBlk + jr) * kBK + c * 8;
-                            uint8_t *bst = b_stage(S, bs0 + jr);
-                            for (int r = bl >> 3; r < u.n_mma; r += 8)
-                                cp_async_16(bst + r * 128 + ((sw ^ (r & 7)) << 4), xk + static_cast<size_t>(S.prod_tok[r]) * g.d);
+                            uint8_t *bst = b_stage(S, bs0 + jr) + dst0;
+#pragma unroll
+                            for (int i = 0; i < kTileN / 8; ++i)
+                                if (r0 + 8 * i < u.n_mma) cp_async_16(bst + i * 1024, xk + static_cast<size_t>(tok[i]) * g.d);
                             cp_async_mbar_arrive_noinc(&S.full_b[bs0 + jr]);
                         }
                     }
