@@ -233,9 +233,14 @@ bool tmap_q4(CUtensorMap *m, const uint8_t *q, uint64_t K, uint64_t rows)
 
 namespace {
 
+// Token rows per router GEMM unit: 64 keeps more SMs busy than 128 at the
+// prefill sizes (T = 8192 gives 128 units) at a small loss of MMA width.
+constexpr int kRouterBlockRows = 64;
+
 // ------------------------------------------------------------------ enqueue helpers
 cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, const uint16_t *x,
-                          const lily_moe_routing &r, float *logits, void *ws, cudaStream_t stream)
+                          const lily_moe_routing &r, float *logits, void *ws, cudaStream_t stream,
+                          cudaEvent_t *events = nullptr)
 {
     const PrefillLayout L = prefill_layout(s);
     Ctrl *ctrl = at<Ctrl>(ws, L.ctrl);
@@ -247,10 +252,10 @@ cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, co
     g.mode = kModeRouter;
     g.KT = gemm_k_steps(s.d);
     g.T = s.T; g.d = s.d; g.E = s.E; g.top_k = s.top_k; g.I = s.I;
-    g.bm = 128;
+    g.bm = kRouterBlockRows;
     g.K = s.d;
     g.m_tiles = 1;
-    g.n_shared_blocks = static_cast<int>(ceil_div(s.T, 128));
+    g.n_shared_blocks = static_cast<int>(ceil_div(s.T, kRouterBlockRows));
     g.n_routed_max = 0;
     g.router_bias = w.router_bias;
     g.logits = logits;
@@ -259,6 +264,7 @@ cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, co
     const int grid = std::max(1, std::min(sms, g.n_shared_blocks));
     cudaError_t e = launch_grouped_gemm(g, tmX, tmWr, tmWr, tmWr, tmWr, grid, stream);
     if (e != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
 
     RouteArgs ra{};
     ra.T = s.T; ra.E = s.E; ra.top_k = s.top_k; ra.bm = s.block_rows;
@@ -271,7 +277,10 @@ cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, co
     ra.n_chunks = static_cast<int>(ceil_div(s.T, kRouteChunkTokens));
     ra.ctrl = ctrl;
     if ((e = launch_topk_count(ra, stream)) != cudaSuccess) return e;
-    return launch_scatter(ra, stream);
+    if ((e = launch_route_scan(ra, stream)) != cudaSuccess) return e;
+    if ((e = launch_scatter(ra, stream)) != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[2], stream)) != cudaSuccess) return e;
+    return cudaSuccess;
 }
 
 cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, const uint16_t *x,
@@ -481,12 +490,7 @@ int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *
     const lily_moe_routing rr = r ? *r : internal_routing(*shape, ws);
     float *logits = rr.logits ? rr.logits : at<float>(ws, prefill_layout(*shape).logits);
     if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return LILY_ERR_LAUNCH;
-    if (enqueue_route(*shape, *w, x, rr, logits, ws, stream) != cudaSuccess) return LILY_ERR_LAUNCH;
-    if (events) {
-        // the router GEMM and the two routing kernels are one unit here
-        if (cudaEventRecord(events[1], stream) != cudaSuccess || cudaEventRecord(events[2], stream) != cudaSuccess)
-            return LILY_ERR_LAUNCH;
-    }
+    if (enqueue_route(*shape, *w, x, rr, logits, ws, stream, events) != cudaSuccess) return LILY_ERR_LAUNCH;
     return to_status(enqueue_experts(*shape, *w, x, rr, out, ws, stream, events));
 }
 

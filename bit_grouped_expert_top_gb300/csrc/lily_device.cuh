@@ -527,9 +527,20 @@ __device__ __forceinline__ uint16_t pick16(const uint4 v, int j)
     return static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
 }
 
-// silu(z) = z / (1 + e^-z) with the fast exponential and division intrinsics
-// (about 2 ulp in fp32, far below the fp16 rounding of the result).
-__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+// silu(z) = z sigmoid(z), with sigmoid(z) = (1 + tanh(z / 2)) / 2 and the
+// hardware tanh approximation (one special-function op per value; its error,
+// about 2^-11 of |tanh|, stays near the fp16 rounding of the result).
+__device__ __forceinline__ float tanh_approx(float v)
+{
+    float r;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float silu_f(float z)
+{
+    const float hz = 0.5f * z;
+    return fmaf(hz, tanh_approx(hz), hz);
+}
 
 // ----------------------------------------------------------------- top-8 of 256 (one warp)
 // Order-preserving map of a float to uint32 (larger float -> larger key).

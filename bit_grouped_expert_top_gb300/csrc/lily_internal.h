@@ -66,12 +66,13 @@ struct RouteArgs {
     float *topk_w;
     int *counts, *offsets, *perm, *block_map, *n_blocks;
     int *chunk_counts;  // [C][E]
-    int *chunk_base;    // [C][E]
+    int *chunk_base;    // [C][E]: chunk's first row within its expert (relative to offsets[e])
     int n_chunks;
     Ctrl *ctrl;
 };
 constexpr int kRouteChunkTokens = 64;
 cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream);
+cudaError_t launch_route_scan(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_scatter(const RouteArgs &a, cudaStream_t stream);
 
 // Decode path (1 <= T <= 8).

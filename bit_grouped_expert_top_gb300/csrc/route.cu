@@ -5,15 +5,17 @@
 // routing histogram, prefix scan, scatter and block map stay inside one GPU
 // submission with no CPU synchronisation (section "Prefill e decode").
 //
-// Two kernels, one stream, no host sync:
+// Three kernels, one stream, no host sync:
 //   topk_count_kernel : one warp per token selects the top 8 of 256 fp32 logits
 //                       (descending; lower index first among equal logits) with
 //                       shuffle arg-max rounds and computes the renormalised
 //                       softmax weights; each CTA then counts its 64-token chunk
-//                       per expert.  The last CTA to finish (ticket counter)
-//                       scans the per-chunk counts column-wise (per expert) into
-//                       each chunk's write base, produces counts, the exclusive
-//                       scan over experts, and the block map.
+//                       per expert.
+//   scan_kernel       : one CTA per expert scans that expert's per-chunk counts
+//                       in chunk order (each chunk's base within the expert) and
+//                       writes its total; the last CTA to finish (ticket
+//                       counter) scans the totals over experts into offsets and
+//                       writes the block map.
 //   scatter_kernel    : each CTA writes its chunk's assignments into
 //                       expert-sorted order; ranks inside the chunk come from
 //                       __match_any_sync plus per-warp counts, so the order
@@ -59,8 +61,6 @@ __global__ void __launch_bounds__(kRouteThreads)
 topk_count_kernel(const RouteArgs a)
 {
     __shared__ int hist[kE];
-    __shared__ int scratch[8];
-    __shared__ int is_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int chunk = blockIdx.x;
 
@@ -81,8 +81,29 @@ topk_count_kernel(const RouteArgs a)
     }
     __syncthreads();
     a.chunk_counts[static_cast<size_t>(chunk) * kE + threadIdx.x] = hist[threadIdx.x];
+}
 
-    // Last CTA to finish builds the scans and the block map.
+// CTA e: exclusive scan of expert e's per-chunk counts in chunk order (chunk
+// bases relative to the expert's first sorted row) and the expert's total.
+// The last CTA scans the totals over experts and writes the block map.
+__global__ void __launch_bounds__(kRouteThreads)
+scan_kernel(const RouteArgs a)
+{
+    __shared__ int scratch[8];
+    __shared__ int is_last;
+    const int e = blockIdx.x;
+    int carry = 0;
+    for (int c0 = 0; c0 < a.n_chunks; c0 += kRouteThreads) {
+        const int c = c0 + threadIdx.x;
+        const size_t i = static_cast<size_t>(c) * kE + e;
+        const int v = c < a.n_chunks ? a.chunk_counts[i] : 0;
+        int tile_total;
+        const int ex = block_exclusive_scan_256(v, scratch, &tile_total);
+        if (c < a.n_chunks) a.chunk_base[i] = carry + ex;
+        carry += tile_total;
+    }
+    if (threadIdx.x == 0) a.counts[e] = carry;
+
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -93,29 +114,19 @@ topk_count_kernel(const RouteArgs a)
     if (!is_last) return;
     __threadfence();
 
-    const int e = threadIdx.x;
-    int total_e = 0;
-    for (int c = 0; c < a.n_chunks; ++c) total_e += __ldcg(a.chunk_counts + static_cast<size_t>(c) * kE + e);
+    const int x = threadIdx.x;  // expert
+    const int total_e = __ldcg(a.counts + x);
     int sum_all;
     const int off = block_exclusive_scan_256(total_e, scratch, &sum_all);
     const int nb = (total_e + a.bm - 1) / a.bm;
     int nb_all;
     const int bstart = block_exclusive_scan_256(nb, scratch, &nb_all);
-
-    a.counts[e] = total_e;
-    a.offsets[e] = off;
-    if (e == kE - 1) a.offsets[kE] = off + total_e;
-    if (e == 0) *a.n_blocks = nb_all;
-    int running = off;
-    for (int c = 0; c < a.n_chunks; ++c) {
-        const size_t i = static_cast<size_t>(c) * kE + e;
-        const int v = __ldcg(a.chunk_counts + i);
-        a.chunk_base[i] = running;
-        running += v;
-    }
+    a.offsets[x] = off;
+    if (x == kE - 1) a.offsets[kE] = off + total_e;
+    if (x == 0) *a.n_blocks = nb_all;
     for (int b = 0; b < nb; ++b) {
         int *ent = a.block_map + 3 * static_cast<size_t>(bstart + b);
-        ent[0] = e;
+        ent[0] = x;
         ent[1] = off + b * a.bm;
         ent[2] = min(a.bm, total_e - b * a.bm);
     }
@@ -132,7 +143,7 @@ scatter_kernel(const RouteArgs a)
     const int n_assign = kRouteChunkTokens * kTopK;  // 512 per chunk
     const int total = a.T * kTopK;
 
-    base[threadIdx.x] = a.chunk_base[static_cast<size_t>(chunk) * kE + threadIdx.x];
+    base[threadIdx.x] = a.offsets[threadIdx.x] + a.chunk_base[static_cast<size_t>(chunk) * kE + threadIdx.x];
     const unsigned lt_mask = (1u << lane) - 1u;
 
     for (int round = 0; round < n_assign / kRouteThreads; ++round) {
@@ -177,6 +188,12 @@ scatter_kernel(const RouteArgs a)
 cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream)
 {
     topk_count_kernel<<<a.n_chunks, kRouteThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_scan(const RouteArgs &a, cudaStream_t stream)
+{
+    scan_kernel<<<kE, kRouteThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
