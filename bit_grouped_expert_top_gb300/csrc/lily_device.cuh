@@ -550,59 +550,75 @@ __device__ __forceinline__ uint32_t float_order_key(float v)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
+// Larger key first: (a, b) <- (max, min).
+__device__ __forceinline__ void cmpx_desc(unsigned long long &a, unsigned long long &b)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-        v = w > v ? w : v;
-    }
-    return v;
+    const unsigned long long x = a, y = b;
+    a = x > y ? x : y;
+    b = x > y ? y : x;
 }
 
-// Selects the 8 largest of 256 fp32 logits (row in global memory, 16-byte
-// aligned), ordered by descending logit with the lower expert index first among
-// equal logits, and their renormalised softmax weights
-// w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0).  Lane j < 8 receives slot j.
-__device__ __forceinline__ void warp_top8_of_256(const float *row, int lane, int &sel_e, float &sel_w)
+// Inverse of float_order_key.
+__device__ __forceinline__ float float_from_order_key(uint32_t k)
 {
-    const float4 *src = reinterpret_cast<const float4 *>(row + lane * 8);
-    const float4 l0 = __ldcg(src), l1 = __ldcg(src + 1);
-    const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-    unsigned long long key[8];
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Selects the 8 largest of 256 fp32 logits given as 8 per lane (lane l holds
+// logits 8l..8l+7), ordered by descending logit with the lower expert index
+// first among equal logits, and their renormalised softmax weights
+// w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0).  Lane j < 8 receives slot j.
+// Each lane sorts its 8 keys (key = order-preserving logit bits, then 255 -
+// index) with a 19-exchange network; five butterfly rounds then merge the
+// lists: the top 8 of two descending lists A, B is max(A[j], B[7 - j]), a
+// bitonic sequence that three half-cleaner stages sort.
+__device__ __forceinline__ void warp_top8_keys(const float (&lv)[8], int lane, int &sel_e, float &sel_w)
+{
+    unsigned long long k[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-        key[j] = (static_cast<unsigned long long>(float_order_key(lv[j])) << 32) |
-                 static_cast<unsigned long long>(255 - (lane * 8 + j));
-    float sel_v = 0.0f;
-    sel_e = 0;
-#pragma unroll 1
-    for (int r = 0; r < 8; ++r) {
-        unsigned long long best = 0;
+        k[j] = (static_cast<unsigned long long>(float_order_key(lv[j])) << 32) |
+               static_cast<unsigned long long>(255 - (lane * 8 + j));
+    cmpx_desc(k[0], k[2]); cmpx_desc(k[1], k[3]); cmpx_desc(k[4], k[6]); cmpx_desc(k[5], k[7]);
+    cmpx_desc(k[0], k[4]); cmpx_desc(k[1], k[5]); cmpx_desc(k[2], k[6]); cmpx_desc(k[3], k[7]);
+    cmpx_desc(k[0], k[1]); cmpx_desc(k[2], k[3]); cmpx_desc(k[4], k[5]); cmpx_desc(k[6], k[7]);
+    cmpx_desc(k[2], k[4]); cmpx_desc(k[3], k[5]);
+    cmpx_desc(k[1], k[4]); cmpx_desc(k[3], k[6]);
+    cmpx_desc(k[1], k[2]); cmpx_desc(k[3], k[4]); cmpx_desc(k[5], k[6]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) best = key[j] > best ? key[j] : best;
-        best = warp_max_u64(best);
-        const int e = 255 - static_cast<int>(best & 0xFFFFFFFFull);
-        float v = 0.0f;
+    for (int m = 1; m < 32; m <<= 1) {
+        unsigned long long o[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (j == (e & 7)) {
-                v = lv[j];
-                if ((e >> 3) == lane) key[j] = 0;
-            }
-        }
-        v = __shfl_sync(0xffffffffu, v, e >> 3);
-        if (lane == r) {
-            sel_e = e;
-            sel_v = v;
-        }
+        for (int j = 0; j < 8; ++j) o[j] = __shfl_xor_sync(0xffffffffu, k[7 - j], m);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) k[j] = k[j] > o[j] ? k[j] : o[j];
+#pragma unroll
+        for (int d = 4; d > 0; d >>= 1)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if ((j & d) == 0) cmpx_desc(k[j], k[j + d]);
     }
-    const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
+    unsigned long long mine = k[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j)
+        if (lane == j) mine = k[j];
+    sel_e = 255 - static_cast<int>(mine & 0xFFFFFFFFull);
+    const float sel_v = float_from_order_key(static_cast<uint32_t>(mine >> 32));
+    const float vmax = float_from_order_key(static_cast<uint32_t>(k[0] >> 32));
     const float ex = lane < 8 ? expf(sel_v - vmax) : 0.0f;
     float den = ex;
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     sel_w = ex / den;
+}
+
+// As warp_top8_keys, reading the row (global memory, 16-byte aligned).
+__device__ __forceinline__ void warp_top8_of_256(const float *row, int lane, int &sel_e, float &sel_w)
+{
+    const float4 *src = reinterpret_cast<const float4 *>(row + lane * 8);
+    const float4 l0 = __ldcg(src), l1 = __ldcg(src + 1);
+    const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+    warp_top8_keys(lv, lane, sel_e, sel_w);
 }
 
 }  // namespace lily

@@ -67,12 +67,26 @@ topk_count_kernel(const RouteArgs a)
     hist[threadIdx.x] = 0;
     __syncthreads();
 
+    // each warp's tokens, the next token's logits loaded while this one is ranked
+    const int t0 = chunk * kRouteChunkTokens + warp * kTokPerWarp;
+    float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
+    if (t0 < a.T) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.logits + static_cast<size_t>(t0) * kE + lane * 8);
+        n0 = __ldcg(src);
+        n1 = __ldcg(src + 1);
+    }
     for (int i = 0; i < kTokPerWarp; ++i) {
-        const int t = chunk * kRouteChunkTokens + warp * kTokPerWarp + i;
+        const int t = t0 + i;
         if (t >= a.T) break;
+        const float lv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+        if (i + 1 < kTokPerWarp && t + 1 < a.T) {
+            const float4 *src = reinterpret_cast<const float4 *>(a.logits + static_cast<size_t>(t + 1) * kE + lane * 8);
+            n0 = __ldcg(src);
+            n1 = __ldcg(src + 1);
+        }
         int sel_e;
         float sel_w;
-        warp_top8_of_256(a.logits + static_cast<size_t>(t) * kE, lane, sel_e, sel_w);
+        warp_top8_keys(lv, lane, sel_e, sel_w);
         if (lane < kTopK) {
             a.topk_idx[static_cast<size_t>(t) * kTopK + lane] = sel_e;
             a.topk_w[static_cast<size_t>(t) * kTopK + lane] = sel_w;
