@@ -21,9 +21,10 @@
 //                 down h), or cp.async gathers of token rows of x by the
 //                 routing permutation (gate/up);
 //   warp 1        TMEM allocator + single-thread tcgen05.mma issuer;
-//   warps 4..11   dequantisers (expert modes): int4 -> fp16, one matrix per
-//                 warpgroup, one row per thread, written to tensor memory with
-//                 tcgen05.st; the MMA reads A from tensor memory (TS form);
+//   warps 4..11   dequantisers (expert modes): int4 -> fp16, one row per
+//                 thread, each warp 32 rows of one matrix on its own pace,
+//                 written to tensor memory with tcgen05.st; the MMA reads A
+//                 from tensor memory (TS form);
 //   warps 12..19  epilogue: tcgen05.ld from TMEM, then per mode the router
 //                 logits (+bias), SwiGLU into h (fp16), or the down projection
 //                 scaled by the routing weight and added (red.global.add.f32)
@@ -63,7 +64,7 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns: accumulators at [0, 256) per buffer (router: two buffers, [0, 512));
 // expert modes: one accumulator buffer and the A ring at [256, 512), 64 columns per stage.
 constexpr uint32_t kTmemAOffset = 256;
-constexpr int kBarDequant0 = 1, kBarEpilogue = 3, kBarBProducer = 4;  // named barrier ids
+constexpr int kBarEpilogue = 3, kBarBProducer = 4;  // named barrier ids
 static_assert(kTAStages == kBlk, "one tensor-memory A stage per k-step of a block");
 static_assert(kBStagesX == 2 * kBlk && kBStages == kBlk && kAStages == 2, "ring slots are compile-time within a block");
 
@@ -79,7 +80,6 @@ struct __align__(1024) Smem {
     uint32_t tmem_base;
     int abort_flag;
     int prod_tok[kTileN];  // B producers: source row of each B row of the current unit
-    int dq_go[2];          // dequant group's wait result, published by its waiting thread
     int ep_go;             // epilogue's wait result, published by its waiting thread
     int ep_tok[kTileN];    // epilogue: token of each column (down)
     float ep_w[kTileN];    // epilogue: routing weight of each column (down)
@@ -192,14 +192,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRStages; ++s) {
             mbar_init(&S.full_r[s], 1);
-            mbar_init(&S.empty_r[s], 2);
+            mbar_init(&S.empty_r[s], 8);  // the eight dequantiser warps
         }
         for (int s = 0; s < kBStagesX; ++s) {
             mbar_init(&S.full_b[s], gather_b ? 64 : 1);
             mbar_init(&S.empty_b[s], 1);
         }
         for (int s = 0; s < kTAStages; ++s) {
-            mbar_init(&S.full_a[s], dequant_mode ? 2 : 1);
+            mbar_init(&S.full_a[s], dequant_mode ? 8 : 1);  // dequantiser warps / router TMA
             mbar_init(&S.empty_a[s], 1);  // router only
         }
         for (int s = 0; s < 2; ++s) {
@@ -531,18 +531,18 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     const uint8_t *rowp = S.raw[rs][mi] + r * kRawRow;
 #pragma unroll
                     for (int jr = 0; jr < kBlk; ++jr) {
-                        // One thread per group polls the mbarriers; the rest wait at
-                        // the group's hardware barrier.
-                        if (r == 0) {
+                        // Each warp runs on its own: lane 0 polls the mbarriers and
+                        // broadcasts the result.
+                        int go = 0;
+                        if (lane == 0) {
                             bool w = ok;
                             if (w && jr == 0) w = mbar_wait(&S.full_r[rs], rpar, abort_flag, status);
                             // TMEM A stage jr was last read by the MMAs of the k-step four
                             // back, which released B slot (bs0 ^ 4) + jr
                             if (w) w = mbar_wait(&S.empty_b[((blk & 1) ^ 1) * kBlk + jr], ((blk - 1) >> 1) & 1, abort_flag, status);
-                            S.dq_go[mi] = w;
+                            go = w;
                         }
-                        named_barrier_sync(kBarDequant0 + mi, 128);
-                        const bool got = S.dq_go[mi] != 0;
+                        const bool got = __shfl_sync(0xffffffffu, go, 0) != 0;
                         if (!got) ok = false;
                         tc_fence_after();  // the MMAs that read this TMEM stage are complete (empty_a)
                         if (got) {
@@ -567,8 +567,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                             tmem_st_wait();
                             tc_fence_before();
                         }
-                        named_barrier_sync(kBarDequant0 + mi, 128);
-                        if (r == 0 && ok) {
+                        __syncwarp();
+                        if (lane == 0 && ok) {
                             mbar_arrive(&S.full_a[jr]);
                             if (jr == kBlk - 1) mbar_arrive(&S.empty_r[rs]);
                         }
