@@ -34,7 +34,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // ------------------------------------------------------------------ workspace layouts
 struct PrefillLayout {
-    size_t ctrl, chunk_counts, chunk_base, h, xh, logits, idx, w, counts, offsets, perm, block_map, n_blocks, total;
+    size_t ctrl, chunk_counts, chunk_base, h, xs, logits, idx, w, counts, offsets, perm, block_map, n_blocks, total;
 };
 
 int64_t block_capacity(const lily_moe_shape &s)
@@ -58,7 +58,7 @@ PrefillLayout prefill_layout(const lily_moe_shape &s)
     L.chunk_counts = take(C * E * 4);
     L.chunk_base = take(C * E * 4);
     L.h = take((k + 1) * T * s.I * 2);
-    L.xh = take(T * s.d * 2);
+    L.xs = take((k + 1) * T * s.d * 2);
     L.logits = take(T * E * 4);
     L.idx = take(T * k * 4);
     L.w = take(T * k * 4);
@@ -290,17 +290,17 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
     const PrefillLayout L = prefill_layout(s);
     Ctrl *ctrl = at<Ctrl>(ws, L.ctrl);
     __half *h = at<__half>(ws, L.h);
-    __half *xh = at<__half>(ws, L.xh);
+    __half *xs = at<__half>(ws, L.xs);
     const int64_t hrows = static_cast<int64_t>(s.top_k + 1) * s.T;
-    CUtensorMap tmX, tmH, tmG, tmU, tmD, tmSG, tmSU, tmSD;
-    if (!tmap_bf16_sw128(&tmX, x, s.d, s.T) || !tmap_f16_sw128(&tmH, h, s.I, hrows) ||
+    CUtensorMap tmXs, tmH, tmG, tmU, tmD, tmSG, tmSU, tmSD;
+    if (!tmap_f16_sw128(&tmXs, xs, s.d, hrows) || !tmap_f16_sw128(&tmH, h, s.I, hrows) ||
         !tmap_q4(&tmG, w.gate.q, s.d, static_cast<uint64_t>(s.E) * s.I) ||
         !tmap_q4(&tmU, w.up.q, s.d, static_cast<uint64_t>(s.E) * s.I) ||
         !tmap_q4(&tmD, w.down.q, s.I, static_cast<uint64_t>(s.E) * s.d) || !tmap_q4(&tmSG, w.sh_gate.q, s.d, s.I) ||
         !tmap_q4(&tmSU, w.sh_up.q, s.d, s.I) || !tmap_q4(&tmSD, w.sh_down.q, s.I, s.d))
         return cudaErrorInvalidValue;
 
-    cudaError_t e = launch_prep_experts(x, xh, out, static_cast<int64_t>(s.T) * s.d, stream);
+    cudaError_t e = launch_prep_experts(x, r.perm, xs, out, s.T, s.d, s.top_k, &ctrl->status, stream);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[3], stream)) != cudaSuccess) return e;
 
@@ -315,7 +315,7 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
     g.block_map = r.block_map;
     g.perm = r.perm;
     g.topk_w = r.topk_w;
-    g.xh = xh;
+    g.xs = xs;
     g.h = h;
     g.out = out;
     g.ctrl = ctrl;
@@ -329,7 +329,7 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
     g.ss0 = w.sh_gate.scale; g.sb0 = w.sh_gate.bias; g.ss1 = w.sh_up.scale; g.sb1 = w.sh_up.bias;
     int64_t units = (cap + g.n_shared_blocks) * g.m_tiles;
     int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, units)));
-    if ((e = launch_grouped_gemm(g, tmX, tmG, tmU, tmSG, tmSU, grid, stream)) != cudaSuccess) return e;
+    if ((e = launch_grouped_gemm(g, tmXs, tmG, tmU, tmSG, tmSU, grid, stream)) != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[4], stream)) != cudaSuccess) return e;
 
     // down + weighted combine

@@ -17,9 +17,9 @@
 // One CTA per SM loops over work units:
 //   warp 0        A-side producer: TMA of the packed int4 tiles (expert modes)
 //                 or of the bf16 router weights;
-//   warps 2-3     B producer: one TMA per k-step for contiguous rows (router x,
-//                 down h), or cp.async gathers of token rows of x by the
-//                 routing permutation (gate/up);
+//   warp 2        B producer: 2-D TMA of contiguous token rows: x (router),
+//                 x in routing order (gate/up; written by the prep kernel),
+//                 h (down);
 //   warp 1        TMEM allocator + single-thread tcgen05.mma issuer;
 //   warps 4..11   dequantisers (expert modes): int4 -> fp16, one row per
 //                 thread, each warp 32 rows of one matrix on its own pace,
@@ -50,9 +50,10 @@ constexpr int kThreads = 640;  // 20 warps: 4 producer/MMA, 8 dequant, 8 epilogu
 constexpr int kBlk = 4;        // k-steps per block: one raw stage, one tensor-memory A ring cycle
 constexpr int kRStages = 2;    // raw int4 ring (TMA), one block per stage
 constexpr int kBStages = 4;    // B ring in the dedicated buffers (router)
-constexpr int kBStagesX = 8;   // expert modes: 4 more B stages in the shared-memory A buffers they do not use
+constexpr int kBSlotBars = 4;  // B ring slots (router: 4 x 1 k-step; expert modes: 4 x 2 k-steps, the last
+                               // two in the shared-memory A buffers they do not use)
 constexpr int kAStages = 2;    // shared-memory A ring (bf16 router weights by TMA)
-constexpr int kTAStages = 4;   // tensor-memory A ring (fp16 dequantised weights, expert modes) = kBlk
+constexpr int kTAStages = 2;   // tensor-memory A ring (expert modes: 2 stages of 2 k-steps) / router A ring
 constexpr int kTileM = 128;
 constexpr int kBK = 64;        // one quantisation group, one 128-byte swizzle row
 constexpr int kTileN = 128;
@@ -62,32 +63,31 @@ constexpr int kRawRow = kBlk * kBK / 2;      // 128 B of packed int4 per row per
 constexpr int kRawBytes = kTileM * kRawRow;  // 16 KB int4 per matrix
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: accumulators at [0, 256) per buffer (router: two buffers, [0, 512));
-// expert modes: one accumulator buffer and the A ring at [256, 512), 64 columns per stage.
+// expert modes: one accumulator buffer and the A ring at [256, 512): stage h at
+// 256 + 128 h, matrix m at + 64 m, k-step j of the stage at + 32 j.
 constexpr uint32_t kTmemAOffset = 256;
-constexpr int kBarEpilogue = 3, kBarBProducer = 4;  // named barrier ids
-static_assert(kTAStages == kBlk, "one tensor-memory A stage per k-step of a block");
-static_assert(kBStagesX == 2 * kBlk && kBStages == kBlk && kAStages == 2, "ring slots are compile-time within a block");
+constexpr int kBarEpilogue = 3;  // named barrier id
+static_assert(kBStages == kBlk && kAStages == 2 && kTAStages == 2, "ring slots are compile-time within a block");
 
 struct __align__(1024) Smem {
     uint8_t b[kBStages][kBBytes];         // B ring; expert modes continue into `a`
     uint8_t a[kAStages][2][kABytes];      // router: bf16 A ring; expert modes: B stages 4..7
     uint8_t raw[kRStages][2][kRawBytes];
     uint64_t full_r[kRStages], empty_r[kRStages];
-    uint64_t full_b[kBStagesX], empty_b[kBStagesX];
+    uint64_t full_b[kBSlotBars], empty_b[kBSlotBars];
     uint64_t full_a[kTAStages], empty_a[kTAStages];
     uint64_t full_acc[2], empty_acc[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    int prod_tok[kTileN];  // B producers: source row of each B row of the current unit
     int ep_go;             // epilogue's wait result, published by its waiting thread
     int ep_tok[kTileN];    // epilogue: token of each column (down)
     float ep_w[kTileN];    // epilogue: routing weight of each column (down)
 };
 static_assert(sizeof(Smem) + 1024 <= 200 * 1024, "shared memory budget of one CTA");
 static_assert(offsetof(Smem, a) == offsetof(Smem, b) + sizeof(Smem::b) &&
-                  sizeof(Smem::a) == (kBStagesX - kBStages) * kBBytes,
-              "expert-mode B stages 4..7 continue the B ring in the A buffers");
+                  sizeof(Smem::a) == sizeof(Smem::b),
+              "expert-mode B slots 2..3 continue the B ring in the A buffers");
 
 struct Unit {
     int e, p0, rows, n_mma, mt;
@@ -167,11 +167,12 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, int depth, int issued
     }
 }
 
-// B stage i (0..7): stages 0..3 in the dedicated buffers, 4..7 (expert modes)
-// in the shared-memory A buffers that follow them.
+// B slot i of SS k-steps: slots continue from the dedicated buffers into the
+// shared-memory A buffers (expert modes: 4 slots of 2 k-steps = 128 KB).
+template <int SS>
 __device__ __forceinline__ uint8_t *b_stage(Smem &S, int i)
 {
-    return reinterpret_cast<uint8_t *>(&S) + offsetof(Smem, b) + static_cast<size_t>(i) * kBBytes;
+    return reinterpret_cast<uint8_t *>(&S) + offsetof(Smem, b) + static_cast<size_t>(i) * SS * kBBytes;
 }
 
 template <int MODE>
@@ -186,16 +187,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     const int lane = threadIdx.x & 31;
     int *status = &g.ctrl->status;
     constexpr bool dequant_mode = MODE != kModeRouter;
-    constexpr bool gather_b = MODE == kModeGateUp;
-    constexpr int b_stages = dequant_mode ? kBStagesX : kBStages;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRStages; ++s) {
             mbar_init(&S.full_r[s], 1);
             mbar_init(&S.empty_r[s], 8);  // the eight dequantiser warps
         }
-        for (int s = 0; s < kBStagesX; ++s) {
-            mbar_init(&S.full_b[s], gather_b ? 64 : 1);
+        for (int s = 0; s < kBSlotBars; ++s) {
+            mbar_init(&S.full_b[s], 1);
             mbar_init(&S.empty_b[s], 1);
         }
         for (int s = 0; s < kTAStages; ++s) {
@@ -214,7 +213,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA0);
         prefetch_tmap(&tmA1);
-        if (!gather_b) prefetch_tmap(&tmB);
+        prefetch_tmap(&tmB);
         if (dequant_mode) {
             prefetch_tmap(&tmSA0);
             prefetch_tmap(&tmSA1);
@@ -246,13 +245,20 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     // multi-warp groups keep walking their loops (skipping work) so that every
     // thread still reaches every named barrier of its group.
     //
-    // Ring bookkeeping: `blk` counts blocks over all units of this CTA.  Raw
-    // stage = blk % 2 (phase (blk / 2) % 2); tensor-memory A stage = k-step of
-    // the block (full phase blk % 2; it is free again once the MMAs of the
-    // k-step four back, in B slot 4 ((blk - 1) % 2) + k-step, completed);
-    // router shared-memory A stage = k-step % 2 (phase k-step / 2); B stage =
-    // k-step (router, phase blk % 2) or 4 (blk % 2) + k-step (expert modes,
-    // phase (blk / 2) % 2).
+    // Ring bookkeeping: `blk` counts blocks of four k-steps over all units of
+    // this CTA; a block holds SPB stages of SS k-steps (expert modes: 2 stages
+    // of 2 k-steps; router: 4 stages of 1).  Raw stage = blk % 2 (phase
+    // (blk / 2) % 2).  Expert modes: tensor-memory A stage h (phase blk % 2),
+    // free again once the MMAs of the same stage one block back completed,
+    // i.e. B slot 2 ((blk - 1) % 2) + h (phase ((blk - 1) / 2) % 2); B slot
+    // 2 (blk % 2) + h (phase (blk / 2) % 2).  Router: shared-memory A stage
+    // = k-step % 2 (phase k-step / 2); B slot = k-step (phase blk % 2).
+    constexpr int SS = dequant_mode ? 2 : 1;  // k-steps per stage
+    constexpr int SPB = kBlk / SS;            // stages per block
+    // B slots: router 4 x 1 k-step, expert modes 4 x 2 k-steps (two blocks per
+    // ring cycle)
+    constexpr int NSLOT = 4;
+    constexpr int CYC = NSLOT / SPB;  // blocks per B ring cycle (1 or 2)
     if (warp == 0) {
         // ------------------------------------------------ A-side producer (one thread)
         if (lane == 0) {
@@ -304,106 +310,48 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     } else if (warp == 2 || warp == 3) {
         // ------------------------------------------------ B producers (token rows)
         const int bl = (warp - 2) * 32 + lane;  // 0..63
-        if (gather_b) {
-            // two warps gather token rows of fp16 x with 16-byte cp.async into the
-            // 128-byte-swizzled layout; the copy hardware arrives on the stage's
-            // full barrier (64 arrivals) once each lane's copies have landed
-            int blk = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-                const Unit u = unit_info<MODE>(g, tile, n_routed);
-                if (u.rows <= 0) continue;
-                named_barrier_sync(kBarBProducer, 64);  // previous unit's rows no longer read
-                for (int r = bl; r < u.n_mma; r += 64) {
-                    const int rr = min(r, u.rows - 1);
-                    int src = u.p0 + rr;
-                    if (!u.shared) src = g.perm[u.p0 + rr] / g.top_k;
-                    if (src < 0 || src >= g.T) {
-                        record_error(status, kErrDeviceIndex);
-                        src = 0;
-                    }
-                    S.prod_tok[r] = src;
-                }
-                named_barrier_sync(kBarBProducer, 64);
-                {
-                    // warm L2 with the token rows of this CTA's next unit
-                    const int nt = tile + gridDim.x;
-                    if (nt < total_tiles) {
-                        const Unit un = unit_info<MODE>(g, nt, n_routed);
-                        for (int r = bl; r < un.rows; r += 64) {
-                            int src = un.shared ? un.p0 + r : g.perm[un.p0 + r] / g.top_k;
-                            if (src >= 0 && src < g.T)
-                                bulk_prefetch_l2(g.xh + static_cast<size_t>(src) * g.d, static_cast<uint32_t>(g.d) * 2u);
-                        }
-                    }
-                }
-                // this lane copies 16-byte chunk c of B rows (bl / 8) + 8 i, i < 16; the
-                // source rows live in registers for the whole unit, and chunk c of
-                // row r lands at chunk c ^ (r % 8) = c ^ (bl / 8) of its 128-byte row
-                const int c = bl & 7;
-                const int r0 = bl >> 3;
-                const uint32_t dst0 = static_cast<uint32_t>(r0 * 128 + ((c ^ r0) << 4));
-                int tok[kTileN / 8];
-#pragma unroll
-                for (int i = 0; i < kTileN / 8; ++i) tok[i] = S.prod_tok[min(r0 + 8 * i, u.n_mma - 1)];
-                for (int kb = 0; kb < KB; ++kb, ++blk) {
-                    const int bs0 = (blk & 1) * kBlk;
-                    const uint32_t bpar = (blk >> 1) & 1;
-#pragma unroll
-                    for (int jr = 0; jr < kBlk; ++jr) {
-                        int good = 0;
-                        if (ok) {
-                            if (lane == 0) good = mbar_wait(&S.empty_b[bs0 + jr], bpar ^ 1, abort_flag, status);
-                            good = __shfl_sync(0xffffffffu, good, 0);
-                            if (!good) ok = false;
-                        }
-                        if (good) {
-                            const __half *xk = g.xh + (kb * kBlk + jr) * kBK + c * 8;
-                            uint8_t *bst = b_stage(S, bs0 + jr) + dst0;
-#pragma unroll
-                            for (int i = 0; i < kTileN / 8; ++i)
-                                if (r0 + 8 * i < u.n_mma) cp_async_16(bst + i * 1024, xk + static_cast<size_t>(tok[i]) * g.d);
-                            cp_async_mbar_arrive_noinc(&S.full_b[bs0 + jr]);
-                        }
-                    }
-                }
-            }
-            cp_async_wait_all();  // no copy into shared memory in flight at exit
-        } else if (bl == 0) {
-            // contiguous rows (x for the router, h for the down projection): one 2-D TMA per k-step
+        if (bl == 0) {
+            // contiguous rows (x for the router; x in routing order for gate/up; h for
+            // the down projection): one 2-D TMA per k-step
             int blk = 0, issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 const Unit u = unit_info<MODE>(g, tile, n_routed);
                 if (u.rows <= 0) continue;
-                const int b_row0 = (MODE == kModeDown && u.shared) ? g.T * g.top_k + u.p0 : u.p0;
-                if (MODE == kModeDown) {
-                    // warm L2 with the h rows of this CTA's next unit (contiguous rows)
+                // expert modes: routed rows in routing order, then the shared expert's
+                // rows (token order) after the T * top_k routed rows
+                const int b_row0 = (dequant_mode && u.shared) ? g.T * g.top_k + u.p0 : u.p0;
+                if (dequant_mode) {
+                    // warm L2 with the B rows of this CTA's next unit (contiguous rows)
                     const int nt = tile + gridDim.x;
                     if (nt < total_tiles) {
                         const Unit un = unit_info<MODE>(g, nt, n_routed);
                         if (un.rows > 0) {
                             const size_t row0 = un.shared ? static_cast<size_t>(g.T) * g.top_k + un.p0 : un.p0;
-                            bulk_prefetch_l2(g.h + row0 * g.I, static_cast<uint32_t>(un.rows) * g.I * 2u);
+                            const __half *src = MODE == kModeGateUp ? g.xs : g.h;
+                            bulk_prefetch_l2(src + row0 * g.K, static_cast<uint32_t>(un.rows) * g.K * 2u);
                         }
                     }
                 }
                 for (int kb = 0; kb < KB && ok; ++kb, ++blk) {
-                    const int bs0 = dequant_mode ? (blk & 1) * kBlk : 0;
-                    const uint32_t bpar = dequant_mode ? ((blk >> 1) & 1) : (blk & 1);
+                    const uint32_t bpar = (CYC == 2 ? (blk >> 1) : blk) & 1;
 #pragma unroll
-                    for (int jr = 0; jr < kBlk; ++jr) {
-                        if (!mbar_wait(&S.empty_b[bs0 + jr], bpar ^ 1, abort_flag, status)) {
+                    for (int h = 0; h < SPB; ++h) {
+                        const int bs = (CYC == 2 ? (blk & 1) : 0) * SPB + h;
+                        if (!mbar_wait(&S.empty_b[bs], bpar ^ 1, abort_flag, status)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&S.full_b[bs0 + jr], kBBytes);
-                        tma_load_2d(b_stage(S, bs0 + jr), &tmB, &S.full_b[bs0 + jr], (kb * kBlk + jr) * kBK, b_row0);
+                        mbar_arrive_expect_tx(&S.full_b[bs], SS * kBBytes);
+#pragma unroll
+                        for (int j = 0; j < SS; ++j)
+                            tma_load_2d(b_stage<SS>(S, bs) + j * kBBytes, &tmB, &S.full_b[bs], (kb * kBlk + h * SS + j) * kBK,
+                                        b_row0);
                         ++issued;
                     }
                 }
             }
-            drain_ring(S.full_b, b_stages, issued, status);
+            drain_ring(S.full_b, NSLOT, issued, status);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -414,7 +362,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             bool ok = true;
             const uint32_t fmt = dequant_mode ? kFmtF16 : kFmtBF16;
             const int n_acc = dequant_mode ? 1 : 2;  // accumulator buffers in TMEM
-            const uint64_t bd0 = sdesc_sw128(smem_u32(b_stage(S, 0)));
+            const uint64_t bd0 = sdesc_sw128(smem_u32(b_stage<SS>(S, 0)));
             const uint32_t b_lo = static_cast<uint32_t>(bd0), b_hi = static_cast<uint32_t>(bd0 >> 32);
             const uint64_t ad0 = sdesc_sw128(smem_u32(S.a[0][0]));
             const uint32_t a_lo = static_cast<uint32_t>(ad0), a_hi = static_cast<uint32_t>(ad0 >> 32);
@@ -428,43 +376,45 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(ab * 2 * kTileM);
                 const uint32_t d1 = d0 + kTileM;
                 for (int kb = 0; kb < KB && ok; ++kb, ++blk) {
-                    const int bs0 = dequant_mode ? (blk & 1) * kBlk : 0;
-                    const uint32_t bpar = dequant_mode ? ((blk >> 1) & 1) : (blk & 1);
-                    const uint32_t apar = blk & 1;
+                    const uint32_t bpar = (CYC == 2 ? (blk >> 1) : blk) & 1;
 #pragma unroll
-                    for (int jr = 0; jr < kBlk; ++jr) {
-                        const int as = dequant_mode ? jr : (jr & 1);
-                        const uint32_t ap = dequant_mode ? apar : ((jr >> 1) & 1);
-                        if (!mbar_wait2(&S.full_a[as], ap, &S.full_b[bs0 + jr], bpar, abort_flag, status)) {
+                    for (int h = 0; h < SPB; ++h) {
+                        const int bs = (CYC == 2 ? (blk & 1) : 0) * SPB + h;
+                        const int as = dequant_mode ? h : (h & 1);
+                        const uint32_t ap = dequant_mode ? (blk & 1) : ((h >> 1) & 1);
+                        if (!mbar_wait2(&S.full_a[as], ap, &S.full_b[bs], bpar, abort_flag, status)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        if (gather_b) fence_proxy_async_smem();  // gathered rows were written by cp.async
-                        const uint32_t blo = b_lo + static_cast<uint32_t>((bs0 + jr) * (kBBytes >> 4));
-                        if (dequant_mode) {
-                            // A from tensor memory: 64 K elements of a stage = 32 columns per matrix
-                            const uint32_t at = ta + static_cast<uint32_t>(jr * 64);
 #pragma unroll
-                            for (int kk = 0; kk < kBK / 16; ++kk) {
-                                const uint32_t acc = (kb | jr | kk) != 0;
-                                umma_ts(d0, at + kk * 8, desc64(blo + kk * 2, b_hi), idesc, acc);
-                                umma_ts(d1, at + 32 + kk * 8, desc64(blo + kk * 2, b_hi), idesc, acc);
-                            }
-                        } else {
-                            const uint32_t alo = a_lo + static_cast<uint32_t>(as * (2 * kABytes >> 4));
+                        for (int j = 0; j < SS; ++j) {
+                            const uint32_t blo = b_lo + static_cast<uint32_t>((bs * SS + j) * (kBBytes >> 4));
+                            if (dequant_mode) {
+                                // A from tensor memory: stage h at 128 h, matrix m at + 64 m,
+                                // k-step j at + 32 j (64 K elements = 32 columns)
+                                const uint32_t at = ta + static_cast<uint32_t>(h * 128 + j * 32);
 #pragma unroll
-                            for (int kk = 0; kk < kBK / 16; ++kk) {
-                                const uint32_t acc = (kb | jr | kk) != 0;
-                                umma_ss(d0, desc64(alo + kk * 2, a_hi), desc64(blo + kk * 2, b_hi), idesc, acc);
-                                umma_ss(d1, desc64(alo + (kABytes >> 4) + kk * 2, a_hi), desc64(blo + kk * 2, b_hi), idesc,
-                                        acc);
+                                for (int kk = 0; kk < kBK / 16; ++kk) {
+                                    const uint32_t acc = (kb | h | j | kk) != 0;
+                                    umma_ts(d0, at + kk * 8, desc64(blo + kk * 2, b_hi), idesc, acc);
+                                    umma_ts(d1, at + 64 + kk * 8, desc64(blo + kk * 2, b_hi), idesc, acc);
+                                }
+                            } else {
+                                const uint32_t alo = a_lo + static_cast<uint32_t>(as * (2 * kABytes >> 4));
+#pragma unroll
+                                for (int kk = 0; kk < kBK / 16; ++kk) {
+                                    const uint32_t acc = (kb | h | kk) != 0;
+                                    umma_ss(d0, desc64(alo + kk * 2, a_hi), desc64(blo + kk * 2, b_hi), idesc, acc);
+                                    umma_ss(d1, desc64(alo + (kABytes >> 4) + kk * 2, a_hi), desc64(blo + kk * 2, b_hi),
+                                            idesc, acc);
+                                }
                             }
                         }
-                        // expert modes: one release per k-step; the dequantisers wait on the
-                        // B slot of the k-step four back, whose MMAs read the same A stage
+                        // expert modes: one release per stage; the dequantisers wait on the
+                        // B slot of the same stage one block back
                         if (!dequant_mode) umma_commit(&S.empty_a[as]);
-                        umma_commit(&S.empty_b[bs0 + jr]);
+                        umma_commit(&S.empty_b[bs]);
                     }
                 }
                 if (!ok) break;
@@ -489,7 +439,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             const bool vec8 = (ngroups & 7) == 0;
             // this warp's TMEM lane quarter holds rows [32 * (warp % 4), +32)
             const uint32_t ta_row = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kTmemAOffset +
-                                    static_cast<uint32_t>(mi * 32);
+                                    static_cast<uint32_t>(mi * 64);
             int blk = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -530,47 +480,53 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     const int jb = (kb & 1) * kBlk;  // first group of this block within the register block
                     const uint8_t *rowp = S.raw[rs][mi] + r * kRawRow;
 #pragma unroll
-                    for (int jr = 0; jr < kBlk; ++jr) {
+                    for (int h = 0; h < SPB; ++h) {
                         // Each warp runs on its own: lane 0 polls the mbarriers and
                         // broadcasts the result.
                         int go = 0;
                         if (lane == 0) {
                             bool w = ok;
-                            if (w && jr == 0) w = mbar_wait(&S.full_r[rs], rpar, abort_flag, status);
-                            // TMEM A stage jr was last read by the MMAs of the k-step four
-                            // back, which released B slot (bs0 ^ 4) + jr
-                            if (w) w = mbar_wait(&S.empty_b[((blk & 1) ^ 1) * kBlk + jr], ((blk - 1) >> 1) & 1, abort_flag, status);
+                            if (w && h == 0) w = mbar_wait(&S.full_r[rs], rpar, abort_flag, status);
+                            // TMEM A stage h was last read by the MMAs of the same stage one
+                            // block back, which released that block's B slot h
+                            if (w)
+                                w = mbar_wait(&S.empty_b[(CYC == 2 ? ((blk & 1) ^ 1) : 0) * SPB + h],
+                                              (CYC == 2 ? ((blk - 1) >> 1) : (blk - 1)) & 1, abort_flag, status);
                             go = w;
                         }
                         const bool got = __shfl_sync(0xffffffffu, go, 0) != 0;
                         if (!got) ok = false;
-                        tc_fence_after();  // the MMAs that read this TMEM stage are complete (empty_a)
+                        tc_fence_after();  // the MMAs that read this TMEM stage are complete
                         if (got) {
-                            const uint16_t sc = pick16(s_cur, jb + jr), bi = pick16(b_cur, jb + jr);
-                            // 128-byte rows written by TMA with the 128-byte swizzle:
-                            // 16-byte chunk c of row r sits at chunk c ^ (r % 8)
-                            const uint4 q0 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr) ^ sw) << 4));
-                            const uint4 q1 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr + 1) ^ sw) << 4));
-                            const __half2 s2 = half2_from_bf16_bits(sc), b2 = half2_from_bf16_bits(bi);
-                            const __half2 s2_16 = __hmul2(s2, __floats2half2_rn(0.0625f, 0.0625f));
-                            const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                            uint32_t cols[32];  // TMEM column 4c + j holds K positions 8c + 2j, 8c + 2j + 1
 #pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                const uint4 o = dequant8_f16_kperm(words[c], s2, s2_16, b2);
-                                cols[4 * c + 0] = o.x;
-                                cols[4 * c + 1] = o.y;
-                                cols[4 * c + 2] = o.z;
-                                cols[4 * c + 3] = o.w;
+                            for (int j = 0; j < SS; ++j) {
+                                const int jr = h * SS + j;  // k-step within the block
+                                const uint16_t sc = pick16(s_cur, jb + jr), bi = pick16(b_cur, jb + jr);
+                                // 128-byte rows written by TMA with the 128-byte swizzle:
+                                // 16-byte chunk c of row r sits at chunk c ^ (r % 8)
+                                const uint4 q0 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr) ^ sw) << 4));
+                                const uint4 q1 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr + 1) ^ sw) << 4));
+                                const __half2 s2 = half2_from_bf16_bits(sc), b2 = half2_from_bf16_bits(bi);
+                                const __half2 s2_16 = __hmul2(s2, __floats2half2_rn(0.0625f, 0.0625f));
+                                const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                                uint32_t cols[32];  // TMEM column 4c + i holds K positions 8c + 2i, 8c + 2i + 1
+#pragma unroll
+                                for (int cc = 0; cc < 8; ++cc) {
+                                    const uint4 o = dequant8_f16_kperm(words[cc], s2, s2_16, b2);
+                                    cols[4 * cc + 0] = o.x;
+                                    cols[4 * cc + 1] = o.y;
+                                    cols[4 * cc + 2] = o.z;
+                                    cols[4 * cc + 3] = o.w;
+                                }
+                                tmem_st_32x32b_x32(ta_row + static_cast<uint32_t>(h * 128 + j * 32), cols);
                             }
-                            tmem_st_32x32b_x32(ta_row + static_cast<uint32_t>(jr * 64), cols);
                             tmem_st_wait();
                             tc_fence_before();
                         }
                         __syncwarp();
                         if (lane == 0 && ok) {
-                            mbar_arrive(&S.full_a[jr]);
-                            if (jr == kBlk - 1) mbar_arrive(&S.empty_r[rs]);
+                            mbar_arrive(&S.full_a[h]);
+                            if (h == SPB - 1) mbar_arrive(&S.empty_r[rs]);
                         }
                     }
                 }
@@ -695,19 +651,33 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-// Before the expert GEMMs: xh = fp16(x) with K permuted inside each group of 8
-// (the order the dequantisers write the weights in), and out = 0.
-__global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, uint4 *xh, float4 *out, int64_t n8)
+// Before the expert GEMMs: xs = fp16(x) in routing order with K permuted
+// inside each group of 8 (the order the dequantisers write the weights in):
+// row p < T top_k is token perm[p] / top_k, row T top_k + t is token t (the
+// shared expert's rows); and out = 0.  Flat grid-stride loop, 8 elements per
+// thread and iteration, so the 16-byte stores stream in order.
+__global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, const int *perm, uint4 *xs, float4 *out,
+                                                           int T, int d8, int top_k, int *status)
 {
-    for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n8; i += static_cast<int64_t>(gridDim.x) * 256) {
-        const uint4 v = x[i];
+    const int64_t routed = static_cast<int64_t>(T) * top_k;
+    const int64_t n = (routed + T) * d8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * 256;
+    for (int64_t q = blockIdx.x * 256LL + threadIdx.x; q < n; q += stride) {
+        const int64_t p = q / d8;
+        const int i = static_cast<int>(q - p * d8);
+        int t = p < routed ? __ldg(perm + p) / top_k : static_cast<int>(p - routed);
+        if (t < 0 || t >= T) {
+            record_error(status, kErrDeviceIndex);
+            t = 0;
+        }
+        const uint4 v = __ldg(x + static_cast<int64_t>(t) * d8 + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         float f[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
-            f[2 * j] = p.x;
-            f[2 * j + 1] = p.y;
+            const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
+            f[2 * j] = qq.x;
+            f[2 * j + 1] = qq.y;
         }
         uint32_t o[4];
 #pragma unroll
@@ -715,26 +685,25 @@ __global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, uint4
             const __half2 hv = __floats2half2_rn(f[j], f[j + 4]);
             o[j] = *reinterpret_cast<const uint32_t *>(&hv);
         }
-        xh[i] = make_uint4(o[0], o[1], o[2], o[3]);
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        out[2 * i] = z;
-        out[2 * i + 1] = z;
+        xs[q] = make_uint4(o[0], o[1], o[2], o[3]);
     }
+    const int64_t n4 = static_cast<int64_t>(T) * d8 * 2;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t q = blockIdx.x * 256LL + threadIdx.x; q < n4; q += stride) out[q] = z;
 }
 
 }  // namespace
 
-cudaError_t launch_prep_experts(const uint16_t *x, __half *xh, float *out, int64_t n_elems, cudaStream_t stream)
+cudaError_t launch_prep_experts(const uint16_t *x, const int *perm, __half *xs, float *out, int T, int d, int top_k,
+                                int *status, cudaStream_t stream)
 {
-    const int64_t n8 = n_elems / 8;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t want = (n8 + 255) / 256;
-    const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sms) * 8));
-    prep_experts_kernel<<<grid > 0 ? grid : 1, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(x),
-                                                                reinterpret_cast<uint4 *>(xh),
-                                                                reinterpret_cast<float4 *>(out), n8);
+    const int64_t n = static_cast<int64_t>(T) * (top_k + 1) * (d / 8);
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(sms) * 16)));
+    prep_experts_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(x), perm, reinterpret_cast<uint4 *>(xs),
+                                                  reinterpret_cast<float4 *>(out), T, d / 8, top_k, status);
     return cudaGetLastError();
 }
 

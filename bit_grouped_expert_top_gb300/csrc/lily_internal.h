@@ -38,7 +38,7 @@ struct GemmArgs {
     // and shared (ss*, sb*) weights; rows of K/64 groups.
     const uint16_t *s0, *b0, *s1, *b1, *ss0, *sb0, *ss1, *sb1;
     const float *router_bias;
-    const __half *xh;        // gate/up gather source: x converted to fp16 [T][d]
+    const __half *xs;        // gate/up B: fp16 x in routing order [(top_k+1)*T][d] (routed rows, then shared)
     float *logits;           // router output [T][E]
     __half *h;               // gate/up output, down input, fp16 [(top_k+1)*T][I]
     float *out;              // down output [T][d], accumulated
@@ -48,10 +48,12 @@ struct GemmArgs {
 // Dynamic shared memory bytes of grouped_gemm_kernel.
 size_t grouped_gemm_smem_bytes();
 
-// Before the expert GEMMs: out = 0 and xh = fp16(x)  (T x d elements).
-cudaError_t launch_prep_experts(const uint16_t *x, __half *xh, float *out, int64_t n_elems, cudaStream_t stream);
+// Before the expert GEMMs: out = 0 and xs = fp16(x) in routing order (routed
+// rows by perm, then the T shared-expert rows), [(top_k+1)*T][d].
+cudaError_t launch_prep_experts(const uint16_t *x, const int *perm, __half *xs, float *out, int T, int d, int top_k,
+                                int *status, cudaStream_t stream);
 
-// tmB: B operand (x for router, h for down; unused for gate/up which gathers x).
+// tmB: B operand rows (x for the router, xs for gate/up, h for down).
 // tmA0/tmA1: routed weight maps of the two 128-row tiles (router: Wr for both);
 // tmSA0/tmSA1: shared-expert weight maps.
 cudaError_t launch_grouped_gemm(const GemmArgs &g, const CUtensorMap &tmB, const CUtensorMap &tmA0,
