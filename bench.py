@@ -32,6 +32,31 @@ METRIC = "MoE-layer prefill tokens/s @T=2048/8192; decode µs/layer; % of roofli
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def gateup_traffic():
+    """DRAM bytes per gate/up launch from the committed ncu summary, or None when
+    the kernel sources changed since the counters were taken."""
+    import hashlib
+    try:
+        txt = open(os.path.join(ROOT, "profiles", "grouped_gemm_t8192_dram.md")).read()
+        csrc = os.path.join(ROOT, "bit_grouped_expert_top_gb300", "csrc")
+        h = hashlib.sha256()
+        for f in ("grouped_gemm.cu", "lily_device.cuh"):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    except OSError:
+        return None
+    vals = {}
+    for ln in txt.splitlines():
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_prefix") != h.hexdigest()[:16]:
+        return None
+    try:
+        return int(vals["traffic_bytes_per_launch gateup"])
+    except (KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -322,14 +347,15 @@ def run_ours(args):
         "stage_us": {k: round(v, 2) for k, v in st.items()},
         "roofline": {"kernel": "grouped_gemm_kernel (gate/up + SwiGLU)", "bound": "tensor",
                      "achieved": round(achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak_tc, 4), "traffic": None,
+                     "frac": round(achieved / peak_tc, 4), "traffic": gateup_traffic(),
+                     "traffic_unit": "bytes per launch (ncu dram read+write, profiles/grouped_gemm_t8192_dram.md)",
                      "peak_note": f"{peaks['source']} bf16 sustained (fp16 dense rate = bf16 rate)",
                      "algorithmic_flops_per_launch": flops_gu},
         "layer_tflops": round(flops_total / (ms * 1e-3) / 1e12, 1),
         "clocks": clocks,
         "e2e": {"value": round(cfg.T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 4},
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": 7 * args.steps,  # router GEMM, top-8, scan, scatter, prep, gate/up, down
         "also": also,
     }
     if rank == 0:

@@ -1,0 +1,43 @@
+"""Runs a few whole-layer forward passes of one seeded workload, for profilers.
+
+  python -m bit_grouped_expert_top_gb300.profile_run --config prefill_t8192 --reps 2
+
+Each pass launches, in order: router GEMM, top-8 + per-chunk counts, per-expert
+scan + block map, scatter, prep (fp16 x in routing order, out = 0), gate/up
+GEMM + SwiGLU, down GEMM + weighted combine.  Exits non-zero if the device
+status word reports an error.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import torch
+
+import bit_grouped_expert_top_gb300 as lm
+from bit_grouped_expert_top_gb300.inputs import CONFIGS, make_layer, make_x
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--config", default="prefill_t2048_zipf", choices=sorted(k for k in CONFIGS if k.startswith("prefill")))
+    ap.add_argument("--reps", type=int, default=2)
+    a = ap.parse_args(argv)
+    cfg = CONFIGS[a.config]
+    layer = make_layer(cfg, "cuda")
+    w = lm.make_weights(layer)
+    x = make_x(cfg, "cuda")
+    s = lm.make_shape(T=cfg.T, d=cfg.d, E=cfg.E, top_k=cfg.top_k, I=cfg.I, I_shared=cfg.I_shared,
+                      group=cfg.group, block_rows=cfg.block_rows)
+    ws = lm.alloc_workspace(s)
+    out = torch.empty((cfg.T, cfg.d), device="cuda")
+    for _ in range(a.reps):
+        lm.lily_moe_forward(s, w, x, out, ws)
+    torch.cuda.synchronize()
+    st = lm.lily_moe_device_status(ws)
+    print(f"{a.config}: {a.reps} forward passes, device status {st}")
+    return 0 if st == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
