@@ -14,12 +14,15 @@
 //                       last CTA the top-8 selection per token and the list of
 //                       distinct experts ("units") with per-token weights; the
 //                       shared expert is the last unit with weight 1.
-//   dec_gateup_kernel : one warp per (unit, intermediate row): gate and up rows
-//                       dequantised and dotted with the unit's tokens, SwiGLU,
-//                       h stored as fp16.
-//   dec_down_kernel   : one warp per output row: the down rows of every unit,
-//                       dotted with h, scaled by the routing weight and summed
-//                       in registers (deterministic, no atomics).
+//   dec_gateup_kernel : tensor-core GEMV (mma.sync m16n8k16, the tokens as the
+//                       8 columns): per unit and 32 rows of I, gate and up
+//                       dequantised in registers, SwiGLU, scaled by the unit's
+//                       routing weight per token, h' stored as fp16.
+//   dec_down_kernel   : tensor-core GEMV over K = units x I: per 16 output
+//                       rows, sum over the units of Wd h' (deterministic, no
+//                       atomics).
+#include <algorithm>
+
 #include "lily_device.cuh"
 #include "lily_internal.h"
 
@@ -29,51 +32,6 @@ namespace {
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMaxT = 8;
-constexpr int kChunk = 32;       // weights per 16-byte int4 chunk
-constexpr int kPadChunk = 40;    // bf16 elements per chunk slot in shared memory (80 B: bank-conflict-free)
-
-// Shared-memory copy of activations: [rows][n_chunks][kPadChunk] bf16.
-__device__ __forceinline__ int pad_index(int row, int k, int n_chunks)
-{
-    return (row * n_chunks + (k >> 5)) * kPadChunk + (k & 31);
-}
-
-// 16-bit activation pair -> float2 (bf16 layer input or fp16 h).
-__device__ __forceinline__ float2 act2_to_float2(uint32_t u, const __nv_bfloat16 *)
-{
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
-}
-__device__ __forceinline__ float2 act2_to_float2(uint32_t u, const __half *)
-{
-    return __half22float2(*reinterpret_cast<const __half2 *>(&u));
-}
-
-// dot of 32 dequantised weights (one 16-byte int4 chunk; each weight rounded
-// once to fp16, as in the prefill path) with 32 activations stored
-// contiguously in shared memory; fp32 accumulation.
-template <typename Act>
-__device__ __forceinline__ float dot32(const uint4 q, __half2 s2, __half2 b2, const Act *xs)
-{
-    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-    const uint4 *xv = reinterpret_cast<const uint4 *>(xs);
-    float acc = 0.0f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint4 wv = dequant8_f16(words[c], s2, b2);
-        const uint4 x8 = xv[c];
-        const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
-        const uint32_t xu[4] = {x8.x, x8.y, x8.z, x8.w};
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const float2 wf = __half22float2(*reinterpret_cast<const __half2 *>(&wu[p]));
-            const float2 xf = act2_to_float2(xu[p], xs);
-            acc = fmaf(wf.x, xf.x, acc);
-            acc = fmaf(wf.y, xf.y, acc);
-        }
-    }
-    return acc;
-}
-
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -251,216 +209,247 @@ dec_route_kernel(const DecodeLayerArgs a)
     }
 }
 
-// Loads the layer input x_cur [T][d] into the padded shared layout.
-template <typename Act>
-__device__ __forceinline__ void load_padded(const uint16_t *src, Act *dst, int rows, int K)
+// ---------------------------------------------------------------- tensor-core GEMVs
+// The expert GEMVs run on mma.sync m16n8k16 (f16 x f16 -> f32): 16 weight rows
+// x 16 K x 8 token columns per instruction (tokens >= T are zero columns), so a
+// weight is dequantised once for all tokens.  Lane (g = lane / 4, t = lane % 4)
+// loads 16 bytes (32 weights) of rows g and g + 8 for each 128-wide K block:
+// weights [32 t, 32 t + 32) of the block.  The K order inside the block is
+// permuted so that these weights are exactly this lane's A-fragment entries:
+// within 32-bit word w (weights 8w..8w+7, dequantised in pairs (0,4) (1,5)
+// (2,6) (3,7)), weight e goes to slice 2w + ((e & 3) >> 1), entry
+// ((e & 1) << 1) | (e >> 2) of the lane's four K positions.  The B operand
+// (x, or h for the down projection) is stored in the same permuted order, so
+// each lane reads its B fragment with one 8-byte load.
+constexpr int kKB = 128;  // K block
+
+// Position of element k (of a K range starting at 0) in the permuted B layout
+// [kb][n][t][s][4] for token column n of 8.
+__device__ __forceinline__ int perm_b_index(int k, int n)
 {
-    const int n_chunks = K / kChunk;
-    for (int i = threadIdx.x; i < rows * K / 8; i += kDecThreads) {
-        const int row = (i * 8) / K, k = (i * 8) % K;
-        *reinterpret_cast<uint4 *>(dst + pad_index(row, k, n_chunks)) = reinterpret_cast<const uint4 *>(src)[i];
+    const int kb = k >> 7, r = k & 127, t = r >> 5, w = (r & 31) >> 3, e = r & 7;
+    const int s = 2 * w + ((e & 3) >> 1), idx = ((e & 1) << 1) | (e >> 2);
+    return (((kb * 8 + n) * 4 + t) * 8 + s) * 4 + idx;
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One 128-wide K block of a 16-row tile: q_g / q_g8 hold this lane's 16 bytes of
+// rows g and g + 8, sb_g / sb_g8 the bf16 scale (low half) and bias (high
+// half) of its group; b points at the lane's B fragments of the block
+// (8 slices x 4 fp16, consecutive).
+__device__ __forceinline__ void mma_kblock(float (&d)[4], uint4 q_g, uint4 q_g8, uint32_t sb_g, uint32_t sb_g8,
+                                           const uint2 *b)
+{
+    const __half2 s_g = half2_from_bf16_bits(static_cast<uint16_t>(sb_g & 0xFFFFu));
+    const __half2 b_g = half2_from_bf16_bits(static_cast<uint16_t>(sb_g >> 16));
+    const __half2 s_g8 = half2_from_bf16_bits(static_cast<uint16_t>(sb_g8 & 0xFFFFu));
+    const __half2 b_g8 = half2_from_bf16_bits(static_cast<uint16_t>(sb_g8 >> 16));
+    const __half2 k16 = __floats2half2_rn(0.0625f, 0.0625f);
+    const __half2 s_g16 = __hmul2(s_g, k16), s_g816 = __hmul2(s_g8, k16);
+    const uint32_t wg[4] = {q_g.x, q_g.y, q_g.z, q_g.w}, wg8[4] = {q_g8.x, q_g8.y, q_g8.z, q_g8.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint4 pg = dequant8_f16_kperm(wg[w], s_g, s_g16, b_g);
+        const uint4 pg8 = dequant8_f16_kperm(wg8[w], s_g8, s_g816, b_g8);
+        const uint2 b0 = b[2 * w], b1 = b[2 * w + 1];
+        const uint32_t a0[4] = {pg.x, pg8.x, pg.y, pg8.y};  // slice 2w: pairs (0,4) and (1,5)
+        const uint32_t a1[4] = {pg.z, pg8.z, pg.w, pg8.w};  // slice 2w + 1: pairs (2,6) and (3,7)
+        mma_16816(d, a0, b0.x, b0.y);
+        mma_16816(d, a1, b1.x, b1.y);
     }
 }
 
-__global__ void __launch_bounds__(kDecThreads, 2)
+// Scale and bias of this lane's group in a K block, packed (scale low, bias high).
+__device__ __forceinline__ uint32_t load_sb(const uint16_t *s_row, const uint16_t *b_row, int group)
+{
+    return static_cast<uint32_t>(__ldg(s_row + group)) | (static_cast<uint32_t>(__ldg(b_row + group)) << 16);
+}
+
+// gate/up: task = (unit, 32 rows of I); warp w takes rows 16 (w % 2) .. + 16
+// and the K blocks kb = w / 2 (mod 4), both matrices; the four K-split partial
+// tiles are summed in shared memory, then h' = f16(w_u[t] * silu(gate) * up) is
+// written in the permuted B layout of the down projection (K = units x I).
+__global__ void __launch_bounds__(kDecThreads)
 dec_gateup_kernel(const DecodeLayerArgs a)
 {
     extern __shared__ __align__(16) uint8_t dsm[];
-    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(dsm);
+    __half *xp = reinterpret_cast<__half *>(dsm);                                 // [d/128][8][4][8][4]
+    float *red = reinterpret_cast<float *>(dsm + static_cast<size_t>(a.d) * 8 * 2);  // [8 warps][2][32][4]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int T = a.T, d = a.d, I = a.I;
-    const int n_chunks = d / kChunk, ngroups = d / 64;
-    load_padded(a.x_cur, xs, T, d);
-    __syncthreads();
-
-    const int n_units = *a.n_units;
-    const int items = n_units * I;
-    const int n_pairs = (items + 1) / 2;
-    // A warp takes two (unit, row) items at a time; each lane first issues every
-    // 16-byte weight load of both items (gate and up), then computes.
-    for (int pr = blockIdx.x * kDecWarps + warp; pr < n_pairs; pr += gridDim.x * kDecWarps) {
-        const uint4 *gq[2], *uq[2];
-        const uint16_t *gs[2], *gb[2], *us[2], *ub[2];
-        int mask[2], uu[2], ii[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int item = min(2 * pr + k, items - 1);
-            const int u = item / I, i = item - u * I;
-            const int e = a.unit_expert[u];
-            int m = a.unit_mask[u] & ((1 << T) - 1);
-            if (e >= a.E || m == 0) {
-                if (lane == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
-                m = 0;
-            }
-            if (2 * pr + k >= items) m = 0;  // odd tail: the duplicate item does nothing
-            const bool sh = e < 0;
-            const size_t row = sh ? static_cast<size_t>(i) : static_cast<size_t>(e < a.E ? e : 0) * I + i;
-            gq[k] = reinterpret_cast<const uint4 *>((sh ? a.sh_gate_q : a.gate_q) + row * (d / 2));
-            uq[k] = reinterpret_cast<const uint4 *>((sh ? a.sh_up_q : a.up_q) + row * (d / 2));
-            gs[k] = (sh ? a.sh_gate_s : a.gate_s) + row * ngroups;
-            gb[k] = (sh ? a.sh_gate_b : a.gate_b) + row * ngroups;
-            us[k] = (sh ? a.sh_up_s : a.up_s) + row * ngroups;
-            ub[k] = (sh ? a.sh_up_b : a.up_b) + row * ngroups;
-            mask[k] = m;
-            uu[k] = u;
-            ii[k] = i;
-        }
-        float accg[2][kMaxT], accu[2][kMaxT];
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-            for (int t = 0; t < kMaxT; ++t) accg[k][t] = accu[k][t] = 0.0f;
-        for (int c0 = 0; c0 < n_chunks; c0 += 2 * 32) {
-            uint4 qg[2][2], qu[2][2];
-            uint16_t vgs[2][2], vgb[2][2], vus[2][2], vub[2][2];
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int c = c0 + q * 32 + lane;
-                    if (c < n_chunks && mask[k]) {
-                        qg[k][q] = __ldg(gq[k] + c);
-                        qu[k][q] = __ldg(uq[k] + c);
-                        vgs[k][q] = __ldg(gs[k] + (c >> 1));
-                        vgb[k][q] = __ldg(gb[k] + (c >> 1));
-                        vus[k][q] = __ldg(us[k] + (c >> 1));
-                        vub[k][q] = __ldg(ub[k] + (c >> 1));
-                    }
-                }
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int c = c0 + q * 32 + lane;
-                    if (c < n_chunks && mask[k]) {
-                        const __half2 sg = half2_from_bf16_bits(vgs[k][q]), bg = half2_from_bf16_bits(vgb[k][q]);
-                        const __half2 su = half2_from_bf16_bits(vus[k][q]), bu = half2_from_bf16_bits(vub[k][q]);
-#pragma unroll
-                        for (int t = 0; t < kMaxT; ++t) {
-                            if (t < T && ((mask[k] >> t) & 1)) {
-                                const __nv_bfloat16 *xr = xs + pad_index(t, c * kChunk, n_chunks);
-                                accg[k][t] += dot32(qg[k][q], sg, bg, xr);
-                                accu[k][t] += dot32(qu[k][q], su, bu, xr);
-                            }
-                        }
-                    }
-                }
-        }
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-            for (int t = 0; t < kMaxT; ++t) {
-                if (t < T && ((mask[k] >> t) & 1)) {
-                    const float gv = warp_sum(accg[k][t]);
-                    const float uv = warp_sum(accu[k][t]);
-                    if (lane == 0)
-                        a.h[(static_cast<size_t>(uu[k]) * kMaxT + t) * I + ii[k]] = __float2half_rn(silu_f(gv) * uv);
-                }
-            }
+    const int g = lane >> 2, t = lane & 3;
+    const int T = a.T, d = a.d, I = a.I, nkb = d / kKB, ngroups = d / 64;
+    for (int i = threadIdx.x; i < 8 * d; i += kDecThreads) {
+        const int n = i / d, k = i - n * d;
+        const float v = n < T ? bf16_bits_to_float(a.x_cur[static_cast<size_t>(n) * d + k]) : 0.0f;
+        xp[perm_b_index(k, n)] = __float2half_rn(v);
     }
-}
-
-__global__ void __launch_bounds__(kDecThreads)
-dec_down_kernel(const DecodeLayerArgs a)
-{
-    extern __shared__ __align__(16) uint8_t dsm[];
-    __half *hs = reinterpret_cast<__half *>(dsm);  // compact (unit, token) rows of h, padded
-    __shared__ int s_expert[kMaxT * 8 + 1];
-    __shared__ int s_mask[kMaxT * 8 + 1];
-    __shared__ int s_slot[kMaxT * 8 + 1];  // first compact h slot of each unit
-    __shared__ float s_w[kMaxT * 8 + 1][kMaxT];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int T = a.T, d = a.d, I = a.I;
-    const int n_chunks = I / kChunk, ngroups = I / 64;
+    __syncthreads();
     const int n_units = *a.n_units;
-    if (n_units < 1 || n_units > kMaxT * 8 + 1) {
+    if (n_units < 1 || n_units > a.top_k * T + 1) {  // the h buffer holds top_k * T + 1 units
         if (threadIdx.x == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
         return;
     }
-    for (int u = threadIdx.x; u < n_units; u += kDecThreads) {
-        s_expert[u] = a.unit_expert[u];
-        s_mask[u] = a.unit_mask[u] & ((1 << T) - 1);
+    const int tpu = I / 32;  // tasks per unit
+    const int rt = warp & 1, ks = warp >> 1;
+    for (int task = blockIdx.x; task < n_units * tpu; task += gridDim.x) {
+        const int u = task / tpu;
+        const int i0 = (task - u * tpu) * 32 + rt * 16;
+        int e = a.unit_expert[u];
+        if (e >= a.E) {
+            if (lane == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
+            e = 0;
+        }
+        const bool sh = e < 0;
+        const size_t row_g = (sh ? 0 : static_cast<size_t>(e) * I) + i0 + g, row_g8 = row_g + 8;
+        const uint8_t *gq = sh ? a.sh_gate_q : a.gate_q, *uq = sh ? a.sh_up_q : a.up_q;
+        const uint16_t *gs = sh ? a.sh_gate_s : a.gate_s, *gb = sh ? a.sh_gate_b : a.gate_b;
+        const uint16_t *us = sh ? a.sh_up_s : a.up_s, *ub = sh ? a.sh_up_b : a.up_b;
+        float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kb0 = ks; kb0 < nkb; kb0 += 4 * 4) {
+            // up to 4 K blocks of this warp: all loads first, then the MMAs
+            uint4 qg[4], qg8[4], qu[4], qu8[4];
+            uint32_t sg[4], sg8[4], su[4], su8[4];
 #pragma unroll
-        for (int t = 0; t < kMaxT; ++t) s_w[u][t] = a.unit_w[u * kMaxT + t];
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int u = 0; u < n_units; ++u) {
-            s_slot[u] = run;
-            run += __popc(s_mask[u]);
+            for (int m = 0; m < 4; ++m) {
+                const int kb = kb0 + 4 * m;
+                if (kb < nkb) {
+                    const size_t off = static_cast<size_t>(kb) * (kKB / 2) + t * 16;
+                    qg[m] = __ldg(reinterpret_cast<const uint4 *>(gq + row_g * (d / 2) + off));
+                    qg8[m] = __ldg(reinterpret_cast<const uint4 *>(gq + row_g8 * (d / 2) + off));
+                    qu[m] = __ldg(reinterpret_cast<const uint4 *>(uq + row_g * (d / 2) + off));
+                    qu8[m] = __ldg(reinterpret_cast<const uint4 *>(uq + row_g8 * (d / 2) + off));
+                    const int grp = 2 * kb + (t >> 1);
+                    sg[m] = load_sb(gs + row_g * ngroups, gb + row_g * ngroups, grp);
+                    sg8[m] = load_sb(gs + row_g8 * ngroups, gb + row_g8 * ngroups, grp);
+                    su[m] = load_sb(us + row_g * ngroups, ub + row_g * ngroups, grp);
+                    su8[m] = load_sb(us + row_g8 * ngroups, ub + row_g8 * ngroups, grp);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int kb = kb0 + 4 * m;
+                if (kb < nkb) {
+                    const uint2 *bf = reinterpret_cast<const uint2 *>(xp + (((kb * 8 + g) * 4 + t) * 8) * 4);
+                    mma_kblock(accg, qg[m], qg8[m], sg[m], sg8[m], bf);
+                    mma_kblock(accu, qu[m], qu8[m], su[m], su8[m], bf);
+                }
+            }
         }
-    }
-    __syncthreads();
-    // Compact copy of h: one padded row per (unit, token served by the unit).
-    for (int u = warp; u < n_units; u += kDecWarps) {
-        const int mask = s_mask[u];
-        int slot = s_slot[u];
-        for (int t = 0; t < T; ++t) {
-            if (!((mask >> t) & 1)) continue;
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.h + (static_cast<size_t>(u) * kMaxT + t) * I);
-            for (int i = lane; i < I / 8; i += 32)
-                *reinterpret_cast<uint4 *>(hs + pad_index(slot, i * 8, n_chunks)) = src[i];
-            ++slot;
+        // sum the four K-split partial tiles of each row tile
+        float *mine = red + (warp * 2) * 32 * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            mine[lane * 4 + q] = accg[q];
+            mine[32 * 4 + lane * 4 + q] = accu[q];
         }
+        __syncthreads();
+        if (ks == 0) {
+#pragma unroll
+            for (int p = 1; p < 4; ++p) {
+                const float *o = red + ((rt + 2 * p) * 2) * 32 * 4;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    accg[q] += o[lane * 4 + q];
+                    accu[q] += o[32 * 4 + lane * 4 + q];
+                }
+            }
+            // fragment: q = 0/1 -> row g, tokens 2t, 2t+1; q = 2/3 -> row g + 8
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int n = 2 * t + (q & 1);
+                const int i = i0 + g + 8 * (q >> 1);
+                const float wt = a.unit_w[u * kMaxT + n];
+                const float hv = wt * silu_f(accg[q]) * accu[q];
+                a.h[perm_b_index(u * I + i, n)] = __float2half_rn(hv);
+            }
+        }
+        __syncthreads();
     }
-    __syncthreads();
+}
 
-    for (int j = blockIdx.x * kDecWarps + warp; j < d; j += gridDim.x * kDecWarps) {
-        float acc[kMaxT];
+// down: task = 16 output rows; the 8 warps split the K blocks of
+// K = units x I (unit u, block j), accumulate in one tile, and the partial
+// tiles are summed in shared memory.  out[t][row] = sum over units of
+// Wd_u[row] . h'_u[t] (the routing weight is already in h').
+__global__ void __launch_bounds__(kDecThreads)
+dec_down_kernel(const DecodeLayerArgs a)
+{
+    __shared__ float red[kDecWarps][32][4];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int T = a.T, d = a.d, I = a.I, kpu = I / kKB, ngroups = I / 64;
+    const int n_units = *a.n_units;
+    if (n_units < 1 || n_units > a.top_k * T + 1) {  // the h buffer holds top_k * T + 1 units
+        if (threadIdx.x == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
+        return;
+    }
+    const int n_kb = n_units * kpu;
+    for (int task = blockIdx.x; task < d / 16; task += gridDim.x) {
+        const int j0 = task * 16;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kb0 = warp; kb0 < n_kb; kb0 += 2 * kDecWarps) {
+            uint4 q[2], q8[2];
+            uint32_t sb[2], sb8[2];
+            uint2 bfr[2][8];
 #pragma unroll
-        for (int t = 0; t < kMaxT; ++t) acc[t] = 0.0f;
-        const int n_items = n_units * n_chunks;
-        constexpr int kB = 8;  // chunk-items per lane with loads in flight together
-        for (int it0 = 0; it0 < n_items; it0 += kB * 32) {
-            uint4 q[kB];
-            uint16_t vs[kB], vb[kB];
-#pragma unroll
-            for (int m = 0; m < kB; ++m) {
-                const int it = it0 + m * 32 + lane;
-                if (it < n_items) {
-                    const int u = it / n_chunks, c = it - u * n_chunks;
-                    const int e = s_expert[u];
-                    const bool sh = e < 0;
-                    const size_t row = sh ? static_cast<size_t>(j) : static_cast<size_t>(e) * d + j;
-                    q[m] = __ldg(reinterpret_cast<const uint4 *>((sh ? a.sh_down_q : a.down_q) + row * (I / 2)) + c);
-                    vs[m] = __ldg((sh ? a.sh_down_s : a.down_s) + row * ngroups + (c >> 1));
-                    vb[m] = __ldg((sh ? a.sh_down_b : a.down_b) + row * ngroups + (c >> 1));
-                }
-            }
-#pragma unroll
-            for (int m = 0; m < kB; ++m) {
-                const int it = it0 + m * 32 + lane;
-                if (it < n_items) {
-                    const int u = it / n_chunks, c = it - u * n_chunks;
-                    const __half2 s2 = half2_from_bf16_bits(vs[m]), b2 = half2_from_bf16_bits(vb[m]);
-                    const int mask = s_mask[u];
-                    int slot = s_slot[u];
-#pragma unroll
-                    for (int t = 0; t < kMaxT; ++t) {
-                        if (t < T && ((mask >> t) & 1)) {
-                            acc[t] += s_w[u][t] * dot32(q[m], s2, b2, hs + pad_index(slot, c * kChunk, n_chunks));
-                            ++slot;
-                        }
+            for (int m = 0; m < 2; ++m) {
+                const int kb = kb0 + m * kDecWarps;
+                if (kb < n_kb) {
+                    const int u = kb / kpu, jb = kb - u * kpu;
+                    int e = a.unit_expert[u];
+                    if (e >= a.E) {
+                        if (lane == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
+                        e = 0;
                     }
+                    const bool sh = e < 0;
+                    const size_t row = (sh ? 0 : static_cast<size_t>(e) * d) + j0 + g;
+                    const uint8_t *dq = sh ? a.sh_down_q : a.down_q;
+                    const uint16_t *ds = sh ? a.sh_down_s : a.down_s, *db = sh ? a.sh_down_b : a.down_b;
+                    const size_t off = static_cast<size_t>(jb) * (kKB / 2) + t * 16;
+                    q[m] = __ldg(reinterpret_cast<const uint4 *>(dq + row * (I / 2) + off));
+                    q8[m] = __ldg(reinterpret_cast<const uint4 *>(dq + (row + 8) * (I / 2) + off));
+                    const int grp = 2 * jb + (t >> 1);
+                    sb[m] = load_sb(ds + row * ngroups, db + row * ngroups, grp);
+                    sb8[m] = load_sb(ds + (row + 8) * ngroups, db + (row + 8) * ngroups, grp);
+                    const uint2 *src = reinterpret_cast<const uint2 *>(a.h) + ((kb * 8 + g) * 4 + t) * 8;
+#pragma unroll
+                    for (int s2 = 0; s2 < 8; ++s2) bfr[m][s2] = __ldcg(src + s2);
                 }
             }
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+                if (kb0 + m * kDecWarps < n_kb) mma_kblock(acc, q[m], q8[m], sb[m], sb8[m], bfr[m]);
         }
 #pragma unroll
-        for (int t = 0; t < kMaxT; ++t) {
-            if (t < T) {
-                const float sm = warp_sum(acc[t]);
-                if (lane == 0) a.out[static_cast<size_t>(t) * d + j] = sm;
+        for (int q = 0; q < 4; ++q) red[warp][lane][q] = acc[q];
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int p = 1; p < kDecWarps; ++p)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[q] += red[p][lane][q];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int n = 2 * t + (q & 1);
+                if (n < T) a.out[static_cast<size_t>(n) * d + j0 + g + 8 * (q >> 1)] = acc[q];
             }
         }
+        __syncthreads();
     }
 }
 
 }  // namespace
 
 size_t decode_smem_route(int T, int d) { return static_cast<size_t>(T) * d * 2; }
-size_t decode_smem_gateup(int T, int d) { return static_cast<size_t>(T) * (d / kChunk) * kPadChunk * 2; }
-size_t decode_smem_down(int T, int I) { return static_cast<size_t>(T * 8 + T) * (I / kChunk) * kPadChunk * 2; }
+size_t decode_smem_gateup(int T, int d) { return static_cast<size_t>(d) * 8 * 2 + kDecWarps * 2 * 32 * 4 * 4 + 0 * T; }
+size_t decode_smem_down(int T, int I) { return 0 * static_cast<size_t>(T + I); }
 
 cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStream_t stream)
 {
@@ -473,8 +462,8 @@ cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStrea
         configured = true;
     }
     dec_route_kernel<<<(a.E + kDecWarps - 1) / kDecWarps, kDecThreads, decode_smem_route(a.T, a.d), stream>>>(a);
-    dec_gateup_kernel<<<2 * num_sms, kDecThreads, decode_smem_gateup(a.T, a.d), stream>>>(a);
-    dec_down_kernel<<<(a.d + kDecWarps - 1) / kDecWarps, kDecThreads, decode_smem_down(a.T, a.I), stream>>>(a);
+    dec_gateup_kernel<<<num_sms, kDecThreads, decode_smem_gateup(a.T, a.d), stream>>>(a);
+    dec_down_kernel<<<std::min(num_sms, a.d / 16), kDecThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -1,6 +1,7 @@
 """Runs a few whole-layer forward passes of one seeded workload, for profilers.
 
   python -m bit_grouped_expert_top_gb300.profile_run --config prefill_t8192 --reps 2
+  python -m bit_grouped_expert_top_gb300.profile_run --config decode_t1_l40 --layers 4 --T 1 --reps 3
 
 Each pass launches, in order: router GEMM, top-8 + per-chunk counts, per-expert
 scan + block map, scatter, prep (fp16 x in routing order, out = 0), gate/up
@@ -20,10 +21,14 @@ from bit_grouped_expert_top_gb300.inputs import CONFIGS, make_layer, make_x
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("--config", default="prefill_t2048_zipf", choices=sorted(k for k in CONFIGS if k.startswith("prefill")))
+    ap.add_argument("--config", default="prefill_t2048_zipf", choices=sorted(CONFIGS))
     ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--layers", type=int, default=4, help="decode: distinct layers per call")
+    ap.add_argument("--T", type=int, default=1, help="decode: tokens")
     a = ap.parse_args(argv)
     cfg = CONFIGS[a.config]
+    if a.config.startswith("decode"):
+        return run_decode(cfg, a)
     layer = make_layer(cfg, "cuda")
     w = lm.make_weights(layer)
     x = make_x(cfg, "cuda")
@@ -36,6 +41,22 @@ def main(argv=None) -> int:
     torch.cuda.synchronize()
     st = lm.lily_moe_device_status(ws)
     print(f"{a.config}: {a.reps} forward passes, device status {st}")
+    return 0 if st == 0 else 1
+
+
+def run_decode(cfg, a) -> int:
+    layers = [make_layer(cfg, "cuda", i) for i in range(a.layers)]
+    wl = [lm.make_weights(x) for x in layers]
+    s = lm.make_shape(T=a.T, d=cfg.d, E=cfg.E, top_k=cfg.top_k, I=cfg.I, I_shared=cfg.I_shared,
+                      group=cfg.group, block_rows=cfg.block_rows)
+    ws = lm.alloc_workspace(s, n_layers_decode=a.layers)
+    x = make_x(cfg, "cuda", T=a.T)
+    out = torch.empty((a.layers, a.T, cfg.d), device="cuda")
+    for _ in range(a.reps):
+        lm.lily_moe_decode(s, wl, x, out, ws)
+    torch.cuda.synchronize()
+    st = lm.lily_moe_device_status(ws)
+    print(f"{cfg.name}: {a.reps} decode calls of {a.layers} layers at T={a.T}, device status {st}")
     return 0 if st == 0 else 1
 
 
