@@ -72,7 +72,7 @@ PrefillLayout prefill_layout(const lily_moe_shape &s)
 }
 
 struct DecodeLayout {
-    size_t ctrl, x_cur, logits, n_units, unit_expert, unit_mask, unit_w, h, total;
+    size_t ctrl, x_cur, xp, logits, n_units, unit_expert, unit_mask, unit_w, h, total;
 };
 
 DecodeLayout decode_layout(const lily_moe_shape &s)
@@ -87,6 +87,7 @@ DecodeLayout decode_layout(const lily_moe_shape &s)
     };
     L.ctrl = take(sizeof(Ctrl));
     L.x_cur = take(T * s.d * 2);
+    L.xp = take(8 * s.d * 2);  // fp16 layer input, 8 token columns, permuted for the tensor-core GEMV
     L.logits = take(T * s.E * 4);
     L.n_units = take(4);
     L.unit_expert = take(U * 4);
@@ -547,6 +548,7 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
                 a.trace_w = trace->topk_w ? trace->topk_w + static_cast<size_t>(l) * s.T * s.top_k : nullptr;
             }
             a.x_cur = at<uint16_t>(ws, L.x_cur);
+            a.xp = at<__half>(ws, L.xp);
             a.logits = at<float>(ws, L.logits);
             a.n_units = at<int>(ws, L.n_units);
             a.unit_expert = at<int>(ws, L.unit_expert);

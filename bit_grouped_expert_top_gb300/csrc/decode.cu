@@ -32,11 +32,40 @@ namespace {
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMaxT = 8;
+// Programmatic dependent launch: this grid lets the next one start launching,
+// and waits (before reading anything an earlier kernel wrote) until the
+// preceding grid has completed and its memory is visible.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// ---------------------------------------------------------------- tensor-core GEMVs
+// The expert GEMVs run on mma.sync m16n8k16 (f16 x f16 -> f32): 16 weight rows
+// x 16 K x 8 token columns per instruction (tokens >= T are zero columns), so a
+// weight is dequantised once for all tokens.  Lane (g = lane / 4, t = lane % 4)
+// loads 16 bytes (32 weights) of rows g and g + 8 for each 128-wide K block:
+// weights [32 t, 32 t + 32) of the block.  The K order inside the block is
+// permuted so that these weights are exactly this lane's A-fragment entries:
+// within 32-bit word w (weights 8w..8w+7, dequantised in pairs (0,4) (1,5)
+// (2,6) (3,7)), weight e goes to slice 2w + ((e & 3) >> 1), entry
+// ((e & 1) << 1) | (e >> 2) of the lane's four K positions.  The B operand
+// (x, or h for the down projection) is stored in the same permuted order, so
+// each lane reads its B fragment with one 8-byte load.
+constexpr int kKB = 128;  // K block
+
+// Position of element k (of a K range starting at 0) in the permuted B layout
+// [kb][n][t][s][4] for token column n of 8.
+__device__ __forceinline__ int perm_b_index(int k, int n)
+{
+    const int kb = k >> 7, r = k & 127, t = r >> 5, w = (r & 31) >> 3, e = r & 7;
+    const int s = 2 * w + ((e & 3) >> 1), idx = ((e & 1) << 1) | (e >> 2);
+    return (((kb * 8 + n) * 4 + t) * 8 + s) * 4 + idx;
 }
 
 __global__ void __launch_bounds__(kDecThreads)
@@ -46,7 +75,6 @@ dec_route_kernel(const DecodeLayerArgs a)
     __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(dsm);  // [T][d] plain layout
     __shared__ float red[kDecWarps][kMaxT];
     __shared__ float inv_rms[kMaxT];
-    __shared__ int is_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int T = a.T, d = a.d;
     const int e = blockIdx.x * kDecWarps + warp;  // this warp's expert
@@ -61,6 +89,9 @@ dec_route_kernel(const DecodeLayerArgs a)
         const int c = lane + 32 * m;
         if (e < a.E && c < n8) wpre[m] = __ldg(wrow + c);
     }
+
+    pdl_trigger();
+    pdl_wait();  // the previous layer's output (and this call's buffers) are ready
 
     // ---- layer input
     if (a.prev_out == nullptr) {
@@ -104,6 +135,33 @@ dec_route_kernel(const DecodeLayerArgs a)
             if (a.x_export) reinterpret_cast<uint4 *>(a.x_export)[i] = v;
         }
     }
+    {
+        // fp16 copy in the permuted B layout of the expert GEMVs (8 token columns),
+        // split over the CTAs: the 8 elements of one 32-bit weight word land as
+        // 16 contiguous bytes (x0 x4 x1 x5 | x2 x6 x3 x7)
+        const int wpt = d / 8;  // words per token
+        const int per = (8 * wpt + gridDim.x - 1) / gridDim.x;
+        for (int q = blockIdx.x * per + threadIdx.x; q < min(8 * wpt, (blockIdx.x + 1) * per); q += kDecThreads) {
+            const int n = q / wpt, k0 = (q - n * wpt) * 8;
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+            if (n < T) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(xs + static_cast<size_t>(n) * d + k0);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 p2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
+                    f[2 * j] = p2.x;
+                    f[2 * j + 1] = p2.y;
+                }
+                const __half2 h0 = __floats2half2_rn(f[0], f[4]), h1 = __floats2half2_rn(f[1], f[5]);
+                const __half2 h2 = __floats2half2_rn(f[2], f[6]), h3 = __floats2half2_rn(f[3], f[7]);
+                o = make_uint4(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1),
+                               *reinterpret_cast<const uint32_t *>(&h2), *reinterpret_cast<const uint32_t *>(&h3));
+            }
+            *reinterpret_cast<uint4 *>(a.xp + perm_b_index(k0, n)) = o;
+        }
+    }
 
     // ---- router GEMV: one warp per expert
     if (e < a.E) {
@@ -145,91 +203,6 @@ dec_route_kernel(const DecodeLayerArgs a)
             }
         }
     }
-
-    // ---- last CTA: top-8 per token and the unit list
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned int prev = atomicAdd(&a.ctrl->ticket2, 1u);
-        is_last = (prev == static_cast<unsigned int>(gridDim.x) - 1u);
-    }
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-
-    __shared__ int umask[256];
-    __shared__ float uw[256][kMaxT];
-    __shared__ int scan_tmp[kDecWarps];
-    umask[threadIdx.x] = 0;
-#pragma unroll
-    for (int t = 0; t < kMaxT; ++t) uw[threadIdx.x][t] = 0.0f;
-    __syncthreads();
-    if (warp < T) {
-        const int t = warp;
-        int sel_e;
-        float sel_w;
-        warp_top8_of_256(a.logits + t * a.E, lane, sel_e, sel_w);
-        if (lane < 8) {
-            if (a.trace_idx) a.trace_idx[t * 8 + lane] = sel_e;
-            if (a.trace_w) a.trace_w[t * 8 + lane] = sel_w;
-            atomicOr(&umask[sel_e], 1 << t);
-            uw[sel_e][t] = sel_w;
-        }
-    }
-    __syncthreads();
-    // compact the used experts in ascending order
-    const int used = umask[threadIdx.x] != 0;
-    int incl = used;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-    }
-    if (lane == 31) scan_tmp[warp] = incl;
-    __syncthreads();
-    int off = 0, n_used = 0;
-    for (int w = 0; w < kDecWarps; ++w) {
-        if (w < warp) off += scan_tmp[w];
-        n_used += scan_tmp[w];
-    }
-    const int u = off + incl - used;
-    if (used) {
-        a.unit_expert[u] = threadIdx.x;
-        a.unit_mask[u] = umask[threadIdx.x];
-#pragma unroll
-        for (int t = 0; t < kMaxT; ++t) a.unit_w[u * kMaxT + t] = uw[threadIdx.x][t];
-    }
-    if (threadIdx.x == 0) {
-        a.unit_expert[n_used] = -1;  // shared expert
-        a.unit_mask[n_used] = (1 << T) - 1;
-#pragma unroll
-        for (int t = 0; t < kMaxT; ++t) a.unit_w[n_used * kMaxT + t] = 1.0f;
-        *a.n_units = n_used + 1;
-        a.ctrl->ticket2 = 0u;
-    }
-}
-
-// ---------------------------------------------------------------- tensor-core GEMVs
-// The expert GEMVs run on mma.sync m16n8k16 (f16 x f16 -> f32): 16 weight rows
-// x 16 K x 8 token columns per instruction (tokens >= T are zero columns), so a
-// weight is dequantised once for all tokens.  Lane (g = lane / 4, t = lane % 4)
-// loads 16 bytes (32 weights) of rows g and g + 8 for each 128-wide K block:
-// weights [32 t, 32 t + 32) of the block.  The K order inside the block is
-// permuted so that these weights are exactly this lane's A-fragment entries:
-// within 32-bit word w (weights 8w..8w+7, dequantised in pairs (0,4) (1,5)
-// (2,6) (3,7)), weight e goes to slice 2w + ((e & 3) >> 1), entry
-// ((e & 1) << 1) | (e >> 2) of the lane's four K positions.  The B operand
-// (x, or h for the down projection) is stored in the same permuted order, so
-// each lane reads its B fragment with one 8-byte load.
-constexpr int kKB = 128;  // K block
-
-// Position of element k (of a K range starting at 0) in the permuted B layout
-// [kb][n][t][s][4] for token column n of 8.
-__device__ __forceinline__ int perm_b_index(int k, int n)
-{
-    const int kb = k >> 7, r = k & 127, t = r >> 5, w = (r & 31) >> 3, e = r & 7;
-    const int s = 2 * w + ((e & 3) >> 1), idx = ((e & 1) << 1) | (e >> 2);
-    return (((kb * 8 + n) * 4 + t) * 8 + s) * 4 + idx;
 }
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
@@ -285,34 +258,111 @@ dec_gateup_kernel(const DecodeLayerArgs a)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int T = a.T, d = a.d, I = a.I, nkb = d / kKB, ngroups = d / 64;
-    for (int i = threadIdx.x; i < 8 * d; i += kDecThreads) {
-        const int n = i / d, k = i - n * d;
-        const float v = n < T ? bf16_bits_to_float(a.x_cur[static_cast<size_t>(n) * d + k]) : 0.0f;
-        xp[perm_b_index(k, n)] = __float2half_rn(v);
+    pdl_trigger();
+    if (threadIdx.x == 0 && blockIdx.x < 2) {
+        // the shared expert is always used: warm L2 with its gate (CTA 0) / up (CTA 1)
+        // rows while the routing kernel finishes
+        const uint8_t *q = blockIdx.x == 0 ? a.sh_gate_q : a.sh_up_q;
+        bulk_prefetch_l2(q, static_cast<uint32_t>(I) * (d / 2));
+    }
+    pdl_wait();
+    // the fp16 input goes to shared memory asynchronously; the first round of
+    // weight loads is issued before waiting for it
+    for (int i = threadIdx.x; i < d; i += kDecThreads)  // 8 x d fp16 = d uint4
+        cp_async_16(reinterpret_cast<uint4 *>(xp) + i, reinterpret_cast<const uint4 *>(a.xp) + i);
+    cp_async_commit();
+    bool xp_ready = false;
+
+    // Top-8 per token and the list of distinct experts ("units", ascending, the
+    // shared expert last with weight 1), computed by every CTA from the logits;
+    // CTA 0 publishes it for the down projection and the trace.
+    __shared__ int umask[256];
+    __shared__ float uw[256][kMaxT];
+    __shared__ int scan_tmp[kDecWarps];
+    __shared__ int s_expert[kMaxT * 8 + 1];
+    __shared__ float s_w[kMaxT * 8 + 1][kMaxT];
+    __shared__ int s_n_units;
+    umask[threadIdx.x] = 0;
+#pragma unroll
+    for (int q = 0; q < kMaxT; ++q) uw[threadIdx.x][q] = 0.0f;
+    __syncthreads();
+    if (warp < T) {
+        const int tok = warp;
+        const float4 *src = reinterpret_cast<const float4 *>(a.logits + tok * a.E + lane * 8);
+        const float4 l0 = __ldcg(src), l1 = __ldcg(src + 1);
+        const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+        int sel_e;
+        float sel_w;
+        warp_top8_keys(lv, lane, sel_e, sel_w);
+        if (lane < 8) {
+            if (blockIdx.x == 0 && a.trace_idx) a.trace_idx[tok * 8 + lane] = sel_e;
+            if (blockIdx.x == 0 && a.trace_w) a.trace_w[tok * 8 + lane] = sel_w;
+            atomicOr(&umask[sel_e], 1 << tok);
+            uw[sel_e][tok] = sel_w;
+        }
     }
     __syncthreads();
-    const int n_units = *a.n_units;
-    if (n_units < 1 || n_units > a.top_k * T + 1) {  // the h buffer holds top_k * T + 1 units
-        if (threadIdx.x == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
-        return;
+    {
+        const int used = umask[threadIdx.x] != 0;
+        int incl = used;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += nb;
+        }
+        if (lane == 31) scan_tmp[warp] = incl;
+        __syncthreads();
+        int off = 0, n_used = 0;
+        for (int w = 0; w < kDecWarps; ++w) {
+            if (w < warp) off += scan_tmp[w];
+            n_used += scan_tmp[w];
+        }
+        const int u = off + incl - used;
+        if (used) {
+            s_expert[u] = threadIdx.x;
+#pragma unroll
+            for (int q = 0; q < kMaxT; ++q) s_w[u][q] = uw[threadIdx.x][q];
+            if (blockIdx.x == 0) {
+                a.unit_expert[u] = threadIdx.x;
+                a.unit_mask[u] = umask[threadIdx.x];
+#pragma unroll
+                for (int q = 0; q < kMaxT; ++q) a.unit_w[u * kMaxT + q] = uw[threadIdx.x][q];
+            }
+        }
+        if (threadIdx.x == 0) {
+            s_expert[n_used] = -1;  // shared expert
+#pragma unroll
+            for (int q = 0; q < kMaxT; ++q) s_w[n_used][q] = 1.0f;
+            s_n_units = n_used + 1;
+            if (blockIdx.x == 0) {
+                a.unit_expert[n_used] = -1;
+                a.unit_mask[n_used] = (1 << T) - 1;
+#pragma unroll
+                for (int q = 0; q < kMaxT; ++q) a.unit_w[n_used * kMaxT + q] = 1.0f;
+                *a.n_units = n_used + 1;
+            }
+        }
+        __syncthreads();
     }
+    const int n_units = s_n_units;
     const int tpu = I / 32;  // tasks per unit
     const int rt = warp & 1, ks = warp >> 1;
+    if (blockIdx.x >= n_units * tpu) {
+        cp_async_wait_all();  // no copy into shared memory in flight at exit
+        return;
+    }
     for (int task = blockIdx.x; task < n_units * tpu; task += gridDim.x) {
         const int u = task / tpu;
         const int i0 = (task - u * tpu) * 32 + rt * 16;
-        int e = a.unit_expert[u];
-        if (e >= a.E) {
-            if (lane == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
-            e = 0;
-        }
+        const int e = s_expert[u];
         const bool sh = e < 0;
         const size_t row_g = (sh ? 0 : static_cast<size_t>(e) * I) + i0 + g, row_g8 = row_g + 8;
         const uint8_t *gq = sh ? a.sh_gate_q : a.gate_q, *uq = sh ? a.sh_up_q : a.up_q;
         const uint16_t *gs = sh ? a.sh_gate_s : a.gate_s, *gb = sh ? a.sh_gate_b : a.gate_b;
         const uint16_t *us = sh ? a.sh_up_s : a.up_s, *ub = sh ? a.sh_up_b : a.up_b;
         float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int kb0 = ks; kb0 < nkb; kb0 += 4 * 4) {
+        for (int r0 = 0; r0 < nkb; r0 += 4 * 4) {  // rounds: the same count in every warp
+            const int kb0 = r0 + ks;
             // up to 4 K blocks of this warp: all loads first, then the MMAs
             uint4 qg[4], qg8[4], qu[4], qu8[4];
             uint32_t sg[4], sg8[4], su[4], su8[4];
@@ -331,6 +381,11 @@ dec_gateup_kernel(const DecodeLayerArgs a)
                     su[m] = load_sb(us + row_g * ngroups, ub + row_g * ngroups, grp);
                     su8[m] = load_sb(us + row_g8 * ngroups, ub + row_g8 * ngroups, grp);
                 }
+            }
+            if (!xp_ready) {
+                cp_async_wait_all();
+                __syncthreads();
+                xp_ready = true;
             }
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -365,7 +420,7 @@ dec_gateup_kernel(const DecodeLayerArgs a)
             for (int q = 0; q < 4; ++q) {
                 const int n = 2 * t + (q & 1);
                 const int i = i0 + g + 8 * (q >> 1);
-                const float wt = a.unit_w[u * kMaxT + n];
+                const float wt = s_w[u][n];
                 const float hv = wt * silu_f(accg[q]) * accu[q];
                 a.h[perm_b_index(u * I + i, n)] = __float2half_rn(hv);
             }
@@ -378,13 +433,18 @@ dec_gateup_kernel(const DecodeLayerArgs a)
 // K = units x I (unit u, block j), accumulate in one tile, and the partial
 // tiles are summed in shared memory.  out[t][row] = sum over units of
 // Wd_u[row] . h'_u[t] (the routing weight is already in h').
-__global__ void __launch_bounds__(kDecThreads)
+constexpr int kDownWarps = 16;  // 512 threads: every K block of a row tile in flight at once for T = 1
+
+__global__ void __launch_bounds__(kDownWarps * 32)
 dec_down_kernel(const DecodeLayerArgs a)
 {
-    __shared__ float red[kDecWarps][32][4];
+    __shared__ float red[kDownWarps][32][4];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int T = a.T, d = a.d, I = a.I, kpu = I / kKB, ngroups = I / 64;
+    pdl_trigger();
+    if (threadIdx.x == 0 && blockIdx.x == 0) bulk_prefetch_l2(a.sh_down_q, static_cast<uint32_t>(d) * (I / 2));
+    pdl_wait();
     const int n_units = *a.n_units;
     if (n_units < 1 || n_units > a.top_k * T + 1) {  // the h buffer holds top_k * T + 1 units
         if (threadIdx.x == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
@@ -394,13 +454,13 @@ dec_down_kernel(const DecodeLayerArgs a)
     for (int task = blockIdx.x; task < d / 16; task += gridDim.x) {
         const int j0 = task * 16;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int kb0 = warp; kb0 < n_kb; kb0 += 2 * kDecWarps) {
-            uint4 q[2], q8[2];
-            uint32_t sb[2], sb8[2];
-            uint2 bfr[2][8];
+        for (int kb0 = warp; kb0 < n_kb; kb0 += 3 * kDownWarps) {
+            uint4 q[3], q8[3];
+            uint32_t sb[3], sb8[3];
+            uint2 bfr[3][8];
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int kb = kb0 + m * kDecWarps;
+            for (int m = 0; m < 3; ++m) {
+                const int kb = kb0 + m * kDownWarps;
                 if (kb < n_kb) {
                     const int u = kb / kpu, jb = kb - u * kpu;
                     int e = a.unit_expert[u];
@@ -424,15 +484,15 @@ dec_down_kernel(const DecodeLayerArgs a)
                 }
             }
 #pragma unroll
-            for (int m = 0; m < 2; ++m)
-                if (kb0 + m * kDecWarps < n_kb) mma_kblock(acc, q[m], q8[m], sb[m], sb8[m], bfr[m]);
+            for (int m = 0; m < 3; ++m)
+                if (kb0 + m * kDownWarps < n_kb) mma_kblock(acc, q[m], q8[m], sb[m], sb8[m], bfr[m]);
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) red[warp][lane][q] = acc[q];
         __syncthreads();
         if (warp == 0) {
 #pragma unroll
-            for (int p = 1; p < kDecWarps; ++p)
+            for (int p = 1; p < kDownWarps; ++p)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[q] += red[p][lane][q];
 #pragma unroll
@@ -461,9 +521,26 @@ cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStrea
         if ((e = cudaFuncSetAttribute(dec_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) != cudaSuccess) return e;
         configured = true;
     }
-    dec_route_kernel<<<(a.E + kDecWarps - 1) / kDecWarps, kDecThreads, decode_smem_route(a.T, a.d), stream>>>(a);
-    dec_gateup_kernel<<<num_sms, kDecThreads, decode_smem_gateup(a.T, a.d), stream>>>(a);
-    dec_down_kernel<<<std::min(num_sms, a.d / 16), kDecThreads, 0, stream>>>(a);
+    // programmatic dependent launches: each kernel starts while its predecessor finishes
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    cfg.gridDim = dim3((a.E + kDecWarps - 1) / kDecWarps);
+    cfg.dynamicSmemBytes = decode_smem_route(a.T, a.d);
+    if ((e = cudaLaunchKernelEx(&cfg, dec_route_kernel, a)) != cudaSuccess) return e;
+    cfg.gridDim = dim3(num_sms);
+    cfg.dynamicSmemBytes = decode_smem_gateup(a.T, a.d);
+    if ((e = cudaLaunchKernelEx(&cfg, dec_gateup_kernel, a)) != cudaSuccess) return e;
+    cfg.gridDim = dim3(std::min(num_sms, a.d / 16));
+    cfg.blockDim = dim3(kDownWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    if ((e = cudaLaunchKernelEx(&cfg, dec_down_kernel, a)) != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

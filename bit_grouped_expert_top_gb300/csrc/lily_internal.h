@@ -95,6 +95,7 @@ struct DecodeLayerArgs {
     float *trace_w;           // [T][top_k] or NULL
     // workspace
     uint16_t *x_cur;          // bf16 [T][d]
+    __half *xp;               // fp16 [8][d] layer input in the permuted B layout of the expert GEMVs (tokens >= T zero)
     float *logits;            // [T][E]
     int *n_units;             // [1]: distinct experts used + 1 (shared last)
     int *unit_expert;         // [top_k*T+1]
