@@ -38,6 +38,36 @@ constexpr int kMaxT = 8;
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Read-only loads issued as volatile asm, so that the compiler keeps them where
+// they are written (a plain read-only load may be moved past pdl_wait to its
+// first use, which would undo a prefetch meant to overlap the previous grid).
+__device__ __forceinline__ uint4 ld_early(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint16_t ld_early_u16(const uint16_t *p)
+{
+    uint16_t v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+// acc + dot of 8 bf16 weights with 8 bf16 activations (fp32).
+__device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x, float acc)
+{
+    const uint32_t wu[4] = {w.x, w.y, w.z, w.w}, xu[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float2 wf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wu[p]));
+        const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xu[p]));
+        acc = fmaf(wf.x, xf.x, acc);
+        acc = fmaf(wf.y, xf.y, acc);
+    }
+    return acc;
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -87,7 +117,7 @@ dec_route_kernel(const DecodeLayerArgs a)
 #pragma unroll
     for (int m = 0; m < kPre; ++m) {
         const int c = lane + 32 * m;
-        if (e < a.E && c < n8) wpre[m] = __ldg(wrow + c);
+        if (e < a.E && c < n8) wpre[m] = ld_early(wrow + c);
     }
 
     pdl_trigger();
@@ -98,16 +128,21 @@ dec_route_kernel(const DecodeLayerArgs a)
         for (int i = threadIdx.x; i < T * d / 8; i += kDecThreads)
             reinterpret_cast<uint4 *>(xs)[i] = reinterpret_cast<const uint4 *>(a.x_in)[i];
     } else {
+        // two passes over the previous output, each with all of a thread's loads in
+        // flight at once (d <= 4096: at most 4 float4 per thread and token)
+        const int d4 = d / 4;
+        const float4 *po = reinterpret_cast<const float4 *>(a.prev_out);
         float ss[kMaxT];
 #pragma unroll
         for (int t = 0; t < kMaxT; ++t) ss[t] = 0.0f;
-#pragma unroll 4
-        for (int c = threadIdx.x; c < d; c += kDecThreads) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = threadIdx.x + j * kDecThreads;
 #pragma unroll
             for (int t = 0; t < kMaxT; ++t)
-                if (t < T) {
-                    const float v = a.prev_out[static_cast<size_t>(t) * d + c];
-                    ss[t] = fmaf(v, v, ss[t]);
+                if (t < T && c < d4) {
+                    const float4 v = __ldcg(po + static_cast<size_t>(t) * d4 + c);
+                    ss[t] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[t]))));
                 }
         }
 #pragma unroll
@@ -122,9 +157,20 @@ dec_route_kernel(const DecodeLayerArgs a)
             inv_rms[threadIdx.x] = 1.0f / sqrtf(s / static_cast<float>(d) + 1e-6f);
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < T * d; i += kDecThreads) {
-            const int t = i / d;
-            xs[i] = __float2bfloat16_rn(a.prev_out[i] * inv_rms[t]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = threadIdx.x + j * kDecThreads;
+#pragma unroll
+            for (int t = 0; t < kMaxT; ++t)
+                if (t < T && c < d4) {
+                    const float4 v = __ldcg(po + static_cast<size_t>(t) * d4 + c);
+                    const float r = inv_rms[t];
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * r, v.y * r), hi = __floats2bfloat162_rn(v.z * r, v.w * r);
+                    uint2 o;
+                    o.x = *reinterpret_cast<const uint32_t *>(&lo);
+                    o.y = *reinterpret_cast<const uint32_t *>(&hi);
+                    *reinterpret_cast<uint2 *>(xs + static_cast<size_t>(t) * d + 4 * c) = o;
+                }
         }
     }
     __syncthreads();
@@ -165,41 +211,24 @@ dec_route_kernel(const DecodeLayerArgs a)
 
     // ---- router GEMV: one warp per expert
     if (e < a.E) {
-        float acc[kMaxT];
-#pragma unroll
-        for (int t = 0; t < kMaxT; ++t) acc[t] = 0.0f;
-        for (int m0 = 0; m0 * 32 < n8; m0 += kPre) {
+        // compact code (one token per loop trip): this kernel runs once per layer,
+        // so its instructions are fetched cold and unrolled copies cost fetch time
+        const float bias = a.router_bias ? a.router_bias[e] : 0.0f;
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            const uint4 *xrow = reinterpret_cast<const uint4 *>(xs + static_cast<size_t>(t) * d);
+            float acc = 0.0f;
 #pragma unroll
             for (int m = 0; m < kPre; ++m) {
-                const int c = lane + 32 * (m0 + m);
-                if (c >= n8) continue;
-                const uint4 wv = m0 == 0 ? wpre[m] : __ldg(wrow + c);
-                const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                for (int t = 0; t < kMaxT; ++t) {
-                    if (t < T) {
-                        const uint4 xv = reinterpret_cast<const uint4 *>(xs + static_cast<size_t>(t) * d)[c];
-                        const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            const float2 wf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wu[p]));
-                            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xu[p]));
-                            acc[t] = fmaf(wf.x, xf.x, acc[t]);
-                            acc[t] = fmaf(wf.y, xf.y, acc[t]);
-                        }
-                    }
-                }
+                const int c = lane + 32 * m;
+                if (c < n8) acc = dot8_bf16(wpre[m], xrow[c], acc);
             }
-        }
-        const float bias = a.router_bias ? a.router_bias[e] : 0.0f;
-#pragma unroll
-        for (int t = 0; t < kMaxT; ++t) {
-            if (t < T) {
-                const float s = warp_sum(acc[t]) + bias;
-                if (lane == 0) {
-                    a.logits[t * a.E + e] = s;
-                    if (a.trace_logits) a.trace_logits[t * a.E + e] = s;
-                }
+#pragma unroll 1
+            for (int c = lane + 32 * kPre; c < n8; c += 32) acc = dot8_bf16(__ldg(wrow + c), xrow[c], acc);
+            const float sum = warp_sum(acc) + bias;
+            if (lane == 0) {
+                a.logits[t * a.E + e] = sum;
+                if (a.trace_logits) a.trace_logits[t * a.E + e] = sum;
             }
         }
     }
@@ -242,7 +271,7 @@ __device__ __forceinline__ void mma_kblock(float (&d)[4], uint4 q_g, uint4 q_g8,
 // Scale and bias of this lane's group in a K block, packed (scale low, bias high).
 __device__ __forceinline__ uint32_t load_sb(const uint16_t *s_row, const uint16_t *b_row, int group)
 {
-    return static_cast<uint32_t>(__ldg(s_row + group)) | (static_cast<uint32_t>(__ldg(b_row + group)) << 16);
+    return static_cast<uint32_t>(ld_early_u16(s_row + group)) | (static_cast<uint32_t>(ld_early_u16(b_row + group)) << 16);
 }
 
 // gate/up: task = (unit, 32 rows of I); warp w takes rows 16 (w % 2) .. + 16
@@ -258,13 +287,41 @@ dec_gateup_kernel(const DecodeLayerArgs a)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int T = a.T, d = a.d, I = a.I, nkb = d / kKB, ngroups = d / 64;
+    const int tpu = I / 32;  // tasks per unit (32 rows of I each)
+    const int rt = warp & 1, ks = warp >> 1;
+
+    // One round of weight loads of a task: up to 4 K blocks of this warp, both
+    // matrices, rows g and g + 8 of its 16-row tile.
+    uint4 qg[4], qg8[4], qu[4], qu8[4];
+    uint32_t sg[4], sg8[4], su[4], su8[4];
+    auto issue_loads = [&](int e, int i0, int kb0) {
+        const bool sh = e < 0;
+        const size_t row_g = (sh ? 0 : static_cast<size_t>(e) * I) + i0 + g, row_g8 = row_g + 8;
+        const uint8_t *gq = sh ? a.sh_gate_q : a.gate_q, *uq = sh ? a.sh_up_q : a.up_q;
+        const uint16_t *gs = sh ? a.sh_gate_s : a.gate_s, *gb = sh ? a.sh_gate_b : a.gate_b;
+        const uint16_t *us = sh ? a.sh_up_s : a.up_s, *ub = sh ? a.sh_up_b : a.up_b;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int kb = kb0 + 4 * m;
+            if (kb < nkb) {
+                const size_t off = static_cast<size_t>(kb) * (kKB / 2) + t * 16;
+                qg[m] = ld_early(gq + row_g * (d / 2) + off);
+                qg8[m] = ld_early(gq + row_g8 * (d / 2) + off);
+                qu[m] = ld_early(uq + row_g * (d / 2) + off);
+                qu8[m] = ld_early(uq + row_g8 * (d / 2) + off);
+                const int grp = 2 * kb + (t >> 1);
+                sg[m] = load_sb(gs + row_g * ngroups, gb + row_g * ngroups, grp);
+                sg8[m] = load_sb(gs + row_g8 * ngroups, gb + row_g8 * ngroups, grp);
+                su[m] = load_sb(us + row_g * ngroups, ub + row_g * ngroups, grp);
+                su8[m] = load_sb(us + row_g8 * ngroups, ub + row_g8 * ngroups, grp);
+            }
+        }
+    };
     pdl_trigger();
-    if (threadIdx.x == 0 && blockIdx.x < 2) {
-        // the shared expert is always used: warm L2 with its gate (CTA 0) / up (CTA 1)
-        // rows while the routing kernel finishes
-        const uint8_t *q = blockIdx.x == 0 ? a.sh_gate_q : a.sh_up_q;
-        bulk_prefetch_l2(q, static_cast<uint32_t>(I) * (d / 2));
-    }
+    // The shared expert is unit 0 and does not depend on the routing: its CTAs
+    // issue their first weight loads before waiting for the router.
+    const bool preloaded = blockIdx.x < tpu;
+    if (preloaded) issue_loads(-1, blockIdx.x * 32 + rt * 16, ks);
     pdl_wait();
     // the fp16 input goes to shared memory asynchronously; the first round of
     // weight loads is issued before waiting for it
@@ -273,8 +330,9 @@ dec_gateup_kernel(const DecodeLayerArgs a)
     cp_async_commit();
     bool xp_ready = false;
 
-    // Top-8 per token and the list of distinct experts ("units", ascending, the
-    // shared expert last with weight 1), computed by every CTA from the logits;
+    // Top-8 per token and the list of distinct experts ("units": the shared
+    // expert first with weight 1, then the routed experts ascending), computed by
+    // every CTA from the logits;
     // CTA 0 publishes it for the down projection and the trace.
     __shared__ int umask[256];
     __shared__ float uw[256][kMaxT];
@@ -317,7 +375,7 @@ dec_gateup_kernel(const DecodeLayerArgs a)
             if (w < warp) off += scan_tmp[w];
             n_used += scan_tmp[w];
         }
-        const int u = off + incl - used;
+        const int u = 1 + off + incl - used;
         if (used) {
             s_expert[u] = threadIdx.x;
 #pragma unroll
@@ -330,23 +388,21 @@ dec_gateup_kernel(const DecodeLayerArgs a)
             }
         }
         if (threadIdx.x == 0) {
-            s_expert[n_used] = -1;  // shared expert
+            s_expert[0] = -1;  // shared expert
 #pragma unroll
-            for (int q = 0; q < kMaxT; ++q) s_w[n_used][q] = 1.0f;
+            for (int q = 0; q < kMaxT; ++q) s_w[0][q] = 1.0f;
             s_n_units = n_used + 1;
             if (blockIdx.x == 0) {
-                a.unit_expert[n_used] = -1;
-                a.unit_mask[n_used] = (1 << T) - 1;
+                a.unit_expert[0] = -1;
+                a.unit_mask[0] = (1 << T) - 1;
 #pragma unroll
-                for (int q = 0; q < kMaxT; ++q) a.unit_w[n_used * kMaxT + q] = 1.0f;
+                for (int q = 0; q < kMaxT; ++q) a.unit_w[q] = 1.0f;
                 *a.n_units = n_used + 1;
             }
         }
         __syncthreads();
     }
     const int n_units = s_n_units;
-    const int tpu = I / 32;  // tasks per unit
-    const int rt = warp & 1, ks = warp >> 1;
     if (blockIdx.x >= n_units * tpu) {
         cp_async_wait_all();  // no copy into shared memory in flight at exit
         return;
@@ -355,33 +411,11 @@ dec_gateup_kernel(const DecodeLayerArgs a)
         const int u = task / tpu;
         const int i0 = (task - u * tpu) * 32 + rt * 16;
         const int e = s_expert[u];
-        const bool sh = e < 0;
-        const size_t row_g = (sh ? 0 : static_cast<size_t>(e) * I) + i0 + g, row_g8 = row_g + 8;
-        const uint8_t *gq = sh ? a.sh_gate_q : a.gate_q, *uq = sh ? a.sh_up_q : a.up_q;
-        const uint16_t *gs = sh ? a.sh_gate_s : a.gate_s, *gb = sh ? a.sh_gate_b : a.gate_b;
-        const uint16_t *us = sh ? a.sh_up_s : a.up_s, *ub = sh ? a.sh_up_b : a.up_b;
         float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
         for (int r0 = 0; r0 < nkb; r0 += 4 * 4) {  // rounds: the same count in every warp
             const int kb0 = r0 + ks;
             // up to 4 K blocks of this warp: all loads first, then the MMAs
-            uint4 qg[4], qg8[4], qu[4], qu8[4];
-            uint32_t sg[4], sg8[4], su[4], su8[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int kb = kb0 + 4 * m;
-                if (kb < nkb) {
-                    const size_t off = static_cast<size_t>(kb) * (kKB / 2) + t * 16;
-                    qg[m] = __ldg(reinterpret_cast<const uint4 *>(gq + row_g * (d / 2) + off));
-                    qg8[m] = __ldg(reinterpret_cast<const uint4 *>(gq + row_g8 * (d / 2) + off));
-                    qu[m] = __ldg(reinterpret_cast<const uint4 *>(uq + row_g * (d / 2) + off));
-                    qu8[m] = __ldg(reinterpret_cast<const uint4 *>(uq + row_g8 * (d / 2) + off));
-                    const int grp = 2 * kb + (t >> 1);
-                    sg[m] = load_sb(gs + row_g * ngroups, gb + row_g * ngroups, grp);
-                    sg8[m] = load_sb(gs + row_g8 * ngroups, gb + row_g8 * ngroups, grp);
-                    su[m] = load_sb(us + row_g * ngroups, ub + row_g * ngroups, grp);
-                    su8[m] = load_sb(us + row_g8 * ngroups, ub + row_g8 * ngroups, grp);
-                }
-            }
+            if (!(preloaded && task == blockIdx.x && r0 == 0)) issue_loads(e, i0, kb0);
             if (!xp_ready) {
                 cp_async_wait_all();
                 __syncthreads();
@@ -442,8 +476,27 @@ dec_down_kernel(const DecodeLayerArgs a)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int T = a.T, d = a.d, I = a.I, kpu = I / kKB, ngroups = I / 64;
+    uint4 q[3], q8[3];
+    uint32_t sb[3], sb8[3];
+    uint2 bfr[3][8];
+    // weight loads of K block kb (unit u, block jb) for output rows j0 + g, j0 + g + 8
+    auto load_w = [&](int m, int e, int jb, int j0) {
+        const bool sh = e < 0;
+        const size_t row = (sh ? 0 : static_cast<size_t>(e) * d) + j0 + g;
+        const uint8_t *dq = sh ? a.sh_down_q : a.down_q;
+        const uint16_t *ds = sh ? a.sh_down_s : a.down_s, *db = sh ? a.sh_down_b : a.down_b;
+        const size_t off = static_cast<size_t>(jb) * (kKB / 2) + t * 16;
+        q[m] = ld_early(dq + row * (I / 2) + off);
+        q8[m] = ld_early(dq + (row + 8) * (I / 2) + off);
+        const int grp = 2 * jb + (t >> 1);
+        sb[m] = load_sb(ds + row * ngroups, db + row * ngroups, grp);
+        sb8[m] = load_sb(ds + (row + 8) * ngroups, db + (row + 8) * ngroups, grp);
+    };
     pdl_trigger();
-    if (threadIdx.x == 0 && blockIdx.x == 0) bulk_prefetch_l2(a.sh_down_q, static_cast<uint32_t>(d) * (I / 2));
+    // unit 0 is the shared expert: the warps whose first K block lies in it issue
+    // those weight loads before waiting for the gate/up kernel
+    const bool preloaded = warp < kpu && blockIdx.x < d / 16;
+    if (preloaded) load_w(0, -1, warp, blockIdx.x * 16);
     pdl_wait();
     const int n_units = *a.n_units;
     if (n_units < 1 || n_units > a.top_k * T + 1) {  // the h buffer holds top_k * T + 1 units
@@ -455,32 +508,23 @@ dec_down_kernel(const DecodeLayerArgs a)
         const int j0 = task * 16;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int kb0 = warp; kb0 < n_kb; kb0 += 3 * kDownWarps) {
-            uint4 q[3], q8[3];
-            uint32_t sb[3], sb8[3];
-            uint2 bfr[3][8];
 #pragma unroll
             for (int m = 0; m < 3; ++m) {
                 const int kb = kb0 + m * kDownWarps;
                 if (kb < n_kb) {
                     const int u = kb / kpu, jb = kb - u * kpu;
-                    int e = a.unit_expert[u];
-                    if (e >= a.E) {
-                        if (lane == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
-                        e = 0;
+                    if (!(preloaded && m == 0 && task == blockIdx.x && kb0 == warp)) {
+                        int e = a.unit_expert[u];
+                        if (e >= a.E) {
+                            if (lane == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
+                            e = 0;
+                        }
+                        load_w(m, e, jb, j0);
                     }
-                    const bool sh = e < 0;
-                    const size_t row = (sh ? 0 : static_cast<size_t>(e) * d) + j0 + g;
-                    const uint8_t *dq = sh ? a.sh_down_q : a.down_q;
-                    const uint16_t *ds = sh ? a.sh_down_s : a.down_s, *db = sh ? a.sh_down_b : a.down_b;
-                    const size_t off = static_cast<size_t>(jb) * (kKB / 2) + t * 16;
-                    q[m] = __ldg(reinterpret_cast<const uint4 *>(dq + row * (I / 2) + off));
-                    q8[m] = __ldg(reinterpret_cast<const uint4 *>(dq + (row + 8) * (I / 2) + off));
-                    const int grp = 2 * jb + (t >> 1);
-                    sb[m] = load_sb(ds + row * ngroups, db + row * ngroups, grp);
-                    sb8[m] = load_sb(ds + (row + 8) * ngroups, db + (row + 8) * ngroups, grp);
+                    // token column g of h' is zero for g >= T: no load
                     const uint2 *src = reinterpret_cast<const uint2 *>(a.h) + ((kb * 8 + g) * 4 + t) * 8;
 #pragma unroll
-                    for (int s2 = 0; s2 < 8; ++s2) bfr[m][s2] = __ldcg(src + s2);
+                    for (int s2 = 0; s2 < 8; ++s2) bfr[m][s2] = g < T ? __ldcg(src + s2) : make_uint2(0u, 0u);
                 }
             }
 #pragma unroll
