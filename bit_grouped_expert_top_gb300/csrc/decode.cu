@@ -132,23 +132,19 @@ dec_route_kernel(const DecodeLayerArgs a)
         // flight at once (d <= 4096: at most 4 float4 per thread and token)
         const int d4 = d / 4;
         const float4 *po = reinterpret_cast<const float4 *>(a.prev_out);
-        float ss[kMaxT];
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {  // one token per loop trip: compact code
+            float ss = 0.0f;
 #pragma unroll
-        for (int t = 0; t < kMaxT; ++t) ss[t] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int c = threadIdx.x + j * kDecThreads;
-#pragma unroll
-            for (int t = 0; t < kMaxT; ++t)
-                if (t < T && c < d4) {
+            for (int j = 0; j < 4; ++j) {
+                const int c = threadIdx.x + j * kDecThreads;
+                if (c < d4) {
                     const float4 v = __ldcg(po + static_cast<size_t>(t) * d4 + c);
-                    ss[t] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[t]))));
+                    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
                 }
-        }
-#pragma unroll
-        for (int t = 0; t < kMaxT; ++t) {
-            const float s = warp_sum(ss[t]);
-            if (lane == 0) red[warp][t] = s;
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) red[warp][t] = ss;
         }
         __syncthreads();
         if (threadIdx.x < T) {
@@ -157,20 +153,21 @@ dec_route_kernel(const DecodeLayerArgs a)
             inv_rms[threadIdx.x] = 1.0f / sqrtf(s / static_cast<float>(d) + 1e-6f);
         }
         __syncthreads();
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            const float r = inv_rms[t];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int c = threadIdx.x + j * kDecThreads;
-#pragma unroll
-            for (int t = 0; t < kMaxT; ++t)
-                if (t < T && c < d4) {
+            for (int j = 0; j < 4; ++j) {
+                const int c = threadIdx.x + j * kDecThreads;
+                if (c < d4) {
                     const float4 v = __ldcg(po + static_cast<size_t>(t) * d4 + c);
-                    const float r = inv_rms[t];
                     const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * r, v.y * r), hi = __floats2bfloat162_rn(v.z * r, v.w * r);
                     uint2 o;
                     o.x = *reinterpret_cast<const uint32_t *>(&lo);
                     o.y = *reinterpret_cast<const uint32_t *>(&hi);
                     *reinterpret_cast<uint2 *>(xs + static_cast<size_t>(t) * d + 4 * c) = o;
                 }
+            }
         }
     }
     __syncthreads();
