@@ -132,8 +132,8 @@ dec_route_kernel(const DecodeLayerArgs a)
         // flight at once (d <= 4096: at most 4 float4 per thread and token)
         const int d4 = d / 4;
         const float4 *po = reinterpret_cast<const float4 *>(a.prev_out);
-#pragma unroll 1
-        for (int t = 0; t < T; ++t) {  // one token per loop trip: compact code
+#pragma unroll 4
+        for (int t = 0; t < T; ++t) {  // up to four tokens' loads in flight together
             float ss = 0.0f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -153,7 +153,7 @@ dec_route_kernel(const DecodeLayerArgs a)
             inv_rms[threadIdx.x] = 1.0f / sqrtf(s / static_cast<float>(d) + 1e-6f);
         }
         __syncthreads();
-#pragma unroll 1
+#pragma unroll 4
         for (int t = 0; t < T; ++t) {
             const float r = inv_rms[t];
 #pragma unroll

@@ -590,8 +590,8 @@ __device__ __forceinline__ void warp_top8_keys(const float (&lv)[8], int lane, i
     cmpx_desc(k[2], k[4]); cmpx_desc(k[3], k[5]);
     cmpx_desc(k[1], k[4]); cmpx_desc(k[3], k[6]);
     cmpx_desc(k[1], k[2]); cmpx_desc(k[3], k[4]); cmpx_desc(k[5], k[6]);
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll 1
+    for (int m = 1; m < 32; m <<= 1) {  // not unrolled: short code, fetched once per kernel
         unsigned long long o[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) o[j] = __shfl_xor_sync(0xffffffffu, k[7 - j], m);
