@@ -208,7 +208,7 @@ def lily_moe_forward(shape, weights, x, out, ws, routing=None, stream=None, *, c
 def lily_moe_forward_timed(shape, weights, x, out, ws, events: Sequence[torch.cuda.Event], routing=None,
                            stream=None, *, check: bool = True) -> int:
     """As lily_moe_forward, recording 6 events (start, after router GEMM, after
-    routing tables, after zeroing out, after gate/up, after down)."""
+    routing tables, after the routing-order copy of x, after gate/up, after down)."""
     assert len(events) == 6
     for e in events:
         if not e.cuda_event:  # torch creates the CUDA event on first record

@@ -301,7 +301,7 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
         !tmap_q4(&tmSU, w.sh_up.q, s.d, s.I) || !tmap_q4(&tmSD, w.sh_down.q, s.I, s.d))
         return cudaErrorInvalidValue;
 
-    cudaError_t e = launch_prep_experts(x, r.perm, xs, out, s.T, s.d, s.top_k, &ctrl->status, stream);
+    cudaError_t e = launch_prep_experts(x, r.perm, xs, s.T, s.d, s.top_k, &ctrl->status, stream);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[3], stream)) != cudaSuccess) return e;
 

@@ -20,6 +20,8 @@
 //   warp 2        B producer: 2-D TMA of contiguous token rows: x (router),
 //                 x in routing order (gate/up; written by the prep kernel),
 //                 h (down);
+//   warp 3        gate/up mode: zeroes this CTA's slice of `out` for the down
+//                 projection while the GEMM runs;
 //   warp 1        TMEM allocator + single-thread tcgen05.mma issuer;
 //   warps 4..11   dequantisers (expert modes): int4 -> fp16, one row per
 //                 thread, each warp 32 rows of one matrix on its own pace,
@@ -352,6 +354,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 }
             }
             drain_ring(S.full_b, NSLOT, issued, status);
+        } else if (MODE == kModeGateUp && warp == 3) {
+            // out = 0 for the down projection that follows: this CTA's slice,
+            // written while the GEMM runs instead of in a separate pass
+            const int64_t n4 = static_cast<int64_t>(g.T) * g.d / 4;
+            const int64_t per = (n4 + gridDim.x - 1) / gridDim.x;
+            const int64_t b0 = blockIdx.x * per, b1 = min(n4, b0 + per);
+            float4 *o = reinterpret_cast<float4 *>(g.out);
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int64_t i = b0 + lane; i < b1; i += 32) o[i] = z;
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -654,56 +665,71 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
 // Before the expert GEMMs: xs = fp16(x) in routing order with K permuted
 // inside each group of 8 (the order the dequantisers write the weights in):
 // row p < T top_k is token perm[p] / top_k, row T top_k + t is token t (the
-// shared expert's rows); and out = 0.  Flat grid-stride loop, 8 elements per
-// thread and iteration, so the 16-byte stores stream in order.
-__global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, const int *perm, uint4 *xs, float4 *out,
-                                                           int T, int d8, int top_k, int *status)
+// shared expert's rows).  One warp per row; each lane has up to 8 16-byte
+// loads in flight before it converts and stores them (x itself is L2-resident
+// after the router GEMM read it).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_kperm(const uint4 v)
 {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 q = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
+        f[2 * j] = q.x;
+        f[2 * j + 1] = q.y;
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // slot pair j holds elements (j, j + 4)
+        const __half2 hv = __floats2half2_rn(f[j], f[j + 4]);
+        o[j] = *reinterpret_cast<const uint32_t *>(&hv);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, const int *perm, uint4 *xs, int T, int d8,
+                                                           int top_k, int *status)
+{
+    const int lane = threadIdx.x & 31;
     const int64_t routed = static_cast<int64_t>(T) * top_k;
-    const int64_t n = (routed + T) * d8;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * 256;
-    for (int64_t q = blockIdx.x * 256LL + threadIdx.x; q < n; q += stride) {
-        const int64_t p = q / d8;
-        const int i = static_cast<int>(q - p * d8);
+    const int64_t rows = routed + T;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * 8;
+    for (int64_t p = blockIdx.x * 8LL + (threadIdx.x >> 5); p < rows; p += stride) {
         int t = p < routed ? __ldg(perm + p) / top_k : static_cast<int>(p - routed);
         if (t < 0 || t >= T) {
-            record_error(status, kErrDeviceIndex);
+            if (lane == 0) record_error(status, kErrDeviceIndex);
             t = 0;
         }
-        const uint4 v = __ldg(x + static_cast<int64_t>(t) * d8 + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float f[8];
+        const uint4 *src = x + static_cast<int64_t>(t) * d8;
+        uint4 *dst = xs + p * d8;
+        for (int i0 = 0; i0 < d8; i0 += 256) {
+            uint4 v[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 qq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
-            f[2 * j] = qq.x;
-            f[2 * j + 1] = qq.y;
-        }
-        uint32_t o[4];
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j * 32 + lane;
+                if (i < d8) v[j] = __ldg(src + i);
+            }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // slot pair j holds elements (j, j + 4)
-            const __half2 hv = __floats2half2_rn(f[j], f[j + 4]);
-            o[j] = *reinterpret_cast<const uint32_t *>(&hv);
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j * 32 + lane;
+                if (i < d8) dst[i] = bf16x8_to_f16x8_kperm(v[j]);
+            }
         }
-        xs[q] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    const int64_t n4 = static_cast<int64_t>(T) * d8 * 2;
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t q = blockIdx.x * 256LL + threadIdx.x; q < n4; q += stride) out[q] = z;
 }
 
 }  // namespace
 
-cudaError_t launch_prep_experts(const uint16_t *x, const int *perm, __half *xs, float *out, int T, int d, int top_k,
-                                int *status, cudaStream_t stream)
+cudaError_t launch_prep_experts(const uint16_t *x, const int *perm, __half *xs, int T, int d, int top_k, int *status,
+                                cudaStream_t stream)
 {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t n = static_cast<int64_t>(T) * (top_k + 1) * (d / 8);
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(sms) * 16)));
-    prep_experts_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(x), perm, reinterpret_cast<uint4 *>(xs),
-                                                  reinterpret_cast<float4 *>(out), T, d / 8, top_k, status);
+    const int64_t rows = static_cast<int64_t>(T) * (top_k + 1);
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 8)));
+    prep_experts_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(x), perm, reinterpret_cast<uint4 *>(xs), T,
+                                                  d / 8, top_k, status);
     return cudaGetLastError();
 }
 

@@ -48,10 +48,11 @@ struct GemmArgs {
 // Dynamic shared memory bytes of grouped_gemm_kernel.
 size_t grouped_gemm_smem_bytes();
 
-// Before the expert GEMMs: out = 0 and xs = fp16(x) in routing order (routed
-// rows by perm, then the T shared-expert rows), [(top_k+1)*T][d].
-cudaError_t launch_prep_experts(const uint16_t *x, const int *perm, __half *xs, float *out, int T, int d, int top_k,
-                                int *status, cudaStream_t stream);
+// Before the expert GEMMs: xs = fp16(x) in routing order (routed rows by perm,
+// then the T shared-expert rows), [(top_k+1)*T][d].  (out is zeroed by the
+// gate/up GEMM launch.)
+cudaError_t launch_prep_experts(const uint16_t *x, const int *perm, __half *xs, int T, int d, int top_k, int *status,
+                                cudaStream_t stream);
 
 // tmB: B operand rows (x for the router, xs for gate/up, h for down).
 // tmA0/tmA1: routed weight maps of the two 128-row tiles (router: Wr for both);

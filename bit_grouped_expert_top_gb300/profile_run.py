@@ -4,8 +4,8 @@
   python -m bit_grouped_expert_top_gb300.profile_run --config decode_t1_l40 --layers 4 --T 1 --reps 3
 
 Each pass launches, in order: router GEMM, top-8 + per-chunk counts, per-expert
-scan + block map, scatter, prep (fp16 x in routing order, out = 0), gate/up
-GEMM + SwiGLU, down GEMM + weighted combine.  Exits non-zero if the device
+scan + block map, scatter, prep (fp16 x in routing order), gate/up GEMM +
+SwiGLU (which also zeroes out), down GEMM + weighted combine.  Exits non-zero if the device
 status word reports an error.
 """
 from __future__ import annotations

@@ -193,8 +193,8 @@ int lily_moe_forward(const lily_moe_shape *shape, const lily_moe_weights *w, con
 /*
  * lily_moe_forward with stage timing: if `events` is non-NULL it must hold 6
  * created CUDA events, recorded on `stream` at: start, after the router GEMM,
- * after the routing tables, after zeroing out, after the gate/up GEMM, after
- * the down GEMM.
+ * after the routing tables, after the routing-order copy of x, after the
+ * gate/up GEMM (which also zeroes out), after the down GEMM.
  */
 int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,
                            float *out, lily_moe_routing *r, void *ws, size_t ws_bytes,
