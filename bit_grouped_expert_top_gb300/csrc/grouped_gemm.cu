@@ -585,21 +585,45 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 const uint32_t t0 = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(ab * 2 * kTileM);
                 const uint32_t t1 = t0 + kTileM;
                 if (MODE == kModeGateUp) {
+                    // this thread's column chunks c0 = 16 half + 32 q: h = silu(gate) up
+                    // packed as fp16 pairs in registers, so the accumulator is released
+                    // before the stores
+                    uint32_t hp[kTileN / 32][8];
+#pragma unroll
+                    for (int q = 0; q < kTileN / 32; ++q) {
+                        const int c0 = half * 16 + 32 * q;
+                        if (c0 < u.n_mma) {
+                            uint32_t v0[16], v1[16];
+                            tmem_ld_32x32b_x16(t0 + c0, v0);
+                            tmem_ld_32x32b_x16(t1 + c0, v1);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const __half2 hv = __floats2half2_rn(
+                                    silu_f(__uint_as_float(v0[2 * j])) * __uint_as_float(v1[2 * j]),
+                                    silu_f(__uint_as_float(v0[2 * j + 1])) * __uint_as_float(v1[2 * j + 1]));
+                                hp[q][j] = *reinterpret_cast<const uint32_t *>(&hv);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.empty_acc[ab]);
                     // h columns in the K order of dequant8_f16_kperm (the down GEMM's A)
                     const int hcol = kperm8(u.mt * kTileM + et);
                     const size_t prow0 = u.shared ? static_cast<size_t>(g.T) * g.top_k + u.p0 : static_cast<size_t>(u.p0);
                     __half *hbase = g.h + prow0 * g.I + hcol;
-                    for (int c0 = half * 16; c0 < u.n_mma; c0 += 32) {
-                        uint32_t v0[16], v1[16];
-                        tmem_ld_32x32b_x16(t0 + c0, v0);
-                        tmem_ld_32x32b_x16(t1 + c0, v1);
-                        tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int n = c0 + j;
-                            if (n < u.rows)
-                                hbase[static_cast<size_t>(n) * g.I] =
-                                    __float2half_rn(silu_f(__uint_as_float(v0[j])) * __uint_as_float(v1[j]));
+                    for (int q = 0; q < kTileN / 32; ++q) {
+                        const int c0 = half * 16 + 32 * q;
+                        if (c0 < u.n_mma) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int n = c0 + j;
+                                if (n < u.rows)
+                                    hbase[static_cast<size_t>(n) * g.I] =
+                                        __ushort_as_half(static_cast<unsigned short>(hp[q][j >> 1] >> (16 * (j & 1))));
+                            }
                         }
                     }
                 } else if (MODE == kModeDown) {
@@ -643,9 +667,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         }
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.empty_acc[ab]);
+                if (MODE != kModeGateUp) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.empty_acc[ab]);
+                }
             }
             named_barrier_sync(kBarEpilogue, 256);  // ep_tok / ep_w free for the next unit
             if (++ab == n_acc) {
