@@ -20,9 +20,11 @@
 //   warp 2        B producer: 2-D TMA of contiguous token rows: x (router),
 //                 x in routing order (gate/up; written by the prep kernel),
 //                 h (down);
-//   warp 3        gate/up mode: zeroes this CTA's slice of `out` for the down
-//                 projection while the GEMM runs;
-//   warp 1        TMEM allocator + single-thread tcgen05.mma issuer;
+//   warps 1, 3    tcgen05.mma issuers, one thread each: warp 1 the first
+//                 weight tile's accumulator, warp 3 the second's (one thread
+//                 alone cannot issue the MMAs as fast as the tensor core runs
+//                 them while the dequantisers share its SM sub-partition);
+//                 warp 1 also allocates TMEM;
 //   warps 4..11   dequantisers (expert modes): int4 -> fp16, one row per
 //                 thread, each warp 32 rows of one matrix on its own pace,
 //                 written to tensor memory with tcgen05.st; the MMA reads A
@@ -30,7 +32,9 @@
 //   warps 12..19  epilogue: tcgen05.ld from TMEM, then per mode the router
 //                 logits (+bias), SwiGLU into h (fp16), or the down projection
 //                 scaled by the routing weight and added (red.global.add.f32)
-//                 into token order.
+//                 into token order; in gate/up mode they first zero this CTA's
+//                 slice of `out` (for the down projection) while the first
+//                 unit's MMAs run.
 // The K loop runs in blocks of four 64-wide k-steps (one raw int4 stage, one
 // pass over the 4-stage tensor-memory A ring), so every ring slot and phase
 // parity inside a block is a compile-time constant and the single-thread roles
@@ -69,6 +73,7 @@ constexpr uint32_t kTmemCols = 512;
 // 256 + 128 h, matrix m at + 64 m, k-step j of the stage at + 32 j.
 constexpr uint32_t kTmemAOffset = 256;
 constexpr int kBarEpilogue = 3;  // named barrier id
+constexpr int kIssuers = 2;      // MMA-issuing threads (warps 1 and 3), one per weight tile
 static_assert(kBStages == kBlk && kAStages == 2 && kTAStages == 2, "ring slots are compile-time within a block");
 
 struct __align__(1024) Smem {
@@ -197,17 +202,17 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         }
         for (int s = 0; s < kBSlotBars; ++s) {
             mbar_init(&S.full_b[s], 1);
-            mbar_init(&S.empty_b[s], 1);
+            mbar_init(&S.empty_b[s], kIssuers);  // one commit per MMA issuer
         }
         for (int s = 0; s < kTAStages; ++s) {
             mbar_init(&S.full_a[s], dequant_mode ? 8 : 1);  // dequantiser warps / router TMA
-            mbar_init(&S.empty_a[s], 1);  // router only
+            mbar_init(&S.empty_a[s], kIssuers);  // router only
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&S.full_acc[s], 1);
+            mbar_init(&S.full_acc[s], kIssuers);
             mbar_init(&S.empty_acc[s], 8);
         }
-        mbar_init(&S.drain, 1);
+        mbar_init(&S.drain, kIssuers);
         S.abort_flag = 0;
         fence_mbar_init();
         if (MODE == kModeRouter && blockIdx.x == 0) g.ctrl->ticket = 0u;  // reset for the routing kernel
@@ -309,10 +314,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 drain_ring(S.full_a, kAStages, issued, status);
         }
         __syncwarp();
-    } else if (warp == 2 || warp == 3) {
-        // ------------------------------------------------ B producers (token rows)
-        const int bl = (warp - 2) * 32 + lane;  // 0..63
-        if (bl == 0) {
+    } else if (warp == 2) {
+        // ------------------------------------------------ B producer (token rows)
+        if (lane == 0) {
             // contiguous rows (x for the router; x in routing order for gate/up; h for
             // the down projection): one 2-D TMA per k-step
             int blk = 0, issued = 0;
@@ -354,19 +358,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 }
             }
             drain_ring(S.full_b, NSLOT, issued, status);
-        } else if (MODE == kModeGateUp && warp == 3) {
-            // out = 0 for the down projection that follows: this CTA's slice,
-            // written while the GEMM runs instead of in a separate pass
-            const int64_t n4 = static_cast<int64_t>(g.T) * g.d / 4;
-            const int64_t per = (n4 + gridDim.x - 1) / gridDim.x;
-            const int64_t b0 = blockIdx.x * per, b1 = min(n4, b0 + per);
-            float4 *o = reinterpret_cast<float4 *>(g.out);
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int64_t i = b0 + lane; i < b1; i += 32) o[i] = z;
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer (one thread)
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------ MMA issuers (one thread each)
+        // Thread of warp 1: the first weight tile (accumulator d0); warp 3: the
+        // second (d1).  Each accumulator has one issuer, so its MMAs keep their
+        // order; both wait for the same stages and both commit every release.
+        const int mat = warp == 1 ? 0 : 1;
         if (lane == 0) {
             int blk = 0, ab = 0;
             uint32_t acc_ph = 0;
@@ -384,8 +383,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 if (!mbar_wait(&S.empty_acc[ab], acc_ph ^ 1, abort_flag, status)) break;
                 tc_fence_after();
                 const uint32_t idesc = idesc_f32acc(fmt, kTileM, u.n_mma);
-                const uint32_t d0 = tmem_base + static_cast<uint32_t>(ab * 2 * kTileM);
-                const uint32_t d1 = d0 + kTileM;
+                const uint32_t dm = tmem_base + static_cast<uint32_t>(ab * 2 * kTileM + mat * kTileM);
                 for (int kb = 0; kb < KB && ok; ++kb, ++blk) {
                     const uint32_t bpar = (CYC == 2 ? (blk >> 1) : blk) & 1;
 #pragma unroll
@@ -404,21 +402,18 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                             if (dequant_mode) {
                                 // A from tensor memory: stage h at 128 h, matrix m at + 64 m,
                                 // k-step j at + 32 j (64 K elements = 32 columns)
-                                const uint32_t at = ta + static_cast<uint32_t>(h * 128 + j * 32);
+                                const uint32_t at = ta + static_cast<uint32_t>(h * 128 + j * 32 + mat * 64);
 #pragma unroll
                                 for (int kk = 0; kk < kBK / 16; ++kk) {
                                     const uint32_t acc = (kb | h | j | kk) != 0;
-                                    umma_ts(d0, at + kk * 8, desc64(blo + kk * 2, b_hi), idesc, acc);
-                                    umma_ts(d1, at + 64 + kk * 8, desc64(blo + kk * 2, b_hi), idesc, acc);
+                                    umma_ts(dm, at + kk * 8, desc64(blo + kk * 2, b_hi), idesc, acc);
                                 }
                             } else {
-                                const uint32_t alo = a_lo + static_cast<uint32_t>(as * (2 * kABytes >> 4));
+                                const uint32_t alo = a_lo + static_cast<uint32_t>(as * (2 * kABytes >> 4) + mat * (kABytes >> 4));
 #pragma unroll
                                 for (int kk = 0; kk < kBK / 16; ++kk) {
                                     const uint32_t acc = (kb | h | kk) != 0;
-                                    umma_ss(d0, desc64(alo + kk * 2, a_hi), desc64(blo + kk * 2, b_hi), idesc, acc);
-                                    umma_ss(d1, desc64(alo + (kABytes >> 4) + kk * 2, a_hi), desc64(blo + kk * 2, b_hi),
-                                            idesc, acc);
+                                    umma_ss(dm, desc64(alo + kk * 2, a_hi), desc64(blo + kk * 2, b_hi), idesc, acc);
                                 }
                             }
                         }
@@ -555,6 +550,16 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         uint32_t acc_ph = 0;
         bool ok = true;
         const int n_acc = dequant_mode ? 1 : 2;
+        if (MODE == kModeGateUp) {
+            // out = 0 for the down projection that follows: this CTA's slice,
+            // written while the first unit's MMAs run
+            const int64_t n4 = static_cast<int64_t>(g.T) * g.d / 4;
+            const int64_t per = (n4 + gridDim.x - 1) / gridDim.x;
+            const int64_t z0 = blockIdx.x * per, z1 = min(n4, z0 + per);
+            float4 *o = reinterpret_cast<float4 *>(g.out);
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int64_t i = z0 + eid; i < z1; i += 256) o[i] = z;
+        }
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             const Unit u = unit_info<MODE>(g, tile, n_routed);
             if (u.rows <= 0) continue;
