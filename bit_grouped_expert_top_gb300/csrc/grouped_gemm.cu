@@ -483,7 +483,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     }
                     const int rs = blk & 1;
                     const uint32_t rpar = (blk >> 1) & 1;
-                    const int jb = (kb & 1) * kBlk;  // first group of this block within the register block
+                    // this block's four groups of the 8-group register block
+                    const uint2 s_blk = (kb & 1) ? make_uint2(s_cur.z, s_cur.w) : make_uint2(s_cur.x, s_cur.y);
+                    const uint2 b_blk = (kb & 1) ? make_uint2(b_cur.z, b_cur.w) : make_uint2(b_cur.x, b_cur.y);
                     const uint8_t *rowp = S.raw[rs][mi] + r * kRawRow;
 #pragma unroll
                     for (int h = 0; h < SPB; ++h) {
@@ -507,18 +509,18 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
 #pragma unroll
                             for (int j = 0; j < SS; ++j) {
                                 const int jr = h * SS + j;  // k-step within the block
-                                const uint16_t sc = pick16(s_cur, jb + jr), bi = pick16(b_cur, jb + jr);
+                                const uint16_t sc = pick16x4(s_blk, jr), bi = pick16x4(b_blk, jr);
                                 // 128-byte rows written by TMA with the 128-byte swizzle:
                                 // 16-byte chunk c of row r sits at chunk c ^ (r % 8)
                                 const uint4 q0 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr) ^ sw) << 4));
                                 const uint4 q1 = *reinterpret_cast<const uint4 *>(rowp + (((2 * jr + 1) ^ sw) << 4));
-                                const __half2 s2 = half2_from_bf16_bits(sc), b2 = half2_from_bf16_bits(bi);
-                                const __half2 s2_16 = __hmul2(s2, __floats2half2_rn(0.0625f, 0.0625f));
+                                const __half2 b2 = half2_from_bf16_bits(bi);
+                                const __half2 s8 = __hmul2(half2_from_bf16_bits(sc), __floats2half2_rn(8.0f, 8.0f));
                                 const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                                 uint32_t cols[32];  // TMEM column 4c + i holds K positions 8c + 2i, 8c + 2i + 1
 #pragma unroll
                                 for (int cc = 0; cc < 8; ++cc) {
-                                    const uint4 o = dequant8_f16_kperm(words[cc], s2, s2_16, b2);
+                                    const uint4 o = dequant8_f16_e2m3(words[cc], s8, b2);
                                     cols[4 * cc + 0] = o.x;
                                     cols[4 * cc + 1] = o.y;
                                     cols[4 * cc + 2] = o.z;
@@ -614,8 +616,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&S.empty_acc[ab]);
-                    // h columns in the K order of dequant8_f16_kperm (the down GEMM's A)
-                    const int hcol = kperm8(u.mt * kTileM + et);
+                    // h columns in the K order of dequant8_f16_e2m3 (the down GEMM's A)
+                    const int hcol = kperm8_e2m3(u.mt * kTileM + et);
                     const size_t prow0 = u.shared ? static_cast<size_t>(g.T) * g.top_k + u.p0 : static_cast<size_t>(u.p0);
                     __half *hbase = g.h + prow0 * g.I + hcol;
 #pragma unroll
@@ -711,8 +713,9 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8_kperm(const uint4 v)
     }
     uint32_t o[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {  // slot pair j holds elements (j, j + 4)
-        const __half2 hv = __floats2half2_rn(f[j], f[j + 4]);
+    for (int j = 0; j < 4; ++j) {  // slot pairs (0,2) (4,6) (1,3) (5,7): the order of dequant8_f16_e2m3
+        const int e = (j & 1) * 4 + (j >> 1);
+        const __half2 hv = __floats2half2_rn(f[e], f[e + 2]);
         o[j] = *reinterpret_cast<const uint32_t *>(&hv);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);

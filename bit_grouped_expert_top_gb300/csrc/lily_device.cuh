@@ -474,6 +474,50 @@ __device__ __forceinline__ uint4 dequant8_f16_kperm(uint32_t v, __half2 s2, __ha
     return o;
 }
 
+// Two 6-bit e2m3 values (one per byte, low 6 bits) -> fp16 pair, low byte to
+// the low half.  A byte holding a nibble q in its low 4 bits (sign 0, exponent
+// bits 0 q3, mantissa q2 q1 q0) is exactly q / 8: subnormal q/8 for q < 8,
+// (1 + (q-8)/8) for q >= 8.
+__device__ __forceinline__ uint32_t cvt_e2m3x2_lo(uint32_t v)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e2m3x2 %0, lo;\n\t}" : "=r"(r) : "r"(v));
+    return r;
+}
+__device__ __forceinline__ uint32_t cvt_e2m3x2_hi(uint32_t v)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e2m3x2 %0, hi;\n\t}" : "=r"(r) : "r"(v));
+    return r;
+}
+
+// Eight packed 4-bit weights (element i in bits [4i, 4i+4)) -> eight fp16
+// weights w_i = q_i * s + b, each rounded once: the nibbles are spread one per
+// byte, converted to q/8 exactly (e2m3), then fma.rn.f16x2(q/8, 8 s, b), which
+// equals fma(q, s, b) because 8 s is exact.  `s8` = 8 s.  Output K order within
+// the group of 8: (0,2, 4,6, 1,3, 5,7); the other GEMM operand must use the same
+// order (kperm8_e2m3).
+__device__ __forceinline__ uint4 dequant8_f16_e2m3(uint32_t v, __half2 s8, __half2 b2)
+{
+    const uint32_t lo = v & 0x0F0F0F0Fu, hi = (v >> 4) & 0x0F0F0F0Fu;  // nibbles 0,2,4,6 / 1,3,5,7
+    const uint32_t q02 = cvt_e2m3x2_lo(lo), q46 = cvt_e2m3x2_hi(lo);
+    const uint32_t q13 = cvt_e2m3x2_lo(hi), q57 = cvt_e2m3x2_hi(hi);
+    __half2 f0 = __hfma2(*reinterpret_cast<const __half2 *>(&q02), s8, b2);
+    __half2 f1 = __hfma2(*reinterpret_cast<const __half2 *>(&q46), s8, b2);
+    __half2 f2 = __hfma2(*reinterpret_cast<const __half2 *>(&q13), s8, b2);
+    __half2 f3 = __hfma2(*reinterpret_cast<const __half2 *>(&q57), s8, b2);
+    return make_uint4(*reinterpret_cast<uint32_t *>(&f0), *reinterpret_cast<uint32_t *>(&f1),
+                      *reinterpret_cast<uint32_t *>(&f2), *reinterpret_cast<uint32_t *>(&f3));
+}
+
+// Position of logical K index k in the order used by dequant8_f16_e2m3: inside
+// each group of 8, even elements j at j/2, odd ones at 4 + j/2.
+__host__ __device__ __forceinline__ int kperm8_e2m3(int k)
+{
+    const int j = k & 7;
+    return (k & ~7) | ((j >> 1) + ((j & 1) << 2));
+}
+
 // Position of logical K index k in the order used by dequant8_f16_kperm:
 // inside each group of 8, element j sits at 2j (j < 4) or 2(j-4)+1 (j >= 4).
 __host__ __device__ __forceinline__ int kperm8(int k)
@@ -523,6 +567,13 @@ __device__ __forceinline__ uint4 load_groups8(const uint16_t *row, int g0, int n
     for (int j = 0; j < 8; ++j)
         if (g0 + j < n) w[j >> 1] |= static_cast<uint32_t>(__ldg(row + g0 + j)) << (16 * (j & 1));
     return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Value j (0..3) of four 16-bit values packed two per word.
+__device__ __forceinline__ uint16_t pick16x4(const uint2 v, int j)
+{
+    const uint32_t w = (j & 2) ? v.y : v.x;
+    return static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
 }
 
 // Value j (0..7) of a block loaded by load_groups8.
