@@ -64,6 +64,15 @@ def test_zero_routed_weights_leave_shared_expert():
     _full_check(cfg, 64, overrides=over)
 
 
+@pytest.mark.parametrize("I", [256, 384, 1024])
+def test_intermediate_sizes(I):
+    # K of the down projection is I: 4 and 8 k-steps run the down kernel with the
+    # unit's B resident in shared memory (384 pads 6 k-steps to 8 and has a group
+    # count that is not a multiple of 8); 1024 (16 k-steps) runs the general one.
+    cfg = TINY.with_(I=I, I_shared=I)
+    _full_check(cfg, 100, seed_offset=I)
+
+
 def test_medium_full_hidden_size():
     # d = 2048, I = 512 at a token count the oracle finishes in seconds:
     # many weight tiles per unit and ragged expert groups.
