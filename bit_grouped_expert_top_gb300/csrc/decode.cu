@@ -32,12 +32,6 @@ namespace {
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMaxT = 8;
-// Programmatic dependent launch: this grid lets the next one start launching,
-// and waits (before reading anything an earlier kernel wrote) until the
-// preceding grid has completed and its memory is visible.
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Read-only loads issued as volatile asm, so that the compiler keeps them where
 // they are written (a plain read-only load may be moved past pdl_wait to its
 // first use, which would undo a prefetch meant to overlap the previous grid).

@@ -215,7 +215,6 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         mbar_init(&S.drain, kIssuers);
         S.abort_flag = 0;
         fence_mbar_init();
-        if (MODE == kModeRouter && blockIdx.x == 0) g.ctrl->ticket = 0u;  // reset for the routing kernel
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA0);
@@ -235,6 +234,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem_base = S.tmem_base;
     volatile int *abort_flag = &S.abort_flag;
+    // the setup above overlaps the previous kernel's tail; global memory only from here
+    pdl_trigger();
+    pdl_wait();
+    if (MODE == kModeRouter && threadIdx.x == 0 && blockIdx.x == 0) g.ctrl->ticket = 0u;  // reset for the routing kernels
 
     int n_routed = 0;
     if (MODE != kModeRouter) {
@@ -728,6 +731,8 @@ __global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, const
     const int64_t routed = static_cast<int64_t>(T) * top_k;
     const int64_t rows = routed + T;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * 8;
+    pdl_trigger();
+    pdl_wait();  // the permutation is complete
     for (int64_t p = blockIdx.x * 8LL + (threadIdx.x >> 5); p < rows; p += stride) {
         int t = p < routed ? __ldg(perm + p) / top_k : static_cast<int>(p - routed);
         if (t < 0 || t >= T) {
@@ -762,9 +767,8 @@ cudaError_t launch_prep_experts(const uint16_t *x, const int *perm, __half *xs, 
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t rows = static_cast<int64_t>(T) * (top_k + 1);
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 8)));
-    prep_experts_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(x), perm, reinterpret_cast<uint4 *>(xs), T,
-                                                  d / 8, top_k, status);
-    return cudaGetLastError();
+    return launch_pdl(prep_experts_kernel, dim3(grid), dim3(256), 0, stream, reinterpret_cast<const uint4 *>(x), perm,
+                      reinterpret_cast<uint4 *>(xs), T, d / 8, top_k, status);
 }
 
 size_t grouped_gemm_smem_bytes() { return sizeof(Smem) + 1024; }
@@ -781,8 +785,8 @@ static cudaError_t launch_mode(const GemmArgs &g, const CUtensorMap &tmB, const 
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    grouped_gemm_kernel<MODE><<<grid, kThreads, smem, stream>>>(g, tmB, tmA0, tmA1, tmSA0, tmSA1);
-    return cudaGetLastError();
+    return launch_pdl(grouped_gemm_kernel<MODE>, dim3(grid), dim3(kThreads), smem, stream, g, tmB, tmA0, tmA1, tmSA0,
+                      tmSA1);
 }
 
 cudaError_t launch_grouped_gemm(const GemmArgs &g, const CUtensorMap &tmB, const CUtensorMap &tmA0,

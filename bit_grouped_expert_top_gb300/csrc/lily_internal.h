@@ -1,6 +1,7 @@
 // Internal host-side interface between the C-ABI entry points (api.cu) and the
 // kernel translation units.  Not part of the public ABI.
 #pragma once
+#include <utility>
 
 #include <cstdint>
 #include <cuda.h>
@@ -44,6 +45,26 @@ struct GemmArgs {
     float *out;              // down output [T][d], accumulated
     Ctrl *ctrl;
 };
+
+// Launches `kernel` as a programmatic dependent of the previous kernel in the
+// stream: it may start while that one finishes; it calls pdl_wait before its
+// first global memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Dynamic shared memory bytes of grouped_gemm_kernel.
 size_t grouped_gemm_smem_bytes();

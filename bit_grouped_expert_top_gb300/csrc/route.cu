@@ -65,6 +65,8 @@ topk_count_kernel(const RouteArgs a)
     const int chunk = blockIdx.x;
 
     hist[threadIdx.x] = 0;
+    pdl_trigger();
+    pdl_wait();  // the router's logits are complete
     __syncthreads();
 
     // each warp's tokens, the next token's logits loaded while this one is ranked
@@ -107,6 +109,8 @@ scan_kernel(const RouteArgs a)
     __shared__ int is_last;
     const int e = blockIdx.x;
     int carry = 0;
+    pdl_trigger();
+    pdl_wait();  // the per-chunk counts are complete
     for (int c0 = 0; c0 < a.n_chunks; c0 += kRouteThreads) {
         const int c = c0 + threadIdx.x;
         const size_t i = static_cast<size_t>(c) * kE + e;
@@ -156,6 +160,8 @@ scatter_kernel(const RouteArgs a)
     const int chunk = blockIdx.x;
     const int n_assign = kRouteChunkTokens * kTopK;  // 512 per chunk
     const int total = a.T * kTopK;
+    pdl_trigger();
+    pdl_wait();  // offsets and chunk bases are complete
 
     base[threadIdx.x] = a.offsets[threadIdx.x] + a.chunk_base[static_cast<size_t>(chunk) * kE + threadIdx.x];
     const unsigned lt_mask = (1u << lane) - 1u;
@@ -201,20 +207,17 @@ scatter_kernel(const RouteArgs a)
 
 cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream)
 {
-    topk_count_kernel<<<a.n_chunks, kRouteThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(topk_count_kernel, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
 }
 
 cudaError_t launch_route_scan(const RouteArgs &a, cudaStream_t stream)
 {
-    scan_kernel<<<kE, kRouteThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(scan_kernel, dim3(kE), dim3(kRouteThreads), 0, stream, a);
 }
 
 cudaError_t launch_scatter(const RouteArgs &a, cudaStream_t stream)
 {
-    scatter_kernel<<<a.n_chunks, kRouteThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(scatter_kernel, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
 }
 
 }  // namespace lily
