@@ -314,8 +314,15 @@ dec_gateup_kernel(const DecodeLayerArgs a)
     const bool preloaded = blockIdx.x < tpu;
     if (preloaded) issue_loads(-1, blockIdx.x * 32 + rt * 16, ks);
     pdl_wait();
-    // the fp16 input goes to shared memory asynchronously; the first round of
-    // weight loads is issued before waiting for it
+    // this token's logits first (the top-8 waits for them), then the fp16 input
+    // to shared memory asynchronously; the first round of weight loads is
+    // issued before waiting for it
+    float4 l0 = make_float4(0.f, 0.f, 0.f, 0.f), l1 = l0;
+    if (warp < T) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.logits + warp * a.E + lane * 8);
+        l0 = __ldcg(src);
+        l1 = __ldcg(src + 1);
+    }
     for (int i = threadIdx.x; i < d; i += kDecThreads)  // 8 x d fp16 = d uint4
         cp_async_16(reinterpret_cast<uint4 *>(xp) + i, reinterpret_cast<const uint4 *>(a.xp) + i);
     cp_async_commit();
@@ -337,8 +344,6 @@ dec_gateup_kernel(const DecodeLayerArgs a)
     __syncthreads();
     if (warp < T) {
         const int tok = warp;
-        const float4 *src = reinterpret_cast<const float4 *>(a.logits + tok * a.E + lane * 8);
-        const float4 l0 = __ldcg(src), l1 = __ldcg(src + 1);
         const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
         int sel_e;
         float sel_w;
