@@ -94,7 +94,7 @@ struct RouteArgs {
     int n_chunks;
     Ctrl *ctrl;
 };
-constexpr int kRouteChunkTokens = 64;
+constexpr int kRouteChunkTokens = 32;
 cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_route_scan(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_scatter(const RouteArgs &a, cudaStream_t stream);

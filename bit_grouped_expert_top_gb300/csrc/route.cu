@@ -158,7 +158,7 @@ scatter_kernel(const RouteArgs a)
     __shared__ int base[kE];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int chunk = blockIdx.x;
-    const int n_assign = kRouteChunkTokens * kTopK;  // 512 per chunk
+    const int n_assign = kRouteChunkTokens * kTopK;  // assignments per chunk
     const int total = a.T * kTopK;
     pdl_trigger();
     pdl_wait();  // offsets and chunk bases are complete
