@@ -34,7 +34,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // ------------------------------------------------------------------ workspace layouts
 struct PrefillLayout {
-    size_t ctrl, chunk_counts, chunk_base, h, xs, logits, idx, w, counts, offsets, perm, block_map, n_blocks, total;
+    size_t ctrl, chunk_counts, chunk_base, h, xs, inv, logits, idx, w, counts, offsets, perm, block_map, n_blocks, total;
 };
 
 int64_t block_capacity(const lily_moe_shape &s)
@@ -59,6 +59,7 @@ PrefillLayout prefill_layout(const lily_moe_shape &s)
     L.chunk_base = take(C * E * 4);
     L.h = take((k + 1) * T * s.I * 2);
     L.xs = take((k + 1) * T * s.d * 2);
+    L.inv = take(T * k * 4);
     L.logits = take(T * E * 4);
     L.idx = take(T * k * 4);
     L.w = take(T * k * 4);
@@ -239,9 +240,10 @@ namespace {
 constexpr int kRouterBlockRows = 64;
 
 // ------------------------------------------------------------------ enqueue helpers
+// inv: where the scatter also writes the inverse permutation (NULL: not written).
 cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, const uint16_t *x,
                           const lily_moe_routing &r, float *logits, void *ws, cudaStream_t stream,
-                          cudaEvent_t *events = nullptr)
+                          cudaEvent_t *events = nullptr, int *inv = nullptr)
 {
     const PrefillLayout L = prefill_layout(s);
     Ctrl *ctrl = at<Ctrl>(ws, L.ctrl);
@@ -273,6 +275,7 @@ cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, co
     ra.topk_idx = r.topk_idx; ra.topk_w = r.topk_w;
     ra.counts = r.counts; ra.offsets = r.offsets; ra.perm = r.perm;
     ra.block_map = r.block_map; ra.n_blocks = r.n_blocks;
+    ra.inv = inv;
     ra.chunk_counts = at<int>(ws, L.chunk_counts);
     ra.chunk_base = at<int>(ws, L.chunk_base);
     ra.n_chunks = static_cast<int>(ceil_div(s.T, kRouteChunkTokens));
@@ -284,14 +287,17 @@ cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, co
     return cudaSuccess;
 }
 
+// inv_ready: this workspace already holds the inverse of r.perm (the routing
+// kernels of the same call wrote it).
 cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, const uint16_t *x,
                             const lily_moe_routing &r, float *out, void *ws, cudaStream_t stream,
-                            cudaEvent_t *events)
+                            cudaEvent_t *events, bool inv_ready)
 {
     const PrefillLayout L = prefill_layout(s);
     Ctrl *ctrl = at<Ctrl>(ws, L.ctrl);
     __half *h = at<__half>(ws, L.h);
     __half *xs = at<__half>(ws, L.xs);
+    int *inv = at<int>(ws, L.inv);
     const int64_t hrows = static_cast<int64_t>(s.top_k + 1) * s.T;
     CUtensorMap tmXs, tmH, tmG, tmU, tmD, tmSG, tmSU, tmSD;
     if (!tmap_f16_sw128(&tmXs, xs, s.d, hrows) || !tmap_f16_sw128(&tmH, h, s.I, hrows) ||
@@ -301,8 +307,9 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
         !tmap_q4(&tmSU, w.sh_up.q, s.d, s.I) || !tmap_q4(&tmSD, w.sh_down.q, s.I, s.d))
         return cudaErrorInvalidValue;
 
-    cudaError_t e = launch_prep_experts(x, r.perm, xs, s.T, s.d, s.top_k, &ctrl->status, stream);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (!inv_ready && (e = launch_invert_perm(r.perm, inv, s.T * s.top_k, &ctrl->status, stream)) != cudaSuccess) return e;
+    if ((e = launch_prep_experts(x, inv, xs, s.T, s.d, s.top_k, &ctrl->status, stream)) != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[3], stream)) != cudaSuccess) return e;
 
     const int sms = num_sms_current();
@@ -465,7 +472,7 @@ int lily_moe_route(const lily_moe_shape *shape, const lily_moe_weights *w, const
     if (shape->T == 0) return LILY_OK;
     if ((rc = check_ptr(x))) return rc;
     float *logits = r->logits ? r->logits : at<float>(ws, prefill_layout(*shape).logits);
-    return to_status(enqueue_route(*shape, *w, x, *r, logits, ws, stream));
+    return to_status(enqueue_route(*shape, *w, x, *r, logits, ws, stream, nullptr, at<int>(ws, prefill_layout(*shape).inv)));
 }
 
 int lily_moe_grouped_gemm(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,
@@ -476,7 +483,7 @@ int lily_moe_grouped_gemm(const lily_moe_shape *shape, const lily_moe_weights *w
     if ((rc = check_ws(ws, ws_bytes, prefill_layout(*shape).total))) return rc;
     if (shape->T == 0) return LILY_OK;
     if ((rc = check_ptr(x)) || (rc = check_ptr(out))) return rc;
-    return to_status(enqueue_experts(*shape, *w, x, *r, out, ws, stream, nullptr));
+    return to_status(enqueue_experts(*shape, *w, x, *r, out, ws, stream, nullptr, false));
 }
 
 int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x, float *out,
@@ -491,8 +498,9 @@ int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *
     const lily_moe_routing rr = r ? *r : internal_routing(*shape, ws);
     float *logits = rr.logits ? rr.logits : at<float>(ws, prefill_layout(*shape).logits);
     if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return LILY_ERR_LAUNCH;
-    if (enqueue_route(*shape, *w, x, rr, logits, ws, stream, events) != cudaSuccess) return LILY_ERR_LAUNCH;
-    return to_status(enqueue_experts(*shape, *w, x, rr, out, ws, stream, events));
+    if (enqueue_route(*shape, *w, x, rr, logits, ws, stream, events, at<int>(ws, prefill_layout(*shape).inv)) != cudaSuccess)
+        return LILY_ERR_LAUNCH;
+    return to_status(enqueue_experts(*shape, *w, x, rr, out, ws, stream, events, true));
 }
 
 int lily_moe_forward(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x, float *out,

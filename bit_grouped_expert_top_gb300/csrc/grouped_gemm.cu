@@ -701,9 +701,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
 // Before the expert GEMMs: xs = fp16(x) in routing order with K permuted
 // inside each group of 8 (the order the dequantisers write the weights in):
 // row p < T top_k is token perm[p] / top_k, row T top_k + t is token t (the
-// shared expert's rows).  One warp per row; each lane has up to 8 16-byte
-// loads in flight before it converts and stores them (x itself is L2-resident
-// after the router GEMM read it).
+// shared expert's rows).  One warp per token: it reads the token's row of x
+// once (8 16-byte loads in flight per lane), converts it once and writes it to
+// the token's top_k routed rows inv[t top_k + j] and to its shared row.
 __device__ __forceinline__ uint4 bf16x8_to_f16x8_kperm(const uint4 v)
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -724,51 +724,81 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8_kperm(const uint4 v)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, const int *perm, uint4 *xs, int T, int d8,
+__global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, const int *inv, uint4 *xs, int T, int d8,
                                                            int top_k, int *status)
 {
     const int lane = threadIdx.x & 31;
     const int64_t routed = static_cast<int64_t>(T) * top_k;
-    const int64_t rows = routed + T;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * 8;
+    const int stride = gridDim.x * 8;
     pdl_trigger();
-    pdl_wait();  // the permutation is complete
-    for (int64_t p = blockIdx.x * 8LL + (threadIdx.x >> 5); p < rows; p += stride) {
-        int t = p < routed ? __ldg(perm + p) / top_k : static_cast<int>(p - routed);
-        if (t < 0 || t >= T) {
-            if (lane == 0) record_error(status, kErrDeviceIndex);
-            t = 0;
+    pdl_wait();  // the inverse permutation is complete
+    for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += stride) {
+        // lane j < top_k holds the row of slot j; lane top_k the shared expert's row
+        int64_t row = -1;
+        if (lane < top_k) {
+            const int p = __ldg(inv + static_cast<int64_t>(t) * top_k + lane);
+            if (p >= 0 && p < routed)
+                row = p;
+            else
+                record_error(status, kErrDeviceIndex);
+        } else if (lane == top_k) {
+            row = routed + t;
         }
         const uint4 *src = x + static_cast<int64_t>(t) * d8;
-        uint4 *dst = xs + p * d8;
         for (int i0 = 0; i0 < d8; i0 += 256) {
             uint4 v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = i0 + j * 32 + lane;
-                if (i < d8) v[j] = __ldg(src + i);
+                if (i < d8) v[j] = bf16x8_to_f16x8_kperm(__ldg(src + i));
             }
+            for (int k = 0; k <= top_k; ++k) {  // the token's top_k routed rows and its shared row
+                const int64_t r = __shfl_sync(0xffffffffu, row, k);
+                if (r < 0) continue;
+                uint4 *dst = xs + r * d8;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int i = i0 + j * 32 + lane;
-                if (i < d8) dst[i] = bf16x8_to_f16x8_kperm(v[j]);
+                for (int j = 0; j < 8; ++j) {
+                    const int i = i0 + j * 32 + lane;
+                    if (i < d8) dst[i] = v[j];
+                }
             }
         }
     }
 }
 
+// inv[perm[p]] = p, for routing tables that come from an earlier call.
+__global__ void __launch_bounds__(256) invert_perm_kernel(const int *perm, int *inv, int n, int *status)
+{
+    pdl_trigger();
+    pdl_wait();
+    for (int p = blockIdx.x * 256 + threadIdx.x; p < n; p += gridDim.x * 256) {
+        const int a = __ldg(perm + p);
+        if (a >= 0 && a < n)
+            inv[a] = p;
+        else
+            record_error(status, kErrDeviceIndex);
+    }
+}
+
 }  // namespace
 
-cudaError_t launch_prep_experts(const uint16_t *x, const int *perm, __half *xs, int T, int d, int top_k, int *status,
+cudaError_t launch_prep_experts(const uint16_t *x, const int *inv, __half *xs, int T, int d, int top_k, int *status,
                                 cudaStream_t stream)
 {
+    if (T <= 0) return cudaSuccess;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t rows = static_cast<int64_t>(T) * (top_k + 1);
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 8)));
-    return launch_pdl(prep_experts_kernel, dim3(grid), dim3(256), 0, stream, reinterpret_cast<const uint4 *>(x), perm,
+    const int grid = std::max(1, std::min((T + 7) / 8, sms * 8));
+    return launch_pdl(prep_experts_kernel, dim3(grid), dim3(256), 0, stream, reinterpret_cast<const uint4 *>(x), inv,
                       reinterpret_cast<uint4 *>(xs), T, d / 8, top_k, status);
+}
+
+cudaError_t launch_invert_perm(const int *perm, int *inv, int n, int *status, cudaStream_t stream)
+{
+    if (n <= 0) return cudaSuccess;
+    const int grid = std::max(1, std::min((n + 255) / 256, 4096));
+    return launch_pdl(invert_perm_kernel, dim3(grid), dim3(256), 0, stream, perm, inv, n, status);
 }
 
 size_t grouped_gemm_smem_bytes() { return sizeof(Smem) + 1024; }

@@ -70,10 +70,12 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 size_t grouped_gemm_smem_bytes();
 
 // Before the expert GEMMs: xs = fp16(x) in routing order (routed rows by perm,
-// then the T shared-expert rows), [(top_k+1)*T][d].  (out is zeroed by the
-// gate/up GEMM launch.)
-cudaError_t launch_prep_experts(const uint16_t *x, const int *perm, __half *xs, int T, int d, int top_k, int *status,
+// then the T shared-expert rows), [(top_k+1)*T][d], written token by token from
+// inv = the inverse of perm.  (out is zeroed by the gate/up GEMM launch.)
+cudaError_t launch_prep_experts(const uint16_t *x, const int *inv, __half *xs, int T, int d, int top_k, int *status,
                                 cudaStream_t stream);
+// inv[perm[p]] = p for p < T*top_k (when the routing tables come from elsewhere).
+cudaError_t launch_invert_perm(const int *perm, int *inv, int n, int *status, cudaStream_t stream);
 
 // tmB: B operand rows (x for the router, xs for gate/up, h for down).
 // tmA0/tmA1: routed weight maps of the two 128-row tiles (router: Wr for both);
@@ -89,6 +91,7 @@ struct RouteArgs {
     int *topk_idx;
     float *topk_w;
     int *counts, *offsets, *perm, *block_map, *n_blocks;
+    int *inv;           // [T*top_k]: row of assignment t*top_k + j (inverse of perm), or NULL
     int *chunk_counts;  // [C][E]
     int *chunk_base;    // [C][E]: chunk's first row within its expert (relative to offsets[e])
     int n_chunks;

@@ -192,10 +192,12 @@ scatter_kernel(const RouteArgs a)
         __syncthreads();
         if (e >= 0) {
             const int pos = base[e] + cnt[warp][e] + rank;
-            if (pos >= 0 && pos < total)
+            if (pos >= 0 && pos < total) {
                 a.perm[pos] = ga;
-            else
+                if (a.inv) a.inv[ga] = pos;
+            } else {
                 record_error(&a.ctrl->status, kErrDeviceIndex);
+            }
         }
         __syncthreads();
         base[threadIdx.x] += run;

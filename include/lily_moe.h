@@ -254,7 +254,7 @@ int lily_moe_clear_status(void *ws, cudaStream_t stream);
  * Allocates nothing: no cudaMalloc, no cudaFree, no library allocation.
  */
 #define LILY_NOALLOC_MAX_TOKENS 8192
-#define LILY_NOALLOC_SCRATCH_BYTES (256 + 2 * 4 * 256 * (LILY_NOALLOC_MAX_TOKENS / 64))
+#define LILY_NOALLOC_SCRATCH_BYTES (256 + 2 * 4 * 256 * (LILY_NOALLOC_MAX_TOKENS / 32))
 int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,
                            lily_moe_routing *r, int32_t *device_status, cudaStream_t stream);
 

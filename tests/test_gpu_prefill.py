@@ -7,8 +7,9 @@ import pytest
 import torch
 
 from bit_grouped_expert_top_gb300.inputs import CONFIGS, LayerConfig
+import bit_grouped_expert_top_gb300 as lm
 from gpu_util import (Layer, assert_logits_close, assert_out_close, assert_routing_exact, oracle_layer_out,
-                      run_forward, sample_tokens, x_for)
+                      run_forward, sample_tokens, shape_of, x_for)
 from helpers import bits
 
 pytestmark = pytest.mark.gpu
@@ -66,11 +67,28 @@ def test_zero_routed_weights_leave_shared_expert():
 
 @pytest.mark.parametrize("I", [256, 384, 1024])
 def test_intermediate_sizes(I):
-    # K of the down projection is I: 4 and 8 k-steps run the down kernel with the
-    # unit's B resident in shared memory (384 pads 6 k-steps to 8 and has a group
-    # count that is not a multiple of 8); 1024 (16 k-steps) runs the general one.
+    # K of the down projection is I: 4, 8 and 16 k-steps (384 pads 6 k-steps to 8
+    # and has a group count that is not a multiple of 8).
     cfg = TINY.with_(I=I, I_shared=I)
     _full_check(cfg, 100, seed_offset=I)
+
+
+def test_route_then_experts_in_separate_calls():
+    # routing tables from lily_moe_route, then lily_moe_grouped_gemm with a workspace
+    # of its own: the expert path derives the inverse permutation from perm itself
+    cfg, T = TINY, 150
+    layer = Layer(cfg)
+    x = x_for(cfg, T=T, seed_offset=11)
+    s = shape_of(cfg, T)
+    rt = lm.alloc_routing(s)
+    lm.lily_moe_route(s, layer.w, x, lm.make_routing(rt), lm.alloc_workspace(s))
+    ws2 = lm.alloc_workspace(s)
+    out = torch.full((T, cfg.d), float("nan"), dtype=torch.float32, device="cuda")
+    lm.lily_moe_grouped_gemm(s, layer.w, x, lm.make_routing(rt), out, ws2)
+    torch.cuda.synchronize()
+    assert lm.lily_moe_device_status(ws2) == 0
+    ref = oracle_layer_out(cfg, layer, bits(x), rt["logits"].cpu().numpy())
+    assert_out_close(out.cpu().numpy(), ref)
 
 
 def test_medium_full_hidden_size():

@@ -51,7 +51,8 @@ def _route_pair(cfg, T, seed_offset):
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_route_on_two_calls_in_a_row():
-    cases = [(CONFIGS["prefill_t2048_zipf"], 2048, 1), (CONFIGS["tiny"], 300, 2)]
+    # the largest T the fixed scratch is sized for, a Zipf-routed case and a small one
+    cases = [(CONFIGS["prefill_t8192"], 8192, 3), (CONFIGS["prefill_t2048_zipf"], 2048, 1), (CONFIGS["tiny"], 300, 2)]
     prepared = [_route_pair(cfg, T, so) for cfg, T, so in cases]
     torch.cuda.synchronize()
     status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
