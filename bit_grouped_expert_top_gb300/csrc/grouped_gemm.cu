@@ -555,16 +555,27 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
         uint32_t acc_ph = 0;
         bool ok = true;
         const int n_acc = dequant_mode ? 1 : 2;
+        // gate/up: out = 0 for the down projection that follows, this CTA's slice,
+        // written a share after each unit (not all at the start, where it would
+        // compete with the first units' copies) and the rest at the end
+        int64_t zpos = 0, zend = 0, zstep = 0;
         if (MODE == kModeGateUp) {
-            // out = 0 for the down projection that follows: this CTA's slice,
-            // written while the first unit's MMAs run
             const int64_t n4 = static_cast<int64_t>(g.T) * g.d / 4;
             const int64_t per = (n4 + gridDim.x - 1) / gridDim.x;
-            const int64_t z0 = blockIdx.x * per, z1 = min(n4, z0 + per);
+            zpos = min(n4, blockIdx.x * per);
+            zend = min(n4, zpos + per);
+            const int my_units = total_tiles > static_cast<int>(blockIdx.x)
+                                     ? (total_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                                     : 1;
+            zstep = ((zend - zpos + my_units - 1) / my_units + 255) / 256 * 256;
+        }
+        auto zero_out = [&](int64_t n) {
             float4 *o = reinterpret_cast<float4 *>(g.out);
             const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int64_t i = z0 + eid; i < z1; i += 256) o[i] = z;
-        }
+            const int64_t stop = min(zend, zpos + n);
+            for (int64_t i = zpos + eid; i < stop; i += 256) o[i] = z;
+            zpos = stop;
+        };
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             const Unit u = unit_info<MODE>(g, tile, n_routed);
             if (u.rows <= 0) continue;
@@ -688,7 +699,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 ab = 0;
                 acc_ph ^= 1;
             }
+            if (MODE == kModeGateUp) zero_out(zstep);
         }
+        if (MODE == kModeGateUp) zero_out(zend - zpos);
     }
 
     __syncwarp();  // every role reconverges its warp before the CTA-wide barrier
