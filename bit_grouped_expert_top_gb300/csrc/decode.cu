@@ -76,9 +76,9 @@ __device__ __forceinline__ float warp_sum(float v)
 // loads 16 bytes (32 weights) of rows g and g + 8 for each 128-wide K block:
 // weights [32 t, 32 t + 32) of the block.  The K order inside the block is
 // permuted so that these weights are exactly this lane's A-fragment entries:
-// within 32-bit word w (weights 8w..8w+7, dequantised in pairs (0,4) (1,5)
-// (2,6) (3,7)), weight e goes to slice 2w + ((e & 3) >> 1), entry
-// ((e & 1) << 1) | (e >> 2) of the lane's four K positions.  The B operand
+// within 32-bit word w (weights 8w..8w+7, rebuilt in pairs (0,2) (4,6) (1,3)
+// (5,7) by dequant8_f16_e2m3), weight e goes to slice 2w + (e & 1), entry e >> 1
+// of the lane's four K positions.  The B operand
 // (x, or h for the down projection) is stored in the same permuted order, so
 // each lane reads its B fragment with one 8-byte load.
 constexpr int kKB = 128;  // K block
@@ -88,7 +88,7 @@ constexpr int kKB = 128;  // K block
 __device__ __forceinline__ int perm_b_index(int k, int n)
 {
     const int kb = k >> 7, r = k & 127, t = r >> 5, w = (r & 31) >> 3, e = r & 7;
-    const int s = 2 * w + ((e & 3) >> 1), idx = ((e & 1) << 1) | (e >> 2);
+    const int s = 2 * w + (e & 1), idx = e >> 1;
     return (((kb * 8 + n) * 4 + t) * 8 + s) * 4 + idx;
 }
 
@@ -175,7 +175,7 @@ dec_route_kernel(const DecodeLayerArgs a)
     {
         // fp16 copy in the permuted B layout of the expert GEMVs (8 token columns),
         // split over the CTAs: the 8 elements of one 32-bit weight word land as
-        // 16 contiguous bytes (x0 x4 x1 x5 | x2 x6 x3 x7)
+        // 16 contiguous bytes (x0 x2 x4 x6 | x1 x3 x5 x7)
         const int wpt = d / 8;  // words per token
         const int per = (8 * wpt + gridDim.x - 1) / gridDim.x;
         for (int q = blockIdx.x * per + threadIdx.x; q < min(8 * wpt, (blockIdx.x + 1) * per); q += kDecThreads) {
@@ -191,8 +191,8 @@ dec_route_kernel(const DecodeLayerArgs a)
                     f[2 * j] = p2.x;
                     f[2 * j + 1] = p2.y;
                 }
-                const __half2 h0 = __floats2half2_rn(f[0], f[4]), h1 = __floats2half2_rn(f[1], f[5]);
-                const __half2 h2 = __floats2half2_rn(f[2], f[6]), h3 = __floats2half2_rn(f[3], f[7]);
+                const __half2 h0 = __floats2half2_rn(f[0], f[2]), h1 = __floats2half2_rn(f[4], f[6]);
+                const __half2 h2 = __floats2half2_rn(f[1], f[3]), h3 = __floats2half2_rn(f[5], f[7]);
                 o = make_uint4(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1),
                                *reinterpret_cast<const uint32_t *>(&h2), *reinterpret_cast<const uint32_t *>(&h3));
             }
@@ -240,20 +240,19 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 __device__ __forceinline__ void mma_kblock(float (&d)[4], uint4 q_g, uint4 q_g8, uint32_t sb_g, uint32_t sb_g8,
                                            const uint2 *b)
 {
-    const __half2 s_g = half2_from_bf16_bits(static_cast<uint16_t>(sb_g & 0xFFFFu));
+    const __half2 k8 = __floats2half2_rn(8.0f, 8.0f);
+    const __half2 s8_g = __hmul2(half2_from_bf16_bits(static_cast<uint16_t>(sb_g & 0xFFFFu)), k8);
     const __half2 b_g = half2_from_bf16_bits(static_cast<uint16_t>(sb_g >> 16));
-    const __half2 s_g8 = half2_from_bf16_bits(static_cast<uint16_t>(sb_g8 & 0xFFFFu));
+    const __half2 s8_g8 = __hmul2(half2_from_bf16_bits(static_cast<uint16_t>(sb_g8 & 0xFFFFu)), k8);
     const __half2 b_g8 = half2_from_bf16_bits(static_cast<uint16_t>(sb_g8 >> 16));
-    const __half2 k16 = __floats2half2_rn(0.0625f, 0.0625f);
-    const __half2 s_g16 = __hmul2(s_g, k16), s_g816 = __hmul2(s_g8, k16);
     const uint32_t wg[4] = {q_g.x, q_g.y, q_g.z, q_g.w}, wg8[4] = {q_g8.x, q_g8.y, q_g8.z, q_g8.w};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        const uint4 pg = dequant8_f16_kperm(wg[w], s_g, s_g16, b_g);
-        const uint4 pg8 = dequant8_f16_kperm(wg8[w], s_g8, s_g816, b_g8);
+        const uint4 pg = dequant8_f16_e2m3(wg[w], s8_g, b_g);
+        const uint4 pg8 = dequant8_f16_e2m3(wg8[w], s8_g8, b_g8);
         const uint2 b0 = b[2 * w], b1 = b[2 * w + 1];
-        const uint32_t a0[4] = {pg.x, pg8.x, pg.y, pg8.y};  // slice 2w: pairs (0,4) and (1,5)
-        const uint32_t a1[4] = {pg.z, pg8.z, pg.w, pg8.w};  // slice 2w + 1: pairs (2,6) and (3,7)
+        const uint32_t a0[4] = {pg.x, pg8.x, pg.y, pg8.y};  // slice 2w: pairs (0,2) and (4,6)
+        const uint32_t a1[4] = {pg.z, pg8.z, pg.w, pg8.w};  // slice 2w + 1: pairs (1,3) and (5,7)
         mma_16816(d, a0, b0.x, b0.y);
         mma_16816(d, a1, b1.x, b1.y);
     }

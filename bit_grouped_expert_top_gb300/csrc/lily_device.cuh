@@ -456,33 +456,6 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t v, __half2 s2, __half2 b2
     return o;
 }
 
-// Eight packed 4-bit weights (element i in bits [4i, 4i+4)) -> eight fp16
-// weights w_i = q_i * s + b, each rounded once (fma.rn.f16x2), written in the
-// K order (0,4, 1,5, 2,6, 3,7) of one 16-byte chunk: the order that needs no
-// byte permutes.  The other GEMM operand must use the same order within each
-// group of 8 (see kperm8).  Nibbles 1,3,5,7 are used in place (16*q) with the
-// scale s/16 (s2_16), exact for |s| >= 2^-10.
-__device__ __forceinline__ uint4 dequant8_f16_kperm(uint32_t v, __half2 s2, __half2 s2_16, __half2 b2)
-{
-    const uint32_t kMagic = 0x64006400u;
-    const uint32_t v8 = v >> 8;
-    uint32_t p04 = (v & 0x000F000Fu) | kMagic;    // (1024 + q0, 1024 + q4)
-    uint32_t p15 = (v & 0x00F000F0u) | kMagic;    // (1024 + 16 q1, 1024 + 16 q5)
-    uint32_t p26 = (v8 & 0x000F000Fu) | kMagic;   // (1024 + q2, 1024 + q6)
-    uint32_t p37 = (v8 & 0x00F000F0u) | kMagic;   // (1024 + 16 q3, 1024 + 16 q7)
-    const __half2 k1024 = __floats2half2_rn(1024.0f, 1024.0f);
-    __half2 f04 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p04), k1024), s2, b2);
-    __half2 f15 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p15), k1024), s2_16, b2);
-    __half2 f26 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p26), k1024), s2, b2);
-    __half2 f37 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p37), k1024), s2_16, b2);
-    uint4 o;
-    o.x = *reinterpret_cast<uint32_t *>(&f04);
-    o.y = *reinterpret_cast<uint32_t *>(&f15);
-    o.z = *reinterpret_cast<uint32_t *>(&f26);
-    o.w = *reinterpret_cast<uint32_t *>(&f37);
-    return o;
-}
-
 // Two 6-bit e2m3 values (one per byte, low 6 bits) -> fp16 pair, low byte to
 // the low half.  A byte holding a nibble q in its low 4 bits (sign 0, exponent
 // bits 0 q3, mantissa q2 q1 q0) is exactly q / 8: subnormal q/8 for q < 8,
@@ -525,14 +498,6 @@ __host__ __device__ __forceinline__ int kperm8_e2m3(int k)
 {
     const int j = k & 7;
     return (k & ~7) | ((j >> 1) + ((j & 1) << 2));
-}
-
-// Position of logical K index k in the order used by dequant8_f16_kperm:
-// inside each group of 8, element j sits at 2j (j < 4) or 2(j-4)+1 (j >= 4).
-__host__ __device__ __forceinline__ int kperm8(int k)
-{
-    const int j = k & 7;
-    return (k & ~7) | (j < 4 ? 2 * j : 2 * (j - 4) + 1);
 }
 
 // bf16 bit pattern -> fp16 pair (value converted with round-to-nearest).
@@ -582,13 +547,6 @@ __device__ __forceinline__ uint4 load_groups8(const uint16_t *row, int g0, int n
 __device__ __forceinline__ uint16_t pick16x4(const uint2 v, int j)
 {
     const uint32_t w = (j & 2) ? v.y : v.x;
-    return static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
-}
-
-// Value j (0..7) of a block loaded by load_groups8.
-__device__ __forceinline__ uint16_t pick16(const uint4 v, int j)
-{
-    const uint32_t w = (j & 4) ? ((j & 2) ? v.w : v.z) : ((j & 2) ? v.y : v.x);
     return static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
 }
 
