@@ -59,7 +59,9 @@ constexpr int kBStages = 4;    // B ring in the dedicated buffers (router)
 constexpr int kBSlotBars = 4;  // B ring slots (router: 4 x 1 k-step; expert modes: 4 x 2 k-steps, the last
                                // two in the shared-memory A buffers they do not use)
 constexpr int kAStages = 2;    // shared-memory A ring (bf16 router weights by TMA)
-constexpr int kTAStages = 2;   // tensor-memory A ring (expert modes: 2 stages of 2 k-steps) / router A ring
+constexpr int kTAStages = 2;   // tensor-memory A ring (expert modes: 2 stages of 2 k-steps)
+constexpr int kRouterAStages = 4;  // router: bf16 A ring in `a` and `raw` (which it does not otherwise use)
+constexpr int kABars = 4;          // full_a / empty_a barriers: max(kTAStages, kRouterAStages)
 constexpr int kTileM = 128;
 constexpr int kBK = 64;        // one quantisation group, one 128-byte swizzle row
 constexpr int kTileN = 128;
@@ -82,7 +84,7 @@ struct __align__(1024) Smem {
     uint8_t raw[kRStages][2][kRawBytes];
     uint64_t full_r[kRStages], empty_r[kRStages];
     uint64_t full_b[kBSlotBars], empty_b[kBSlotBars];
-    uint64_t full_a[kTAStages], empty_a[kTAStages];
+    uint64_t full_a[kABars], empty_a[kABars];
     uint64_t full_acc[2], empty_acc[2];
     uint64_t drain;
     uint32_t tmem_base;
@@ -95,6 +97,9 @@ static_assert(sizeof(Smem) + 1024 <= 200 * 1024, "shared memory budget of one CT
 static_assert(offsetof(Smem, a) == offsetof(Smem, b) + sizeof(Smem::b) &&
                   sizeof(Smem::a) == sizeof(Smem::b),
               "expert-mode B slots 2..3 continue the B ring in the A buffers");
+static_assert(offsetof(Smem, raw) == offsetof(Smem, a) + sizeof(Smem::a) && sizeof(Smem::raw) == sizeof(Smem::a) &&
+                  kRouterAStages * 2 * kABytes == sizeof(Smem::a) + sizeof(Smem::raw),
+              "router A stages 2..3 continue the A ring in the raw buffers");
 
 struct Unit {
     int e, p0, rows, n_mma, mt;
@@ -204,7 +209,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             mbar_init(&S.full_b[s], 1);
             mbar_init(&S.empty_b[s], kIssuers);  // one commit per MMA issuer
         }
-        for (int s = 0; s < kTAStages; ++s) {
+        for (int s = 0; s < kABars; ++s) {
             mbar_init(&S.full_a[s], dequant_mode ? 8 : 1);  // dequantiser warps / router TMA
             mbar_init(&S.empty_a[s], kIssuers);  // router only
         }
@@ -262,7 +267,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
     // free again once the MMAs of the same stage one block back completed,
     // i.e. B slot 2 ((blk - 1) % 2) + h (phase ((blk - 1) / 2) % 2); B slot
     // 2 (blk % 2) + h (phase (blk / 2) % 2).  Router: shared-memory A stage
-    // = k-step % 2 (phase k-step / 2); B slot = k-step (phase blk % 2).
+    // = k-step within the block (phase blk % 2; four stages, the last two in the
+    // raw buffers); B slot = k-step (phase blk % 2).
     constexpr int SS = dequant_mode ? 2 : 1;  // k-steps per stage
     constexpr int SPB = kBlk / SS;            // stages per block
     // B slots: router 4 x 1 k-step, expert modes 4 x 2 k-steps (two blocks per
@@ -294,17 +300,19 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         tma_load_2d(S.raw[rs][1], mA1, &S.full_r[rs], kb * kRawRow, r1);
                         ++issued;
                     } else {
+                        // one ring cycle per block: stage jr (k-step jr of the block), phase blk % 2
 #pragma unroll
                         for (int jr = 0; jr < kBlk; ++jr) {
-                            const int as = jr & 1;
-                            if (!mbar_wait(&S.empty_a[as], ((jr >> 1) & 1) ^ 1, abort_flag, status)) {
+                            const int as = jr;
+                            if (!mbar_wait(&S.empty_a[as], (blk & 1) ^ 1, abort_flag, status)) {
                                 ok = false;
                                 break;
                             }
                             mbar_arrive_expect_tx(&S.full_a[as], 2 * kABytes);
                             const int kc = (kb * kBlk + jr) * kBK;
-                            tma_load_2d(S.a[as][0], &tmA0, &S.full_a[as], kc, r0);
-                            tma_load_2d(S.a[as][1], &tmA0, &S.full_a[as], kc, r1);
+                            uint8_t *dst = &S.a[0][0][0] + static_cast<size_t>(as) * 2 * kABytes;
+                            tma_load_2d(dst, &tmA0, &S.full_a[as], kc, r0);
+                            tma_load_2d(dst + kABytes, &tmA0, &S.full_a[as], kc, r1);
                             ++issued;
                         }
                     }
@@ -314,7 +322,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             if (dequant_mode)
                 drain_ring(S.full_r, kRStages, issued, status);
             else
-                drain_ring(S.full_a, kAStages, issued, status);
+                drain_ring(S.full_a, kRouterAStages, issued, status);
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -392,8 +400,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
 #pragma unroll
                     for (int h = 0; h < SPB; ++h) {
                         const int bs = (CYC == 2 ? (blk & 1) : 0) * SPB + h;
-                        const int as = dequant_mode ? h : (h & 1);
-                        const uint32_t ap = dequant_mode ? (blk & 1) : ((h >> 1) & 1);
+                        const int as = h;  // expert modes: TMEM A stage; router: shared-memory A stage
+                        const uint32_t ap = blk & 1;
                         if (!mbar_wait2(&S.full_a[as], ap, &S.full_b[bs], bpar, abort_flag, status)) {
                             ok = false;
                             break;
