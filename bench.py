@@ -127,9 +127,16 @@ def max_over_ranks(v: float, world: int) -> float:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput of independent replicas: the units every rank processed in
+    one step, over the slowest rank's step time (ms)."""
+    return units_per_rank * world / (ms_max * 1e-3)
 
 
 def barrier(world: int):
@@ -293,7 +300,7 @@ def run_ours(args):
     st = stage_means(ctx)
     if lm.lily_moe_device_status(ctx["ws"], stream) != 0:
         raise RuntimeError("device status error in timed region")
-    tokens_per_s = cfg.T * world / (ms * 1e-3)
+    tokens_per_s = job_rate(cfg.T, world, ms)
     flops_total, flops_gu, flops_down = prefill_flops(cfg, cfg.T)
     peak_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])  # fp16 dense rate = bf16 rate
     achieved = flops_gu / (st["gateup"] * 1e-6) / 1e12
@@ -353,7 +360,7 @@ def run_ours(args):
                      "algorithmic_flops_per_launch": flops_gu},
         "layer_tflops": round(flops_total / (ms * 1e-3) / 1e12, 1),
         "clocks": clocks,
-        "e2e": {"value": round(cfg.T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_rate(cfg.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 4},
         "gpu_launches": 7 * args.steps,  # router GEMM, top-8, scan, scatter, prep, gate/up, down
         "also": also,
