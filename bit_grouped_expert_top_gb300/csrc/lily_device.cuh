@@ -573,14 +573,6 @@ __device__ __forceinline__ uint32_t float_order_key(float v)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Larger key first: (a, b) <- (max, min).
-__device__ __forceinline__ void cmpx_desc(unsigned long long &a, unsigned long long &b)
-{
-    const unsigned long long x = a, y = b;
-    a = x > y ? x : y;
-    b = x > y ? y : x;
-}
-
 // Inverse of float_order_key.
 __device__ __forceinline__ float float_from_order_key(uint32_t k)
 {
@@ -591,43 +583,42 @@ __device__ __forceinline__ float float_from_order_key(uint32_t k)
 // logits 8l..8l+7), ordered by descending logit with the lower expert index
 // first among equal logits, and their renormalised softmax weights
 // w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0).  Lane j < 8 receives slot j.
-// Each lane sorts its 8 keys (key = order-preserving logit bits, then 255 -
-// index) with a 19-exchange network; five butterfly rounds then merge the
-// lists: the top 8 of two descending lists A, B is max(A[j], B[7 - j]), a
-// bitonic sequence that three half-cleaner stages sort.
+// Eight rounds on 32-bit order-preserving keys: each lane takes the maximum of
+// its remaining keys, one warp reduction gives the round's maximum, and the
+// lowest lane holding it wins (lane l holds the lower indices 8l..8l+7); the
+// winner takes out its first key equal to the maximum (its lowest index among
+// equal logits).  Key 0 marks a taken slot: it is below the key of every
+// finite logit, -inf included.
 __device__ __forceinline__ void warp_top8_keys(const float (&lv)[8], int lane, int &sel_e, float &sel_w)
 {
-    unsigned long long k[8];
+    uint32_t key[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        k[j] = (static_cast<unsigned long long>(float_order_key(lv[j])) << 32) |
-               static_cast<unsigned long long>(255 - (lane * 8 + j));
-    cmpx_desc(k[0], k[2]); cmpx_desc(k[1], k[3]); cmpx_desc(k[4], k[6]); cmpx_desc(k[5], k[7]);
-    cmpx_desc(k[0], k[4]); cmpx_desc(k[1], k[5]); cmpx_desc(k[2], k[6]); cmpx_desc(k[3], k[7]);
-    cmpx_desc(k[0], k[1]); cmpx_desc(k[2], k[3]); cmpx_desc(k[4], k[5]); cmpx_desc(k[6], k[7]);
-    cmpx_desc(k[2], k[4]); cmpx_desc(k[3], k[5]);
-    cmpx_desc(k[1], k[4]); cmpx_desc(k[3], k[6]);
-    cmpx_desc(k[1], k[2]); cmpx_desc(k[3], k[4]); cmpx_desc(k[5], k[6]);
-#pragma unroll 1
-    for (int m = 1; m < 32; m <<= 1) {  // not unrolled: short code, fetched once per kernel
-        unsigned long long o[8];
+    for (int j = 0; j < 8; ++j) key[j] = float_order_key(lv[j]);
+    uint32_t top = 0u, mine = 0u;
+    int mine_e = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[j] = __shfl_xor_sync(0xffffffffu, k[7 - j], m);
+    for (int r = 0; r < 8; ++r) {
+        const uint32_t lm = max(max(max(key[0], key[1]), max(key[2], key[3])),
+                                max(max(key[4], key[5]), max(key[6], key[7])));
+        const uint32_t wm = __reduce_max_sync(0xffffffffu, lm);
+        const int win = __ffs(__ballot_sync(0xffffffffu, lm == wm)) - 1;
+        int pos = 7;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) k[j] = k[j] > o[j] ? k[j] : o[j];
+        for (int j = 6; j >= 0; --j)
+            if (key[j] == wm) pos = j;
 #pragma unroll
-        for (int d = 4; d > 0; d >>= 1)
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if ((j & d) == 0) cmpx_desc(k[j], k[j + d]);
+        for (int j = 0; j < 8; ++j)
+            if (lane == win && j == pos) key[j] = 0u;
+        const int wpos = __shfl_sync(0xffffffffu, pos, win);
+        if (r == 0) top = wm;
+        if (lane == r) {
+            mine = wm;
+            mine_e = win * 8 + wpos;
+        }
     }
-    unsigned long long mine = k[0];
-#pragma unroll
-    for (int j = 1; j < 8; ++j)
-        if (lane == j) mine = k[j];
-    sel_e = 255 - static_cast<int>(mine & 0xFFFFFFFFull);
-    const float sel_v = float_from_order_key(static_cast<uint32_t>(mine >> 32));
-    const float vmax = float_from_order_key(static_cast<uint32_t>(k[0] >> 32));
+    sel_e = mine_e;
+    const float sel_v = float_from_order_key(mine);
+    const float vmax = float_from_order_key(top);
     const float ex = lane < 8 ? expf(sel_v - vmax) : 0.0f;
     float den = ex;
 #pragma unroll

@@ -7,10 +7,10 @@
 //
 // Three kernels, one stream, no host sync:
 //   topk_count_kernel : one warp per token selects the top 8 of 256 fp32 logits
-//                       (descending; lower index first among equal logits) with
-//                       shuffle arg-max rounds and computes the renormalised
-//                       softmax weights; each CTA then counts its 64-token chunk
-//                       per expert.
+//                       (descending; lower index first among equal logits) in
+//                       eight warp-maximum rounds and computes the renormalised
+//                       softmax weights; each CTA then counts its chunk of
+//                       kRouteChunkTokens tokens per expert.
 //   scan_kernel       : one CTA per expert scans that expert's per-chunk counts
 //                       in chunk order (each chunk's base within the expert) and
 //                       writes its total; the last CTA to finish (ticket
