@@ -374,7 +374,7 @@ def run_ours(args):
         stream.wait_stream(torch.cuda.current_stream())
         lm.lily_moe_route(ctx["shape"], ctx["ws_l"][0], ctx["xs"][0], r, ctx["ws"], stream=stream)
         stream.synchronize()
-        n_tok = args.cpu_tokens
+        n_tok = args.cpu_baseline_tokens
         rate, dt = oracle_sample_rate(cfg, _np_layer(ctx["layers"][0]), _bits(ctx["xs"][0]), lg.cpu().numpy(), n_tok)
         line["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
                                 "kind": "oracle",
@@ -424,7 +424,10 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--cpu-tokens", type=int, default=24, help="oracle sample size (tokens)")
+    ap.add_argument("--cpu-tokens", type=int, default=24,
+                    help="oracle sample per step of the reference arm (tokens)")
+    ap.add_argument("--cpu-baseline-tokens", type=int, default=1024,
+                    help="oracle sample of the cpu_baseline entry (tokens; about 10 s on 16 cores)")
     ap.add_argument("--quick", action="store_true", help="headline workload only (no extra configs / decode)")
     args = ap.parse_args()
     if args.warmup < 3:
