@@ -92,10 +92,17 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
 
 # ------------------------------------------------------------------ marshalling helpers
 def _ptr(t) -> Optional[int]:
+    """Device address of a tensor argument (None stays NULL; an int is taken as a
+    raw device pointer).  Tensors must be dense CUDA tensors: the library reads
+    them as row-major device arrays and cannot tell a host address from a device one."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device} (shape {tuple(t.shape)})")
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got strides {t.stride()} (shape {tuple(t.shape)})")
     return t.data_ptr()
 
 

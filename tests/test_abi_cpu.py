@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import bit_grouped_expert_top_gb300 as lm
 from bit_grouped_expert_top_gb300 import _abi
@@ -128,3 +129,19 @@ def test_zero_tokens_is_a_noop_without_gpu():
     assert L.lily_moe_route(by(s), by(W), None, by(R), FAKE, need, None) == 0
     assert L.lily_moe_grouped_gemm(by(s), by(W), None, by(R), None, FAKE, need, None) == 0
     assert L.lily_moe_forward(by(s), by(W), None, None, None, FAKE, need, None) == 0
+
+
+def test_binding_rejects_host_tensors_before_calling_the_library():
+    # a host tensor's address would reach the kernels as if it were device memory
+    s = _shape(T=4)
+    w = _fake_weights()
+    r = _fake_routing()
+    x_host = torch.zeros((4, 512), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lm.lily_moe_forward(s, w, x_host, FAKE, FAKE)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lm.make_routing({"perm": torch.zeros(32, dtype=torch.int32)})
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lm.make_weights({k: torch.zeros(4) for k in ("router_w",)})
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lm.lily_moe_route(s, w, FAKE, r, torch.zeros(64, dtype=torch.uint8))
