@@ -14,9 +14,6 @@
 #include "lily_moe.h"
 
 namespace lily {
-size_t decode_smem_route(int T, int d);
-size_t decode_smem_gateup(int T, int d);
-size_t decode_smem_down(int T, int I);
 cudaError_t launch_decode_final_norm(const float *prev_out, uint16_t *x_export, int T, int d, cudaStream_t stream);
 }  // namespace lily
 

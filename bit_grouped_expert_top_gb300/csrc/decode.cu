@@ -544,11 +544,13 @@ dec_down_kernel(const DecodeLayerArgs a)
     }
 }
 
-}  // namespace
-
+// Dynamic shared memory: the router kernel stages the bf16 inputs [T][d]; the
+// gate/up kernel the fp16 inputs of up to 8 tokens in the permuted B layout
+// plus the per-warp partial sums [warps][2][32][4] floats.
 size_t decode_smem_route(int T, int d) { return static_cast<size_t>(T) * d * 2; }
-size_t decode_smem_gateup(int T, int d) { return static_cast<size_t>(d) * 8 * 2 + kDecWarps * 2 * 32 * 4 * 4 + 0 * T; }
-size_t decode_smem_down(int T, int I) { return 0 * static_cast<size_t>(T + I); }
+size_t decode_smem_gateup(int d) { return static_cast<size_t>(d) * 8 * 2 + kDecWarps * 2 * 32 * 4 * 4; }
+
+}  // namespace
 
 cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStream_t stream)
 {
@@ -574,7 +576,7 @@ cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStrea
     cfg.dynamicSmemBytes = decode_smem_route(a.T, a.d);
     if ((e = cudaLaunchKernelEx(&cfg, dec_route_kernel, a)) != cudaSuccess) return e;
     cfg.gridDim = dim3(num_sms);
-    cfg.dynamicSmemBytes = decode_smem_gateup(a.T, a.d);
+    cfg.dynamicSmemBytes = decode_smem_gateup(a.d);
     if ((e = cudaLaunchKernelEx(&cfg, dec_gateup_kernel, a)) != cudaSuccess) return e;
     cfg.gridDim = dim3(std::min(num_sms, a.d / 16));
     cfg.blockDim = dim3(kDownWarps * 32);
