@@ -133,6 +133,14 @@ def max_over_ranks(v: float, world: int) -> float:
     return float(t.item())
 
 
+def workload_config(cfg, world: int) -> dict:
+    """The `config` object of the JSON line; both arms report the same one."""
+    return {"workload": "prefill_t8192: one MoE layer, T=8192, d=2048, E=256 top-8 + 1 shared, I=512, "
+                        "int4 group-64 bf16 scale/bias, 4 weight+activation sets cycled",
+            "global_batch": cfg.T * world, "seq_len": cfg.T, "parallelism": f"replicas{world}",
+            "l2": "inputs larger than L2 (each step reads a 456 MB weight set)"}
+
+
 def job_rate(units_per_rank: int, world: int, ms_max: float) -> float:
     """Whole-job throughput of independent replicas: the units every rank processed in
     one step, over the slowest rank's step time (ms)."""
@@ -347,10 +355,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16xint4 (fp32 accumulate); router bf16",
         "data": "synthetic (seeded; int4 g64 affine weights, N(0,1) activations)",
-        "config": {"workload": "prefill_t8192: one MoE layer, T=8192, d=2048, E=256 top-8 + 1 shared, I=512, "
-                               "int4 group-64 bf16 scale/bias, 4 weight+activation sets cycled",
-                   "global_batch": cfg.T * world, "seq_len": cfg.T, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2 (each step reads a 456 MB weight set)"},
+        "config": workload_config(cfg, world),
         "stage_us": {k: round(v, 2) for k, v in st.items()},
         "roofline": {"kernel": "grouped_gemm_kernel (gate/up + SwiGLU)", "bound": "tensor",
                      "achieved": round(achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
@@ -410,10 +415,11 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
-            "config": {"workload": "prefill_t8192 (bounded sample per step)", "global_batch": cfg.T,
-                       "seq_len": cfg.T, "parallelism": "cpu"},
+            "config": workload_config(cfg, args.gpus),
             "cpu_baseline": {"value": round(rate, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
-                             "kind": "oracle", "sample": f"{n_tok} tokens of prefill_t8192 per step"},
+                             "kind": "oracle",
+                             "sample": f"{n_tok} tokens of the prefill_t8192 workload per step (router + top-8 "
+                                       f"+ 9 experts each), weight set 0"},
             "e2e": {"value": round(rate, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

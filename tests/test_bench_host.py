@@ -1,4 +1,5 @@
-"""Multi-process host logic of the benchmark on CPU (gloo, world size 2).
+"""Host logic of the benchmark on CPU: the multi-process plumbing (gloo, world size 2) and
+the reference arm's JSON line.
 
 The layer has no exchange step, so N GPUs run N independent replicas: the only
 cross-rank traffic is the barrier around the timed region and the max of the
@@ -73,3 +74,27 @@ def test_reference_arm_on_a_nonzero_rank_exits_without_work():
                        timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_prints_one_contract_line_on_cpu():
+    # the oracle arm runs on host cores only: one step on a 2-token sample
+    import json
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3", "--cpu-tokens", "2"], cwd=ROOT, capture_output=True, text=True, timeout=300,
+                       env={k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1 and "2 tokens" in d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    sys.path.insert(0, ROOT)
+    import bench
+    from bit_grouped_expert_top_gb300.inputs import CONFIGS
+    assert d["config"] == bench.workload_config(CONFIGS["prefill_t8192"], 1)  # the GPU arm's config
