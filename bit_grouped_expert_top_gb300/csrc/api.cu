@@ -6,7 +6,9 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <set>
 #include <string>
+#include <tuple>
 #include <unordered_map>
 #include <vector>
 
@@ -15,6 +17,21 @@
 
 namespace lily {
 cudaError_t launch_decode_final_norm(const float *prev_out, uint16_t *x_export, int T, int d, cudaStream_t stream);
+
+cudaError_t set_max_dynamic_smem(const void *kernel, int bytes)
+{
+    static std::mutex mu;
+    static std::set<std::tuple<const void *, int, int>> done;  // (kernel, device, bytes)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const auto key = std::make_tuple(kernel, dev, bytes);
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert(key);
+    return e;
+}
 }  // namespace lily
 
 namespace {

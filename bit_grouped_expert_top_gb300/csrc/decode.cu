@@ -554,13 +554,10 @@ size_t decode_smem_gateup(int d) { return static_cast<size_t>(d) * 8 * 2 + kDecW
 
 cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStream_t stream)
 {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e;
-        if ((e = cudaFuncSetAttribute(dec_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) != cudaSuccess) return e;
-        if ((e = cudaFuncSetAttribute(dec_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) != cudaSuccess) return e;
-        if ((e = cudaFuncSetAttribute(dec_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) != cudaSuccess) return e;
-        configured = true;
+    for (const void *k : {reinterpret_cast<const void *>(dec_route_kernel), reinterpret_cast<const void *>(dec_gateup_kernel),
+                          reinterpret_cast<const void *>(dec_down_kernel)}) {
+        const cudaError_t e = set_max_dynamic_smem(k, 200 * 1024);
+        if (e != cudaSuccess) return e;
     }
     // programmatic dependent launches: each kernel starts while its predecessor finishes
     cudaLaunchAttribute attr[1];

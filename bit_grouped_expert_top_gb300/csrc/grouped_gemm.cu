@@ -828,14 +828,10 @@ template <int MODE>
 static cudaError_t launch_mode(const GemmArgs &g, const CUtensorMap &tmB, const CUtensorMap &tmA0, const CUtensorMap &tmA1,
                                const CUtensorMap &tmSA0, const CUtensorMap &tmSA1, int grid, cudaStream_t stream)
 {
-    static bool configured = false;
     const size_t smem = grouped_gemm_smem_bytes();
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    const cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(grouped_gemm_kernel<MODE>),
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
     return launch_pdl(grouped_gemm_kernel<MODE>, dim3(grid), dim3(kThreads), smem, stream, g, tmB, tmA0, tmA1, tmSA0,
                       tmSA1);
 }

@@ -66,6 +66,11 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device.  Function attributes belong to a device, so this runs once per
+// (kernel, device, size); safe to call from several host threads.
+cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
+
 // Dynamic shared memory bytes of grouped_gemm_kernel.
 size_t grouped_gemm_smem_bytes();
 
