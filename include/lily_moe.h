@@ -230,7 +230,7 @@ int lily_moe_device_status(const void *ws, cudaStream_t stream);
 int lily_moe_clear_status(void *ws, cudaStream_t stream);
 
 /*
- * Routing without a caller workspace.  The paper has no counterpart: this entry
+ * Routing without a caller workspace.  The method has no counterpart: this entry
  * point exists for callers that may not allocate device memory when they call
  * the layer, e.g. a plugin that runs inside another engine's fixed memory
  * budget, or a serving loop that forbids device allocation after start-up, and
