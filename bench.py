@@ -191,6 +191,48 @@ def prefill_flops(cfg, T):
     return T * per_tok, T * 2 * 2 * cfg.d * cfg.I * (cfg.top_k + 1), T * 2 * cfg.d * cfg.I * (cfg.top_k + 1)
 
 
+def tensor_peak(peaks, clocks):
+    """Dense bf16 tensor peak to divide by (the fp16 dense rate is the same).
+    The burst figure applies while the SM clock stays at its maximum during the
+    timed region (the step is short and under the power limit); the sustained
+    one, measured under the power cap, when the clock was held down."""
+    burst, sust = peaks["bf16_tflops"], peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    if sm and mx and sm < 0.95 * mx:
+        return sust, f"{peaks['source']} bf16 sustained (SM clock {sm:.0f} of {mx:.0f} MHz under load)"
+    return burst, (f"{peaks['source']} bf16 burst (SM clock {sm:.0f} of {mx:.0f} MHz under load; "
+                   f"sustained figure {sust})" if sm and mx else f"{peaks['source']} bf16 burst")
+
+
+def routing_counts(ctx, stream):
+    """Expert histogram of the first weight/activation set (one routing call)."""
+    import bit_grouped_expert_top_gb300 as lm
+    rt = lm.alloc_routing(ctx["shape"])
+    stream.wait_stream(__import__("torch").cuda.current_stream())
+    lm.lily_moe_route(ctx["shape"], ctx["ws_l"][0], ctx["xs"][0], lm.make_routing(rt), ctx["ws"], stream=stream)
+    stream.synchronize()
+    return rt["counts"].cpu().numpy()
+
+
+def config_roofline(cfg, ms, counts, peaks, peak_tc):
+    """Roofline of one prefill workload from its realised expert counts: the
+    method's FLOPs (9 experts per token + router) against the tensor peak, and
+    its bytes (int4 + scale/bias of every expert with a token, the shared
+    expert, the router, x in and out) against HBM; the bound is the larger time."""
+    from bit_grouped_expert_top_gb300.inputs import weight_bytes
+    wb = weight_bytes(cfg)
+    touched = int((counts > 0).sum())
+    nbytes = (touched + 1) * wb["expert"] + wb["router"] + cfg.T * cfg.d * 2 + cfg.T * cfg.d * 4
+    flops = prefill_flops(cfg, cfg.T)[0]
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peak_tc * 1e12)
+    t = ms * 1e-3
+    return {"bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": round(max(t_hbm, t_tc) / t, 4),
+            "hbm_gbs": round(nbytes / t / 1e9, 1), "hbm_peak": peaks["hbm_gbs"],
+            "tflops": round(flops / t / 1e12, 1), "tensor_peak": peak_tc,
+            "algorithmic_bytes": int(nbytes), "algorithmic_flops": int(flops), "experts_touched": touched}
+
+
 def time_prefill(cfg, steps, warmup, n_sets, stream, with_stages=True):
     """Device time of `steps` forward passes cycling n_sets weight/activation sets."""
     import torch
@@ -240,7 +282,7 @@ def stage_means(ctx):
     return {n: statistics.mean(v) for n, v in acc.items()}
 
 
-def bench_decode(cfg, Ts, reps, stream):
+def bench_decode(cfg, Ts, reps, stream, peaks):
     """µs per layer of lily_moe_decode over cfg.n_layers distinct layers."""
     import numpy as np
     import torch
@@ -277,6 +319,7 @@ def bench_decode(cfg, Ts, reps, stream):
         res[f"T{T}"] = {"us_per_layer": round(us_layer, 3), "experts_read_per_layer": round(float(distinct) + 1, 2),
                         "weight_bytes_per_layer": int(total_bytes),
                         "achieved_gbs": round(total_bytes / (us_layer * 1e-6) / 1e9, 1),
+                        "frac_of_hbm": round(total_bytes / (us_layer * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
                         "expert_bytes_gbs": round(expert_bytes / (us_layer * 1e-6) / 1e9, 1)}
     return res
 
@@ -310,8 +353,9 @@ def run_ours(args):
         raise RuntimeError("device status error in timed region")
     tokens_per_s = job_rate(cfg.T, world, ms)
     flops_total, flops_gu, flops_down = prefill_flops(cfg, cfg.T)
-    peak_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])  # fp16 dense rate = bf16 rate
+    peak_tc, peak_note = tensor_peak(peaks, clocks)
     achieved = flops_gu / (st["gateup"] * 1e-6) / 1e12
+    layer_tflops = flops_total / (ms * 1e-3) / 1e12
 
     # e2e: host buffers through the public call, H2D of x and D2H of out inside the timed region
     x_host = [x.cpu().pin_memory() for x in ctx["xs"]]
@@ -344,11 +388,14 @@ def run_ours(args):
             stream.synchronize()
             ms_c = cx["start"].elapsed_time(cx["end"]) / 50
             stc = stage_means(cx)
+            counts = routing_counts(cx, stream)
             also[name] = {"tokens_per_s": round(c.T / (ms_c * 1e-3)), "us_per_layer": round(ms_c * 1e3, 2),
-                          "stage_us": {k: round(v, 2) for k, v in stc.items()}, "inputs_vs_l2": "weights 456 MB > L2"}
+                          "stage_us": {k: round(v, 2) for k, v in stc.items()},
+                          "roofline": config_roofline(c, ms_c, counts, peaks, peak_tc),
+                          "inputs_vs_l2": "weights 456 MB > L2"}
             del cx
         torch.cuda.empty_cache()
-        also["decode_l40"] = bench_decode(CONFIGS["decode_t1_l40"], (1, 2, 4, 8), 20, stream)
+        also["decode_l40"] = bench_decode(CONFIGS["decode_t1_l40"], (1, 2, 4, 8), 20, stream, peaks)
 
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
@@ -360,10 +407,15 @@ def run_ours(args):
         "roofline": {"kernel": "grouped_gemm_kernel (gate/up + SwiGLU)", "bound": "tensor",
                      "achieved": round(achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tc, 4), "traffic": gateup_traffic(),
-                     "traffic_unit": "bytes per launch (ncu dram read+write, profiles/grouped_gemm_t8192_dram.md)",
-                     "peak_note": f"{peaks['source']} bf16 sustained (fp16 dense rate = bf16 rate)",
+                     "traffic_unit": "bytes per launch (ncu dram read+write of the current kernel source, "
+                                     "null if the source changed since the capture)",
+                     "peak_note": peak_note,
                      "algorithmic_flops_per_launch": flops_gu},
-        "layer_tflops": round(flops_total / (ms * 1e-3) / 1e12, 1),
+        "roofline_layer": {"what": "whole layer: router + routing tables + expert GEMMs, ms_per_step",
+                           "bound": "tensor", "achieved": round(layer_tflops, 1), "peak": peak_tc,
+                           "unit": "TFLOP/s", "frac": round(layer_tflops / peak_tc, 4),
+                           "algorithmic_flops_per_step": flops_total, "peak_note": peak_note},
+        "layer_tflops": round(layer_tflops, 1),
         "clocks": clocks,
         "e2e": {"value": round(job_rate(cfg.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 4},

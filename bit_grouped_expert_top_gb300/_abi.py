@@ -23,7 +23,7 @@ _lib: Optional[ctypes.CDLL] = None
 LILY_OK = 0
 STATUS_NAMES = {0: "LILY_OK", -1: "LILY_ERR_INVALID", -2: "LILY_ERR_UNSUPPORTED", -3: "LILY_ERR_MISALIGNED",
                 -4: "LILY_ERR_WORKSPACE", -5: "LILY_ERR_LAUNCH", -6: "LILY_ERR_DEVICE_TIMEOUT",
-                -7: "LILY_ERR_DEVICE_INDEX", -8: "LILY_ERR_SCRATCH_LIMIT"}
+                -7: "LILY_ERR_DEVICE_INDEX", -8: "LILY_ERR_SCRATCH_LIMIT", -9: "LILY_ERR_DEVICE_RANGE"}
 
 
 class LilyError(RuntimeError):
@@ -54,6 +54,33 @@ class lily_moe_decode_trace(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("logits", "topk_idx", "topk_w")]
 
 
+def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Declares the argument and return types of every entry point."""
+    P, S, I32, I64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64
+    PS, PW, PR = ctypes.POINTER(lily_moe_shape), ctypes.POINTER(lily_moe_weights), ctypes.POINTER(lily_moe_routing)
+    L.lily_moe_version.restype = I32
+    L.lily_moe_status_string.restype = ctypes.c_char_p
+    L.lily_moe_status_string.argtypes = [I32]
+    L.lily_moe_check_shape.argtypes = [PS]
+    L.lily_moe_block_capacity.restype = I64
+    L.lily_moe_block_capacity.argtypes = [PS]
+    L.lily_moe_workspace_bytes.restype = S
+    L.lily_moe_workspace_bytes.argtypes = [PS, ctypes.c_int32]
+    L.lily_moe_route.argtypes = [PS, PW, P, PR, P, S, P]
+    L.lily_moe_grouped_gemm.argtypes = [PS, PW, P, PR, P, P, S, P]
+    L.lily_moe_forward.argtypes = [PS, PW, P, P, PR, P, S, P]
+    L.lily_moe_forward_timed.argtypes = [PS, PW, P, P, PR, P, S, P, ctypes.POINTER(ctypes.c_void_p)]
+    L.lily_moe_decode.argtypes = [PS, ctypes.c_int32, PW, P, P, P, ctypes.POINTER(lily_moe_decode_trace), P, S, P]
+    L.lily_moe_route_noalloc.argtypes = [PS, PW, P, PR, P, P]
+    L.lily_moe_device_status.argtypes = [P, P]
+    L.lily_moe_clear_status.argtypes = [P, P]
+    for n in ("lily_moe_check_shape", "lily_moe_route", "lily_moe_grouped_gemm", "lily_moe_forward",
+              "lily_moe_forward_timed", "lily_moe_decode", "lily_moe_device_status", "lily_moe_route_noalloc",
+              "lily_moe_clear_status"):
+        getattr(L, n).restype = I32
+    return L
+
+
 def load(path: Optional[str] = None) -> ctypes.CDLL:
     """Loads the in-tree library (building it first if needed)."""
     global _lib
@@ -62,32 +89,20 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             p = path or _build.build()
             if not os.path.exists(p):
                 raise OSError(f"liblily_moe.so not found at {p}")
-            L = ctypes.CDLL(p)
-            P, S, I32, I64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64
-            PS, PW, PR = ctypes.POINTER(lily_moe_shape), ctypes.POINTER(lily_moe_weights), ctypes.POINTER(lily_moe_routing)
-            L.lily_moe_version.restype = I32
-            L.lily_moe_status_string.restype = ctypes.c_char_p
-            L.lily_moe_status_string.argtypes = [I32]
-            L.lily_moe_check_shape.argtypes = [PS]
-            L.lily_moe_block_capacity.restype = I64
-            L.lily_moe_block_capacity.argtypes = [PS]
-            L.lily_moe_workspace_bytes.restype = S
-            L.lily_moe_workspace_bytes.argtypes = [PS, ctypes.c_int32]
-            L.lily_moe_route.argtypes = [PS, PW, P, PR, P, S, P]
-            L.lily_moe_grouped_gemm.argtypes = [PS, PW, P, PR, P, P, S, P]
-            L.lily_moe_forward.argtypes = [PS, PW, P, P, PR, P, S, P]
-            L.lily_moe_forward_timed.argtypes = [PS, PW, P, P, PR, P, S, P, ctypes.POINTER(ctypes.c_void_p)]
-            L.lily_moe_decode.argtypes = [PS, ctypes.c_int32, PW, P, P, P, ctypes.POINTER(lily_moe_decode_trace),
-                                          P, S, P]
-            L.lily_moe_route_noalloc.argtypes = [PS, PW, P, PR, P, P]
-            L.lily_moe_device_status.argtypes = [P, P]
-            L.lily_moe_clear_status.argtypes = [P, P]
-            for n in ("lily_moe_check_shape", "lily_moe_route", "lily_moe_grouped_gemm", "lily_moe_forward",
-                      "lily_moe_forward_timed", "lily_moe_decode", "lily_moe_device_status", "lily_moe_route_noalloc",
-                      "lily_moe_clear_status"):
-                getattr(L, n).restype = I32
-            _lib = L
+            _lib = _configure(ctypes.CDLL(p))
     return _lib
+
+
+_variants: Dict[str, ctypes.CDLL] = {}
+
+
+def load_variant(variant: str) -> ctypes.CDLL:
+    """Loads a test-only build variant of the library (see build.VARIANTS) as a
+    separate library with its own kernels and static device data."""
+    with _lock:
+        if variant not in _variants:
+            _variants[variant] = _configure(ctypes.CDLL(_build.build(variants=(variant,))))
+    return _variants[variant]
 
 
 # ------------------------------------------------------------------ marshalling helpers

@@ -15,21 +15,26 @@
 #include "lily_internal.h"
 #include "lily_moe.h"
 
+namespace {
+unsigned long long current_context_id();
+}  // namespace
+
 namespace lily {
 cudaError_t launch_decode_final_norm(const float *prev_out, uint16_t *x_export, int T, int d, cudaStream_t stream);
 
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes)
 {
     static std::mutex mu;
-    static std::set<std::tuple<const void *, int, int>> done;  // (kernel, device, bytes)
+    static std::set<std::tuple<const void *, int, unsigned long long, int>> done;  // (kernel, device, context, bytes)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const auto key = std::make_tuple(kernel, dev, bytes);
+    const unsigned long long ctx_id = current_context_id();
+    const auto key = std::make_tuple(kernel, dev, ctx_id, bytes);
     std::lock_guard<std::mutex> lock(mu);
     if (done.count(key)) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) done.insert(key);
+    if (e == cudaSuccess && ctx_id != 0) done.insert(key);
     return e;
 }
 }  // namespace lily
@@ -38,7 +43,40 @@ namespace {
 
 using namespace lily;
 
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 10100;  // 1.1.0
+
+// Unique id of the CUDA context current on this thread (the runtime's primary
+// context of the current device), 0 if none is current yet.  Caches of
+// device-side state (symbol addresses, instantiated graphs) are keyed by it:
+// after cudaDeviceReset the device gets a new context with a new id, so no
+// entry made in the old context is used again.
+// The two driver calls are looked up through the runtime (the library does
+// not link the driver library, so it still loads on a machine without one).
+unsigned long long current_context_id()
+{
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr, *q = nullptr;
+        cudaDriverEntryPointQueryResult r1, r2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r1) == cudaSuccess &&
+            r1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) == cudaSuccess &&
+            r2 == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+            get_id = reinterpret_cast<GetIdFn>(q);
+        }
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -419,20 +457,23 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[LILY_NOALLOC_SC
 
 namespace {
 
-// Device address of g_noalloc_scratch on the current device, looked up once per
-// device (with that device current).  Returns nullptr if the lookup fails.
+// Device address of g_noalloc_scratch in the current context, looked up once
+// per context (with its device current).  Returns nullptr if the lookup fails.
 void *noalloc_scratch_address()
 {
     static std::mutex mu;
-    static std::unordered_map<int, void *> addr;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    static std::unordered_map<unsigned long long, void *> addr;  // context id -> address
     std::lock_guard<std::mutex> lock(mu);
-    auto it = addr.find(dev);
-    if (it != addr.end()) return it->second;
+    const unsigned long long id = current_context_id();
+    if (id != 0) {
+        auto it = addr.find(id);
+        if (it != addr.end()) return it->second;
+    }
+    // the lookup makes the device's primary context current if none was yet
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    addr[dev] = p;
+    const unsigned long long id2 = current_context_id();
+    if (id2 != 0) addr[id2] = p;
     return p;
 }
 
@@ -454,6 +495,7 @@ const char *lily_moe_status_string(int status)
     case LILY_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case LILY_ERR_DEVICE_INDEX: return "device index out of range";
     case LILY_ERR_SCRATCH_LIMIT: return "token count above the fixed scratch of lily_moe_route_noalloc";
+    case LILY_ERR_DEVICE_RANGE: return "a value of x or h beyond the fp16 range of the expert GEMMs";
     default: return "unknown status";
     }
 }
@@ -595,6 +637,9 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
     int dev = 0;
     cudaGetDevice(&dev);
     put(&dev, sizeof dev);
+    // the context the graph was instantiated in (a reset device gets a new one)
+    const unsigned long long ctx_id = current_context_id();
+    put(&ctx_id, sizeof ctx_id);
     put(&s, sizeof s);
     put(&n_layers, sizeof n_layers);
     put(layers, sizeof(lily_moe_weights) * n_layers);
@@ -643,7 +688,12 @@ int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *
     if (L.chunk_base + static_cast<size_t>(ceil_div(shape->T, kRouteChunkTokens)) * shape->E * 4 >
         LILY_NOALLOC_SCRATCH_BYTES)
         return LILY_ERR_SCRATCH_LIMIT;
-    if (shape->T == 0) return LILY_OK;
+    if (shape->T == 0) {
+        // nothing to route; the call's status (OK) still goes to device_status
+        if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int32_t), stream) != cudaSuccess)
+            return LILY_ERR_LAUNCH;
+        return LILY_OK;
+    }
     if ((rc = check_ptr(x))) return rc;
     void *scratch = noalloc_scratch_address();
     if (!scratch) return LILY_ERR_LAUNCH;

@@ -10,14 +10,15 @@
 // Three kernels per layer:
 //   dec_route_kernel  : builds the layer input (layer 0: x; later layers: the
 //                       parameter-free RMS norm of the previous output, rounded
-//                       to bf16), router GEMV (one warp per expert), and in the
-//                       last CTA the top-8 selection per token and the list of
-//                       distinct experts ("units") with per-token weights; the
-//                       shared expert is the last unit with weight 1.
-//   dec_gateup_kernel : tensor-core GEMV (mma.sync m16n8k16, the tokens as the
-//                       8 columns): per unit and 32 rows of I, gate and up
-//                       dequantised in registers, SwiGLU, scaled by the unit's
-//                       routing weight per token, h' stored as fp16.
+//                       to bf16) and the router GEMV (one warp per expert).
+//   dec_gateup_kernel : every CTA computes the top-8 selection per token from
+//                       the logits and the list of distinct experts ("units")
+//                       with per-token weights (the shared expert is unit 0
+//                       with weight 1); then a tensor-core GEMV (mma.sync
+//                       m16n8k16, the tokens as the 8 columns): per unit and 32
+//                       rows of I, gate and up dequantised in registers, SwiGLU,
+//                       scaled by the unit's routing weight per token, h' stored
+//                       as fp16.
 //   dec_down_kernel   : tensor-core GEMV over K = units x I: per 16 output
 //                       rows, sum over the units of Wd h' (deterministic, no
 //                       atomics).
@@ -195,6 +196,8 @@ dec_route_kernel(const DecodeLayerArgs a)
                 const __half2 h2 = __floats2half2_rn(f[1], f[3]), h3 = __floats2half2_rn(f[5], f[7]);
                 o = make_uint4(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1),
                                *reinterpret_cast<const uint32_t *>(&h2), *reinterpret_cast<const uint32_t *>(&h3));
+                if (f16x2_has_inf(o.x) | f16x2_has_inf(o.y) | f16x2_has_inf(o.z) | f16x2_has_inf(o.w))
+                    record_error(&a.ctrl->status, kErrDeviceRange);
             }
             *reinterpret_cast<uint4 *>(a.xp + perm_b_index(k0, n)) = o;
         }
@@ -451,7 +454,9 @@ dec_gateup_kernel(const DecodeLayerArgs a)
                 const int i = i0 + g + 8 * (q >> 1);
                 const float wt = s_w[u][n];
                 const float hv = wt * silu_f(accg[q]) * accu[q];
-                a.h[perm_b_index(u * I + i, n)] = __float2half_rn(hv);
+                const __half hh = __float2half_rn(hv);
+                if (__hisinf(hh)) record_error(&a.ctrl->status, kErrDeviceRange);
+                a.h[perm_b_index(u * I + i, n)] = hh;
             }
         }
         __syncthreads();

@@ -87,6 +87,9 @@ struct __align__(1024) Smem {
     uint64_t full_a[kABars], empty_a[kABars];
     uint64_t full_acc[2], empty_acc[2];
     uint64_t drain;
+#ifdef LILY_TEST_STALL_T
+    uint64_t never;        // test builds only: a barrier nothing arrives on
+#endif
     uint32_t tmem_base;
     int abort_flag;
     int ep_go;             // epilogue's wait result, published by its waiting thread
@@ -155,7 +158,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, int *
     const uint32_t addr = smem_u32(bar);
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(addr, parity)) {
-        if (global_timer_ns() - t0 > LILY_WAIT_LIMIT_NS) {
+        if (global_timer_ns() - t0 > LILY_DRAIN_LIMIT_NS) {
             record_error(status, kErrDeviceTimeout);
             return;
         }
@@ -218,6 +221,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             mbar_init(&S.empty_acc[s], 8);
         }
         mbar_init(&S.drain, kIssuers);
+#ifdef LILY_TEST_STALL_T
+        mbar_init(&S.never, 1);
+#endif
         S.abort_flag = 0;
         fence_mbar_init();
     }
@@ -605,7 +611,19 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             }
             // one thread waits for the accumulator; the group-wide result keeps the
             // warp-collective tcgen05.ld below uniform
-            if (eid == 0) S.ep_go = ok && mbar_wait(&S.full_acc[ab], acc_ph, abort_flag, status);
+            if (eid == 0) {
+                bool go = ok;
+#ifdef LILY_TEST_STALL_T
+                // Test builds only: for T == LILY_TEST_STALL_T the first unit's
+                // accumulator wait is preceded by a wait on a barrier that nothing
+                // completes, so the bounded wait runs out and the abort path
+                // (every role gives up, in-flight copies and MMAs drain, TMEM is
+                // freed) executes.
+                if (go && g.T == LILY_TEST_STALL_T && tile == static_cast<int>(blockIdx.x))
+                    go = mbar_wait(&S.never, 0, abort_flag, status);
+#endif
+                S.ep_go = go && mbar_wait(&S.full_acc[ab], acc_ph, abort_flag, status);
+            }
             named_barrier_sync(kBarEpilogue, 256);  // also publishes ep_tok / ep_w
             const bool got = S.ep_go != 0;
             if (!got) ok = false;
@@ -618,6 +636,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                     // packed as fp16 pairs in registers, so the accumulator is released
                     // before the stores
                     uint32_t hp[kTileN / 32][8];
+                    bool inf = false;
 #pragma unroll
                     for (int q = 0; q < kTileN / 32; ++q) {
                         const int c0 = half * 16 + 32 * q;
@@ -632,9 +651,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                                     silu_f(__uint_as_float(v0[2 * j])) * __uint_as_float(v1[2 * j]),
                                     silu_f(__uint_as_float(v0[2 * j + 1])) * __uint_as_float(v1[2 * j + 1]));
                                 hp[q][j] = *reinterpret_cast<const uint32_t *>(&hv);
+                                // only this unit's tokens count (padding columns hold other rows)
+                                const uint32_t a = hp[q][j] & 0x7FFF7FFFu;
+                                inf |= (c0 + 2 * j < u.rows && (a & 0xFFFFu) == 0x7C00u) |
+                                       (c0 + 2 * j + 1 < u.rows && (a >> 16) == 0x7C00u);
                             }
                         }
                     }
+                    if (inf) record_error(status, kErrDeviceRange);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&S.empty_acc[ab]);
@@ -768,11 +792,17 @@ __global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, const
         const uint4 *src = x + static_cast<int64_t>(t) * d8;
         for (int i0 = 0; i0 < d8; i0 += 256) {
             uint4 v[8];
+            bool inf = false;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = i0 + j * 32 + lane;
-                if (i < d8) v[j] = bf16x8_to_f16x8_kperm(__ldg(src + i));
+                if (i < d8) {
+                    v[j] = bf16x8_to_f16x8_kperm(__ldg(src + i));
+                    inf |= f16x2_has_inf(v[j].x) | f16x2_has_inf(v[j].y) | f16x2_has_inf(v[j].z) |
+                           f16x2_has_inf(v[j].w);
+                }
             }
+            if (inf) record_error(status, kErrDeviceRange);
             for (int k = 0; k <= top_k; ++k) {  // the token's top_k routed rows and its shared row
                 const int64_t r = __shfl_sync(0xffffffffu, row, k);
                 if (r < 0) continue;

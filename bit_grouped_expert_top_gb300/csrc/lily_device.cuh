@@ -1,7 +1,8 @@
 // Device-side building blocks for the sm_103a kernels: inline PTX wrappers for
 // mbarrier, TMA (cp.async.bulk.tensor), cp.async, the 5th-generation tensor core
 // (tcgen05.mma / tcgen05.ld with accumulators in tensor memory), bounded waits
-// that report a timeout instead of hanging, and the int4 -> bf16 dequantisation.
+// that report a timeout instead of hanging, the int4 -> fp16 dequantisation and
+// the warp top-8 selection.
 #pragma once
 
 #include <cstdint>
@@ -15,6 +16,7 @@ namespace lily {
 // Device-detected error codes (same values as LILY_ERR_DEVICE_* in lily_moe.h).
 constexpr int kErrDeviceTimeout = -6;
 constexpr int kErrDeviceIndex = -7;
+constexpr int kErrDeviceRange = -9;  // a finite value beyond the fp16 range of the expert GEMM operands
 
 // Control block at the start of every workspace.
 struct Ctrl {
@@ -25,11 +27,17 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 
-// Wall-clock bound of every spin-wait (nanoseconds).  A wait that exceeds it
-// records kErrDeviceTimeout and gives up.
+// Wall-clock bound of every pipeline spin-wait (nanoseconds).  A wait that
+// exceeds it records kErrDeviceTimeout and gives up.
 #ifndef LILY_WAIT_LIMIT_NS
 #define LILY_WAIT_LIMIT_NS 2000000000ull
 #endif
+// Bound of the waits on a kernel's exit path, which wait for copies and
+// tensor-core work already in flight before shared and tensor memory are
+// given back.  It stays at 2 s in every build (a test build that shortens
+// LILY_WAIT_LIMIT_NS keeps it), so nothing can still be writing when a CTA
+// frees its tensor memory or exits.
+#define LILY_DRAIN_LIMIT_NS 2000000000ull
 
 __device__ __forceinline__ void record_error(int *status, int code)
 {
@@ -153,27 +161,6 @@ __device__ __forceinline__ bool mbar_wait2(uint64_t *bar0, uint32_t parity0, uin
     return (ok0 || mbar_wait(bar0, parity0, abort_flag, status)) && (ok1 || mbar_wait(bar1, parity1, abort_flag, status));
 }
 
-// Latency-critical wait: polls with the non-blocking test_wait so the thread
-// sees the phase flip at once; same bounds and abort handling as mbar_wait.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status)
-{
-    const uint32_t addr = smem_u32(bar);
-#pragma unroll 1
-    for (int i = 0; i < 4096; ++i)
-        if (mbar_test_wait(addr, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-#pragma unroll 1
-    while (true) {
-        if (mbar_test_wait(addr, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > LILY_WAIT_LIMIT_NS) {
-            record_error(status, kErrDeviceTimeout);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
 // Programmatic dependent launch: this grid lets the next one start launching,
 // and waits (before touching any global memory an earlier kernel of the stream
 // reads or writes) until the preceding grid has completed and its memory is
@@ -198,21 +185,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// Row gather: four rows (r0..r3) of a 2-D tensor whose box is one row high,
-// each box_inner elements from column c0, written one after another into
-// shared memory (the swizzle follows the shared-memory address, so four-row
-// groups at 512-byte offsets of a 1024-aligned buffer form the same layout as
-// one tiled load).  Completion is signalled on `bar` as transaction bytes.
-__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int4 rows)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w),
-        "r"(smem_u32(bar))
-        : "memory");
-}
-
 // ----------------------------------------------------------------- cp.async (16-byte gathers)
 __device__ __forceinline__ void cp_async_16(void *dst, const void *src)
 {
@@ -220,51 +192,7 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
-// Arrive on `bar` once every cp.async this thread issued so far has landed
-// (the barrier's expected count already includes this arrival: noinc).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// Bulk (non-tensor) asynchronous copies shared -> global, tracked per thread in
-// bulk groups.  Addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
-                 "r"(bytes)
-                 : "memory");
-}
-// gdst[i] += ssrc[i] (fp32), performed by the memory system.
-__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const float *ssrc, uint32_t bytes)
-{
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
-                 "r"(smem_u32(ssrc)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until the shared-memory sources of all but the N most recent of this
-// thread's bulk groups have been read.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Waits until this thread's bulk groups have fully completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy reads (tensor core operands).
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // Named barrier over `nthreads` threads (whole warps); the warp is reconverged
 // first, as bar.sync is warp-aligned.
@@ -352,21 +280,6 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t ab_fmt, int M, int 
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// 32 lanes x 32 columns of 32-bit accumulator: thread i of the warp gets lane
-// (base lane + i), columns [col, col + 32).
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-          "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
 // 32 lanes x 16 columns of 32-bit accumulator.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
 {
@@ -394,67 +307,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
         : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// ----------------------------------------------------------------- int4 -> bf16
-// Eight packed 4-bit weights (one 32-bit word: element i in bits [4i, 4i+4),
-// i.e. low nibble first within each byte) -> eight bf16 values
-// w_i = q_i * s + b, each rounded once to bf16 (fma.rn.bf16x2), returned in
-// element order as four bf16x2 words.
-//
-// Nibbles are placed into the mantissa of the bf16 number 128 (0x4300): the
-// pattern 0x4300 | q encodes exactly 128 + q for q in 0..15, so subtracting 128
-// recovers q exactly (the int -> float trick of placing an integer in the
-// mantissa of a power of two).
-__device__ __forceinline__ uint4 dequant8_bf16(uint32_t v, __nv_bfloat162 s2, __nv_bfloat162 b2)
-{
-    const uint32_t kMagic = 0x43004300u;
-    const uint32_t kMask = 0x000F000Fu;
-    uint32_t p04 = (v & kMask) | kMagic;          // (q0, q4)
-    uint32_t p15 = ((v >> 4) & kMask) | kMagic;   // (q1, q5)
-    uint32_t p26 = ((v >> 8) & kMask) | kMagic;   // (q2, q6)
-    uint32_t p37 = ((v >> 12) & kMask) | kMagic;  // (q3, q7)
-    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
-    __nv_bfloat162 f04 = __hfma2(__hsub2(*reinterpret_cast<__nv_bfloat162 *>(&p04), k128), s2, b2);
-    __nv_bfloat162 f15 = __hfma2(__hsub2(*reinterpret_cast<__nv_bfloat162 *>(&p15), k128), s2, b2);
-    __nv_bfloat162 f26 = __hfma2(__hsub2(*reinterpret_cast<__nv_bfloat162 *>(&p26), k128), s2, b2);
-    __nv_bfloat162 f37 = __hfma2(__hsub2(*reinterpret_cast<__nv_bfloat162 *>(&p37), k128), s2, b2);
-    const uint32_t u04 = *reinterpret_cast<uint32_t *>(&f04), u15 = *reinterpret_cast<uint32_t *>(&f15);
-    const uint32_t u26 = *reinterpret_cast<uint32_t *>(&f26), u37 = *reinterpret_cast<uint32_t *>(&f37);
-    uint4 o;
-    o.x = __byte_perm(u04, u15, 0x5410);  // (w0, w1)
-    o.y = __byte_perm(u26, u37, 0x5410);  // (w2, w3)
-    o.z = __byte_perm(u04, u15, 0x7632);  // (w4, w5)
-    o.w = __byte_perm(u26, u37, 0x7632);  // (w6, w7)
-    return o;
-}
-
-// Same as dequant8_bf16 but the eight weights are rounded once to fp16
-// (fma.rn.f16x2), whose 11-bit significand holds q*s+b 8x more finely than
-// bf16.  The nibble goes into the mantissa of the fp16 number 1024 (0x6400):
-// 0x6400 | q encodes exactly 1024 + q.  s2/b2 are fp16 copies of the bf16
-// scale and bias (exact for magnitudes in [2^-14, 65504]).
-__device__ __forceinline__ uint4 dequant8_f16(uint32_t v, __half2 s2, __half2 b2)
-{
-    const uint32_t kMagic = 0x64006400u;
-    const uint32_t kMask = 0x000F000Fu;
-    uint32_t p04 = (v & kMask) | kMagic;
-    uint32_t p15 = ((v >> 4) & kMask) | kMagic;
-    uint32_t p26 = ((v >> 8) & kMask) | kMagic;
-    uint32_t p37 = ((v >> 12) & kMask) | kMagic;
-    const __half2 k1024 = __floats2half2_rn(1024.0f, 1024.0f);
-    __half2 f04 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p04), k1024), s2, b2);
-    __half2 f15 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p15), k1024), s2, b2);
-    __half2 f26 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p26), k1024), s2, b2);
-    __half2 f37 = __hfma2(__hsub2(*reinterpret_cast<__half2 *>(&p37), k1024), s2, b2);
-    const uint32_t u04 = *reinterpret_cast<uint32_t *>(&f04), u15 = *reinterpret_cast<uint32_t *>(&f15);
-    const uint32_t u26 = *reinterpret_cast<uint32_t *>(&f26), u37 = *reinterpret_cast<uint32_t *>(&f37);
-    uint4 o;
-    o.x = __byte_perm(u04, u15, 0x5410);
-    o.y = __byte_perm(u26, u37, 0x5410);
-    o.z = __byte_perm(u04, u15, 0x7632);
-    o.w = __byte_perm(u26, u37, 0x7632);
-    return o;
-}
 
 // Two 6-bit e2m3 values (one per byte, low 6 bits) -> fp16 pair, low byte to
 // the low half.  A byte holding a nibble q in its low 4 bits (sign 0, exponent
@@ -500,22 +352,20 @@ __host__ __device__ __forceinline__ int kperm8_e2m3(int k)
     return (k & ~7) | ((j >> 1) + ((j & 1) << 2));
 }
 
+// True if either half of a packed fp16 pair is infinite: a finite input
+// (bf16 x, or the fp32 SwiGLU product h) at or beyond 65520 in magnitude
+// rounds to infinity when it is converted to an fp16 GEMM operand.
+__device__ __forceinline__ bool f16x2_has_inf(uint32_t v)
+{
+    const uint32_t a = v & 0x7FFF7FFFu;
+    return ((a & 0xFFFFu) == 0x7C00u) | ((a >> 16) == 0x7C00u);
+}
+
 // bf16 bit pattern -> fp16 pair (value converted with round-to-nearest).
 __device__ __forceinline__ __half2 half2_from_bf16_bits(uint16_t bits)
 {
     const __half h = __float2half_rn(__uint_as_float(static_cast<uint32_t>(bits) << 16));
     return __halves2half2(h, h);
-}
-
-__device__ __forceinline__ __nv_bfloat162 bf16x2_splat(uint16_t bits)
-{
-    uint32_t u = static_cast<uint32_t>(bits) | (static_cast<uint32_t>(bits) << 16);
-    return *reinterpret_cast<__nv_bfloat162 *>(&u);
-}
-
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t bits)
-{
-    return __uint_as_float(static_cast<uint32_t>(bits) << 16);
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *p)
@@ -624,15 +474,6 @@ __device__ __forceinline__ void warp_top8_keys(const float (&lv)[8], int lane, i
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     sel_w = ex / den;
-}
-
-// As warp_top8_keys, reading the row (global memory, 16-byte aligned).
-__device__ __forceinline__ void warp_top8_of_256(const float *row, int lane, int &sel_e, float &sel_w)
-{
-    const float4 *src = reinterpret_cast<const float4 *>(row + lane * 8);
-    const float4 l0 = __ldcg(src), l1 = __ldcg(src + 1);
-    const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-    warp_top8_keys(lv, lane, sel_e, sel_w);
 }
 
 }  // namespace lily

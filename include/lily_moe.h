@@ -23,11 +23,24 @@
  *   - Every device pointer must be 16-byte aligned.
  *   - Return value: LILY_OK (0) or a negative LILY_ERR_* code.  Host-side errors
  *     are returned before anything is enqueued.  Errors detected by a kernel
- *     (a device wait that timed out, an index out of range) are written, first
- *     one wins, into a status word at the start of the workspace and are read
- *     with lily_moe_device_status().
+ *     (a device wait that timed out, an index out of range, a value beyond the
+ *     fp16 range) are written, first one wins, into a status word at the start
+ *     of the workspace and are read with lily_moe_device_status().
  *   - T = 0 is valid and enqueues nothing.
  *   - Inputs are assumed finite; NaN or Inf inputs give unspecified results.
+ *   - Range: the expert GEMMs run on fp16 operands (the rebuilt weights, x and
+ *     the SwiGLU product h; fp32 accumulation).  Every |x| and every |h| =
+ *     |silu(gate x) * (up x)| must stay below 65520, which rounds to the fp16
+ *     maximum 65504; a larger finite value would become infinite.  The kernels
+ *     check every converted x and h value and record LILY_ERR_DEVICE_RANGE in
+ *     the status word when one overflows (the outputs of that call are then
+ *     unspecified).  The router logits are computed from bf16 x in fp32 and
+ *     have no such limit.
+ *   - lily_moe_forward / lily_moe_grouped_gemm: the routing tables and logits
+ *     are bit-reproducible from run to run; the layer output is not: the down
+ *     projection adds each token's nine weighted expert rows into `out` with
+ *     fp32 atomic adds whose order varies, so `out` may differ between runs in
+ *     its last bits.  lily_moe_decode is bit-reproducible.
  *   - bf16 values are passed as their uint16 bit patterns.
  *   - A workspace must not be shared by calls that may run concurrently.
  */
@@ -51,7 +64,8 @@ enum {
     LILY_ERR_LAUNCH = -5,         /* a CUDA call failed while enqueueing */
     LILY_ERR_DEVICE_TIMEOUT = -6, /* a kernel's bounded wait ran out (device-detected) */
     LILY_ERR_DEVICE_INDEX = -7,   /* a kernel saw an index out of range (device-detected) */
-    LILY_ERR_SCRATCH_LIMIT = -8   /* size above the fixed scratch of lily_moe_route_noalloc */
+    LILY_ERR_SCRATCH_LIMIT = -8,  /* size above the fixed scratch of lily_moe_route_noalloc */
+    LILY_ERR_DEVICE_RANGE = -9    /* a value beyond the fp16 range of the expert GEMMs (device-detected) */
 };
 
 /*
@@ -174,7 +188,7 @@ int lily_moe_route(const lily_moe_shape *shape, const lily_moe_weights *w, const
 
 /*
  * Grouped expert GEMMs from given routing tables: for every expert block, the
- * gate/up GEMM with the 4-bit weights dequantised to bf16 inside the GEMM, SwiGLU,
+ * gate/up GEMM with the 4-bit weights dequantised to fp16 inside the GEMM, SwiGLU,
  * then the down GEMM whose epilogue scales by topk_w and adds into token order;
  * the shared expert is added with weight 1.  out: f32 [T][d] device, overwritten.
  * r: topk_w, perm, block_map and n_blocks are read (must be non-NULL).
@@ -245,9 +259,11 @@ int lily_moe_clear_status(void *ws, cudaStream_t stream);
  *   - r->logits must be non-NULL (the logits are an output here, not scratch).
  *   - device_status: device int32 or NULL; if given, the call's device status
  *     (LILY_OK or a LILY_ERR_DEVICE_* code) is copied there on `stream` at the
- *     end.  The scratch status word is cleared at the start of every call.
- *   - The first call on a device looks up the array's device address (no
- *     allocation); make that first call outside any stream capture.
+ *     end (T = 0: LILY_OK is written there).  The scratch status word is
+ *     cleared at the start of every call.
+ *   - The first call in a CUDA context looks up the array's device address
+ *     (no allocation; again after a device reset, which creates a new
+ *     context); make that first call outside any stream capture.
  *   - Every call on a device shares the one array: calls that may overlap on
  *     the GPU (other streams, other threads) race and must be serialised by the
  *     caller.

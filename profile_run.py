@@ -1,7 +1,8 @@
-"""Runs a few whole-layer forward passes of one seeded workload, for profilers.
+"""Runs a few whole-layer forward passes of one seeded workload, for profilers
+(a fixed, short launch sequence to put under ncu).
 
-  python -m bit_grouped_expert_top_gb300.profile_run --config prefill_t8192 --reps 2
-  python -m bit_grouped_expert_top_gb300.profile_run --config decode_t1_l40 --layers 4 --T 1 --reps 3
+  python profile_run.py --config prefill_t8192 --reps 2
+  python profile_run.py --config decode_t1_l40 --layers 4 --T 1 --reps 3
 
 Each pass launches, in order: router GEMM, top-8 + per-chunk counts, per-expert
 scan + block map, scatter, prep (fp16 x in routing order), gate/up GEMM +
@@ -11,12 +12,15 @@ status word reports an error.
 from __future__ import annotations
 
 import argparse
+import os
 import sys
 
-import torch
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
 
-import bit_grouped_expert_top_gb300 as lm
-from bit_grouped_expert_top_gb300.inputs import CONFIGS, make_layer, make_x
+import torch  # noqa: E402
+
+import bit_grouped_expert_top_gb300 as lm  # noqa: E402
+from bit_grouped_expert_top_gb300.inputs import CONFIGS, make_layer, make_x  # noqa: E402
 
 
 def main(argv=None) -> int:

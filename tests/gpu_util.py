@@ -13,7 +13,8 @@ from bit_grouped_expert_top_gb300.inputs import LayerConfig, make_layer, make_x
 from helpers import bits, layer_np
 
 # Output bound of the layer: max|gpu - oracle| <= 1e-2 * rms(oracle)
-# (weights and h rounded to bf16 inside the GPU path, fp32 accumulation).
+# (the rebuilt weights, x and h rounded to fp16 inside the GPU path, fp32
+# accumulation).
 OUT_TOL = 1e-2
 # Router logits: bf16 x bf16 products are exact in fp32; only the fp32
 # summation order differs from the fp64 oracle.
@@ -43,19 +44,61 @@ class Layer:
         return self._np
 
 
-def run_forward(cfg: LayerConfig, layer: Layer, x: torch.Tensor, block_rows: Optional[int] = None):
+GUARD_BYTES = 4096
+GUARD_BYTE = 0xA5
+
+
+class Guarded:
+    """Device tensors allocated with a GUARD_BYTES tail of GUARD_BYTE after
+    them; check() asserts that no kernel wrote past the end of any of them."""
+
+    def __init__(self):
+        self.bufs = {}
+
+    def empty(self, name: str, shape, dtype) -> torch.Tensor:
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        raw = torch.full((n + GUARD_BYTES,), GUARD_BYTE, dtype=torch.uint8, device="cuda")
+        self.bufs[name] = (raw, n)
+        return raw[:n].view(dtype).view(shape)
+
+    def check(self):
+        for name, (raw, n) in self.bufs.items():
+            tail = raw[n:].cpu().numpy()
+            assert np.all(tail == GUARD_BYTE), f"{name}: {int(np.sum(tail != GUARD_BYTE))} guard bytes overwritten"
+
+
+def run_forward(cfg: LayerConfig, layer: Layer, x: torch.Tensor, block_rows: Optional[int] = None,
+                poison_workspace: bool = False):
+    """lily_moe_forward through the C ABI with caller-owned routing tables.
+    Every output buffer carries a guard tail that is checked afterwards; with
+    poison_workspace the workspace starts as all-ones bytes (NaN as floats,
+    -1 as integers) apart from the cleared status word."""
     T = x.shape[0]
     s = shape_of(cfg, T)
     if block_rows is not None:
         s.block_rows = block_rows
     ws = lm.alloc_workspace(s)
-    rt = lm.alloc_routing(s)
+    if poison_workspace:
+        ws.fill_(0xFF)
+        lm.lily_moe_clear_status(ws)
+    g = Guarded()
+    cap = max(lm.lily_moe_block_capacity(s), 1)
+    E, k = cfg.E, cfg.top_k
+    rt = {"logits": g.empty("logits", (T, E), torch.float32),
+          "topk_idx": g.empty("topk_idx", (T, k), torch.int32),
+          "topk_w": g.empty("topk_w", (T, k), torch.float32),
+          "counts": g.empty("counts", (E,), torch.int32),
+          "offsets": g.empty("offsets", (E + 1,), torch.int32),
+          "perm": g.empty("perm", (T * k,), torch.int32),
+          "block_map": g.empty("block_map", (cap, 3), torch.int32),
+          "n_blocks": g.empty("n_blocks", (1,), torch.int32)}
     r = lm.make_routing(rt)
-    out = torch.empty((T, cfg.d), dtype=torch.float32, device="cuda")
+    out = g.empty("out", (T, cfg.d), torch.float32)
     lm.lily_moe_forward(s, layer.w, x, out, ws, routing=r)
     status = lm.lily_moe_device_status(ws)
     assert status == 0, lm.lily_moe_status_string(status)
     torch.cuda.synchronize()
+    g.check()
     res = {k: v.cpu().numpy() for k, v in rt.items()}
     res["out"] = out.cpu().numpy()
     res["n_blocks"] = int(res["n_blocks"][0])

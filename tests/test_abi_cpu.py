@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_status_strings():
     assert lm.lily_moe_version() >= 10000
-    for code in range(-7, 1):
+    for code in range(-9, 1):
         s = lm.lily_moe_status_string(code)
         assert s and s != "unknown status"
     assert lm.lily_moe_status_string(-99) == "unknown status"

@@ -72,3 +72,47 @@ def test_noalloc_matches_workspace_route_on_two_calls_in_a_row():
         np.testing.assert_allclose(got_t["topk_w"].cpu().numpy(), ref_t["topk_w"].cpu().numpy(), rtol=0, atol=2e-6)
         lg_ref = ref_t["logits"].cpu().numpy()
         assert np.max(np.abs(got_t["logits"].cpu().numpy() - lg_ref)) <= LOGIT_TOL * max(1.0, float(np.sqrt(np.mean(lg_ref ** 2))))
+
+
+@pytest.mark.gpu
+def test_noalloc_t0_writes_ok_status():
+    # no tokens: nothing runs, but the call's status (OK) still reaches device_status
+    cfg = CONFIGS["tiny"]
+    w = lm.make_weights(make_layer(cfg, "cuda"))
+    s = shape_of(cfg, 0)
+    rt = lm.alloc_routing(lm.make_shape(T=1, d=cfg.d, I=cfg.I))
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    lm.lily_moe_route_noalloc(s, w, None, lm.make_routing(rt), device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
+@pytest.mark.gpu
+def test_noalloc_status_is_cleared_between_calls():
+    # The scratch keeps the last call's contents, its status word included.  A
+    # call whose bounded wait runs out (test-only library variant: the router
+    # GEMM stalls for T == 77) leaves LILY_ERR_DEVICE_TIMEOUT there; the next
+    # call must start from a cleared status and report OK.  The variant is a
+    # separate library with its own scratch array, built from the same code.
+    from bit_grouped_expert_top_gb300 import _abi
+    from bit_grouped_expert_top_gb300.build import STALL_TEST_T
+    L = _abi.load_variant("stalltest")
+    cfg = CONFIGS["tiny"]
+    w = lm.make_weights(make_layer(cfg, "cuda"))
+    stream = torch.cuda.current_stream().cuda_stream
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    for T, want in ((STALL_TEST_T, -6), (STALL_TEST_T + 23, 0), (STALL_TEST_T, -6), (STALL_TEST_T + 23, 0)):
+        x = make_x(cfg, "cuda", seed_offset=T, T=T)
+        s = shape_of(cfg, T)
+        got_t = lm.alloc_routing(s)
+        rc = L.lily_moe_route_noalloc(ctypes.byref(s), ctypes.byref(w), x.data_ptr(),
+                                      ctypes.byref(lm.make_routing(got_t)), status.data_ptr(), stream)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert int(status.item()) == want, (T, int(status.item()))
+        if want == 0:
+            ref_t = lm.alloc_routing(s)
+            lm.lily_moe_route(s, w, x, lm.make_routing(ref_t), lm.alloc_workspace(s))
+            torch.cuda.synchronize()
+            for k in ("topk_idx", "counts", "offsets", "perm"):
+                np.testing.assert_array_equal(got_t[k].cpu().numpy(), ref_t[k].cpu().numpy(), err_msg=k)
