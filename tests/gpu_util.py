@@ -9,6 +9,7 @@ import torch
 
 import bit_grouped_expert_top_gb300 as lm
 import oracle
+from oracle import numpy_ref as npr
 from bit_grouped_expert_top_gb300.inputs import LayerConfig, make_layer, make_x
 from helpers import bits, layer_np
 
@@ -16,9 +17,25 @@ from helpers import bits, layer_np
 # (the rebuilt weights, x and h rounded to fp16 inside the GPU path, fp32
 # accumulation).
 OUT_TOL = 1e-2
-# Router logits: bf16 x bf16 products are exact in fp32; only the fp32
-# summation order differs from the fp64 oracle.
-LOGIT_TOL = 1e-5
+# Router logits: bf16 x bf16 products are exact in fp32; the fp32 sums are not.
+# A sum of K products, added in at most D rounded steps along any path, is off
+# from the exact value by at most D * 2^-24 * sum_k |x_k w_k| (first order).
+# D = K/8 + 64 covers the tensor core's K/16 chained MMAs (plus its adds inside
+# one MMA) and the CUDA-core GEMVs (at most 64 sequential adds per lane, then
+# the warp and block reductions); the bias add is one more rounding.
+LOGIT_TOL = 1e-5  # identical computations (two entry points over the same kernels)
+
+
+def logit_error_bound(x_bits: np.ndarray, wr_bits: np.ndarray, bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """Per-logit bound [T, E] of the fp32 accumulation error (see above)."""
+    xa = np.abs(npr.bf16_to_f64(np.asarray(x_bits)))
+    wa = np.abs(npr.bf16_to_f64(np.asarray(wr_bits)))
+    K = xa.shape[1]
+    u = 2.0 ** -24
+    b = (K // 8 + 64) * u * (xa @ wa.T)
+    if bias is not None:
+        b = b + 2 * u * np.abs(np.asarray(bias, np.float64))[None, :]
+    return b + 1e-30
 
 
 def shape_of(cfg: LayerConfig, T: Optional[int] = None):
@@ -140,9 +157,9 @@ def assert_logits_close(cfg: LayerConfig, layer: Layer, x_bits: np.ndarray, gpu_
     xs = x_bits if tokens is None else x_bits[np.asarray(tokens)]
     gl = gpu_logits if tokens is None else gpu_logits[np.asarray(tokens)]
     ref = oracle.logits(xs, layer.np["router_w"], layer.np.get("router_bias"))
-    rms = float(np.sqrt(np.mean(np.square(ref))))
-    err = float(np.max(np.abs(gl - ref)))
-    assert err <= LOGIT_TOL * max(rms, 1.0), f"logits max err {err:.3e}, rms {rms:.3e}"
+    bound = logit_error_bound(xs, layer.np["router_w"], layer.np.get("router_bias"))
+    ratio = np.abs(gl.astype(np.float64) - ref) / bound
+    assert float(ratio.max()) <= 1.0, f"logits error {float(ratio.max()):.2f} x the fp32 accumulation bound"
 
 
 def sample_tokens(T: int, n: int, seed: int = 0):
