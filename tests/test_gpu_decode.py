@@ -65,14 +65,21 @@ def test_decode_full_size_layers(T):
     _check_decode(cfg, n_layers=2, T=T)
 
 
-def test_decode_graph_replay_matches_first_run():
+def test_decode_repeat_call_is_bit_identical():
     cfg = CONFIGS["tiny"]
     layers, x, out, x_next, trace, ws, s = _run_decode(cfg, 2, 4)
     first = out.clone()
+    first_x = x_next.clone()
     out.zero_()
     lm.lily_moe_decode(s, [L.w for L in layers], x, out, ws, x_next=x_next, trace=trace)
     torch.cuda.synchronize()
-    assert torch.equal(first, out)
+    assert torch.equal(first, out) and torch.equal(first_x, x_next)
+
+
+def test_decode_more_layers_than_one_launch():
+    # 45 layers: two launches (40 + 5) continue one chain through the workspace
+    cfg = CONFIGS["tiny"]
+    _check_decode(cfg, n_layers=45, T=1)
 
 
 def test_decode_matches_prefill_on_same_tokens():
