@@ -6,5 +6,5 @@ loads nothing; the library is built / loaded on first use.
 """
 from ._abi import (LilyError, alloc_routing, alloc_workspace, lily_moe_block_capacity, lily_moe_check_shape,  # noqa: F401
                    lily_moe_clear_status, lily_moe_decode, lily_moe_device_status, lily_moe_forward,
-                   lily_moe_forward_timed, lily_moe_grouped_gemm, lily_moe_route, lily_moe_route_noalloc, lily_moe_status_string,
+                   lily_moe_forward_timed, lily_moe_grouped_gemm, lily_moe_last_error_detail, lily_moe_route, lily_moe_route_noalloc, lily_moe_status_string,
                    lily_moe_version, lily_moe_workspace_bytes, load, make_routing, make_shape, make_weights)

@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "LILY_OK", -1: "LILY_ERR_INVALID", -2: "LILY_ERR_UNSUPPORTED"
 class LilyError(RuntimeError):
     def __init__(self, fn: str, code: int):
         self.code = code
-        super().__init__(f"{fn} returned {code} ({STATUS_NAMES.get(code, '?')}: {lily_moe_status_string(code)})")
+        detail = f"; {lily_moe_last_error_detail()}" if code == -5 else ""
+        super().__init__(f"{fn} returned {code} ({STATUS_NAMES.get(code, '?')}: {lily_moe_status_string(code)}){detail}")
 
 
 class lily_moe_shape(ctypes.Structure):
@@ -61,6 +62,8 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.lily_moe_version.restype = I32
     L.lily_moe_status_string.restype = ctypes.c_char_p
     L.lily_moe_status_string.argtypes = [I32]
+    L.lily_moe_last_error_detail.restype = ctypes.c_char_p
+    L.lily_moe_last_error_detail.argtypes = []
     L.lily_moe_check_shape.argtypes = [PS]
     L.lily_moe_block_capacity.restype = I64
     L.lily_moe_block_capacity.argtypes = [PS]
@@ -193,6 +196,10 @@ def lily_moe_version() -> int:
 
 def lily_moe_status_string(code: int) -> str:
     return load().lily_moe_status_string(int(code)).decode()
+
+
+def lily_moe_last_error_detail() -> str:
+    return load().lily_moe_last_error_detail().decode()
 
 
 def lily_moe_check_shape(shape: lily_moe_shape) -> int:

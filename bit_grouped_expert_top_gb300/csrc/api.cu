@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 #include <set>
+#include <string>
 #include <tuple>
 #include <unordered_map>
 #include <vector>
@@ -440,7 +441,19 @@ lily_moe_routing internal_routing(const lily_moe_shape &s, void *ws)
     return r;
 }
 
-int to_status(cudaError_t e) { return e == cudaSuccess ? LILY_OK : LILY_ERR_LAUNCH; }
+// Text of the CUDA error behind this thread's last LILY_ERR_LAUNCH.
+thread_local std::string t_last_error;
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    t_last_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return LILY_ERR_LAUNCH;
+}
+
+int to_status(cudaError_t e, const char *what = "launch")
+{
+    return e == cudaSuccess ? LILY_OK : cuda_fail(e, what);
+}
 
 }  // namespace
 
@@ -494,6 +507,8 @@ const char *lily_moe_status_string(int status)
     }
 }
 
+const char *lily_moe_last_error_detail(void) { return t_last_error.c_str(); }
+
 int lily_moe_check_shape(const lily_moe_shape *shape) { return check_shape(shape); }
 
 int64_t lily_moe_block_capacity(const lily_moe_shape *shape)
@@ -522,7 +537,8 @@ int lily_moe_route(const lily_moe_shape *shape, const lily_moe_weights *w, const
     if (shape->T == 0) return LILY_OK;
     if ((rc = check_ptr(x))) return rc;
     float *logits = r->logits ? r->logits : at<float>(ws, prefill_layout(*shape).logits);
-    return to_status(enqueue_route(*shape, *w, x, *r, logits, ws, stream, nullptr, at<int>(ws, prefill_layout(*shape).inv)));
+    return to_status(enqueue_route(*shape, *w, x, *r, logits, ws, stream, nullptr, at<int>(ws, prefill_layout(*shape).inv)),
+                     "routing launch");
 }
 
 int lily_moe_grouped_gemm(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,
@@ -533,7 +549,7 @@ int lily_moe_grouped_gemm(const lily_moe_shape *shape, const lily_moe_weights *w
     if ((rc = check_ws(ws, ws_bytes, prefill_layout(*shape).total))) return rc;
     if (shape->T == 0) return LILY_OK;
     if ((rc = check_ptr(x)) || (rc = check_ptr(out))) return rc;
-    return to_status(enqueue_experts(*shape, *w, x, *r, out, ws, stream, nullptr, false));
+    return to_status(enqueue_experts(*shape, *w, x, *r, out, ws, stream, nullptr, false), "expert launch");
 }
 
 int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x, float *out,
@@ -547,10 +563,12 @@ int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *
     if ((rc = check_ptr(x)) || (rc = check_ptr(out))) return rc;
     const lily_moe_routing rr = r ? *r : internal_routing(*shape, ws);
     float *logits = rr.logits ? rr.logits : at<float>(ws, prefill_layout(*shape).logits);
-    if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return LILY_ERR_LAUNCH;
-    if (enqueue_route(*shape, *w, x, rr, logits, ws, stream, events, at<int>(ws, prefill_layout(*shape).inv)) != cudaSuccess)
-        return LILY_ERR_LAUNCH;
-    return to_status(enqueue_experts(*shape, *w, x, rr, out, ws, stream, events, true));
+    cudaError_t e;
+    if (events && (e = cudaEventRecord(events[0], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if ((e = enqueue_route(*shape, *w, x, rr, logits, ws, stream, events, at<int>(ws, prefill_layout(*shape).inv))) !=
+        cudaSuccess)
+        return cuda_fail(e, "routing launch");
+    return to_status(enqueue_experts(*shape, *w, x, rr, out, ws, stream, events, true), "expert launch");
 }
 
 int lily_moe_forward(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x, float *out,
@@ -601,8 +619,8 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
     a.ctrl = at<Ctrl>(ws, L.ctrl);
 
     // the exchange area starts from zero tags on every call
-    if (cudaMemsetAsync(at<uint8_t>(ws, L.abort_flag), 0, L.total - L.abort_flag, stream) != cudaSuccess)
-        return LILY_ERR_LAUNCH;
+    cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, L.abort_flag), 0, L.total - L.abort_flag, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (decode exchange area)");
     for (int l0 = 0; l0 < n_layers; l0 += kDecodeLayersPerLaunch) {
         a.layer0 = l0;
         a.n_layers = std::min(kDecodeLayersPerLaunch, n_layers - l0);
@@ -618,7 +636,7 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
             p.sh_gate_s = w.sh_gate.scale; p.sh_gate_b = w.sh_gate.bias; p.sh_up_s = w.sh_up.scale;
             p.sh_up_b = w.sh_up.bias; p.sh_down_s = w.sh_down.scale; p.sh_down_b = w.sh_down.bias;
         }
-        if (launch_decode(a, grid, stream) != cudaSuccess) return LILY_ERR_LAUNCH;
+        if ((e = launch_decode(a, grid, stream)) != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     }
     return LILY_OK;
 }
@@ -639,35 +657,40 @@ int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *
         return LILY_ERR_SCRATCH_LIMIT;
     if (shape->T == 0) {
         // nothing to route; the call's status (OK) still goes to device_status
-        if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int32_t), stream) != cudaSuccess)
-            return LILY_ERR_LAUNCH;
+        cudaError_t e;
+        if (device_status && (e = cudaMemsetAsync(device_status, 0, sizeof(int32_t), stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemsetAsync (device_status)");
         return LILY_OK;
     }
     if ((rc = check_ptr(x))) return rc;
     void *scratch = noalloc_scratch_address();
-    if (!scratch) return LILY_ERR_LAUNCH;
+    if (!scratch) return cuda_fail(cudaGetLastError(), "cudaGetSymbolAddress (fixed scratch)");
     // The scratch keeps the previous call's contents: start from a clear control block.
-    if (cudaMemsetAsync(scratch, 0, sizeof(Ctrl), stream) != cudaSuccess) return LILY_ERR_LAUNCH;
-    if (enqueue_route(*shape, *w, x, *r, r->logits, scratch, stream) != cudaSuccess) return LILY_ERR_LAUNCH;
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(scratch, 0, sizeof(Ctrl), stream)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    if ((e = enqueue_route(*shape, *w, x, *r, r->logits, scratch, stream)) != cudaSuccess)
+        return cuda_fail(e, "routing launch");
     if (device_status &&
-        cudaMemcpyAsync(device_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
-        return LILY_ERR_LAUNCH;
+        (e = cudaMemcpyAsync(device_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync (device_status)");
     return LILY_OK;
 }
 
 int lily_moe_device_status(const void *ws, cudaStream_t stream)
 {
     if (!ws) return LILY_ERR_INVALID;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return LILY_ERR_LAUNCH;
+    cudaError_t e;
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     int status = 0;
-    if (cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LILY_ERR_LAUNCH;
+    if ((e = cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy (status word)");
     return status;
 }
 
 int lily_moe_clear_status(void *ws, cudaStream_t stream)
 {
     if (!ws) return LILY_ERR_INVALID;
-    return to_status(cudaMemsetAsync(ws, 0, sizeof(int), stream));
+    return to_status(cudaMemsetAsync(ws, 0, sizeof(int), stream), "cudaMemsetAsync (status word)");
 }
 
 }  // extern "C"

@@ -18,10 +18,11 @@
 //      parameter-free RMS norm that links layers), reading the previous
 //      layer's output words from the exchange area;
 //   -  computes its one or two router rows (logit of expert c and c + G) and
-//      publishes them; computes its shared-expert gate/up rows (if any);
+//      publishes them;
 //   B  reads all 256 x T logits, selects the top 8 per token (lower index first
 //      among equal logits) and builds the list of distinct experts ("units":
-//      the shared expert is unit 0 with weight 1);
+//      the shared expert is unit 0 with weight 1); computes its shared-expert
+//      gate/up rows (if any) while the routed experts' bytes load;
 //   -  gate/up tasks (unit, 8 rows of I): tensor-core GEMV (mma.sync m16n8k16,
 //      the tokens as the 8 columns, gate rows and up rows as the two 8-row
 //      halves of the tile), SwiGLU in registers, scaled by the unit's routing
@@ -714,12 +715,8 @@ __global__ void __maxnreg__(224) decode_kernel(const __grid_constant__ DecodeArg
                 if (a.trace_logits) a.trace_logits[(static_cast<size_t>(l) * T + n) * E + e] = v;
             }
         }
-        // ---- the shared expert's gate/up rows of this CTA (no routing needed)
-        if (tid < kMaxT) S.unit_w[0][tid] = 1.0f;
-        compute_sync();
-        for_gu_tasks(P, 0, P.nu_gu, [&](int j) { gu_task(l, j, 0); });
-
         // ---- B: top-8 per token and the unit list
+        if (tid < kMaxT) S.unit_w[0][tid] = 1.0f;  // unit 0: the shared expert, weight 1
         S.umask[tid] = 0;
 #pragma unroll
         for (int n = 0; n < kMaxT; ++n) S.uw[tid][n] = 0.0f;
@@ -768,6 +765,10 @@ __global__ void __maxnreg__(224) decode_kernel(const __grid_constant__ DecodeArg
         }
         if (top8_point()) break;
         const int U = S.n_units;
+
+        // ---- the shared expert's gate/up rows of this CTA (computed while the
+        // routed experts' bytes, issued at the top-8 point, are in flight)
+        for_gu_tasks(P, 0, P.nu_gu, [&](int j) { gu_task(l, j, 0); });
 
         // ---- C: the shared expert's down rows (partial sums kept per down task),
         // routed gate/up, then per down task its routed units

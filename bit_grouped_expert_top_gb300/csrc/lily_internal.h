@@ -118,7 +118,7 @@ struct DecodeLayerPtrs {
     const uint8_t *sh_gate_q, *sh_up_q, *sh_down_q;
     const uint16_t *sh_gate_s, *sh_gate_b, *sh_up_s, *sh_up_b, *sh_down_s, *sh_down_b;
 };
-constexpr int kDecodeLayersPerLaunch = 40;  // layer table passed as a kernel parameter
+constexpr int kDecodeLayersPerLaunch = 20;  // layer table passed as a kernel parameter (<= 4 KB)
 constexpr int kDecodeMaxT = 8;
 constexpr int kDecodeMaxUnits = 8 * kDecodeMaxT + 1;  // distinct routed experts of 8 tokens + the shared one
 
@@ -141,6 +141,7 @@ struct DecodeArgs {
     Ctrl *ctrl;
     DecodeLayerPtrs L[kDecodeLayersPerLaunch];
 };
+static_assert(sizeof(DecodeArgs) <= 4096, "decode kernel parameters stay within 4 KB");
 // Ring slots that fit next to the fixed shared memory for this shape (0: the
 // shape does not fit), the bytes of one slot, and the dynamic shared memory of
 // the launch.

@@ -164,6 +164,13 @@ int lily_moe_version(void);
 /* Human-readable text of a LILY_* code (static storage, never NULL). */
 const char *lily_moe_status_string(int status);
 
+/*
+ * The CUDA error behind the last LILY_ERR_LAUNCH returned on the calling
+ * thread: which step failed and the CUDA error name and text ("" if none).
+ * Thread-local storage, valid until the thread's next failing call.
+ */
+const char *lily_moe_last_error_detail(void);
+
 /* Shape check only: LILY_OK or LILY_ERR_INVALID / LILY_ERR_UNSUPPORTED. */
 int lily_moe_check_shape(const lily_moe_shape *shape);
 
@@ -226,7 +233,7 @@ int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *
  *              for the attention / recurrent blocks between MoE layers)
  *   trace      optional per-layer routing record, or NULL
  * Enqueues one memset of the workspace's exchange area and one cooperative
- * kernel launch per 40 layers (one CTA per SM, every CTA resident; the layers
+ * kernel launch per 20 layers (one CTA per SM, every CTA resident; the layers
  * hand their data between CTAs through the workspace, without a grid-wide
  * barrier).  The result is bit-reproducible from run to run.
  */
