@@ -74,8 +74,9 @@ struct DecSmem {
     int n_units;
     int unit_e[kMaxUnits];        // expert of unit u (-1: shared)
     float unit_w[kMaxUnits][kMaxT];
-    int umask[256];
-    float uw[256][kMaxT];
+    int umask[256];               // tokens that selected expert e (bit n)
+    int sel_e[kMaxT][8];          // the top-8 of each token and their weights
+    float sel_w[kMaxT][8];
     int scan_tmp[kCW];
     float inv_rms[kMaxT];
     float rred[kCW][2][kMaxT];
@@ -87,6 +88,20 @@ struct DecSmem {
 
 __host__ __device__ constexpr size_t align128(size_t v) { return (v + 127) / 128 * 128; }
 constexpr size_t kStaticBytes = align128(sizeof(DecSmem));
+
+// Bytes of one ring slot: a gate/up task (8 rows of gate and up, K = d, with
+// scales and biases) = 9d, or one unit of a down task (16 rows, K = I) = 9I.
+__host__ __device__ inline size_t slot_bytes_of(int d, int I)
+{
+    return align128(static_cast<size_t>(9) * (d > I ? d : I));
+}
+// Staged h' of one down item: units per item (slot / 9I) x I/128 K blocks x T
+// tokens x 64 payload words of 4 bytes.
+__host__ __device__ inline size_t stage_bytes(int T, int d, int I)
+{
+    const size_t upc = slot_bytes_of(d, I) / (static_cast<size_t>(9) * I);
+    return align128(upc * (I / 128) * T * 64 * 4);
+}
 
 // ---------------------------------------------------------------- memory helpers
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -315,15 +330,17 @@ __device__ __forceinline__ void for_gu_tasks(const Plan &p, int j_lo, int j_hi, 
 }
 
 // ---------------------------------------------------------------- the kernel
-// 288 threads: at most 224 registers each, so one CTA fits the 64 K registers of an SM
-__global__ void __maxnreg__(224) decode_kernel(const __grid_constant__ DecodeArgs a)
+// 9 warps: one SM sub-partition holds 3 of them, so at most 168 registers each
+__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a)
 {
     extern __shared__ __align__(128) uint8_t dsm[];
     DecSmem &S = *reinterpret_cast<DecSmem *>(dsm);
     const int T = a.T, d = a.d, I = a.I, E = a.E;
     __nv_bfloat16 *xb = reinterpret_cast<__nv_bfloat16 *>(dsm + kStaticBytes);     // [T][d] bf16
     __half *xp = reinterpret_cast<__half *>(dsm + kStaticBytes + static_cast<size_t>(T) * d * 2);  // permuted fp16
-    uint8_t *ring = dsm + kStaticBytes + align128(static_cast<size_t>(T) * d * 4);
+    // h' of one down item's units, staged from the exchange words: [unit][K block][T][4][16] payloads
+    uint32_t *hs = reinterpret_cast<uint32_t *>(dsm + kStaticBytes + align128(static_cast<size_t>(T) * d * 4));
+    uint8_t *ring = dsm + kStaticBytes + align128(static_cast<size_t>(T) * d * 4) + stage_bytes(T, d, I);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NS = a.n_slots;
     const uint32_t SB = static_cast<uint32_t>(a.slot_bytes);
@@ -599,32 +616,33 @@ __global__ void __maxnreg__(224) decode_kernel(const __grid_constant__ DecodeArg
         rp ^= 1;
     };
 
-    // ---- down item: units [u0, u1) of one down task, accumulated into acc
+    // ---- down item: units [u0, u1) of one down task, accumulated into acc.
+    // All compute threads first poll the item's h' words into `hs` (one round of
+    // loads for the whole item), then each warp runs its (unit, K block) pairs.
     auto down_item = [&](int l, int u0, int u1, float(&acc)[4]) {
         int slot;
         const uint8_t *base = take_item(slot);
+        const int nw = (u1 - u0) * nkb_i * T * 64;  // words of the item
+        const uint64_t *hx = a.h_x + static_cast<size_t>(l & 1) * HX + static_cast<size_t>(u0) * nkb_i * T * 64;
+        const uint32_t tag = static_cast<uint32_t>(l + 1);
+        for (int w0 = tid * 4; w0 < nw; w0 += kComputeThreads * 4) {
+            uint32_t v[4];
+            if (poll_words<4>(hx + w0, tag, v, wt))
+                *reinterpret_cast<uint4 *>(hs + w0) = make_uint4(v[0], v[1], v[2], v[3]);
+        }
+        compute_sync();
         if (base) {
-            const uint64_t *hx = a.h_x + static_cast<size_t>(l & 1) * HX;
-            const uint32_t tag = static_cast<uint32_t>(l + 1);
             const int ng = I / 64;
             for (int pi = warp; pi < (u1 - u0) * nkb_i; pi += kCW) {
-                const int i = pi / nkb_i, kb = pi - i * nkb_i, u = u0 + i;
+                const int i = pi / nkb_i, kb = pi - i * nkb_i;
                 const uint8_t *ubase = base + static_cast<size_t>(i) * 9 * I;
                 const uint16_t *s = reinterpret_cast<const uint16_t *>(ubase + 8 * I);
                 const uint16_t *b = reinterpret_cast<const uint16_t *>(ubase + 8 * I + I / 2);
                 uint2 bfr[8];
-                bool ok = true;
-                if (g < T) {
-                    const uint64_t *p = hx + (((static_cast<size_t>(u) * nkb_i + kb) * T + g) * 4 + t) * 16;
-                    uint32_t v[16];
-                    ok = poll_words<16>(p, tag, v, wt);
+                const uint2 *src =
+                    g < T ? reinterpret_cast<const uint2 *>(hs + ((static_cast<size_t>(pi) * T + g) * 4 + t) * 16) : S.zeros;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) bfr[q] = make_uint2(v[2 * q], v[2 * q + 1]);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) bfr[q] = make_uint2(0u, 0u);
-                }
-                if (!__all_sync(0xffffffffu, ok)) break;
+                for (int q = 0; q < 8; ++q) bfr[q] = src[q];
                 const uint4 qg = lds128(ubase + g * (I / 2) + kb * 64 + t * 16);
                 const uint4 qg8 = lds128(ubase + (g + 8) * (I / 2) + kb * 64 + t * 16);
                 const int grp = 2 * kb + (t >> 1);
@@ -632,6 +650,7 @@ __global__ void __maxnreg__(224) decode_kernel(const __grid_constant__ DecodeArg
             }
         }
         release_item(slot, base);
+        compute_sync();  // hs is reused by the next item
     };
 
     // ---- down task k done: sum the warps' fragments, publish the rows
@@ -718,8 +737,6 @@ __global__ void __maxnreg__(224) decode_kernel(const __grid_constant__ DecodeArg
         // ---- B: top-8 per token and the unit list
         if (tid < kMaxT) S.unit_w[0][tid] = 1.0f;  // unit 0: the shared expert, weight 1
         S.umask[tid] = 0;
-#pragma unroll
-        for (int n = 0; n < kMaxT; ++n) S.uw[tid][n] = 0.0f;
         compute_sync();
         if (warp < T) {
             uint32_t v[8];
@@ -735,7 +752,8 @@ __global__ void __maxnreg__(224) decode_kernel(const __grid_constant__ DecodeArg
                     if (blockIdx.x == 0 && a.trace_idx) a.trace_idx[(static_cast<size_t>(l) * T + warp) * 8 + lane] = sel_e;
                     if (blockIdx.x == 0 && a.trace_w) a.trace_w[(static_cast<size_t>(l) * T + warp) * 8 + lane] = sel_w;
                     atomicOr(&S.umask[sel_e], 1 << warp);
-                    S.uw[sel_e][warp] = sel_w;
+                    S.sel_e[warp][lane] = sel_e;
+                    S.sel_w[warp][lane] = sel_w;
                 }
             }
         }
@@ -758,8 +776,16 @@ __global__ void __maxnreg__(224) decode_kernel(const __grid_constant__ DecodeArg
             if (used) {
                 const int u = 1 + off + incl - used;
                 S.unit_e[u] = tid;
+                const int m = S.umask[tid];
 #pragma unroll
-                for (int n = 0; n < kMaxT; ++n) S.unit_w[u][n] = S.uw[tid][n];
+                for (int n = 0; n < kMaxT; ++n) {
+                    float wv = 0.0f;
+                    if ((m >> n) & 1)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (S.sel_e[n][j] == tid) wv = S.sel_w[n][j];
+                    S.unit_w[u][n] = wv;
+                }
             }
             if (tid == 0) S.n_units = min(n_used + 1, kMaxUnits);
         }
@@ -794,11 +820,12 @@ __global__ void __maxnreg__(224) decode_kernel(const __grid_constant__ DecodeArg
 
 }  // namespace
 
-int decode_slot_bytes(int d, int I) { return static_cast<int>(align128(static_cast<size_t>(9) * std::max(d, I))); }
+int decode_slot_bytes(int d, int I) { return static_cast<int>(slot_bytes_of(d, I)); }
 
 size_t decode_smem_bytes(int T, int d, int I, int n_slots)
 {
-    return kStaticBytes + align128(static_cast<size_t>(T) * d * 4) + static_cast<size_t>(n_slots) * decode_slot_bytes(d, I);
+    return kStaticBytes + align128(static_cast<size_t>(T) * d * 4) + stage_bytes(T, d, I) +
+           static_cast<size_t>(n_slots) * decode_slot_bytes(d, I);
 }
 
 int decode_ring_slots(int T, int d, int I)
