@@ -123,14 +123,14 @@ PrefillLayout prefill_layout(const lily_moe_shape &s)
     return L;
 }
 
-// Decode: the control block, then the exchange area that every call zeroes
-// before its first launch (the global abort flag and the tagged words through
-// which the layers' CTAs hand logits, h' and outputs to each other).
+// Decode: the control block, the part every call zeroes before its first
+// launch (the global abort flag and one set of ready counters per layer), then
+// the buffers through which the CTAs hand logits, h' and outputs to each other.
 struct DecodeLayout {
-    size_t ctrl, abort_flag, logits_x, h_x, out_x, total;
+    size_t ctrl, abort_flag, ready, ready_end, logits_x, h_x, out_x, total;
 };
 
-DecodeLayout decode_layout(const lily_moe_shape &s)
+DecodeLayout decode_layout(const lily_moe_shape &s, int64_t n_layers)
 {
     DecodeLayout L{};
     const int64_t T = s.T;
@@ -142,9 +142,11 @@ DecodeLayout decode_layout(const lily_moe_shape &s)
     };
     L.ctrl = take(sizeof(Ctrl));
     L.abort_flag = take(4);
-    L.logits_x = take(2 * T * s.E * 8);
-    L.h_x = take(2 * static_cast<int64_t>(kDecodeMaxUnits) * (s.I / 128) * T * 64 * 8);
-    L.out_x = take(2 * T * s.d * 8);
+    L.ready = take(std::max<int64_t>(n_layers, 1) * kDecodeReadySlots * 4);
+    L.ready_end = off;
+    L.logits_x = take(2 * T * s.E * 4);
+    L.h_x = take(2 * static_cast<int64_t>(kDecodeMaxUnits) * (s.I / 128) * T * 64 * 4);
+    L.out_x = take(2 * T * s.d * 4);
     L.total = off;
     return L;
 }
@@ -523,7 +525,7 @@ size_t lily_moe_workspace_bytes(const lily_moe_shape *shape, int32_t n_layers_de
     size_t need = prefill_layout(*shape).total;
     if (n_layers_decode > 0) {
         if (!decode_shape_ok(*shape)) return 0;
-        need = std::max(need, decode_layout(*shape).total);
+        need = std::max(need, decode_layout(*shape, n_layers_decode).total);
     }
     return need;
 }
@@ -587,7 +589,7 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
     if (!decode_shape_ok(*shape)) return LILY_ERR_UNSUPPORTED;
     for (int l = 0; l < n_layers; ++l)
         if ((rc = check_weights(&layers[l]))) return rc;
-    if ((rc = check_ws(ws, ws_bytes, decode_layout(*shape).total))) return rc;
+    if ((rc = check_ws(ws, ws_bytes, decode_layout(*shape, n_layers).total))) return rc;
     if ((rc = check_ptr(x)) || (rc = check_ptr(out))) return rc;
     if (x_next && !aligned16(x_next)) return LILY_ERR_MISALIGNED;
     if (trace && ((trace->logits && !aligned16(trace->logits)) || (trace->topk_idx && !aligned16(trace->topk_idx)) ||
@@ -595,7 +597,7 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
         return LILY_ERR_MISALIGNED;
 
     const lily_moe_shape s = *shape;
-    const DecodeLayout L = decode_layout(s);
+    const DecodeLayout L = decode_layout(s, n_layers);
     // one CTA per SM; every CTA owns at most two router rows and two down tasks
     const int grid = num_sms_current();
     if (grid * 2 < s.E || grid * 2 * 16 < s.d) return LILY_ERR_UNSUPPORTED;
@@ -612,15 +614,16 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
         a.trace_idx = trace->topk_idx;
         a.trace_w = trace->topk_w;
     }
-    a.logits_x = at<uint64_t>(ws, L.logits_x);
-    a.h_x = at<uint64_t>(ws, L.h_x);
-    a.out_x = at<uint64_t>(ws, L.out_x);
+    a.logits_x = at<float>(ws, L.logits_x);
+    a.h_x = at<uint32_t>(ws, L.h_x);
+    a.out_x = at<float>(ws, L.out_x);
+    a.ready = at<unsigned int>(ws, L.ready);
     a.abort_flag = at<int>(ws, L.abort_flag);
     a.ctrl = at<Ctrl>(ws, L.ctrl);
 
-    // the exchange area starts from zero tags on every call
-    cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, L.abort_flag), 0, L.total - L.abort_flag, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (decode exchange area)");
+    // every call starts with a lowered abort flag and zero ready counters
+    cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, L.abort_flag), 0, L.ready_end - L.abort_flag, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (decode ready counters)");
     for (int l0 = 0; l0 < n_layers; l0 += kDecodeLayersPerLaunch) {
         a.layer0 = l0;
         a.n_layers = std::min(kDecodeLayersPerLaunch, n_layers - l0);

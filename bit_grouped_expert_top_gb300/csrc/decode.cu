@@ -29,11 +29,14 @@
 //      weight, published as fp16 h';
 //   C  down tasks (16 output rows): the sum over all units of Wd_u h'_u in one
 //      fragment (deterministic), published as the layer output.
-// Data moves between CTAs as 64-bit words {payload, tag = layer + 1} written
-// and read with relaxed gpu-scope accesses: a reader polls the words it needs
-// until every tag is current, so each hand-off costs one write-to-read trip
-// through L2 and no grid-wide barrier.  The exchange buffers are double
-// buffered by layer parity and zeroed at the start of every call.
+// Data moves between CTAs through workspace buffers (double buffered by layer
+// parity) and per-layer ready counters: a writer stores its part, then one
+// thread adds 1 to the counter with release semantics; one thread of each
+// reading CTA polls that one counter with acquire loads until every writer has
+// signalled, and the CTA then reads the data from L2.  No grid-wide barrier is
+// involved, and the polling touches one word per CTA (polling the data itself,
+// with every CTA spinning on the same lines, queued up at the L2 slices).  The
+// counters are per layer and zeroed at the start of every call.
 //
 // The producer warp streams every weight a CTA needs through a ring of
 // shared-memory slots with cp.async.bulk (TMA bulk copies).  Items that do not
@@ -112,17 +115,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
-// Tagged exchange words: payload in the low half, tag in the high half; one
-// aligned 64-bit access, so a reader sees payload and tag of the same write.
-__device__ __forceinline__ void st_tag(uint64_t *p, uint32_t payload, uint32_t tag)
+// Ready counters: release add by the writer, acquire load by the reader.
+__device__ __forceinline__ void signal_ready(unsigned int *p)
 {
-    const uint64_t v = (static_cast<uint64_t>(tag) << 32) | payload;
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
 }
-__device__ __forceinline__ uint64_t ld_tag(const uint64_t *p)
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int *p)
 {
-    uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 __device__ __forceinline__ int ld_flag(const int *p)
@@ -148,29 +149,14 @@ __device__ __forceinline__ void raise_abort(const Waiter &w)
     st_flag(w.g_abort, 1);
 }
 
-// Polls N consecutive tagged words until every tag equals `tag`; payloads to v.
-template <int N>
-__device__ __forceinline__ bool poll_words(const uint64_t *p, uint32_t tag, uint32_t (&v)[N], const Waiter &w)
+// Waits (one thread) until the counter reaches `target`; bounded, gives up on
+// an abort raised in this CTA or by another one.
+__device__ __forceinline__ bool wait_ready(const unsigned int *p, unsigned int target, const Waiter &w)
 {
-    static_assert(N <= 31, "pending mask");
-    uint32_t pending = (1u << N) - 1u;
     uint64_t t0 = 0;
 #pragma unroll 1
     for (int iter = 0;; ++iter) {
-        // all loads of a round are issued before any tag is checked
-        const uint32_t todo = pending;
-        uint64_t x[N];
-#pragma unroll
-        for (int i = 0; i < N; ++i)
-            if (todo & (1u << i)) x[i] = ld_tag(p + i);
-#pragma unroll
-        for (int i = 0; i < N; ++i) {
-            if ((todo & (1u << i)) && static_cast<uint32_t>(x[i] >> 32) == tag) {
-                v[i] = static_cast<uint32_t>(x[i]);
-                pending &= ~(1u << i);
-            }
-        }
-        if (pending == 0) return true;
+        if (ld_acquire(p) >= target) return true;
         if (*w.s_abort) return false;
         if ((iter & 15) == 15 && ld_flag(w.g_abort)) {
             *w.s_abort = 1;
@@ -471,6 +457,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     int rp = 0;        // red buffer parity
     const size_t TD = static_cast<size_t>(T) * d;
     const size_t HX = static_cast<size_t>(kMaxUnits) * nkb_i * T * 64;  // words of one h' buffer
+    auto ready_of = [&](int l) { return a.ready + static_cast<size_t>(l) * kDecodeReadySlots; };
 
     // Waits for the next item; returns its slot base (nullptr: giving up).  The
     // result is uniform within each warp.
@@ -500,18 +487,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                 *reinterpret_cast<uint4 *>(xp + perm_b_offset(k0, n, T)) = bf16x8_to_perm_f16(v, inf);
             }
         } else {
-            const uint64_t *src = a.out_x + static_cast<size_t>((l - 1) & 1) * TD;
-            const uint32_t tag = static_cast<uint32_t>(l);  // tag of layer l - 1
+            const float *src = a.out_x + static_cast<size_t>((l - 1) & 1) * TD;
+            if (tid == 0) wait_ready(ready_of(l - 1) + 1, static_cast<unsigned int>(P.n_down), wt);
+            compute_sync();
 #pragma unroll
             for (int n = 0; n < kMaxT; ++n) {
                 if (n < T) {
                     float ss = 0.0f;
                     for (int k0 = tid * 8; k0 < d; k0 += kComputeThreads * 8) {
-                        uint32_t v[8];
-                        if (poll_words<8>(src + static_cast<size_t>(n) * d + k0, tag, v, wt)) {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) ss = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss);
-                        }
+                        const float4 *p = reinterpret_cast<const float4 *>(src + static_cast<size_t>(n) * d + k0);
+                        const float4 v0 = __ldcg(p), v1 = __ldcg(p + 1);
+                        ss = fmaf(v0.x, v0.x, fmaf(v0.y, v0.y, fmaf(v0.z, v0.z, fmaf(v0.w, v0.w, ss))));
+                        ss = fmaf(v1.x, v1.x, fmaf(v1.y, v1.y, fmaf(v1.z, v1.z, fmaf(v1.w, v1.w, ss))));
                     }
                     ss = warp_sum(ss);
                     if (lane == 0) S.sred[warp][n] = ss;
@@ -527,16 +514,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
             for (int q = tid; q < T * (d / 8); q += kComputeThreads) {
                 const int n = q / (d / 8), k0 = (q - n * (d / 8)) * 8;
                 const float r = S.inv_rms[n];
-                const uint64_t *p = src + static_cast<size_t>(n) * d + k0;
-                uint32_t o[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float v0 = __uint_as_float(static_cast<uint32_t>(ld_tag(p + 2 * j)));
-                    const float v1 = __uint_as_float(static_cast<uint32_t>(ld_tag(p + 2 * j + 1)));
-                    const __nv_bfloat162 bv = __floats2bfloat162_rn(v0 * r, v1 * r);
-                    o[j] = *reinterpret_cast<const uint32_t *>(&bv);
-                }
-                const uint4 v = make_uint4(o[0], o[1], o[2], o[3]);
+                const float4 *p = reinterpret_cast<const float4 *>(src + static_cast<size_t>(n) * d + k0);
+                const float4 v0 = __ldcg(p), v1 = __ldcg(p + 1);
+                const __nv_bfloat162 b0 = __floats2bfloat162_rn(v0.x * r, v0.y * r), b1 = __floats2bfloat162_rn(v0.z * r, v0.w * r);
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(v1.x * r, v1.y * r), b3 = __floats2bfloat162_rn(v1.z * r, v1.w * r);
+                const uint4 v = make_uint4(*reinterpret_cast<const uint32_t *>(&b0), *reinterpret_cast<const uint32_t *>(&b1),
+                                           *reinterpret_cast<const uint32_t *>(&b2), *reinterpret_cast<const uint32_t *>(&b3));
                 if (blockIdx.x == 0 && a.x_next)
                     *reinterpret_cast<uint4 *>(a.x_next + static_cast<size_t>(l - 1) * TD + static_cast<size_t>(n) * d + k0) = v;
                 if (!export_only) {
@@ -601,35 +584,35 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                 const int i0 = (j % P.nu_gu) * kGURows;
                 const int kbI = i0 >> 7, r0 = i0 & 127, t4 = r0 >> 5, w8 = (r0 >> 3) & 3;
                 const int s = 2 * w8 + (g & 1), pw = g >> 2;
-                const uint32_t tag = static_cast<uint32_t>(l + 1);
-                uint64_t *hx = a.h_x + static_cast<size_t>(l & 1) * HX;
+                uint32_t *hx = a.h_x + static_cast<size_t>(l & 1) * HX;
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
                     const int n = 2 * t + m;
                     if (n < T) {
                         const size_t idx = ((((static_cast<size_t>(u) * nkb_i + kbI) * T + n) * 4 + t4) * 8 + s) * 2 + pw;
-                        st_tag(hx + idx, hh[m] | ((m ? ph1 : ph0) << 16), tag);
+                        hx[idx] = hh[m] | ((m ? ph1 : ph0) << 16);
                     }
                 }
             }
+            __syncwarp();
+            if (lane == 0) signal_ready(ready_of(l) + 2 + u);
         }
         rp ^= 1;
     };
 
     // ---- down item: units [u0, u1) of one down task, accumulated into acc.
-    // All compute threads first poll the item's h' words into `hs` (one round of
-    // loads for the whole item), then each warp runs its (unit, K block) pairs.
+    // Once the item's units are ready, all compute threads copy its h' words
+    // into `hs`, then each warp runs its (unit, K block) pairs.
     auto down_item = [&](int l, int u0, int u1, float(&acc)[4]) {
         int slot;
         const uint8_t *base = take_item(slot);
         const int nw = (u1 - u0) * nkb_i * T * 64;  // words of the item
-        const uint64_t *hx = a.h_x + static_cast<size_t>(l & 1) * HX + static_cast<size_t>(u0) * nkb_i * T * 64;
-        const uint32_t tag = static_cast<uint32_t>(l + 1);
-        for (int w0 = tid * 4; w0 < nw; w0 += kComputeThreads * 4) {
-            uint32_t v[4];
-            if (poll_words<4>(hx + w0, tag, v, wt))
-                *reinterpret_cast<uint4 *>(hs + w0) = make_uint4(v[0], v[1], v[2], v[3]);
-        }
+        const uint32_t *hx = a.h_x + static_cast<size_t>(l & 1) * HX + static_cast<size_t>(u0) * nkb_i * T * 64;
+        if (tid == 0)
+            for (int u = u0; u < u1; ++u) wait_ready(ready_of(l) + 2 + u, static_cast<unsigned int>(P.nu_gu), wt);
+        compute_sync();
+        for (int w0 = tid * 4; w0 < nw; w0 += kComputeThreads * 4)
+            *reinterpret_cast<uint4 *>(hs + w0) = __ldcg(reinterpret_cast<const uint4 *>(hx + w0));
         compute_sync();
         if (base) {
             const int ng = I / 64;
@@ -665,17 +648,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
 #pragma unroll
                 for (int q = 0; q < 4; ++q) D[q] += S.red[rp][w][lane][q];
             const int j0 = (P.c + k * P.G) * kDownRows;
-            const uint32_t tag = static_cast<uint32_t>(l + 1);
-            uint64_t *ox = a.out_x + static_cast<size_t>(l & 1) * TD;
+            float *ox = a.out_x + static_cast<size_t>(l & 1) * TD;
             float *out = a.out + static_cast<size_t>(l) * TD;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int n = 2 * t + (q & 1), j = j0 + g + 8 * (q >> 1);
                 if (n < T) {
                     out[static_cast<size_t>(n) * d + j] = D[q];
-                    st_tag(ox + static_cast<size_t>(n) * d + j, __float_as_uint(D[q]), tag);
+                    ox[static_cast<size_t>(n) * d + j] = D[q];
                 }
             }
+            __syncwarp();
+            if (lane == 0) signal_ready(ready_of(l) + 1);
         }
         rp ^= 1;
     };
@@ -683,7 +667,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     for (int li = 0; li < a.n_layers; ++li) {
         const int l = a.layer0 + li;
         const DecodeLayerPtrs &W = a.L[li];
-        const uint32_t tag = static_cast<uint32_t>(l + 1);
 
         // ---- A: input, router rows
         build_input(l, false);
@@ -713,38 +696,42 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int n = 0; n < kMaxT; ++n) {
-                    const float v = warp_sum(part[r][n]);
-                    if (lane == 0) S.rred[warp][r][n] = v;
-                }
+                for (int n = 0; n < kMaxT; ++n)
+                    if (r < P.n_rrows && n < T) {
+                        const float v = warp_sum(part[r][n]);
+                        if (lane == 0) S.rred[warp][r][n] = v;
+                    }
             compute_sync();
-            if (tid < P.n_rrows * T && base) {
-                const int r = tid / T, n = tid - r * T, e = P.c + r * P.G;
-                float v = 0.0f;
-                for (int w = 0; w < kCW; ++w) v += S.rred[w][r][n];
-                if (W.router_bias) v += W.router_bias[e];
+            if (warp == 0) {
+                if (tid < P.n_rrows * T && base) {
+                    const int r = tid / T, n = tid - r * T, e = P.c + r * P.G;
+                    float v = 0.0f;
+                    for (int w = 0; w < kCW; ++w) v += S.rred[w][r][n];
+                    if (W.router_bias) v += W.router_bias[e];
+                    a.logits_x[(static_cast<size_t>(l & 1) * T + n) * E + e] = v;
+                    if (a.trace_logits) a.trace_logits[(static_cast<size_t>(l) * T + n) * E + e] = v;
+                }
+                __syncwarp();
 #ifdef LILY_TEST_STALL_DECODE_LAYERS
                 // Test builds only: in a call of exactly this many layers, CTA 0
-                // never publishes its logits of layer 3, so every CTA's bounded
-                // wait for them runs out and the abort path executes.
+                // never signals its logits of layer 3, so every CTA's bounded wait
+                // for them runs out and the abort path executes.
                 if (!(a.last_launch && a.layer0 + a.n_layers == LILY_TEST_STALL_DECODE_LAYERS && l == 3 &&
                       blockIdx.x == 0))
 #endif
-                st_tag(a.logits_x + (static_cast<size_t>(l & 1) * T + n) * E + e, __float_as_uint(v), tag);
-                if (a.trace_logits) a.trace_logits[(static_cast<size_t>(l) * T + n) * E + e] = v;
+                    if (lane == 0) signal_ready(ready_of(l));
             }
         }
         // ---- B: top-8 per token and the unit list
         if (tid < kMaxT) S.unit_w[0][tid] = 1.0f;  // unit 0: the shared expert, weight 1
         S.umask[tid] = 0;
+        if (tid == 0) wait_ready(ready_of(l), static_cast<unsigned int>(P.G), wt);
         compute_sync();
         if (warp < T) {
-            uint32_t v[8];
-            const bool ok = poll_words<8>(a.logits_x + (static_cast<size_t>(l & 1) * T + warp) * E + lane * 8, tag, v, wt);
-            if (__all_sync(0xffffffffu, ok)) {
-                float lv[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) lv[i] = __uint_as_float(v[i]);
+            {
+                const float4 *p = reinterpret_cast<const float4 *>(a.logits_x + (static_cast<size_t>(l & 1) * T + warp) * E + lane * 8);
+                const float4 l0 = __ldcg(p), l1 = __ldcg(p + 1);
+                const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
                 int sel_e;
                 float sel_w;
                 warp_top8_keys(lv, lane, sel_e, sel_w);

@@ -121,6 +121,9 @@ struct DecodeLayerPtrs {
 constexpr int kDecodeLayersPerLaunch = 20;  // layer table passed as a kernel parameter (<= 4 KB)
 constexpr int kDecodeMaxT = 8;
 constexpr int kDecodeMaxUnits = 8 * kDecodeMaxT + 1;  // distinct routed experts of 8 tokens + the shared one
+// Ready counters of one layer: [0] CTAs whose router rows are written, [1] down
+// tasks whose output rows are written, [2 + u] gate/up tasks of unit u written.
+constexpr int kDecodeReadySlots = 2 + kDecodeMaxUnits;
 
 struct DecodeArgs {
     int T, d, E, top_k, I;
@@ -133,10 +136,12 @@ struct DecodeArgs {
     float *trace_logits;    // [total layers][T][E] or NULL
     int *trace_idx;         // [total layers][T][top_k] or NULL
     float *trace_w;         // [total layers][T][top_k] or NULL
-    // exchange area in the workspace (zeroed before the first launch of a call)
-    uint64_t *logits_x;     // [2][T][E] tagged logits
-    uint64_t *h_x;          // [2][kDecodeMaxUnits][I/128][T][4][16] tagged h' pairs
-    uint64_t *out_x;        // [2][T][d] tagged outputs
+    // exchange area in the workspace: data double buffered by layer parity,
+    // per-layer ready counters (zeroed before the first launch of a call)
+    float *logits_x;        // [2][T][E] router logits
+    uint32_t *h_x;          // [2][kDecodeMaxUnits][I/128][T][4][16] h' pairs in the down projection's B layout
+    float *out_x;           // [2][T][d] layer outputs
+    unsigned int *ready;    // [layers of the call][kDecodeReadySlots]
     int *abort_flag;        // raised by the CTA whose wait ran out; the others give up too
     Ctrl *ctrl;
     DecodeLayerPtrs L[kDecodeLayersPerLaunch];

@@ -78,7 +78,8 @@ def test_noalloc_matches_workspace_route_on_two_calls_in_a_row():
 def test_noalloc_t0_writes_ok_status():
     # no tokens: nothing runs, but the call's status (OK) still reaches device_status
     cfg = CONFIGS["tiny"]
-    w = lm.make_weights(make_layer(cfg, "cuda"))
+    layer = make_layer(cfg, "cuda")  # the weight tensors must outlive the call
+    w = lm.make_weights(layer)
     s = shape_of(cfg, 0)
     rt = lm.alloc_routing(lm.make_shape(T=1, d=cfg.d, I=cfg.I))
     status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
@@ -98,7 +99,8 @@ def test_noalloc_status_is_cleared_between_calls():
     from bit_grouped_expert_top_gb300.build import STALL_TEST_T
     L = _abi.load_variant("stalltest")
     cfg = CONFIGS["tiny"]
-    w = lm.make_weights(make_layer(cfg, "cuda"))
+    layer = make_layer(cfg, "cuda")  # the weight tensors must outlive the calls
+    w = lm.make_weights(layer)
     stream = torch.cuda.current_stream().cuda_stream
     status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
     for T, want in ((STALL_TEST_T, -6), (STALL_TEST_T + 23, 0), (STALL_TEST_T, -6), (STALL_TEST_T + 23, 0)):
