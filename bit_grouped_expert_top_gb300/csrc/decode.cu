@@ -40,10 +40,10 @@
 //
 // The producer warp streams every weight a CTA needs through a ring of
 // shared-memory slots with cp.async.bulk (TMA bulk copies).  Items that do not
-// depend on the routing (the router rows, the shared expert's gate/up rows and
-// its part of the down rows) of layer l + 1 are issued as soon as the slots of
-// layer l free up, so they load while layer l finishes; the routed experts'
-// bytes are issued the moment the top-8 is known.
+// depend on the routing (the router rows and the shared expert's gate/up rows)
+// of layer l + 1 are issued as soon as the slots of layer l free up, so they
+// load while layer l finishes; the routed experts' gate/up rows and then the
+// down rows of all units are issued the moment the top-8 is known.
 //
 // Every wait (mbarrier or polled word) is bounded; a wait that runs out records
 // LILY_ERR_DEVICE_TIMEOUT, raises a global abort flag that the other CTAs see,
@@ -86,7 +86,6 @@ struct DecSmem {
     float sred[kCW][kMaxT];
     uint2 zeros[8];
     float red[2][kCW][32][4];     // cross-warp sums of mma fragments, double buffered
-    float sacc[2][kCW][32][4];    // per-warp partial sums of the shared expert's down rows, per down task
 };
 
 __host__ __device__ constexpr size_t align128(size_t v) { return (v + 127) / 128 * 128; }
@@ -433,13 +432,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                              W.router_w + static_cast<size_t>(P.c + lane * P.G) * d, 2u * d, &S.full[slot]);
             }
             for_gu_tasks(P, 0, P.nu_gu, [&](int j) { issue_gu(W, j, -1); });
-            for (int k = 0; k < P.n_mydown; ++k) issue_down(W, k, 0, 1);
             if (top8_point()) break;
-            // ---- routed experts of this layer (the unit list is in shared memory)
+            // ---- routed experts of this layer (the unit list is in shared memory),
+            // then the down rows of every unit (the shared expert's first)
             const int U = S.n_units;
             for_gu_tasks(P, P.nu_gu, U * P.nu_gu, [&](int j) { issue_gu(W, j, S.unit_e[j / P.nu_gu]); });
             for (int k = 0; k < P.n_mydown; ++k)
-                for (int u0 = 1; u0 < U; u0 += P.upc) issue_down(W, k, u0, min(U, u0 + P.upc));
+                for (int u0 = 0; u0 < U; u0 += P.upc) issue_down(W, k, u0, min(U, u0 + P.upc));
         }
         // no copy into this CTA's shared memory may still be in flight at exit
         if (lane == 0) {
@@ -783,20 +782,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         // routed experts' bytes, issued at the top-8 point, are in flight)
         for_gu_tasks(P, 0, P.nu_gu, [&](int j) { gu_task(l, j, 0); });
 
-        // ---- C: the shared expert's down rows (partial sums kept per down task),
-        // routed gate/up, then per down task its routed units
-        for (int k = 0; k < P.n_mydown; ++k) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            down_item(l, 0, 1, acc);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) S.sacc[k][warp][lane][q] = acc[q];
-        }
+        // ---- C: routed gate/up, then per down task the down rows of every unit
         for_gu_tasks(P, P.nu_gu, U * P.nu_gu, [&](int j) { gu_task(l, j, j / P.nu_gu); });
         for (int k = 0; k < P.n_mydown; ++k) {
-            float acc[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[q] = S.sacc[k][warp][lane][q];
-            for (int u0 = 1; u0 < U; u0 += P.upc) down_item(l, u0, min(U, u0 + P.upc), acc);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int u0 = 0; u0 < U; u0 += P.upc) down_item(l, u0, min(U, u0 + P.upc), acc);
             finish_down(l, k, acc);
         }
     }
