@@ -12,7 +12,7 @@
 // resident kernel instead of kernel boundaries.
 //
 // GB300 design.  One CTA per SM (a cooperative launch, so every CTA is
-// resident), 8 compute warps and 1 producer warp.  Per layer l, every CTA:
+// resident), 8 warps.  Per layer l, every CTA:
 //   A  builds the layer input x_l in shared memory (layer 0: x; later layers:
 //      bf16 of the previous output over sqrt(mean(out^2) + 1e-6), the
 //      parameter-free RMS norm that links layers), reading the previous
@@ -38,17 +38,22 @@
 // with every CTA spinning on the same lines, queued up at the L2 slices).  The
 // counters are per layer and zeroed at the start of every call.
 //
-// The producer warp streams every weight a CTA needs through a ring of
-// shared-memory slots with cp.async.bulk (TMA bulk copies).  Items that do not
-// depend on the routing (the router rows and the shared expert's gate/up rows)
-// of layer l + 1 are issued as soon as the slots of layer l free up, so they
-// load while layer l finishes; the routed experts' gate/up rows and then the
-// down rows of all units are issued the moment the top-8 is known.
+// Every weight a CTA needs streams through a ring of shared-memory slots: all
+// 256 threads copy 16-byte pieces of an item with cp.async and arrive on the
+// slot's mbarrier when their pieces have landed.  (One SM's TMA unit takes
+// 30-50 ns to start each bulk copy whatever its size, so the ~60 copies of a
+// layer's rows and scale/bias arrays, issued by one thread, kept the bytes of
+// the last items waiting; the load/store units have no such cost per copy.)
+// Items that do not depend on the routing (the router rows and the shared
+// expert's gate/up rows) of layer l + 1 are issued as soon as the slots of
+// layer l free up, so they load while layer l finishes; the routed experts'
+// gate/up rows and then the down rows of all units are issued the moment the
+// top-8 is known.
 //
-// Every wait (mbarrier or polled word) is bounded; a wait that runs out records
-// LILY_ERR_DEVICE_TIMEOUT, raises a global abort flag that the other CTAs see,
-// and every CTA leaves its layer loop at the next top-8 point after waiting for
-// its own copies in flight.
+// Every wait (mbarrier or ready counter) is bounded; a wait that runs out
+// records LILY_ERR_DEVICE_TIMEOUT, raises a global abort flag that the other
+// CTAs see, and every CTA leaves its layer loop at the next top-8 point and
+// waits for its own copies in flight before it exits.
 #include <algorithm>
 
 #include "lily_device.cuh"
@@ -59,19 +64,18 @@ namespace {
 
 constexpr int kMaxT = kDecodeMaxT;
 constexpr int kMaxUnits = kDecodeMaxUnits;
-constexpr int kCW = 8;                        // compute warps
-constexpr int kDecThreads = (kCW + 1) * 32;   // + the producer warp
-constexpr int kProdWarp = kCW;
-constexpr int kComputeThreads = kCW * 32;
+constexpr int kCW = 8;                        // warps
+constexpr int kDecThreads = kCW * 32;
+constexpr int kComputeThreads = kDecThreads;
 constexpr int kKB = 128;                      // K block of one lane pass (16 bytes of int4 per row)
 constexpr int kGURows = 8;                    // I rows of one gate/up task
 constexpr int kDownRows = 16;                 // output rows of one down task
 constexpr int kMaxSlots = 16;
 constexpr int kSmemLimit = 232448;            // 227 KB of dynamic shared memory per CTA
-constexpr int kBarTop8 = 1, kBarCompute = 2;  // named barriers (0 is __syncthreads)
+constexpr int kBarCompute = 1;                // named barrier of the CTA (0 is __syncthreads)
 
 struct DecSmem {
-    uint64_t full[kMaxSlots], empty[kMaxSlots];
+    uint64_t full[kMaxSlots];     // ring slot filled (one arrival per thread)
     int abort;                    // this CTA gives up (set by any failed wait)
     int decide;                   // the abort decision taken at the top-8 point
     int n_units;
@@ -106,13 +110,6 @@ __host__ __device__ inline size_t stage_bytes(int T, int d, int I)
 }
 
 // ---------------------------------------------------------------- memory helpers
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
 
 // Ready counters: release add by the writer, acquire load by the reader.
 __device__ __forceinline__ void signal_ready(unsigned int *p)
@@ -172,26 +169,13 @@ __device__ __forceinline__ bool wait_ready(const unsigned int *p, unsigned int t
     }
 }
 
-// mbarrier wait of a compute or producer thread (bounded; a failure also
+// mbarrier wait (bounded; a failure also
 // raises the global abort flag).
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, const Waiter &w)
 {
     if (mbar_wait(bar, parity, w.s_abort, w.status)) return true;
     raise_abort(w);
     return false;
-}
-
-// Waits on the exit path (bounded, ignores the abort flag).
-__device__ __forceinline__ void drain_bar(uint64_t *bar, uint32_t parity, int *status)
-{
-    const uint32_t addr = smem_u32(bar);
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(addr, parity)) {
-        if (global_timer_ns() - t0 > LILY_DRAIN_LIMIT_NS) {
-            record_error(status, kErrDeviceTimeout);
-            return;
-        }
-    }
 }
 
 __device__ __forceinline__ uint4 lds128(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
@@ -315,7 +299,6 @@ __device__ __forceinline__ void for_gu_tasks(const Plan &p, int j_lo, int j_hi, 
 }
 
 // ---------------------------------------------------------------- the kernel
-// 9 warps: one SM sub-partition holds 3 of them, so at most 168 registers each
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a)
 {
     extern __shared__ __align__(128) uint8_t dsm[];
@@ -323,10 +306,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     const int T = a.T, d = a.d, I = a.I, E = a.E;
     __nv_bfloat16 *xb = reinterpret_cast<__nv_bfloat16 *>(dsm + kStaticBytes);     // [T][d] bf16
     __half *xp = reinterpret_cast<__half *>(dsm + kStaticBytes + static_cast<size_t>(T) * d * 2);  // permuted fp16
-    // h' of one down item's units, staged from the exchange words: [unit][K block][T][4][16] payloads
+    // h' of one down item's units, staged from the exchange buffer: [unit][K block][T][4][16] words
     uint32_t *hs = reinterpret_cast<uint32_t *>(dsm + kStaticBytes + align128(static_cast<size_t>(T) * d * 4));
     uint8_t *ring = dsm + kStaticBytes + align128(static_cast<size_t>(T) * d * 4) + stage_bytes(T, d, I);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x;  // 0..255
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
     const int NS = a.n_slots;
     const uint32_t SB = static_cast<uint32_t>(a.slot_bytes);
     const Waiter wt{&S.abort, a.abort_flag, &a.ctrl->status};
@@ -341,118 +326,122 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     P.n_rrows = (P.c < E) + (P.c + P.G < E);
     const int nkb_d = d / kKB, nkb_i = I / kKB;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&S.full[s], 1);
-            mbar_init(&S.empty[s], kCW);
-        }
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], kDecThreads);  // one arrival per thread and item
         S.abort = 0;
         S.decide = 0;
         S.unit_e[0] = -1;  // unit 0 is always the shared expert
         fence_mbar_init();
     }
-    if (threadIdx.x < 8) S.zeros[threadIdx.x] = make_uint2(0u, 0u);
+    if (tid < 8) S.zeros[tid] = make_uint2(0u, 0u);
     __syncthreads();
 
-    // Abort decision at the top-8 point of every layer, the same for all warps:
-    // one thread reads the flag between two barriers of the whole CTA.
-    auto top8_point = [&]() -> bool {
-        named_barrier_sync(kBarTop8, kDecThreads);
-        if (threadIdx.x == 0) S.decide = *reinterpret_cast<volatile int *>(&S.abort);
-        named_barrier_sync(kBarTop8, kDecThreads);
-        return *reinterpret_cast<volatile int *>(&S.decide) != 0;
+    // ---------------------------------------------------------------- the ring
+    // Items, in the order they are issued and consumed, per layer li:
+    //   stage 0  the router rows of this CTA
+    //   stage 1  the shared expert's gate/up tasks of this CTA
+    //   stage 2  the routed gate/up tasks of this CTA       (after the top-8 of li)
+    //   stage 3  per down task, chunks of units [u0, u0 + upc) (after the top-8 of li)
+    // Every thread copies its 16-byte pieces of an item with cp.async and then
+    // arrives (noinc) on the item's full barrier, which completes once all
+    // copies of all threads have landed.  Item n goes to slot n % NS; it is
+    // issued only once item n - NS has been consumed by every thread.
+    uint32_t iss = 0, done = 0;       // items issued / consumed (all threads)
+    int q_li = 0, q_stage = 0, q_pos = 0, q_k = 0;  // cursor of the next item to issue
+    int units_li = -1;                // layer whose unit list is in shared memory
+
+    // pieces of one item: copies [first piece, +n) of `bytes`-byte segment
+    auto copy_seg = [&](uint8_t *dst, const void *src, uint32_t bytes) {
+        for (uint32_t o = static_cast<uint32_t>(tid) * 16u; o < bytes; o += kDecThreads * 16u)
+            cp_async_16(dst + o, static_cast<const uint8_t *>(src) + o);
+    };
+    auto finish_issue = [&](int slot) {
+        cp_async_mbar_arrive_noinc(&S.full[slot]);
+        ++iss;
+    };
+    // gate/up task j of expert e (e < 0: the shared expert)
+    auto issue_gu = [&](const DecodeLayerPtrs &W, int j, int e) {
+        const int slot = static_cast<int>(iss % NS);
+        uint8_t *base = ring + static_cast<size_t>(slot) * SB;
+        const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * I) + static_cast<size_t>(j % P.nu_gu) * kGURows;
+        const size_t ng = d / 64;
+        copy_seg(base, (e < 0 ? W.sh_gate_q : W.gate_q) + r0 * (d / 2), 4u * d);
+        copy_seg(base + 4 * d, (e < 0 ? W.sh_up_q : W.up_q) + r0 * (d / 2), 4u * d);
+        copy_seg(base + 8 * d, (e < 0 ? W.sh_gate_s : W.gate_s) + r0 * ng, d / 4);
+        copy_seg(base + 8 * d + d / 4, (e < 0 ? W.sh_gate_b : W.gate_b) + r0 * ng, d / 4);
+        copy_seg(base + 8 * d + d / 2, (e < 0 ? W.sh_up_s : W.up_s) + r0 * ng, d / 4);
+        copy_seg(base + 8 * d + 3 * d / 4, (e < 0 ? W.sh_up_b : W.up_b) + r0 * ng, d / 4);
+        finish_issue(slot);
+    };
+    // units [u0, u1) of down task k: 16 rows of Wd of each unit's expert
+    auto issue_down = [&](const DecodeLayerPtrs &W, int k, int u0, int u1) {
+        const int slot = static_cast<int>(iss % NS);
+        uint8_t *base = ring + static_cast<size_t>(slot) * SB;
+        const size_t j0 = static_cast<size_t>(P.c + k * P.G) * kDownRows;
+        const size_t ng = I / 64;
+        for (int i = 0; i < u1 - u0; ++i) {
+            const int e = S.unit_e[u0 + i];
+            const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * d) + j0;
+            uint8_t *ub = base + static_cast<size_t>(i) * 9 * I;
+            copy_seg(ub, (e < 0 ? W.sh_down_q : W.down_q) + r0 * (I / 2), 8u * I);
+            copy_seg(ub + 8 * I, (e < 0 ? W.sh_down_s : W.down_s) + r0 * ng, I / 2);
+            copy_seg(ub + 8 * I + I / 2, (e < 0 ? W.sh_down_b : W.down_b) + r0 * ng, I / 2);
+        }
+        finish_issue(slot);
+    };
+    auto issue_router = [&](const DecodeLayerPtrs &W) {
+        const int slot = static_cast<int>(iss % NS);
+        uint8_t *base = ring + static_cast<size_t>(slot) * SB;
+        for (int r = 0; r < P.n_rrows; ++r)
+            copy_seg(base + static_cast<size_t>(r) * 2 * d, W.router_w + static_cast<size_t>(P.c + r * P.G) * d, 2u * d);
+        finish_issue(slot);
+    };
+    // Issues items while slots are free and the next item is known.  Called by
+    // every thread at the same points, right after a barrier that follows the
+    // last read of the item consumed before.
+    auto top_up = [&]() {
+        while (q_li < a.n_layers && iss < done + static_cast<uint32_t>(NS)) {
+            const DecodeLayerPtrs &W = a.L[q_li];
+            if (q_stage == 0) {
+                issue_router(W);
+                q_stage = 1;
+                q_pos = P.gu_first();
+            } else if (q_stage == 1) {
+                if (q_pos < P.nu_gu) {
+                    issue_gu(W, q_pos, -1);
+                    q_pos += P.G;
+                } else {
+                    q_stage = 2;
+                }
+            } else {
+                if (units_li != a.layer0 + q_li) break;  // the routing of this layer is not known yet
+                const int U = S.n_units;
+                if (q_stage == 2) {
+                    if (q_pos < U * P.nu_gu) {
+                        if (q_pos >= P.nu_gu) issue_gu(W, q_pos, S.unit_e[q_pos / P.nu_gu]);
+                        q_pos += P.G;
+                    } else {
+                        q_stage = 3;
+                        q_k = 0;
+                        q_pos = 0;
+                    }
+                } else if (q_k < P.n_mydown) {
+                    if (q_pos < U) {
+                        issue_down(W, q_k, q_pos, min(U, q_pos + P.upc));
+                        q_pos += P.upc;
+                    } else {
+                        ++q_k;
+                        q_pos = 0;
+                    }
+                } else {
+                    ++q_li;
+                    q_stage = 0;
+                }
+            }
+        }
     };
 
-    if (warp == kProdWarp) {
-        // ============================================================ producer
-        uint32_t pit = 0;  // items issued
-        bool pok = true;
-        // Starts an item of `bytes`: waits for a free slot, expects the bytes on
-        // its full barrier; returns the slot index or -1 (giving up).
-        auto begin_item = [&](uint32_t bytes) -> int {
-            if (!pok) return -1;
-            const int slot = static_cast<int>(pit % NS);
-            int ok = 1;
-            if (lane == 0) {
-                ok = wait_bar(&S.empty[slot], ((pit / NS) & 1) ^ 1, wt);
-                if (ok) mbar_arrive_expect_tx(&S.full[slot], bytes);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
-                pok = false;
-                return -1;
-            }
-            ++pit;
-            return slot;
-        };
-        // gate/up task j of expert e (e < 0: the shared expert)
-        auto issue_gu = [&](const DecodeLayerPtrs &W, int j, int e) {
-            const int slot = begin_item(9u * d);
-            if (slot < 0) return;
-            uint8_t *base = ring + static_cast<size_t>(slot) * SB;
-            const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * I) + static_cast<size_t>(j % P.nu_gu) * kGURows;
-            const uint8_t *gq = e < 0 ? W.sh_gate_q : W.gate_q, *uq = e < 0 ? W.sh_up_q : W.up_q;
-            const uint16_t *gs = e < 0 ? W.sh_gate_s : W.gate_s, *gb = e < 0 ? W.sh_gate_b : W.gate_b;
-            const uint16_t *us = e < 0 ? W.sh_up_s : W.up_s, *ub = e < 0 ? W.sh_up_b : W.up_b;
-            const size_t ng = d / 64;
-            if (lane == 0) bulk_g2s(base, gq + r0 * (d / 2), 4u * d, &S.full[slot]);
-            if (lane == 1) bulk_g2s(base + 4 * d, uq + r0 * (d / 2), 4u * d, &S.full[slot]);
-            if (lane == 2) bulk_g2s(base + 8 * d, gs + r0 * ng, d / 4, &S.full[slot]);
-            if (lane == 3) bulk_g2s(base + 8 * d + d / 4, gb + r0 * ng, d / 4, &S.full[slot]);
-            if (lane == 4) bulk_g2s(base + 8 * d + d / 2, us + r0 * ng, d / 4, &S.full[slot]);
-            if (lane == 5) bulk_g2s(base + 8 * d + 3 * d / 4, ub + r0 * ng, d / 4, &S.full[slot]);
-        };
-        // units [u0, u1) of down task k: 16 rows of Wd of each unit's expert
-        auto issue_down = [&](const DecodeLayerPtrs &W, int k, int u0, int u1) {
-            const int slot = begin_item(9u * I * (u1 - u0));
-            if (slot < 0) return;
-            uint8_t *base = ring + static_cast<size_t>(slot) * SB;
-            const size_t j0 = static_cast<size_t>(P.c + k * P.G) * kDownRows;
-            const size_t ng = I / 64;
-            for (int q = lane; q < 3 * (u1 - u0); q += 32) {
-                const int i = q / 3, part = q - 3 * i;
-                const int e = S.unit_e[u0 + i];
-                const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * d) + j0;
-                uint8_t *ub = base + static_cast<size_t>(i) * 9 * I;
-                if (part == 0)
-                    bulk_g2s(ub, (e < 0 ? W.sh_down_q : W.down_q) + r0 * (I / 2), 8u * I, &S.full[slot]);
-                else if (part == 1)
-                    bulk_g2s(ub + 8 * I, (e < 0 ? W.sh_down_s : W.down_s) + r0 * ng, I / 2, &S.full[slot]);
-                else
-                    bulk_g2s(ub + 8 * I + I / 2, (e < 0 ? W.sh_down_b : W.down_b) + r0 * ng, I / 2, &S.full[slot]);
-            }
-        };
-        for (int li = 0; li < a.n_layers; ++li) {
-            const DecodeLayerPtrs &W = a.L[li];
-            // ---- items that do not depend on the routing
-            {
-                const int slot = begin_item(2u * d * P.n_rrows);
-                if (slot >= 0 && lane < P.n_rrows)
-                    bulk_g2s(ring + static_cast<size_t>(slot) * SB + static_cast<size_t>(lane) * 2 * d,
-                             W.router_w + static_cast<size_t>(P.c + lane * P.G) * d, 2u * d, &S.full[slot]);
-            }
-            for_gu_tasks(P, 0, P.nu_gu, [&](int j) { issue_gu(W, j, -1); });
-            if (top8_point()) break;
-            // ---- routed experts of this layer (the unit list is in shared memory),
-            // then the down rows of every unit (the shared expert's first)
-            const int U = S.n_units;
-            for_gu_tasks(P, P.nu_gu, U * P.nu_gu, [&](int j) { issue_gu(W, j, S.unit_e[j / P.nu_gu]); });
-            for (int k = 0; k < P.n_mydown; ++k)
-                for (int u0 = 0; u0 < U; u0 += P.upc) issue_down(W, k, u0, min(U, u0 + P.upc));
-        }
-        // no copy into this CTA's shared memory may still be in flight at exit
-        if (lane == 0) {
-            const uint32_t from = pit > static_cast<uint32_t>(NS) ? pit - NS : 0u;
-            for (uint32_t i = from; i < pit; ++i) drain_bar(&S.full[i % NS], (i / NS) & 1, wt.status);
-        }
-        __syncwarp();
-        return;
-    }
-
-    // ================================================================ compute warps
-    const int tid = threadIdx.x;  // 0..255
-    const int g = lane >> 2, t = lane & 3;
-    uint32_t cit = 0;  // items consumed
+    uint32_t cit = 0;  // index of the next item to consume
     int rp = 0;        // red buffer parity
     const size_t TD = static_cast<size_t>(T) * d;
     const size_t HX = static_cast<size_t>(kMaxUnits) * nkb_i * T * 64;  // words of one h' buffer
@@ -467,11 +456,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         slot_out = slot;
         return __all_sync(0xffffffffu, got) ? ring + static_cast<size_t>(slot) * SB : nullptr;
     };
-    // An item whose copy did not arrive (giving up) is not released: the slot
-    // may still be written, so the producer must not reuse it.
-    auto release_item = [&](int slot, const uint8_t *base) {
-        __syncwarp();
-        if (lane == 0 && base) mbar_arrive(&S.empty[slot]);
+    // After the barrier that ends every thread's reads of the item just taken:
+    // its slot is free for the next item.
+    auto item_done = [&]() {
+        done = cit;
+        top_up();
     };
 
     // ---- layer input x_l into xb (bf16) and xp (permuted fp16); export_only:
@@ -554,11 +543,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                 mma_kblock(acc, qg, qu, sb_of(gs, gb, g, ng, grp), sb_of(us, ub, g, ng, grp), bfr);
             }
         }
-        release_item(slot, base);
         float *r = S.red[rp][warp][lane];
 #pragma unroll
         for (int q = 0; q < 4; ++q) r[q] = acc[q];
         compute_sync();
+        item_done();
         if (warp == 0 && base != nullptr) {
             float D[4] = {0.f, 0.f, 0.f, 0.f};
             for (int w = 0; w < kCW; ++w)
@@ -631,8 +620,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                 mma_kblock(acc, qg, qg8, sb_of(s, b, g, ng, grp), sb_of(s, b, g + 8, ng, grp), bfr);
             }
         }
-        release_item(slot, base);
-        compute_sync();  // hs is reused by the next item
+        compute_sync();  // hs and the slot are free for the next item
+        item_done();
     };
 
     // ---- down task k done: sum the warps' fragments, publish the rows
@@ -663,6 +652,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         rp ^= 1;
     };
 
+    top_up();  // layer 0's router and shared rows
     for (int li = 0; li < a.n_layers; ++li) {
         const int l = a.layer0 + li;
         const DecodeLayerPtrs &W = a.L[li];
@@ -691,7 +681,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                     }
                 }
             }
-            release_item(slot, base);
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
@@ -701,6 +690,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                         if (lane == 0) S.rred[warp][r][n] = v;
                     }
             compute_sync();
+            item_done();
             if (warp == 0) {
                 if (tid < P.n_rrows * T && base) {
                     const int r = tid / T, n = tid - r * T, e = P.c + r * P.G;
@@ -773,10 +763,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                     S.unit_w[u][n] = wv;
                 }
             }
-            if (tid == 0) S.n_units = min(n_used + 1, kMaxUnits);
+            if (tid == 0) {
+                S.n_units = min(n_used + 1, kMaxUnits);
+                S.decide = *reinterpret_cast<volatile int *>(&S.abort);  // one decision for every warp
+            }
         }
-        if (top8_point()) break;
+        compute_sync();
+        if (*reinterpret_cast<volatile int *>(&S.decide)) break;
         const int U = S.n_units;
+        units_li = l;
+        top_up();  // the routed experts' bytes, then the next layer's router and shared rows
 
         // ---- the shared expert's gate/up rows of this CTA (computed while the
         // routed experts' bytes, issued at the top-8 point, are in flight)
@@ -791,8 +787,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         }
     }
     // the normalised output of the last layer (the input a next layer would take)
-    if (a.last_launch && a.x_next && blockIdx.x == 0 && !*reinterpret_cast<volatile int *>(&S.abort))
+    if (a.last_launch && a.x_next && blockIdx.x == 0 && !*reinterpret_cast<volatile int *>(&S.decide))
         build_input(a.layer0 + a.n_layers, true);
+    // no copy into this CTA's shared memory may still be in flight at exit
+    cp_async_wait_all();
 }
 
 }  // namespace
