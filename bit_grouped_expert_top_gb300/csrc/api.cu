@@ -604,7 +604,8 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
 
     DecodeArgs a{};
     a.T = s.T; a.d = s.d; a.E = s.E; a.top_k = s.top_k; a.I = s.I;
-    a.n_slots = decode_ring_slots(s.T, s.d, s.I);
+    a.n_slots = decode_launch_slots(s.T, s.d, s.I);
+    if (a.n_slots == 0) return LILY_ERR_UNSUPPORTED;
     a.slot_bytes = decode_slot_bytes(s.d, s.I);
     a.x_in = x;
     a.out = out;

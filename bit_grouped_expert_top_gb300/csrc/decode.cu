@@ -811,6 +811,22 @@ int decode_ring_slots(int T, int d, int I)
     return n >= 3 ? n : 0;
 }
 
+// Ring slots of a launch on the current device: at most decode_ring_slots(),
+// fewer if the device cannot keep one CTA with that much shared memory
+// resident on every SM (a cooperative launch needs every CTA resident).
+int decode_launch_slots(int T, int d, int I)
+{
+    for (int n = decode_ring_slots(T, d, I); n >= 3; --n) {
+        const int smem = static_cast<int>(decode_smem_bytes(T, d, I, n));
+        if (set_max_dynamic_smem(reinterpret_cast<const void *>(decode_kernel), smem) != cudaSuccess) continue;
+        int blocks = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, decode_kernel, kDecThreads, smem) == cudaSuccess &&
+            blocks >= 1)
+            return n;
+    }
+    return 0;
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t stream)
 {
     const size_t smem = decode_smem_bytes(a.T, a.d, a.I, a.n_slots);

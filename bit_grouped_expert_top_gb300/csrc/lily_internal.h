@@ -151,6 +151,7 @@ static_assert(sizeof(DecodeArgs) <= 4096, "decode kernel parameters stay within 
 // shape does not fit), the bytes of one slot, and the dynamic shared memory of
 // the launch.
 int decode_ring_slots(int T, int d, int I);
+int decode_launch_slots(int T, int d, int I);  // device-checked (needs the device current)
 int decode_slot_bytes(int d, int I);
 size_t decode_smem_bytes(int T, int d, int I, int n_slots);
 cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t stream);
