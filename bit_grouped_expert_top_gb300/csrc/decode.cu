@@ -39,11 +39,13 @@
 // counters are per layer and zeroed at the start of every call.
 //
 // Every weight a CTA needs streams through a ring of shared-memory slots: all
-// 256 threads copy 16-byte pieces of an item with cp.async and arrive on the
-// slot's mbarrier when their pieces have landed.  (One SM's TMA unit takes
-// 30-50 ns to start each bulk copy whatever its size, so the ~60 copies of a
-// layer's rows and scale/bias arrays, issued by one thread, kept the bytes of
-// the last items waiting; the load/store units have no such cost per copy.)
+// 256 threads copy 16-byte pieces of an item with cp.async, one commit group
+// per item, and wait for an item's group before the CTA barrier that starts
+// its use.  (One SM's TMA unit takes 30-50 ns to start each bulk copy whatever
+// its size, so the ~60 copies of a layer's rows and scale/bias arrays, issued
+// by one thread, kept the bytes of the last items waiting; and an mbarrier
+// arrival tied to a thread's cp.async completion held back the thread's later
+// copies, so items streamed one at a time.)
 // Items that do not depend on the routing (the router rows and the shared
 // expert's gate/up rows) of layer l + 1 are issued as soon as the slots of
 // layer l free up, so they load while layer l finishes; the routed experts'
@@ -75,7 +77,6 @@ constexpr int kSmemLimit = 232448;            // 227 KB of dynamic shared memory
 constexpr int kBarCompute = 1;                // named barrier of the CTA (0 is __syncthreads)
 
 struct DecSmem {
-    uint64_t full[kMaxSlots];     // ring slot filled (one arrival per thread)
     int abort;                    // this CTA gives up (set by any failed wait)
     int decide;                   // the abort decision taken at the top-8 point
     int n_units;
@@ -169,13 +170,19 @@ __device__ __forceinline__ bool wait_ready(const unsigned int *p, unsigned int t
     }
 }
 
-// mbarrier wait (bounded; a failure also
-// raises the global abort flag).
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, const Waiter &w)
+// Waits until at most n of this thread's most recent cp.async groups are
+// still in flight (n clamped to 15; the ring has at most 16 slots).
+__device__ __forceinline__ void cp_async_wait_pending(uint32_t n)
 {
-    if (mbar_wait(bar, parity, w.s_abort, w.status)) return true;
-    raise_abort(w);
-    return false;
+    switch (n < 15u ? n : 15u) {
+#define LILY_WAIT_GROUP(k) \
+    case k: asm volatile("cp.async.wait_group " #k ";" ::: "memory"); break;
+        LILY_WAIT_GROUP(0) LILY_WAIT_GROUP(1) LILY_WAIT_GROUP(2) LILY_WAIT_GROUP(3) LILY_WAIT_GROUP(4)
+        LILY_WAIT_GROUP(5) LILY_WAIT_GROUP(6) LILY_WAIT_GROUP(7) LILY_WAIT_GROUP(8) LILY_WAIT_GROUP(9)
+        LILY_WAIT_GROUP(10) LILY_WAIT_GROUP(11) LILY_WAIT_GROUP(12) LILY_WAIT_GROUP(13) LILY_WAIT_GROUP(14)
+        LILY_WAIT_GROUP(15)
+#undef LILY_WAIT_GROUP
+    }
 }
 
 __device__ __forceinline__ uint4 lds128(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
@@ -327,11 +334,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     const int nkb_d = d / kKB, nkb_i = I / kKB;
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], kDecThreads);  // one arrival per thread and item
         S.abort = 0;
         S.decide = 0;
         S.unit_e[0] = -1;  // unit 0 is always the shared expert
-        fence_mbar_init();
     }
     if (tid < 8) S.zeros[tid] = make_uint2(0u, 0u);
     __syncthreads();
@@ -342,10 +347,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     //   stage 1  the shared expert's gate/up tasks of this CTA
     //   stage 2  the routed gate/up tasks of this CTA       (after the top-8 of li)
     //   stage 3  per down task, chunks of units [u0, u0 + upc) (after the top-8 of li)
-    // Every thread copies its 16-byte pieces of an item with cp.async and then
-    // arrives (noinc) on the item's full barrier, which completes once all
-    // copies of all threads have landed.  Item n goes to slot n % NS; it is
-    // issued only once item n - NS has been consumed by every thread.
+    // Every thread copies its 16-byte pieces of an item with cp.async and
+    // commits them as one group; a thread's groups complete in issue order, so
+    // waiting until at most (issued - n - 1) groups are pending means item n
+    // has landed.  Item n goes to slot n % NS; it is issued only once item
+    // n - NS has been consumed by every thread.
     uint32_t iss = 0, done = 0;       // items issued / consumed (all threads)
     int q_li = 0, q_stage = 0, q_pos = 0, q_k = 0;  // cursor of the next item to issue
     int units_li = -1;                // layer whose unit list is in shared memory
@@ -355,8 +361,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         for (uint32_t o = static_cast<uint32_t>(tid) * 16u; o < bytes; o += kDecThreads * 16u)
             cp_async_16(dst + o, static_cast<const uint8_t *>(src) + o);
     };
-    auto finish_issue = [&](int slot) {
-        cp_async_mbar_arrive_noinc(&S.full[slot]);
+    auto finish_issue = [&](int) {
+        cp_async_commit();  // one group per item and thread, in issue order
         ++iss;
     };
     // gate/up task j of expert e (e < 0: the shared expert)
@@ -447,14 +453,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     const size_t HX = static_cast<size_t>(kMaxUnits) * nkb_i * T * 64;  // words of one h' buffer
     auto ready_of = [&](int l) { return a.ready + static_cast<size_t>(l) * kDecodeReadySlots; };
 
-    // Waits for the next item; returns its slot base (nullptr: giving up).  The
-    // result is uniform within each warp.
+    // Waits for the next item: every thread waits for its own copies of it (its
+    // groups complete in issue order), then the CTA barrier makes all threads'
+    // pieces visible.  Returns the slot base.
     auto take_item = [&](int &slot_out) -> const uint8_t * {
         const int slot = static_cast<int>(cit % NS);
-        const bool got = wait_bar(&S.full[slot], (cit / NS) & 1, wt);
+        if (iss <= cit && tid == 0) record_error(wt.status, kErrDeviceIndex);  // an item is issued before its use
+        cp_async_wait_pending(iss - cit - 1);
+        compute_sync();
         ++cit;
         slot_out = slot;
-        return __all_sync(0xffffffffu, got) ? ring + static_cast<size_t>(slot) * SB : nullptr;
+        return ring + static_cast<size_t>(slot) * SB;
     };
     // After the barrier that ends every thread's reads of the item just taken:
     // its slot is free for the next item.
