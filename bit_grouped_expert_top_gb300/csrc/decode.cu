@@ -12,7 +12,7 @@
 // resident kernel instead of kernel boundaries.
 //
 // GB300 design.  One CTA per SM (a cooperative launch, so every CTA is
-// resident), 8 warps.  Per layer l, every CTA:
+// resident), 8 compute warps and 1 producer warp.  Per layer l, every CTA:
 //   A  builds the layer input x_l in shared memory (layer 0: x; later layers:
 //      bf16 of the previous output over sqrt(mean(out^2) + 1e-6), the
 //      parameter-free RMS norm that links layers), reading the previous
@@ -38,14 +38,14 @@
 // with every CTA spinning on the same lines, queued up at the L2 slices).  The
 // counters are per layer and zeroed at the start of every call.
 //
-// Every weight a CTA needs streams through a ring of shared-memory slots: all
-// 256 threads copy 16-byte pieces of an item with cp.async, one commit group
-// per item, and wait for an item's group before the CTA barrier that starts
-// its use.  (One SM's TMA unit takes 30-50 ns to start each bulk copy whatever
-// its size, so the ~60 copies of a layer's rows and scale/bias arrays, issued
-// by one thread, kept the bytes of the last items waiting; and an mbarrier
-// arrival tied to a thread's cp.async completion held back the thread's later
-// copies, so items streamed one at a time.)
+// Every weight a CTA needs streams through a ring of shared-memory slots.  The
+// producer warp copies each item as 16-byte cp.async pieces spread over its 32
+// lanes and the lanes arrive on the slot's mbarrier once their pieces land; the
+// compute warps release a slot after reading it.  (One SM's TMA unit takes
+// 30-50 ns to start each bulk copy whatever its size, and a layer needs ~60
+// copies of rows and of the scale/bias arrays; with the compute warps issuing
+// cp.async themselves, they stalled on the full load queue instead of working
+// on the items already there.)
 // Items that do not depend on the routing (the router rows and the shared
 // expert's gate/up rows) of layer l + 1 are issued as soon as the slots of
 // layer l free up, so they load while layer l finishes; the routed experts'
@@ -66,17 +66,19 @@ namespace {
 
 constexpr int kMaxT = kDecodeMaxT;
 constexpr int kMaxUnits = kDecodeMaxUnits;
-constexpr int kCW = 8;                        // warps
-constexpr int kDecThreads = kCW * 32;
-constexpr int kComputeThreads = kDecThreads;
+constexpr int kCW = 8;                        // compute warps
+constexpr int kDecThreads = (kCW + 1) * 32;   // + the producer warp
+constexpr int kProdWarp = kCW;
+constexpr int kComputeThreads = kCW * 32;
 constexpr int kKB = 128;                      // K block of one lane pass (16 bytes of int4 per row)
 constexpr int kGURows = 8;                    // I rows of one gate/up task
 constexpr int kDownRows = 16;                 // output rows of one down task
 constexpr int kMaxSlots = 16;
 constexpr int kSmemLimit = 232448;            // 227 KB of dynamic shared memory per CTA
-constexpr int kBarCompute = 1;                // named barrier of the CTA (0 is __syncthreads)
+constexpr int kBarTop8 = 1, kBarCompute = 2;  // named barriers (0 is __syncthreads)
 
 struct DecSmem {
+    uint64_t full[kMaxSlots], empty[kMaxSlots];  // ring slot landed / free again
     int abort;                    // this CTA gives up (set by any failed wait)
     int decide;                   // the abort decision taken at the top-8 point
     int n_units;
@@ -170,19 +172,12 @@ __device__ __forceinline__ bool wait_ready(const unsigned int *p, unsigned int t
     }
 }
 
-// Waits until at most n of this thread's most recent cp.async groups are
-// still in flight (n clamped to 15; the ring has at most 16 slots).
-__device__ __forceinline__ void cp_async_wait_pending(uint32_t n)
+// mbarrier wait (bounded; a failure also raises the global abort flag).
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, const Waiter &w)
 {
-    switch (n < 15u ? n : 15u) {
-#define LILY_WAIT_GROUP(k) \
-    case k: asm volatile("cp.async.wait_group " #k ";" ::: "memory"); break;
-        LILY_WAIT_GROUP(0) LILY_WAIT_GROUP(1) LILY_WAIT_GROUP(2) LILY_WAIT_GROUP(3) LILY_WAIT_GROUP(4)
-        LILY_WAIT_GROUP(5) LILY_WAIT_GROUP(6) LILY_WAIT_GROUP(7) LILY_WAIT_GROUP(8) LILY_WAIT_GROUP(9)
-        LILY_WAIT_GROUP(10) LILY_WAIT_GROUP(11) LILY_WAIT_GROUP(12) LILY_WAIT_GROUP(13) LILY_WAIT_GROUP(14)
-        LILY_WAIT_GROUP(15)
-#undef LILY_WAIT_GROUP
-    }
+    if (mbar_wait(bar, parity, w.s_abort, w.status)) return true;
+    raise_abort(w);
+    return false;
 }
 
 __device__ __forceinline__ uint4 lds128(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
@@ -306,6 +301,7 @@ __device__ __forceinline__ void for_gu_tasks(const Plan &p, int j_lo, int j_hi, 
 }
 
 // ---------------------------------------------------------------- the kernel
+// 9 warps: one SM sub-partition holds 3 of them, so at most 168 registers each
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a)
 {
     extern __shared__ __align__(128) uint8_t dsm[];
@@ -316,7 +312,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     // h' of one down item's units, staged from the exchange buffer: [unit][K block][T][4][16] words
     uint32_t *hs = reinterpret_cast<uint32_t *>(dsm + kStaticBytes + align128(static_cast<size_t>(T) * d * 4));
     uint8_t *ring = dsm + kStaticBytes + align128(static_cast<size_t>(T) * d * 4) + stage_bytes(T, d, I);
-    const int tid = threadIdx.x;  // 0..255
+    const int tid = threadIdx.x;  // compute threads 0..255, producer warp 256..287
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     const int NS = a.n_slots;
@@ -334,118 +330,115 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     const int nkb_d = d / kKB, nkb_i = I / kKB;
 
     if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&S.full[s], 32);     // the producer's 32 lanes, each once its copies landed
+            mbar_init(&S.empty[s], kCW);   // the compute warps, each once done reading
+        }
         S.abort = 0;
         S.decide = 0;
         S.unit_e[0] = -1;  // unit 0 is always the shared expert
+        fence_mbar_init();
     }
     if (tid < 8) S.zeros[tid] = make_uint2(0u, 0u);
     __syncthreads();
 
+    // Abort decision at the top-8 point of every layer, the same for all warps:
+    // one thread reads the flag between two barriers of the whole CTA.  The
+    // producer learns here that the unit list of the layer is complete.
+    auto top8_point = [&]() -> bool {
+        named_barrier_sync(kBarTop8, kDecThreads);
+        if (tid == 0) S.decide = *reinterpret_cast<volatile int *>(&S.abort);
+        named_barrier_sync(kBarTop8, kDecThreads);
+        return *reinterpret_cast<volatile int *>(&S.decide) != 0;
+    };
+
     // ---------------------------------------------------------------- the ring
     // Items, in the order they are issued and consumed, per layer li:
-    //   stage 0  the router rows of this CTA
-    //   stage 1  the shared expert's gate/up tasks of this CTA
-    //   stage 2  the routed gate/up tasks of this CTA       (after the top-8 of li)
-    //   stage 3  per down task, chunks of units [u0, u0 + upc) (after the top-8 of li)
-    // Every thread copies its 16-byte pieces of an item with cp.async and
-    // commits them as one group; a thread's groups complete in issue order, so
-    // waiting until at most (issued - n - 1) groups are pending means item n
-    // has landed.  Item n goes to slot n % NS; it is issued only once item
-    // n - NS has been consumed by every thread.
-    uint32_t iss = 0, done = 0;       // items issued / consumed (all threads)
-    int q_li = 0, q_stage = 0, q_pos = 0, q_k = 0;  // cursor of the next item to issue
-    int units_li = -1;                // layer whose unit list is in shared memory
-
-    // pieces of one item: copies [first piece, +n) of `bytes`-byte segment
-    auto copy_seg = [&](uint8_t *dst, const void *src, uint32_t bytes) {
-        for (uint32_t o = static_cast<uint32_t>(tid) * 16u; o < bytes; o += kDecThreads * 16u)
-            cp_async_16(dst + o, static_cast<const uint8_t *>(src) + o);
-    };
-    auto finish_issue = [&](int) {
-        cp_async_commit();  // one group per item and thread, in issue order
-        ++iss;
-    };
-    // gate/up task j of expert e (e < 0: the shared expert)
-    auto issue_gu = [&](const DecodeLayerPtrs &W, int j, int e) {
-        const int slot = static_cast<int>(iss % NS);
-        uint8_t *base = ring + static_cast<size_t>(slot) * SB;
-        const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * I) + static_cast<size_t>(j % P.nu_gu) * kGURows;
-        const size_t ng = d / 64;
-        copy_seg(base, (e < 0 ? W.sh_gate_q : W.gate_q) + r0 * (d / 2), 4u * d);
-        copy_seg(base + 4 * d, (e < 0 ? W.sh_up_q : W.up_q) + r0 * (d / 2), 4u * d);
-        copy_seg(base + 8 * d, (e < 0 ? W.sh_gate_s : W.gate_s) + r0 * ng, d / 4);
-        copy_seg(base + 8 * d + d / 4, (e < 0 ? W.sh_gate_b : W.gate_b) + r0 * ng, d / 4);
-        copy_seg(base + 8 * d + d / 2, (e < 0 ? W.sh_up_s : W.up_s) + r0 * ng, d / 4);
-        copy_seg(base + 8 * d + 3 * d / 4, (e < 0 ? W.sh_up_b : W.up_b) + r0 * ng, d / 4);
-        finish_issue(slot);
-    };
-    // units [u0, u1) of down task k: 16 rows of Wd of each unit's expert
-    auto issue_down = [&](const DecodeLayerPtrs &W, int k, int u0, int u1) {
-        const int slot = static_cast<int>(iss % NS);
-        uint8_t *base = ring + static_cast<size_t>(slot) * SB;
-        const size_t j0 = static_cast<size_t>(P.c + k * P.G) * kDownRows;
-        const size_t ng = I / 64;
-        for (int i = 0; i < u1 - u0; ++i) {
-            const int e = S.unit_e[u0 + i];
-            const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * d) + j0;
-            uint8_t *ub = base + static_cast<size_t>(i) * 9 * I;
-            copy_seg(ub, (e < 0 ? W.sh_down_q : W.down_q) + r0 * (I / 2), 8u * I);
-            copy_seg(ub + 8 * I, (e < 0 ? W.sh_down_s : W.down_s) + r0 * ng, I / 2);
-            copy_seg(ub + 8 * I + I / 2, (e < 0 ? W.sh_down_b : W.down_b) + r0 * ng, I / 2);
-        }
-        finish_issue(slot);
-    };
-    auto issue_router = [&](const DecodeLayerPtrs &W) {
-        const int slot = static_cast<int>(iss % NS);
-        uint8_t *base = ring + static_cast<size_t>(slot) * SB;
-        for (int r = 0; r < P.n_rrows; ++r)
-            copy_seg(base + static_cast<size_t>(r) * 2 * d, W.router_w + static_cast<size_t>(P.c + r * P.G) * d, 2u * d);
-        finish_issue(slot);
-    };
-    // Issues items while slots are free and the next item is known.  Called by
-    // every thread at the same points, right after a barrier that follows the
-    // last read of the item consumed before.
-    auto top_up = [&]() {
-        while (q_li < a.n_layers && iss < done + static_cast<uint32_t>(NS)) {
-            const DecodeLayerPtrs &W = a.L[q_li];
-            if (q_stage == 0) {
-                issue_router(W);
-                q_stage = 1;
-                q_pos = P.gu_first();
-            } else if (q_stage == 1) {
-                if (q_pos < P.nu_gu) {
-                    issue_gu(W, q_pos, -1);
-                    q_pos += P.G;
-                } else {
-                    q_stage = 2;
-                }
-            } else {
-                if (units_li != a.layer0 + q_li) break;  // the routing of this layer is not known yet
-                const int U = S.n_units;
-                if (q_stage == 2) {
-                    if (q_pos < U * P.nu_gu) {
-                        if (q_pos >= P.nu_gu) issue_gu(W, q_pos, S.unit_e[q_pos / P.nu_gu]);
-                        q_pos += P.G;
-                    } else {
-                        q_stage = 3;
-                        q_k = 0;
-                        q_pos = 0;
-                    }
-                } else if (q_k < P.n_mydown) {
-                    if (q_pos < U) {
-                        issue_down(W, q_k, q_pos, min(U, q_pos + P.upc));
-                        q_pos += P.upc;
-                    } else {
-                        ++q_k;
-                        q_pos = 0;
-                    }
-                } else {
-                    ++q_li;
-                    q_stage = 0;
+    //   router rows of this CTA; the shared expert's gate/up tasks of this CTA;
+    //   [top-8 point]  the routed gate/up tasks of this CTA; per down task,
+    //   chunks of units [u0, u0 + upc).
+    // The producer warp copies each item with 16-byte cp.async pieces spread
+    // over its 32 lanes; every lane then arrives (noinc) on the slot's full
+    // barrier, which fires once all lanes' copies have landed.  Only the
+    // producer waits while the load queue is full; the compute warps work on
+    // the items already there.  Item n goes to slot n % NS once its previous
+    // occupant has been released by all compute warps.
+    if (warp == kProdWarp) {
+        uint32_t pit = 0;  // items issued
+        bool pok = true;
+        auto copy_seg = [&](uint8_t *dst, const void *src, uint32_t bytes) {
+            for (uint32_t o = static_cast<uint32_t>(lane) * 16u; o < bytes; o += 32u * 16u)
+                cp_async_16(dst + o, static_cast<const uint8_t *>(src) + o);
+        };
+        // waits for a free slot; returns it, or -1 when giving up
+        auto begin_item = [&]() -> int {
+            if (!pok) return -1;
+            const int slot = static_cast<int>(pit % NS);
+            int ok = 1;
+            if (lane == 0) ok = wait_bar(&S.empty[slot], ((pit / NS) & 1) ^ 1, wt);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) pok = false;
+            return ok ? slot : -1;
+        };
+        auto end_item = [&](int slot) {
+            cp_async_mbar_arrive_noinc(&S.full[slot]);
+            ++pit;
+        };
+        // gate/up task j of expert e (e < 0: the shared expert)
+        auto issue_gu = [&](const DecodeLayerPtrs &W, int j, int e) {
+            const int slot = begin_item();
+            if (slot < 0) return;
+            uint8_t *base = ring + static_cast<size_t>(slot) * SB;
+            const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * I) + static_cast<size_t>(j % P.nu_gu) * kGURows;
+            const size_t ng = d / 64;
+            copy_seg(base, (e < 0 ? W.sh_gate_q : W.gate_q) + r0 * (d / 2), 4u * d);
+            copy_seg(base + 4 * d, (e < 0 ? W.sh_up_q : W.up_q) + r0 * (d / 2), 4u * d);
+            copy_seg(base + 8 * d, (e < 0 ? W.sh_gate_s : W.gate_s) + r0 * ng, d / 4);
+            copy_seg(base + 8 * d + d / 4, (e < 0 ? W.sh_gate_b : W.gate_b) + r0 * ng, d / 4);
+            copy_seg(base + 8 * d + d / 2, (e < 0 ? W.sh_up_s : W.up_s) + r0 * ng, d / 4);
+            copy_seg(base + 8 * d + 3 * d / 4, (e < 0 ? W.sh_up_b : W.up_b) + r0 * ng, d / 4);
+            end_item(slot);
+        };
+        // units [u0, u1) of down task k: 16 rows of Wd of each unit's expert
+        auto issue_down = [&](const DecodeLayerPtrs &W, int k, int u0, int u1) {
+            const int slot = begin_item();
+            if (slot < 0) return;
+            uint8_t *base = ring + static_cast<size_t>(slot) * SB;
+            const size_t j0 = static_cast<size_t>(P.c + k * P.G) * kDownRows;
+            const size_t ng = I / 64;
+            for (int i = 0; i < u1 - u0; ++i) {
+                const int e = S.unit_e[u0 + i];
+                const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * d) + j0;
+                uint8_t *ub = base + static_cast<size_t>(i) * 9 * I;
+                copy_seg(ub, (e < 0 ? W.sh_down_q : W.down_q) + r0 * (I / 2), 8u * I);
+                copy_seg(ub + 8 * I, (e < 0 ? W.sh_down_s : W.down_s) + r0 * ng, I / 2);
+                copy_seg(ub + 8 * I + I / 2, (e < 0 ? W.sh_down_b : W.down_b) + r0 * ng, I / 2);
+            }
+            end_item(slot);
+        };
+        for (int li = 0; li < a.n_layers; ++li) {
+            const DecodeLayerPtrs &W = a.L[li];
+            {
+                const int slot = begin_item();
+                if (slot >= 0) {
+                    uint8_t *base = ring + static_cast<size_t>(slot) * SB;
+                    for (int r = 0; r < P.n_rrows; ++r)
+                        copy_seg(base + static_cast<size_t>(r) * 2 * d,
+                                 W.router_w + static_cast<size_t>(P.c + r * P.G) * d, 2u * d);
+                    end_item(slot);
                 }
             }
+            for_gu_tasks(P, 0, P.nu_gu, [&](int j) { issue_gu(W, j, -1); });
+            if (top8_point()) break;
+            const int U = S.n_units;
+            for_gu_tasks(P, P.nu_gu, U * P.nu_gu, [&](int j) { issue_gu(W, j, S.unit_e[j / P.nu_gu]); });
+            for (int k = 0; k < P.n_mydown; ++k)
+                for (int u0 = 0; u0 < U; u0 += P.upc) issue_down(W, k, u0, min(U, u0 + P.upc));
         }
-    };
+        // no copy into this CTA's shared memory may still be in flight at exit
+        cp_async_wait_all();
+        return;
+    }
 
     uint32_t cit = 0;  // index of the next item to consume
     int rp = 0;        // red buffer parity
@@ -453,23 +446,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     const size_t HX = static_cast<size_t>(kMaxUnits) * nkb_i * T * 64;  // words of one h' buffer
     auto ready_of = [&](int l) { return a.ready + static_cast<size_t>(l) * kDecodeReadySlots; };
 
-    // Waits for the next item: every thread waits for its own copies of it (its
-    // groups complete in issue order), then the CTA barrier makes all threads'
-    // pieces visible.  Returns the slot base.
+    // Waits for the next item; returns its slot base (nullptr: giving up).  The
+    // result is uniform within each warp.
     auto take_item = [&](int &slot_out) -> const uint8_t * {
         const int slot = static_cast<int>(cit % NS);
-        if (iss <= cit && tid == 0) record_error(wt.status, kErrDeviceIndex);  // an item is issued before its use
-        cp_async_wait_pending(iss - cit - 1);
-        compute_sync();
+        const bool got = wait_bar(&S.full[slot], (cit / NS) & 1, wt);
         ++cit;
         slot_out = slot;
-        return ring + static_cast<size_t>(slot) * SB;
+        return __all_sync(0xffffffffu, got) ? ring + static_cast<size_t>(slot) * SB : nullptr;
     };
-    // After the barrier that ends every thread's reads of the item just taken:
-    // its slot is free for the next item.
-    auto item_done = [&]() {
-        done = cit;
-        top_up();
+    // This warp is done reading the item's slot.  An item whose copies did not
+    // arrive (giving up) is not released: the slot may still be written.
+    auto release_item = [&](int slot, const uint8_t *base) {
+        __syncwarp();
+        if (lane == 0 && base) mbar_arrive(&S.empty[slot]);
     };
 
     // ---- layer input x_l into xb (bf16) and xp (permuted fp16); export_only:
@@ -552,11 +542,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                 mma_kblock(acc, qg, qu, sb_of(gs, gb, g, ng, grp), sb_of(us, ub, g, ng, grp), bfr);
             }
         }
+        release_item(slot, base);
         float *r = S.red[rp][warp][lane];
 #pragma unroll
         for (int q = 0; q < 4; ++q) r[q] = acc[q];
         compute_sync();
-        item_done();
         if (warp == 0 && base != nullptr) {
             float D[4] = {0.f, 0.f, 0.f, 0.f};
             for (int w = 0; w < kCW; ++w)
@@ -629,8 +619,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                 mma_kblock(acc, qg, qg8, sb_of(s, b, g, ng, grp), sb_of(s, b, g + 8, ng, grp), bfr);
             }
         }
-        compute_sync();  // hs and the slot are free for the next item
-        item_done();
+        release_item(slot, base);
+        compute_sync();  // hs is reused by the next item
     };
 
     // ---- down task k done: sum the warps' fragments, publish the rows
@@ -661,7 +651,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         rp ^= 1;
     };
 
-    top_up();  // layer 0's router and shared rows
     for (int li = 0; li < a.n_layers; ++li) {
         const int l = a.layer0 + li;
         const DecodeLayerPtrs &W = a.L[li];
@@ -698,8 +687,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                         const float v = warp_sum(part[r][n]);
                         if (lane == 0) S.rred[warp][r][n] = v;
                     }
+            release_item(slot, base);
             compute_sync();
-            item_done();
             if (warp == 0) {
                 if (tid < P.n_rrows * T && base) {
                     const int r = tid / T, n = tid - r * T, e = P.c + r * P.G;
@@ -772,16 +761,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                     S.unit_w[u][n] = wv;
                 }
             }
-            if (tid == 0) {
-                S.n_units = min(n_used + 1, kMaxUnits);
-                S.decide = *reinterpret_cast<volatile int *>(&S.abort);  // one decision for every warp
-            }
+            if (tid == 0) S.n_units = min(n_used + 1, kMaxUnits);
         }
-        compute_sync();
-        if (*reinterpret_cast<volatile int *>(&S.decide)) break;
+        if (top8_point()) break;  // the producer issues the routed experts' bytes from here
         const int U = S.n_units;
-        units_li = l;
-        top_up();  // the routed experts' bytes, then the next layer's router and shared rows
 
         // ---- the shared expert's gate/up rows of this CTA (computed while the
         // routed experts' bytes, issued at the top-8 point, are in flight)
@@ -798,8 +781,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     // the normalised output of the last layer (the input a next layer would take)
     if (a.last_launch && a.x_next && blockIdx.x == 0 && !*reinterpret_cast<volatile int *>(&S.decide))
         build_input(a.layer0 + a.n_layers, true);
-    // no copy into this CTA's shared memory may still be in flight at exit
-    cp_async_wait_all();
 }
 
 }  // namespace
