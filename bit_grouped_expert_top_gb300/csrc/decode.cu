@@ -38,14 +38,15 @@
 // with every CTA spinning on the same lines, queued up at the L2 slices).  The
 // counters are per layer and zeroed at the start of every call.
 //
-// Every weight a CTA needs streams through a ring of shared-memory slots.  The
-// producer warp copies each item as 16-byte cp.async pieces spread over its 32
-// lanes and the lanes arrive on the slot's mbarrier once their pieces land; the
-// compute warps release a slot after reading it.  (One SM's TMA unit takes
-// 30-50 ns to start each bulk copy whatever its size, and a layer needs ~60
-// copies of rows and of the scale/bias arrays; with the compute warps issuing
-// cp.async themselves, they stalled on the full load queue instead of working
-// on the items already there.)
+// Every weight a CTA needs streams through a ring of shared-memory slots.  A
+// producer warp copies the weight rows of each item with bulk (TMA) copies
+// (2 KB to 8 KB each) and the 256-512 byte scale/bias slices as 16-byte
+// cp.async pieces from its 32 lanes; the compute warps release a slot after
+// reading it.  (One SM's TMA unit takes 30-50 ns to start each bulk copy
+// whatever its size, so the small slices, four per gate/up task and two per
+// down unit, go through the load/store units instead; and with the compute
+// warps issuing cp.async themselves they stalled on the full load queue
+// instead of working on the items already there.)
 // Items that do not depend on the routing (the router rows and the shared
 // expert's gate/up rows) of layer l + 1 are issued as soon as the slots of
 // layer l free up, so they load while layer l finishes; the routed experts'
@@ -113,6 +114,15 @@ __host__ __device__ inline size_t stage_bytes(int T, int d, int I)
 }
 
 // ---------------------------------------------------------------- memory helpers
+
+// Bulk (TMA) copy global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 
 // Ready counters: release add by the writer, acquire load by the reader.
 __device__ __forceinline__ void signal_ready(unsigned int *p)
@@ -331,7 +341,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&S.full[s], 32);     // the producer's 32 lanes, each once its copies landed
+            mbar_init(&S.full[s], 33);     // the bulk copies' byte count, then the producer's 32 lanes
             mbar_init(&S.empty[s], kCW);   // the compute warps, each once done reading
         }
         S.abort = 0;
@@ -357,11 +367,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     //   router rows of this CTA; the shared expert's gate/up tasks of this CTA;
     //   [top-8 point]  the routed gate/up tasks of this CTA; per down task,
     //   chunks of units [u0, u0 + upc).
-    // The producer warp copies each item with 16-byte cp.async pieces spread
-    // over its 32 lanes; every lane then arrives (noinc) on the slot's full
-    // barrier, which fires once all lanes' copies have landed.  Only the
-    // producer waits while the load queue is full; the compute warps work on
-    // the items already there.  Item n goes to slot n % NS once its previous
+    // The producer warp copies the weight rows of an item with bulk (TMA)
+    // copies, counted in bytes on the slot's full barrier, and the small
+    // scale/bias slices with 16-byte cp.async pieces spread over its 32 lanes,
+    // each lane arriving (noinc) once its pieces land; the barrier fires when
+    // both are complete.  Only the producer waits on the copy engines; the
+    // compute warps work on the items already there.  Item n goes to slot n % NS once its previous
     // occupant has been released by all compute warps.
     if (warp == kProdWarp) {
         uint32_t pit = 0;  // items issued
@@ -370,12 +381,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
             for (uint32_t o = static_cast<uint32_t>(lane) * 16u; o < bytes; o += 32u * 16u)
                 cp_async_16(dst + o, static_cast<const uint8_t *>(src) + o);
         };
-        // waits for a free slot; returns it, or -1 when giving up
-        auto begin_item = [&]() -> int {
+        // waits for a free slot and announces the item's bulk-copy bytes;
+        // returns the slot, or -1 when giving up
+        auto begin_item = [&](uint32_t bulk_bytes) -> int {
             if (!pok) return -1;
             const int slot = static_cast<int>(pit % NS);
             int ok = 1;
-            if (lane == 0) ok = wait_bar(&S.empty[slot], ((pit / NS) & 1) ^ 1, wt);
+            if (lane == 0) {
+                ok = wait_bar(&S.empty[slot], ((pit / NS) & 1) ^ 1, wt);
+                if (ok) mbar_arrive_expect_tx(&S.full[slot], bulk_bytes);
+            }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) pok = false;
             return ok ? slot : -1;
@@ -386,13 +401,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         };
         // gate/up task j of expert e (e < 0: the shared expert)
         auto issue_gu = [&](const DecodeLayerPtrs &W, int j, int e) {
-            const int slot = begin_item();
+            const int slot = begin_item(8u * d);
             if (slot < 0) return;
             uint8_t *base = ring + static_cast<size_t>(slot) * SB;
             const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * I) + static_cast<size_t>(j % P.nu_gu) * kGURows;
             const size_t ng = d / 64;
-            copy_seg(base, (e < 0 ? W.sh_gate_q : W.gate_q) + r0 * (d / 2), 4u * d);
-            copy_seg(base + 4 * d, (e < 0 ? W.sh_up_q : W.up_q) + r0 * (d / 2), 4u * d);
+            // rows: two bulk copies; scale/bias slices: cp.async pieces
+            if (lane == 0) bulk_g2s(base, (e < 0 ? W.sh_gate_q : W.gate_q) + r0 * (d / 2), 4u * d, &S.full[slot]);
+            if (lane == 1) bulk_g2s(base + 4 * d, (e < 0 ? W.sh_up_q : W.up_q) + r0 * (d / 2), 4u * d, &S.full[slot]);
             copy_seg(base + 8 * d, (e < 0 ? W.sh_gate_s : W.gate_s) + r0 * ng, d / 4);
             copy_seg(base + 8 * d + d / 4, (e < 0 ? W.sh_gate_b : W.gate_b) + r0 * ng, d / 4);
             copy_seg(base + 8 * d + d / 2, (e < 0 ? W.sh_up_s : W.up_s) + r0 * ng, d / 4);
@@ -401,7 +417,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         };
         // units [u0, u1) of down task k: 16 rows of Wd of each unit's expert
         auto issue_down = [&](const DecodeLayerPtrs &W, int k, int u0, int u1) {
-            const int slot = begin_item();
+            const int slot = begin_item(8u * I * (u1 - u0));
             if (slot < 0) return;
             uint8_t *base = ring + static_cast<size_t>(slot) * SB;
             const size_t j0 = static_cast<size_t>(P.c + k * P.G) * kDownRows;
@@ -410,7 +426,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
                 const int e = S.unit_e[u0 + i];
                 const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * d) + j0;
                 uint8_t *ub = base + static_cast<size_t>(i) * 9 * I;
-                copy_seg(ub, (e < 0 ? W.sh_down_q : W.down_q) + r0 * (I / 2), 8u * I);
+                if (lane == i) bulk_g2s(ub, (e < 0 ? W.sh_down_q : W.down_q) + r0 * (I / 2), 8u * I, &S.full[slot]);
                 copy_seg(ub + 8 * I, (e < 0 ? W.sh_down_s : W.down_s) + r0 * ng, I / 2);
                 copy_seg(ub + 8 * I + I / 2, (e < 0 ? W.sh_down_b : W.down_b) + r0 * ng, I / 2);
             }
@@ -419,12 +435,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         for (int li = 0; li < a.n_layers; ++li) {
             const DecodeLayerPtrs &W = a.L[li];
             {
-                const int slot = begin_item();
+                const int slot = begin_item(2u * d * P.n_rrows);
                 if (slot >= 0) {
                     uint8_t *base = ring + static_cast<size_t>(slot) * SB;
-                    for (int r = 0; r < P.n_rrows; ++r)
-                        copy_seg(base + static_cast<size_t>(r) * 2 * d,
-                                 W.router_w + static_cast<size_t>(P.c + r * P.G) * d, 2u * d);
+                    if (lane < P.n_rrows)
+                        bulk_g2s(base + static_cast<size_t>(lane) * 2 * d,
+                                 W.router_w + static_cast<size_t>(P.c + lane * P.G) * d, 2u * d, &S.full[slot]);
                     end_item(slot);
                 }
             }
