@@ -5,10 +5,9 @@ objects are linked into one shared library under ``_build/``.  The build is
 skipped when the library is newer than every source and header.
 
 Besides the product library there is one test-only variant,
-``liblily_moe_stalltest.so``, built from the same sources with three macros: the
-pipeline waits give up after 1 ms instead of 2 s; for T == 77 the grouped
-GEMM's epilogue first waits on a barrier that nothing completes, and in a
-7-layer decode call one CTA never publishes its layer-3 router logits.  The
+``liblily_moe_stalltest.so``, built from the same sources with two macros: the
+pipeline waits of the grouped GEMM give up after 1 ms instead of 2 s, and for
+T == 77 the epilogue first waits on a barrier that nothing completes.  The
 failure-path tests use it to make a bounded wait run out on purpose and check
 that the kernel reports LILY_ERR_DEVICE_TIMEOUT, drains its in-flight work and
 leaves the GPU usable.  The product library is never built with these macros.
@@ -31,12 +30,10 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 # variant name -> (library file, extra nvcc flags)
 STALL_TEST_T = 77
-STALL_TEST_DECODE_LAYERS = 7
 VARIANTS: Dict[str, tuple] = {
     "product": ("liblily_moe.so", []),
     "stalltest": ("liblily_moe_stalltest.so",
-                  ["-DLILY_WAIT_LIMIT_NS=1000000ull", f"-DLILY_TEST_STALL_T={STALL_TEST_T}",
-                   f"-DLILY_TEST_STALL_DECODE_LAYERS={STALL_TEST_DECODE_LAYERS}"]),
+                  ["-DLILY_WAIT_LIMIT_NS=1000000ull", f"-DLILY_TEST_STALL_T={STALL_TEST_T}"]),
 }
 
 

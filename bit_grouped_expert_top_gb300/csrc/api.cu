@@ -20,6 +20,7 @@ unsigned long long current_context_id();
 }  // namespace
 
 namespace lily {
+cudaError_t launch_decode_final_norm(const float *prev_out, uint16_t *x_export, int T, int d, cudaStream_t stream);
 
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes)
 {
@@ -46,7 +47,8 @@ constexpr int kVersion = 10100;  // 1.1.0
 
 // Unique id of the CUDA context current on this thread (the runtime's primary
 // context of the current device), 0 if none is current yet.  Caches of
-// per-context state (symbol addresses, kernel attributes) are keyed by it:
+// per-context state (symbol addresses, kernel attributes, instantiated graphs)
+// are keyed by it:
 // after cudaDeviceReset the device gets a new context with a new id, so no
 // entry made in the old context is used again.
 // The two driver calls are looked up through the runtime (the library does
@@ -123,17 +125,14 @@ PrefillLayout prefill_layout(const lily_moe_shape &s)
     return L;
 }
 
-// Decode: the control block, the part every call zeroes before its first
-// launch (the global abort flag and one set of ready counters per layer), then
-// the buffers through which the CTAs hand logits, h' and outputs to each other.
 struct DecodeLayout {
-    size_t ctrl, abort_flag, ready, ready_end, logits_x, h_x, out_x, total;
+    size_t ctrl, x_cur, xp, logits, n_units, unit_expert, unit_mask, unit_w, h, total;
 };
 
-DecodeLayout decode_layout(const lily_moe_shape &s, int64_t n_layers)
+DecodeLayout decode_layout(const lily_moe_shape &s)
 {
     DecodeLayout L{};
-    const int64_t T = s.T;
+    const int64_t T = s.T, U = static_cast<int64_t>(s.top_k) * s.T + 1;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t at = off;
@@ -141,22 +140,16 @@ DecodeLayout decode_layout(const lily_moe_shape &s, int64_t n_layers)
         return at;
     };
     L.ctrl = take(sizeof(Ctrl));
-    L.abort_flag = take(4);
-    L.ready = take(std::max<int64_t>(n_layers, 1) * kDecodeReadySlots * 4);
-    L.ready_end = off;
-    L.logits_x = take(2 * T * s.E * 4);
-    L.h_x = take(2 * static_cast<int64_t>(kDecodeMaxUnits) * (s.I / 128) * T * 64 * 4);
-    L.out_x = take(2 * T * s.d * 4);
+    L.x_cur = take(T * s.d * 2);
+    L.xp = take(8 * s.d * 2);  // fp16 layer input, 8 token columns, permuted for the tensor-core GEMV
+    L.logits = take(T * s.E * 4);
+    L.n_units = take(4);
+    L.unit_expert = take(U * 4);
+    L.unit_mask = take(U * 4);
+    L.unit_w = take(U * 8 * 4);
+    L.h = take(U * 8 * s.I * 2);
     L.total = off;
     return L;
-}
-
-// Shapes the decode kernel runs: 1 <= T <= 8, d <= 4096, I <= 1024, T * d <=
-// 16384 (its shared memory then holds the inputs and at least three ring slots).
-bool decode_shape_ok(const lily_moe_shape &s)
-{
-    return s.T >= 1 && s.T <= kDecodeMaxT && s.d <= 4096 && s.I <= 1024 && s.T * s.d <= 16384 &&
-           decode_ring_slots(s.T, s.d, s.I) > 0;
 }
 
 template <typename P>
@@ -457,6 +450,17 @@ int to_status(cudaError_t e, const char *what = "launch")
     return e == cudaSuccess ? LILY_OK : cuda_fail(e, what);
 }
 
+// ------------------------------------------------------------------ decode graph cache
+struct GraphCache {
+    std::mutex mu;
+    std::unordered_map<std::string, cudaGraphExec_t> execs;
+};
+GraphCache &graph_cache()
+{
+    static GraphCache *c = new GraphCache();  // never destroyed: graphs live until process exit
+    return *c;
+}
+
 }  // namespace
 
 // Fixed scratch of lily_moe_route_noalloc.  Every GPU that loads the library
@@ -524,8 +528,8 @@ size_t lily_moe_workspace_bytes(const lily_moe_shape *shape, int32_t n_layers_de
     if (check_shape(shape) != LILY_OK) return 0;
     size_t need = prefill_layout(*shape).total;
     if (n_layers_decode > 0) {
-        if (!decode_shape_ok(*shape)) return 0;
-        need = std::max(need, decode_layout(*shape, n_layers_decode).total);
+        if (shape->T < 1 || shape->T > 8 || shape->d > 4096 || shape->I > 1024) return 0;
+        need = std::max(need, decode_layout(*shape).total);
     }
     return need;
 }
@@ -586,10 +590,10 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
     int rc;
     if ((rc = check_shape(shape))) return rc;
     if (n_layers < 1 || !layers) return LILY_ERR_INVALID;
-    if (!decode_shape_ok(*shape)) return LILY_ERR_UNSUPPORTED;
+    if (shape->T < 1 || shape->T > 8 || shape->d > 4096 || shape->I > 1024) return LILY_ERR_UNSUPPORTED;
     for (int l = 0; l < n_layers; ++l)
         if ((rc = check_weights(&layers[l]))) return rc;
-    if ((rc = check_ws(ws, ws_bytes, decode_layout(*shape, n_layers).total))) return rc;
+    if ((rc = check_ws(ws, ws_bytes, decode_layout(*shape).total))) return rc;
     if ((rc = check_ptr(x)) || (rc = check_ptr(out))) return rc;
     if (x_next && !aligned16(x_next)) return LILY_ERR_MISALIGNED;
     if (trace && ((trace->logits && !aligned16(trace->logits)) || (trace->topk_idx && !aligned16(trace->topk_idx)) ||
@@ -597,52 +601,97 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
         return LILY_ERR_MISALIGNED;
 
     const lily_moe_shape s = *shape;
-    const DecodeLayout L = decode_layout(s, n_layers);
-    // one CTA per SM; every CTA owns at most two router rows and two down tasks
-    const int grid = num_sms_current();
-    if (grid * 2 < s.E || grid * 2 * 16 < s.d) return LILY_ERR_UNSUPPORTED;
+    const DecodeLayout L = decode_layout(s);
+    const int sms = num_sms_current();
+    const size_t td = static_cast<size_t>(s.T) * s.d;
 
-    DecodeArgs a{};
-    a.T = s.T; a.d = s.d; a.E = s.E; a.top_k = s.top_k; a.I = s.I;
-    a.n_slots = decode_launch_slots(s.T, s.d, s.I);
-    if (a.n_slots == 0) return LILY_ERR_UNSUPPORTED;
-    a.slot_bytes = decode_slot_bytes(s.d, s.I);
-    a.x_in = x;
-    a.out = out;
-    a.x_next = x_next;
-    if (trace) {
-        a.trace_logits = trace->logits;
-        a.trace_idx = trace->topk_idx;
-        a.trace_w = trace->topk_w;
-    }
-    a.logits_x = at<float>(ws, L.logits_x);
-    a.h_x = at<uint32_t>(ws, L.h_x);
-    a.out_x = at<float>(ws, L.out_x);
-    a.ready = at<unsigned int>(ws, L.ready);
-    a.abort_flag = at<int>(ws, L.abort_flag);
-    a.ctrl = at<Ctrl>(ws, L.ctrl);
-
-    // every call starts with a lowered abort flag and zero ready counters
-    cudaError_t e = cudaMemsetAsync(at<uint8_t>(ws, L.abort_flag), 0, L.ready_end - L.abort_flag, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (decode ready counters)");
-    for (int l0 = 0; l0 < n_layers; l0 += kDecodeLayersPerLaunch) {
-        a.layer0 = l0;
-        a.n_layers = std::min(kDecodeLayersPerLaunch, n_layers - l0);
-        a.last_launch = l0 + a.n_layers == n_layers;
-        for (int i = 0; i < a.n_layers; ++i) {
-            const lily_moe_weights &w = layers[l0 + i];
-            DecodeLayerPtrs &p = a.L[i];
-            p.router_w = w.router_w; p.router_bias = w.router_bias;
-            p.gate_q = w.gate.q; p.up_q = w.up.q; p.down_q = w.down.q;
-            p.gate_s = w.gate.scale; p.gate_b = w.gate.bias; p.up_s = w.up.scale; p.up_b = w.up.bias;
-            p.down_s = w.down.scale; p.down_b = w.down.bias;
-            p.sh_gate_q = w.sh_gate.q; p.sh_up_q = w.sh_up.q; p.sh_down_q = w.sh_down.q;
-            p.sh_gate_s = w.sh_gate.scale; p.sh_gate_b = w.sh_gate.bias; p.sh_up_s = w.sh_up.scale;
-            p.sh_up_b = w.sh_up.bias; p.sh_down_s = w.sh_down.scale; p.sh_down_b = w.sh_down.bias;
+    auto enqueue_all = [&](cudaStream_t st) -> cudaError_t {
+        Ctrl *ctrl = at<Ctrl>(ws, L.ctrl);
+        cudaError_t e = cudaMemsetAsync(&ctrl->ticket2, 0, sizeof(unsigned int), st);
+        if (e != cudaSuccess) return e;
+        for (int l = 0; l < n_layers; ++l) {
+            const lily_moe_weights &w = layers[l];
+            DecodeLayerArgs a{};
+            a.T = s.T; a.d = s.d; a.E = s.E; a.top_k = s.top_k; a.I = s.I; a.layer = l;
+            a.router_w = w.router_w; a.router_bias = w.router_bias;
+            a.gate_q = w.gate.q; a.up_q = w.up.q; a.down_q = w.down.q;
+            a.gate_s = w.gate.scale; a.gate_b = w.gate.bias; a.up_s = w.up.scale; a.up_b = w.up.bias;
+            a.down_s = w.down.scale; a.down_b = w.down.bias;
+            a.sh_gate_q = w.sh_gate.q; a.sh_up_q = w.sh_up.q; a.sh_down_q = w.sh_down.q;
+            a.sh_gate_s = w.sh_gate.scale; a.sh_gate_b = w.sh_gate.bias; a.sh_up_s = w.sh_up.scale;
+            a.sh_up_b = w.sh_up.bias; a.sh_down_s = w.sh_down.scale; a.sh_down_b = w.sh_down.bias;
+            a.x_in = l == 0 ? x : nullptr;
+            a.prev_out = l == 0 ? nullptr : out + (l - 1) * td;
+            a.out = out + l * td;
+            a.x_export = (l > 0 && x_next) ? x_next + (l - 1) * td : nullptr;
+            if (trace) {
+                a.trace_logits = trace->logits ? trace->logits + static_cast<size_t>(l) * s.T * s.E : nullptr;
+                a.trace_idx = trace->topk_idx ? trace->topk_idx + static_cast<size_t>(l) * s.T * s.top_k : nullptr;
+                a.trace_w = trace->topk_w ? trace->topk_w + static_cast<size_t>(l) * s.T * s.top_k : nullptr;
+            }
+            a.x_cur = at<uint16_t>(ws, L.x_cur);
+            a.xp = at<__half>(ws, L.xp);
+            a.logits = at<float>(ws, L.logits);
+            a.n_units = at<int>(ws, L.n_units);
+            a.unit_expert = at<int>(ws, L.unit_expert);
+            a.unit_mask = at<int>(ws, L.unit_mask);
+            a.unit_w = at<float>(ws, L.unit_w);
+            a.h = at<__half>(ws, L.h);
+            a.ctrl = ctrl;
+            if ((e = launch_decode_layer(a, sms, st)) != cudaSuccess) return e;
         }
-        if ((e = launch_decode(a, grid, stream)) != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+        if (x_next)
+            return launch_decode_final_norm(out + (n_layers - 1) * td, x_next + (n_layers - 1) * td, s.T, s.d, st);
+        return cudaSuccess;
+    };
+
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t ce = cudaStreamIsCapturing(stream, &cs);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone) return to_status(enqueue_all(stream), "decode launch (capturing stream)");
+
+    // Key: every argument value that the recorded launches depend on.
+    std::string key;
+    auto put = [&key](const void *p, size_t n) { key.append(static_cast<const char *>(p), n); };
+    int dev = 0;
+    cudaGetDevice(&dev);
+    put(&dev, sizeof dev);
+    // the context the graph was instantiated in (a reset device gets a new one)
+    const unsigned long long ctx_id = current_context_id();
+    put(&ctx_id, sizeof ctx_id);
+    put(&s, sizeof s);
+    put(&n_layers, sizeof n_layers);
+    put(layers, sizeof(lily_moe_weights) * n_layers);
+    put(&x, sizeof x); put(&out, sizeof out); put(&x_next, sizeof x_next); put(&ws, sizeof ws);
+    const lily_moe_decode_trace tr = trace ? *trace : lily_moe_decode_trace{};
+    put(&tr, sizeof tr);
+
+    GraphCache &gc = graph_cache();
+    std::lock_guard<std::mutex> lock(gc.mu);
+    auto it = gc.execs.find(key);
+    if (it == gc.execs.end()) {
+        cudaStream_t cap;
+        if ((ce = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(ce, "cudaStreamCreateWithFlags");
+        cudaGraph_t graph = nullptr;
+        cudaError_t e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+        if (e == cudaSuccess) {
+            const cudaError_t e1 = enqueue_all(cap);
+            const cudaError_t e2 = cudaStreamEndCapture(cap, &graph);
+            e = e1 != cudaSuccess ? e1 : e2;
+        }
+        cudaGraphExec_t exec = nullptr;
+        if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+        if (graph) cudaGraphDestroy(graph);
+        cudaStreamDestroy(cap);
+        if (e != cudaSuccess) return cuda_fail(e, "decode graph capture / instantiate");
+        if (gc.execs.size() >= 64) {
+            for (auto &kv : gc.execs) cudaGraphExecDestroy(kv.second);
+            gc.execs.clear();
+        }
+        it = gc.execs.emplace(key, exec).first;
     }
-    return LILY_OK;
+    return to_status(cudaGraphLaunch(it->second, stream), "cudaGraphLaunch (decode)");
 }
 
 int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,

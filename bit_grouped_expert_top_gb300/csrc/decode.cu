@@ -1,62 +1,27 @@
-// Decode path of the MoE layer for 1..8 tokens: one persistent kernel runs the
-// whole chain of layers.
+// Decode path of the MoE layer for 1..8 tokens: fused dequant-GEMVs.
 //
 // Method (page "Perplexity libera o Lily", noticiai.com.br, section "Prefill e
 // decode: onde estao os ganhos"): at batch 1 there is almost no weight reuse,
-// so memory bandwidth sets the ceiling.  Only the bytes of the selected experts
-// (plus the shared expert and the router) are read, each exactly once, with
-// coalesced bulk copies, dequantised in registers (weights rounded once to
-// fp16, as in the prefill path) and multiplied with fp32 accumulation.  The
-// page's decode step overlaps its kernels by tracking the real dependencies
-// between them; here those dependencies are carried by data inside one
-// resident kernel instead of kernel boundaries.
+// so memory bandwidth sets the ceiling.  Only the bytes of the selected
+// experts (plus the shared expert and the router) are read, each exactly once,
+// with 16-byte coalesced loads, dequantised in registers (weights rounded once
+// to fp16, as in the prefill path) and accumulated in fp32.
 //
-// GB300 design.  One CTA per SM (a cooperative launch, so every CTA is
-// resident), 8 compute warps and 1 producer warp.  Per layer l, every CTA:
-//   A  builds the layer input x_l in shared memory (layer 0: x; later layers:
-//      bf16 of the previous output over sqrt(mean(out^2) + 1e-6), the
-//      parameter-free RMS norm that links layers), reading the previous
-//      layer's output words from the exchange area;
-//   -  computes its one or two router rows (logit of expert c and c + G) and
-//      publishes them;
-//   B  reads all 256 x T logits, selects the top 8 per token (lower index first
-//      among equal logits) and builds the list of distinct experts ("units":
-//      the shared expert is unit 0 with weight 1); computes its shared-expert
-//      gate/up rows (if any) while the routed experts' bytes load;
-//   -  gate/up tasks (unit, 8 rows of I): tensor-core GEMV (mma.sync m16n8k16,
-//      the tokens as the 8 columns, gate rows and up rows as the two 8-row
-//      halves of the tile), SwiGLU in registers, scaled by the unit's routing
-//      weight, published as fp16 h';
-//   C  down tasks (16 output rows): the sum over all units of Wd_u h'_u in one
-//      fragment (deterministic), published as the layer output.
-// Data moves between CTAs through workspace buffers (double buffered by layer
-// parity) and per-layer ready counters: a writer stores its part, then one
-// thread adds 1 to the counter with release semantics; one thread of each
-// reading CTA polls that one counter with acquire loads until every writer has
-// signalled, and the CTA then reads the data from L2.  No grid-wide barrier is
-// involved, and the polling touches one word per CTA (polling the data itself,
-// with every CTA spinning on the same lines, queued up at the L2 slices).  The
-// counters are per layer and zeroed at the start of every call.
-//
-// Every weight a CTA needs streams through a ring of shared-memory slots.  A
-// producer warp copies the weight rows of each item with bulk (TMA) copies
-// (2 KB to 8 KB each) and the 256-512 byte scale/bias slices as 16-byte
-// cp.async pieces from its 32 lanes; the compute warps release a slot after
-// reading it.  (One SM's TMA unit takes 30-50 ns to start each bulk copy
-// whatever its size, so the small slices, four per gate/up task and two per
-// down unit, go through the load/store units instead; and with the compute
-// warps issuing cp.async themselves they stalled on the full load queue
-// instead of working on the items already there.)
-// Items that do not depend on the routing (the router rows and the shared
-// expert's gate/up rows) of layer l + 1 are issued as soon as the slots of
-// layer l free up, so they load while layer l finishes; the routed experts'
-// gate/up rows and then the down rows of all units are issued the moment the
-// top-8 is known.
-//
-// Every wait (mbarrier or ready counter) is bounded; a wait that runs out
-// records LILY_ERR_DEVICE_TIMEOUT, raises a global abort flag that the other
-// CTAs see, and every CTA leaves its layer loop at the next top-8 point and
-// waits for its own copies in flight before it exits.
+// Three kernels per layer:
+//   dec_route_kernel  : builds the layer input (layer 0: x; later layers: the
+//                       parameter-free RMS norm of the previous output, rounded
+//                       to bf16) and the router GEMV (one warp per expert).
+//   dec_gateup_kernel : every CTA computes the top-8 selection per token from
+//                       the logits and the list of distinct experts ("units")
+//                       with per-token weights (the shared expert is unit 0
+//                       with weight 1); then a tensor-core GEMV (mma.sync
+//                       m16n8k16, the tokens as the 8 columns): per unit and 32
+//                       rows of I, gate and up dequantised in registers, SwiGLU,
+//                       scaled by the unit's routing weight per token, h' stored
+//                       as fp16.
+//   dec_down_kernel   : tensor-core GEMV over K = units x I: per 16 output
+//                       rows, sum over the units of Wd h' (deterministic, no
+//                       atomics).
 #include <algorithm>
 
 #include "lily_device.cuh"
@@ -65,132 +30,24 @@
 namespace lily {
 namespace {
 
-constexpr int kMaxT = kDecodeMaxT;
-constexpr int kMaxUnits = kDecodeMaxUnits;
-constexpr int kCW = 8;                        // compute warps
-constexpr int kDecThreads = (kCW + 1) * 32;   // + the producer warp
-constexpr int kProdWarp = kCW;
-constexpr int kComputeThreads = kCW * 32;
-constexpr int kKB = 128;                      // K block of one lane pass (16 bytes of int4 per row)
-constexpr int kGURows = 8;                    // I rows of one gate/up task
-constexpr int kDownRows = 16;                 // output rows of one down task
-constexpr int kMaxSlots = 16;
-constexpr int kSmemLimit = 232448;            // 227 KB of dynamic shared memory per CTA
-constexpr int kBarTop8 = 1, kBarCompute = 2;  // named barriers (0 is __syncthreads)
-
-struct DecSmem {
-    uint64_t full[kMaxSlots], empty[kMaxSlots];  // ring slot landed / free again
-    int abort;                    // this CTA gives up (set by any failed wait)
-    int decide;                   // the abort decision taken at the top-8 point
-    int n_units;
-    int unit_e[kMaxUnits];        // expert of unit u (-1: shared)
-    float unit_w[kMaxUnits][kMaxT];
-    int umask[256];               // tokens that selected expert e (bit n)
-    int sel_e[kMaxT][8];          // the top-8 of each token and their weights
-    float sel_w[kMaxT][8];
-    int scan_tmp[kCW];
-    float inv_rms[kMaxT];
-    float rred[kCW][2][kMaxT];
-    float sred[kCW][kMaxT];
-    uint2 zeros[8];
-    float red[2][kCW][32][4];     // cross-warp sums of mma fragments, double buffered
-};
-
-__host__ __device__ constexpr size_t align128(size_t v) { return (v + 127) / 128 * 128; }
-constexpr size_t kStaticBytes = align128(sizeof(DecSmem));
-
-// Bytes of one ring slot: a gate/up task (8 rows of gate and up, K = d, with
-// scales and biases) = 9d, or one unit of a down task (16 rows, K = I) = 9I.
-__host__ __device__ inline size_t slot_bytes_of(int d, int I)
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kMaxT = 8;
+// Read-only loads issued as volatile asm, so that the compiler keeps them where
+// they are written (a plain read-only load may be moved past pdl_wait to its
+// first use, which would undo a prefetch meant to overlap the previous grid).
+__device__ __forceinline__ uint4 ld_early(const void *p)
 {
-    return align128(static_cast<size_t>(9) * (d > I ? d : I));
-}
-// Staged h' of one down item: units per item (slot / 9I) x I/128 K blocks x T
-// tokens x 64 payload words of 4 bytes.
-__host__ __device__ inline size_t stage_bytes(int T, int d, int I)
-{
-    const size_t upc = slot_bytes_of(d, I) / (static_cast<size_t>(9) * I);
-    return align128(upc * (I / 128) * T * 64 * 4);
-}
-
-// ---------------------------------------------------------------- memory helpers
-
-// Bulk (TMA) copy global -> shared, completion counted on `bar` in bytes.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-// Ready counters: release add by the writer, acquire load by the reader.
-__device__ __forceinline__ void signal_ready(unsigned int *p)
-{
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
-}
-__device__ __forceinline__ unsigned int ld_acquire(const unsigned int *p)
-{
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
-__device__ __forceinline__ int ld_flag(const int *p)
+__device__ __forceinline__ uint16_t ld_early_u16(const uint16_t *p)
 {
-    int v;
-    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    uint16_t v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
 }
-__device__ __forceinline__ void st_flag(int *p, int v)
-{
-    asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-struct Waiter {
-    volatile int *s_abort;
-    int *g_abort;
-    int *status;
-};
-
-__device__ __forceinline__ void raise_abort(const Waiter &w)
-{
-    *w.s_abort = 1;
-    st_flag(w.g_abort, 1);
-}
-
-// Waits (one thread) until the counter reaches `target`; bounded, gives up on
-// an abort raised in this CTA or by another one.
-__device__ __forceinline__ bool wait_ready(const unsigned int *p, unsigned int target, const Waiter &w)
-{
-    uint64_t t0 = 0;
-#pragma unroll 1
-    for (int iter = 0;; ++iter) {
-        if (ld_acquire(p) >= target) return true;
-        if (*w.s_abort) return false;
-        if ((iter & 15) == 15 && ld_flag(w.g_abort)) {
-            *w.s_abort = 1;
-            return false;
-        }
-        const uint64_t now = global_timer_ns();
-        if (t0 == 0) {
-            t0 = now;
-        } else if (now - t0 > LILY_WAIT_LIMIT_NS) {
-            record_error(w.status, kErrDeviceTimeout);
-            raise_abort(w);
-            return false;
-        }
-    }
-}
-
-// mbarrier wait (bounded; a failure also raises the global abort flag).
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, const Waiter &w)
-{
-    if (mbar_wait(bar, parity, w.s_abort, w.status)) return true;
-    raise_abort(w);
-    return false;
-}
-
-__device__ __forceinline__ uint4 lds128(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
 
 // acc + dot of 8 bf16 weights with 8 bf16 activations (fp32).
 __device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x, float acc)
@@ -213,20 +70,164 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-__device__ __forceinline__ void compute_sync() { named_barrier_sync(kBarCompute, kComputeThreads); }
-
-// ---------------------------------------------------------------- tensor-core GEMV
+// ---------------------------------------------------------------- tensor-core GEMVs
 // The expert GEMVs run on mma.sync m16n8k16 (f16 x f16 -> f32): 16 weight rows
 // x 16 K x 8 token columns per instruction (tokens >= T are zero columns), so a
 // weight is dequantised once for all tokens.  Lane (g = lane / 4, t = lane % 4)
-// reads 16 bytes (32 weights) of rows g and g + 8 for each 128-wide K block:
+// loads 16 bytes (32 weights) of rows g and g + 8 for each 128-wide K block:
 // weights [32 t, 32 t + 32) of the block.  The K order inside the block is
 // permuted so that these weights are exactly this lane's A-fragment entries:
 // within 32-bit word w (weights 8w..8w+7, rebuilt in pairs (0,2) (4,6) (1,3)
-// (5,7) by dequant8_f16_e2m3), weight e goes to slice 2w + (e & 1), entry
-// e >> 1 of the lane's four K positions.  The B operand (x, or h' for the down
-// projection) is stored in the same permuted order, so each lane reads its B
-// fragment of a slice as one 8-byte value: layout [K block][token][t][slice][4].
+// (5,7) by dequant8_f16_e2m3), weight e goes to slice 2w + (e & 1), entry e >> 1
+// of the lane's four K positions.  The B operand
+// (x, or h for the down projection) is stored in the same permuted order, so
+// each lane reads its B fragment with one 8-byte load.
+constexpr int kKB = 128;  // K block
+
+// Position of element k (of a K range starting at 0) in the permuted B layout
+// [kb][n][t][s][4] for token column n of 8.
+__device__ __forceinline__ int perm_b_index(int k, int n)
+{
+    const int kb = k >> 7, r = k & 127, t = r >> 5, w = (r & 31) >> 3, e = r & 7;
+    const int s = 2 * w + (e & 1), idx = e >> 1;
+    return (((kb * 8 + n) * 4 + t) * 8 + s) * 4 + idx;
+}
+
+__global__ void __launch_bounds__(kDecThreads)
+dec_route_kernel(const DecodeLayerArgs a)
+{
+    extern __shared__ __align__(16) uint8_t dsm[];
+    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(dsm);  // [T][d] plain layout
+    __shared__ float red[kDecWarps][kMaxT];
+    __shared__ float inv_rms[kMaxT];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int T = a.T, d = a.d;
+    const int e = blockIdx.x * kDecWarps + warp;  // this warp's expert
+    const uint4 *wrow = reinterpret_cast<const uint4 *>(a.router_w + static_cast<size_t>(e < a.E ? e : 0) * d);
+    const int n8 = d / 8;  // 16-byte chunks of a router row
+
+    // The router row does not depend on the layer input: start its loads first.
+    constexpr int kPre = 8;
+    uint4 wpre[kPre];
+#pragma unroll
+    for (int m = 0; m < kPre; ++m) {
+        const int c = lane + 32 * m;
+        if (e < a.E && c < n8) wpre[m] = ld_early(wrow + c);
+    }
+
+    pdl_trigger();
+    pdl_wait();  // the previous layer's output (and this call's buffers) are ready
+
+    // ---- layer input
+    if (a.prev_out == nullptr) {
+        for (int i = threadIdx.x; i < T * d / 8; i += kDecThreads)
+            reinterpret_cast<uint4 *>(xs)[i] = reinterpret_cast<const uint4 *>(a.x_in)[i];
+    } else {
+        // two passes over the previous output, each with all of a thread's loads in
+        // flight at once (d <= 4096: at most 4 float4 per thread and token)
+        const int d4 = d / 4;
+        const float4 *po = reinterpret_cast<const float4 *>(a.prev_out);
+#pragma unroll 4
+        for (int t = 0; t < T; ++t) {  // up to four tokens' loads in flight together
+            float ss = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = threadIdx.x + j * kDecThreads;
+                if (c < d4) {
+                    const float4 v = __ldcg(po + static_cast<size_t>(t) * d4 + c);
+                    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+                }
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) red[warp][t] = ss;
+        }
+        __syncthreads();
+        if (threadIdx.x < T) {
+            float s = 0.0f;
+            for (int w = 0; w < kDecWarps; ++w) s += red[w][threadIdx.x];
+            inv_rms[threadIdx.x] = 1.0f / sqrtf(s / static_cast<float>(d) + 1e-6f);
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int t = 0; t < T; ++t) {
+            const float r = inv_rms[t];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = threadIdx.x + j * kDecThreads;
+                if (c < d4) {
+                    const float4 v = __ldcg(po + static_cast<size_t>(t) * d4 + c);
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * r, v.y * r), hi = __floats2bfloat162_rn(v.z * r, v.w * r);
+                    uint2 o;
+                    o.x = *reinterpret_cast<const uint32_t *>(&lo);
+                    o.y = *reinterpret_cast<const uint32_t *>(&hi);
+                    *reinterpret_cast<uint2 *>(xs + static_cast<size_t>(t) * d + 4 * c) = o;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < T * d / 8; i += kDecThreads) {
+            const uint4 v = reinterpret_cast<const uint4 *>(xs)[i];
+            reinterpret_cast<uint4 *>(a.x_cur)[i] = v;
+            if (a.x_export) reinterpret_cast<uint4 *>(a.x_export)[i] = v;
+        }
+    }
+    {
+        // fp16 copy in the permuted B layout of the expert GEMVs (8 token columns),
+        // split over the CTAs: the 8 elements of one 32-bit weight word land as
+        // 16 contiguous bytes (x0 x2 x4 x6 | x1 x3 x5 x7)
+        const int wpt = d / 8;  // words per token
+        const int per = (8 * wpt + gridDim.x - 1) / gridDim.x;
+        for (int q = blockIdx.x * per + threadIdx.x; q < min(8 * wpt, (blockIdx.x + 1) * per); q += kDecThreads) {
+            const int n = q / wpt, k0 = (q - n * wpt) * 8;
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+            if (n < T) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(xs + static_cast<size_t>(n) * d + k0);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 p2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
+                    f[2 * j] = p2.x;
+                    f[2 * j + 1] = p2.y;
+                }
+                const __half2 h0 = __floats2half2_rn(f[0], f[2]), h1 = __floats2half2_rn(f[4], f[6]);
+                const __half2 h2 = __floats2half2_rn(f[1], f[3]), h3 = __floats2half2_rn(f[5], f[7]);
+                o = make_uint4(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1),
+                               *reinterpret_cast<const uint32_t *>(&h2), *reinterpret_cast<const uint32_t *>(&h3));
+                if (f16x2_has_inf(o.x) | f16x2_has_inf(o.y) | f16x2_has_inf(o.z) | f16x2_has_inf(o.w))
+                    record_error(&a.ctrl->status, kErrDeviceRange);
+            }
+            *reinterpret_cast<uint4 *>(a.xp + perm_b_index(k0, n)) = o;
+        }
+    }
+
+    // ---- router GEMV: one warp per expert
+    if (e < a.E) {
+        // compact code (one token per loop trip): this kernel runs once per layer,
+        // so its instructions are fetched cold and unrolled copies cost fetch time
+        const float bias = a.router_bias ? a.router_bias[e] : 0.0f;
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            const uint4 *xrow = reinterpret_cast<const uint4 *>(xs + static_cast<size_t>(t) * d);
+            float acc = 0.0f;
+#pragma unroll
+            for (int m = 0; m < kPre; ++m) {
+                const int c = lane + 32 * m;
+                if (c < n8) acc = dot8_bf16(wpre[m], xrow[c], acc);
+            }
+#pragma unroll 1
+            for (int c = lane + 32 * kPre; c < n8; c += 32) acc = dot8_bf16(__ldg(wrow + c), xrow[c], acc);
+            const float sum = warp_sum(acc) + bias;
+            if (lane == 0) {
+                a.logits[t * a.E + e] = sum;
+                if (a.trace_logits) a.trace_logits[t * a.E + e] = sum;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
     asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -237,9 +238,10 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 
 // One 128-wide K block of a 16-row tile: q_g / q_g8 hold this lane's 16 bytes of
 // rows g and g + 8, sb_g / sb_g8 the bf16 scale (low half) and bias (high
-// half) of its group; b holds the lane's B fragments of the block (8 slices).
+// half) of its group; b points at the lane's B fragments of the block
+// (8 slices x 4 fp16, consecutive).
 __device__ __forceinline__ void mma_kblock(float (&d)[4], uint4 q_g, uint4 q_g8, uint32_t sb_g, uint32_t sb_g8,
-                                           const uint2 (&b)[8])
+                                           const uint2 *b)
 {
     const __half2 k8 = __floats2half2_rn(8.0f, 8.0f);
     const __half2 s8_g = __hmul2(half2_from_bf16_bits(static_cast<uint16_t>(sb_g & 0xFFFFu)), k8);
@@ -251,605 +253,369 @@ __device__ __forceinline__ void mma_kblock(float (&d)[4], uint4 q_g, uint4 q_g8,
     for (int w = 0; w < 4; ++w) {
         const uint4 pg = dequant8_f16_e2m3(wg[w], s8_g, b_g);
         const uint4 pg8 = dequant8_f16_e2m3(wg8[w], s8_g8, b_g8);
+        const uint2 b0 = b[2 * w], b1 = b[2 * w + 1];
         const uint32_t a0[4] = {pg.x, pg8.x, pg.y, pg8.y};  // slice 2w: pairs (0,2) and (4,6)
         const uint32_t a1[4] = {pg.z, pg8.z, pg.w, pg8.w};  // slice 2w + 1: pairs (1,3) and (5,7)
-        mma_16816(d, a0, b[2 * w].x, b[2 * w].y);
-        mma_16816(d, a1, b[2 * w + 1].x, b[2 * w + 1].y);
+        mma_16816(d, a0, b0.x, b0.y);
+        mma_16816(d, a1, b1.x, b1.y);
     }
 }
 
-// Scale and bias of group `grp` of row `row`, packed (scale low, bias high).
-__device__ __forceinline__ uint32_t sb_of(const uint16_t *s, const uint16_t *b, int row, int ngroups, int grp)
+// Scale and bias of this lane's group in a K block, packed (scale low, bias high).
+__device__ __forceinline__ uint32_t load_sb(const uint16_t *s_row, const uint16_t *b_row, int group)
 {
-    return static_cast<uint32_t>(s[row * ngroups + grp]) | (static_cast<uint32_t>(b[row * ngroups + grp]) << 16);
+    return static_cast<uint32_t>(ld_early_u16(s_row + group)) | (static_cast<uint32_t>(ld_early_u16(b_row + group)) << 16);
 }
 
-// Eight bf16 inputs (k0..k0+7 of one token) -> fp16 in the permuted B order
-// (x0 x2 x4 x6 | x1 x3 x5 x7); raises the range flag on an infinite result.
-__device__ __forceinline__ uint4 bf16x8_to_perm_f16(uint4 v, bool &inf)
+// gate/up: task = (unit, 32 rows of I); warp w takes rows 16 (w % 2) .. + 16
+// and the K blocks kb = w / 2 (mod 4), both matrices; the four K-split partial
+// tiles are summed in shared memory, then h' = f16(w_u[t] * silu(gate) * up) is
+// written in the permuted B layout of the down projection (K = units x I).
+__global__ void __launch_bounds__(kDecThreads)
+dec_gateup_kernel(const DecodeLayerArgs a)
 {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float f[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float2 p2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
-        f[2 * j] = p2.x;
-        f[2 * j + 1] = p2.y;
-    }
-    const __half2 h0 = __floats2half2_rn(f[0], f[2]), h1 = __floats2half2_rn(f[4], f[6]);
-    const __half2 h2 = __floats2half2_rn(f[1], f[3]), h3 = __floats2half2_rn(f[5], f[7]);
-    const uint4 o = make_uint4(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1),
-                               *reinterpret_cast<const uint32_t *>(&h2), *reinterpret_cast<const uint32_t *>(&h3));
-    inf |= f16x2_has_inf(o.x) | f16x2_has_inf(o.y) | f16x2_has_inf(o.z) | f16x2_has_inf(o.w);
-    return o;
-}
-
-// Half offset of K element k0 (a multiple of 8) of token n in the permuted B
-// layout [k / 128][T][4][8][4].
-__device__ __forceinline__ int perm_b_offset(int k0, int n, int T)
-{
-    const int kb = k0 >> 7, r = k0 & 127, t4 = r >> 5, w = (r >> 3) & 3;
-    return (((kb * T + n) * 4 + t4) * 8 + 2 * w) * 4;
-}
-
-// ---------------------------------------------------------------- per-CTA work plan
-// Gate/up tasks j = 0 .. U * I/8 - 1 (unit j / (I/8), I rows 8 (j % (I/8)) ..),
-// task j on CTA G - 1 - (j mod G); down tasks (16 output rows) k = c, c + G.
-struct Plan {
-    int G, c, nu_gu;       // CTAs, this CTA, gate/up tasks per unit (I / 8)
-    int n_down, n_mydown;  // down tasks in all, of this CTA (0..2)
-    int upc;               // units per down item
-    int n_rrows;           // router rows of this CTA (1 or 2)
-    __device__ int gu_first() const { return G - 1 - c; }
-};
-
-template <typename F>
-__device__ __forceinline__ void for_gu_tasks(const Plan &p, int j_lo, int j_hi, F &&f)
-{
-    for (int j = p.gu_first(); j < j_hi; j += p.G)
-        if (j >= j_lo) f(j);
-}
-
-// ---------------------------------------------------------------- the kernel
-// 9 warps: one SM sub-partition holds 3 of them, so at most 168 registers each
-__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a)
-{
-    extern __shared__ __align__(128) uint8_t dsm[];
-    DecSmem &S = *reinterpret_cast<DecSmem *>(dsm);
-    const int T = a.T, d = a.d, I = a.I, E = a.E;
-    __nv_bfloat16 *xb = reinterpret_cast<__nv_bfloat16 *>(dsm + kStaticBytes);     // [T][d] bf16
-    __half *xp = reinterpret_cast<__half *>(dsm + kStaticBytes + static_cast<size_t>(T) * d * 2);  // permuted fp16
-    // h' of one down item's units, staged from the exchange buffer: [unit][K block][T][4][16] words
-    uint32_t *hs = reinterpret_cast<uint32_t *>(dsm + kStaticBytes + align128(static_cast<size_t>(T) * d * 4));
-    uint8_t *ring = dsm + kStaticBytes + align128(static_cast<size_t>(T) * d * 4) + stage_bytes(T, d, I);
-    const int tid = threadIdx.x;  // compute threads 0..255, producer warp 256..287
-    const int warp = tid >> 5, lane = tid & 31;
+    extern __shared__ __align__(16) uint8_t dsm[];
+    __half *xp = reinterpret_cast<__half *>(dsm);                                 // [d/128][8][4][8][4]
+    float *red = reinterpret_cast<float *>(dsm + static_cast<size_t>(a.d) * 8 * 2);  // [8 warps][2][32][4]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int NS = a.n_slots;
-    const uint32_t SB = static_cast<uint32_t>(a.slot_bytes);
-    const Waiter wt{&S.abort, a.abort_flag, &a.ctrl->status};
+    const int T = a.T, d = a.d, I = a.I, nkb = d / kKB, ngroups = d / 64;
+    const int tpu = I / 32;  // tasks per unit (32 rows of I each)
+    const int rt = warp & 1, ks = warp >> 1;
 
-    Plan P;
-    P.G = gridDim.x;
-    P.c = blockIdx.x;
-    P.nu_gu = I / kGURows;
-    P.n_down = d / kDownRows;
-    P.n_mydown = (P.c < P.n_down) + (P.c + P.G < P.n_down);
-    P.upc = static_cast<int>(SB / (9u * I));
-    P.n_rrows = (P.c < E) + (P.c + P.G < E);
-    const int nkb_d = d / kKB, nkb_i = I / kKB;
-
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&S.full[s], 33);     // the bulk copies' byte count, then the producer's 32 lanes
-            mbar_init(&S.empty[s], kCW);   // the compute warps, each once done reading
+    // One round of weight loads of a task: up to 4 K blocks of this warp, both
+    // matrices, rows g and g + 8 of its 16-row tile.
+    uint4 qg[4], qg8[4], qu[4], qu8[4];
+    uint32_t sg[4], sg8[4], su[4], su8[4];
+    auto issue_loads = [&](int e, int i0, int kb0) {
+        const bool sh = e < 0;
+        const size_t row_g = (sh ? 0 : static_cast<size_t>(e) * I) + i0 + g, row_g8 = row_g + 8;
+        const uint8_t *gq = sh ? a.sh_gate_q : a.gate_q, *uq = sh ? a.sh_up_q : a.up_q;
+        const uint16_t *gs = sh ? a.sh_gate_s : a.gate_s, *gb = sh ? a.sh_gate_b : a.gate_b;
+        const uint16_t *us = sh ? a.sh_up_s : a.up_s, *ub = sh ? a.sh_up_b : a.up_b;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int kb = kb0 + 4 * m;
+            if (kb < nkb) {
+                const size_t off = static_cast<size_t>(kb) * (kKB / 2) + t * 16;
+                qg[m] = ld_early(gq + row_g * (d / 2) + off);
+                qg8[m] = ld_early(gq + row_g8 * (d / 2) + off);
+                qu[m] = ld_early(uq + row_g * (d / 2) + off);
+                qu8[m] = ld_early(uq + row_g8 * (d / 2) + off);
+                const int grp = 2 * kb + (t >> 1);
+                sg[m] = load_sb(gs + row_g * ngroups, gb + row_g * ngroups, grp);
+                sg8[m] = load_sb(gs + row_g8 * ngroups, gb + row_g8 * ngroups, grp);
+                su[m] = load_sb(us + row_g * ngroups, ub + row_g * ngroups, grp);
+                su8[m] = load_sb(us + row_g8 * ngroups, ub + row_g8 * ngroups, grp);
+            }
         }
-        S.abort = 0;
-        S.decide = 0;
-        S.unit_e[0] = -1;  // unit 0 is always the shared expert
-        fence_mbar_init();
-    }
-    if (tid < 8) S.zeros[tid] = make_uint2(0u, 0u);
-    __syncthreads();
-
-    // Abort decision at the top-8 point of every layer, the same for all warps:
-    // one thread reads the flag between two barriers of the whole CTA.  The
-    // producer learns here that the unit list of the layer is complete.
-    auto top8_point = [&]() -> bool {
-        named_barrier_sync(kBarTop8, kDecThreads);
-        if (tid == 0) S.decide = *reinterpret_cast<volatile int *>(&S.abort);
-        named_barrier_sync(kBarTop8, kDecThreads);
-        return *reinterpret_cast<volatile int *>(&S.decide) != 0;
     };
+    pdl_trigger();
+    // The shared expert is unit 0 and does not depend on the routing: its CTAs
+    // issue their first weight loads before waiting for the router.
+    const bool preloaded = blockIdx.x < tpu;
+    if (preloaded) issue_loads(-1, blockIdx.x * 32 + rt * 16, ks);
+    pdl_wait();
+    // this token's logits first (the top-8 waits for them), then the fp16 input
+    // to shared memory asynchronously; the first round of weight loads is
+    // issued before waiting for it
+    float4 l0 = make_float4(0.f, 0.f, 0.f, 0.f), l1 = l0;
+    if (warp < T) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.logits + warp * a.E + lane * 8);
+        l0 = __ldcg(src);
+        l1 = __ldcg(src + 1);
+    }
+    for (int i = threadIdx.x; i < d; i += kDecThreads)  // 8 x d fp16 = d uint4
+        cp_async_16(reinterpret_cast<uint4 *>(xp) + i, reinterpret_cast<const uint4 *>(a.xp) + i);
+    cp_async_commit();
+    bool xp_ready = false;
 
-    // ---------------------------------------------------------------- the ring
-    // Items, in the order they are issued and consumed, per layer li:
-    //   router rows of this CTA; the shared expert's gate/up tasks of this CTA;
-    //   [top-8 point]  the routed gate/up tasks of this CTA; per down task,
-    //   chunks of units [u0, u0 + upc).
-    // The producer warp copies the weight rows of an item with bulk (TMA)
-    // copies, counted in bytes on the slot's full barrier, and the small
-    // scale/bias slices with 16-byte cp.async pieces spread over its 32 lanes,
-    // each lane arriving (noinc) once its pieces land; the barrier fires when
-    // both are complete.  Only the producer waits on the copy engines; the
-    // compute warps work on the items already there.  Item n goes to slot n % NS once its previous
-    // occupant has been released by all compute warps.
-    if (warp == kProdWarp) {
-        uint32_t pit = 0;  // items issued
-        bool pok = true;
-        auto copy_seg = [&](uint8_t *dst, const void *src, uint32_t bytes) {
-            for (uint32_t o = static_cast<uint32_t>(lane) * 16u; o < bytes; o += 32u * 16u)
-                cp_async_16(dst + o, static_cast<const uint8_t *>(src) + o);
-        };
-        // waits for a free slot and announces the item's bulk-copy bytes;
-        // returns the slot, or -1 when giving up
-        auto begin_item = [&](uint32_t bulk_bytes) -> int {
-            if (!pok) return -1;
-            const int slot = static_cast<int>(pit % NS);
-            int ok = 1;
-            if (lane == 0) {
-                ok = wait_bar(&S.empty[slot], ((pit / NS) & 1) ^ 1, wt);
-                if (ok) mbar_arrive_expect_tx(&S.full[slot], bulk_bytes);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) pok = false;
-            return ok ? slot : -1;
-        };
-        auto end_item = [&](int slot) {
-            cp_async_mbar_arrive_noinc(&S.full[slot]);
-            ++pit;
-        };
-        // gate/up task j of expert e (e < 0: the shared expert)
-        auto issue_gu = [&](const DecodeLayerPtrs &W, int j, int e) {
-            const int slot = begin_item(8u * d);
-            if (slot < 0) return;
-            uint8_t *base = ring + static_cast<size_t>(slot) * SB;
-            const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * I) + static_cast<size_t>(j % P.nu_gu) * kGURows;
-            const size_t ng = d / 64;
-            // rows: two bulk copies; scale/bias slices: cp.async pieces
-            if (lane == 0) bulk_g2s(base, (e < 0 ? W.sh_gate_q : W.gate_q) + r0 * (d / 2), 4u * d, &S.full[slot]);
-            if (lane == 1) bulk_g2s(base + 4 * d, (e < 0 ? W.sh_up_q : W.up_q) + r0 * (d / 2), 4u * d, &S.full[slot]);
-            copy_seg(base + 8 * d, (e < 0 ? W.sh_gate_s : W.gate_s) + r0 * ng, d / 4);
-            copy_seg(base + 8 * d + d / 4, (e < 0 ? W.sh_gate_b : W.gate_b) + r0 * ng, d / 4);
-            copy_seg(base + 8 * d + d / 2, (e < 0 ? W.sh_up_s : W.up_s) + r0 * ng, d / 4);
-            copy_seg(base + 8 * d + 3 * d / 4, (e < 0 ? W.sh_up_b : W.up_b) + r0 * ng, d / 4);
-            end_item(slot);
-        };
-        // units [u0, u1) of down task k: 16 rows of Wd of each unit's expert
-        auto issue_down = [&](const DecodeLayerPtrs &W, int k, int u0, int u1) {
-            const int slot = begin_item(8u * I * (u1 - u0));
-            if (slot < 0) return;
-            uint8_t *base = ring + static_cast<size_t>(slot) * SB;
-            const size_t j0 = static_cast<size_t>(P.c + k * P.G) * kDownRows;
-            const size_t ng = I / 64;
-            for (int i = 0; i < u1 - u0; ++i) {
-                const int e = S.unit_e[u0 + i];
-                const size_t r0 = (e < 0 ? 0 : static_cast<size_t>(e) * d) + j0;
-                uint8_t *ub = base + static_cast<size_t>(i) * 9 * I;
-                if (lane == i) bulk_g2s(ub, (e < 0 ? W.sh_down_q : W.down_q) + r0 * (I / 2), 8u * I, &S.full[slot]);
-                copy_seg(ub + 8 * I, (e < 0 ? W.sh_down_s : W.down_s) + r0 * ng, I / 2);
-                copy_seg(ub + 8 * I + I / 2, (e < 0 ? W.sh_down_b : W.down_b) + r0 * ng, I / 2);
-            }
-            end_item(slot);
-        };
-        for (int li = 0; li < a.n_layers; ++li) {
-            const DecodeLayerPtrs &W = a.L[li];
-            {
-                const int slot = begin_item(2u * d * P.n_rrows);
-                if (slot >= 0) {
-                    uint8_t *base = ring + static_cast<size_t>(slot) * SB;
-                    if (lane < P.n_rrows)
-                        bulk_g2s(base + static_cast<size_t>(lane) * 2 * d,
-                                 W.router_w + static_cast<size_t>(P.c + lane * P.G) * d, 2u * d, &S.full[slot]);
-                    end_item(slot);
-                }
-            }
-            for_gu_tasks(P, 0, P.nu_gu, [&](int j) { issue_gu(W, j, -1); });
-            if (top8_point()) break;
-            const int U = S.n_units;
-            for_gu_tasks(P, P.nu_gu, U * P.nu_gu, [&](int j) { issue_gu(W, j, S.unit_e[j / P.nu_gu]); });
-            for (int k = 0; k < P.n_mydown; ++k)
-                for (int u0 = 0; u0 < U; u0 += P.upc) issue_down(W, k, u0, min(U, u0 + P.upc));
+    // Top-8 per token and the list of distinct experts ("units": the shared
+    // expert first with weight 1, then the routed experts ascending), computed by
+    // every CTA from the logits;
+    // CTA 0 publishes it for the down projection and the trace.
+    __shared__ int umask[256];
+    __shared__ float uw[256][kMaxT];
+    __shared__ int scan_tmp[kDecWarps];
+    __shared__ int s_expert[kMaxT * 8 + 1];
+    __shared__ float s_w[kMaxT * 8 + 1][kMaxT];
+    __shared__ int s_n_units;
+    umask[threadIdx.x] = 0;
+#pragma unroll
+    for (int q = 0; q < kMaxT; ++q) uw[threadIdx.x][q] = 0.0f;
+    __syncthreads();
+    if (warp < T) {
+        const int tok = warp;
+        const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+        int sel_e;
+        float sel_w;
+        warp_top8_keys(lv, lane, sel_e, sel_w);
+        if (lane < 8) {
+            if (blockIdx.x == 0 && a.trace_idx) a.trace_idx[tok * 8 + lane] = sel_e;
+            if (blockIdx.x == 0 && a.trace_w) a.trace_w[tok * 8 + lane] = sel_w;
+            atomicOr(&umask[sel_e], 1 << tok);
+            uw[sel_e][tok] = sel_w;
         }
-        // no copy into this CTA's shared memory may still be in flight at exit
-        cp_async_wait_all();
+    }
+    __syncthreads();
+    {
+        const int used = umask[threadIdx.x] != 0;
+        int incl = used;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += nb;
+        }
+        if (lane == 31) scan_tmp[warp] = incl;
+        __syncthreads();
+        int off = 0, n_used = 0;
+        for (int w = 0; w < kDecWarps; ++w) {
+            if (w < warp) off += scan_tmp[w];
+            n_used += scan_tmp[w];
+        }
+        const int u = 1 + off + incl - used;
+        if (used) {
+            s_expert[u] = threadIdx.x;
+#pragma unroll
+            for (int q = 0; q < kMaxT; ++q) s_w[u][q] = uw[threadIdx.x][q];
+            if (blockIdx.x == 0) {
+                a.unit_expert[u] = threadIdx.x;
+                a.unit_mask[u] = umask[threadIdx.x];
+#pragma unroll
+                for (int q = 0; q < kMaxT; ++q) a.unit_w[u * kMaxT + q] = uw[threadIdx.x][q];
+            }
+        }
+        if (threadIdx.x == 0) {
+            s_expert[0] = -1;  // shared expert
+#pragma unroll
+            for (int q = 0; q < kMaxT; ++q) s_w[0][q] = 1.0f;
+            s_n_units = n_used + 1;
+            if (blockIdx.x == 0) {
+                a.unit_expert[0] = -1;
+                a.unit_mask[0] = (1 << T) - 1;
+#pragma unroll
+                for (int q = 0; q < kMaxT; ++q) a.unit_w[q] = 1.0f;
+                *a.n_units = n_used + 1;
+            }
+        }
+        __syncthreads();
+    }
+    const int n_units = s_n_units;
+    if (blockIdx.x >= n_units * tpu) {
+        cp_async_wait_all();  // no copy into shared memory in flight at exit
         return;
     }
-
-    uint32_t cit = 0;  // index of the next item to consume
-    int rp = 0;        // red buffer parity
-    const size_t TD = static_cast<size_t>(T) * d;
-    const size_t HX = static_cast<size_t>(kMaxUnits) * nkb_i * T * 64;  // words of one h' buffer
-    auto ready_of = [&](int l) { return a.ready + static_cast<size_t>(l) * kDecodeReadySlots; };
-
-    // Waits for the next item; returns its slot base (nullptr: giving up).  The
-    // result is uniform within each warp.
-    auto take_item = [&](int &slot_out) -> const uint8_t * {
-        const int slot = static_cast<int>(cit % NS);
-        const bool got = wait_bar(&S.full[slot], (cit / NS) & 1, wt);
-        ++cit;
-        slot_out = slot;
-        return __all_sync(0xffffffffu, got) ? ring + static_cast<size_t>(slot) * SB : nullptr;
-    };
-    // This warp is done reading the item's slot.  An item whose copies did not
-    // arrive (giving up) is not released: the slot may still be written.
-    auto release_item = [&](int slot, const uint8_t *base) {
-        __syncwarp();
-        if (lane == 0 && base) mbar_arrive(&S.empty[slot]);
-    };
-
-    // ---- layer input x_l into xb (bf16) and xp (permuted fp16); export_only:
-    // only write x_next[l - 1] (the normalised output of the last layer)
-    auto build_input = [&](int l, bool export_only) {
-        bool inf = false;
-        if (l == 0) {
-            for (int q = tid; q < T * (d / 8); q += kComputeThreads) {
-                const int n = q / (d / 8), k0 = (q - n * (d / 8)) * 8;
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.x_in + static_cast<size_t>(n) * d + k0));
-                *reinterpret_cast<uint4 *>(xb + static_cast<size_t>(n) * d + k0) = v;
-                *reinterpret_cast<uint4 *>(xp + perm_b_offset(k0, n, T)) = bf16x8_to_perm_f16(v, inf);
+    for (int task = blockIdx.x; task < n_units * tpu; task += gridDim.x) {
+        const int u = task / tpu;
+        const int i0 = (task - u * tpu) * 32 + rt * 16;
+        const int e = s_expert[u];
+        float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r0 = 0; r0 < nkb; r0 += 4 * 4) {  // rounds: the same count in every warp
+            const int kb0 = r0 + ks;
+            // up to 4 K blocks of this warp: all loads first, then the MMAs
+            if (!(preloaded && task == blockIdx.x && r0 == 0)) issue_loads(e, i0, kb0);
+            if (!xp_ready) {
+                cp_async_wait_all();
+                __syncthreads();
+                xp_ready = true;
             }
-        } else {
-            const float *src = a.out_x + static_cast<size_t>((l - 1) & 1) * TD;
-            if (tid == 0) wait_ready(ready_of(l - 1) + 1, static_cast<unsigned int>(P.n_down), wt);
-            compute_sync();
 #pragma unroll
-            for (int n = 0; n < kMaxT; ++n) {
-                if (n < T) {
-                    float ss = 0.0f;
-                    for (int k0 = tid * 8; k0 < d; k0 += kComputeThreads * 8) {
-                        const float4 *p = reinterpret_cast<const float4 *>(src + static_cast<size_t>(n) * d + k0);
-                        const float4 v0 = __ldcg(p), v1 = __ldcg(p + 1);
-                        ss = fmaf(v0.x, v0.x, fmaf(v0.y, v0.y, fmaf(v0.z, v0.z, fmaf(v0.w, v0.w, ss))));
-                        ss = fmaf(v1.x, v1.x, fmaf(v1.y, v1.y, fmaf(v1.z, v1.z, fmaf(v1.w, v1.w, ss))));
-                    }
-                    ss = warp_sum(ss);
-                    if (lane == 0) S.sred[warp][n] = ss;
-                }
-            }
-            compute_sync();
-            if (tid < T) {
-                float s = 0.0f;
-                for (int w = 0; w < kCW; ++w) s += S.sred[w][tid];
-                S.inv_rms[tid] = 1.0f / sqrtf(s / static_cast<float>(d) + 1e-6f);
-            }
-            compute_sync();
-            for (int q = tid; q < T * (d / 8); q += kComputeThreads) {
-                const int n = q / (d / 8), k0 = (q - n * (d / 8)) * 8;
-                const float r = S.inv_rms[n];
-                const float4 *p = reinterpret_cast<const float4 *>(src + static_cast<size_t>(n) * d + k0);
-                const float4 v0 = __ldcg(p), v1 = __ldcg(p + 1);
-                const __nv_bfloat162 b0 = __floats2bfloat162_rn(v0.x * r, v0.y * r), b1 = __floats2bfloat162_rn(v0.z * r, v0.w * r);
-                const __nv_bfloat162 b2 = __floats2bfloat162_rn(v1.x * r, v1.y * r), b3 = __floats2bfloat162_rn(v1.z * r, v1.w * r);
-                const uint4 v = make_uint4(*reinterpret_cast<const uint32_t *>(&b0), *reinterpret_cast<const uint32_t *>(&b1),
-                                           *reinterpret_cast<const uint32_t *>(&b2), *reinterpret_cast<const uint32_t *>(&b3));
-                if (blockIdx.x == 0 && a.x_next)
-                    *reinterpret_cast<uint4 *>(a.x_next + static_cast<size_t>(l - 1) * TD + static_cast<size_t>(n) * d + k0) = v;
-                if (!export_only) {
-                    *reinterpret_cast<uint4 *>(xb + static_cast<size_t>(n) * d + k0) = v;
-                    *reinterpret_cast<uint4 *>(xp + perm_b_offset(k0, n, T)) = bf16x8_to_perm_f16(v, inf);
+            for (int m = 0; m < 4; ++m) {
+                const int kb = kb0 + 4 * m;
+                if (kb < nkb) {
+                    const uint2 *bf = reinterpret_cast<const uint2 *>(xp + (((kb * 8 + g) * 4 + t) * 8) * 4);
+                    mma_kblock(accg, qg[m], qg8[m], sg[m], sg8[m], bf);
+                    mma_kblock(accu, qu[m], qu8[m], su[m], su8[m], bf);
                 }
             }
         }
-        if (inf) record_error(wt.status, kErrDeviceRange);
-        compute_sync();
-    };
-
-    // ---- gate/up task j of unit u: h' = w_u silu(gate x) (up x), published
-    auto gu_task = [&](int l, int j, int u) {
-        int slot;
-        const uint8_t *base = take_item(slot);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (base) {
-            const uint8_t *gq = base, *uq = base + 4 * d;
-            const uint16_t *gs = reinterpret_cast<const uint16_t *>(base + 8 * d);
-            const uint16_t *gb = reinterpret_cast<const uint16_t *>(base + 8 * d + d / 4);
-            const uint16_t *us = reinterpret_cast<const uint16_t *>(base + 8 * d + d / 2);
-            const uint16_t *ub = reinterpret_cast<const uint16_t *>(base + 8 * d + 3 * d / 4);
-            const int ng = d / 64;
-            for (int kb = warp; kb < nkb_d; kb += kCW) {
-                const uint4 qg = lds128(gq + g * (d / 2) + kb * 64 + t * 16);
-                const uint4 qu = lds128(uq + g * (d / 2) + kb * 64 + t * 16);
-                const int grp = 2 * kb + (t >> 1);
-                uint2 bfr[8];
-                const uint2 *src = g < T ? reinterpret_cast<const uint2 *>(xp + (((kb * T + g) * 4 + t) * 8) * 4) : S.zeros;
+        // sum the four K-split partial tiles of each row tile
+        float *mine = red + (warp * 2) * 32 * 4;
 #pragma unroll
-                for (int s = 0; s < 8; ++s) bfr[s] = src[s];
-                mma_kblock(acc, qg, qu, sb_of(gs, gb, g, ng, grp), sb_of(us, ub, g, ng, grp), bfr);
-            }
+        for (int q = 0; q < 4; ++q) {
+            mine[lane * 4 + q] = accg[q];
+            mine[32 * 4 + lane * 4 + q] = accu[q];
         }
-        release_item(slot, base);
-        float *r = S.red[rp][warp][lane];
+        __syncthreads();
+        if (ks == 0) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) r[q] = acc[q];
-        compute_sync();
-        if (warp == 0 && base != nullptr) {
-            float D[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int w = 0; w < kCW; ++w)
+            for (int p = 1; p < 4; ++p) {
+                const float *o = red + ((rt + 2 * p) * 2) * 32 * 4;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) D[q] += S.red[rp][w][lane][q];
-            // D[0], D[1]: gate row g, tokens 2t, 2t+1; D[2], D[3]: up row g
-            uint32_t hh[2];
-            bool inf = false;
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int n = 2 * t + m;
-                const float wu = n < T ? S.unit_w[u][n] : 0.0f;
-                const __half h = __float2half_rn(wu * silu_f(D[m]) * D[2 + m]);
-                inf |= __hisinf(h);
-                hh[m] = __half_as_ushort(h);
-            }
-            if (inf) record_error(wt.status, kErrDeviceRange);
-            // pair row g with row g + 2 (lane + 8): the two halves of one word
-            const uint32_t ph0 = __shfl_down_sync(0xffffffffu, hh[0], 8);
-            const uint32_t ph1 = __shfl_down_sync(0xffffffffu, hh[1], 8);
-            if ((g & 2) == 0) {
-                const int i0 = (j % P.nu_gu) * kGURows;
-                const int kbI = i0 >> 7, r0 = i0 & 127, t4 = r0 >> 5, w8 = (r0 >> 3) & 3;
-                const int s = 2 * w8 + (g & 1), pw = g >> 2;
-                uint32_t *hx = a.h_x + static_cast<size_t>(l & 1) * HX;
-#pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const int n = 2 * t + m;
-                    if (n < T) {
-                        const size_t idx = ((((static_cast<size_t>(u) * nkb_i + kbI) * T + n) * 4 + t4) * 8 + s) * 2 + pw;
-                        hx[idx] = hh[m] | ((m ? ph1 : ph0) << 16);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    accg[q] += o[lane * 4 + q];
+                    accu[q] += o[32 * 4 + lane * 4 + q];
                 }
             }
-            __syncwarp();
-            if (lane == 0) signal_ready(ready_of(l) + 2 + u);
-        }
-        rp ^= 1;
-    };
-
-    // ---- down item: units [u0, u1) of one down task, accumulated into acc.
-    // Once the item's units are ready, all compute threads copy its h' words
-    // into `hs`, then each warp runs its (unit, K block) pairs.
-    auto down_item = [&](int l, int u0, int u1, float(&acc)[4]) {
-        int slot;
-        const uint8_t *base = take_item(slot);
-        const int nw = (u1 - u0) * nkb_i * T * 64;  // words of the item
-        const uint32_t *hx = a.h_x + static_cast<size_t>(l & 1) * HX + static_cast<size_t>(u0) * nkb_i * T * 64;
-        if (tid == 0)
-            for (int u = u0; u < u1; ++u) wait_ready(ready_of(l) + 2 + u, static_cast<unsigned int>(P.nu_gu), wt);
-        compute_sync();
-        for (int w0 = tid * 4; w0 < nw; w0 += kComputeThreads * 4)
-            *reinterpret_cast<uint4 *>(hs + w0) = __ldcg(reinterpret_cast<const uint4 *>(hx + w0));
-        compute_sync();
-        if (base) {
-            const int ng = I / 64;
-            for (int pi = warp; pi < (u1 - u0) * nkb_i; pi += kCW) {
-                const int i = pi / nkb_i, kb = pi - i * nkb_i;
-                const uint8_t *ubase = base + static_cast<size_t>(i) * 9 * I;
-                const uint16_t *s = reinterpret_cast<const uint16_t *>(ubase + 8 * I);
-                const uint16_t *b = reinterpret_cast<const uint16_t *>(ubase + 8 * I + I / 2);
-                uint2 bfr[8];
-                const uint2 *src =
-                    g < T ? reinterpret_cast<const uint2 *>(hs + ((static_cast<size_t>(pi) * T + g) * 4 + t) * 16) : S.zeros;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) bfr[q] = src[q];
-                const uint4 qg = lds128(ubase + g * (I / 2) + kb * 64 + t * 16);
-                const uint4 qg8 = lds128(ubase + (g + 8) * (I / 2) + kb * 64 + t * 16);
-                const int grp = 2 * kb + (t >> 1);
-                mma_kblock(acc, qg, qg8, sb_of(s, b, g, ng, grp), sb_of(s, b, g + 8, ng, grp), bfr);
-            }
-        }
-        release_item(slot, base);
-        compute_sync();  // hs is reused by the next item
-    };
-
-    // ---- down task k done: sum the warps' fragments, publish the rows
-    auto finish_down = [&](int l, int k, float(&acc)[4]) {
-        float *r = S.red[rp][warp][lane];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) r[q] = acc[q];
-        compute_sync();
-        if (warp == 0) {
-            float D[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int w = 0; w < kCW; ++w)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) D[q] += S.red[rp][w][lane][q];
-            const int j0 = (P.c + k * P.G) * kDownRows;
-            float *ox = a.out_x + static_cast<size_t>(l & 1) * TD;
-            float *out = a.out + static_cast<size_t>(l) * TD;
+            // fragment: q = 0/1 -> row g, tokens 2t, 2t+1; q = 2/3 -> row g + 8
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int n = 2 * t + (q & 1), j = j0 + g + 8 * (q >> 1);
-                if (n < T) {
-                    out[static_cast<size_t>(n) * d + j] = D[q];
-                    ox[static_cast<size_t>(n) * d + j] = D[q];
-                }
-            }
-            __syncwarp();
-            if (lane == 0) signal_ready(ready_of(l) + 1);
-        }
-        rp ^= 1;
-    };
-
-    for (int li = 0; li < a.n_layers; ++li) {
-        const int l = a.layer0 + li;
-        const DecodeLayerPtrs &W = a.L[li];
-
-        // ---- A: input, router rows
-        build_input(l, false);
-        {
-            int slot;
-            const uint8_t *base = take_item(slot);
-            float part[2][kMaxT];
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-#pragma unroll
-                for (int n = 0; n < kMaxT; ++n) part[r][n] = 0.0f;
-            if (base) {
-                const int kw = d / kCW;
-                for (int k0 = warp * kw + lane * 8; k0 < (warp + 1) * kw; k0 += 256) {
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        if (r < P.n_rrows) {
-                            const uint4 wv = lds128(base + static_cast<size_t>(r) * 2 * d + k0 * 2);
-#pragma unroll
-                            for (int n = 0; n < kMaxT; ++n)
-                                if (n < T) part[r][n] = dot8_bf16(wv, lds128(xb + static_cast<size_t>(n) * d + k0), part[r][n]);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-#pragma unroll
-                for (int n = 0; n < kMaxT; ++n)
-                    if (r < P.n_rrows && n < T) {
-                        const float v = warp_sum(part[r][n]);
-                        if (lane == 0) S.rred[warp][r][n] = v;
-                    }
-            release_item(slot, base);
-            compute_sync();
-            if (warp == 0) {
-                if (tid < P.n_rrows * T && base) {
-                    const int r = tid / T, n = tid - r * T, e = P.c + r * P.G;
-                    float v = 0.0f;
-                    for (int w = 0; w < kCW; ++w) v += S.rred[w][r][n];
-                    if (W.router_bias) v += W.router_bias[e];
-                    a.logits_x[(static_cast<size_t>(l & 1) * T + n) * E + e] = v;
-                    if (a.trace_logits) a.trace_logits[(static_cast<size_t>(l) * T + n) * E + e] = v;
-                }
-                __syncwarp();
-#ifdef LILY_TEST_STALL_DECODE_LAYERS
-                // Test builds only: in a call of exactly this many layers, CTA 0
-                // never signals its logits of layer 3, so every CTA's bounded wait
-                // for them runs out and the abort path executes.
-                if (!(a.last_launch && a.layer0 + a.n_layers == LILY_TEST_STALL_DECODE_LAYERS && l == 3 &&
-                      blockIdx.x == 0))
-#endif
-                    if (lane == 0) signal_ready(ready_of(l));
+                const int n = 2 * t + (q & 1);
+                const int i = i0 + g + 8 * (q >> 1);
+                const float wt = s_w[u][n];
+                const float hv = wt * silu_f(accg[q]) * accu[q];
+                const __half hh = __float2half_rn(hv);
+                if (__hisinf(hh)) record_error(&a.ctrl->status, kErrDeviceRange);
+                a.h[perm_b_index(u * I + i, n)] = hh;
             }
         }
-        // ---- B: top-8 per token and the unit list
-        if (tid < kMaxT) S.unit_w[0][tid] = 1.0f;  // unit 0: the shared expert, weight 1
-        S.umask[tid] = 0;
-        if (tid == 0) wait_ready(ready_of(l), static_cast<unsigned int>(P.G), wt);
-        compute_sync();
-        if (warp < T) {
-            {
-                const float4 *p = reinterpret_cast<const float4 *>(a.logits_x + (static_cast<size_t>(l & 1) * T + warp) * E + lane * 8);
-                const float4 l0 = __ldcg(p), l1 = __ldcg(p + 1);
-                const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-                int sel_e;
-                float sel_w;
-                warp_top8_keys(lv, lane, sel_e, sel_w);
-                if (lane < 8) {
-                    if (blockIdx.x == 0 && a.trace_idx) a.trace_idx[(static_cast<size_t>(l) * T + warp) * 8 + lane] = sel_e;
-                    if (blockIdx.x == 0 && a.trace_w) a.trace_w[(static_cast<size_t>(l) * T + warp) * 8 + lane] = sel_w;
-                    atomicOr(&S.umask[sel_e], 1 << warp);
-                    S.sel_e[warp][lane] = sel_e;
-                    S.sel_w[warp][lane] = sel_w;
-                }
-            }
-        }
-        compute_sync();
-        {
-            const int used = S.umask[tid] != 0;
-            int incl = used;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int nb = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += nb;
-            }
-            if (lane == 31) S.scan_tmp[warp] = incl;
-            compute_sync();
-            int off = 0, n_used = 0;
-            for (int w = 0; w < kCW; ++w) {
-                if (w < warp) off += S.scan_tmp[w];
-                n_used += S.scan_tmp[w];
-            }
-            if (used) {
-                const int u = 1 + off + incl - used;
-                S.unit_e[u] = tid;
-                const int m = S.umask[tid];
-#pragma unroll
-                for (int n = 0; n < kMaxT; ++n) {
-                    float wv = 0.0f;
-                    if ((m >> n) & 1)
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (S.sel_e[n][j] == tid) wv = S.sel_w[n][j];
-                    S.unit_w[u][n] = wv;
-                }
-            }
-            if (tid == 0) S.n_units = min(n_used + 1, kMaxUnits);
-        }
-        if (top8_point()) break;  // the producer issues the routed experts' bytes from here
-        const int U = S.n_units;
-
-        // ---- the shared expert's gate/up rows of this CTA (computed while the
-        // routed experts' bytes, issued at the top-8 point, are in flight)
-        for_gu_tasks(P, 0, P.nu_gu, [&](int j) { gu_task(l, j, 0); });
-
-        // ---- C: routed gate/up, then per down task the down rows of every unit
-        for_gu_tasks(P, P.nu_gu, U * P.nu_gu, [&](int j) { gu_task(l, j, j / P.nu_gu); });
-        for (int k = 0; k < P.n_mydown; ++k) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int u0 = 0; u0 < U; u0 += P.upc) down_item(l, u0, min(U, u0 + P.upc), acc);
-            finish_down(l, k, acc);
-        }
+        __syncthreads();
     }
-    // the normalised output of the last layer (the input a next layer would take)
-    if (a.last_launch && a.x_next && blockIdx.x == 0 && !*reinterpret_cast<volatile int *>(&S.decide))
-        build_input(a.layer0 + a.n_layers, true);
+}
+
+// down: task = 16 output rows; the 8 warps split the K blocks of
+// K = units x I (unit u, block j), accumulate in one tile, and the partial
+// tiles are summed in shared memory.  out[t][row] = sum over units of
+// Wd_u[row] . h'_u[t] (the routing weight is already in h').
+constexpr int kDownWarps = 16;  // 512 threads: every K block of a row tile in flight at once for T = 1
+
+__global__ void __launch_bounds__(kDownWarps * 32)
+dec_down_kernel(const DecodeLayerArgs a)
+{
+    __shared__ float red[kDownWarps][32][4];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int T = a.T, d = a.d, I = a.I, kpu = I / kKB, ngroups = I / 64;
+    uint4 q[3], q8[3];
+    uint32_t sb[3], sb8[3];
+    uint2 bfr[3][8];
+    // weight loads of K block kb (unit u, block jb) for output rows j0 + g, j0 + g + 8
+    auto load_w = [&](int m, int e, int jb, int j0) {
+        const bool sh = e < 0;
+        const size_t row = (sh ? 0 : static_cast<size_t>(e) * d) + j0 + g;
+        const uint8_t *dq = sh ? a.sh_down_q : a.down_q;
+        const uint16_t *ds = sh ? a.sh_down_s : a.down_s, *db = sh ? a.sh_down_b : a.down_b;
+        const size_t off = static_cast<size_t>(jb) * (kKB / 2) + t * 16;
+        q[m] = ld_early(dq + row * (I / 2) + off);
+        q8[m] = ld_early(dq + (row + 8) * (I / 2) + off);
+        const int grp = 2 * jb + (t >> 1);
+        sb[m] = load_sb(ds + row * ngroups, db + row * ngroups, grp);
+        sb8[m] = load_sb(ds + (row + 8) * ngroups, db + (row + 8) * ngroups, grp);
+    };
+    pdl_trigger();
+    // unit 0 is the shared expert: the warps whose first K block lies in it issue
+    // those weight loads before waiting for the gate/up kernel
+    const bool preloaded = warp < kpu && blockIdx.x < d / 16;
+    if (preloaded) load_w(0, -1, warp, blockIdx.x * 16);
+    pdl_wait();
+    const int n_units = *a.n_units;
+    if (n_units < 1 || n_units > a.top_k * T + 1) {  // the h buffer holds top_k * T + 1 units
+        if (threadIdx.x == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
+        return;
+    }
+    const int n_kb = n_units * kpu;
+    for (int task = blockIdx.x; task < d / 16; task += gridDim.x) {
+        const int j0 = task * 16;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kb0 = warp; kb0 < n_kb; kb0 += 3 * kDownWarps) {
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                const int kb = kb0 + m * kDownWarps;
+                if (kb < n_kb) {
+                    const int u = kb / kpu, jb = kb - u * kpu;
+                    if (!(preloaded && m == 0 && task == blockIdx.x && kb0 == warp)) {
+                        int e = a.unit_expert[u];
+                        if (e >= a.E) {
+                            if (lane == 0) record_error(&a.ctrl->status, kErrDeviceIndex);
+                            e = 0;
+                        }
+                        load_w(m, e, jb, j0);
+                    }
+                    // token column g of h' is zero for g >= T: no load
+                    const uint2 *src = reinterpret_cast<const uint2 *>(a.h) + ((kb * 8 + g) * 4 + t) * 8;
+#pragma unroll
+                    for (int s2 = 0; s2 < 8; ++s2) bfr[m][s2] = g < T ? __ldcg(src + s2) : make_uint2(0u, 0u);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 3; ++m)
+                if (kb0 + m * kDownWarps < n_kb) mma_kblock(acc, q[m], q8[m], sb[m], sb8[m], bfr[m]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) red[warp][lane][q] = acc[q];
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int p = 1; p < kDownWarps; ++p)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[q] += red[p][lane][q];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int n = 2 * t + (q & 1);
+                if (n < T) a.out[static_cast<size_t>(n) * d + j0 + g + 8 * (q >> 1)] = acc[q];
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Dynamic shared memory: the router kernel stages the bf16 inputs [T][d]; the
+// gate/up kernel the fp16 inputs of up to 8 tokens in the permuted B layout
+// plus the per-warp partial sums [warps][2][32][4] floats.
+size_t decode_smem_route(int T, int d) { return static_cast<size_t>(T) * d * 2; }
+size_t decode_smem_gateup(int d) { return static_cast<size_t>(d) * 8 * 2 + kDecWarps * 2 * 32 * 4 * 4; }
+
+}  // namespace
+
+cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStream_t stream)
+{
+    for (const void *k : {reinterpret_cast<const void *>(dec_route_kernel), reinterpret_cast<const void *>(dec_gateup_kernel),
+                          reinterpret_cast<const void *>(dec_down_kernel)}) {
+        const cudaError_t e = set_max_dynamic_smem(k, 200 * 1024);
+        if (e != cudaSuccess) return e;
+    }
+    // programmatic dependent launches: each kernel starts while its predecessor finishes
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    cfg.gridDim = dim3((a.E + kDecWarps - 1) / kDecWarps);
+    cfg.dynamicSmemBytes = decode_smem_route(a.T, a.d);
+    if ((e = cudaLaunchKernelEx(&cfg, dec_route_kernel, a)) != cudaSuccess) return e;
+    cfg.gridDim = dim3(num_sms);
+    cfg.dynamicSmemBytes = decode_smem_gateup(a.d);
+    if ((e = cudaLaunchKernelEx(&cfg, dec_gateup_kernel, a)) != cudaSuccess) return e;
+    cfg.gridDim = dim3(std::min(num_sms, a.d / 16));
+    cfg.blockDim = dim3(kDownWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    if ((e = cudaLaunchKernelEx(&cfg, dec_down_kernel, a)) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace lily
+
+namespace lily {
+namespace {
+
+// Final export of the decode chain: x_next = bf16(out / sqrt(mean(out^2) + 1e-6)).
+__global__ void __launch_bounds__(256) dec_final_norm_kernel(const float *prev_out, uint16_t *x_export, int d)
+{
+    __shared__ float red[8];
+    const int t = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float *row = prev_out + static_cast<size_t>(t) * d;
+    float ss = 0.0f;
+    for (int c = threadIdx.x; c < d; c += 256) ss = fmaf(row[c], row[c], ss);
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float s = 0.0f;
+    for (int w = 0; w < 8; ++w) s += red[w];
+    const float inv = 1.0f / sqrtf(s / static_cast<float>(d) + 1e-6f);
+    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(x_export) + static_cast<size_t>(t) * d;
+    for (int c = threadIdx.x; c < d; c += 256) dst[c] = __float2bfloat16_rn(row[c] * inv);
 }
 
 }  // namespace
 
-int decode_slot_bytes(int d, int I) { return static_cast<int>(slot_bytes_of(d, I)); }
-
-size_t decode_smem_bytes(int T, int d, int I, int n_slots)
+cudaError_t launch_decode_final_norm(const float *prev_out, uint16_t *x_export, int T, int d, cudaStream_t stream)
 {
-    return kStaticBytes + align128(static_cast<size_t>(T) * d * 4) + stage_bytes(T, d, I) +
-           static_cast<size_t>(n_slots) * decode_slot_bytes(d, I);
-}
-
-int decode_ring_slots(int T, int d, int I)
-{
-    const size_t fixed = decode_smem_bytes(T, d, I, 0);
-    if (fixed >= static_cast<size_t>(kSmemLimit)) return 0;
-    const int n = static_cast<int>(std::min<size_t>(kMaxSlots, (kSmemLimit - fixed) / decode_slot_bytes(d, I)));
-    return n >= 3 ? n : 0;
-}
-
-// Ring slots of a launch on the current device: at most decode_ring_slots(),
-// fewer if the device cannot keep one CTA with that much shared memory
-// resident on every SM (a cooperative launch needs every CTA resident).
-int decode_launch_slots(int T, int d, int I)
-{
-    for (int n = decode_ring_slots(T, d, I); n >= 3; --n) {
-        const int smem = static_cast<int>(decode_smem_bytes(T, d, I, n));
-        if (set_max_dynamic_smem(reinterpret_cast<const void *>(decode_kernel), smem) != cudaSuccess) continue;
-        int blocks = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, decode_kernel, kDecThreads, smem) == cudaSuccess &&
-            blocks >= 1)
-            return n;
-    }
-    return 0;
-}
-
-cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t stream)
-{
-    const size_t smem = decode_smem_bytes(a.T, a.d, a.I, a.n_slots);
-    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(decode_kernel), static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    // cooperative: every CTA is resident at once (CTAs wait on each other's data)
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kDecThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel, a);
+    dec_final_norm_kernel<<<T, 256, 0, stream>>>(prev_out, x_export, d);
+    return cudaGetLastError();
 }
 
 }  // namespace lily

@@ -192,13 +192,6 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
-// Arrive (once) on `bar` when every cp.async this thread issued so far has
-// landed; the arrival is counted in the barrier's initial count (noinc).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Named barrier over `nthreads` threads (whole warps); the warp is reconverged

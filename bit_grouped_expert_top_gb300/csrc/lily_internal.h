@@ -107,53 +107,33 @@ cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_route_scan(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_scatter(const RouteArgs &a, cudaStream_t stream);
 
-// Decode path (1 <= T <= 8): one persistent cooperative kernel runs a chain of
-// layers; the layers hand their data to each other through tagged words in the
-// workspace (see decode.cu).
-struct DecodeLayerPtrs {
+// Decode path (1 <= T <= 8).
+struct DecodeLayerArgs {
+    int T, d, E, top_k, I, layer;
     const uint16_t *router_w;
     const float *router_bias;
     const uint8_t *gate_q, *up_q, *down_q;
     const uint16_t *gate_s, *gate_b, *up_s, *up_b, *down_s, *down_b;
     const uint8_t *sh_gate_q, *sh_up_q, *sh_down_q;
     const uint16_t *sh_gate_s, *sh_gate_b, *sh_up_s, *sh_up_b, *sh_down_s, *sh_down_b;
-};
-constexpr int kDecodeLayersPerLaunch = 20;  // layer table passed as a kernel parameter (<= 4 KB)
-constexpr int kDecodeMaxT = 8;
-constexpr int kDecodeMaxUnits = 8 * kDecodeMaxT + 1;  // distinct routed experts of 8 tokens + the shared one
-// Ready counters of one layer: [0] CTAs whose router rows are written, [1] down
-// tasks whose output rows are written, [2 + u] gate/up tasks of unit u written.
-constexpr int kDecodeReadySlots = 2 + kDecodeMaxUnits;
-
-struct DecodeArgs {
-    int T, d, E, top_k, I;
-    int layer0, n_layers;   // this launch runs global layers [layer0, layer0 + n_layers)
-    int last_launch;        // the call's last launch: also exports x_next of its last layer
-    int n_slots, slot_bytes;
-    const uint16_t *x_in;   // bf16 [T][d]: input of global layer 0
-    float *out;             // f32 [total layers][T][d]
-    uint16_t *x_next;       // bf16 [total layers][T][d] or NULL
-    float *trace_logits;    // [total layers][T][E] or NULL
-    int *trace_idx;         // [total layers][T][top_k] or NULL
-    float *trace_w;         // [total layers][T][top_k] or NULL
-    // exchange area in the workspace: data double buffered by layer parity,
-    // per-layer ready counters (zeroed before the first launch of a call)
-    float *logits_x;        // [2][T][E] router logits
-    uint32_t *h_x;          // [2][kDecodeMaxUnits][I/128][T][4][16] h' pairs in the down projection's B layout
-    float *out_x;           // [2][T][d] layer outputs
-    unsigned int *ready;    // [layers of the call][kDecodeReadySlots]
-    int *abort_flag;        // raised by the CTA whose wait ran out; the others give up too
+    const uint16_t *x_in;     // layer 0 input bf16 [T][d] (NULL for later layers)
+    const float *prev_out;    // previous layer output f32 [T][d] (NULL for layer 0)
+    float *out;               // this layer's output f32 [T][d]
+    uint16_t *x_export;       // bf16 [T][d] or NULL: normalised input of this layer (x_next of the previous)
+    float *trace_logits;      // [T][E] or NULL
+    int *trace_idx;           // [T][top_k] or NULL
+    float *trace_w;           // [T][top_k] or NULL
+    // workspace
+    uint16_t *x_cur;          // bf16 [T][d]
+    __half *xp;               // fp16 [8][d] layer input in the permuted B layout of the expert GEMVs (tokens >= T zero)
+    float *logits;            // [T][E]
+    int *n_units;             // [1]: distinct experts used + 1 (shared last)
+    int *unit_expert;         // [top_k*T+1]
+    int *unit_mask;           // [top_k*T+1] token bitmask
+    float *unit_w;            // [top_k*T+1][8]
+    __half *h;                // fp16 [top_k*T+1][8][I]
     Ctrl *ctrl;
-    DecodeLayerPtrs L[kDecodeLayersPerLaunch];
 };
-static_assert(sizeof(DecodeArgs) <= 4096, "decode kernel parameters stay within 4 KB");
-// Ring slots that fit next to the fixed shared memory for this shape (0: the
-// shape does not fit), the bytes of one slot, and the dynamic shared memory of
-// the launch.
-int decode_ring_slots(int T, int d, int I);
-int decode_launch_slots(int T, int d, int I);  // device-checked (needs the device current)
-int decode_slot_bytes(int d, int I);
-size_t decode_smem_bytes(int T, int d, int I, int n_slots);
-cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t stream);
+cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStream_t stream);
 
 }  // namespace lily

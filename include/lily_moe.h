@@ -73,8 +73,7 @@ enum {
  *   E = 256, top_k = 8, group = 64,
  *   d a multiple of 256 in [256, 16384], I a multiple of 128 in [128, 4096],
  *   I_shared = I, block_rows in {16, 32, 64, 128}, 0 <= T <= 1048576.
- * lily_moe_decode additionally needs 1 <= T <= 8, d <= 4096, I <= 1024 and
- * T * d <= 16384, and a GPU with at least max(E, d / 16) / 2 SMs.
+ * lily_moe_decode additionally needs 1 <= T <= 8, d <= 4096 and I <= 1024.
  */
 typedef struct lily_moe_shape {
     int32_t T;          /* tokens */
@@ -232,10 +231,10 @@ int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *
  *              the input of layer l+1 (a parameter-free RMS norm standing in
  *              for the attention / recurrent blocks between MoE layers)
  *   trace      optional per-layer routing record, or NULL
- * Enqueues one memset of the workspace's exchange area and one cooperative
- * kernel launch per 20 layers (one CTA per SM, every CTA resident; the layers
- * hand their data between CTAs through the workspace, without a grid-wide
- * barrier).  The result is bit-reproducible from run to run.
+ * The launches (three kernels per layer) are recorded once into a CUDA graph
+ * cached by argument values and replayed (unless `stream` is already
+ * capturing, then they are enqueued directly).  The result is bit-reproducible
+ * from run to run (no atomics; fixed summation order).
  */
 int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_moe_weights *layers,
                     const uint16_t *x, float *out, uint16_t *x_next,

@@ -77,7 +77,7 @@ def test_decode_repeat_call_is_bit_identical():
 
 
 def test_decode_more_layers_than_one_launch():
-    # 45 layers: three launches (20 + 20 + 5) continue one chain through the workspace
+    # a long chain: every layer's input is the normalised output of the one before
     cfg = CONFIGS["tiny"]
     _check_decode(cfg, n_layers=45, T=1)
 
