@@ -1,4 +1,5 @@
-"""fp64 CPU oracle of the mixture-of-experts layer: ctypes wrappers around oracle.c.
+"""fp64 CPU oracle of the mixture-of-experts layer and of grouped-query decode
+attention over a fixed-block KV cache: ctypes wrappers around oracle.c.
 
 TEST INFRASTRUCTURE ONLY.  Only tests, the smoke check and the benchmark's
 CPU-baseline leg may import this package.  The CUDA library never calls it and
@@ -62,6 +63,7 @@ def lib():
             L.oracle_route_tables.argtypes = [P, I64, I64, I64, I64, P, P, P, P, P]
             L.oracle_moe_tokens.argtypes = [ctypes.POINTER(OracleLayer), P, I64, P, P, P, I64, P]
             L.oracle_rms_norm.argtypes = [P, I64, I64, ctypes.c_double, P]
+            L.oracle_attn_decode.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_double, P]
             _lib = L
     return _lib
 
@@ -170,3 +172,31 @@ def rms_norm(out: np.ndarray, eps: float = 1e-6) -> np.ndarray:
     xn = np.empty_like(out)
     lib().oracle_rms_norm(_p(out), T, d, eps, _p(xn))
     return xn
+
+
+def attn_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_table: np.ndarray,
+                seq_lens: np.ndarray, scale: Optional[float] = None) -> np.ndarray:
+    """Grouped-query decode attention over a fixed-block KV cache, fp64.
+
+    q: bf16 bits [B][H_q][D]; k_cache, v_cache: bf16 bits [n_blocks][H_kv][bs][D];
+    block_table: int32 [B][max_blocks]; seq_lens: int32 [B].  Returns [B][H_q][D]
+    doubles: o_h = sum_t softmax_t(scale q_h . k_{g,t}) v_{g,t}, g = h / (H_q / H_kv).
+    """
+    q = _c(q, np.uint16)
+    k_cache = _c(k_cache, np.uint16)
+    v_cache = _c(v_cache, np.uint16)
+    block_table = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    B, H_q, D = q.shape
+    n_blocks, H_kv, bs, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape and H_q % H_kv == 0
+    assert block_table.shape[0] == B and seq_lens.shape == (B,)
+    assert int(seq_lens.max(initial=0)) <= block_table.shape[1] * bs
+    used = np.concatenate([block_table[b, :(int(seq_lens[b]) + bs - 1) // bs] for b in range(B)])
+    assert used.size == 0 or (used.min() >= 0 and used.max() < n_blocks)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    out = np.empty((B, H_q, D), np.float64)
+    lib().oracle_attn_decode(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(seq_lens), B, H_q, H_kv, D, bs,
+                             block_table.shape[1], float(scale), _p(out))
+    return out

@@ -1,5 +1,6 @@
 /*
- * fp64 CPU oracle of one mixture-of-experts (MoE) layer.
+ * fp64 CPU oracle of one mixture-of-experts (MoE) layer, and of the grouped-
+ * query decode attention of the model's full-attention layers (at the end).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
  * this file; only the tests, the smoke check and the benchmark's CPU-baseline leg
@@ -274,5 +275,67 @@ void oracle_rms_norm(const double *out, int64_t T, int64_t d, double eps, double
         for (int64_t c = 0; c < d; ++c) ss += out[t * d + c] * out[t * d + c];
         double inv = 1.0 / sqrt(ss / (double)d + eps);
         for (int64_t c = 0; c < d; ++c) xn[t * d + c] = out[t * d + c] * inv;
+    }
+}
+
+/*
+ * Decode attention over a KV cache stored in fixed-size blocks (grouped-query
+ * attention), one step for each of B sequences.
+ *
+ * Source of the method: the page "Perplexity libera o Lily" (noticiai.com.br):
+ *   - section "O modelo em tres formatos de carga": the full-attention layers
+ *     use grouped-query attention with 16 query heads and two KV heads, over a
+ *     growing KV cache;
+ *   - section "Prefill e decode: onde estao os ganhos": decode packs the query
+ *     heads of a KV head together (GQA packing), reads the cache coalesced, and
+ *     keeps it in a fixed-block layout.
+ * Readings where the page is silent: plain scaled dot-product attention,
+ *   o_h = sum_t softmax_t(scale * q_h . k_{g,t}) v_{g,t},  g = h / (H_q / H_kv),
+ * with the caller's scale (1/sqrt(D) by default); K and V of token t of a
+ * sequence sit in cache block block_table[t / bs], row t % bs of that block,
+ * laid out [block][kv head][row][D].
+ *
+ * q: bf16 [B][H_q][D]; k_cache, v_cache: bf16 [n_blocks][H_kv][bs][D];
+ * block_table: [B][max_blocks]; seq_lens: [B] (>= 1); out: [B][H_q][D] doubles.
+ */
+void oracle_attn_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *block_table, const int32_t *seq_lens,
+                        int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t bs, int64_t max_blocks,
+                        double scale, double *out)
+{
+    const int64_t group = H_q / H_kv;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t h = 0; h < H_q; ++h) {
+            const int64_t g = h / group;
+            const int64_t L = seq_lens[b];
+            const uint16_t *qh = q + (b * H_q + h) * D;
+            double *o = out + (b * H_q + h) * D;
+            double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+            /* scores */
+            double m = -INFINITY;
+            for (int64_t t = 0; t < L; ++t) {
+                const int64_t blk = block_table[b * max_blocks + t / bs];
+                const uint16_t *kt = k_cache + ((blk * H_kv + g) * bs + t % bs) * D;
+                double dot = 0.0;
+                for (int64_t c = 0; c < D; ++c) dot += bf16_value(qh[c]) * bf16_value(kt[c]);
+                s[t] = scale * dot;
+                if (s[t] > m) m = s[t];
+            }
+            /* softmax weights and the weighted sum of values */
+            double den = 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                s[t] = exp(s[t] - m);
+                den += s[t];
+            }
+            for (int64_t c = 0; c < D; ++c) o[c] = 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                const int64_t blk = block_table[b * max_blocks + t / bs];
+                const uint16_t *vt = v_cache + ((blk * H_kv + g) * bs + t % bs) * D;
+                const double w = s[t] / den;
+                for (int64_t c = 0; c < D; ++c) o[c] += w * bf16_value(vt[c]);
+            }
+            free(s);
+        }
     }
 }
