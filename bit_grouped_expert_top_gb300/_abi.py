@@ -9,6 +9,7 @@ fallback: if the library cannot be loaded, the first call raises.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import threading
 from typing import Dict, Optional, Sequence
@@ -51,6 +52,10 @@ class lily_moe_routing(ctypes.Structure):
                 ("logits", "topk_idx", "topk_w", "counts", "offsets", "perm", "block_map", "n_blocks")]
 
 
+class lily_attn_shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "H_q", "H_kv", "D", "block_size", "max_blocks")]
+
+
 class lily_moe_decode_trace(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("logits", "topk_idx", "topk_w")]
 
@@ -75,6 +80,11 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.lily_moe_forward_timed.argtypes = [PS, PW, P, P, PR, P, S, P, ctypes.POINTER(ctypes.c_void_p)]
     L.lily_moe_decode.argtypes = [PS, ctypes.c_int32, PW, P, P, P, ctypes.POINTER(lily_moe_decode_trace), P, S, P]
     L.lily_moe_route_noalloc.argtypes = [PS, PW, P, PR, P, P]
+    PA = ctypes.POINTER(lily_attn_shape)
+    L.lily_attn_workspace_bytes.restype = S
+    L.lily_attn_workspace_bytes.argtypes = [PA]
+    L.lily_attn_decode.argtypes = [PA, P, P, P, I64, P, P, ctypes.c_float, P, P, S, P]
+    L.lily_attn_decode.restype = I32
     L.lily_moe_device_status.argtypes = [P, P]
     L.lily_moe_clear_status.argtypes = [P, P]
     for n in ("lily_moe_check_shape", "lily_moe_route", "lily_moe_grouped_gemm", "lily_moe_forward",
@@ -279,3 +289,32 @@ def lily_moe_route_noalloc(shape, weights, x, routing, device_status=None, strea
     rc = load().lily_moe_route_noalloc(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), ctypes.byref(routing),
                                        _ptr(device_status), _stream(stream))
     return _check("lily_moe_route_noalloc", rc) if check else rc
+
+
+# ------------------------------------------------------------------ decode attention
+def make_attn_shape(B: int, H_q: int, H_kv: int, D: int, block_size: int, max_blocks: int) -> lily_attn_shape:
+    return lily_attn_shape(B, H_q, H_kv, D, block_size, max_blocks)
+
+
+def lily_attn_workspace_bytes(shape: lily_attn_shape) -> int:
+    return load().lily_attn_workspace_bytes(ctypes.byref(shape))
+
+
+def alloc_attn_workspace(shape: lily_attn_shape, device="cuda") -> torch.Tensor:
+    n = lily_attn_workspace_bytes(shape)
+    if n == 0:
+        raise ValueError("unsupported attention shape")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def lily_attn_decode(shape: lily_attn_shape, q, k_cache, v_cache, block_table, seq_lens, out, ws,
+                     scale: Optional[float] = None, stream=None, *, check: bool = True) -> int:
+    """Grouped-query decode attention over a fixed-block KV cache (see
+    include/lily_moe.h).  scale defaults to 1/sqrt(D)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(shape.D)
+    n_blocks = k_cache.shape[0] if isinstance(k_cache, torch.Tensor) else 0
+    rc = load().lily_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache), n_blocks,
+                                 _ptr(block_table), _ptr(seq_lens), float(scale), _ptr(out), _ptr(ws),
+                                 ws.numel() if isinstance(ws, torch.Tensor) else 0, _stream(stream))
+    return _check("lily_attn_decode", rc) if check else rc

@@ -3,8 +3,10 @@
 // launch sequence of each call.  No entry point allocates device memory or
 // synchronises, except lily_moe_device_status.
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <set>
 #include <string>
@@ -24,17 +26,20 @@ cudaError_t launch_decode_final_norm(const float *prev_out, uint16_t *x_export, 
 
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes)
 {
+    // The attribute only ever grows: a launch with less shared memory than the
+    // limit is fine, so the largest size asked for so far is what is set.
     static std::mutex mu;
-    static std::set<std::tuple<const void *, int, unsigned long long, int>> done;  // (kernel, device, context, bytes)
+    static std::map<std::tuple<const void *, int, unsigned long long>, int> set_to;  // (kernel, device, context)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long ctx_id = current_context_id();
-    const auto key = std::make_tuple(kernel, dev, ctx_id, bytes);
+    const auto key = std::make_tuple(kernel, dev, ctx_id);
     std::lock_guard<std::mutex> lock(mu);
-    if (done.count(key)) return cudaSuccess;
+    auto it = set_to.find(key);
+    if (it != set_to.end() && it->second >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess && ctx_id != 0) done.insert(key);
+    if (e == cudaSuccess && ctx_id != 0) set_to[key] = bytes;
     return e;
 }
 }  // namespace lily
@@ -148,6 +153,49 @@ DecodeLayout decode_layout(const lily_moe_shape &s)
     L.unit_mask = take(U * 4);
     L.unit_w = take(U * 8 * 4);
     L.h = take(U * 8 * s.I * 2);
+    L.total = off;
+    return L;
+}
+
+// ------------------------------------------------------------------ decode attention
+constexpr int kAttnMaxSplits = 256;
+
+int attn_check_shape(const lily_attn_shape *s)
+{
+    if (!s) return LILY_ERR_INVALID;
+    if (s->B < 1 || s->H_q < 1 || s->H_kv < 1 || s->max_blocks < 1 || s->H_q % s->H_kv != 0) return LILY_ERR_INVALID;
+    if (s->H_q / s->H_kv > kAttnMaxGroup || attn_stages(s->D, s->block_size) == 0) return LILY_ERR_UNSUPPORTED;
+    return LILY_OK;
+}
+
+// Splits per (sequence, KV head): about one CTA per SM in all, at most one per
+// cache block of the longest sequence.
+int attn_splits(const lily_attn_shape &s, int sms)
+{
+    const int per = static_cast<int>(ceil_div(sms, static_cast<int64_t>(s.B) * s.H_kv));
+    return std::max(1, std::min({per, s.max_blocks, kAttnMaxSplits}));
+}
+
+// Workspace: control block, then the partials of every (sequence, KV head,
+// split) for up to kAttnMaxSplits splits (or max_blocks, if fewer).
+struct AttnLayout {
+    size_t ctrl, part_ml, part_acc, total;
+};
+
+AttnLayout attn_layout(const lily_attn_shape &s)
+{
+    const int64_t S = std::min(s.max_blocks, kAttnMaxSplits);
+    const int64_t units = static_cast<int64_t>(s.B) * s.H_kv * S * kAttnMaxGroup;
+    AttnLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + std::max<size_t>(bytes, 1));
+        return at;
+    };
+    L.ctrl = take(sizeof(Ctrl));
+    L.part_ml = take(units * 2 * 4);
+    L.part_acc = take(units * s.D * 4);
     L.total = off;
     return L;
 }
@@ -692,6 +740,51 @@ int lily_moe_decode(const lily_moe_shape *shape, int32_t n_layers, const lily_mo
         it = gc.execs.emplace(key, exec).first;
     }
     return to_status(cudaGraphLaunch(it->second, stream), "cudaGraphLaunch (decode)");
+}
+
+size_t lily_attn_workspace_bytes(const lily_attn_shape *shape)
+{
+    if (attn_check_shape(shape) != LILY_OK) return 0;
+    return attn_layout(*shape).total;
+}
+
+int lily_attn_decode(const lily_attn_shape *shape, const uint16_t *q, const uint16_t *k_cache,
+                     const uint16_t *v_cache, int64_t n_cache_blocks, const int32_t *block_table,
+                     const int32_t *seq_lens, float scale, float *out, void *ws, size_t ws_bytes,
+                     cudaStream_t stream)
+{
+    int rc;
+    if ((rc = attn_check_shape(shape))) return rc;
+    const lily_attn_shape s = *shape;
+    if (n_cache_blocks < 1 || !std::isfinite(scale)) return LILY_ERR_INVALID;
+    if (n_cache_blocks * s.H_kv * s.block_size >= (int64_t(1) << 31)) return LILY_ERR_UNSUPPORTED;
+    const AttnLayout L = attn_layout(s);
+    if ((rc = check_ws(ws, ws_bytes, L.total))) return rc;
+    for (const void *p : {static_cast<const void *>(q), static_cast<const void *>(k_cache),
+                          static_cast<const void *>(v_cache), static_cast<const void *>(block_table),
+                          static_cast<const void *>(seq_lens), static_cast<const void *>(out)})
+        if ((rc = check_ptr(p))) return rc;
+    const uint64_t rows = static_cast<uint64_t>(n_cache_blocks) * s.H_kv * s.block_size;
+    CUtensorMap tmK, tmV;
+    if (!make_tmap(&tmK, k_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.D, rows, 64, s.block_size,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap(&tmV, v_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.D, rows, 64, s.block_size,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled (KV cache)");
+    AttnArgs a{};
+    a.B = s.B; a.H_q = s.H_q; a.H_kv = s.H_kv; a.D = s.D; a.bs = s.block_size; a.max_blocks = s.max_blocks;
+    a.group = s.H_q / s.H_kv;
+    a.n_splits = attn_splits(s, num_sms_current());
+    a.n_cache_blocks = n_cache_blocks;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.q = q;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.part_ml = at<float>(ws, L.part_ml);
+    a.part_acc = at<float>(ws, L.part_acc);
+    a.out = out;
+    a.ctrl = at<Ctrl>(ws, L.ctrl);
+    return to_status(launch_attn_decode(a, tmK, tmV, stream), "attention launch");
 }
 
 int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,

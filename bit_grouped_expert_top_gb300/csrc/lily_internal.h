@@ -66,9 +66,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
-// device.  Function attributes belong to a device, so this runs once per
-// (kernel, device, size); safe to call from several host threads.
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device (never lowers it: the limit is the largest size asked for in
+// this context).  Safe to call from several host threads.
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
 
 // Dynamic shared memory bytes of grouped_gemm_kernel.
@@ -135,5 +135,30 @@ struct DecodeLayerArgs {
     Ctrl *ctrl;
 };
 cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStream_t stream);
+
+// Grouped-query decode attention over a fixed-block KV cache (attention.cu).
+// Split-K: CTA (split s, KV head g, sequence b) takes the cache blocks
+// [s nblk / S, (s + 1) nblk / S) of sequence b and all query heads of group g,
+// and writes an unnormalised partial (running max in log2 units, sum of
+// weights, weighted sum of values); the combine kernel merges the splits.
+struct AttnArgs {
+    int B, H_q, H_kv, D, bs, max_blocks, n_splits, group;
+    long long n_cache_blocks;
+    float scale_log2;           // scale * log2(e)
+    const uint16_t *q;          // bf16 [B][H_q][D]
+    const int *block_table;     // [B][max_blocks]
+    const int *seq_lens;        // [B]
+    float *part_ml;             // [B][H_kv][S][8][2]: max (log2 units), sum of weights
+    float *part_acc;            // [B][H_kv][S][8][D]
+    float *out;                 // [B][H_q][D]
+    Ctrl *ctrl;
+};
+constexpr int kAttnMaxGroup = 8;  // query heads per KV head (the N = 8 side of the MMA)
+// Ring stages of K+V block tiles for this shape (0: unsupported), and the
+// dynamic shared memory of the split kernel.
+int attn_stages(int D, int bs);
+size_t attn_smem_bytes(int D, int bs);
+// tmK / tmV: the caches as 2-D bf16 [n_blocks * H_kv * bs][D], box 64 x bs, 128-byte swizzle.
+cudaError_t launch_attn_decode(const AttnArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t stream);
 
 }  // namespace lily

@@ -252,6 +252,55 @@ int lily_moe_device_status(const void *ws, cudaStream_t stream);
 int lily_moe_clear_status(void *ws, cudaStream_t stream);
 
 /*
+ * Grouped-query decode attention over a fixed-block KV cache: one decode step
+ * of the model's full-attention layers for B sequences.
+ *
+ * Method: the page "Perplexity libera o Lily" (noticiai.com.br), section "O
+ * modelo em tres formatos de carga" (grouped-query attention, 16 query heads
+ * over two KV heads, a growing KV cache) and section "Prefill e decode: onde
+ * estao os ganhos" (query heads of a KV head packed together, coalesced cache
+ * reads, a fixed-block cache layout).  For each sequence b and query head h,
+ * with group = H_q / H_kv and g = h / group:
+ *   out[b][h] = sum_t softmax_t(scale * q[b][h] . K_g[t]) V_g[t],
+ * over the sequence's tokens t < seq_lens[b]; K_g[t] / V_g[t] is row t % bs of
+ * cache block block_table[b][t / bs], KV head g.  Computed with bf16 inputs,
+ * fp32 scores and accumulation; the softmax weights are rounded to bf16 before
+ * they multiply V (their sum is taken over the rounded values).
+ *
+ * Layouts (row-major, device memory, all 16-byte aligned):
+ *   q         bf16 [B][H_q][D] (positional rotation already applied)
+ *   k_cache   bf16 [n_cache_blocks][H_kv][block_size][D]; v_cache the same
+ *   block_table int32 [B][max_blocks]: physical block of each logical block
+ *   seq_lens  int32 [B]: tokens in each sequence's cache, 0..max_blocks*block_size
+ *   out       f32 [B][H_q][D]; a sequence with no tokens gets zeros
+ * Supported: D in {64, 128, 256}; block_size in {32, 64, 128} with
+ * block_size * D <= 16384; H_q % H_kv == 0 and H_q / H_kv <= 8;
+ * n_cache_blocks * H_kv * block_size < 2^31.
+ * Device-detected: a used table entry outside [0, n_cache_blocks) or a length
+ * outside [0, max_blocks * block_size] records LILY_ERR_DEVICE_INDEX (read it
+ * with lily_moe_device_status on the same workspace); the kernels then read
+ * block 0 / clamp the length instead.
+ * Enqueues two kernels (split and combine) on `stream`; no host sync.  The
+ * result is bit-reproducible from run to run.
+ */
+typedef struct lily_attn_shape {
+    int32_t B;           /* sequences */
+    int32_t H_q, H_kv;   /* query heads, KV heads */
+    int32_t D;           /* head dimension */
+    int32_t block_size;  /* tokens per cache block */
+    int32_t max_blocks;  /* columns of block_table */
+} lily_attn_shape;
+
+/* Workspace bytes of lily_attn_decode (0: unsupported shape). */
+size_t lily_attn_workspace_bytes(const lily_attn_shape *shape);
+
+/* scale: multiplies q . k (1 / sqrt(D) for plain scaled dot-product attention). */
+int lily_attn_decode(const lily_attn_shape *shape, const uint16_t *q, const uint16_t *k_cache,
+                     const uint16_t *v_cache, int64_t n_cache_blocks, const int32_t *block_table,
+                     const int32_t *seq_lens, float scale, float *out, void *ws, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/*
  * Routing without a caller workspace.  The method has no counterpart: this entry
  * point exists for callers that may not allocate device memory when they call
  * the layer, e.g. a plugin that runs inside another engine's fixed memory
