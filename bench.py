@@ -324,6 +324,48 @@ def bench_decode(cfg, Ts, reps, stream, peaks):
     return res
 
 
+def bench_attention(names, reps, stream, peaks):
+    """µs per call of lily_attn_decode (batch-1 grouped-query decode attention)
+    at the given context lengths, against HBM on the K/V bytes read; the caches
+    of n_sets workloads are cycled so that the bytes of consecutive calls
+    exceed L2."""
+    import torch
+    import bit_grouped_expert_top_gb300 as lm
+    from bit_grouped_expert_top_gb300.attn_inputs import ATTN_CONFIGS, kv_bytes, make_attn
+    res = {}
+    for name in names:
+        cfg = ATTN_CONFIGS[name]
+        sets = [{k: v.cuda() for k, v in make_attn(cfg, "cpu", i).items()} for i in range(cfg.n_sets)]
+        s = lm.make_attn_shape(cfg.B, cfg.H_q, cfg.H_kv, cfg.D, cfg.block_size, cfg.max_blocks)
+        ws = lm.alloc_attn_workspace(s)
+        out = torch.empty((cfg.B, cfg.H_q, cfg.D), dtype=torch.float32, device="cuda")
+        stream.wait_stream(torch.cuda.current_stream())
+
+        def call(a):
+            lm.lily_attn_decode(s, a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["seq_lens"], out, ws,
+                                stream=stream)
+        for i in range(3 * cfg.n_sets):
+            call(sets[i % cfg.n_sets])
+        stream.synchronize()
+        assert lm.lily_moe_device_status(ws, stream) == 0
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            call(sets[i % cfg.n_sets])
+        b.record(stream)
+        b.synchronize()
+        us = a.elapsed_time(b) * 1e3 / reps
+        nbytes = kv_bytes(cfg)
+        res[name] = {"context_tokens": sum(cfg.seq_lens), "heads": f"{cfg.H_q}q/{cfg.H_kv}kv", "D": cfg.D,
+                     "block_size": cfg.block_size, "us_per_call": round(us, 2), "kv_bytes": nbytes,
+                     "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "frac_of_hbm": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                     "bytes_cycled": nbytes * cfg.n_sets}
+        del sets
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -396,6 +438,7 @@ def run_ours(args):
             del cx
         torch.cuda.empty_cache()
         also["decode_l40"] = bench_decode(CONFIGS["decode_t1_l40"], (1, 2, 4, 8), 20, stream, peaks)
+        also["attn_decode"] = bench_attention(("attn_32k", "attn_64k", "attn_128k"), 50, stream, peaks)
 
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,

@@ -158,8 +158,6 @@ DecodeLayout decode_layout(const lily_moe_shape &s)
 }
 
 // ------------------------------------------------------------------ decode attention
-constexpr int kAttnMaxSplits = 256;
-
 int attn_check_shape(const lily_attn_shape *s)
 {
     if (!s) return LILY_ERR_INVALID;

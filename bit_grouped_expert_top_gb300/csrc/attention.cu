@@ -348,34 +348,60 @@ attn_split_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CU
     }
 }
 
-// One CTA per (sequence, query head), one thread per element of D: the splits'
-// partials rescaled to their common max, o = sum_s 2^(m_s - m) O_s / sum_s
-// 2^(m_s - m) l_s (splits without tokens skipped; a sequence without tokens
-// gives zeros).
+// Merges the splits: o = sum_s 2^(m_s - m) O_s / sum_s 2^(m_s - m) l_s over the
+// splits that saw tokens (a sequence without tokens gives zeros).  CTA
+// (sequence x query head, 64-wide slice of D), 256 threads: the splits' weights
+// 2^(m_s - m) / den go to shared memory first; then four groups of 64 threads
+// (one per element of the slice) sum every fourth split, so each thread keeps
+// several independent loads in flight, and the four partial sums are added.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a)
 {
+    __shared__ float wsplit[kAttnMaxSplits];
+    __shared__ float part[4][64];
+    __shared__ float s_m, s_den;
     const int b = blockIdx.x / a.H_q, h = blockIdx.x - b * a.H_q;
     const int g = h / a.group, n = h - g * a.group;
+    const int tid = threadIdx.x, lane = tid & 31;
     pdl_trigger();
     pdl_wait();  // the split kernel is complete
     const size_t p0 = (static_cast<size_t>(b) * a.H_kv + g) * a.n_splits;
-    float m = -INFINITY;
-    for (int s = 0; s < a.n_splits; ++s) {
-        const float *ml = a.part_ml + (p0 + s) * kAttnMaxGroup * 2 + n * 2;
-        if (ml[1] > 0.0f) m = fmaxf(m, ml[0]);
-    }
-    float den = 0.0f;
-    for (int s = 0; s < a.n_splits; ++s) {
-        const float *ml = a.part_ml + (p0 + s) * kAttnMaxGroup * 2 + n * 2;
-        if (ml[1] > 0.0f) den += exp2f(ml[0] - m) * ml[1];
-    }
-    for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
-        float num = 0.0f;
-        for (int s = 0; s < a.n_splits; ++s) {
+    const int S = a.n_splits;
+    if (tid < 32) {
+        float m = -INFINITY;
+        for (int s = lane; s < S; s += 32) {
             const float *ml = a.part_ml + (p0 + s) * kAttnMaxGroup * 2 + n * 2;
-            if (ml[1] > 0.0f) num += exp2f(ml[0] - m) * a.part_acc[((p0 + s) * kAttnMaxGroup + n) * a.D + d];
+            if (ml[1] > 0.0f) m = fmaxf(m, ml[0]);
         }
-        a.out[(static_cast<size_t>(b) * a.H_q + h) * a.D + d] = den > 0.0f ? num / den : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float den = 0.0f;
+        for (int s = lane; s < S; s += 32) {
+            const float *ml = a.part_ml + (p0 + s) * kAttnMaxGroup * 2 + n * 2;
+            const float w = ml[1] > 0.0f ? exp2f(ml[0] - m) : 0.0f;
+            wsplit[s] = w;
+            den += w * ml[1];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (lane == 0) {
+            s_m = m;
+            s_den = den;
+        }
+    }
+    __syncthreads();
+    const int sg = tid >> 6, d = blockIdx.y * 64 + (tid & 63);
+    float num = 0.0f;
+    if (d < a.D) {
+        const float *acc = a.part_acc + (p0 * kAttnMaxGroup + n) * a.D + d;
+#pragma unroll 4
+        for (int s = sg; s < S; s += 4)
+            if (wsplit[s] != 0.0f) num += wsplit[s] * acc[static_cast<size_t>(s) * kAttnMaxGroup * a.D];
+    }
+    part[sg][tid & 63] = num;
+    __syncthreads();
+    if (tid < 64 && d < a.D) {
+        const float t = part[0][tid] + part[1][tid] + part[2][tid] + part[3][tid];
+        a.out[(static_cast<size_t>(b) * a.H_q + h) * a.D + d] = s_den > 0.0f ? t / s_den : 0.0f;
     }
 }
 
@@ -395,7 +421,7 @@ cudaError_t launch_attn_decode(const AttnArgs &a, const CUtensorMap &tmK, const 
     if (e != cudaSuccess) return e;
     e = launch_pdl(attn_split_kernel, dim3(a.n_splits, a.H_kv, a.B), dim3(kAttnThreads), smem, stream, a, tmK, tmV);
     if (e != cudaSuccess) return e;
-    return launch_pdl(attn_combine_kernel, dim3(a.B * a.H_q), dim3(std::min(a.D, 256)), 0, stream, a);
+    return launch_pdl(attn_combine_kernel, dim3(a.B * a.H_q, (a.D + 63) / 64), dim3(256), 0, stream, a);
 }
 
 }  // namespace lily

@@ -153,7 +153,8 @@ struct AttnArgs {
     float *out;                 // [B][H_q][D]
     Ctrl *ctrl;
 };
-constexpr int kAttnMaxGroup = 8;  // query heads per KV head (the N = 8 side of the MMA)
+constexpr int kAttnMaxGroup = 8;    // query heads per KV head (the N = 8 side of the MMA)
+constexpr int kAttnMaxSplits = 256; // splits per (sequence, KV head)
 // Ring stages of K+V block tiles for this shape (0: unsupported), and the
 // dynamic shared memory of the split kernel.
 int attn_stages(int D, int bs);
