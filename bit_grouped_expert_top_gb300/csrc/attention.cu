@@ -350,15 +350,16 @@ attn_split_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CU
 
 // Merges the splits: o = sum_s 2^(m_s - m) O_s / sum_s 2^(m_s - m) l_s over the
 // splits that saw tokens (a sequence without tokens gives zeros).  CTA
-// (sequence x query head, 64-wide slice of D), 256 threads: the splits' weights
-// 2^(m_s - m) / den go to shared memory first; then four groups of 64 threads
-// (one per element of the slice) sum every fourth split, so each thread keeps
-// several independent loads in flight, and the four partial sums are added.
+// (sequence x query head, 64-wide slice of D), 256 threads.  Warp 0 loads every
+// split's (m, l) at once (up to 8 per lane), forms the common max and the
+// denominator, and leaves the splits' weights in shared memory; then four
+// groups of 64 threads (one per element of the slice) each take every fourth
+// split, issuing their loads 16 at a time, and the four partial sums are added.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a)
 {
     __shared__ float wsplit[kAttnMaxSplits];
     __shared__ float part[4][64];
-    __shared__ float s_m, s_den;
+    __shared__ float s_den;
     const int b = blockIdx.x / a.H_q, h = blockIdx.x - b * a.H_q;
     const int g = h / a.group, n = h - g * a.group;
     const int tid = threadIdx.x, lane = tid & 31;
@@ -367,35 +368,55 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a)
     const size_t p0 = (static_cast<size_t>(b) * a.H_kv + g) * a.n_splits;
     const int S = a.n_splits;
     if (tid < 32) {
-        float m = -INFINITY;
-        for (int s = lane; s < S; s += 32) {
-            const float *ml = a.part_ml + (p0 + s) * kAttnMaxGroup * 2 + n * 2;
-            if (ml[1] > 0.0f) m = fmaxf(m, ml[0]);
+        float ms[kAttnMaxSplits / 32], ls[kAttnMaxSplits / 32];
+#pragma unroll
+        for (int k = 0; k < kAttnMaxSplits / 32; ++k) {
+            const int s = lane + 32 * k;
+            ms[k] = -INFINITY;
+            ls[k] = 0.0f;
+            if (s < S) {
+                const float2 ml = *reinterpret_cast<const float2 *>(a.part_ml + (p0 + s) * kAttnMaxGroup * 2 + n * 2);
+                ms[k] = ml.x;
+                ls[k] = ml.y;
+            }
         }
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kAttnMaxSplits / 32; ++k)
+            if (ls[k] > 0.0f) m = fmaxf(m, ms[k]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float den = 0.0f;
-        for (int s = lane; s < S; s += 32) {
-            const float *ml = a.part_ml + (p0 + s) * kAttnMaxGroup * 2 + n * 2;
-            const float w = ml[1] > 0.0f ? exp2f(ml[0] - m) : 0.0f;
-            wsplit[s] = w;
-            den += w * ml[1];
+#pragma unroll
+        for (int k = 0; k < kAttnMaxSplits / 32; ++k) {
+            const int s = lane + 32 * k;
+            const float w = ls[k] > 0.0f ? exp2f(ms[k] - m) : 0.0f;
+            if (s < S) wsplit[s] = w;
+            den += w * ls[k];
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        if (lane == 0) {
-            s_m = m;
-            s_den = den;
-        }
+        if (lane == 0) s_den = den;
     }
     __syncthreads();
     const int sg = tid >> 6, d = blockIdx.y * 64 + (tid & 63);
     float num = 0.0f;
     if (d < a.D) {
         const float *acc = a.part_acc + (p0 * kAttnMaxGroup + n) * a.D + d;
-#pragma unroll 4
-        for (int s = sg; s < S; s += 4)
-            if (wsplit[s] != 0.0f) num += wsplit[s] * acc[static_cast<size_t>(s) * kAttnMaxGroup * a.D];
+        const size_t stride = static_cast<size_t>(kAttnMaxGroup) * a.D;
+        for (int s0 = sg; s0 < S; s0 += 64) {
+            float v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int s = s0 + 4 * k;
+                v[k] = s < S ? acc[static_cast<size_t>(s) * stride] : 0.0f;
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int s = s0 + 4 * k;
+                if (s < S) num += wsplit[s] * v[k];
+            }
+        }
     }
     part[sg][tid & 63] = num;
     __syncthreads();
