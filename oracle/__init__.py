@@ -1,5 +1,6 @@
-"""fp64 CPU oracle of the mixture-of-experts layer and of grouped-query decode
-attention over a fixed-block KV cache: ctypes wrappers around oracle.c.
+"""fp64 CPU oracle of the mixture-of-experts layer, of grouped-query decode
+attention over a fixed-block KV cache and of the Gated DeltaNet scan: ctypes
+wrappers around oracle.c.
 
 TEST INFRASTRUCTURE ONLY.  Only tests, the smoke check and the benchmark's
 CPU-baseline leg may import this package.  The CUDA library never calls it and
@@ -64,6 +65,7 @@ def lib():
             L.oracle_moe_tokens.argtypes = [ctypes.POINTER(OracleLayer), P, I64, P, P, P, I64, P]
             L.oracle_rms_norm.argtypes = [P, I64, I64, ctypes.c_double, P]
             L.oracle_attn_decode.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_double, P]
+            L.oracle_gdn_scan.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, ctypes.c_double, P, P]
             _lib = L
     return _lib
 
@@ -200,3 +202,28 @@ def attn_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_t
     lib().oracle_attn_decode(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(seq_lens), B, H_q, H_kv, D, bs,
                              block_table.shape[1], float(scale), _p(out))
     return out
+
+
+def gdn_scan(q: np.ndarray, k: np.ndarray, v: np.ndarray, alpha: np.ndarray, beta: np.ndarray,
+             S0: Optional[np.ndarray] = None, scale: float = 1.0) -> Tuple[np.ndarray, np.ndarray]:
+    """Gated DeltaNet scan over T tokens, fp64.
+
+    q, k: bf16 bits [T][H_k][d_k]; v: bf16 bits [T][H_v][d_v]; alpha, beta: f32
+    [T][H_v]; S0: [H_v][d_v][d_k] or None (zeros).  Returns (o [T][H_v][d_v],
+    S_T [H_v][d_v][d_k]) with S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t
+    S_{t-1} k_t) k_t^T and o_t = scale S_t q_t.
+    """
+    q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    alpha, beta = _c(alpha, np.float32), _c(beta, np.float32)
+    T, H_k, dk = q.shape
+    T2, H_v, dv = v.shape
+    assert k.shape == q.shape and T2 == T and H_v % H_k == 0
+    assert alpha.shape == (T, H_v) and beta.shape == (T, H_v)
+    if S0 is not None:
+        S0 = _c(S0, np.float64)
+        assert S0.shape == (H_v, dv, dk)
+    o = np.empty((T, H_v, dv), np.float64)
+    S = np.empty((H_v, dv, dk), np.float64)
+    lib().oracle_gdn_scan(_p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(S0), T, H_k, H_v, dk, dv, float(scale),
+                          _p(o), _p(S))
+    return o, S

@@ -1,6 +1,7 @@
 /*
- * fp64 CPU oracle of one mixture-of-experts (MoE) layer, and of the grouped-
- * query decode attention of the model's full-attention layers (at the end).
+ * fp64 CPU oracle of one mixture-of-experts (MoE) layer, of the grouped-query
+ * decode attention of the model's full-attention layers and of the Gated
+ * DeltaNet scan of its linear-attention layers (the last two at the end).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
  * this file; only the tests, the smoke check and the benchmark's CPU-baseline leg
@@ -337,5 +338,58 @@ void oracle_attn_decode(const uint16_t *q, const uint16_t *k_cache, const uint16
             }
             free(s);
         }
+    }
+}
+
+/*
+ * Gated DeltaNet scan: the fixed-size recurrence of the model's linear-attention
+ * layers, over T tokens of one sequence.
+ *
+ * Source: the page "Perplexity libera o Lily" (noticiai.com.br), section "O
+ * modelo em tres formatos de carga" (30 Gated DeltaNet layers: a recurrence of
+ * fixed size) and section "Prefill e decode: onde estao os ganhos" (a scan
+ * with the recurrent state held in registers).  The page gives no formula;
+ * the reading is the gated delta rule of Gated DeltaNet.  Per value head h
+ * (key head hk = h / (H_v / H_k)), state S (d_v x d_k), token t:
+ *   S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T
+ *       (= S_{t-1} alpha_t (I - beta_t k_t k_t^T) + beta_t v_t k_t^T)
+ *   o_t = scale S_t q_t
+ * q, k: bf16 [T][H_k][d_k]; v: bf16 [T][H_v][d_v]; alpha, beta: f32 [T][H_v];
+ * S0: [H_v][d_v][d_k] doubles or NULL (zeros); o: [T][H_v][d_v] doubles;
+ * S_out: [H_v][d_v][d_k] doubles (the state after the last token).
+ */
+void oracle_gdn_scan(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                     const float *beta, const double *S0, int64_t T, int64_t H_k, int64_t H_v, int64_t dk,
+                     int64_t dv, double scale, double *o, double *S_out)
+{
+    const int64_t group = H_v / H_k;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t h = 0; h < H_v; ++h) {
+        const int64_t hk = h / group;
+        double *S = S_out + h * dv * dk;
+        double *kv = (double *)malloc(sizeof(double) * (size_t)dk);
+        double *qv = (double *)malloc(sizeof(double) * (size_t)dk);
+        for (int64_t i = 0; i < dv * dk; ++i) S[i] = S0 ? S0[h * dv * dk + i] : 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            const double a = (double)alpha[t * H_v + h], b = (double)beta[t * H_v + h];
+            for (int64_t j = 0; j < dk; ++j) {
+                kv[j] = bf16_value(k[(t * H_k + hk) * dk + j]);
+                qv[j] = bf16_value(q[(t * H_k + hk) * dk + j]);
+            }
+            for (int64_t i = 0; i < dv; ++i) {
+                double *row = S + i * dk;
+                double u = 0.0;                                   /* (S_{t-1} k_t)_i */
+                for (int64_t j = 0; j < dk; ++j) u += row[j] * kv[j];
+                const double c = b * (bf16_value(v[(t * H_v + h) * dv + i]) - a * u);
+                double oi = 0.0;
+                for (int64_t j = 0; j < dk; ++j) {
+                    row[j] = a * row[j] + c * kv[j];
+                    oi += row[j] * qv[j];
+                }
+                o[(t * H_v + h) * dv + i] = scale * oi;
+            }
+        }
+        free(kv);
+        free(qv);
     }
 }
