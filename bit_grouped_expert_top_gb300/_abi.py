@@ -56,6 +56,10 @@ class lily_attn_shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("B", "H_q", "H_kv", "D", "block_size", "max_blocks")]
 
 
+class lily_gdn_shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "H_k", "H_v", "d_k", "d_v")]
+
+
 class lily_moe_decode_trace(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("logits", "topk_idx", "topk_w")]
 
@@ -85,6 +89,8 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.lily_attn_workspace_bytes.argtypes = [PA]
     L.lily_attn_decode.argtypes = [PA, P, P, P, I64, P, P, ctypes.c_float, P, P, S, P]
     L.lily_attn_decode.restype = I32
+    L.lily_gdn_scan.argtypes = [ctypes.POINTER(lily_gdn_shape), P, P, P, P, P, P, ctypes.c_float, P, P, P]
+    L.lily_gdn_scan.restype = I32
     L.lily_moe_device_status.argtypes = [P, P]
     L.lily_moe_clear_status.argtypes = [P, P]
     for n in ("lily_moe_check_shape", "lily_moe_route", "lily_moe_grouped_gemm", "lily_moe_forward",
@@ -318,3 +324,18 @@ def lily_attn_decode(shape: lily_attn_shape, q, k_cache, v_cache, block_table, s
                                  _ptr(block_table), _ptr(seq_lens), float(scale), _ptr(out), _ptr(ws),
                                  ws.numel() if isinstance(ws, torch.Tensor) else 0, _stream(stream))
     return _check("lily_attn_decode", rc) if check else rc
+
+
+# ------------------------------------------------------------------ Gated DeltaNet scan
+def lily_gdn_scan(q, k, v, alpha, beta, out, state_out, state_in=None, scale: Optional[float] = None,
+                  stream=None, *, check: bool = True) -> int:
+    """Gated DeltaNet scan over the T tokens of q/k [T][H_k][d_k], v [T][H_v][d_v]
+    (see include/lily_moe.h).  scale defaults to 1/sqrt(d_k)."""
+    T, H_k, d_k = q.shape
+    _, H_v, d_v = v.shape
+    shape = lily_gdn_shape(T, H_k, H_v, d_k, d_v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    rc = load().lily_gdn_scan(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(state_in),
+                              float(scale), _ptr(out), _ptr(state_out), _stream(stream))
+    return _check("lily_gdn_scan", rc) if check else rc

@@ -785,6 +785,32 @@ int lily_attn_decode(const lily_attn_shape *shape, const uint16_t *q, const uint
     return to_status(launch_attn_decode(a, tmK, tmV, stream), "attention launch");
 }
 
+int lily_gdn_scan(const lily_gdn_shape *shape, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  const float *alpha, const float *beta, const float *state_in, float scale, float *out,
+                  float *state_out, cudaStream_t stream)
+{
+    if (!shape) return LILY_ERR_INVALID;
+    const lily_gdn_shape s = *shape;
+    if (s.T < 0 || s.H_k < 1 || s.H_v < 1 || s.H_v % s.H_k != 0 || !std::isfinite(scale)) return LILY_ERR_INVALID;
+    if ((s.d_k != 64 && s.d_k != 128) || s.d_v < 16 || s.d_v > 1024 || s.d_v % 16 != 0) return LILY_ERR_UNSUPPORTED;
+    int rc;
+    // with T = 0 the token arrays are empty and may be NULL
+    if (s.T > 0)
+        for (const void *p : {static_cast<const void *>(q), static_cast<const void *>(k), static_cast<const void *>(v),
+                              static_cast<const void *>(alpha), static_cast<const void *>(beta),
+                              static_cast<const void *>(out)})
+            if ((rc = check_ptr(p))) return rc;
+    if ((rc = check_ptr(state_out))) return rc;
+    if (state_in && !aligned16(state_in)) return LILY_ERR_MISALIGNED;
+    if (state_in == state_out) return LILY_ERR_INVALID;
+    GdnArgs a{};
+    a.T = s.T; a.H_k = s.H_k; a.H_v = s.H_v; a.d_k = s.d_k; a.d_v = s.d_v;
+    a.scale = scale;
+    a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta;
+    a.state_in = state_in; a.out = out; a.state_out = state_out;
+    return to_status(launch_gdn_scan(a, stream), "Gated DeltaNet scan launch");
+}
+
 int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,
                            lily_moe_routing *r, int32_t *device_status, cudaStream_t stream)
 {

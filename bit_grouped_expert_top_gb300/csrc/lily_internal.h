@@ -162,4 +162,18 @@ size_t attn_smem_bytes(int D, int bs);
 // tmK / tmV: the caches as 2-D bf16 [n_blocks * H_kv * bs][D], box 64 x bs, 128-byte swizzle.
 cudaError_t launch_attn_decode(const AttnArgs &a, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t stream);
 
+// Gated DeltaNet scan (gdn.cu): CTA (16-row slice of the state, value head).
+struct GdnArgs {
+    int T, H_k, H_v, d_k, d_v;
+    float scale;
+    const uint16_t *q, *k;     // bf16 [T][H_k][d_k]
+    const uint16_t *v;         // bf16 [T][H_v][d_v]
+    const float *alpha, *beta; // [T][H_v]
+    const float *state_in;     // [H_v][d_v][d_k] or NULL (zeros)
+    float *out;                // [T][H_v][d_v]
+    float *state_out;          // [H_v][d_v][d_k]
+};
+size_t gdn_smem_bytes(int d_k);
+cudaError_t launch_gdn_scan(const GdnArgs &a, cudaStream_t stream);
+
 }  // namespace lily

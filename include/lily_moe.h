@@ -301,6 +301,40 @@ int lily_attn_decode(const lily_attn_shape *shape, const uint16_t *q, const uint
                      cudaStream_t stream);
 
 /*
+ * Gated DeltaNet scan: the fixed-size recurrence of the model's linear-attention
+ * layers over T tokens of one sequence, the state kept in registers.
+ *
+ * Method: the page "Perplexity libera o Lily" (noticiai.com.br), section "O
+ * modelo em tres formatos de carga" (30 Gated DeltaNet layers, a recurrence of
+ * fixed size) and section "Prefill e decode: onde estao os ganhos" (a scan with
+ * its state in registers).  The page gives no formula; this is the gated delta
+ * rule.  Per value head h (key head h / (H_v / H_k)), state S (d_v x d_k):
+ *   S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T
+ *   o_t = scale * S_t q_t
+ * The normalisation, gating and convolution that produce q, k, v, alpha and
+ * beta come before the scan and are the caller's.  fp32 state and arithmetic.
+ *
+ * Layouts (row-major, device memory, 16-byte aligned):
+ *   q, k   bf16 [T][H_k][d_k];  v  bf16 [T][H_v][d_v]
+ *   alpha, beta  f32 [T][H_v]
+ *   state_in     f32 [H_v][d_v][d_k], or NULL for a zero state
+ *   out          f32 [T][H_v][d_v];  state_out  f32 [H_v][d_v][d_k] (may not
+ *                alias state_in)
+ * Supported: d_k in {64, 128}; d_v a multiple of 16 in [16, 1024];
+ * H_v % H_k == 0; T >= 0 (T = 0 copies the state; the token arrays may then
+ * be NULL).  One kernel on `stream`; bit-reproducible.
+ */
+typedef struct lily_gdn_shape {
+    int32_t T;          /* tokens */
+    int32_t H_k, H_v;   /* query/key heads, value heads */
+    int32_t d_k, d_v;   /* key and value head sizes */
+} lily_gdn_shape;
+
+int lily_gdn_scan(const lily_gdn_shape *shape, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  const float *alpha, const float *beta, const float *state_in, float scale, float *out,
+                  float *state_out, cudaStream_t stream);
+
+/*
  * Routing without a caller workspace.  The method has no counterpart: this entry
  * point exists for callers that may not allocate device memory when they call
  * the layer, e.g. a plugin that runs inside another engine's fixed memory
