@@ -366,6 +366,47 @@ def bench_attention(names, reps, stream, peaks):
     return res
 
 
+def bench_gdn(names, reps, stream, clocks):
+    """µs per call of lily_gdn_scan; the scan is a sequential fp32 recurrence, so
+    its roofline is the fp32 FMA rate of the CUDA cores (152 SMs x 128 lanes x 2
+    flops per cycle at the sampled SM clock)."""
+    import torch
+    import bit_grouped_expert_top_gb300 as lm
+    from bit_grouped_expert_top_gb300.gdn_inputs import GDN_CONFIGS, gdn_bytes, gdn_flops, make_gdn
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    peak = sms * 128 * 2 * mhz * 1e6 / 1e12  # TFLOP/s
+    res = {}
+    for name in names:
+        cfg = GDN_CONFIGS[name]
+        g = {k: v.cuda() for k, v in make_gdn(cfg, "cpu").items()}
+        out = torch.empty((cfg.T, cfg.H_v, cfg.d_v), dtype=torch.float32, device="cuda")
+        st = torch.empty((cfg.H_v, cfg.d_v, cfg.d_k), dtype=torch.float32, device="cuda")
+        stream.wait_stream(torch.cuda.current_stream())
+
+        def call():
+            lm.lily_gdn_scan(g["q"], g["k"], g["v"], g["alpha"], g["beta"], out, st, state_in=g["state"],
+                             stream=stream)
+        for _ in range(3):
+            call()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            call()
+        b.record(stream)
+        b.synchronize()
+        us = a.elapsed_time(b) * 1e3 / reps
+        fl = gdn_flops(cfg)
+        res[name] = {"tokens": cfg.T, "heads": f"{cfg.H_k}qk/{cfg.H_v}v", "d": cfg.d_k, "us_per_call": round(us, 1),
+                     "tokens_per_s": round(cfg.T / (us * 1e-6)),
+                     "roofline": {"bound": "alu", "achieved": round(fl / (us * 1e-6) / 1e12, 2), "peak": round(peak, 1),
+                                  "unit": "TFLOP/s", "frac": round(fl / (us * 1e-6) / 1e12 / peak, 4),
+                                  "peak_note": "fp32 FMA: SMs x 128 lanes x 2 flops x sampled SM clock"},
+                     "hbm_gbs": round(gdn_bytes(cfg) / (us * 1e-6) / 1e9, 1)}
+        del g
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -439,6 +480,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         also["decode_l40"] = bench_decode(CONFIGS["decode_t1_l40"], (1, 2, 4, 8), 20, stream, peaks)
         also["attn_decode"] = bench_attention(("attn_32k", "attn_64k", "attn_128k"), 50, stream, peaks)
+        also["gdn_scan"] = bench_gdn(("gdn_t512", "gdn_t8192"), 10, stream, clocks)
 
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,

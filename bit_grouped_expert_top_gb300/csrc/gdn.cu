@@ -12,16 +12,18 @@
 //
 // GB300 design.  The rows of S evolve independently (row i needs only u_i,
 // v_t[i] and the shared k_t, q_t), so the state is split by rows: CTA
-// (16-row slice, value head), 128 threads, eight threads per row, each owning
-// d_k / 8 columns of its row in registers for the whole sequence.  Per token a
-// thread does its part of S k, the eight partial sums meet in three
-// butterfly shuffles, then the rank-1 update of its columns and its part of
-// S q (three more shuffles).  The token inputs (q and k rows of the key head,
-// this slice's 16 values of v, alpha and beta) are staged in shared memory
-// 64 tokens at a time with cp.async, double buffered, so the scan never waits
-// on global memory; outputs of a chunk are collected in shared memory and
-// written as 16-byte stores.  The sequential dependence through S makes the
-// scan latency- and ALU-bound, not bandwidth-bound.
+// (16-row slice, value head), 8 threads per row (128 threads), each holding
+// d_k / 8 columns of its row in registers for the whole sequence (column
+// groups of 4 interleaved over the row's threads, so their shared-memory
+// reads of k and q hit consecutive banks).  The token inputs (q and k rows of
+// the key head, this slice's 16 values of v, alpha and beta) are copied into
+// shared memory 32 tokens at a time with cp.async, double buffered; k and q
+// are then converted to fp32 once per chunk for all rows.  The token loop is
+// pipelined: after the update with token t a thread forms both dots with the
+// new state, its part of o_t (with q_t) and of u_{t+1} (with k_{t+1}), and
+// the two butterfly reductions over the row's threads interleave.  Outputs of
+// a chunk are collected in shared memory and written as 16-byte stores.  The
+// sequential dependence through S makes the scan latency- and issue-bound.
 #include <cstdint>
 
 #include "lily_device.cuh"
@@ -30,9 +32,8 @@
 namespace lily {
 namespace {
 
-constexpr int kGdnThreads = 128;
 constexpr int kGdnRows = 16;      // state rows per CTA
-constexpr int kGdnChunk = 64;     // tokens staged per buffer
+constexpr int kGdnChunk = 32;     // tokens staged per buffer
 
 template <int DK>
 struct GdnStage {
@@ -45,7 +46,9 @@ struct GdnStage {
 
 template <int DK>
 struct GdnSmem {
-    GdnStage<DK> st[2];
+    GdnStage<DK> st[2];              // bf16 inputs as copied (double buffered)
+    float kf[kGdnChunk][DK];         // this chunk's k and q in fp32, converted once for all rows
+    float qf[kGdnChunk][DK];
     float o[kGdnChunk][kGdnRows];
 };
 
@@ -55,26 +58,16 @@ __device__ __forceinline__ void cp_async_4(void *dst, const void *src)
 }
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// 8 consecutive bf16 values (16 bytes of shared memory) -> floats
-__device__ __forceinline__ void bf16x8_to_f32(const uint16_t *p, float *f)
+// TPR threads per state row, each owning DK / TPR columns; 16 rows per CTA.
+template <int DK, int TPR>
+__global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs a)
 {
-    const uint4 w = *reinterpret_cast<const uint4 *>(p);
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(u[i] << 16);
-        f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-    }
-}
-
-template <int DK>
-__global__ void __launch_bounds__(kGdnThreads) gdn_scan_kernel(const GdnArgs a)
-{
-    constexpr int CPT = DK / 8;  // state columns per thread
+    constexpr int NT = kGdnRows * TPR;  // threads
+    constexpr int CPT = DK / TPR;       // state columns per thread
     extern __shared__ __align__(16) uint8_t gsm[];
     GdnSmem<DK> &S = *reinterpret_cast<GdnSmem<DK> *>(gsm);
     const int slice = blockIdx.x, h = blockIdx.y;
-    const int tid = threadIdx.x, r = tid >> 3, cg = tid & 7;
+    const int tid = threadIdx.x, r = tid / TPR, cg = tid % TPR;
     const int hk = h / (a.H_v / a.H_k);
     const int row = slice * kGdnRows + r;
     const int T = a.T;
@@ -82,13 +75,17 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_scan_kernel(const GdnArgs a)
     pdl_trigger();
     pdl_wait();
 
+    // Column ownership: thread cg of a row holds the 4-column groups m TPR + cg
+    // (m < CPT / 4), so that a float4 step over a row's threads covers
+    // consecutive addresses (no shared-memory bank conflicts).
+    auto col = [&](int j) { return ((j >> 2) * TPR + cg) * 4 + (j & 3); };
     float st[CPT];
     {
-        const float *s0 = a.state_in ? a.state_in + (static_cast<size_t>(h) * a.d_v + row) * DK + cg * CPT : nullptr;
+        const float *s0 = a.state_in ? a.state_in + (static_cast<size_t>(h) * a.d_v + row) * DK : nullptr;
 #pragma unroll
         for (int j = 0; j < CPT; j += 4) {
             float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (s0) v4 = *reinterpret_cast<const float4 *>(s0 + j);
+            if (s0) v4 = *reinterpret_cast<const float4 *>(s0 + col(j));
             st[j] = v4.x;
             st[j + 1] = v4.y;
             st[j + 2] = v4.z;
@@ -101,21 +98,28 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_scan_kernel(const GdnArgs a)
         GdnStage<DK> &B = S.st[b];
         const int n = min(kGdnChunk, T - t0);
         constexpr int kPieces = DK * 2 / 16;  // 16-byte pieces of a q or k row
-        for (int i = tid; i < n * kPieces; i += kGdnThreads) {
+        for (int i = tid; i < n * kPieces; i += NT) {
             const int t = i / kPieces, p = i - t * kPieces;
             const size_t src = (static_cast<size_t>(t0 + t) * a.H_k + hk) * DK + p * 8;
             cp_async_16(&B.k[t][p * 8], a.k + src);
             cp_async_16(&B.q[t][p * 8], a.q + src);
         }
-        for (int i = tid; i < n * 2; i += kGdnThreads) {
+        for (int i = tid; i < n * 2; i += NT) {
             const int t = i >> 1, p = i & 1;
             cp_async_16(&B.v[t][p * 8], a.v + (static_cast<size_t>(t0 + t) * a.H_v + h) * a.d_v + slice * kGdnRows + p * 8);
         }
-        for (int t = tid; t < n; t += kGdnThreads) {
+        for (int t = tid; t < n; t += NT) {
             cp_async_4(&B.alpha[t], a.alpha + static_cast<size_t>(t0 + t) * a.H_v + h);
             cp_async_4(&B.beta[t], a.beta + static_cast<size_t>(t0 + t) * a.H_v + h);
         }
         cp_async_commit();
+    };
+
+    // the row's partial sum over its TPR threads (consecutive lanes)
+    auto row_sum = [](float x) {
+#pragma unroll
+        for (int o = 1; o < TPR; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        return x;
     };
 
     const int n_chunks = (T + kGdnChunk - 1) / kGdnChunk;
@@ -130,66 +134,97 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_scan_kernel(const GdnArgs a)
         }
         __syncthreads();
         const GdnStage<DK> &B = S.st[c & 1];
-        for (int t = 0; t < n; ++t) {
-            float kf[CPT];
+        // k and q of the chunk to fp32, once for all rows (pairs of bf16 -> two floats)
+        for (int i = tid; i < n * DK / 2; i += NT) {
+            const int t = i / (DK / 2), j = (i - t * (DK / 2)) * 2;
+            const uint32_t kw = *reinterpret_cast<const uint32_t *>(&B.k[t][j]);
+            const uint32_t qw = *reinterpret_cast<const uint32_t *>(&B.q[t][j]);
+            *reinterpret_cast<float2 *>(&S.kf[t][j]) = make_float2(__uint_as_float(kw << 16), __uint_as_float(kw & 0xFFFF0000u));
+            *reinterpret_cast<float2 *>(&S.qf[t][j]) = make_float2(__uint_as_float(qw << 16), __uint_as_float(qw & 0xFFFF0000u));
+        }
+        __syncthreads();
+        // Token loop, pipelined: u_t = (S_{t-1} k_t)_row is ready on entry; the
+        // update with token t is followed by both dots with the new state, o_t
+        // (with q_t) and u_{t+1} (with k_{t+1}), whose butterflies interleave.
+        float kf[CPT];
+        auto load_row = [&](const float (*src)[DK], int t, float(&dst)[CPT]) {
 #pragma unroll
-            for (int j = 0; j < CPT; j += 8) bf16x8_to_f32(&B.k[t][cg * CPT + j], kf + j);
-            // u = (S k)_row: four independent partial chains, then the 8 threads of the row
+            for (int j = 0; j < CPT; j += 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(&src[t][col(j)]);
+                dst[j] = v4.x; dst[j + 1] = v4.y; dst[j + 2] = v4.z; dst[j + 3] = v4.w;
+            }
+        };
+        load_row(S.kf, 0, kf);
+        float u;
+        {
             float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < CPT; ++j) p[j & 3] = fmaf(st[j], kf[j], p[j & 3]);
-            float u = (p[0] + p[1]) + (p[2] + p[3]);
-            u += __shfl_xor_sync(0xffffffffu, u, 1);
-            u += __shfl_xor_sync(0xffffffffu, u, 2);
-            u += __shfl_xor_sync(0xffffffffu, u, 4);
+            u = row_sum((p[0] + p[1]) + (p[2] + p[3]));
+        }
+        for (int t = 0; t < n; ++t) {
+            float qf[CPT], kn[CPT];
+            load_row(S.qf, t, qf);
+            const bool more = t + 1 < n;
+            load_row(S.kf, more ? t + 1 : t, kn);
             const float al = B.alpha[t], be = B.beta[t];
             const float vr = __uint_as_float(static_cast<uint32_t>(B.v[t][r]) << 16);
             const float cc = be * (vr - al * u);
-            float qf[CPT];
-#pragma unroll
-            for (int j = 0; j < CPT; j += 8) bf16x8_to_f32(&B.q[t][cg * CPT + j], qf + j);
-            float o4[4] = {0.f, 0.f, 0.f, 0.f};
+            float o4[4] = {0.f, 0.f, 0.f, 0.f}, p4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < CPT; ++j) {
                 st[j] = fmaf(al, st[j], cc * kf[j]);
                 o4[j & 3] = fmaf(st[j], qf[j], o4[j & 3]);
+                p4[j & 3] = fmaf(st[j], kn[j], p4[j & 3]);
             }
             float o = (o4[0] + o4[1]) + (o4[2] + o4[3]);
-            o += __shfl_xor_sync(0xffffffffu, o, 1);
-            o += __shfl_xor_sync(0xffffffffu, o, 2);
-            o += __shfl_xor_sync(0xffffffffu, o, 4);
+            float un = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+#pragma unroll
+            for (int m = 1; m < TPR; m <<= 1) {
+                o += __shfl_xor_sync(0xffffffffu, o, m);
+                un += __shfl_xor_sync(0xffffffffu, un, m);
+            }
             if (cg == 0) S.o[t][r] = a.scale * o;
+            u = un;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) kf[j] = kn[j];
         }
         __syncthreads();
         // the chunk's outputs: per token 16 floats of this slice, four 16-byte stores
-        for (int i = tid; i < n * 4; i += kGdnThreads) {
+        for (int i = tid; i < n * 4; i += NT) {
             const int t = i >> 2, p = i & 3;
             *reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(t0 + t) * a.H_v + h) * a.d_v + slice * kGdnRows + p * 4) =
                 *reinterpret_cast<const float4 *>(&S.o[t][p * 4]);
         }
-        // the buffer just read is restaged two chunks later, after the barrier above
+        // the buffer just read is restaged two chunks later, after the barriers above
     }
-    float *so = a.state_out + (static_cast<size_t>(h) * a.d_v + row) * DK + cg * CPT;
+    float *so = a.state_out + (static_cast<size_t>(h) * a.d_v + row) * DK;
 #pragma unroll
-    for (int j = 0; j < CPT; j += 4) *reinterpret_cast<float4 *>(so + j) = make_float4(st[j], st[j + 1], st[j + 2], st[j + 3]);
+    for (int j = 0; j < CPT; j += 4)
+        *reinterpret_cast<float4 *>(so + col(j)) = make_float4(st[j], st[j + 1], st[j + 2], st[j + 3]);
 }
 
 }  // namespace
 
+#ifndef LILY_GDN_TPR
+#define LILY_GDN_TPR 8
+#endif
+constexpr int kGdnTPR = LILY_GDN_TPR;  // threads per state row
+
 size_t gdn_smem_bytes(int d_k) { return d_k == 64 ? sizeof(GdnSmem<64>) : sizeof(GdnSmem<128>); }
+
+template <int DK>
+static cudaError_t launch_dk(const GdnArgs &a, cudaStream_t stream)
+{
+    const size_t smem = sizeof(GdnSmem<DK>);
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(gdn_scan_kernel<DK, kGdnTPR>), static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(gdn_scan_kernel<DK, kGdnTPR>, dim3(a.d_v / kGdnRows, a.H_v), dim3(kGdnRows * kGdnTPR), smem, stream, a);
+}
 
 cudaError_t launch_gdn_scan(const GdnArgs &a, cudaStream_t stream)
 {
-    const dim3 grid(a.d_v / kGdnRows, a.H_v);
-    const size_t smem = gdn_smem_bytes(a.d_k);
-    if (a.d_k == 64) {
-        cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(gdn_scan_kernel<64>), static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        return launch_pdl(gdn_scan_kernel<64>, grid, dim3(kGdnThreads), smem, stream, a);
-    }
-    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(gdn_scan_kernel<128>), static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    return launch_pdl(gdn_scan_kernel<128>, grid, dim3(kGdnThreads), smem, stream, a);
+    return a.d_k == 64 ? launch_dk<64>(a, stream) : launch_dk<128>(a, stream);
 }
 
 }  // namespace lily
