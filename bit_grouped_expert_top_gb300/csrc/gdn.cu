@@ -12,8 +12,8 @@
 //
 // GB300 design.  The rows of S evolve independently (row i needs only u_i,
 // v_t[i] and the shared k_t, q_t), so the state is split by rows: CTA
-// (16-row slice, value head), 8 threads per row (128 threads), each holding
-// d_k / 8 columns of its row in registers for the whole sequence (column
+// (16-row slice, value head), 4 threads per row (64 threads), each holding
+// d_k / 4 columns of its row in registers for the whole sequence (column
 // groups of 4 interleaved over the row's threads, so their shared-memory
 // reads of k and q hit consecutive banks).  The token inputs (q and k rows of
 // the key head, this slice's 16 values of v, alpha and beta) are copied into
@@ -21,9 +21,11 @@
 // are then converted to fp32 once per chunk for all rows.  The token loop is
 // pipelined: after the update with token t a thread forms both dots with the
 // new state, its part of o_t (with q_t) and of u_{t+1} (with k_{t+1}), and
-// the two butterfly reductions over the row's threads interleave.  Outputs of
-// a chunk are collected in shared memory and written as 16-byte stores.  The
-// sequential dependence through S makes the scan latency- and issue-bound.
+// the two butterfly reductions over the row's threads interleave; column
+// pairs use the packed two-lane fp32 instructions.  Outputs of a chunk are
+// collected in shared memory and written as 16-byte stores.  The sequential
+// dependence through S makes the scan latency-bound: per token a chain of
+// shared-memory loads, a few FMAs and the butterfly shuffles.
 #include <cstdint>
 
 #include "lily_device.cuh"
@@ -58,6 +60,29 @@ __device__ __forceinline__ void cp_async_4(void *dst, const void *src)
 }
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
+// Packed two-lane fp32 arithmetic (one instruction for two values).
+__device__ __forceinline__ unsigned long long f2_bits(float2 v)
+{
+    return static_cast<unsigned long long>(__float_as_uint(v.x)) |
+           (static_cast<unsigned long long>(__float_as_uint(v.y)) << 32);
+}
+__device__ __forceinline__ float2 f2_from(unsigned long long b)
+{
+    return make_float2(__uint_as_float(static_cast<uint32_t>(b)), __uint_as_float(static_cast<uint32_t>(b >> 32)));
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)  // a * b + c, each lane rounded once
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+    return f2_from(r);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return f2_from(r);
+}
+
 // TPR threads per state row, each owning DK / TPR columns; 16 rows per CTA.
 template <int DK, int TPR>
 __global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs a)
@@ -79,17 +104,16 @@ __global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs 
     // (m < CPT / 4), so that a float4 step over a row's threads covers
     // consecutive addresses (no shared-memory bank conflicts).
     auto col = [&](int j) { return ((j >> 2) * TPR + cg) * 4 + (j & 3); };
-    float st[CPT];
+    constexpr int NP = CPT / 2;  // column pairs per thread
+    float2 st[NP];
     {
         const float *s0 = a.state_in ? a.state_in + (static_cast<size_t>(h) * a.d_v + row) * DK : nullptr;
 #pragma unroll
         for (int j = 0; j < CPT; j += 4) {
             float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (s0) v4 = *reinterpret_cast<const float4 *>(s0 + col(j));
-            st[j] = v4.x;
-            st[j + 1] = v4.y;
-            st[j + 2] = v4.z;
-            st[j + 3] = v4.w;
+            st[j / 2] = make_float2(v4.x, v4.y);
+            st[j / 2 + 1] = make_float2(v4.z, v4.w);
         }
     }
 
@@ -146,39 +170,51 @@ __global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs 
         // Token loop, pipelined: u_t = (S_{t-1} k_t)_row is ready on entry; the
         // update with token t is followed by both dots with the new state, o_t
         // (with q_t) and u_{t+1} (with k_{t+1}), whose butterflies interleave.
-        float kf[CPT];
-        auto load_row = [&](const float (*src)[DK], int t, float(&dst)[CPT]) {
+        // Column pairs go through packed two-lane fp32 instructions; the loop
+        // runs two tokens per trip so k_t and k_{t+1} swap register roles.
+        auto load_row = [&](const float (*src)[DK], int t, float2(&dst)[NP]) {
 #pragma unroll
             for (int j = 0; j < CPT; j += 4) {
                 const float4 v4 = *reinterpret_cast<const float4 *>(&src[t][col(j)]);
-                dst[j] = v4.x; dst[j + 1] = v4.y; dst[j + 2] = v4.z; dst[j + 3] = v4.w;
+                dst[j / 2] = make_float2(v4.x, v4.y);
+                dst[j / 2 + 1] = make_float2(v4.z, v4.w);
             }
         };
-        load_row(S.kf, 0, kf);
+        float2 ka[NP], kb[NP];
+        load_row(S.kf, 0, ka);
         float u;
         {
-            float p[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 p0 = make_float2(0.f, 0.f), p1 = p0;
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) p[j & 3] = fmaf(st[j], kf[j], p[j & 3]);
-            u = row_sum((p[0] + p[1]) + (p[2] + p[3]));
+            for (int j = 0; j < NP; j += 2) {
+                p0 = ffma2(st[j], ka[j], p0);
+                if (j + 1 < NP) p1 = ffma2(st[j + 1], ka[j + 1], p1);
+            }
+            u = row_sum((p0.x + p0.y) + (p1.x + p1.y));
         }
-        for (int t = 0; t < n; ++t) {
-            float qf[CPT], kn[CPT];
+        // one token: update with kc (= k_t), dots with q_t and kn (= k_{t+1})
+        auto step = [&](int t, const float2(&kc)[NP], float2(&kn)[NP]) {
+            float2 qf[NP];
             load_row(S.qf, t, qf);
-            const bool more = t + 1 < n;
-            load_row(S.kf, more ? t + 1 : t, kn);
+            load_row(S.kf, t + 1 < n ? t + 1 : t, kn);
             const float al = B.alpha[t], be = B.beta[t];
             const float vr = __uint_as_float(static_cast<uint32_t>(B.v[t][r]) << 16);
             const float cc = be * (vr - al * u);
-            float o4[4] = {0.f, 0.f, 0.f, 0.f}, p4[4] = {0.f, 0.f, 0.f, 0.f};
+            const float2 al2 = make_float2(al, al), cc2 = make_float2(cc, cc);
+            float2 o0 = make_float2(0.f, 0.f), o1 = o0, p0 = o0, p1 = o0;
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) {
-                st[j] = fmaf(al, st[j], cc * kf[j]);
-                o4[j & 3] = fmaf(st[j], qf[j], o4[j & 3]);
-                p4[j & 3] = fmaf(st[j], kn[j], p4[j & 3]);
+            for (int j = 0; j < NP; ++j) {
+                st[j] = ffma2(al2, st[j], fmul2(cc2, kc[j]));
+                if (j & 1) {
+                    o1 = ffma2(st[j], qf[j], o1);
+                    p1 = ffma2(st[j], kn[j], p1);
+                } else {
+                    o0 = ffma2(st[j], qf[j], o0);
+                    p0 = ffma2(st[j], kn[j], p0);
+                }
             }
-            float o = (o4[0] + o4[1]) + (o4[2] + o4[3]);
-            float un = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+            float o = (o0.x + o0.y) + (o1.x + o1.y);
+            float un = (p0.x + p0.y) + (p1.x + p1.y);
 #pragma unroll
             for (int m = 1; m < TPR; m <<= 1) {
                 o += __shfl_xor_sync(0xffffffffu, o, m);
@@ -186,9 +222,13 @@ __global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs 
             }
             if (cg == 0) S.o[t][r] = a.scale * o;
             u = un;
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) kf[j] = kn[j];
+        };
+        int t = 0;
+        for (; t + 1 < n; t += 2) {
+            step(t, ka, kb);
+            step(t + 1, kb, ka);
         }
+        if (t < n) step(t, ka, kb);
         __syncthreads();
         // the chunk's outputs: per token 16 floats of this slice, four 16-byte stores
         for (int i = tid; i < n * 4; i += NT) {
@@ -201,13 +241,13 @@ __global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs 
     float *so = a.state_out + (static_cast<size_t>(h) * a.d_v + row) * DK;
 #pragma unroll
     for (int j = 0; j < CPT; j += 4)
-        *reinterpret_cast<float4 *>(so + col(j)) = make_float4(st[j], st[j + 1], st[j + 2], st[j + 3]);
+        *reinterpret_cast<float4 *>(so + col(j)) = make_float4(st[j / 2].x, st[j / 2].y, st[j / 2 + 1].x, st[j / 2 + 1].y);
 }
 
 }  // namespace
 
 #ifndef LILY_GDN_TPR
-#define LILY_GDN_TPR 8
+#define LILY_GDN_TPR 4
 #endif
 constexpr int kGdnTPR = LILY_GDN_TPR;  // threads per state row
 
