@@ -169,6 +169,47 @@ def oracle_sample_rate(cfg, layer_np, x_bits, logits_f32, n_tokens: int):
     return n_tokens / dt, dt
 
 
+def input_digests(ctx):
+    """sha256 (first 16 hex digits) of every input buffer of the timed workload:
+    each weight set (its tensors in name order) and each activation set."""
+    import hashlib
+    out = {}
+    for i, (layer, x) in enumerate(zip(ctx["layers"], ctx["xs"])):
+        h = hashlib.sha256()
+        for k in sorted(layer):
+            h.update(layer[k].detach().contiguous().view(-1).view(torch_uint8()).cpu().numpy().tobytes())
+        out[f"weights_{i}"] = h.hexdigest()[:16]
+        out[f"x_{i}"] = hashlib.sha256(x.detach().contiguous().view(-1).view(torch_uint8()).cpu().numpy().tobytes()
+                                       ).hexdigest()[:16]
+    return out
+
+
+def torch_uint8():
+    import torch
+    return torch.uint8
+
+
+def oracle_single_thread_rates(peaks_unused=None):
+    """Tokens/s of the fp64 oracle on one host thread, on the tiny workload and on
+    16 tokens of the T=512 workload (a bounded sample)."""
+    import oracle
+    from bit_grouped_expert_top_gb300.inputs import CONFIGS, make_layer, make_x
+    res = {}
+    n_all = oracle.num_threads()
+    oracle.set_threads(1)
+    try:
+        for name, n in (("tiny", 32), ("prefill_t512", 16)):
+            cfg = CONFIGS[name]
+            layer = _np_layer(make_layer(cfg, "cpu"))
+            xb = _bits(make_x(cfg, "cpu"))[:n]
+            lg = oracle.logits(xb, layer["router_w"], layer.get("router_bias")).astype("float32")
+            rate, dt = oracle_sample_rate(cfg, layer, xb, lg, n)
+            res[name] = {"tokens_per_s": round(rate, 3), "tokens": n, "seconds": round(dt, 2), "threads": 1}
+    finally:
+        oracle.set_threads(n_all)
+    return res
+
+
 def _np_layer(layer_t):
     import numpy as np
     import torch
@@ -558,6 +599,9 @@ def run_ours(args):
                                 "kind": "oracle",
                                 "sample": f"{n_tok} tokens of prefill_t8192 (router + top-8 + 9 experts each), "
                                           f"{dt:.1f} s wall"}
+        if not args.quick:
+            line["cpu_baseline"]["single_thread"] = oracle_single_thread_rates()
+            line["inputs_sha256"] = input_digests(ctx)
         print(json.dumps(line), flush=True)
     barrier(world)
 
