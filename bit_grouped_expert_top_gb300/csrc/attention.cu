@@ -350,79 +350,104 @@ attn_split_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CU
 
 // Merges the splits: o = sum_s 2^(m_s - m) O_s / sum_s 2^(m_s - m) l_s over the
 // splits that saw tokens (a sequence without tokens gives zeros).  CTA
-// (sequence x query head, 64-wide slice of D), 256 threads.  Warp 0 loads every
-// split's (m, l) at once (up to 8 per lane), forms the common max and the
-// denominator, and leaves the splits' weights in shared memory; then four
-// groups of 64 threads (one per element of the slice) each take every fourth
-// split, issuing their loads 16 at a time, and the four partial sums are added.
+// (sequence x query head, 64-wide slice of D), 256 threads: thread (e, sg)
+// takes float4 column e of the slice and splits sg, sg + 16, ...; it loads
+// their (m, l) and partial O in one go (8 splits in flight), keeps a running
+// max of its own and rescales as it goes, so the partials are read in a single
+// pass.  The threads then agree on the common max, rescale, and the 16 groups'
+// sums are added in a fixed order.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a)
 {
-    __shared__ float wsplit[kAttnMaxSplits];
-    __shared__ float part[4][64];
-    __shared__ float s_den;
+    constexpr int kCols = 16, kGroups = 16, kBatch = 8;  // float4 columns, split groups, loads in flight
+    __shared__ float4 part[kGroups][kCols];
+    __shared__ float red_max[8], red_den[8];
     const int b = blockIdx.x / a.H_q, h = blockIdx.x - b * a.H_q;
     const int g = h / a.group, n = h - g * a.group;
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int e = tid % kCols, sg = tid / kCols;
     pdl_trigger();
     pdl_wait();  // the split kernel is complete
     const size_t p0 = (static_cast<size_t>(b) * a.H_kv + g) * a.n_splits;
-    const int S = a.n_splits;
-    if (tid < 32) {
-        float ms[kAttnMaxSplits / 32], ls[kAttnMaxSplits / 32];
+    const int S = a.n_splits, Q = a.D / 4, q = blockIdx.y * kCols + e;
+    const bool act = q < Q;
+    const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + (p0 * kAttnMaxGroup + n) * a.D) + (act ? q : 0);
+    const float *mls = a.part_ml + (p0 * kAttnMaxGroup + n) * 2;
+    const size_t stride4 = static_cast<size_t>(kAttnMaxGroup) * Q;
+    float mt = -INFINITY, dt = 0.0f;
+    float4 num = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int s0 = sg; s0 < S; s0 += kBatch * kGroups) {
+        float4 v[kBatch];
+        float2 ml[kBatch];
 #pragma unroll
-        for (int k = 0; k < kAttnMaxSplits / 32; ++k) {
-            const int s = lane + 32 * k;
-            ms[k] = -INFINITY;
-            ls[k] = 0.0f;
-            if (s < S) {
-                const float2 ml = *reinterpret_cast<const float2 *>(a.part_ml + (p0 + s) * kAttnMaxGroup * 2 + n * 2);
-                ms[k] = ml.x;
-                ls[k] = ml.y;
-            }
+        for (int k = 0; k < kBatch; ++k) {
+            const int s = s0 + k * kGroups;
+            ml[k] = s < S ? *reinterpret_cast<const float2 *>(mls + static_cast<size_t>(s) * kAttnMaxGroup * 2)
+                          : make_float2(-INFINITY, 0.0f);
+            v[k] = s < S && act ? src[static_cast<size_t>(s) * stride4] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
-        float m = -INFINITY;
+        float bm = mt;
 #pragma unroll
-        for (int k = 0; k < kAttnMaxSplits / 32; ++k)
-            if (ls[k] > 0.0f) m = fmaxf(m, ms[k]);
+        for (int k = 0; k < kBatch; ++k)
+            if (ml[k].y > 0.0f) bm = fmaxf(bm, ml[k].x);
+        if (bm > -INFINITY) {
+            const float c = exp2f(mt - bm);  // 0 while nothing was taken
+            num.x *= c;
+            num.y *= c;
+            num.z *= c;
+            num.w *= c;
+            dt *= c;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float den = 0.0f;
-#pragma unroll
-        for (int k = 0; k < kAttnMaxSplits / 32; ++k) {
-            const int s = lane + 32 * k;
-            const float w = ls[k] > 0.0f ? exp2f(ms[k] - m) : 0.0f;
-            if (s < S) wsplit[s] = w;
-            den += w * ls[k];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        if (lane == 0) s_den = den;
-    }
-    __syncthreads();
-    const int sg = tid >> 6, d = blockIdx.y * 64 + (tid & 63);
-    float num = 0.0f;
-    if (d < a.D) {
-        const float *acc = a.part_acc + (p0 * kAttnMaxGroup + n) * a.D + d;
-        const size_t stride = static_cast<size_t>(kAttnMaxGroup) * a.D;
-        for (int s0 = sg; s0 < S; s0 += 64) {
-            float v[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int s = s0 + 4 * k;
-                v[k] = s < S ? acc[static_cast<size_t>(s) * stride] : 0.0f;
+            for (int k = 0; k < kBatch; ++k) {
+                if (ml[k].y > 0.0f) {
+                    const float w = exp2f(ml[k].x - bm);
+                    num.x += w * v[k].x;
+                    num.y += w * v[k].y;
+                    num.z += w * v[k].z;
+                    num.w += w * v[k].w;
+                    dt += w * ml[k].y;
+                }
             }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int s = s0 + 4 * k;
-                if (s < S) num += wsplit[s] * v[k];
-            }
+            mt = bm;
         }
     }
-    part[sg][tid & 63] = num;
+    float mx = mt;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red_max[warp] = mx;
     __syncthreads();
-    if (tid < 64 && d < a.D) {
-        const float t = part[0][tid] + part[1][tid] + part[2][tid] + part[3][tid];
-        a.out[(static_cast<size_t>(b) * a.H_q + h) * a.D + d] = s_den > 0.0f ? t / s_den : 0.0f;
+    mx = red_max[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red_max[w]);
+    const float f = mt > -INFINITY ? exp2f(mt - mx) : 0.0f;
+    num.x *= f;
+    num.y *= f;
+    num.z *= f;
+    num.w *= f;
+    part[sg][e] = num;
+    // the sum of weights: the threads of column 0 hold every split once
+    float den = e == 0 ? dt * f : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane == 0) red_den[warp] = den;
+    __syncthreads();
+    if (tid < kCols && act) {
+        float4 t = part[0][tid];
+#pragma unroll
+        for (int g2 = 1; g2 < kGroups; ++g2) {
+            t.x += part[g2][tid].x;
+            t.y += part[g2][tid].y;
+            t.z += part[g2][tid].z;
+            t.w += part[g2][tid].w;
+        }
+        float dsum = red_den[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) dsum += red_den[w];
+        const float r = dsum > 0.0f ? 1.0f / dsum : 0.0f;
+        t.x *= r;
+        t.y *= r;
+        t.z *= r;
+        t.w *= r;
+        reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(b) * a.H_q + h) * a.D)[q] = t;
     }
 }
 

@@ -97,6 +97,30 @@ def test_many_sequences_more_ctas_than_splits():
     _check(make_attn(cfg), cfg)
 
 
+def test_one_split_per_group():
+    # 160 sequences x 2 KV heads: more groups than the GPU holds CTAs, so each
+    # group is one CTA that normalises its own result (no barrier); lengths
+    # 0 .. 400 tokens, one block to seven blocks
+    lens = tuple(int(x) for x in np.random.default_rng(6).integers(0, 400, 160))
+    cfg = AttnConfig("wide", seq_lens=lens, D=128, block_size=64, seed=43)
+    _check(make_attn(cfg), cfg)
+
+
+def test_many_calls_on_one_workspace():
+    # the barrier words are reset by every call: twenty calls on one workspace,
+    # all bit-identical, no status recorded
+    cfg = AttnConfig("reuse", seq_lens=(5000,), D=256, block_size=64, seed=44)
+    got, st, (s, dev, ws, out) = _run(make_attn(cfg), cfg)
+    assert st == 0
+    first = out.clone()
+    for _ in range(20):
+        out.fill_(float("nan"))
+        lm.lily_attn_decode(s, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"], dev["seq_lens"], out, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(first, out)
+    assert lm.lily_moe_device_status(ws) == 0
+
+
 @pytest.mark.parametrize("name", ["attn_32k", "attn_128k"])
 def test_full_size_contexts(name):
     # the benchmark's workloads, in its launch configuration (every head checked)
