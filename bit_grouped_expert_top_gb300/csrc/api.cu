@@ -101,6 +101,34 @@ int64_t block_capacity(const lily_moe_shape &s)
     return std::max<int64_t>(1, std::min<int64_t>(a, s.E + ceil_div(a, s.block_rows)));
 }
 
+// k-steps of 64 of the grouped GEMM for reduction length K: K / 64 rounded up
+// to whole blocks of four (the kernel reads zeros past K).
+int gemm_k_steps(int64_t K)
+{
+    return static_cast<int>(((K / 64) + 3) / 4 * 4);
+}
+
+// Router K splits: about one unit (64 tokens x a share of K) per SM of a
+// 152-SM GPU while the token blocks alone are fewer, at most 8 and at most one
+// per block of four k-steps.  A fixed budget (not the device's SM count) keeps
+// the logits' rounding a function of the shape alone.
+constexpr int kRouterUnitBudget = 152;
+constexpr int kRouterBlockRows = 64;
+
+int router_ksplit(const lily_moe_shape &s)
+{
+    const int64_t blocks = std::max<int64_t>(1, ceil_div(s.T, kRouterBlockRows));
+    const int64_t kb = gemm_k_steps(s.d) / 4;
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({kMaxRouterSplit, kb, kRouterUnitBudget / blocks})));
+}
+
+// Bytes of the router's partial logits (0 without a split).
+size_t router_part_bytes(const lily_moe_shape &s)
+{
+    const int k = router_ksplit(s);
+    return k > 1 ? static_cast<size_t>(k) * s.T * s.E * 4 : 0;
+}
+
 PrefillLayout prefill_layout(const lily_moe_shape &s)
 {
     PrefillLayout L{};
@@ -116,7 +144,8 @@ PrefillLayout prefill_layout(const lily_moe_shape &s)
     L.chunk_counts = take(C * E * 4);
     L.chunk_base = take(C * E * 4);
     L.h = take((k + 1) * T * s.I * 2);
-    L.xs = take((k + 1) * T * s.d * 2);
+    // xs also holds the router's partial logits before the prep kernel writes it
+    L.xs = take(std::max<size_t>((k + 1) * T * s.d * 2, router_part_bytes(s)));
     L.inv = take(T * k * 4);
     L.logits = take(T * E * 4);
     L.idx = take(T * k * 4);
@@ -315,13 +344,6 @@ bool tmap_f16_sw128(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t ro
     return make_tmap(m, ptr, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, inner, rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// k-steps of 64 of the grouped GEMM for reduction length K: K / 64 rounded up
-// to whole blocks of four (the kernel reads zeros past K).
-int gemm_k_steps(int64_t K)
-{
-    return static_cast<int>(((K / 64) + 3) / 4 * 4);
-}
-
 // Packed int4 rows: a box of 128 bytes (four k-steps of 64 weights) x 128 rows
 // with the 128-byte swizzle, so the dequantisers read it without bank
 // conflicts; boxes past the end of a row read zeros.
@@ -336,12 +358,13 @@ namespace {
 
 // Token rows per router GEMM unit: 64 keeps more SMs busy than 128 at the
 // prefill sizes (T = 8192 gives 128 units) at a small loss of MMA width.
-constexpr int kRouterBlockRows = 64;
 
 // ------------------------------------------------------------------ enqueue helpers
 // inv: where the scatter also writes the inverse permutation (NULL: not written).
+// part: router_part_bytes(s) of scratch for the router's partial logits
+// (router_ksplit(s) splits of K; unused when that is 1).
 cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, const uint16_t *x,
-                          const lily_moe_routing &r, float *logits, void *ws, cudaStream_t stream,
+                          const lily_moe_routing &r, float *logits, void *ws, float *part, cudaStream_t stream,
                           cudaEvent_t *events = nullptr, int *inv = nullptr)
 {
     const PrefillLayout L = prefill_layout(s);
@@ -363,7 +386,10 @@ cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, co
     g.logits = logits;
     g.ctrl = ctrl;
     const int sms = num_sms_current();
-    const int grid = std::max(1, std::min(sms, g.n_shared_blocks));
+    const int ksplit = router_ksplit(s);
+    g.ksplit = ksplit;
+    g.logits_part = ksplit > 1 ? part : nullptr;
+    const int grid = std::max(1, std::min(sms, g.n_shared_blocks * ksplit));
     cudaError_t e = launch_grouped_gemm(g, tmX, tmWr, tmWr, tmWr, tmWr, grid, stream);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
@@ -371,6 +397,9 @@ cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, co
     RouteArgs ra{};
     ra.T = s.T; ra.E = s.E; ra.top_k = s.top_k; ra.bm = s.block_rows;
     ra.logits = logits;
+    ra.ksplit = ksplit;
+    ra.logits_part = g.logits_part;
+    ra.router_bias = w.router_bias;
     ra.topk_idx = r.topk_idx; ra.topk_w = r.topk_w;
     ra.counts = r.counts; ra.offsets = r.offsets; ra.perm = r.perm;
     ra.block_map = r.block_map; ra.n_blocks = r.n_blocks;
@@ -427,6 +456,7 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
     g.out = out;
     g.ctrl = ctrl;
 
+    g.ksplit = 1;
     // gate/up + SwiGLU
     g.mode = kModeGateUp;
     g.K = s.d;
@@ -589,7 +619,8 @@ int lily_moe_route(const lily_moe_shape *shape, const lily_moe_weights *w, const
     if (shape->T == 0) return LILY_OK;
     if ((rc = check_ptr(x))) return rc;
     float *logits = r->logits ? r->logits : at<float>(ws, prefill_layout(*shape).logits);
-    return to_status(enqueue_route(*shape, *w, x, *r, logits, ws, stream, nullptr, at<int>(ws, prefill_layout(*shape).inv)),
+    const PrefillLayout L = prefill_layout(*shape);
+    return to_status(enqueue_route(*shape, *w, x, *r, logits, ws, at<float>(ws, L.xs), stream, nullptr, at<int>(ws, L.inv)),
                      "routing launch");
 }
 
@@ -617,7 +648,8 @@ int lily_moe_forward_timed(const lily_moe_shape *shape, const lily_moe_weights *
     float *logits = rr.logits ? rr.logits : at<float>(ws, prefill_layout(*shape).logits);
     cudaError_t e;
     if (events && (e = cudaEventRecord(events[0], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if ((e = enqueue_route(*shape, *w, x, rr, logits, ws, stream, events, at<int>(ws, prefill_layout(*shape).inv))) !=
+    const PrefillLayout L = prefill_layout(*shape);
+    if ((e = enqueue_route(*shape, *w, x, rr, logits, ws, at<float>(ws, L.xs), stream, events, at<int>(ws, L.inv))) !=
         cudaSuccess)
         return cuda_fail(e, "routing launch");
     return to_status(enqueue_experts(*shape, *w, x, rr, out, ws, stream, events, true), "expert launch");
@@ -820,11 +852,12 @@ int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *
     if ((rc = check_ptr(r->logits))) return rc;
     if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u)) return LILY_ERR_MISALIGNED;
     // The routing kernels touch only the control block and the two per-chunk
-    // tables of the prefill workspace layout, which fit in the fixed scratch.
+    // tables of the prefill workspace layout, then the router's partial logits
+    // (placed after the tables here), which fit in the fixed scratch.
     const PrefillLayout L = prefill_layout(*shape);
-    if (L.chunk_base + static_cast<size_t>(ceil_div(shape->T, kRouteChunkTokens)) * shape->E * 4 >
-        LILY_NOALLOC_SCRATCH_BYTES)
-        return LILY_ERR_SCRATCH_LIMIT;
+    const size_t part_off =
+        align_up(L.chunk_base + static_cast<size_t>(ceil_div(shape->T, kRouteChunkTokens)) * shape->E * 4);
+    if (part_off + router_part_bytes(*shape) > LILY_NOALLOC_SCRATCH_BYTES) return LILY_ERR_SCRATCH_LIMIT;
     if (shape->T == 0) {
         // nothing to route; the call's status (OK) still goes to device_status
         cudaError_t e;
@@ -838,7 +871,7 @@ int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *
     // The scratch keeps the previous call's contents: start from a clear control block.
     cudaError_t e;
     if ((e = cudaMemsetAsync(scratch, 0, sizeof(Ctrl), stream)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
-    if ((e = enqueue_route(*shape, *w, x, *r, r->logits, scratch, stream)) != cudaSuccess)
+    if ((e = enqueue_route(*shape, *w, x, *r, r->logits, scratch, at<float>(scratch, part_off), stream)) != cudaSuccess)
         return cuda_fail(e, "routing launch");
     if (device_status &&
         (e = cudaMemcpyAsync(device_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)

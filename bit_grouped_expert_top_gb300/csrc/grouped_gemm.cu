@@ -258,8 +258,16 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             n_routed = 0;
         }
     }
-    const int total_tiles = (n_routed + g.n_shared_blocks) * g.m_tiles;
+    const int KS = (MODE == kModeRouter && g.ksplit > 1) ? g.ksplit : 1;  // router K splits
+    const int total_tiles = (n_routed + g.n_shared_blocks) * g.m_tiles * KS;
     const int KB = g.KT / kBlk;  // blocks of four k-steps per unit (K padded)
+    // tile -> unit ut (router: its block) and the unit's K blocks [kb0, kb1)
+    auto k_range = [&](int tile, int &ut, int &kb0, int &kb1) {
+        ut = tile / KS;
+        const int ks = tile - ut * KS;
+        kb0 = ks * KB / KS;
+        kb1 = (ks + 1) * KB / KS;
+    };
 
     // Abort handling: a bounded wait that gives up raises abort_flag; every
     // later wait then returns at once.  Single-thread roles leave their loops;
@@ -287,13 +295,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             int blk = 0, issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const Unit u = unit_info<MODE>(g, tile, n_routed);
+                int ut, kb0, kb1;
+                k_range(tile, ut, kb0, kb1);
+                const Unit u = unit_info<MODE>(g, ut, n_routed);
                 if (u.rows <= 0) continue;
                 int r0, r1;
                 a_rows<MODE>(g, u, r0, r1);
                 const CUtensorMap *mA0 = u.shared ? &tmSA0 : &tmA0;
                 const CUtensorMap *mA1 = u.shared ? &tmSA1 : &tmA1;
-                for (int kb = 0; kb < KB && ok; ++kb, ++blk) {
+                for (int kb = kb0; kb < kb1 && ok; ++kb, ++blk) {
                     if (dequant_mode) {
                         // one raw stage: 4 k-steps = 128 contiguous bytes of each row
                         const int rs = blk & 1;
@@ -339,7 +349,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             int blk = 0, issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const Unit u = unit_info<MODE>(g, tile, n_routed);
+                int ut, kb0, kb1;
+                k_range(tile, ut, kb0, kb1);
+                const Unit u = unit_info<MODE>(g, ut, n_routed);
                 if (u.rows <= 0) continue;
                 // expert modes: routed rows in routing order, then the shared expert's
                 // rows (token order) after the T * top_k routed rows
@@ -356,7 +368,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         }
                     }
                 }
-                for (int kb = 0; kb < KB && ok; ++kb, ++blk) {
+                for (int kb = kb0; kb < kb1 && ok; ++kb, ++blk) {
                     const uint32_t bpar = (CYC == 2 ? (blk >> 1) : blk) & 1;
 #pragma unroll
                     for (int h = 0; h < SPB; ++h) {
@@ -395,13 +407,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             const uint32_t a_lo = static_cast<uint32_t>(ad0), a_hi = static_cast<uint32_t>(ad0 >> 32);
             const uint32_t ta = tmem_base + kTmemAOffset;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const Unit u = unit_info<MODE>(g, tile, n_routed);
+                int ut, kb0, kb1;
+                k_range(tile, ut, kb0, kb1);
+                const Unit u = unit_info<MODE>(g, ut, n_routed);
                 if (u.rows <= 0) continue;
                 if (!mbar_wait(&S.empty_acc[ab], acc_ph ^ 1, abort_flag, status)) break;
                 tc_fence_after();
                 const uint32_t idesc = idesc_f32acc(fmt, kTileM, u.n_mma);
                 const uint32_t dm = tmem_base + static_cast<uint32_t>(ab * 2 * kTileM + mat * kTileM);
-                for (int kb = 0; kb < KB && ok; ++kb, ++blk) {
+                for (int kb = kb0; kb < kb1 && ok; ++kb, ++blk) {
                     const uint32_t bpar = (CYC == 2 ? (blk >> 1) : blk) & 1;
 #pragma unroll
                     for (int h = 0; h < SPB; ++h) {
@@ -422,14 +436,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                                 const uint32_t at = ta + static_cast<uint32_t>(h * 128 + j * 32 + mat * 64);
 #pragma unroll
                                 for (int kk = 0; kk < kBK / 16; ++kk) {
-                                    const uint32_t acc = (kb | h | j | kk) != 0;
+                                    const uint32_t acc = ((kb - kb0) | h | j | kk) != 0;
                                     umma_ts(dm, at + kk * 8, desc64(blo + kk * 2, b_hi), idesc, acc);
                                 }
                             } else {
                                 const uint32_t alo = a_lo + static_cast<uint32_t>(as * (2 * kABytes >> 4) + mat * (kABytes >> 4));
 #pragma unroll
                                 for (int kk = 0; kk < kBK / 16; ++kk) {
-                                    const uint32_t acc = (kb | h | kk) != 0;
+                                    const uint32_t acc = ((kb - kb0) | h | kk) != 0;
                                     umma_ss(dm, desc64(alo + kk * 2, a_hi), desc64(blo + kk * 2, b_hi), idesc, acc);
                                 }
                             }
@@ -591,7 +605,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
             zpos = stop;
         };
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const Unit u = unit_info<MODE>(g, tile, n_routed);
+            int ut, kb0, kb1;
+            k_range(tile, ut, kb0, kb1);
+            const Unit u = unit_info<MODE>(g, ut, n_routed);
             if (u.rows <= 0) continue;
             if (MODE == kModeDown && eid < u.rows) {
                 int tok = u.p0 + eid;
@@ -698,12 +714,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         }
                     }
                 } else {
+                    // one K split: partial sums without the bias, in the split's slice
                     float bias0 = 0.0f, bias1 = 0.0f;
-                    if (g.router_bias) {
+                    if (g.router_bias && KS == 1) {
                         bias0 = g.router_bias[et];
                         bias1 = g.router_bias[kTileM + et];
                     }
-                    float *lbase = g.logits + static_cast<size_t>(u.p0) * g.E + et;
+                    float *lbase = (KS == 1 ? g.logits : g.logits_part + static_cast<size_t>(tile - ut * KS) * g.T * g.E) +
+                                   static_cast<size_t>(u.p0) * g.E + et;
                     for (int c0 = half * 16; c0 < u.n_mma; c0 += 32) {
                         uint32_t v0[16], v1[16];
                         tmem_ld_32x32b_x16(t0 + c0, v0);

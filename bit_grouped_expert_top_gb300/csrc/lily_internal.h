@@ -21,7 +21,10 @@ enum GemmMode : int { kModeRouter = 0, kModeGateUp = 1, kModeDown = 2 };
 //   kModeDown   : out[t][j] += w * (Wd_e h_p)_j                      (A = dequant(int4), B = h rows)
 // Work units are blocks of token rows (the routing block map for routed
 // experts, then ceil(T/block_rows) identity blocks for the shared expert) times
-// m_tiles pairs of 128-row weight tiles.
+// m_tiles pairs of 128-row weight tiles.  The router may also split K: unit
+// (block, split s) takes blocks [s KB / ksplit, (s + 1) KB / ksplit) of the KB
+// four-k-step blocks of K and writes its partial logits (no bias) to
+// logits_part[s]; the top-8 kernel adds the splits in order and the bias.
 struct GemmArgs {
     int mode;
     int T, d, E, top_k, I;
@@ -40,7 +43,9 @@ struct GemmArgs {
     const uint16_t *s0, *b0, *s1, *b1, *ss0, *sb0, *ss1, *sb1;
     const float *router_bias;
     const __half *xs;        // gate/up B: fp16 x in routing order [(top_k+1)*T][d] (routed rows, then shared)
-    float *logits;           // router output [T][E]
+    float *logits;           // router output [T][E] (ksplit == 1)
+    int ksplit;              // router: K splits (1 <= ksplit <= KT / 4); expert modes: 1
+    float *logits_part;      // router, ksplit > 1: partial logits [ksplit][T][E]
     __half *h;               // gate/up output, down input, fp16 [(top_k+1)*T][I]
     float *out;              // down output [T][d], accumulated
     Ctrl *ctrl;
@@ -92,7 +97,13 @@ cudaError_t launch_grouped_gemm(const GemmArgs &g, const CUtensorMap &tmB, const
 // Routing: top-k + per-chunk histogram (+ last-block scan and block map), then scatter.
 struct RouteArgs {
     int T, E, top_k, bm;
-    const float *logits;
+    // ksplit == 1: the router wrote the logits (bias included).  ksplit > 1: the
+    // router wrote ksplit partial sums; the top-8 kernel adds them in split order,
+    // then the bias, and writes the logits.
+    float *logits;              // [T][E]
+    int ksplit;
+    const float *logits_part;   // [ksplit][T][E]
+    const float *router_bias;   // [E] or NULL
     int *topk_idx;
     float *topk_w;
     int *counts, *offsets, *perm, *block_map, *n_blocks;
@@ -103,6 +114,7 @@ struct RouteArgs {
     Ctrl *ctrl;
 };
 constexpr int kRouteChunkTokens = 32;
+constexpr int kMaxRouterSplit = 8;  // router K splits (partial logits summed by the top-8 kernel)
 cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_route_scan(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_scatter(const RouteArgs &a, cudaStream_t stream);

@@ -6,7 +6,9 @@
 // submission with no CPU synchronisation (section "Prefill e decode").
 //
 // Three kernels, one stream, no host sync:
-//   topk_count_kernel : one warp per token selects the top 8 of 256 fp32 logits
+//   topk_count_kernel : (when the router split K: adds the partial logits in
+//                       split order and the bias, and writes the logits) one
+//                       warp per token selects the top 8 of 256 fp32 logits
 //                       (descending; lower index first among equal logits) in
 //                       eight warp-maximum rounds and computes the renormalised
 //                       softmax weights; each CTA then counts its chunk of
@@ -57,6 +59,8 @@ __device__ __forceinline__ int block_exclusive_scan_256(int v, int *scratch /* [
     return warp_off + incl - v;
 }
 
+// SPLIT: the router split K (a.ksplit > 1 partial sums, no bias).
+template <bool SPLIT>
 __global__ void __launch_bounds__(kRouteThreads)
 topk_count_kernel(const RouteArgs a)
 {
@@ -69,23 +73,50 @@ topk_count_kernel(const RouteArgs a)
     pdl_wait();  // the router's logits are complete
     __syncthreads();
 
-    // each warp's tokens, the next token's logits loaded while this one is ranked
+    // each warp's tokens, the next token's logits (or partial logits) loaded
+    // while this one is ranked; lane l holds experts 8 l .. 8 l + 7
     const int t0 = chunk * kRouteChunkTokens + warp * kTokPerWarp;
-    float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
-    if (t0 < a.T) {
-        const float4 *src = reinterpret_cast<const float4 *>(a.logits + static_cast<size_t>(t0) * kE + lane * 8);
-        n0 = __ldcg(src);
-        n1 = __ldcg(src + 1);
+    const int S = SPLIT ? a.ksplit : 1;
+    constexpr int NS = SPLIT ? kMaxRouterSplit : 1;
+    float4 bias0 = make_float4(0.f, 0.f, 0.f, 0.f), bias1 = bias0;
+    if (SPLIT && a.router_bias) {
+        bias0 = *reinterpret_cast<const float4 *>(a.router_bias + lane * 8);
+        bias1 = *reinterpret_cast<const float4 *>(a.router_bias + lane * 8 + 4);
     }
+    float4 n0[NS], n1[NS];
+    auto load_next = [&](int t) {
+        const float *base = SPLIT ? a.logits_part : a.logits;
+#pragma unroll
+        for (int s2 = 0; s2 < NS; ++s2) {
+            if (s2 < S) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    base + (static_cast<size_t>(s2) * a.T + t) * kE + lane * 8);
+                n0[s2] = __ldcg(src);
+                n1[s2] = __ldcg(src + 1);
+            }
+        }
+    };
+    if (t0 < a.T) load_next(t0);
     for (int i = 0; i < kTokPerWarp; ++i) {
         const int t = t0 + i;
         if (t >= a.T) break;
-        const float lv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-        if (i + 1 < kTokPerWarp && t + 1 < a.T) {
-            const float4 *src = reinterpret_cast<const float4 *>(a.logits + static_cast<size_t>(t + 1) * kE + lane * 8);
-            n0 = __ldcg(src);
-            n1 = __ldcg(src + 1);
+        float4 c0 = n0[0], c1 = n1[0];
+        if (SPLIT) {
+#pragma unroll
+            for (int s2 = 1; s2 < NS; ++s2) {
+                if (s2 < S) {
+                    c0.x += n0[s2].x; c0.y += n0[s2].y; c0.z += n0[s2].z; c0.w += n0[s2].w;
+                    c1.x += n1[s2].x; c1.y += n1[s2].y; c1.z += n1[s2].z; c1.w += n1[s2].w;
+                }
+            }
+            c0.x += bias0.x; c0.y += bias0.y; c0.z += bias0.z; c0.w += bias0.w;
+            c1.x += bias1.x; c1.y += bias1.y; c1.z += bias1.z; c1.w += bias1.w;
+            float4 *dst = reinterpret_cast<float4 *>(a.logits + static_cast<size_t>(t) * kE + lane * 8);
+            dst[0] = c0;
+            dst[1] = c1;
         }
+        const float lv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        if (i + 1 < kTokPerWarp && t + 1 < a.T) load_next(t + 1);
         int sel_e;
         float sel_w;
         warp_top8_keys(lv, lane, sel_e, sel_w);
@@ -209,7 +240,8 @@ scatter_kernel(const RouteArgs a)
 
 cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream)
 {
-    return launch_pdl(topk_count_kernel, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
+    if (a.ksplit > 1) return launch_pdl(topk_count_kernel<true>, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
+    return launch_pdl(topk_count_kernel<false>, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
 }
 
 cudaError_t launch_route_scan(const RouteArgs &a, cudaStream_t stream)

@@ -189,6 +189,10 @@ size_t lily_moe_workspace_bytes(const lily_moe_shape *shape, int32_t n_layers_de
  * Routing (steps: router logits, top-k + weights, histogram, exclusive scan,
  * stable scatter, block map), all on the GPU on `stream`, no host sync.
  * x: bf16 [T][d] device.  r: every member except r->logits must be non-NULL.
+ * When the 64-token blocks are fewer than the SMs, the router GEMM also splits
+ * the reduction over d (up to 8 parts, chosen from the shape alone) and the
+ * top-8 kernel adds the parts in a fixed order, so the logits stay
+ * bit-reproducible.
  */
 int lily_moe_route(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,
                    lily_moe_routing *r, void *ws, size_t ws_bytes, cudaStream_t stream);
@@ -343,9 +347,10 @@ int lily_gdn_scan(const lily_gdn_shape *shape, const uint16_t *q, const uint16_t
  *
  * It computes exactly what lily_moe_route computes (same kernels, same
  * results), but keeps its scratch (per-chunk expert counts, their scanned
- * write offsets, the last-block counter and the status word) in a fixed
- * array that the library holds in device memory on every GPU that loads it,
- * LILY_NOALLOC_SCRATCH_BYTES bytes, for the life of the process.
+ * write offsets, the last-block counter, the status word and the router's
+ * partial logits) in a fixed array that the library holds in device memory on
+ * every GPU that loads it, LILY_NOALLOC_SCRATCH_BYTES bytes (about 10.5 MB),
+ * for the life of the process.
  *   - T must be <= LILY_NOALLOC_MAX_TOKENS, else LILY_ERR_SCRATCH_LIMIT.
  *   - r->logits must be non-NULL (the logits are an output here, not scratch).
  *   - device_status: device int32 or NULL; if given, the call's device status
@@ -361,7 +366,11 @@ int lily_gdn_scan(const lily_gdn_shape *shape, const uint16_t *q, const uint16_t
  * Allocates nothing: no cudaMalloc, no cudaFree, no library allocation.
  */
 #define LILY_NOALLOC_MAX_TOKENS 8192
-#define LILY_NOALLOC_SCRATCH_BYTES (256 + 2 * 4 * 256 * (LILY_NOALLOC_MAX_TOKENS / 32))
+/* control block, two per-chunk tables of 256 int32 per 32 tokens, then the
+ * router's partial logits when it splits K (at most 152 x 64 token rows of 256
+ * fp32 partial logits) */
+#define LILY_NOALLOC_SCRATCH_BYTES \
+    (256 + 2 * 4 * 256 * (LILY_NOALLOC_MAX_TOKENS / 32) + 256 + 4 * 256 * 152 * 64)
 int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *w, const uint16_t *x,
                            lily_moe_routing *r, int32_t *device_status, cudaStream_t stream);
 
