@@ -91,6 +91,15 @@ def test_two_calls_continue_one_scan_exactly():
     assert np.array_equal(S2, S)
 
 
+def test_small_and_zero_decay():
+    # alpha of 1e-6, and 0 on every seventh token (the state is then replaced by
+    # the token's own write): still within the bound of the oracle
+    g = make_gdn(GDNConfig("smalla", T=100, H_k=2, H_v=4, d_k=64, d_v=32, seed=5))
+    g["alpha"] = torch.full_like(g["alpha"], 1e-6)
+    g["alpha"][::7] = 0.0
+    _check(g)
+
+
 def test_repeat_is_bit_identical():
     g = make_gdn(GDN_CONFIGS["gdn_t512"])
     a = _gpu(g)
