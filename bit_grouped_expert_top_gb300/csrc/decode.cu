@@ -93,6 +93,9 @@ __device__ __forceinline__ int perm_b_index(int k, int n)
     return (((kb * 8 + n) * 4 + t) * 8 + s) * 4 + idx;
 }
 
+// KEEP: float4 of the previous output a thread may keep in registers (4 or 8;
+// the smaller copy has less code to fetch when few values are kept).
+template <int KEEP>
 __global__ void __launch_bounds__(kDecThreads)
 dec_route_kernel(const DecodeLayerArgs a)
 {
@@ -123,23 +126,52 @@ dec_route_kernel(const DecodeLayerArgs a)
         for (int i = threadIdx.x; i < T * d / 8; i += kDecThreads)
             reinterpret_cast<uint4 *>(xs)[i] = reinterpret_cast<const uint4 *>(a.x_in)[i];
     } else {
-        // two passes over the previous output, each with all of a thread's loads in
-        // flight at once (d <= 4096: at most 4 float4 per thread and token)
+        // the sum of squares, then the scaled bf16 input; a thread's values are
+        // kept in registers when they are at most KEEP float4 in all,
+        // else read again in a second pass.  Each pass has all of a thread's
+        // loads in flight at once (d <= 4096: at most 4 float4 per thread and token).
         const int d4 = d / 4;
+        const int J = (d4 + kDecThreads - 1) / kDecThreads;  // float4 per thread and token
+        const bool kept = T * J <= KEEP;
         const float4 *po = reinterpret_cast<const float4 *>(a.prev_out);
-#pragma unroll 4
-        for (int t = 0; t < T; ++t) {  // up to four tokens' loads in flight together
-            float ss = 0.0f;
+        float4 keep[KEEP];
+        if (kept) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = threadIdx.x + j * kDecThreads;
-                if (c < d4) {
-                    const float4 v = __ldcg(po + static_cast<size_t>(t) * d4 + c);
-                    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+            for (int q = 0; q < KEEP; ++q) {
+                const int t = q / J, c = threadIdx.x + (q - t * J) * kDecThreads;
+                keep[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < T && c < d4) keep[q] = __ldcg(po + static_cast<size_t>(t) * d4 + c);
+            }
+#pragma unroll
+            for (int t = 0; t < KEEP; ++t) {
+                if (t < T) {
+                    float ss = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < KEEP; ++q) {
+                        if (q / J == t) {
+                            const float4 v = keep[q];
+                            ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+                        }
+                    }
+                    ss = warp_sum(ss);
+                    if (lane == 0) red[warp][t] = ss;
                 }
             }
-            ss = warp_sum(ss);
-            if (lane == 0) red[warp][t] = ss;
+        } else {
+#pragma unroll 4
+            for (int t = 0; t < T; ++t) {  // up to four tokens' loads in flight together
+                float ss = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = threadIdx.x + j * kDecThreads;
+                    if (c < d4) {
+                        const float4 v = __ldcg(po + static_cast<size_t>(t) * d4 + c);
+                        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+                    }
+                }
+                ss = warp_sum(ss);
+                if (lane == 0) red[warp][t] = ss;
+            }
         }
         __syncthreads();
         if (threadIdx.x < T) {
@@ -148,19 +180,27 @@ dec_route_kernel(const DecodeLayerArgs a)
             inv_rms[threadIdx.x] = 1.0f / sqrtf(s / static_cast<float>(d) + 1e-6f);
         }
         __syncthreads();
-#pragma unroll 4
-        for (int t = 0; t < T; ++t) {
+        auto put = [&](int t, int c, float4 v) {
             const float r = inv_rms[t];
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * r, v.y * r), hi = __floats2bfloat162_rn(v.z * r, v.w * r);
+            uint2 o;
+            o.x = *reinterpret_cast<const uint32_t *>(&lo);
+            o.y = *reinterpret_cast<const uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(xs + static_cast<size_t>(t) * d + 4 * c) = o;
+        };
+        if (kept) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = threadIdx.x + j * kDecThreads;
-                if (c < d4) {
-                    const float4 v = __ldcg(po + static_cast<size_t>(t) * d4 + c);
-                    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * r, v.y * r), hi = __floats2bfloat162_rn(v.z * r, v.w * r);
-                    uint2 o;
-                    o.x = *reinterpret_cast<const uint32_t *>(&lo);
-                    o.y = *reinterpret_cast<const uint32_t *>(&hi);
-                    *reinterpret_cast<uint2 *>(xs + static_cast<size_t>(t) * d + 4 * c) = o;
+            for (int q = 0; q < KEEP; ++q) {
+                const int t = q / J, c = threadIdx.x + (q - t * J) * kDecThreads;
+                if (t < T && c < d4) put(t, c, keep[q]);
+            }
+        } else {
+#pragma unroll 4
+            for (int t = 0; t < T; ++t) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = threadIdx.x + j * kDecThreads;
+                    if (c < d4) put(t, c, __ldcg(po + static_cast<size_t>(t) * d4 + c));
                 }
             }
         }
@@ -559,8 +599,8 @@ size_t decode_smem_gateup(int d) { return static_cast<size_t>(d) * 8 * 2 + kDecW
 
 cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStream_t stream)
 {
-    for (const void *k : {reinterpret_cast<const void *>(dec_route_kernel), reinterpret_cast<const void *>(dec_gateup_kernel),
-                          reinterpret_cast<const void *>(dec_down_kernel)}) {
+    for (const void *k : {reinterpret_cast<const void *>(dec_route_kernel<4>), reinterpret_cast<const void *>(dec_route_kernel<8>),
+                          reinterpret_cast<const void *>(dec_gateup_kernel), reinterpret_cast<const void *>(dec_down_kernel)}) {
         const cudaError_t e = set_max_dynamic_smem(k, 200 * 1024);
         if (e != cudaSuccess) return e;
     }
@@ -576,7 +616,8 @@ cudaError_t launch_decode_layer(const DecodeLayerArgs &a, int num_sms, cudaStrea
     cudaError_t e;
     cfg.gridDim = dim3((a.E + kDecWarps - 1) / kDecWarps);
     cfg.dynamicSmemBytes = decode_smem_route(a.T, a.d);
-    if ((e = cudaLaunchKernelEx(&cfg, dec_route_kernel, a)) != cudaSuccess) return e;
+    const int J = (a.d / 4 + kDecThreads - 1) / kDecThreads;  // float4 of the previous output per thread and token
+    if ((e = cudaLaunchKernelEx(&cfg, a.T * J <= 4 ? dec_route_kernel<4> : dec_route_kernel<8>, a)) != cudaSuccess) return e;
     cfg.gridDim = dim3(num_sms);
     cfg.dynamicSmemBytes = decode_smem_gateup(a.d);
     if ((e = cudaLaunchKernelEx(&cfg, dec_gateup_kernel, a)) != cudaSuccess) return e;
