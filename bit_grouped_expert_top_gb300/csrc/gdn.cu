@@ -158,13 +158,20 @@ __global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs 
         }
         __syncthreads();
         const GdnStage<DK> &B = S.st[c & 1];
-        // k and q of the chunk to fp32, once for all rows (pairs of bf16 -> two floats)
-        for (int i = tid; i < n * DK / 2; i += NT) {
-            const int t = i / (DK / 2), j = (i - t * (DK / 2)) * 2;
-            const uint32_t kw = *reinterpret_cast<const uint32_t *>(&B.k[t][j]);
-            const uint32_t qw = *reinterpret_cast<const uint32_t *>(&B.q[t][j]);
-            *reinterpret_cast<float2 *>(&S.kf[t][j]) = make_float2(__uint_as_float(kw << 16), __uint_as_float(kw & 0xFFFF0000u));
-            *reinterpret_cast<float2 *>(&S.qf[t][j]) = make_float2(__uint_as_float(qw << 16), __uint_as_float(qw & 0xFFFF0000u));
+        // k and q of the chunk to fp32, once for all rows (8 bf16 -> 8 floats per step)
+        for (int i = tid; i < n * DK / 8; i += NT) {
+            const int t = i / (DK / 8), j = (i - t * (DK / 8)) * 8;
+            const uint4 kw = *reinterpret_cast<const uint4 *>(&B.k[t][j]);
+            const uint4 qw = *reinterpret_cast<const uint4 *>(&B.q[t][j]);
+            float4 *kd = reinterpret_cast<float4 *>(&S.kf[t][j]), *qd = reinterpret_cast<float4 *>(&S.qf[t][j]);
+            kd[0] = make_float4(__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
+                                __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u));
+            kd[1] = make_float4(__uint_as_float(kw.z << 16), __uint_as_float(kw.z & 0xFFFF0000u),
+                                __uint_as_float(kw.w << 16), __uint_as_float(kw.w & 0xFFFF0000u));
+            qd[0] = make_float4(__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u),
+                                __uint_as_float(qw.y << 16), __uint_as_float(qw.y & 0xFFFF0000u));
+            qd[1] = make_float4(__uint_as_float(qw.z << 16), __uint_as_float(qw.z & 0xFFFF0000u),
+                                __uint_as_float(qw.w << 16), __uint_as_float(qw.w & 0xFFFF0000u));
         }
         __syncthreads();
         // Token loop, pipelined: u_t = (S_{t-1} k_t)_row is ready on entry; the
