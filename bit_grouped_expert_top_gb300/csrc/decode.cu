@@ -42,6 +42,12 @@ __device__ __forceinline__ uint4 ld_early(const void *p)
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
+__device__ __forceinline__ uint2 ld_early8(const void *p)
+{
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ uint16_t ld_early_u16(const uint16_t *p)
 {
     uint16_t v;
@@ -324,9 +330,12 @@ dec_gateup_kernel(const DecodeLayerArgs a)
     const int rt = warp & 1, ks = warp >> 1;
 
     // One round of weight loads of a task: up to 4 K blocks of this warp, both
-    // matrices, rows g and g + 8 of its 16-row tile.
+    // matrices, rows g and g + 8 of its 16-row tile.  The round's scales and
+    // biases (32 groups = 64 bytes of each row) are read as 8-byte pieces of 4
+    // groups, pieces t and t + 4 by lane t of the row's quad (coalesced within
+    // the quad), and handed to the lane that needs each group by a shuffle.
     uint4 qg[4], qg8[4], qu[4], qu8[4];
-    uint32_t sg[4], sg8[4], su[4], su8[4];
+    uint2 sbp[8][2];  // [gate g s, b; gate g+8 s, b; up g s, b; up g+8 s, b][piece t, t + 4]
     auto issue_loads = [&](int e, int i0, int kb0) {
         const bool sh = e < 0;
         const size_t row_g = (sh ? 0 : static_cast<size_t>(e) * I) + i0 + g, row_g8 = row_g + 8;
@@ -342,13 +351,30 @@ dec_gateup_kernel(const DecodeLayerArgs a)
                 qg8[m] = ld_early(gq + row_g8 * (d / 2) + off);
                 qu[m] = ld_early(uq + row_g * (d / 2) + off);
                 qu8[m] = ld_early(uq + row_g8 * (d / 2) + off);
-                const int grp = 2 * kb + (t >> 1);
-                sg[m] = load_sb(gs + row_g * ngroups, gb + row_g * ngroups, grp);
-                sg8[m] = load_sb(gs + row_g8 * ngroups, gb + row_g8 * ngroups, grp);
-                su[m] = load_sb(us + row_g * ngroups, ub + row_g * ngroups, grp);
-                su8[m] = load_sb(us + row_g8 * ngroups, ub + row_g8 * ngroups, grp);
             }
         }
+        const uint16_t *rows[8] = {gs + row_g * ngroups, gb + row_g * ngroups, gs + row_g8 * ngroups,
+                                   gb + row_g8 * ngroups, us + row_g * ngroups, ub + row_g * ngroups,
+                                   us + row_g8 * ngroups, ub + row_g8 * ngroups};
+        const int p0 = 2 * (kb0 - ks);  // the round's first group
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl) {
+                const int gp = p0 + 4 * (t + 4 * sl);  // ngroups is a multiple of 4: pieces are whole
+                sbp[k][sl] = gp < ngroups ? ld_early8(rows[k] + gp) : make_uint2(0u, 0u);
+            }
+        }
+    };
+    // scale (low half) and bias (high half) of group 2 kb + (t >> 1) of row k / 2
+    // of sbp, kb = kb0 + 4 m: piece 2 m + ks / 2 of the round, word ks % 2 of it
+    auto pick_sb = [&](int k, int m) {
+        const int piece = 2 * m + (ks >> 1), src = (lane & ~3) | (piece & 3);
+        const uint2 ps = (piece >> 2) ? sbp[k][1] : sbp[k][0], pb = (piece >> 2) ? sbp[k + 1][1] : sbp[k + 1][0];
+        const uint32_t ws = __shfl_sync(0xffffffffu, (ks & 1) ? ps.y : ps.x, src);
+        const uint32_t wb = __shfl_sync(0xffffffffu, (ks & 1) ? pb.y : pb.x, src);
+        const int hi = (t >> 1) & 1;
+        return (hi ? ws >> 16 : ws & 0xFFFFu) | ((hi ? wb >> 16 : wb & 0xFFFFu) << 16);
     };
     pdl_trigger();
     // The shared expert is unit 0 and does not depend on the routing: its CTAs
@@ -464,8 +490,8 @@ dec_gateup_kernel(const DecodeLayerArgs a)
                 const int kb = kb0 + 4 * m;
                 if (kb < nkb) {
                     const uint2 *bf = reinterpret_cast<const uint2 *>(xp + (((kb * 8 + g) * 4 + t) * 8) * 4);
-                    mma_kblock(accg, qg[m], qg8[m], sg[m], sg8[m], bf);
-                    mma_kblock(accu, qu[m], qu8[m], su[m], su8[m], bf);
+                    mma_kblock(accg, qg[m], qg8[m], pick_sb(0, m), pick_sb(2, m), bf);
+                    mma_kblock(accu, qu[m], qu8[m], pick_sb(4, m), pick_sb(6, m), bf);
                 }
             }
         }
