@@ -587,10 +587,15 @@ dec_down_kernel(const DecodeLayerArgs a)
                         }
                         load_w(m, e, jb, j0);
                     }
-                    // token column g of h' is zero for g >= T: no load
-                    const uint2 *src = reinterpret_cast<const uint2 *>(a.h) + ((kb * 8 + g) * 4 + t) * 8;
+                    // token column g of h' is zero for g >= T: no load.  The lane's 8
+                    // fragments are 64 contiguous bytes: four 16-byte loads
+                    const uint4 *src = reinterpret_cast<const uint4 *>(a.h) + ((kb * 8 + g) * 4 + t) * 4;
 #pragma unroll
-                    for (int s2 = 0; s2 < 8; ++s2) bfr[m][s2] = g < T ? __ldcg(src + s2) : make_uint2(0u, 0u);
+                    for (int s2 = 0; s2 < 4; ++s2) {
+                        const uint4 v = g < T ? __ldcg(src + s2) : make_uint4(0u, 0u, 0u, 0u);
+                        bfr[m][2 * s2] = make_uint2(v.x, v.y);
+                        bfr[m][2 * s2 + 1] = make_uint2(v.z, v.w);
+                    }
                 }
             }
 #pragma unroll
