@@ -48,10 +48,10 @@ __device__ __forceinline__ uint2 ld_early8(const void *p)
     asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
     return v;
 }
-__device__ __forceinline__ uint16_t ld_early_u16(const uint16_t *p)
+__device__ __forceinline__ uint32_t ld_early_u32(const void *p)
 {
-    uint16_t v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
 
@@ -307,12 +307,6 @@ __device__ __forceinline__ void mma_kblock(float (&d)[4], uint4 q_g, uint4 q_g8,
     }
 }
 
-// Scale and bias of this lane's group in a K block, packed (scale low, bias high).
-__device__ __forceinline__ uint32_t load_sb(const uint16_t *s_row, const uint16_t *b_row, int group)
-{
-    return static_cast<uint32_t>(ld_early_u16(s_row + group)) | (static_cast<uint32_t>(ld_early_u16(b_row + group)) << 16);
-}
-
 // gate/up: task = (unit, 32 rows of I); warp w takes rows 16 (w % 2) .. + 16
 // and the K blocks kb = w / 2 (mod 4), both matrices; the four K-split partial
 // tiles are summed in shared memory, then h' = f16(w_u[t] * silu(gate) * up) is
@@ -543,7 +537,10 @@ dec_down_kernel(const DecodeLayerArgs a)
     const int g = lane >> 2, t = lane & 3;
     const int T = a.T, d = a.d, I = a.I, kpu = I / kKB, ngroups = I / 64;
     uint4 q[3], q8[3];
-    uint32_t sb[3], sb8[3];
+    // scale / bias of K block jb: groups 2 jb and 2 jb + 1 (one 32-bit word) of
+    // rows j0 + g and j0 + g + 8; lane t of a row's quad loads word t of
+    // {scale row, bias row, scale row + 8, bias row + 8}, shuffles share them
+    uint32_t sbw[3];
     uint2 bfr[3][8];
     // weight loads of K block kb (unit u, block jb) for output rows j0 + g, j0 + g + 8
     auto load_w = [&](int m, int e, int jb, int j0) {
@@ -554,9 +551,8 @@ dec_down_kernel(const DecodeLayerArgs a)
         const size_t off = static_cast<size_t>(jb) * (kKB / 2) + t * 16;
         q[m] = ld_early(dq + row * (I / 2) + off);
         q8[m] = ld_early(dq + (row + 8) * (I / 2) + off);
-        const int grp = 2 * jb + (t >> 1);
-        sb[m] = load_sb(ds + row * ngroups, db + row * ngroups, grp);
-        sb8[m] = load_sb(ds + (row + 8) * ngroups, db + (row + 8) * ngroups, grp);
+        const uint16_t *w = (t & 1 ? db : ds) + (row + 8 * (t >> 1)) * ngroups + 2 * jb;
+        sbw[m] = ld_early_u32(w);
     };
     pdl_trigger();
     // unit 0 is the shared expert: the warps whose first K block lies in it issue
@@ -599,8 +595,18 @@ dec_down_kernel(const DecodeLayerArgs a)
                 }
             }
 #pragma unroll
-            for (int m = 0; m < 3; ++m)
-                if (kb0 + m * kDownWarps < n_kb) mma_kblock(acc, q[m], q8[m], sb[m], sb8[m], bfr[m]);
+            for (int m = 0; m < 3; ++m) {
+                if (kb0 + m * kDownWarps < n_kb) {
+                    const int quad = lane & ~3, hi = (t >> 1) & 1;
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t v = __shfl_sync(0xffffffffu, sbw[m], quad + k);
+                        wv[k] = hi ? v >> 16 : v & 0xFFFFu;
+                    }
+                    mma_kblock(acc, q[m], q8[m], wv[0] | (wv[1] << 16), wv[2] | (wv[3] << 16), bfr[m]);
+                }
+            }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) red[warp][lane][q] = acc[q];
