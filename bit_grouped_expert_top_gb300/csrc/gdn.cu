@@ -191,13 +191,14 @@ __global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs 
         load_row(S.kf, 0, ka);
         float u;
         {
-            float2 p0 = make_float2(0.f, 0.f), p1 = p0;
+            // the same four partial sums and order as the dots in the token loop,
+            // so a scan split between calls gives the same bits
+            float2 pa[4];
 #pragma unroll
-            for (int j = 0; j < NP; j += 2) {
-                p0 = ffma2(st[j], ka[j], p0);
-                if (j + 1 < NP) p1 = ffma2(st[j + 1], ka[j + 1], p1);
-            }
-            u = row_sum((p0.x + p0.y) + (p1.x + p1.y));
+            for (int c = 0; c < 4; ++c) pa[c] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) pa[j & 3] = ffma2(st[j], ka[j], pa[j & 3]);
+            u = row_sum(((pa[0].x + pa[0].y) + (pa[1].x + pa[1].y)) + ((pa[2].x + pa[2].y) + (pa[3].x + pa[3].y)));
         }
         // one token: update with kc (= k_t), dots with q_t and kn (= k_{t+1})
         auto step = [&](int t, const float2(&kc)[NP], float2(&kn)[NP]) {
@@ -208,20 +209,18 @@ __global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs 
             const float vr = __uint_as_float(static_cast<uint32_t>(B.v[t][r]) << 16);
             const float cc = be * (vr - al * u);
             const float2 al2 = make_float2(al, al), cc2 = make_float2(cc, cc);
-            float2 o0 = make_float2(0.f, 0.f), o1 = o0, p0 = o0, p1 = o0;
+            // four partial sums per dot, so each dependence chain is NP / 4 long
+            float2 oa[4], pa[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) oa[c] = pa[c] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
                 st[j] = ffma2(al2, st[j], fmul2(cc2, kc[j]));
-                if (j & 1) {
-                    o1 = ffma2(st[j], qf[j], o1);
-                    p1 = ffma2(st[j], kn[j], p1);
-                } else {
-                    o0 = ffma2(st[j], qf[j], o0);
-                    p0 = ffma2(st[j], kn[j], p0);
-                }
+                oa[j & 3] = ffma2(st[j], qf[j], oa[j & 3]);
+                pa[j & 3] = ffma2(st[j], kn[j], pa[j & 3]);
             }
-            float o = (o0.x + o0.y) + (o1.x + o1.y);
-            float un = (p0.x + p0.y) + (p1.x + p1.y);
+            float o = ((oa[0].x + oa[0].y) + (oa[1].x + oa[1].y)) + ((oa[2].x + oa[2].y) + (oa[3].x + oa[3].y));
+            float un = ((pa[0].x + pa[0].y) + (pa[1].x + pa[1].y)) + ((pa[2].x + pa[2].y) + (pa[3].x + pa[3].y));
 #pragma unroll
             for (int m = 1; m < TPR; m <<= 1) {
                 o += __shfl_xor_sync(0xffffffffu, o, m);
