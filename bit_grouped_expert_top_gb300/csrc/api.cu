@@ -408,9 +408,13 @@ cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, co
     ra.chunk_base = at<int>(ws, L.chunk_base);
     ra.n_chunks = static_cast<int>(ceil_div(s.T, kRouteChunkTokens));
     ra.ctrl = ctrl;
-    if ((e = launch_topk_count(ra, stream)) != cudaSuccess) return e;
-    if ((e = launch_route_scan(ra, stream)) != cudaSuccess) return e;
-    if ((e = launch_scatter(ra, stream)) != cudaSuccess) return e;
+    if (ra.n_chunks <= kRouteFusedChunks) {
+        if ((e = launch_route_fused(ra, stream)) != cudaSuccess) return e;
+    } else {
+        if ((e = launch_topk_count(ra, stream)) != cudaSuccess) return e;
+        if ((e = launch_route_scan(ra, stream)) != cudaSuccess) return e;
+        if ((e = launch_scatter(ra, stream)) != cudaSuccess) return e;
+    }
     if (events && (e = cudaEventRecord(events[2], stream)) != cudaSuccess) return e;
     return cudaSuccess;
 }

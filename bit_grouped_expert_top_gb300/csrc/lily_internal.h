@@ -116,6 +116,9 @@ struct RouteArgs {
 constexpr int kRouteChunkTokens = 32;
 constexpr int kMaxRouterSplit = 8;  // router K splits (partial logits summed by the top-8 kernel)
 cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream);
+// All three steps in one launch (n_chunks <= kRouteFusedChunks).
+constexpr int kRouteFusedChunks = 64;
+cudaError_t launch_route_fused(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_route_scan(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_scatter(const RouteArgs &a, cudaStream_t stream);
 

@@ -5,7 +5,9 @@
 // routing histogram, prefix scan, scatter and block map stay inside one GPU
 // submission with no CPU synchronisation (section "Prefill e decode").
 //
-// Three kernels, one stream, no host sync:
+// Three kernels, one stream, no host sync (for at most kRouteFusedChunks
+// chunks the three steps run as one kernel, route_fused_kernel, with a grid
+// barrier between the counts and the scatter):
 //   topk_count_kernel : (when the router split K: adds the partial logits in
 //                       split order and the bias, and writes the logits) one
 //                       warp per token selects the top 8 of 256 fp32 logits
@@ -34,6 +36,13 @@ constexpr int kTokPerWarp = kRouteChunkTokens / 8;
 constexpr int kE = 256;                          // experts (one per thread in the scans)
 constexpr int kTopK = 8;
 
+__device__ __forceinline__ unsigned int ld_acquire_gpu_u32(const unsigned int *p)
+{
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Exclusive scan over the 256 threads of the block; returns the exclusive
 // prefix, writes the total to *total.
 __device__ __forceinline__ int block_exclusive_scan_256(int v, int *scratch /* [8] */, int *total)
@@ -59,18 +68,14 @@ __device__ __forceinline__ int block_exclusive_scan_256(int v, int *scratch /* [
     return warp_off + incl - v;
 }
 
-// SPLIT: the router split K (a.ksplit > 1 partial sums, no bias).
+// Top-8 and weights of the chunk's tokens and the chunk's per-expert counts
+// (into hist, zeroed and complete on return).  SPLIT: the router split K
+// (a.ksplit > 1 partial sums, no bias).
 template <bool SPLIT>
-__global__ void __launch_bounds__(kRouteThreads)
-topk_count_kernel(const RouteArgs a)
+__device__ __forceinline__ void topk_chunk(const RouteArgs &a, int chunk, int *hist)
 {
-    __shared__ int hist[kE];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int chunk = blockIdx.x;
-
     hist[threadIdx.x] = 0;
-    pdl_trigger();
-    pdl_wait();  // the router's logits are complete
     __syncthreads();
 
     // each warp's tokens, the next token's logits (or partial logits) loaded
@@ -127,12 +132,46 @@ topk_count_kernel(const RouteArgs a)
         }
     }
     __syncthreads();
-    a.chunk_counts[static_cast<size_t>(chunk) * kE + threadIdx.x] = hist[threadIdx.x];
+}
+
+template <bool SPLIT>
+__global__ void __launch_bounds__(kRouteThreads)
+topk_count_kernel(const RouteArgs a)
+{
+    __shared__ int hist[kE];
+    pdl_trigger();
+    pdl_wait();  // the router's logits are complete
+    topk_chunk<SPLIT>(a, blockIdx.x, hist);
+    a.chunk_counts[static_cast<size_t>(blockIdx.x) * kE + threadIdx.x] = hist[threadIdx.x];
 }
 
 // CTA e: exclusive scan of expert e's per-chunk counts in chunk order (chunk
 // bases relative to the expert's first sorted row) and the expert's total.
 // The last CTA scans the totals over experts and writes the block map.
+// Thread x = expert x with its total total_e: returns the expert's first row in
+// expert-sorted order (exclusive scan over experts); if `write`, also writes
+// counts-derived offsets, n_blocks and the block map.
+__device__ __forceinline__ int expert_tables(const RouteArgs &a, int total_e, int *scratch, bool write)
+{
+    const int x = threadIdx.x;  // expert
+    int sum_all;
+    const int off = block_exclusive_scan_256(total_e, scratch, &sum_all);
+    if (!write) return off;
+    const int nb = (total_e + a.bm - 1) / a.bm;
+    int nb_all;
+    const int bstart = block_exclusive_scan_256(nb, scratch, &nb_all);
+    a.offsets[x] = off;
+    if (x == kE - 1) a.offsets[kE] = off + total_e;
+    if (x == 0) *a.n_blocks = nb_all;
+    for (int b = 0; b < nb; ++b) {
+        int *ent = a.block_map + 3 * static_cast<size_t>(bstart + b);
+        ent[0] = x;
+        ent[1] = off + b * a.bm;
+        ent[2] = min(a.bm, total_e - b * a.bm);
+    }
+    return off;
+}
+
 __global__ void __launch_bounds__(kRouteThreads)
 scan_kernel(const RouteArgs a)
 {
@@ -163,38 +202,17 @@ scan_kernel(const RouteArgs a)
     if (!is_last) return;
     __threadfence();
 
-    const int x = threadIdx.x;  // expert
-    const int total_e = __ldcg(a.counts + x);
-    int sum_all;
-    const int off = block_exclusive_scan_256(total_e, scratch, &sum_all);
-    const int nb = (total_e + a.bm - 1) / a.bm;
-    int nb_all;
-    const int bstart = block_exclusive_scan_256(nb, scratch, &nb_all);
-    a.offsets[x] = off;
-    if (x == kE - 1) a.offsets[kE] = off + total_e;
-    if (x == 0) *a.n_blocks = nb_all;
-    for (int b = 0; b < nb; ++b) {
-        int *ent = a.block_map + 3 * static_cast<size_t>(bstart + b);
-        ent[0] = x;
-        ent[1] = off + b * a.bm;
-        ent[2] = min(a.bm, total_e - b * a.bm);
-    }
+    expert_tables(a, __ldcg(a.counts + threadIdx.x), scratch, true);
     if (threadIdx.x == 0) a.ctrl->ticket = 0u;
 }
 
-__global__ void __launch_bounds__(kRouteThreads)
-scatter_kernel(const RouteArgs a)
+// Writes the chunk's assignments into expert-sorted order; base[e] (shared,
+// set and visible on entry) is the chunk's first row of expert e.
+__device__ __forceinline__ void scatter_chunk(const RouteArgs &a, int chunk, int *base, int (*cnt)[kE])
 {
-    __shared__ int cnt[8][kE];
-    __shared__ int base[kE];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int chunk = blockIdx.x;
     const int n_assign = kRouteChunkTokens * kTopK;  // assignments per chunk
     const int total = a.T * kTopK;
-    pdl_trigger();
-    pdl_wait();  // offsets and chunk bases are complete
-
-    base[threadIdx.x] = a.offsets[threadIdx.x] + a.chunk_base[static_cast<size_t>(chunk) * kE + threadIdx.x];
     const unsigned lt_mask = (1u << lane) - 1u;
 
     for (int round = 0; round < n_assign / kRouteThreads; ++round) {
@@ -236,12 +254,81 @@ scatter_kernel(const RouteArgs a)
     }
 }
 
+__global__ void __launch_bounds__(kRouteThreads)
+scatter_kernel(const RouteArgs a)
+{
+    __shared__ int cnt[8][kE];
+    __shared__ int base[kE];
+    pdl_trigger();
+    pdl_wait();  // offsets and chunk bases are complete
+    base[threadIdx.x] = a.offsets[threadIdx.x] + a.chunk_base[static_cast<size_t>(blockIdx.x) * kE + threadIdx.x];
+    __syncthreads();
+    scatter_chunk(a, blockIdx.x, base, cnt);
+}
+
+// The three steps in one launch, for at most kRouteFusedChunks chunks (all CTAs
+// resident): top-8 and counts per chunk; a grid barrier (arrival count in the
+// control block, reset by the router GEMM of the same call); then every CTA
+// adds up the chunk counts it needs (all chunks for the totals, the earlier
+// ones for its own base), CTA 0 writes counts, offsets and the block map, and
+// each CTA scatters its chunk.
+template <bool SPLIT>
+__global__ void __launch_bounds__(kRouteThreads)
+route_fused_kernel(const RouteArgs a)
+{
+    __shared__ int hist[kE];
+    __shared__ int cnt[8][kE];
+    __shared__ int base[kE];
+    __shared__ int scratch[8];
+    __shared__ int go;
+    const int chunk = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();  // the router's logits (and its reset of the arrival count) are complete
+    topk_chunk<SPLIT>(a, chunk, hist);
+    a.chunk_counts[static_cast<size_t>(chunk) * kE + threadIdx.x] = hist[threadIdx.x];
+    __syncthreads();  // every count of this chunk stored
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        __threadfence();
+        atomicAdd(&a.ctrl->ticket, 1u);
+        const uint64_t t0 = global_timer_ns();
+        while (ld_acquire_gpu_u32(&a.ctrl->ticket) < static_cast<unsigned int>(gridDim.x)) {
+            if (global_timer_ns() - t0 > LILY_WAIT_LIMIT_NS) {
+                record_error(&a.ctrl->status, kErrDeviceTimeout);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence();
+        go = ok;
+    }
+    __syncthreads();
+    if (!go) return;
+    int total_e = 0, prefix_e = 0;
+    for (int c = 0; c < a.n_chunks; ++c) {
+        const int v = __ldcg(a.chunk_counts + static_cast<size_t>(c) * kE + threadIdx.x);
+        total_e += v;
+        if (c < chunk) prefix_e += v;
+    }
+    if (chunk == 0) a.counts[threadIdx.x] = total_e;
+    const int off = expert_tables(a, total_e, scratch, chunk == 0);
+    base[threadIdx.x] = off + prefix_e;
+    __syncthreads();
+    scatter_chunk(a, chunk, base, cnt);
+}
+
 }  // namespace
 
 cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream)
 {
     if (a.ksplit > 1) return launch_pdl(topk_count_kernel<true>, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
     return launch_pdl(topk_count_kernel<false>, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
+}
+
+cudaError_t launch_route_fused(const RouteArgs &a, cudaStream_t stream)
+{
+    if (a.ksplit > 1) return launch_pdl(route_fused_kernel<true>, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
+    return launch_pdl(route_fused_kernel<false>, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
 }
 
 cudaError_t launch_route_scan(const RouteArgs &a, cudaStream_t stream)
