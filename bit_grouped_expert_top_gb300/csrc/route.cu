@@ -305,6 +305,7 @@ route_fused_kernel(const RouteArgs a)
     __syncthreads();
     if (!go) return;
     int total_e = 0, prefix_e = 0;
+#pragma unroll 8
     for (int c = 0; c < a.n_chunks; ++c) {
         const int v = __ldcg(a.chunk_counts + static_cast<size_t>(c) * kE + threadIdx.x);
         total_e += v;
