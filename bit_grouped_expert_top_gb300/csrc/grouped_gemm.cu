@@ -787,15 +787,21 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8_kperm(const uint4 v)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// WPT warps per token (1, 2, 4 or 8): warp `part` of a token converts every
+// WPT-th 32-element stretch of the row, so that few tokens still spread over
+// all SMs.
+template <int WPT>
 __global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, const int *inv, uint4 *xs, int T, int d8,
                                                            int top_k, int *status)
 {
+    constexpr int wpt = WPT;
     const int lane = threadIdx.x & 31;
     const int64_t routed = static_cast<int64_t>(T) * top_k;
     const int stride = gridDim.x * 8;
     pdl_trigger();
     pdl_wait();  // the inverse permutation is complete
-    for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += stride) {
+    for (int tw = blockIdx.x * 8 + (threadIdx.x >> 5); tw < T * wpt; tw += stride) {
+        const int t = tw / wpt, part = tw - t * wpt;
         // lane j < top_k holds the row of slot j; lane top_k the shared expert's row
         int64_t row = -1;
         if (lane < top_k) {
@@ -808,12 +814,12 @@ __global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, const
             row = routed + t;
         }
         const uint4 *src = x + static_cast<int64_t>(t) * d8;
-        for (int i0 = 0; i0 < d8; i0 += 256) {
+        for (int i0 = part * 32; i0 < d8; i0 += 256 * wpt) {
             uint4 v[8];
             bool inf = false;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int i = i0 + j * 32 + lane;
+                const int i = i0 + j * 32 * wpt + lane;
                 if (i < d8) {
                     v[j] = bf16x8_to_f16x8_kperm(__ldg(src + i));
                     inf |= f16x2_has_inf(v[j].x) | f16x2_has_inf(v[j].y) | f16x2_has_inf(v[j].z) |
@@ -827,7 +833,7 @@ __global__ void __launch_bounds__(256) prep_experts_kernel(const uint4 *x, const
                 uint4 *dst = xs + r * d8;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int i = i0 + j * 32 + lane;
+                    const int i = i0 + j * 32 * wpt + lane;
                     if (i < d8) dst[i] = v[j];
                 }
             }
@@ -858,8 +864,13 @@ cudaError_t launch_prep_experts(const uint16_t *x, const int *inv, __half *xs, i
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = std::max(1, std::min((T + 7) / 8, sms * 8));
-    return launch_pdl(prep_experts_kernel, dim3(grid), dim3(256), 0, stream, reinterpret_cast<const uint4 *>(x), inv,
+    // warps per token: about 16 warps per SM in all, at most 8 per token
+    int wpt = 1;
+    while (wpt < 8 && static_cast<int64_t>(T) * wpt < static_cast<int64_t>(sms) * 16) wpt *= 2;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((static_cast<int64_t>(T) * wpt + 7) / 8, sms * 8)));
+    auto kernel = wpt == 8 ? prep_experts_kernel<8> : wpt == 4 ? prep_experts_kernel<4>
+                                                  : wpt == 2 ? prep_experts_kernel<2> : prep_experts_kernel<1>;
+    return launch_pdl(kernel, dim3(grid), dim3(256), 0, stream, reinterpret_cast<const uint4 *>(x), inv,
                       reinterpret_cast<uint4 *>(xs), T, d / 8, top_k, status);
 }
 
