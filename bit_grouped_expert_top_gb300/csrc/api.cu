@@ -133,7 +133,7 @@ PrefillLayout prefill_layout(const lily_moe_shape &s)
 {
     PrefillLayout L{};
     const int64_t T = s.T, E = s.E, k = s.top_k;
-    const int64_t C = std::max<int64_t>(1, ceil_div(T, kRouteChunkTokens));
+    const int64_t C = route_chunks(T);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t at = off;
@@ -406,7 +406,7 @@ cudaError_t enqueue_route(const lily_moe_shape &s, const lily_moe_weights &w, co
     ra.inv = inv;
     ra.chunk_counts = at<int>(ws, L.chunk_counts);
     ra.chunk_base = at<int>(ws, L.chunk_base);
-    ra.n_chunks = static_cast<int>(ceil_div(s.T, kRouteChunkTokens));
+    ra.n_chunks = static_cast<int>(route_chunks(s.T));
     ra.ctrl = ctrl;
     if (ra.n_chunks <= kRouteFusedChunks) {
         if ((e = launch_route_fused(ra, stream)) != cudaSuccess) return e;
@@ -860,7 +860,7 @@ int lily_moe_route_noalloc(const lily_moe_shape *shape, const lily_moe_weights *
     // (placed after the tables here), which fit in the fixed scratch.
     const PrefillLayout L = prefill_layout(*shape);
     const size_t part_off =
-        align_up(L.chunk_base + static_cast<size_t>(ceil_div(shape->T, kRouteChunkTokens)) * shape->E * 4);
+        align_up(L.chunk_base + static_cast<size_t>(route_chunks(shape->T)) * shape->E * 4);
     if (part_off + router_part_bytes(*shape) > LILY_NOALLOC_SCRATCH_BYTES) return LILY_ERR_SCRATCH_LIMIT;
     if (shape->T == 0) {
         // nothing to route; the call's status (OK) still goes to device_status

@@ -114,6 +114,14 @@ struct RouteArgs {
     Ctrl *ctrl;
 };
 constexpr int kRouteChunkTokens = 32;
+// Tokens per routing chunk: 32, fewer for small T (more CTAs in the one-launch
+// path), and the number of chunks.
+inline int route_chunk_tokens(int64_t T) { return T <= 512 ? 8 : T <= 1024 ? 16 : kRouteChunkTokens; }
+inline int64_t route_chunks(int64_t T)
+{
+    const int ct = route_chunk_tokens(T);
+    return T > 0 ? (T + ct - 1) / ct : 1;
+}
 constexpr int kMaxRouterSplit = 8;  // router K splits (partial logits summed by the top-8 kernel)
 cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream);
 // All three steps in one launch (n_chunks <= kRouteFusedChunks).

@@ -14,7 +14,7 @@
 //                       (descending; lower index first among equal logits) in
 //                       eight warp-maximum rounds and computes the renormalised
 //                       softmax weights; each CTA then counts its chunk of
-//                       kRouteChunkTokens tokens per expert.
+//                       tokens per expert (32 tokens; 8 or 16 for small T).
 //   scan_kernel       : one CTA per expert scans that expert's per-chunk counts
 //                       in chunk order (each chunk's base within the expert) and
 //                       writes its total; the last CTA to finish (ticket
@@ -32,7 +32,6 @@ namespace lily {
 namespace {
 
 constexpr int kRouteThreads = 256;               // 8 warps
-constexpr int kTokPerWarp = kRouteChunkTokens / 8;
 constexpr int kE = 256;                          // experts (one per thread in the scans)
 constexpr int kTopK = 8;
 
@@ -68,19 +67,20 @@ __device__ __forceinline__ int block_exclusive_scan_256(int v, int *scratch /* [
     return warp_off + incl - v;
 }
 
-// Top-8 and weights of the chunk's tokens and the chunk's per-expert counts
+// Top-8 and weights of the chunk's CT tokens and the chunk's per-expert counts
 // (into hist, zeroed and complete on return).  SPLIT: the router split K
 // (a.ksplit > 1 partial sums, no bias).
-template <bool SPLIT>
+template <bool SPLIT, int CT>
 __device__ __forceinline__ void topk_chunk(const RouteArgs &a, int chunk, int *hist)
 {
+    constexpr int kTokPerWarp = CT / 8;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     hist[threadIdx.x] = 0;
     __syncthreads();
 
     // each warp's tokens, the next token's logits (or partial logits) loaded
     // while this one is ranked; lane l holds experts 8 l .. 8 l + 7
-    const int t0 = chunk * kRouteChunkTokens + warp * kTokPerWarp;
+    const int t0 = chunk * CT + warp * kTokPerWarp;
     const int S = SPLIT ? a.ksplit : 1;
     constexpr int NS = SPLIT ? kMaxRouterSplit : 1;
     float4 bias0 = make_float4(0.f, 0.f, 0.f, 0.f), bias1 = bias0;
@@ -141,7 +141,7 @@ topk_count_kernel(const RouteArgs a)
     __shared__ int hist[kE];
     pdl_trigger();
     pdl_wait();  // the router's logits are complete
-    topk_chunk<SPLIT>(a, blockIdx.x, hist);
+    topk_chunk<SPLIT, kRouteChunkTokens>(a, blockIdx.x, hist);
     a.chunk_counts[static_cast<size_t>(blockIdx.x) * kE + threadIdx.x] = hist[threadIdx.x];
 }
 
@@ -206,18 +206,19 @@ scan_kernel(const RouteArgs a)
     if (threadIdx.x == 0) a.ctrl->ticket = 0u;
 }
 
-// Writes the chunk's assignments into expert-sorted order; base[e] (shared,
-// set and visible on entry) is the chunk's first row of expert e.
+// Writes the chunk's (CT tokens') assignments into expert-sorted order; base[e]
+// (shared, set and visible on entry) is the chunk's first row of expert e.
+template <int CT>
 __device__ __forceinline__ void scatter_chunk(const RouteArgs &a, int chunk, int *base, int (*cnt)[kE])
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int n_assign = kRouteChunkTokens * kTopK;  // assignments per chunk
+    constexpr int n_assign = CT * kTopK;  // assignments per chunk
     const int total = a.T * kTopK;
     const unsigned lt_mask = (1u << lane) - 1u;
 
-    for (int round = 0; round < n_assign / kRouteThreads; ++round) {
+    for (int round = 0; round < (n_assign + kRouteThreads - 1) / kRouteThreads; ++round) {
         const int ga = chunk * n_assign + round * kRouteThreads + threadIdx.x;  // = t*8 + j
-        const bool valid = ga < total;
+        const bool valid = round * kRouteThreads + static_cast<int>(threadIdx.x) < n_assign && ga < total;
         int e = valid ? a.topk_idx[ga] : -1;
         if (valid && (e < 0 || e >= kE)) {
             record_error(&a.ctrl->status, kErrDeviceIndex);
@@ -263,7 +264,7 @@ scatter_kernel(const RouteArgs a)
     pdl_wait();  // offsets and chunk bases are complete
     base[threadIdx.x] = a.offsets[threadIdx.x] + a.chunk_base[static_cast<size_t>(blockIdx.x) * kE + threadIdx.x];
     __syncthreads();
-    scatter_chunk(a, blockIdx.x, base, cnt);
+    scatter_chunk<kRouteChunkTokens>(a, blockIdx.x, base, cnt);
 }
 
 // The three steps in one launch, for at most kRouteFusedChunks chunks (all CTAs
@@ -272,7 +273,7 @@ scatter_kernel(const RouteArgs a)
 // adds up the chunk counts it needs (all chunks for the totals, the earlier
 // ones for its own base), CTA 0 writes counts, offsets and the block map, and
 // each CTA scatters its chunk.
-template <bool SPLIT>
+template <bool SPLIT, int CT>
 __global__ void __launch_bounds__(kRouteThreads)
 route_fused_kernel(const RouteArgs a)
 {
@@ -284,7 +285,7 @@ route_fused_kernel(const RouteArgs a)
     const int chunk = blockIdx.x;
     pdl_trigger();
     pdl_wait();  // the router's logits (and its reset of the arrival count) are complete
-    topk_chunk<SPLIT>(a, chunk, hist);
+    topk_chunk<SPLIT, CT>(a, chunk, hist);
     a.chunk_counts[static_cast<size_t>(chunk) * kE + threadIdx.x] = hist[threadIdx.x];
     __syncthreads();  // every count of this chunk stored
     if (threadIdx.x == 0) {
@@ -315,7 +316,7 @@ route_fused_kernel(const RouteArgs a)
     const int off = expert_tables(a, total_e, scratch, chunk == 0);
     base[threadIdx.x] = off + prefix_e;
     __syncthreads();
-    scatter_chunk(a, chunk, base, cnt);
+    scatter_chunk<CT>(a, chunk, base, cnt);
 }
 
 }  // namespace
@@ -328,8 +329,19 @@ cudaError_t launch_topk_count(const RouteArgs &a, cudaStream_t stream)
 
 cudaError_t launch_route_fused(const RouteArgs &a, cudaStream_t stream)
 {
-    if (a.ksplit > 1) return launch_pdl(route_fused_kernel<true>, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
-    return launch_pdl(route_fused_kernel<false>, dim3(a.n_chunks), dim3(kRouteThreads), 0, stream, a);
+    const dim3 grid(a.n_chunks), block(kRouteThreads);
+    const bool split = a.ksplit > 1;
+    switch (route_chunk_tokens(a.T)) {
+    case 8:
+        return split ? launch_pdl(route_fused_kernel<true, 8>, grid, block, 0, stream, a)
+                     : launch_pdl(route_fused_kernel<false, 8>, grid, block, 0, stream, a);
+    case 16:
+        return split ? launch_pdl(route_fused_kernel<true, 16>, grid, block, 0, stream, a)
+                     : launch_pdl(route_fused_kernel<false, 16>, grid, block, 0, stream, a);
+    default:
+        return split ? launch_pdl(route_fused_kernel<true, 32>, grid, block, 0, stream, a)
+                     : launch_pdl(route_fused_kernel<false, 32>, grid, block, 0, stream, a);
+    }
 }
 
 cudaError_t launch_route_scan(const RouteArgs &a, cudaStream_t stream)
