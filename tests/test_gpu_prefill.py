@@ -38,6 +38,14 @@ def test_ragged_token_counts(T):
     _full_check(TINY, T, seed_offset=T)
 
 
+@pytest.mark.parametrize("T", [512, 513, 1000, 1025, 2048, 2049])
+def test_routing_chunk_regimes(T):
+    # the routing runs in one launch up to 64 chunks, with 8-token chunks up to
+    # T = 512, 16-token chunks up to 1024 and 32-token chunks up to 2048, and as
+    # three launches above: the edges of each regime, full parity
+    _full_check(TINY, T, seed_offset=T)
+
+
 @pytest.mark.parametrize("block_rows", [16, 32, 64])
 def test_block_rows_variants(block_rows):
     _full_check(TINY, 200, block_rows=block_rows, seed_offset=block_rows)
