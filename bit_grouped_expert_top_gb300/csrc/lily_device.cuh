@@ -129,19 +129,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar_addr), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Waits for two phases; both barriers are tested at once first, so that when
 // both are already complete the thread pays one shared-memory round trip.
 __device__ __forceinline__ bool mbar_wait2(uint64_t *bar0, uint32_t parity0, uint64_t *bar1, uint32_t parity1,
