@@ -12,20 +12,24 @@
 //
 // GB300 design.  The rows of S evolve independently (row i needs only u_i,
 // v_t[i] and the shared k_t, q_t), so the state is split by rows: CTA
-// (16-row slice, value head), 4 threads per row (64 threads), each holding
-// d_k / 4 columns of its row in registers for the whole sequence (column
-// groups of 4 interleaved over the row's threads, so their shared-memory
-// reads of k and q hit consecutive banks).  The token inputs (q and k rows of
-// the key head, this slice's 16 values of v, alpha and beta) are copied into
-// shared memory 32 tokens at a time with cp.async, double buffered; k and q
-// are then converted to fp32 once per chunk for all rows.  The token loop is
-// pipelined: after the update with token t a thread forms both dots with the
-// new state, its part of o_t (with q_t) and of u_{t+1} (with k_{t+1}), and
-// the two butterfly reductions over the row's threads interleave; column
+// (16-row slice, value head), 2 threads per row, each holding d_k / 2 columns
+// of its row in registers for the whole sequence (column groups of 4
+// interleaved over the row's threads, so their shared-memory reads of k and q
+// hit consecutive banks).  Each slice of the state is held twice, by two
+// warps of different roles.  The recurrence warp carries the chain that
+// feeds back (u_t = S_{t-1} k_t, beta_t (v_t - alpha_t u_t), the update) and
+// leaves beta_t (v_t - alpha_t u_t) per token and row in shared memory; the
+// output warp, one chunk behind, repeats the same updates from those values
+// (bit-identical states) and forms o_t with q_t, work that nothing in the
+// recurrence waits for.  The token inputs (q and k rows of the key head, this
+// slice's 16 values of v, alpha and beta) are copied into shared memory 32
+// tokens at a time with cp.async, double buffered; k and q are converted to
+// fp32 once per chunk for all rows.  The recurrence's token loop is
+// pipelined (after the update with token t, the dot with k_{t+1}); column
 // pairs use the packed two-lane fp32 instructions.  Outputs of a chunk are
 // collected in shared memory and written as 16-byte stores.  The sequential
 // dependence through S makes the scan latency-bound: per token a chain of
-// shared-memory loads, a few FMAs and the butterfly shuffles.
+// shared-memory loads, a few FMAs and a butterfly shuffle.
 #include <cstdint>
 
 #include "lily_device.cuh"
@@ -49,8 +53,10 @@ struct GdnStage {
 template <int DK>
 struct GdnSmem {
     GdnStage<DK> st[2];              // bf16 inputs as copied (double buffered)
-    float kf[kGdnChunk][DK];         // this chunk's k and q in fp32, converted once for all rows
-    float qf[kGdnChunk][DK];
+    float kf[2][kGdnChunk][DK];      // k and q in fp32, converted once for all rows; the
+    float qf[2][kGdnChunk][DK];      // output warps read chunk c - 1 while chunk c is written
+    float cc[2][kGdnChunk][kGdnRows];  // per token and row: beta (v - alpha u), from the recurrence warps
+    float al[2][kGdnChunk];          // alpha of the chunk, for the output warps
     float o[kGdnChunk][kGdnRows];
 };
 
@@ -83,16 +89,19 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b)
     return f2_from(r);
 }
 
-// TPR threads per state row, each owning DK / TPR columns; 16 rows per CTA.
+// TPR threads per state row, each owning DK / TPR columns; 16 rows per CTA,
+// held twice: by the recurrence warps and by the output warps.
 template <int DK, int TPR>
-__global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs a)
+__global__ void __launch_bounds__(2 * kGdnRows * TPR) gdn_scan_kernel(const GdnArgs a)
 {
-    constexpr int NT = kGdnRows * TPR;  // threads
+    constexpr int NR = kGdnRows * TPR;  // threads of one role
+    constexpr int NT = 2 * NR;          // threads
     constexpr int CPT = DK / TPR;       // state columns per thread
     extern __shared__ __align__(16) uint8_t gsm[];
     GdnSmem<DK> &S = *reinterpret_cast<GdnSmem<DK> *>(gsm);
     const int slice = blockIdx.x, h = blockIdx.y;
-    const int tid = threadIdx.x, r = tid / TPR, cg = tid % TPR;
+    const int tid = threadIdx.x, rtid = tid % NR, r = rtid / TPR, cg = tid % TPR;
+    const bool recur = tid < NR;  // recurrence warps; the others form the outputs
     const int hk = h / (a.H_v / a.H_k);
     const int row = slice * kGdnRows + r;
     const int T = a.T;
@@ -145,115 +154,147 @@ __global__ void __launch_bounds__(kGdnRows * TPR) gdn_scan_kernel(const GdnArgs 
         for (int o = 1; o < TPR; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
         return x;
     };
+    auto load_row = [&](const float (*src)[DK], int t, float2(&dst)[NP]) {
+#pragma unroll
+        for (int j = 0; j < CPT; j += 4) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(&src[t][col(j)]);
+            dst[j / 2] = make_float2(v4.x, v4.y);
+            dst[j / 2 + 1] = make_float2(v4.z, v4.w);
+        }
+    };
+    // four partial sums per dot, so each dependence chain is NP / 4 long; the
+    // same order at every token, so a scan split between calls gives the same bits
+    auto psum4 = [](const float2(&p)[4]) {
+        return ((p[0].x + p[0].y) + (p[1].x + p[1].y)) + ((p[2].x + p[2].y) + (p[3].x + p[3].y));
+    };
 
+    // Iteration c converts chunk c; the recurrence warps run its tokens and
+    // leave beta (v - alpha u) per token and row in shared memory; the output
+    // warps, one chunk behind, repeat the same state updates from those values
+    // (the same bits) and form o_t with q_t, which nothing downstream in the
+    // recurrence needs.  One extra iteration lets the output warps finish.
     const int n_chunks = (T + kGdnChunk - 1) / kGdnChunk;
     if (n_chunks > 0) stage(0, 0);
-    for (int c = 0; c < n_chunks; ++c) {
+    for (int c = 0; n_chunks > 0 && c <= n_chunks; ++c) {
         const int t0 = c * kGdnChunk, n = min(kGdnChunk, T - t0);
-        if (c + 1 < n_chunks) {
-            stage((c + 1) & 1, t0 + kGdnChunk);
-            cp_async_wait_1();  // this chunk's group has landed (the next one may still be in flight)
-        } else {
-            cp_async_wait_all();
+        const int b = c & 1;
+        if (c < n_chunks) {
+            if (c + 1 < n_chunks) {
+                stage((c + 1) & 1, t0 + kGdnChunk);
+                cp_async_wait_1();  // this chunk's group has landed (the next one may still be in flight)
+            } else {
+                cp_async_wait_all();
+            }
+            __syncthreads();
+            const GdnStage<DK> &B = S.st[b];
+            // k and q of the chunk to fp32, once for all rows (8 bf16 -> 8 floats per step)
+            for (int i = tid; i < n * DK / 8; i += NT) {
+                const int t = i / (DK / 8), j = (i - t * (DK / 8)) * 8;
+                const uint4 kw = *reinterpret_cast<const uint4 *>(&B.k[t][j]);
+                const uint4 qw = *reinterpret_cast<const uint4 *>(&B.q[t][j]);
+                float4 *kd = reinterpret_cast<float4 *>(&S.kf[b][t][j]), *qd = reinterpret_cast<float4 *>(&S.qf[b][t][j]);
+                kd[0] = make_float4(__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
+                                    __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u));
+                kd[1] = make_float4(__uint_as_float(kw.z << 16), __uint_as_float(kw.z & 0xFFFF0000u),
+                                    __uint_as_float(kw.w << 16), __uint_as_float(kw.w & 0xFFFF0000u));
+                qd[0] = make_float4(__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u),
+                                    __uint_as_float(qw.y << 16), __uint_as_float(qw.y & 0xFFFF0000u));
+                qd[1] = make_float4(__uint_as_float(qw.z << 16), __uint_as_float(qw.z & 0xFFFF0000u),
+                                    __uint_as_float(qw.w << 16), __uint_as_float(qw.w & 0xFFFF0000u));
+            }
+            for (int t = tid; t < n; t += NT) S.al[b][t] = B.alpha[t];
+            __syncthreads();
+        }
+        if (recur && c < n_chunks) {
+            // Token loop, pipelined: u_t = (S_{t-1} k_t)_row is ready on entry;
+            // the update with token t is followed by the dot with k_{t+1}.  The
+            // loop runs two tokens per trip so k_t and k_{t+1} swap register roles.
+            const GdnStage<DK> &B = S.st[b];
+            const float (*kf)[DK] = S.kf[b];
+            float2 ka[NP], kb[NP];
+            load_row(kf, 0, ka);
+            float u;
+            {
+                float2 pa[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) pa[q] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) pa[j & 3] = ffma2(st[j], ka[j], pa[j & 3]);
+                u = row_sum(psum4(pa));
+            }
+            auto step = [&](int t, const float2(&kc)[NP], float2(&kn)[NP]) {
+                load_row(kf, t + 1 < n ? t + 1 : t, kn);
+                const float al = B.alpha[t], be = B.beta[t];
+                const float vr = __uint_as_float(static_cast<uint32_t>(B.v[t][r]) << 16);
+                const float cc = be * (vr - al * u);
+                if (cg == 0) S.cc[b][t][r] = cc;
+                const float2 al2 = make_float2(al, al), cc2 = make_float2(cc, cc);
+                float2 pa[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) pa[q] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    st[j] = ffma2(al2, st[j], fmul2(cc2, kc[j]));
+                    pa[j & 3] = ffma2(st[j], kn[j], pa[j & 3]);
+                }
+                u = row_sum(psum4(pa));
+            };
+            int t = 0;
+            for (; t + 1 < n; t += 2) {
+                step(t, ka, kb);
+                step(t + 1, kb, ka);
+            }
+            if (t < n) step(t, ka, kb);
+        } else if (!recur && c > 0) {
+            // the previous chunk: S_t = alpha_t S_{t-1} + cc_t k_t^T, o_t = scale S_t q_t
+            const int pb = b ^ 1, pn = min(kGdnChunk, T - (t0 - kGdnChunk));
+            const float (*kf)[DK] = S.kf[pb];
+            const float (*qf)[DK] = S.qf[pb];
+#pragma unroll 2
+            for (int t = 0; t < pn; ++t) {
+                float2 kc[NP], qv[NP];
+                load_row(kf, t, kc);
+                load_row(qf, t, qv);
+                const float al = S.al[pb][t], cc = S.cc[pb][t][r];
+                const float2 al2 = make_float2(al, al), cc2 = make_float2(cc, cc);
+                float2 oa[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) oa[q] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    st[j] = ffma2(al2, st[j], fmul2(cc2, kc[j]));
+                    oa[j & 3] = ffma2(st[j], qv[j], oa[j & 3]);
+                }
+                const float o = row_sum(psum4(oa));
+                if (cg == 0) S.o[t][r] = a.scale * o;
+            }
         }
         __syncthreads();
-        const GdnStage<DK> &B = S.st[c & 1];
-        // k and q of the chunk to fp32, once for all rows (8 bf16 -> 8 floats per step)
-        for (int i = tid; i < n * DK / 8; i += NT) {
-            const int t = i / (DK / 8), j = (i - t * (DK / 8)) * 8;
-            const uint4 kw = *reinterpret_cast<const uint4 *>(&B.k[t][j]);
-            const uint4 qw = *reinterpret_cast<const uint4 *>(&B.q[t][j]);
-            float4 *kd = reinterpret_cast<float4 *>(&S.kf[t][j]), *qd = reinterpret_cast<float4 *>(&S.qf[t][j]);
-            kd[0] = make_float4(__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
-                                __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u));
-            kd[1] = make_float4(__uint_as_float(kw.z << 16), __uint_as_float(kw.z & 0xFFFF0000u),
-                                __uint_as_float(kw.w << 16), __uint_as_float(kw.w & 0xFFFF0000u));
-            qd[0] = make_float4(__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u),
-                                __uint_as_float(qw.y << 16), __uint_as_float(qw.y & 0xFFFF0000u));
-            qd[1] = make_float4(__uint_as_float(qw.z << 16), __uint_as_float(qw.z & 0xFFFF0000u),
-                                __uint_as_float(qw.w << 16), __uint_as_float(qw.w & 0xFFFF0000u));
-        }
-        __syncthreads();
-        // Token loop, pipelined: u_t = (S_{t-1} k_t)_row is ready on entry; the
-        // update with token t is followed by both dots with the new state, o_t
-        // (with q_t) and u_{t+1} (with k_{t+1}), whose butterflies interleave.
-        // Column pairs go through packed two-lane fp32 instructions; the loop
-        // runs two tokens per trip so k_t and k_{t+1} swap register roles.
-        auto load_row = [&](const float (*src)[DK], int t, float2(&dst)[NP]) {
-#pragma unroll
-            for (int j = 0; j < CPT; j += 4) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(&src[t][col(j)]);
-                dst[j / 2] = make_float2(v4.x, v4.y);
-                dst[j / 2 + 1] = make_float2(v4.z, v4.w);
+        if (c > 0) {
+            // the previous chunk's outputs: per token 16 floats of this slice, four 16-byte stores
+            const int pt0 = t0 - kGdnChunk, pn = min(kGdnChunk, T - pt0);
+            for (int i = tid; i < pn * 4; i += NT) {
+                const int t = i >> 2, p = i & 3;
+                *reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(pt0 + t) * a.H_v + h) * a.d_v + slice * kGdnRows + p * 4) =
+                    *reinterpret_cast<const float4 *>(&S.o[t][p * 4]);
             }
-        };
-        float2 ka[NP], kb[NP];
-        load_row(S.kf, 0, ka);
-        float u;
-        {
-            // the same four partial sums and order as the dots in the token loop,
-            // so a scan split between calls gives the same bits
-            float2 pa[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) pa[c] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < NP; ++j) pa[j & 3] = ffma2(st[j], ka[j], pa[j & 3]);
-            u = row_sum(((pa[0].x + pa[0].y) + (pa[1].x + pa[1].y)) + ((pa[2].x + pa[2].y) + (pa[3].x + pa[3].y)));
         }
-        // one token: update with kc (= k_t), dots with q_t and kn (= k_{t+1})
-        auto step = [&](int t, const float2(&kc)[NP], float2(&kn)[NP]) {
-            float2 qf[NP];
-            load_row(S.qf, t, qf);
-            load_row(S.kf, t + 1 < n ? t + 1 : t, kn);
-            const float al = B.alpha[t], be = B.beta[t];
-            const float vr = __uint_as_float(static_cast<uint32_t>(B.v[t][r]) << 16);
-            const float cc = be * (vr - al * u);
-            const float2 al2 = make_float2(al, al), cc2 = make_float2(cc, cc);
-            // four partial sums per dot, so each dependence chain is NP / 4 long
-            float2 oa[4], pa[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) oa[c] = pa[c] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < NP; ++j) {
-                st[j] = ffma2(al2, st[j], fmul2(cc2, kc[j]));
-                oa[j & 3] = ffma2(st[j], qf[j], oa[j & 3]);
-                pa[j & 3] = ffma2(st[j], kn[j], pa[j & 3]);
-            }
-            float o = ((oa[0].x + oa[0].y) + (oa[1].x + oa[1].y)) + ((oa[2].x + oa[2].y) + (oa[3].x + oa[3].y));
-            float un = ((pa[0].x + pa[0].y) + (pa[1].x + pa[1].y)) + ((pa[2].x + pa[2].y) + (pa[3].x + pa[3].y));
-#pragma unroll
-            for (int m = 1; m < TPR; m <<= 1) {
-                o += __shfl_xor_sync(0xffffffffu, o, m);
-                un += __shfl_xor_sync(0xffffffffu, un, m);
-            }
-            if (cg == 0) S.o[t][r] = a.scale * o;
-            u = un;
-        };
-        int t = 0;
-        for (; t + 1 < n; t += 2) {
-            step(t, ka, kb);
-            step(t + 1, kb, ka);
-        }
-        if (t < n) step(t, ka, kb);
-        __syncthreads();
-        // the chunk's outputs: per token 16 floats of this slice, four 16-byte stores
-        for (int i = tid; i < n * 4; i += NT) {
-            const int t = i >> 2, p = i & 3;
-            *reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(t0 + t) * a.H_v + h) * a.d_v + slice * kGdnRows + p * 4) =
-                *reinterpret_cast<const float4 *>(&S.o[t][p * 4]);
-        }
-        // the buffer just read is restaged two chunks later, after the barriers above
+        // the staging buffer just read is restaged two chunks later, and the
+        // fp32 and cc buffers of this chunk are rewritten two iterations later,
+        // after the barriers above
     }
-    float *so = a.state_out + (static_cast<size_t>(h) * a.d_v + row) * DK;
+    if (recur) {
+        float *so = a.state_out + (static_cast<size_t>(h) * a.d_v + row) * DK;
 #pragma unroll
-    for (int j = 0; j < CPT; j += 4)
-        *reinterpret_cast<float4 *>(so + col(j)) = make_float4(st[j / 2].x, st[j / 2].y, st[j / 2 + 1].x, st[j / 2 + 1].y);
+        for (int j = 0; j < CPT; j += 4)
+            *reinterpret_cast<float4 *>(so + col(j)) = make_float4(st[j / 2].x, st[j / 2].y, st[j / 2 + 1].x, st[j / 2 + 1].y);
+    }
 }
 
 }  // namespace
 
 #ifndef LILY_GDN_TPR
-#define LILY_GDN_TPR 4
+#define LILY_GDN_TPR 2
 #endif
 constexpr int kGdnTPR = LILY_GDN_TPR;  // threads per state row
 
@@ -265,7 +306,7 @@ static cudaError_t launch_dk(const GdnArgs &a, cudaStream_t stream)
     const size_t smem = sizeof(GdnSmem<DK>);
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(gdn_scan_kernel<DK, kGdnTPR>), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return launch_pdl(gdn_scan_kernel<DK, kGdnTPR>, dim3(a.d_v / kGdnRows, a.H_v), dim3(kGdnRows * kGdnTPR), smem, stream, a);
+    return launch_pdl(gdn_scan_kernel<DK, kGdnTPR>, dim3(a.d_v / kGdnRows, a.H_v), dim3(2 * kGdnRows * kGdnTPR), smem, stream, a);
 }
 
 cudaError_t launch_gdn_scan(const GdnArgs &a, cudaStream_t stream)
