@@ -21,12 +21,13 @@
 // leaves beta_t (v_t - alpha_t u_t) per token and row in shared memory; the
 // output warp, one chunk behind, repeats the same updates from those values
 // (bit-identical states) and forms o_t with q_t, work that nothing in the
-// recurrence waits for.  The token inputs (q and k rows of the key head, this
-// slice's 16 values of v, alpha and beta) are copied into shared memory 32
-// tokens at a time with cp.async, double buffered; k and q are converted to
-// fp32 once per chunk for all rows.  The recurrence's token loop is
-// pipelined (after the update with token t, the dot with k_{t+1}); column
-// pairs use the packed two-lane fp32 instructions.  Outputs of a chunk are
+// recurrence waits for.  The recurrence warp also copies the token inputs (q
+// and k rows of the key head, this slice's 16 values of v, alpha and beta)
+// into shared memory 32 tokens at a time with cp.async, two chunks ahead, and
+// converts k and q to fp32 once per chunk for both roles; one block barrier
+// per chunk hands a chunk from one role to the other.  The recurrence's token
+// loop is pipelined (after the update with token t, the dot with k_{t+1});
+// column pairs use the packed two-lane fp32 instructions.  Outputs of a chunk are
 // collected in shared memory and written as 16-byte stores.  The sequential
 // dependence through S makes the scan latency-bound: per token a chain of
 // shared-memory loads, a few FMAs and a butterfly shuffle.
@@ -94,8 +95,7 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b)
 template <int DK, int TPR>
 __global__ void __launch_bounds__(2 * kGdnRows * TPR) gdn_scan_kernel(const GdnArgs a)
 {
-    constexpr int NR = kGdnRows * TPR;  // threads of one role
-    constexpr int NT = 2 * NR;          // threads
+    constexpr int NR = kGdnRows * TPR;  // threads of one role (the block has two roles)
     constexpr int CPT = DK / TPR;       // state columns per thread
     extern __shared__ __align__(16) uint8_t gsm[];
     GdnSmem<DK> &S = *reinterpret_cast<GdnSmem<DK> *>(gsm);
@@ -126,22 +126,22 @@ __global__ void __launch_bounds__(2 * kGdnRows * TPR) gdn_scan_kernel(const GdnA
         }
     }
 
-    // stage tokens [t0, t0 + n) into buffer b (one cp.async group)
+    // recurrence threads: stage tokens [t0, t0 + n) into buffer b (one cp.async group)
     auto stage = [&](int b, int t0) {
         GdnStage<DK> &B = S.st[b];
         const int n = min(kGdnChunk, T - t0);
         constexpr int kPieces = DK * 2 / 16;  // 16-byte pieces of a q or k row
-        for (int i = tid; i < n * kPieces; i += NT) {
+        for (int i = tid; i < n * kPieces; i += NR) {
             const int t = i / kPieces, p = i - t * kPieces;
             const size_t src = (static_cast<size_t>(t0 + t) * a.H_k + hk) * DK + p * 8;
             cp_async_16(&B.k[t][p * 8], a.k + src);
             cp_async_16(&B.q[t][p * 8], a.q + src);
         }
-        for (int i = tid; i < n * 2; i += NT) {
+        for (int i = tid; i < n * 2; i += NR) {
             const int t = i >> 1, p = i & 1;
             cp_async_16(&B.v[t][p * 8], a.v + (static_cast<size_t>(t0 + t) * a.H_v + h) * a.d_v + slice * kGdnRows + p * 8);
         }
-        for (int t = tid; t < n; t += NT) {
+        for (int t = tid; t < n; t += NR) {
             cp_async_4(&B.alpha[t], a.alpha + static_cast<size_t>(t0 + t) * a.H_v + h);
             cp_async_4(&B.beta[t], a.beta + static_cast<size_t>(t0 + t) * a.H_v + h);
         }
@@ -168,44 +168,57 @@ __global__ void __launch_bounds__(2 * kGdnRows * TPR) gdn_scan_kernel(const GdnA
         return ((p[0].x + p[0].y) + (p[1].x + p[1].y)) + ((p[2].x + p[2].y) + (p[3].x + p[3].y));
     };
 
-    // Iteration c converts chunk c; the recurrence warps run its tokens and
-    // leave beta (v - alpha u) per token and row in shared memory; the output
-    // warps, one chunk behind, repeat the same state updates from those values
-    // (the same bits) and form o_t with q_t, which nothing downstream in the
-    // recurrence needs.  One extra iteration lets the output warps finish.
+    // Chunk pipeline.  The recurrence threads stage the inputs two chunks ahead
+    // and convert k and q of a chunk to fp32 before running its tokens; they
+    // leave beta (v - alpha u) per token and row in shared memory.  The output
+    // threads, one chunk behind, repeat the same state updates from those values
+    // (the same bits) and form o_t with q_t, which nothing in the recurrence
+    // waits for.  One barrier per iteration c: after it the recurrence on chunk
+    // c and the outputs of chunk c - 1 are both done, so chunk c + 1 may be
+    // converted into the buffers chunk c - 1 used, and the outputs of chunk c
+    // may start.  One extra iteration lets the output threads finish.
+    auto role_sync = [&]() {  // the NR threads of this thread's role
+        if (recur)
+            asm volatile("bar.sync 1, %0;" ::"n"(NR) : "memory");
+        else
+            asm volatile("bar.sync 2, %0;" ::"n"(NR) : "memory");
+    };
+    auto convert = [&](int c) {  // recurrence threads: k and q of chunk c to fp32, alpha copied
+        const int b = c & 1, n = min(kGdnChunk, T - c * kGdnChunk);
+        const GdnStage<DK> &B = S.st[b];
+        for (int i = tid; i < n * DK / 8; i += NR) {
+            const int t = i / (DK / 8), j = (i - t * (DK / 8)) * 8;
+            const uint4 kw = *reinterpret_cast<const uint4 *>(&B.k[t][j]);
+            const uint4 qw = *reinterpret_cast<const uint4 *>(&B.q[t][j]);
+            float4 *kd = reinterpret_cast<float4 *>(&S.kf[b][t][j]), *qd = reinterpret_cast<float4 *>(&S.qf[b][t][j]);
+            kd[0] = make_float4(__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
+                                __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u));
+            kd[1] = make_float4(__uint_as_float(kw.z << 16), __uint_as_float(kw.z & 0xFFFF0000u),
+                                __uint_as_float(kw.w << 16), __uint_as_float(kw.w & 0xFFFF0000u));
+            qd[0] = make_float4(__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u),
+                                __uint_as_float(qw.y << 16), __uint_as_float(qw.y & 0xFFFF0000u));
+            qd[1] = make_float4(__uint_as_float(qw.z << 16), __uint_as_float(qw.z & 0xFFFF0000u),
+                                __uint_as_float(qw.w << 16), __uint_as_float(qw.w & 0xFFFF0000u));
+        }
+        for (int t = tid; t < n; t += NR) S.al[b][t] = B.alpha[t];
+    };
     const int n_chunks = (T + kGdnChunk - 1) / kGdnChunk;
-    if (n_chunks > 0) stage(0, 0);
+    if (recur && n_chunks > 0) {
+        stage(0, 0);
+        if (n_chunks > 1) {
+            stage(1, kGdnChunk);
+            cp_async_wait_1();  // chunk 0's group has landed (chunk 1's may still be in flight)
+        } else {
+            cp_async_wait_all();
+        }
+        role_sync();  // every thread's copies of chunk 0 are complete
+        convert(0);
+    }
     for (int c = 0; n_chunks > 0 && c <= n_chunks; ++c) {
         const int t0 = c * kGdnChunk, n = min(kGdnChunk, T - t0);
         const int b = c & 1;
-        if (c < n_chunks) {
-            if (c + 1 < n_chunks) {
-                stage((c + 1) & 1, t0 + kGdnChunk);
-                cp_async_wait_1();  // this chunk's group has landed (the next one may still be in flight)
-            } else {
-                cp_async_wait_all();
-            }
-            __syncthreads();
-            const GdnStage<DK> &B = S.st[b];
-            // k and q of the chunk to fp32, once for all rows (8 bf16 -> 8 floats per step)
-            for (int i = tid; i < n * DK / 8; i += NT) {
-                const int t = i / (DK / 8), j = (i - t * (DK / 8)) * 8;
-                const uint4 kw = *reinterpret_cast<const uint4 *>(&B.k[t][j]);
-                const uint4 qw = *reinterpret_cast<const uint4 *>(&B.q[t][j]);
-                float4 *kd = reinterpret_cast<float4 *>(&S.kf[b][t][j]), *qd = reinterpret_cast<float4 *>(&S.qf[b][t][j]);
-                kd[0] = make_float4(__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
-                                    __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u));
-                kd[1] = make_float4(__uint_as_float(kw.z << 16), __uint_as_float(kw.z & 0xFFFF0000u),
-                                    __uint_as_float(kw.w << 16), __uint_as_float(kw.w & 0xFFFF0000u));
-                qd[0] = make_float4(__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u),
-                                    __uint_as_float(qw.y << 16), __uint_as_float(qw.y & 0xFFFF0000u));
-                qd[1] = make_float4(__uint_as_float(qw.z << 16), __uint_as_float(qw.z & 0xFFFF0000u),
-                                    __uint_as_float(qw.w << 16), __uint_as_float(qw.w & 0xFFFF0000u));
-            }
-            for (int t = tid; t < n; t += NT) S.al[b][t] = B.alpha[t];
-            __syncthreads();
-        }
         if (recur && c < n_chunks) {
+            role_sync();  // chunk c's fp32 rows are complete
             // Token loop, pipelined: u_t = (S_{t-1} k_t)_row is ready on entry;
             // the update with token t is followed by the dot with k_{t+1}.  The
             // loop runs two tokens per trip so k_t and k_{t+1} swap register roles.
@@ -245,6 +258,10 @@ __global__ void __launch_bounds__(2 * kGdnRows * TPR) gdn_scan_kernel(const GdnA
                 step(t + 1, kb, ka);
             }
             if (t < n) step(t, ka, kb);
+            if (c + 2 < n_chunks) {
+                role_sync();  // every recurrence thread is done with the staged chunk c
+                stage(b, t0 + 2 * kGdnChunk);
+            }
         } else if (!recur && c > 0) {
             // the previous chunk: S_t = alpha_t S_{t-1} + cc_t k_t^T, o_t = scale S_t q_t
             const int pb = b ^ 1, pn = min(kGdnChunk, T - (t0 - kGdnChunk));
@@ -268,20 +285,25 @@ __global__ void __launch_bounds__(2 * kGdnRows * TPR) gdn_scan_kernel(const GdnA
                 const float o = row_sum(psum4(oa));
                 if (cg == 0) S.o[t][r] = a.scale * o;
             }
-        }
-        __syncthreads();
-        if (c > 0) {
-            // the previous chunk's outputs: per token 16 floats of this slice, four 16-byte stores
-            const int pt0 = t0 - kGdnChunk, pn = min(kGdnChunk, T - pt0);
-            for (int i = tid; i < pn * 4; i += NT) {
+            role_sync();  // the chunk's outputs are complete
+            // per token 16 floats of this slice, four 16-byte stores
+            const int pt0 = t0 - kGdnChunk;
+            for (int i = tid - NR; i < pn * 4; i += NR) {
                 const int t = i >> 2, p = i & 3;
                 *reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(pt0 + t) * a.H_v + h) * a.d_v + slice * kGdnRows + p * 4) =
                     *reinterpret_cast<const float4 *>(&S.o[t][p * 4]);
             }
         }
-        // the staging buffer just read is restaged two chunks later, and the
-        // fp32 and cc buffers of this chunk are rewritten two iterations later,
-        // after the barriers above
+        __syncthreads();
+        if (recur && c + 1 < n_chunks) {
+            // chunk c + 1 has landed: every group but the newest (chunk c + 2, if staged)
+            if (c + 2 < n_chunks)
+                cp_async_wait_1();
+            else
+                cp_async_wait_all();
+            role_sync();  // every thread's copies of chunk c + 1 are complete
+            convert(c + 1);
+        }
     }
     if (recur) {
         float *so = a.state_out + (static_cast<size_t>(h) * a.d_v + row) * DK;
