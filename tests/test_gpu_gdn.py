@@ -91,6 +91,29 @@ def test_two_calls_continue_one_scan_exactly():
     assert np.array_equal(S2, S)
 
 
+@pytest.mark.parametrize("T,d_k", [(31, 128), (32, 128), (33, 64), (64, 128), (96, 64), (97, 128)])
+def test_chunk_pipeline_edges(T, d_k):
+    # whole and ragged 32-token chunks at the ends of the staging pipeline
+    # (one, two and three chunks; the last chunk full or one token long)
+    cfg = GDNConfig("edge", T=T, H_k=2, H_v=4, d_k=d_k, d_v=32, seed=T + d_k)
+    _check(make_gdn(cfg))
+
+
+@pytest.mark.parametrize("split", [1, 37, 64, 95])
+def test_split_anywhere_continues_exactly(split):
+    # a scan split at any token (inside a chunk, on a chunk boundary, one token
+    # in) repeats the single call's bits
+    g = make_gdn(GDNConfig("split", T=130, H_k=2, H_v=4, d_k=128, d_v=32, seed=7))
+    o, S = _gpu(g)
+    first = {k: (v[:split].contiguous() if k != "state" else v) for k, v in g.items()}
+    o1, S1 = _gpu(first)
+    second = {k: (v[split:].contiguous() if k != "state" else torch.from_numpy(S1.astype(np.float32)))
+              for k, v in g.items()}
+    o2, S2 = _gpu(second)
+    assert np.array_equal(np.concatenate([o1, o2]), o)
+    assert np.array_equal(S2, S)
+
+
 def test_small_and_zero_decay():
     # alpha of 1e-6, and 0 on every seventh token (the state is then replaced by
     # the token's own write): still within the bound of the oracle
