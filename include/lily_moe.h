@@ -19,7 +19,9 @@
  *     The library allocates nothing and frees nothing on these calls.
  *   - Every call is asynchronous on `stream`: it validates its arguments on the
  *     host, enqueues kernels and returns.  No call synchronises or copies data
- *     to the host, except lily_moe_device_status().
+ *     to the host, except lily_moe_device_status().  Because a call enqueues
+ *     only stream work, it may be recorded into the caller's CUDA graph by
+ *     stream capture (see lily_moe_route_noalloc for its one exception).
  *   - Every device pointer must be 16-byte aligned.
  *   - Return value: LILY_OK (0) or a negative LILY_ERR_* code.  Host-side errors
  *     are returned before anything is enqueued.  Errors detected by a kernel
