@@ -479,6 +479,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                                     static_cast<uint32_t>(mi * 64);
             int blk = 0;
             bool ok = true;
+            bool have_pre = false;  // s_nxt / b_nxt already hold the next unit's first register block
+            uint4 s_nxt = make_uint4(0u, 0u, 0u, 0u), b_nxt = s_nxt;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
                 const Unit u = unit_info<MODE>(g, tile, n_routed);
                 if (u.rows <= 0) continue;
@@ -487,6 +489,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 const int row = (mi ? r1 : r0) + r;
                 const uint16_t *srow = (u.shared ? (mi ? g.ss1 : g.ss0) : (mi ? g.s1 : g.s0)) + static_cast<size_t>(row) * ngroups;
                 const uint16_t *brow = (u.shared ? (mi ? g.sb1 : g.sb0) : (mi ? g.b1 : g.b0)) + static_cast<size_t>(row) * ngroups;
+                // the next unit this CTA runs (tile + gridDim.x, when it has rows)
+                const uint16_t *nsrow = nullptr, *nbrow = nullptr;
                 {
                     // warm L2 with the next unit's scale / bias rows of this thread
                     const int nt = tile + gridDim.x;
@@ -496,21 +500,42 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                             int n0, n1;
                             a_rows<MODE>(g, un, n0, n1);
                             const size_t nrow = static_cast<size_t>((mi ? n1 : n0) + r) * ngroups;
-                            prefetch_l2((un.shared ? (mi ? g.ss1 : g.ss0) : (mi ? g.s1 : g.s0)) + nrow);
-                            prefetch_l2((un.shared ? (mi ? g.sb1 : g.sb0) : (mi ? g.b1 : g.b0)) + nrow);
+                            nsrow = (un.shared ? (mi ? g.ss1 : g.ss0) : (mi ? g.s1 : g.s0)) + nrow;
+                            nbrow = (un.shared ? (mi ? g.sb1 : g.sb0) : (mi ? g.b1 : g.b0)) + nrow;
+                            prefetch_l2(nsrow);
+                            prefetch_l2(nbrow);
                         }
                     }
                 }
                 // scale / bias of 8 consecutive groups (two blocks) per 16-byte register
-                // block, fetched one register block ahead; groups past K read as zero
-                uint4 s_cur = load_groups8(srow, 0, ngroups, vec8), b_cur = load_groups8(brow, 0, ngroups, vec8);
-                uint4 s_nxt = load_groups8(srow, 8, ngroups, vec8), b_nxt = load_groups8(brow, 8, ngroups, vec8);
+                // block, fetched one register block ahead; groups past K read as zero.
+                // With preload_sb (gate/up at large T) the refill that would fetch
+                // past K fetches the next unit's first register block instead.
+                uint4 s_cur, b_cur;
+                if (have_pre) {
+                    s_cur = s_nxt;
+                    b_cur = b_nxt;
+                    have_pre = false;
+                } else {
+                    s_cur = load_groups8(srow, 0, ngroups, vec8);
+                    b_cur = load_groups8(brow, 0, ngroups, vec8);
+                }
+                s_nxt = load_groups8(srow, 8, ngroups, vec8);
+                b_nxt = load_groups8(brow, 8, ngroups, vec8);
                 for (int kb = 0; kb < KB; ++kb, ++blk) {
                     if ((kb & 1) == 0 && kb > 0) {
                         s_cur = s_nxt;
                         b_cur = b_nxt;
-                        s_nxt = load_groups8(srow, kb * kBlk + 8, ngroups, vec8);
-                        b_nxt = load_groups8(brow, kb * kBlk + 8, ngroups, vec8);
+                        const int gn = kb * kBlk + 8;  // first group of the block to fetch
+                        if (MODE == kModeGateUp && g.preload_sb && gn >= ngroups && nsrow) {
+                            // this unit needs no further block (kb + 2 >= KB)
+                            s_nxt = load_groups8(nsrow, 0, ngroups, vec8);
+                            b_nxt = load_groups8(nbrow, 0, ngroups, vec8);
+                            have_pre = true;
+                        } else {
+                            s_nxt = load_groups8(srow, gn, ngroups, vec8);
+                            b_nxt = load_groups8(brow, gn, ngroups, vec8);
+                        }
                     }
                     const int rs = blk & 1;
                     const uint32_t rpar = (blk >> 1) & 1;
