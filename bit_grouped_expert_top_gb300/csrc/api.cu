@@ -112,10 +112,6 @@ int gemm_k_steps(int64_t K)
 // 152-SM GPU while the token blocks alone are fewer, at most 8 and at most one
 // per block of four k-steps.  A fixed budget (not the device's SM count) keeps
 // the logits' rounding a function of the shape alone.
-// gate/up fetches the next unit's first scale/bias block during the current
-// unit's last blocks from this many tokens on (it shortened the kernel at
-// T = 8192 and lengthened it at T = 512)
-constexpr int kPreloadScaleBiasTokens = 4096;
 constexpr int kRouterUnitBudget = 152;
 constexpr int kRouterBlockRows = 64;
 
@@ -467,7 +463,6 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
     g.ksplit = 1;
     // gate/up + SwiGLU
     g.mode = kModeGateUp;
-    g.preload_sb = s.T >= kPreloadScaleBiasTokens;
     g.K = s.d;
     g.KT = gemm_k_steps(s.d);
     g.m_tiles = s.I / 128;
@@ -480,7 +475,6 @@ cudaError_t enqueue_experts(const lily_moe_shape &s, const lily_moe_weights &w, 
 
     // down + weighted combine
     g.mode = kModeDown;
-    g.preload_sb = 0;
     g.K = s.I;
     g.KT = gemm_k_steps(s.I);
     g.m_tiles = s.d / 256;

@@ -509,8 +509,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                 }
                 // scale / bias of 8 consecutive groups (two blocks) per 16-byte register
                 // block, fetched one register block ahead; groups past K read as zero.
-                // With preload_sb (gate/up at large T) the refill that would fetch
-                // past K fetches the next unit's first register block instead.
+                // In gate/up the refill that would fetch past K fetches the next
+                // unit's first register block instead.
                 uint4 s_cur, b_cur;
                 if (have_pre) {
                     s_cur = s_nxt;
@@ -527,7 +527,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ 
                         s_cur = s_nxt;
                         b_cur = b_nxt;
                         const int gn = kb * kBlk + 8;  // first group of the block to fetch
-                        if (MODE == kModeGateUp && g.preload_sb && gn >= ngroups && nsrow) {
+                        if (MODE == kModeGateUp && gn >= ngroups && nsrow) {
                             // this unit needs no further block (kb + 2 >= KB)
                             s_nxt = load_groups8(nsrow, 0, ngroups, vec8);
                             b_nxt = load_groups8(nbrow, 0, ngroups, vec8);

@@ -45,7 +45,6 @@ struct GemmArgs {
     const __half *xs;        // gate/up B: fp16 x in routing order [(top_k+1)*T][d] (routed rows, then shared)
     float *logits;           // router output [T][E] (ksplit == 1)
     int ksplit;              // router: K splits (1 <= ksplit <= KT / 4); expert modes: 1
-    int preload_sb;          // gate/up: fetch the next unit's first scale/bias block during this unit's last ones
     float *logits_part;      // router, ksplit > 1: partial logits [ksplit][T][E]
     __half *h;               // gate/up output, down input, fp16 [(top_k+1)*T][I]
     float *out;              // down output [T][d], accumulated
