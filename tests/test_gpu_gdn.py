@@ -59,10 +59,11 @@ def test_tiny(state):
 
 
 @pytest.mark.parametrize("T,H_k,H_v,d_k,d_v", [(300, 2, 4, 128, 128), (65, 1, 1, 128, 32), (129, 2, 8, 64, 256),
-                                               (1, 4, 4, 128, 64), (200, 3, 6, 64, 48)])
+                                               (1, 4, 4, 128, 64), (200, 3, 6, 64, 48), (40, 1, 16, 128, 1024),
+                                               (33, 2, 2, 64, 16)])
 def test_shapes(T, H_k, H_v, d_k, d_v):
-    # ragged chunks (300 = 4 x 64 + 44), one token (a decode step), group sizes 1, 2, 4,
-    # one to sixteen 16-row slices per head
+    # ragged chunks (300 = 4 x 64 + 44), one token (a decode step), group sizes 1, 2, 4
+    # and 16, one to sixty-four 16-row slices per head (d_v from 16 to the largest, 1024)
     cfg = GDNConfig("shape", T=T, H_k=H_k, H_v=H_v, d_k=d_k, d_v=d_v, seed=T + d_v)
     _check(make_gdn(cfg))
 
